@@ -1,0 +1,193 @@
+/*
+ * pafp8.h -- C ABI of libpafp8: batched attention of a query against a paged
+ * KV cache stored in fp8 (OCP e4m3fn or e5m2) with per-tensor scales, for
+ * NVIDIA GB300 (sm_103a).
+ *
+ * Two workloads share one plan/run interface:
+ *   - decode: one query row per request against its whole KV sequence; the
+ *     plan splits long sequences across CTAs and a merge kernel combines the
+ *     partial states by their log-sum-exp;
+ *   - prefill: a ragged batch of new query rows per request, bottom-right
+ *     aligned causal mask (query row i of a request with qo_len new rows and
+ *     kv_len keys sees key j iff j <= i + kv_len - qo_len).
+ *
+ * The plan()/run() split, o_data_type fixed at plan time and checked at run
+ * time, and the scale threading follow "Enable Hopper FA3 FP8 attention in
+ * decode.py" (flashinfer PR 2148), Changes table and review notes on
+ * o_data_type and the FP8 scales.  The dtype refusals follow "fp8 KV cache in
+ * the in-tree prefill kernel" (AMD-Ecosystem/flashinfer PR 368), What changed
+ * / Refusals and Architecture / design notes.
+ *
+ * Conventions shared by every entry point:
+ *   - Device pointers are plain CUDA device addresses; host pointers are
+ *     ordinary host memory.  The caller owns every buffer, the stream and the
+ *     workspace; the library owns only the plan object.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default).
+ *   - Every function returns a pafp8_status; on failure pafp8_last_error()
+ *     returns a sentence naming the offending values (thread-local, valid
+ *     until the next failing call on this thread).  Nothing aborts.
+ *   - pafp8_run neither allocates nor synchronizes.
+ */
+#ifndef PAFP8_H
+#define PAFP8_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define PAFP8_ABI_VERSION 1
+
+/* Element types, as int32 codes.  F32, INT8 and UINT8 exist only so that a
+ * caller holding such a tensor gets a refusal naming it: an integer cache has
+ * no floating-point reading, and reading its bytes as fp8 (or as 0..255) is
+ * the silent misread the in-tree prefill page (Architecture / design notes,
+ * "kv_smem_type_t keys on the fp8 types") rules out. */
+enum {
+    PAFP8_DTYPE_DEFAULT = 0, /* only for plan desc o_dtype: see below */
+    PAFP8_F16 = 1,
+    PAFP8_BF16 = 2,
+    PAFP8_E4M3FN = 3,
+    PAFP8_E5M2 = 4,
+    PAFP8_F32 = 5,
+    PAFP8_INT8 = 6,
+    PAFP8_UINT8 = 7
+};
+
+typedef enum pafp8_status {
+    PAFP8_OK = 0,
+    PAFP8_ERR_DTYPE = 1,       /* dtype not served, or differs from the plan */
+    PAFP8_ERR_SHAPE = 2,       /* head counts, head_dim, page size, lengths  */
+    PAFP8_ERR_ARG = 3,         /* NULL pointer, bad scale, bad option        */
+    PAFP8_ERR_WORKSPACE = 4,   /* workspace too small / plan not uploaded    */
+    PAFP8_ERR_CUDA = 5,        /* a CUDA runtime call failed                 */
+    PAFP8_ERR_TIMEOUT = 6,     /* a kernel's bounded wait expired            */
+    PAFP8_ERR_BOUNDS = 7,      /* a page index outside [0, num_pages)        */
+    PAFP8_ERR_UNSUPPORTED = 8  /* valid request this build does not serve    */
+} pafp8_status;
+
+enum { PAFP8_MODE_DECODE = 0, PAFP8_MODE_PREFILL = 1 };
+
+/* Static description of one batch.  Shapes served by this build:
+ * head_dim 128, page_size 16, num_qo_heads a multiple of num_kv_heads with
+ * group size num_qo_heads/num_kv_heads <= 8 (decode) or <= 16 (prefill).
+ *
+ * Dtype rules (checked by pafp8_plan_create, re-checked by pafp8_run):
+ *   kv_dtype   E4M3FN or E5M2.  F16/BF16 caches are refused by this build;
+ *              F32/INT8/UINT8 caches are refused with their own sentence.
+ *   q_dtype    F16 or BF16 (a 2-byte query against the fp8 cache, which is
+ *              dequantized on load), or E4M3FN/E5M2 (an fp8 query; q_scale
+ *              then folds into sm_scale like the FP8 BMM1 scale).
+ *   o_dtype    F16 or BF16.  fp8 outputs are refused (fp8 inputs produce a
+ *              16-bit output).  DEFAULT means q_dtype for a 2-byte query and
+ *              BF16 for an fp8 query.
+ * sm_scale     softmax scale applied to q.k; <= 0 means 1/sqrt(head_dim).
+ * Split-KV options (decode; prefill ignores them):
+ *   fixed_split_pages > 0  every request is cut into chunks of that many pages;
+ *   disable_split_kv != 0  one chunk per request;
+ *   otherwise              balanced: the concatenated pages of all
+ *                          (request, KV-head block) rows are cut into
+ *                          num_ctas equal ranges, one per CTA.
+ * num_ctas     persistent CTAs to launch; 0 = the SM count of the device that
+ *              is current when the plan is created. */
+typedef struct pafp8_plan_desc {
+    int32_t mode;  /* PAFP8_MODE_DECODE or PAFP8_MODE_PREFILL */
+    int32_t batch;
+    int32_t num_qo_heads;
+    int32_t num_kv_heads;
+    int32_t head_dim;
+    int32_t page_size;
+    int32_t num_pages; /* pages in the cache pool (rows of k_cache/v_cache) */
+    int32_t q_dtype;
+    int32_t kv_dtype;
+    int32_t o_dtype;
+    float sm_scale;
+    int32_t fixed_split_pages;
+    int32_t disable_split_kv;
+    int32_t num_ctas;
+} pafp8_plan_desc;
+
+typedef struct pafp8_plan pafp8_plan;
+
+/* ABI version of the loaded library (PAFP8_ABI_VERSION at build time). */
+int32_t pafp8_abi_version(void);
+
+/* Thread-local sentence describing the last failure on this thread ("" if
+ * none).  The pointer stays valid until the next failing call. */
+const char *pafp8_last_error(void);
+
+/* Build a plan on the host.  No device memory is touched.
+ *   kv_indptr_h     host int32 [batch+1], non-decreasing, kv_indptr_h[0] = 0;
+ *                   request b owns pages kv_indices[kv_indptr_h[b] ..
+ *                   kv_indptr_h[b+1]-1], in token order.
+ *   last_page_len_h host int32 [batch], in [1, page_size] for a request with
+ *                   pages (its kv_len = (npages-1)*page_size + last_page_len);
+ *                   ignored for a request with no pages (kv_len 0: output 0,
+ *                   lse -inf).
+ *   qo_indptr_h     host int32 [batch+1] for prefill (request b owns query
+ *                   rows qo_indptr_h[b] .. qo_indptr_h[b+1]-1, with
+ *                   qo_len <= kv_len); NULL for decode (row b is request b).
+ * The arrays are copied; the caller may free them after the call.  On
+ * success *out owns a plan freed by pafp8_plan_destroy. */
+pafp8_status pafp8_plan_create(const pafp8_plan_desc *desc, const int32_t *kv_indptr_h,
+                               const int32_t *last_page_len_h, const int32_t *qo_indptr_h,
+                               pafp8_plan **out);
+
+/* Free a plan (NULL is ignored). */
+void pafp8_plan_destroy(pafp8_plan *plan);
+
+/* Bytes of device workspace pafp8_run needs for this plan: the uploaded
+ * partition metadata, the split-KV partial states and a status word. */
+size_t pafp8_workspace_bytes(const pafp8_plan *plan);
+
+/* Read-only host view of the plan's partition metadata, the exact int32 words
+ * pafp8_plan_upload copies to the device (layout in the library source).
+ * Owned by the plan. */
+pafp8_status pafp8_plan_metadata(const pafp8_plan *plan, const int32_t **words, size_t *count);
+
+/* Copy the plan's metadata into the head of `workspace` (device memory of at
+ * least pafp8_workspace_bytes) on `stream` and clear its status word.  Must
+ * precede pafp8_run with this workspace; the plan records the workspace
+ * address and pafp8_run refuses any other. */
+pafp8_status pafp8_plan_upload(pafp8_plan *plan, void *workspace, size_t workspace_bytes,
+                               void *stream);
+
+/* Launch the attention for the planned batch on `stream`.
+ *   q           device, [nnz_qo, num_qo_heads, head_dim] of q_dtype
+ *               (nnz_qo = batch for decode, qo_indptr_h[batch] for prefill)
+ *   k_cache,
+ *   v_cache     device, [num_pages, page_size, num_kv_heads, head_dim] of
+ *               kv_dtype (token-major within a page), 16-byte aligned
+ *   kv_indices  device int32 [kv_indptr_h[batch]], each in [0, num_pages)
+ *   q_scale     dequantization scale of an fp8 query; must be 1 for a 2-byte
+ *               query (it would otherwise be silently ignored)
+ *   k_scale,
+ *   v_scale     per-tensor dequantization scales of the cache.  k_scale (and
+ *               q_scale) fold into sm_scale; v_scale multiplies the output
+ *               once, in fp32, before the cast.  Finite and > 0.
+ *   o           device, [nnz_qo, num_qo_heads, head_dim] of o_dtype
+ *   lse         device float [nnz_qo, num_qo_heads] or NULL: natural-log
+ *               log-sum-exp of the scaled logits (sm_scale, q_scale and
+ *               k_scale included; v_scale not)
+ *   workspace   the buffer given to pafp8_plan_upload for this plan
+ * The dtype arguments must equal the planned ones, and k_dtype must equal
+ * v_dtype.  A page index out of range is not read (the kernel records it in
+ * the workspace status word; see pafp8_device_status). */
+pafp8_status pafp8_run(const pafp8_plan *plan, int32_t q_dtype, const void *q,
+                       int32_t k_dtype, const void *k_cache, int32_t v_dtype, const void *v_cache,
+                       const int32_t *kv_indices, float q_scale, float k_scale, float v_scale,
+                       int32_t o_dtype, void *o, float *lse, void *workspace,
+                       size_t workspace_bytes, void *stream);
+
+/* Synchronize `stream`, read and clear the workspace status word that the
+ * kernels set.  Returns PAFP8_OK, PAFP8_ERR_BOUNDS (a page index was out of
+ * range) or PAFP8_ERR_TIMEOUT (a bounded pipeline wait expired). */
+pafp8_status pafp8_device_status(const pafp8_plan *plan, void *workspace, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAFP8_H */

@@ -1,0 +1,128 @@
+"""Split-KV partition rule for decode, restated plainly (test infrastructure).
+
+The library's plan scheduler must produce exactly these int32 words.  The
+rule (the pages only say that the plan splits KV across CTAs, with
+fixed-split and disable-split options; the balanced rule is this library's):
+
+* Rows are (request b, KV-head block hb), row r = b * nhb + hb, where a block
+  holds hpc KV heads, hpc = the largest divisor of num_kv_heads that is <= 8,
+  and nhb = num_kv_heads / hpc.  Row r holds npages[b] pages.
+* disable_split_kv: one segment (r, 0, npages) per non-empty row; segment k
+  goes to CTA k mod G, G = min(num_ctas, #segments).
+* fixed_split_pages = c > 0: each row cut into [0,c), [c,2c), ...; dealt the
+  same way.
+* otherwise (balanced): T = total pages of all rows, G = min(num_ctas, T);
+  CTA i owns global pages [i*T//G, (i+1)*T//G) of the rows laid end to end,
+  cut at row boundaries.
+* A segment that spans its whole row has out_slot -1; the others get slots
+  0, 1, 2, ... in segment order (CTA by CTA).
+* Merge rows: rows with no pages or with two or more segments, ascending;
+  each lists its slots ordered by first page.
+"""
+from __future__ import annotations
+
+HEADER_WORDS = 32
+MAGIC = 0x38464150
+
+
+def heads_per_cta(num_kv_heads: int) -> int:
+    return max(d for d in range(1, 9) if num_kv_heads % d == 0)
+
+
+def decode_metadata(kv_indptr, last_page_len, *, num_qo_heads, num_kv_heads, num_ctas,
+                    page_size=16, fixed_split_pages=0, disable_split_kv=False):
+    kv_indptr = [int(x) for x in kv_indptr]
+    last_page_len = [int(x) for x in last_page_len]
+    B = len(kv_indptr) - 1
+    hpc = heads_per_cta(num_kv_heads)
+    nhb = num_kv_heads // hpc
+    group = num_qo_heads // num_kv_heads
+    npages = []
+    for b in range(B):
+        for _ in range(nhb):
+            npages.append(kv_indptr[b + 1] - kv_indptr[b])
+    R = B * nhb
+
+    per_cta = []
+    if disable_split_kv or fixed_split_pages > 0:
+        segs = []
+        for r in range(R):
+            c = npages[r] if disable_split_kv else fixed_split_pages
+            a = 0
+            while a < npages[r]:
+                segs.append([r, a, min(a + c, npages[r]), 0])
+                a += c
+        G = min(num_ctas, len(segs))
+        per_cta = [[] for _ in range(G)]
+        for k, s in enumerate(segs):
+            per_cta[k % G].append(s)
+    else:
+        T = sum(npages)
+        G = min(num_ctas, T)
+        per_cta = [[] for _ in range(G)]
+        starts = [0]
+        for n in npages:
+            starts.append(starts[-1] + n)
+        for i in range(G):
+            lo, hi = i * T // G, (i + 1) * T // G
+            for r in range(R):
+                a = max(lo, starts[r]) - starts[r]
+                e = min(hi, starts[r + 1]) - starts[r]
+                if e > a:
+                    per_cta[i].append([r, a, e, 0])
+
+    slot = 0
+    seg_count = [0] * R
+    row_slots = [[] for _ in range(R)]
+    for segs in per_cta:
+        for s in segs:
+            seg_count[s[0]] += 1
+            if s[1] == 0 and s[2] == npages[s[0]]:
+                s[3] = -1
+            else:
+                s[3] = slot
+                row_slots[s[0]].append((s[1], slot))
+                slot += 1
+    merge_rows, merge_ptr, merge_slots = [], [0], []
+    for r in range(R):
+        if npages[r] == 0 or seg_count[r] >= 2:
+            merge_rows.append(r)
+            merge_slots += [sl for _, sl in sorted(row_slots[r])]
+            merge_ptr.append(len(merge_slots))
+
+    req_page = [kv_indptr[b] for b in range(B)]
+    req_kv = []
+    for b in range(B):
+        n = kv_indptr[b + 1] - kv_indptr[b]
+        req_kv.append((n - 1) * page_size + last_page_len[b] if n > 0 else 0)
+    cta_ptr = [0]
+    flat = []
+    for segs in per_cta:
+        cta_ptr.append(cta_ptr[-1] + len(segs))
+        for s in segs:
+            flat += s
+
+    words = [0] * HEADER_WORDS
+    words[0] = MAGIC
+    words[1] = 0
+    words[2] = B
+    words[3] = nhb
+    words[4] = hpc
+    words[5] = group
+    words[6] = len(per_cta)
+    words[7] = sum(len(s) for s in per_cta)
+    words[8] = slot
+    words[9] = len(merge_rows)
+
+    def put(field, arr):
+        words[field] = len(words)
+        words.extend(arr)
+
+    put(10, req_page)
+    put(11, req_kv)
+    put(12, cta_ptr)
+    put(13, flat)
+    put(14, merge_ptr)
+    put(15, merge_rows)
+    put(16, merge_slots)
+    return words

@@ -1,0 +1,564 @@
+// decode.cu -- paged decode attention over an fp8 KV cache, and the split-KV
+// merge.  sm_103a.
+//
+// What it computes: for every request b and query head h (KV head
+// h / group), o = v_scale * softmax_j(sm_scale * q_scale * k_scale * q.k_j) V_j
+// over the request's kv_len cached tokens, with lse = ln sum_j exp(logit_j).
+// The KV bytes stay fp8 in HBM and are dequantized on load ("fp8 KV cache in
+// the in-tree prefill kernel", Kernel note and Architecture / design notes);
+// k_scale (with q_scale) folds into the softmax scale and v_scale multiplies
+// the output once, the two folds of that page's Test plan.
+//
+// Design (one persistent CTA per SM):
+//  * Warp `HPC` is the producer.  It walks the CTA's segments (row, page
+//    range) from the plan, prefetches 32 page indices per warp-wide load, and
+//    for each page issues one TMA box per KV head and tensor (16 tokens x 128
+//    bytes, 128B-swizzled) into a ring of shared-memory stages guarded by
+//    full/empty mbarriers.  Every wait is bounded; on expiry the kernel sets a
+//    status bit and returns after its copies in flight have landed.
+//  * Warps 0..HPC-1 are consumers, one per KV head of the block.  Each
+//    consumer keeps the whole GQA group (up to 8 query heads) of its KV head,
+//    so every KV byte is read from HBM once.  Per 16-token page:
+//      S^T[16 tok x 8 heads] = K[16 x 128] . Q^T   (m16n8k16, f16 in, f32 acc)
+//    with fp8 -> f16 conversion in registers (exact for e4m3fn and e5m2), an
+//    online softmax in the log2 domain (column max by warp shuffles), P
+//    transposed in registers with movmatrix, then
+//      O^T[128 x 8] += V^T[128 x 16 tok] . P^T.
+//    The head dimension is permuted consistently between K and Q (thread t
+//    owns dims 32t..32t+31 of every row) and between V and O (thread g owns
+//    dims 16g..16g+15), so every shared-memory read is one conflict-free
+//    16-byte load.
+//  * A segment covering its whole request writes o and lse; a partial one
+//    writes (O/l, lse in log2 units) to the workspace for the merge kernel.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "../../include/pafp8.h"
+#include "internal.h"
+
+namespace pafp8 {
+namespace {
+
+constexpr int D = kHeadDim;
+constexpr int P = kPageSize;
+constexpr int kTileBytes = P * D;           // one KV head of one page
+constexpr long long kWaitCycles = 2000000000LL;  // ~1 s at 2 GHz
+constexpr int kStageBudget = 192 * 1024;
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait for the phase of `parity` to complete; false after ~kWaitCycles.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity))
+        if (clock64() - t0 > kWaitCycles) return false;
+    return true;
+}
+
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int c0, int c1, int c2, int c3) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+    uint32_t r;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+    return r;
+}
+
+// Two fp8 codes (bytes 0,1 or 2,3 of w) -> f16x2, exactly.  e4m3fn uses the
+// hardware conversion; an e5m2 code is the high byte of the f16 with the same
+// value (same exponent bias and width, two mantissa bits instead of ten).
+template <int KT>
+__device__ __forceinline__ uint32_t fp8x2_lo(uint32_t w);
+template <int KT>
+__device__ __forceinline__ uint32_t fp8x2_hi(uint32_t w);
+
+template <>
+__device__ __forceinline__ uint32_t fp8x2_lo<PAFP8_E4M3FN>(uint32_t w) {
+    uint32_t r;
+    asm("{\n .reg .b16 l, h;\n mov.b32 {l, h}, %1;\n cvt.rn.f16x2.e4m3x2 %0, l;\n}\n"
+        : "=r"(r)
+        : "r"(w));
+    return r;
+}
+template <>
+__device__ __forceinline__ uint32_t fp8x2_hi<PAFP8_E4M3FN>(uint32_t w) {
+    uint32_t r;
+    asm("{\n .reg .b16 l, h;\n mov.b32 {l, h}, %1;\n cvt.rn.f16x2.e4m3x2 %0, h;\n}\n"
+        : "=r"(r)
+        : "r"(w));
+    return r;
+}
+template <>
+__device__ __forceinline__ uint32_t fp8x2_lo<PAFP8_E5M2>(uint32_t w) {
+    return prmt(w, 0u, 0x1404u);
+}
+template <>
+__device__ __forceinline__ uint32_t fp8x2_hi<PAFP8_E5M2>(uint32_t w) {
+    return prmt(w, 0u, 0x3424u);
+}
+
+__device__ __forceinline__ void mma_16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                          uint32_t a3, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7},"
+        " {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
+    uint32_t r;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(r) : "r"(x));
+    return r;
+}
+
+__device__ __forceinline__ float ex2(float x) {
+    float r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ uint32_t pack_out2(float lo, float hi, int o_dtype) {
+    if (o_dtype == PAFP8_BF16) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+        return *reinterpret_cast<uint32_t*>(&h);
+    }
+    return pack_half2(lo, hi);
+}
+
+__device__ __forceinline__ void flag(uint32_t* status, uint32_t bit) { atomicOr(status, bit); }
+
+// Q fragment for the QK product: B operand (K = head dim, N = 8 query heads).
+// Lane (g, t) holds head g of the group, dims 32t .. 32t+31, as 16 f16x2
+// words; word j = dims 32t+2j, 32t+2j+1.  Returns the power-of-two factor the
+// logits must be multiplied by (a bf16 query is brought into f16 range by an
+// exact power-of-two scaling when its magnitude needs it).
+template <int KT_UNUSED>
+__device__ __forceinline__ float load_q(uint32_t (&qf)[16], const void* q, int q_dtype,
+                                        size_t head_off, bool active, int t) {
+    float factor = 1.0f;
+    if (q_dtype == PAFP8_F16 || q_dtype == PAFP8_BF16) {
+        uint4 w[4] = {};
+        if (active) {
+            const uint4* src = reinterpret_cast<const uint4*>(
+                static_cast<const uint16_t*>(q) + head_off + 32 * t);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) w[i] = __ldg(src + i);
+        }
+        const uint32_t* ws = reinterpret_cast<const uint32_t*>(w);
+        if (q_dtype == PAFP8_F16) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) qf[j] = ws[j];
+        } else {
+            // Largest |q| over the warp decides the power-of-two shift.
+            uint32_t mx = 0;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                mx = max(mx, (ws[j] & 0x7FFFu) << 16);
+                mx = max(mx, ws[j] & 0x7FFF0000u);
+            }
+            mx = __reduce_max_sync(0xFFFFFFFFu, mx);
+            const int e = (int)((mx >> 23) & 0xFF) - 127;
+            const int shift = e > 14 ? e - 14 : 0;
+            const float down = __int_as_float((127 - shift) << 23);
+            factor = __int_as_float((127 + shift) << 23);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const float lo = __uint_as_float(ws[j] << 16) * down;
+                const float hi = __uint_as_float(ws[j] & 0xFFFF0000u) * down;
+                qf[j] = pack_half2(lo, hi);
+            }
+        }
+    } else {
+        uint4 w[2] = {};
+        if (active) {
+            const uint4* src = reinterpret_cast<const uint4*>(
+                static_cast<const uint8_t*>(q) + head_off + 32 * t);
+            w[0] = __ldg(src);
+            w[1] = __ldg(src + 1);
+        }
+        const uint32_t* ws = reinterpret_cast<const uint32_t*>(w);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            if (q_dtype == PAFP8_E4M3FN) {
+                qf[2 * j] = fp8x2_lo<PAFP8_E4M3FN>(ws[j]);
+                qf[2 * j + 1] = fp8x2_hi<PAFP8_E4M3FN>(ws[j]);
+            } else {
+                qf[2 * j] = fp8x2_lo<PAFP8_E5M2>(ws[j]);
+                qf[2 * j + 1] = fp8x2_hi<PAFP8_E5M2>(ws[j]);
+            }
+        }
+    }
+    return factor;
+}
+
+template <int KT>
+__global__ void __launch_bounds__(32 * 9, 1)
+    decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtensorMap tmk,
+                  const __grid_constant__ CUtensorMap tmv, int hpc, int group, int stages) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_addr(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;      // 128B swizzle wants 1024-B alignment
+    const uint32_t stage_bytes = 2u * hpc * kTileBytes;  // K heads then V heads
+    const uint32_t bar_full = base + stages * stage_bytes;
+    const uint32_t bar_empty = bar_full + 8u * stages;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int* meta = p.meta;
+    const int nhb = meta[kMetaHeadBlocks];
+    const int* req_page = meta + meta[kMetaOffReqPage];
+    const int* req_kv = meta + meta[kMetaOffReqKvLen];
+    const int* cta_seg = meta + meta[kMetaOffCtaSeg];
+    const int* segs = meta + meta[kMetaOffSeg];
+    const int seg_begin = cta_seg[blockIdx.x], seg_end = cta_seg[blockIdx.x + 1];
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < stages; ++s) {
+            mbar_init(bar_full + 8u * s, 1);
+            mbar_init(bar_empty + 8u * s, 32u * hpc);
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    __syncthreads();
+
+    if (warp == hpc) {
+        // ---------------------------------------------------------- producer
+        if (lane == 0) {
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmk)) : "memory");
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmv)) : "memory");
+        }
+        int stage = 0;
+        uint32_t phase = 0;
+        long long issued = 0;
+        bool ok = true;
+        for (int si = seg_begin; si < seg_end && ok; ++si) {
+            const int row = segs[4 * si], p0 = segs[4 * si + 1], p1 = segs[4 * si + 2];
+            const int b = row / nhb, hb = row - b * nhb;
+            const int* idx = p.kv_indices + req_page[b];
+            for (int pb = p0; pb < p1 && ok; pb += 32) {
+                const int n = min(32, p1 - pb);
+                int page = lane < n ? __ldg(idx + pb + lane) : 0;
+                const bool bad = lane < n && (page < 0 || page >= p.num_pages);
+                if (bad) page = 0;  // never read outside the pool
+                if (__any_sync(0xFFFFFFFFu, bad) && lane == 0) flag(p.status, kStatusBounds);
+                for (int j = 0; j < n; ++j) {
+                    const int pg = __shfl_sync(0xFFFFFFFFu, page, j);
+                    if (lane == 0) {
+                        if (!mbar_wait(bar_empty + 8u * stage, phase ^ 1u)) {
+                            ok = false;
+                        } else {
+                            const uint32_t fb = bar_full + 8u * stage;
+                            mbar_arrive_expect_tx(fb, stage_bytes);
+                            const uint32_t sk = base + stage * stage_bytes;
+                            const uint32_t sv = sk + hpc * kTileBytes;
+                            for (int h = 0; h < hpc; ++h) {
+                                tma_load_4d(sk + h * kTileBytes, &tmk, fb, 0, hb * hpc + h, 0, pg);
+                                tma_load_4d(sv + h * kTileBytes, &tmv, fb, 0, hb * hpc + h, 0, pg);
+                            }
+                            ++issued;
+                        }
+                    }
+                    ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+                    if (!ok) break;
+                    if (++stage == stages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+        }
+        if (lane == 0) {
+            if (!ok) flag(p.status, kStatusTimeout);
+            // Let every copy this CTA issued land before it may exit.
+            for (int s = 0; s < stages && s < issued; ++s) {
+                const long long times = (issued - 1 - s) / stages + 1;
+                if (!mbar_wait(bar_full + 8u * s, (uint32_t)((times - 1) & 1))) {
+                    flag(p.status, kStatusTimeout);
+                    break;
+                }
+            }
+        }
+        return;
+    }
+
+    // -------------------------------------------------------------- consumers
+    const int g = lane >> 2, t = lane & 3;
+    const int Hq = p.num_qo_heads;
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int si = seg_begin; si < seg_end && ok; ++si) {
+        const int row = segs[4 * si], p0 = segs[4 * si + 1], p1 = segs[4 * si + 2];
+        const int slot = segs[4 * si + 3];
+        const int b = row / nhb, hb = row - b * nhb;
+        const int kvh = hb * hpc + warp;
+        const int kv_len = req_kv[b];
+
+        uint32_t qf[16];
+        const size_t q_head_off = ((size_t)b * Hq + (size_t)kvh * group + g) * D;
+        const float qfactor = load_q<KT>(qf, p.q, p.q_dtype, q_head_off, g < group, t);
+        const float sc = p.sm_scale_log2 * qfactor;
+
+        float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+        float acc[8][4];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+
+        for (int pg = p0; pg < p1; ++pg) {
+            if (!mbar_wait(bar_full + 8u * stage, phase)) {
+                ok = false;
+                break;
+            }
+            const uint32_t kt = base + stage * stage_bytes + warp * kTileBytes;
+            const uint32_t vt = kt + hpc * kTileBytes;
+            // K rows g and g+8, 16-byte chunks 2t and 2t+1 (swizzled by row & 7 = g).
+            const uint4 k0 = lds128(kt + g * 128 + (((2 * t) ^ g) << 4));
+            const uint4 k1 = lds128(kt + g * 128 + (((2 * t + 1) ^ g) << 4));
+            const uint4 k2 = lds128(kt + (g + 8) * 128 + (((2 * t) ^ g) << 4));
+            const uint4 k3 = lds128(kt + (g + 8) * 128 + (((2 * t + 1) ^ g) << 4));
+            // V rows 2t, 2t+1, 2t+8, 2t+9, chunk g (swizzled by the row's low 3 bits).
+            uint4 v0 = lds128(vt + (2 * t) * 128 + ((g ^ (2 * t)) << 4));
+            uint4 v1 = lds128(vt + (2 * t + 1) * 128 + ((g ^ (2 * t + 1)) << 4));
+            uint4 v2 = lds128(vt + (2 * t + 8) * 128 + ((g ^ (2 * t)) << 4));
+            uint4 v3 = lds128(vt + (2 * t + 9) * 128 + ((g ^ (2 * t + 1)) << 4));
+            mbar_arrive(bar_empty + 8u * stage);
+            if (++stage == stages) {
+                stage = 0;
+                phase ^= 1u;
+            }
+
+            const int valid = kv_len - pg * P;  // tokens of this page that exist (>= 1)
+            if (valid < P) {
+                const uint4 z = make_uint4(0, 0, 0, 0);
+                if (2 * t >= valid) v0 = z;
+                if (2 * t + 1 >= valid) v1 = z;
+                if (2 * t + 8 >= valid) v2 = z;
+                if (2 * t + 9 >= valid) v3 = z;
+            }
+
+            // S^T = K . Q^T over 8 k-steps, two accumulators for ILP.
+            float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+            const uint32_t kr0[8] = {k0.x, k0.y, k0.z, k0.w, k1.x, k1.y, k1.z, k1.w};
+            const uint32_t kr8[8] = {k2.x, k2.y, k2.z, k2.w, k3.x, k3.y, k3.z, k3.w};
+#pragma unroll
+            for (int s = 0; s < 8; ++s) {
+                const uint32_t a0 = fp8x2_lo<KT>(kr0[s]), a1 = fp8x2_lo<KT>(kr8[s]);
+                const uint32_t a2 = fp8x2_hi<KT>(kr0[s]), a3 = fp8x2_hi<KT>(kr8[s]);
+                if (s & 1)
+                    mma_16816(sb, a0, a1, a2, a3, qf[2 * s], qf[2 * s + 1]);
+                else
+                    mma_16816(sa, a0, a1, a2, a3, qf[2 * s], qf[2 * s + 1]);
+            }
+            // (tok g | tok g+8) x (head 2t | head 2t+1), log2 units.
+            float x0 = (sa[0] + sb[0]) * sc, x1 = (sa[1] + sb[1]) * sc;
+            float x2 = (sa[2] + sb[2]) * sc, x3 = (sa[3] + sb[3]) * sc;
+            if (g >= valid) x0 = x1 = -INFINITY;
+            if (g + 8 >= valid) x2 = x3 = -INFINITY;
+            float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+#pragma unroll
+            for (int off = 4; off < 32; off <<= 1) {
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xFFFFFFFFu, mx0, off));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xFFFFFFFFu, mx1, off));
+            }
+            const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+            const float al0 = ex2(m0 - mn0), al1 = ex2(m1 - mn1);
+            const float e0 = ex2(x0 - mn0), e1 = ex2(x1 - mn1);
+            const float e2 = ex2(x2 - mn0), e3 = ex2(x3 - mn1);
+            l0 = l0 * al0 + e0 + e2;
+            l1 = l1 * al1 + e1 + e3;
+            m0 = mn0;
+            m1 = mn1;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                acc[i][0] *= al0;
+                acc[i][1] *= al1;
+                acc[i][2] *= al0;
+                acc[i][3] *= al1;
+            }
+            // P^T as the B operand: transpose the two 8x8 (token x head) blocks.
+            const uint32_t pb0 = movmatrix_t(pack_half2(e0, e1));
+            const uint32_t pb1 = movmatrix_t(pack_half2(e2, e3));
+
+            const uint32_t va[4] = {v0.x, v0.y, v0.z, v0.w}, vb[4] = {v1.x, v1.y, v1.z, v1.w};
+            const uint32_t vc[4] = {v2.x, v2.y, v2.z, v2.w}, vd[4] = {v3.x, v3.y, v3.z, v3.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const uint32_t ab_lo = prmt(va[j], vb[j], 0x5140u), ab_hi = prmt(va[j], vb[j], 0x7362u);
+                const uint32_t cd_lo = prmt(vc[j], vd[j], 0x5140u), cd_hi = prmt(vc[j], vd[j], 0x7362u);
+                mma_16816(acc[2 * j], fp8x2_lo<KT>(ab_lo), fp8x2_hi<KT>(ab_lo), fp8x2_lo<KT>(cd_lo),
+                          fp8x2_hi<KT>(cd_lo), pb0, pb1);
+                mma_16816(acc[2 * j + 1], fp8x2_lo<KT>(ab_hi), fp8x2_hi<KT>(ab_hi),
+                          fp8x2_lo<KT>(cd_hi), fp8x2_hi<KT>(cd_hi), pb0, pb1);
+            }
+        }
+        if (!ok) break;
+
+        // ------------------------------------------------------- epilogue
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+            l0 += __shfl_xor_sync(0xFFFFFFFFu, l0, off);
+            l1 += __shfl_xor_sync(0xFFFFFFFFu, l1, off);
+        }
+        // This lane holds dims 16g .. 16g+15 of heads 2t and 2t+1 of the group.
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            const int n = 2 * t + hh;
+            if (n >= group) continue;
+            const float l = hh ? l1 : l0, m = hh ? m1 : m0;
+            const float inv = 1.0f / l;
+            float vals[16];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                vals[2 * i] = acc[i][hh] * inv;
+                vals[2 * i + 1] = acc[i][2 + hh] * inv;
+            }
+            const int head = kvh * group + n;
+            if (slot < 0) {
+                const float vs = p.v_scale;
+                uint32_t w[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) w[i] = pack_out2(vals[2 * i] * vs, vals[2 * i + 1] * vs, p.o_dtype);
+                uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) +
+                                                      ((size_t)b * Hq + head) * D + 16 * g);
+                dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+                dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+                if (g == 0 && p.lse != nullptr)
+                    p.lse[(size_t)b * Hq + head] = (m + __log2f(l)) * 0.69314718055994531f;
+            } else {
+                const int hpb = hpc * group;
+                float4* dst = reinterpret_cast<float4*>(
+                    p.part_o + ((size_t)slot * hpb + warp * group + n) * D + 16 * g);
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    dst[i] = make_float4(vals[4 * i], vals[4 * i + 1], vals[4 * i + 2], vals[4 * i + 3]);
+                if (g == 0) p.part_lse[(size_t)slot * hpb + warp * group + n] = m + __log2f(l);
+            }
+        }
+    }
+    if (!ok && lane == 0) flag(p.status, kStatusTimeout);
+}
+
+// Combine the partial states of each split request (and write o = 0,
+// lse = -inf for requests with no KV).  Block = one (merge row, KV head of the
+// block), 128 threads = the head dimension.
+__global__ void __launch_bounds__(128)
+    merge_kernel(const __grid_constant__ DecodeParams p, int hpc, int group) {
+    const int* meta = p.meta;
+    const int nhb = meta[kMetaHeadBlocks];
+    const int* mptr = meta + meta[kMetaOffMergePtr];
+    const int* mrow = meta + meta[kMetaOffMergeRow];
+    const int* mslot = meta + meta[kMetaOffMergeSlot];
+    const int e = blockIdx.x, hl = blockIdx.y, d = threadIdx.x;
+    const int row = mrow[e];
+    const int b = row / nhb, hb = row - b * nhb;
+    const int s0 = mptr[e], s1 = mptr[e + 1];
+    const int hpb = hpc * group;
+    const int Hq = p.num_qo_heads;
+    for (int n = 0; n < group; ++n) {
+        const int hh = hl * group + n;
+        const int head = (hb * hpc + hl) * group + n;
+        float L = -INFINITY;
+        for (int s = s0; s < s1; ++s) L = fmaxf(L, p.part_lse[(size_t)mslot[s] * hpb + hh]);
+        float o = 0.f, lse = -INFINITY;
+        if (L != -INFINITY) {
+            float sum = 0.f;
+            for (int s = s0; s < s1; ++s) {
+                const float w = ex2(p.part_lse[(size_t)mslot[s] * hpb + hh] - L);
+                sum += w;
+                o += w * p.part_o[((size_t)mslot[s] * hpb + hh) * D + d];
+            }
+            o = o / sum * p.v_scale;
+            lse = (L + __log2f(sum)) * 0.69314718055994531f;
+        }
+        uint16_t* dst = static_cast<uint16_t*>(p.o) + ((size_t)b * Hq + head) * D + d;
+        if (p.o_dtype == PAFP8_BF16) {
+            __nv_bfloat16 h = __float2bfloat16_rn(o);
+            *dst = *reinterpret_cast<uint16_t*>(&h);
+        } else {
+            __half h = __float2half_rn(o);
+            *dst = *reinterpret_cast<uint16_t*>(&h);
+        }
+        if (d == 0 && p.lse != nullptr) p.lse[(size_t)b * Hq + head] = lse;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& tmap_k, const CUtensorMap& tmap_v,
+                          int num_ctas, int hpc, int group, cudaStream_t stream) {
+    const int stage_bytes = 2 * hpc * kTileBytes;
+    int stages = kStageBudget / stage_bytes;
+    if (stages > 8) stages = 8;
+    if (stages < 2) stages = 2;
+    const size_t smem = 1024 + (size_t)stages * stage_bytes + 16 * (size_t)stages;
+    const dim3 grid(num_ctas), block(32 * (hpc + 1));
+    cudaError_t e;
+    if (p.kv_dtype == PAFP8_E4M3FN) {
+        e = cudaFuncSetAttribute(decode_kernel<PAFP8_E4M3FN>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        decode_kernel<PAFP8_E4M3FN><<<grid, block, smem, stream>>>(p, tmap_k, tmap_v, hpc, group, stages);
+    } else {
+        e = cudaFuncSetAttribute(decode_kernel<PAFP8_E5M2>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        decode_kernel<PAFP8_E5M2><<<grid, block, smem, stream>>>(p, tmap_k, tmap_v, hpc, group, stages);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_merge(const DecodeParams& p, int num_merge, int hpc, int group,
+                         cudaStream_t stream) {
+    merge_kernel<<<dim3(num_merge, hpc), 128, 0, stream>>>(p, hpc, group);
+    return cudaGetLastError();
+}
+
+}  // namespace pafp8

@@ -1,0 +1,544 @@
+// host.cu -- the C ABI of libpafp8: validation and refusal sentences, the
+// split-KV plan scheduler, metadata upload and kernel dispatch.
+//
+// Refusals follow "fp8 KV cache in the in-tree prefill kernel", What changed /
+// Refusals and Test plan (refusals): every combination the kernels cannot
+// serve returns a status with a sentence naming the dtypes, k and v dtypes
+// must match at every run, and integer caches are refused rather than read as
+// values.  The o_data_type contract (fixed at plan, checked at run; fp8
+// outputs refused) follows "Enable Hopper FA3 FP8 attention in decode.py",
+// Changes table and the module-validation review note.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "../../include/pafp8.h"
+#include "internal.h"
+
+using namespace pafp8;
+
+namespace {
+
+thread_local std::string g_last_error;
+
+pafp8_status fail(pafp8_status st, const char* fmt, ...) {
+    char buf[1024];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return st;
+}
+
+const char* dtype_name(int32_t dt) {
+    switch (dt) {
+        case PAFP8_F16: return "float16";
+        case PAFP8_BF16: return "bfloat16";
+        case PAFP8_E4M3FN: return "float8_e4m3fn";
+        case PAFP8_E5M2: return "float8_e5m2";
+        case PAFP8_F32: return "float32";
+        case PAFP8_INT8: return "int8";
+        case PAFP8_UINT8: return "uint8";
+        case PAFP8_DTYPE_DEFAULT: return "default";
+        default: return "unknown";
+    }
+}
+
+bool is_fp8(int32_t dt) { return dt == PAFP8_E4M3FN || dt == PAFP8_E5M2; }
+bool is_2byte(int32_t dt) { return dt == PAFP8_F16 || dt == PAFP8_BF16; }
+
+pafp8_status check_kv_dtype(int32_t kv, const char* what) {
+    if (is_fp8(kv)) return PAFP8_OK;
+    if (kv == PAFP8_INT8 || kv == PAFP8_UINT8)
+        return fail(PAFP8_ERR_DTYPE,
+                    "%s has dtype %s: an integer cache has no floating-point reading, and this "
+                    "library refuses it rather than reading its bytes as fp8 or as 0..255 values; "
+                    "the cache must be float8_e4m3fn or float8_e5m2",
+                    what, dtype_name(kv));
+    if (is_2byte(kv))
+        return fail(PAFP8_ERR_DTYPE,
+                    "%s has dtype %s: a 2-byte KV cache is not served by this build; the cache "
+                    "must be float8_e4m3fn or float8_e5m2",
+                    what, dtype_name(kv));
+    if (kv == PAFP8_F32)
+        return fail(PAFP8_ERR_DTYPE,
+                    "%s has dtype float32, which is not served; the cache must be "
+                    "float8_e4m3fn or float8_e5m2",
+                    what);
+    return fail(PAFP8_ERR_DTYPE, "%s has an unknown dtype code %d", what, (int)kv);
+}
+
+pafp8_status check_q_dtype(int32_t q) {
+    if (is_2byte(q) || is_fp8(q)) return PAFP8_OK;
+    if (q == PAFP8_INT8 || q == PAFP8_UINT8 || q == PAFP8_F32)
+        return fail(PAFP8_ERR_DTYPE,
+                    "q has dtype %s, which is not served; the query must be float16, bfloat16, "
+                    "float8_e4m3fn or float8_e5m2",
+                    dtype_name(q));
+    return fail(PAFP8_ERR_DTYPE, "q has an unknown dtype code %d", (int)q);
+}
+
+pafp8_status check_o_dtype(int32_t o, int32_t q) {
+    if (is_2byte(o)) return PAFP8_OK;
+    if (is_fp8(o))
+        return fail(PAFP8_ERR_DTYPE,
+                    "o_data_type %s is refused: fp8 outputs are not produced; with q %s and an "
+                    "fp8 cache the output must be float16 or bfloat16",
+                    dtype_name(o), dtype_name(q));
+    return fail(PAFP8_ERR_DTYPE,
+                "o_data_type %s is not served; the output must be float16 or bfloat16",
+                dtype_name(o));
+}
+
+int heads_per_cta_for(int hkv) {
+    int best = 1;
+    for (int d = 1; d <= 8; ++d)
+        if (hkv % d == 0) best = d;
+    return best;
+}
+
+}  // namespace
+
+struct pafp8_plan {
+    pafp8_plan_desc desc;    // with defaults resolved
+    std::vector<int32_t> kv_indptr, last_page_len, qo_indptr;
+    std::vector<int32_t> meta;
+    int64_t nnz_pages = 0, nnz_qo = 0;
+    int heads_per_cta = 1, head_blocks = 1, group = 1;
+    int num_ctas = 0, num_partials = 0, num_merge = 0;
+    size_t meta_bytes = 0, part_o_off = 0, part_lse_off = 0, status_off = 0, ws_bytes = 0;
+    void* uploaded_ws = nullptr;
+};
+
+namespace {
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Decode partition.  Rows are (request b, KV-head block hb), row r = b*nhb + hb,
+// each holding the npages[b] pages of its request.  The rule:
+//   disable_split_kv: one segment per non-empty row; CTA i takes segments
+//                     i, i+G, i+2G, ... (G = min(num_ctas, #segments));
+//   fixed_split_pages c: rows cut into chunks of c pages, dealt the same way;
+//   balanced (default): with T the total pages over all rows and
+//                     G = min(num_ctas, T), CTA i takes the global page range
+//                     [floor(i*T/G), floor((i+1)*T/G)) of the rows laid end to
+//                     end, cut at row boundaries into segments.
+// A segment spanning its whole row writes the final output (slot -1); every
+// other segment writes a partial state to the next free slot (in segment
+// order).  Rows with no pages or with several segments are merged.
+void build_decode_meta(pafp8_plan* pl) {
+    const int B = pl->desc.batch;
+    const int nhb = pl->head_blocks;
+    const int R = B * nhb;
+    std::vector<int64_t> np(R);
+    for (int b = 0; b < B; ++b)
+        for (int hb = 0; hb < nhb; ++hb)
+            np[(size_t)b * nhb + hb] = pl->kv_indptr[b + 1] - pl->kv_indptr[b];
+
+    struct Seg { int32_t row, p0, p1, slot; };
+    std::vector<std::vector<Seg>> per_cta;
+    const int64_t target = pl->desc.num_ctas;
+
+    if (pl->desc.disable_split_kv || pl->desc.fixed_split_pages > 0) {
+        std::vector<Seg> segs;
+        for (int r = 0; r < R; ++r) {
+            if (np[r] == 0) continue;
+            const int64_t c = pl->desc.disable_split_kv ? np[r] : pl->desc.fixed_split_pages;
+            for (int64_t a = 0; a < np[r]; a += c)
+                segs.push_back({r, (int32_t)a, (int32_t)std::min<int64_t>(a + c, np[r]), 0});
+        }
+        const int64_t G = std::min<int64_t>(target, (int64_t)segs.size());
+        per_cta.assign((size_t)G, {});
+        for (size_t k = 0; k < segs.size(); ++k) per_cta[k % G].push_back(segs[k]);
+    } else {
+        int64_t T = 0;
+        for (int r = 0; r < R; ++r) T += np[r];
+        const int64_t G = std::min<int64_t>(target, T);
+        per_cta.assign((size_t)G, {});
+        std::vector<int64_t> row_start(R + 1, 0);
+        for (int r = 0; r < R; ++r) row_start[r + 1] = row_start[r] + np[r];
+        int r = 0;
+        for (int64_t i = 0; i < G; ++i) {
+            const int64_t lo = i * T / G, hi = (i + 1) * T / G;
+            while (r < R && row_start[r + 1] <= lo) ++r;
+            for (int rr = r; rr < R && row_start[rr] < hi; ++rr) {
+                const int64_t a = std::max(lo, row_start[rr]) - row_start[rr];
+                const int64_t e = std::min(hi, row_start[rr + 1]) - row_start[rr];
+                if (e > a) per_cta[i].push_back({rr, (int32_t)a, (int32_t)e, 0});
+            }
+        }
+    }
+
+    // Output slots and the merge lists.
+    std::vector<int> nseg_row(R, 0);
+    for (auto& v : per_cta)
+        for (auto& s : v) nseg_row[s.row]++;
+    int32_t nslot = 0;
+    std::vector<std::vector<std::pair<int32_t, int32_t>>> row_slots(R);  // (p0, slot)
+    for (auto& v : per_cta)
+        for (auto& s : v) {
+            if (s.p0 == 0 && s.p1 == np[s.row]) {
+                s.slot = -1;
+            } else {
+                s.slot = nslot++;
+                row_slots[s.row].push_back({s.p0, s.slot});
+            }
+        }
+    std::vector<int32_t> merge_rows, merge_ptr{0}, merge_slots;
+    for (int r = 0; r < R; ++r) {
+        if (np[r] == 0 || nseg_row[r] >= 2) {
+            std::sort(row_slots[r].begin(), row_slots[r].end());
+            merge_rows.push_back(r);
+            for (auto& ps : row_slots[r]) merge_slots.push_back(ps.second);
+            merge_ptr.push_back((int32_t)merge_slots.size());
+        }
+    }
+
+    const int G = (int)per_cta.size();
+    int nseg = 0;
+    for (auto& v : per_cta) nseg += (int)v.size();
+
+    std::vector<int32_t>& m = pl->meta;
+    m.assign(kMetaHeaderWords, 0);
+    auto put = [&](int field, const std::vector<int32_t>& arr) {
+        m[field] = (int32_t)m.size();
+        m.insert(m.end(), arr.begin(), arr.end());
+    };
+    m[kMetaMagic] = kMetaMagicValue;
+    m[kMetaMode] = PAFP8_MODE_DECODE;
+    m[kMetaBatch] = B;
+    m[kMetaHeadBlocks] = nhb;
+    m[kMetaHeadsPerCta] = pl->heads_per_cta;
+    m[kMetaGroup] = pl->group;
+    m[kMetaNumCtas] = G;
+    m[kMetaNumSegs] = nseg;
+    m[kMetaNumPartials] = nslot;
+    m[kMetaNumMerge] = (int32_t)merge_rows.size();
+    std::vector<int32_t> req_page(B), req_kv(B);
+    for (int b = 0; b < B; ++b) {
+        req_page[b] = pl->kv_indptr[b];
+        const int32_t n = pl->kv_indptr[b + 1] - pl->kv_indptr[b];
+        req_kv[b] = n > 0 ? (n - 1) * pl->desc.page_size + pl->last_page_len[b] : 0;
+    }
+    put(kMetaOffReqPage, req_page);
+    put(kMetaOffReqKvLen, req_kv);
+    std::vector<int32_t> cta_ptr(G + 1, 0), seg;
+    for (int i = 0; i < G; ++i) {
+        cta_ptr[i + 1] = cta_ptr[i] + (int32_t)per_cta[i].size();
+        for (auto& s : per_cta[i]) {
+            seg.push_back(s.row);
+            seg.push_back(s.p0);
+            seg.push_back(s.p1);
+            seg.push_back(s.slot);
+        }
+    }
+    put(kMetaOffCtaSeg, cta_ptr);
+    put(kMetaOffSeg, seg);
+    put(kMetaOffMergePtr, merge_ptr);
+    put(kMetaOffMergeRow, merge_rows);
+    put(kMetaOffMergeSlot, merge_slots);
+
+    pl->num_ctas = G;
+    pl->num_partials = nslot;
+    pl->num_merge = (int)merge_rows.size();
+}
+
+void layout_workspace(pafp8_plan* pl) {
+    const size_t heads = (size_t)pl->heads_per_cta * pl->group;
+    pl->meta_bytes = align_up(pl->meta.size() * sizeof(int32_t), 256);
+    pl->part_o_off = pl->meta_bytes;
+    pl->part_lse_off = align_up(pl->part_o_off + (size_t)pl->num_partials * heads * kHeadDim * 4, 256);
+    pl->status_off = align_up(pl->part_lse_off + (size_t)pl->num_partials * heads * 4, 256);
+    pl->ws_bytes = pl->status_off + 256;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = (PFN_cuTensorMapEncodeTiled_v12000)p;
+    }
+    return fn;
+}
+
+// 4-D map over one cache tensor [num_pages, P, Hkv, D] (bytes), dims listed
+// innermost first: (d, kv head, token slot, page).  One box is one KV head of
+// one page, 16 tokens x 128 bytes, landing in shared memory as [16][128] with
+// the 128-byte swizzle (16-byte chunk c of token row t stored at c ^ (t & 7)).
+pafp8_status encode_cache_map(CUtensorMap* map, const void* base, int num_pages, int hkv) {
+    auto enc = get_encode();
+    if (!enc) return fail(PAFP8_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    cuuint64_t dims[4] = {(cuuint64_t)kHeadDim, (cuuint64_t)hkv, (cuuint64_t)kPageSize,
+                          (cuuint64_t)num_pages};
+    cuuint64_t strides[3] = {(cuuint64_t)kHeadDim, (cuuint64_t)hkv * kHeadDim,
+                             (cuuint64_t)kPageSize * hkv * kHeadDim};
+    cuuint32_t box[4] = {(cuuint32_t)kHeadDim, 1, (cuuint32_t)kPageSize, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(base), dims, strides,
+                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(PAFP8_ERR_CUDA, "cuTensorMapEncodeTiled failed for the KV cache (CUresult %d)",
+                    (int)r);
+    return PAFP8_OK;
+}
+
+bool scale_ok(float s) { return std::isfinite(s) && s > 0.0f; }
+
+}  // namespace
+
+extern "C" {
+
+int32_t pafp8_abi_version(void) { return PAFP8_ABI_VERSION; }
+
+const char* pafp8_last_error(void) { return g_last_error.c_str(); }
+
+pafp8_status pafp8_plan_create(const pafp8_plan_desc* desc_in, const int32_t* kv_indptr_h,
+                               const int32_t* last_page_len_h, const int32_t* qo_indptr_h,
+                               pafp8_plan** out) {
+    if (out == nullptr) return fail(PAFP8_ERR_ARG, "out (plan pointer) is NULL");
+    *out = nullptr;
+    if (desc_in == nullptr) return fail(PAFP8_ERR_ARG, "plan description is NULL");
+    pafp8_plan_desc d = *desc_in;
+
+    if (d.mode != PAFP8_MODE_DECODE && d.mode != PAFP8_MODE_PREFILL)
+        return fail(PAFP8_ERR_ARG, "mode %d is neither decode (0) nor prefill (1)", (int)d.mode);
+    if (d.mode == PAFP8_MODE_PREFILL)
+        return fail(PAFP8_ERR_UNSUPPORTED, "prefill is not served by this build yet");
+
+    pafp8_status st;
+    if ((st = check_kv_dtype(d.kv_dtype, "the KV cache")) != PAFP8_OK) return st;
+    if ((st = check_q_dtype(d.q_dtype)) != PAFP8_OK) return st;
+    if (d.o_dtype == PAFP8_DTYPE_DEFAULT) d.o_dtype = is_2byte(d.q_dtype) ? d.q_dtype : PAFP8_BF16;
+    if ((st = check_o_dtype(d.o_dtype, d.q_dtype)) != PAFP8_OK) return st;
+
+    if (d.batch < 0) return fail(PAFP8_ERR_SHAPE, "batch %d is negative", (int)d.batch);
+    if (d.num_qo_heads <= 0 || d.num_kv_heads <= 0)
+        return fail(PAFP8_ERR_SHAPE, "head counts must be positive (num_qo_heads %d, num_kv_heads %d)",
+                    (int)d.num_qo_heads, (int)d.num_kv_heads);
+    if (d.num_qo_heads % d.num_kv_heads != 0)
+        return fail(PAFP8_ERR_SHAPE, "num_qo_heads %d is not a multiple of num_kv_heads %d",
+                    (int)d.num_qo_heads, (int)d.num_kv_heads);
+    const int group = d.num_qo_heads / d.num_kv_heads;
+    if (group > kMaxGroupDecode)
+        return fail(PAFP8_ERR_UNSUPPORTED,
+                    "decode serves up to %d query heads per KV head; got %d (%d / %d)",
+                    kMaxGroupDecode, group, (int)d.num_qo_heads, (int)d.num_kv_heads);
+    if (d.head_dim != kHeadDim)
+        return fail(PAFP8_ERR_UNSUPPORTED, "head_dim %d is not served by this build (only %d)",
+                    (int)d.head_dim, kHeadDim);
+    if (d.page_size != kPageSize)
+        return fail(PAFP8_ERR_UNSUPPORTED, "page_size %d is not served by this build (only %d)",
+                    (int)d.page_size, kPageSize);
+    if (d.num_pages < 0) return fail(PAFP8_ERR_SHAPE, "num_pages %d is negative", (int)d.num_pages);
+    if (std::isnan(d.sm_scale) || std::isinf(d.sm_scale))
+        return fail(PAFP8_ERR_ARG, "sm_scale is not finite");
+    if (d.sm_scale <= 0.0f) d.sm_scale = 1.0f / std::sqrt((float)d.head_dim);
+    if (d.fixed_split_pages < 0)
+        return fail(PAFP8_ERR_ARG, "fixed_split_pages %d is negative", (int)d.fixed_split_pages);
+    if (d.num_ctas < 0) return fail(PAFP8_ERR_ARG, "num_ctas %d is negative", (int)d.num_ctas);
+    if (d.batch > 0 && (kv_indptr_h == nullptr || last_page_len_h == nullptr))
+        return fail(PAFP8_ERR_ARG, "kv_indptr and last_page_len host arrays are required");
+    if (d.mode == PAFP8_MODE_DECODE && qo_indptr_h != nullptr)
+        return fail(PAFP8_ERR_ARG, "decode takes no qo_indptr (one query row per request)");
+
+    if (d.batch > 0 && kv_indptr_h[0] != 0)
+        return fail(PAFP8_ERR_SHAPE, "kv_indptr[0] is %d, not 0", (int)kv_indptr_h[0]);
+    for (int b = 0; b < d.batch; ++b) {
+        const int64_t n = (int64_t)kv_indptr_h[b + 1] - kv_indptr_h[b];
+        if (n < 0)
+            return fail(PAFP8_ERR_SHAPE, "kv_indptr decreases at request %d (%d -> %d)", b,
+                        (int)kv_indptr_h[b], (int)kv_indptr_h[b + 1]);
+        if (n > 0 && (last_page_len_h[b] < 1 || last_page_len_h[b] > d.page_size))
+            return fail(PAFP8_ERR_SHAPE, "last_page_len[%d] = %d is outside [1, %d]", b,
+                        (int)last_page_len_h[b], (int)d.page_size);
+        if (n > 0 && d.num_pages == 0)
+            return fail(PAFP8_ERR_SHAPE, "request %d has pages but num_pages is 0", b);
+    }
+
+    if (d.num_ctas == 0) {
+        int dev = 0, sms = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            sms <= 0) {
+            cudaGetLastError();
+            return fail(PAFP8_ERR_CUDA,
+                        "num_ctas is 0 and the SM count of the current device is unavailable");
+        }
+        d.num_ctas = sms;
+    }
+
+    pafp8_plan* pl = new pafp8_plan();
+    pl->desc = d;
+    pl->group = group;
+    pl->heads_per_cta = heads_per_cta_for(d.num_kv_heads);
+    pl->head_blocks = d.num_kv_heads / pl->heads_per_cta;
+    if (d.batch > 0) {
+        pl->kv_indptr.assign(kv_indptr_h, kv_indptr_h + d.batch + 1);
+        pl->last_page_len.assign(last_page_len_h, last_page_len_h + d.batch);
+    } else {
+        pl->kv_indptr.assign(1, 0);
+    }
+    pl->nnz_pages = pl->kv_indptr.back();
+    pl->nnz_qo = d.batch;
+    build_decode_meta(pl);
+    layout_workspace(pl);
+    *out = pl;
+    return PAFP8_OK;
+}
+
+void pafp8_plan_destroy(pafp8_plan* plan) { delete plan; }
+
+size_t pafp8_workspace_bytes(const pafp8_plan* plan) { return plan ? plan->ws_bytes : 0; }
+
+pafp8_status pafp8_plan_metadata(const pafp8_plan* plan, const int32_t** words, size_t* count) {
+    if (plan == nullptr || words == nullptr || count == nullptr)
+        return fail(PAFP8_ERR_ARG, "plan, words and count must be non-NULL");
+    *words = plan->meta.data();
+    *count = plan->meta.size();
+    return PAFP8_OK;
+}
+
+pafp8_status pafp8_plan_upload(pafp8_plan* plan, void* workspace, size_t workspace_bytes,
+                               void* stream) {
+    if (plan == nullptr) return fail(PAFP8_ERR_ARG, "plan is NULL");
+    if (workspace == nullptr) return fail(PAFP8_ERR_ARG, "workspace is NULL");
+    if ((uintptr_t)workspace % 256 != 0)
+        return fail(PAFP8_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+    if (workspace_bytes < plan->ws_bytes)
+        return fail(PAFP8_ERR_WORKSPACE, "workspace has %zu bytes; the plan needs %zu",
+                    workspace_bytes, plan->ws_bytes);
+    cudaStream_t s = (cudaStream_t)stream;
+    cudaError_t e = cudaMemcpyAsync(workspace, plan->meta.data(), plan->meta.size() * 4,
+                                    cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess)
+        e = cudaMemsetAsync((char*)workspace + plan->status_off, 0, 256, s);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(PAFP8_ERR_CUDA, "metadata upload failed: %s", cudaGetErrorString(e));
+    }
+    plan->uploaded_ws = workspace;
+    return PAFP8_OK;
+}
+
+pafp8_status pafp8_run(const pafp8_plan* plan, int32_t q_dtype, const void* q, int32_t k_dtype,
+                       const void* k_cache, int32_t v_dtype, const void* v_cache,
+                       const int32_t* kv_indices, float q_scale, float k_scale, float v_scale,
+                       int32_t o_dtype, void* o, float* lse, void* workspace,
+                       size_t workspace_bytes, void* stream) {
+    if (plan == nullptr) return fail(PAFP8_ERR_ARG, "plan is NULL");
+    const pafp8_plan_desc& d = plan->desc;
+    pafp8_status st;
+    if (k_dtype != v_dtype)
+        return fail(PAFP8_ERR_DTYPE, "k_cache has dtype %s but v_cache has %s",
+                    dtype_name(k_dtype), dtype_name(v_dtype));
+    if ((st = check_kv_dtype(k_dtype, "k_cache")) != PAFP8_OK) return st;
+    if ((st = check_q_dtype(q_dtype)) != PAFP8_OK) return st;
+    if ((st = check_o_dtype(o_dtype, q_dtype)) != PAFP8_OK) return st;
+    if (q_dtype != d.q_dtype)
+        return fail(PAFP8_ERR_DTYPE, "q has dtype %s but the plan was made for %s",
+                    dtype_name(q_dtype), dtype_name(d.q_dtype));
+    if (k_dtype != d.kv_dtype)
+        return fail(PAFP8_ERR_DTYPE, "the KV cache has dtype %s but the plan was made for %s",
+                    dtype_name(k_dtype), dtype_name(d.kv_dtype));
+    if (o_dtype != d.o_dtype)
+        return fail(PAFP8_ERR_DTYPE, "o has dtype %s but the plan fixed o_data_type %s",
+                    dtype_name(o_dtype), dtype_name(d.o_dtype));
+    if (!scale_ok(q_scale) || !scale_ok(k_scale) || !scale_ok(v_scale))
+        return fail(PAFP8_ERR_ARG, "scales must be finite and > 0 (q %g, k %g, v %g)",
+                    (double)q_scale, (double)k_scale, (double)v_scale);
+    if (is_2byte(q_dtype) && q_scale != 1.0f)
+        return fail(PAFP8_ERR_ARG,
+                    "q_scale %g given with a %s query: only an fp8 query is dequantized by "
+                    "q_scale, so it would be silently ignored",
+                    (double)q_scale, dtype_name(q_dtype));
+    if (workspace == nullptr || workspace != plan->uploaded_ws)
+        return fail(PAFP8_ERR_WORKSPACE,
+                    "workspace %p is not the one this plan's metadata was uploaded to (%p)",
+                    workspace, plan->uploaded_ws);
+    if (workspace_bytes < plan->ws_bytes)
+        return fail(PAFP8_ERR_WORKSPACE, "workspace has %zu bytes; the plan needs %zu",
+                    workspace_bytes, plan->ws_bytes);
+    if (plan->nnz_qo > 0 && (q == nullptr || o == nullptr))
+        return fail(PAFP8_ERR_ARG, "q and o must be non-NULL");
+    if (plan->nnz_pages > 0 && (k_cache == nullptr || v_cache == nullptr || kv_indices == nullptr))
+        return fail(PAFP8_ERR_ARG, "k_cache, v_cache and kv_indices must be non-NULL");
+    if (((uintptr_t)q | (uintptr_t)o | (uintptr_t)k_cache | (uintptr_t)v_cache) % 16 != 0)
+        return fail(PAFP8_ERR_ARG, "q, o, k_cache and v_cache must be 16-byte aligned");
+    if ((uintptr_t)lse % 4 != 0 || (uintptr_t)kv_indices % 4 != 0)
+        return fail(PAFP8_ERR_ARG, "lse and kv_indices must be 4-byte aligned");
+
+    cudaStream_t s = (cudaStream_t)stream;
+    char* ws = (char*)workspace;
+    DecodeParams p{};
+    p.q = q;
+    p.kv_indices = kv_indices;
+    p.o = o;
+    p.lse = lse;
+    p.meta = (const int32_t*)ws;
+    p.part_o = (float*)(ws + plan->part_o_off);
+    p.part_lse = (float*)(ws + plan->part_lse_off);
+    p.status = (uint32_t*)(ws + plan->status_off);
+    p.q_dtype = q_dtype;
+    p.kv_dtype = k_dtype;
+    p.o_dtype = o_dtype;
+    p.num_qo_heads = d.num_qo_heads;
+    p.num_kv_heads = d.num_kv_heads;
+    p.num_pages = d.num_pages;
+    p.sm_scale_log2 = (float)((double)d.sm_scale * (is_fp8(q_dtype) ? (double)q_scale : 1.0) *
+                              (double)k_scale * 1.4426950408889634);
+    p.v_scale = v_scale;
+
+    cudaError_t e = cudaSuccess;
+    if (plan->num_ctas > 0) {
+        CUtensorMap tk, tv;
+        if ((st = encode_cache_map(&tk, k_cache, d.num_pages, d.num_kv_heads)) != PAFP8_OK) return st;
+        if ((st = encode_cache_map(&tv, v_cache, d.num_pages, d.num_kv_heads)) != PAFP8_OK) return st;
+        e = launch_decode(p, tk, tv, plan->num_ctas, plan->heads_per_cta, plan->group, s);
+    }
+    if (e == cudaSuccess && plan->num_merge > 0)
+        e = launch_merge(p, plan->num_merge, plan->heads_per_cta, plan->group, s);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(PAFP8_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(e));
+    }
+    return PAFP8_OK;
+}
+
+pafp8_status pafp8_device_status(const pafp8_plan* plan, void* workspace, void* stream) {
+    if (plan == nullptr || workspace == nullptr) return fail(PAFP8_ERR_ARG, "plan and workspace are required");
+    cudaStream_t s = (cudaStream_t)stream;
+    uint32_t word = 0;
+    char* st_ptr = (char*)workspace + plan->status_off;
+    cudaError_t e = cudaMemcpyAsync(&word, st_ptr, 4, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(st_ptr, 0, 4, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(PAFP8_ERR_CUDA, "reading the device status failed: %s", cudaGetErrorString(e));
+    }
+    if (word & kStatusTimeout)
+        return fail(PAFP8_ERR_TIMEOUT, "a kernel's bounded pipeline wait expired (status 0x%x)", word);
+    if (word & kStatusBounds)
+        return fail(PAFP8_ERR_BOUNDS, "a page index outside [0, num_pages) was skipped (status 0x%x)",
+                    word);
+    return PAFP8_OK;
+}
+
+}  // extern "C"

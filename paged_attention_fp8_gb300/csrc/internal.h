@@ -1,0 +1,72 @@
+// internal.h -- declarations shared by the host code and the kernels of
+// libpafp8 (not part of the public ABI).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace pafp8 {
+
+constexpr int kHeadDim = 128;   // head_dim served by this build
+constexpr int kPageSize = 16;   // page_size served by this build
+constexpr int kMaxGroupDecode = 8;
+
+// Layout of the int32 partition metadata that the plan builds on the host and
+// uploads to the head of the workspace.  Word offsets of the variable-length
+// arrays are stored in the header.
+enum MetaHeader : int {
+    kMetaMagic = 0,      // 0x38464150 ("PAF8" little-endian)
+    kMetaMode,           // 0 decode, 1 prefill
+    kMetaBatch,
+    kMetaHeadBlocks,     // number of KV-head blocks (nhb)
+    kMetaHeadsPerCta,    // KV heads per block (hpc)
+    kMetaGroup,          // query heads per KV head
+    kMetaNumCtas,        // persistent CTAs of the main kernel (0: no launch)
+    kMetaNumSegs,
+    kMetaNumPartials,
+    kMetaNumMerge,
+    kMetaOffReqPage,     // int32[batch]   first entry of the request in kv_indices
+    kMetaOffReqKvLen,    // int32[batch]   kv_len of the request
+    kMetaOffCtaSeg,      // int32[num_ctas+1] CSR of segments per CTA
+    kMetaOffSeg,         // int32[4*num_segs] (row, page_begin, page_end, out_slot)
+    kMetaOffMergePtr,    // int32[num_merge+1]
+    kMetaOffMergeRow,    // int32[num_merge]
+    kMetaOffMergeSlot,   // int32[num_partials]
+    kMetaOffReqQo,       // int32[batch+1] qo_indptr (prefill)
+    kMetaNumTiles,       // prefill tiles
+    kMetaOffTile,        // int32[4*num_tiles] prefill tiles
+    kMetaTileRows,       // packed query rows per prefill tile
+    kMetaHeaderWords = 32
+};
+constexpr int32_t kMetaMagicValue = 0x38464150;
+
+// Status word bits written by the kernels into the workspace.
+enum : uint32_t {
+    kStatusBounds = 1u,   // a page index outside [0, num_pages)
+    kStatusTimeout = 2u,  // a bounded mbarrier wait expired
+};
+
+struct DecodeParams {
+    const void* q;           // [batch, Hq, D]
+    const int32_t* kv_indices;
+    void* o;                 // [batch, Hq, D]
+    float* lse;              // [batch, Hq] or nullptr
+    const int32_t* meta;     // device copy of the metadata words
+    float* part_o;           // [num_partials, hpc*group, D]
+    float* part_lse;         // [num_partials, hpc*group] (log2 domain)
+    uint32_t* status;
+    int q_dtype, kv_dtype, o_dtype;
+    int num_qo_heads, num_kv_heads, num_pages;
+    float sm_scale_log2;     // sm_scale * q_scale * k_scale * log2(e)
+    float v_scale;
+};
+
+// Launchers (decode.cu).  Return the launch's cudaError_t.
+cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& tmap_k,
+                          const CUtensorMap& tmap_v, int num_ctas, int heads_per_cta,
+                          int group, cudaStream_t stream);
+cudaError_t launch_merge(const DecodeParams& p, int num_merge, int heads_per_cta, int group,
+                         cudaStream_t stream);
+
+}  // namespace pafp8

@@ -1,0 +1,224 @@
+"""Host-side checks of libpafp8 (no GPU): the library loads and exports every
+entry point its header declares, the plan's partition words equal the
+independently restated rule bit for bit, the partition covers every page
+exactly once, and every refused dtype or shape combination returns a status
+and a sentence instead of running."""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+import torch
+
+import paged_attention_fp8_gb300 as pa
+from oracle import plan as plan_rule
+from paged_attention_fp8_gb300 import build as pbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built_library():
+    pbuild.build()
+    return pa.lib()
+
+
+def header_symbols():
+    text = open(os.path.join(ROOT, "include", "pafp8.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pafp8_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol():
+    syms = header_symbols()
+    assert "pafp8_run" in syms and "pafp8_plan_create" in syms
+    L = ctypes.CDLL(pa.LIB_PATH)
+    for s in syms:
+        assert hasattr(L, s), f"{s} declared in include/pafp8.h but not exported"
+    assert set(pa.EXPORTS) == set(syms)
+    assert pa.pafp8_abi_version() == 1
+
+
+# ------------------------------------------------------------------- plans
+
+def _decode_plan(kv_lens, *, hq=32, hkv=8, num_ctas=152, **kw):
+    P = 16
+    npages = [(L + P - 1) // P for L in kv_lens]
+    indptr = np.concatenate([[0], np.cumsum(npages)]).astype(np.int32)
+    last = np.array([(L - (n - 1) * P) if n else 0 for L, n in zip(kv_lens, npages)], dtype=np.int32)
+    plan = pa.Plan(mode="decode", num_qo_heads=hq, num_kv_heads=hkv, num_pages=max(1, int(indptr[-1])),
+                   kv_indptr=indptr, last_page_len=last, q_dtype="bf16", kv_dtype="e4m3fn",
+                   num_ctas=num_ctas, **kw)
+    ref = plan_rule.decode_metadata(indptr, last, num_qo_heads=hq, num_kv_heads=hkv,
+                                    num_ctas=num_ctas, fixed_split_pages=kw.get("fixed_split_pages", 0),
+                                    disable_split_kv=kw.get("disable_split_kv", False))
+    return plan, np.array(ref, dtype=np.int32), npages
+
+
+PLAN_CASES = [
+    dict(kv_lens=[37, 64, 100, 129], hq=8, hkv=2, num_ctas=152),
+    dict(kv_lens=[37, 64, 100, 129], hq=8, hkv=2, num_ctas=3),
+    dict(kv_lens=[0, 5, 0, 300, 17], hq=8, hkv=8, num_ctas=7),
+    dict(kv_lens=[32768] * 8, hq=64, hkv=8, num_ctas=152),
+    dict(kv_lens=list(range(512, 4097, 57))[:64], hq=32, hkv=8, num_ctas=152),
+    dict(kv_lens=[1000, 17, 4096], hq=32, hkv=8, num_ctas=152, fixed_split_pages=16),
+    dict(kv_lens=[1000, 17, 4096], hq=32, hkv=8, num_ctas=2, disable_split_kv=True),
+    dict(kv_lens=[100] * 5, hq=24, hkv=12, num_ctas=9),  # 12 KV heads -> blocks of 6
+    dict(kv_lens=[0, 0], hq=4, hkv=4, num_ctas=152),
+    dict(kv_lens=[], hq=4, hkv=4, num_ctas=152),
+]
+
+
+@pytest.mark.parametrize("case", PLAN_CASES)
+def test_plan_metadata_bit_exact(case):
+    plan, ref, _ = _decode_plan(**case)
+    got = plan.metadata()
+    assert got.dtype == np.int32
+    assert np.array_equal(got, ref)
+
+
+@pytest.mark.parametrize("case", PLAN_CASES)
+def test_plan_partition_covers_every_page_once(case):
+    plan, _, npages = _decode_plan(**case)
+    m = plan.metadata()
+    nhb = m[3]
+    G, nseg = m[6], m[7]
+    cta = m[m[12]:m[12] + G + 1]
+    segs = m[m[13]:m[13] + 4 * nseg].reshape(-1, 4)
+    cover = {}
+    for r, a, e, _ in segs:
+        for p in range(a, e):
+            key = (int(r), p)
+            assert key not in cover
+            cover[key] = 1
+    want = {(b * nhb + hb, p) for b, n in enumerate(npages) for hb in range(nhb) for p in range(n)}
+    assert set(cover) == want
+    assert cta[0] == 0 and cta[-1] == nseg and np.all(np.diff(cta) >= 1)
+    if not case.get("fixed_split_pages") and not case.get("disable_split_kv") and G > 0:
+        loads = [int((segs[cta[i]:cta[i + 1], 2] - segs[cta[i]:cta[i + 1], 1]).sum()) for i in range(G)]
+        assert max(loads) - min(loads) <= 1  # balanced to within one page
+
+
+def test_workspace_grows_with_partials():
+    p1, _, _ = _decode_plan([4096] * 4, num_ctas=1)
+    p2, _, _ = _decode_plan([4096] * 4, num_ctas=152)
+    assert p2.workspace_bytes > p1.workspace_bytes > 0
+
+
+# ---------------------------------------------------------------- refusals
+
+def _desc(**over):
+    d = dict(mode=0, batch=1, num_qo_heads=8, num_kv_heads=2, head_dim=128, page_size=16, num_pages=4,
+             q_dtype=pa.BF16, kv_dtype=pa.E4M3FN, o_dtype=0, sm_scale=0.0, fixed_split_pages=0,
+             disable_split_kv=0, num_ctas=4)
+    d.update(over)
+    return pa.plan_desc(**d)
+
+
+def _create(**over):
+    return pa.pafp8_plan_create(_desc(**over), np.array([0, 2], np.int32), np.array([5], np.int32))
+
+
+@pytest.mark.parametrize("kv,words", [
+    (pa.INT8, ["int8", "integer"]), (pa.UINT8, ["uint8", "integer"]), (pa.F32, ["float32"]),
+    (pa.F16, ["float16", "2-byte"]), (pa.BF16, ["bfloat16", "2-byte"]), (99, ["unknown"])])
+def test_plan_refuses_kv_dtype(kv, words):
+    with pytest.raises(pa.Pafp8Error) as ei:
+        _create(kv_dtype=kv)
+    assert ei.value.status == 1
+    for w in words:
+        assert w in str(ei.value)
+
+
+@pytest.mark.parametrize("q", [pa.F32, pa.INT8, pa.UINT8, 42])
+def test_plan_refuses_q_dtype(q):
+    with pytest.raises(pa.Pafp8Error) as ei:
+        _create(q_dtype=q)
+    assert ei.value.status == 1
+
+
+@pytest.mark.parametrize("o,word", [(pa.E4M3FN, "float8_e4m3fn"), (pa.E5M2, "float8_e5m2"),
+                                    (pa.F32, "float32"), (pa.INT8, "int8")])
+def test_plan_refuses_o_dtype(o, word):
+    with pytest.raises(pa.Pafp8Error) as ei:
+        _create(o_dtype=o)
+    assert ei.value.status == 1 and word in str(ei.value)
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(num_qo_heads=6, num_kv_heads=4), 2), (dict(head_dim=64), 8), (dict(page_size=32), 8),
+    (dict(num_qo_heads=32, num_kv_heads=2), 8), (dict(mode=5), 3), (dict(num_ctas=-1), 3),
+    (dict(fixed_split_pages=-2), 3), (dict(sm_scale=float("nan")), 3)])
+def test_plan_refuses_shapes_and_args(over, status):
+    with pytest.raises(pa.Pafp8Error) as ei:
+        _create(**over)
+    assert ei.value.status == status and len(str(ei.value)) > 20
+
+
+def test_plan_refuses_bad_page_table():
+    with pytest.raises(pa.Pafp8Error, match="last_page_len"):
+        pa.pafp8_plan_create(_desc(), np.array([0, 2], np.int32), np.array([17], np.int32))
+    with pytest.raises(pa.Pafp8Error, match="last_page_len"):
+        pa.pafp8_plan_create(_desc(), np.array([0, 2], np.int32), np.array([0], np.int32))
+    with pytest.raises(pa.Pafp8Error, match="decreases"):
+        pa.pafp8_plan_create(_desc(batch=2), np.array([0, 2, 1], np.int32), np.array([3, 3], np.int32))
+
+
+def test_default_o_dtype():
+    """o_data_type defaults to a 2-byte query's dtype and to bf16 for an fp8 query."""
+    import paged_attention_fp8_gb300 as m
+    for q, want in [(pa.F16, "float16"), (pa.BF16, "bfloat16"), (pa.E4M3FN, "bfloat16")]:
+        h = _create(q_dtype=q)
+        try:
+            # A run with a mismatched o dtype names the planned one.
+            other = pa.BF16 if want == "float16" else pa.F16
+            st = m.lib().pafp8_run(h, q, 16, pa.E4M3FN, 16, pa.E4M3FN, 16, 16, 1.0, 1.0, 1.0, other,
+                                   16, None, 256, 1 << 20, None)
+            assert st == 1 and want in pa.pafp8_last_error()
+        finally:
+            pa.pafp8_plan_destroy(h)
+
+
+@pytest.mark.parametrize("k,v,q,o,qs,status,word", [
+    (pa.E4M3FN, pa.E5M2, pa.BF16, pa.BF16, 1.0, 1, "v_cache has float8_e5m2"),
+    (pa.F16, pa.BF16, pa.BF16, pa.BF16, 1.0, 1, "k_cache has dtype float16 but v_cache has bfloat16"),
+    (pa.INT8, pa.INT8, pa.BF16, pa.BF16, 1.0, 1, "integer"),
+    (pa.E5M2, pa.E5M2, pa.BF16, pa.BF16, 1.0, 1, "plan was made for float8_e4m3fn"),
+    (pa.E4M3FN, pa.E4M3FN, pa.F16, pa.BF16, 1.0, 1, "plan was made for bfloat16"),
+    (pa.E4M3FN, pa.E4M3FN, pa.BF16, pa.E4M3FN, 1.0, 1, "refused"),
+    (pa.E4M3FN, pa.E4M3FN, pa.BF16, pa.BF16, 0.5, 3, "silently ignored"),
+])
+def test_run_refuses_before_touching_memory(k, v, q, o, qs, status, word):
+    """The run-time dtype checks come before any device access, so fake
+    (never dereferenced) pointers suffice here."""
+    h = _create()
+    try:
+        st = pa.lib().pafp8_run(h, q, 16, k, 16, v, 16, 16, qs, 1.0, 1.0, o, 16, None, 256, 1 << 20, None)
+        assert st == status
+        assert word in pa.pafp8_last_error()
+    finally:
+        pa.pafp8_plan_destroy(h)
+
+
+def test_run_refuses_workspace_not_uploaded():
+    h = _create()
+    try:
+        st = pa.lib().pafp8_run(h, pa.BF16, 16, pa.E4M3FN, 16, pa.E4M3FN, 16, 16, 1.0, 1.0, 1.0, pa.BF16,
+                                16, None, 256, 1 << 20, None)
+        assert st == 4 and "uploaded" in pa.pafp8_last_error()
+    finally:
+        pa.pafp8_plan_destroy(h)
+
+
+def test_run_refuses_bad_scales():
+    h = _create()
+    try:
+        for ks in (0.0, -1.0, float("inf"), float("nan")):
+            st = pa.lib().pafp8_run(h, pa.BF16, 16, pa.E4M3FN, 16, pa.E4M3FN, 16, 16, 1.0, ks, 1.0,
+                                    pa.BF16, 16, None, 256, 1 << 20, None)
+            assert st == 3 and "scales" in pa.pafp8_last_error()
+    finally:
+        pa.pafp8_plan_destroy(h)
