@@ -1,0 +1,386 @@
+#!/usr/bin/env python
+"""Benchmark of paged attention over an fp8 KV cache on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Headline workload: serving batch decode -- 64 requests with KV lengths
+uniform in [512, 4096], 32 query / 8 KV heads, head_dim 128, page 16, bf16
+query and output, e4m3fn KV cache with per-tensor scales (seeded, synthetic).
+A step is one pass of the decode hot path over that batch: the split-KV
+attention kernel and the LSE merge (the plan is built once, outside the timed
+region; the end-to-end figure re-plans every step).
+
+value = algorithmic bytes per step / device time per step, where the bytes
+count the fp8 K and V rows the requests own at 1 byte per element, plus q, o,
+lse and the page indices.  Split-KV partial states are not counted.
+
+Timing: W warm-up steps, then exactly K timed steps between a barrier and a
+device synchronize; an L2 flush (256 MiB write) separates the timed steps and
+sits outside the CUDA events that time each step on the launching stream.
+Under torchrun every rank runs the same workload on its own GPU (replicas, no
+collective on the data path) and rank 0 prints one JSON line with the max
+time over ranks.
+
+--impl reference times the CPU oracle (fp64, all host cores) on a bounded
+sample of the same workload, as the reference arm.
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import hashlib
+import io
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "paged fp8-KV decode HBM GB/s (% of peak); causal prefill TFLOPS (% of peak)"
+FALLBACK_HBM_GBS = 6800.0
+L2_FLUSH_BYTES = 256 << 20
+
+# DRAM bytes (read + write) per launch of the decode kernel on the serving
+# workload, from one ncu capture of the kernel source with this SHA-256; a
+# changed kernel reports null until it is captured again.
+NCU_TRAFFIC = {}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def decode_bytes(b) -> int:
+    """Algorithmic bytes of one decode pass over batch b."""
+    qb = 1 if b.q_dtype in ("e4m3fn", "e5m2") else 2
+    kv = b.kv_bytes()
+    q = b.nnz_qo * b.num_qo_heads * b.head_dim * qb
+    o = b.nnz_qo * b.num_qo_heads * b.head_dim * 2
+    lse = b.nnz_qo * b.num_qo_heads * 4
+    idx = 4 * int(b.kv_indptr[-1])
+    return kv + q + o + lse + idx
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_sha(name: str) -> str:
+    with open(os.path.join(ROOT, "paged_attention_fp8_gb300", "csrc", name), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+
+    FIELDS = ["index", "clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, gpu_id: str):
+        self.proc = None
+        self.file = tempfile.NamedTemporaryFile(mode="w+", suffix=".csv", delete=False)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", gpu_id, "--query-gpu=" + ",".join(self.FIELDS),
+                 "--format=csv,noheader,nounits", "-lms", "20"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        rows = [r for r in csv.reader(io.StringIO(self.file.read())) if len(r) == len(self.FIELDS)]
+        self.file.close()
+        os.unlink(self.file.name)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, r[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def gpu_id_for(torch, dev) -> str:
+    try:
+        u = str(torch.cuda.get_device_properties(dev).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        return str(dev.index or 0)
+
+
+def oracle_decode_rate(b, budget_s: float = 12.0):
+    """Oracle GB/s on a prefix of the batch's requests (doubling until the
+    last run takes ~budget_s/2 or covers every request)."""
+    import numpy as np
+
+    import oracle
+    from paged_attention_fp8_gb300.workloads import raw_numpy
+
+    raw = dict(q=raw_numpy(b.q), k=raw_numpy(b.k_cache), v=raw_numpy(b.v_cache))
+    n = 1
+    while True:
+        rows = np.repeat(np.arange(n), b.num_qo_heads)
+        heads = np.tile(np.arange(b.num_qo_heads), n)
+        t0 = time.perf_counter()
+        oracle.paged_attention(q=raw["q"], q_dtype=b.q_dtype, k_cache=raw["k"], v_cache=raw["v"],
+                               kv_dtype=b.kv_dtype, qo_indptr=b.qo_indptr.numpy(),
+                               kv_indptr=b.kv_indptr.numpy(), kv_indices=b.kv_indices.numpy(),
+                               last_page_len=b.last_page_len.numpy(), num_qo_heads=b.num_qo_heads,
+                               num_kv_heads=b.num_kv_heads, q_scale=b.q_scale, k_scale=b.k_scale,
+                               v_scale=b.v_scale, sm_scale=b.sm_scale, causal=False, rows=rows,
+                               heads=heads)
+        dt = time.perf_counter() - t0
+        if dt >= budget_s / 2 or n >= b.batch:
+            break
+        n = min(b.batch, max(n + 1, int(n * min(4.0, budget_s / 2 / max(dt, 1e-3)))))
+    kv_tokens = sum(b.kv_lens[:n])
+    by = 2 * kv_tokens * b.num_kv_heads * b.head_dim + n * b.num_qo_heads * b.head_dim * 6 + \
+        4 * int(b.kv_indptr[n])
+    return by / dt / 1e9, n, dt, oracle.num_threads()
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    from paged_attention_fp8_gb300.workloads import WORKLOADS, workload
+
+    b = workload(2)
+    times, rates = [], []
+    budget = max(2.0, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
+    for i in range(args.warmup + args.steps):
+        gbs, n, dt, cores = oracle_decode_rate(b, budget)
+        if i >= args.warmup:
+            rates.append(gbs)
+            times.append(dt)
+    value = statistics.median(rates)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * statistics.median(times), 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOADS[2], "batch": b.batch, "num_qo_heads": b.num_qo_heads,
+                   "num_kv_heads": b.num_kv_heads, "head_dim": b.head_dim, "page_size": b.page_size,
+                   "kv_dtype": b.kv_dtype, "q_dtype": b.q_dtype, "o_dtype": b.o_dtype,
+                   "parallelism": f"replicas{args.gpus}"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": f"first {n} of {b.batch} requests, every query head, per step"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import paged_attention_fp8_gb300 as pa
+    from paged_attention_fp8_gb300 import build as pbuild
+    from paged_attention_fp8_gb300.workloads import TORCH_DTYPES, WORKLOADS, workload
+
+    world, rank, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pbuild.build()
+
+    b = workload(2)
+    nbytes = decode_bytes(b)
+    q = b.q.to(dev)
+    k = b.k_cache.to(dev)
+    v = b.v_cache.to(dev)
+    idx = b.kv_indices.to(dev)
+    plan = pa.Plan(mode="decode", num_qo_heads=b.num_qo_heads, num_kv_heads=b.num_kv_heads,
+                   num_pages=b.num_pages, kv_indptr=b.kv_indptr, last_page_len=b.last_page_len,
+                   q_dtype=b.q_dtype, kv_dtype=b.kv_dtype, o_dtype=b.o_dtype, sm_scale=b.sm_scale)
+    meta = plan.metadata()
+    num_ctas, num_merge = int(meta[6]), int(meta[9])
+    ws = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device=dev)
+    plan.upload(ws)
+    o = torch.empty(b.batch, b.num_qo_heads, b.head_dim, dtype=TORCH_DTYPES[b.o_dtype], device=dev)
+    lse = torch.empty(b.batch, b.num_qo_heads, dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    scales = dict(q_scale=b.q_scale, k_scale=b.k_scale, v_scale=b.v_scale)
+    stream = torch.cuda.current_stream()
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        plan.run_stage(1, q, k, v, idx, o, lse, ws, **scales)
+        if ev is not None:
+            ev[1].record(stream)
+        plan.run_stage(2, q, k, v, idx, o, lse, ws, **scales)
+        if ev is not None:
+            ev[2].record(stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    plan.device_status(ws)
+
+    launches_per_step = (1 if num_ctas > 0 else 0) + (1 if num_merge > 0 else 0)
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    sampler = ClockSampler(gpu_id_for(torch, dev)) if rank == 0 else None
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()
+        step(events[i])
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    wall = time.perf_counter() - t0
+    clocks = sampler.stop() if sampler else None
+    plan.device_status(ws)
+    dec_ms = [e[0].elapsed_time(e[1]) for e in events]
+    step_ms = [e[0].elapsed_time(e[2]) for e in events]
+    ms_step = statistics.mean(step_ms)
+    ms_dec = statistics.mean(dec_ms)
+    if world > 1:
+        t = torch.tensor([ms_step, ms_dec], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_step, ms_dec = float(t[0]), float(t[1])
+
+    # ---- end to end through the public API: re-plan, H2D inputs from pinned
+    # host memory, run, D2H of the result, every step.
+    q_h = b.q.pin_memory()
+    idx_h = b.kv_indices.pin_memory()
+    o_h = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    indptr_h, last_h = b.kv_indptr.numpy(), b.last_page_len.numpy()
+    h2d = q_h.numel() * q_h.element_size() + idx_h.numel() * 4 + int(meta.size) * 4
+    d2h = o_h.numel() * o_h.element_size() + lse_h.numel() * 4
+    e2e_steps = max(1, min(args.e2e_steps, args.steps))
+
+    def e2e_step():
+        p2 = pa.Plan(mode="decode", num_qo_heads=b.num_qo_heads, num_kv_heads=b.num_kv_heads,
+                     num_pages=b.num_pages, kv_indptr=indptr_h, last_page_len=last_h,
+                     q_dtype=b.q_dtype, kv_dtype=b.kv_dtype, o_dtype=b.o_dtype, sm_scale=b.sm_scale)
+        p2.upload(ws)
+        q.copy_(q_h, non_blocking=True)
+        idx.copy_(idx_h, non_blocking=True)
+        p2.run(q, k, v, idx, o, lse, ws, **scales)
+        o_h.copy_(o, non_blocking=True)
+        lse_h.copy_(lse, non_blocking=True)
+        torch.cuda.synchronize()
+        return p2
+
+    for _ in range(3):
+        e2e_step()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t1 = time.perf_counter()
+    for _ in range(e2e_steps):
+        last_plan = e2e_step()
+    torch.cuda.synchronize()
+    e2e_s = (time.perf_counter() - t1) / e2e_steps
+    last_plan.device_status(ws)
+    if world > 1:
+        t = torch.tensor([e2e_s], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_s = float(t[0])
+
+    if rank != 0:
+        dist.destroy_process_group()
+        return
+
+    peak, peak_kind = measured_peaks()
+    achieved = nbytes / (ms_dec * 1e-3) / 1e9
+    sha = kernel_sha("decode.cu")
+    traffic = NCU_TRAFFIC.get(sha)
+    value = world * nbytes / (ms_step * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": f"{b.kv_dtype} KV -> f16 MMA, f32 accumulate ({b.q_dtype} q, {b.o_dtype} o)",
+        "data": "synthetic",
+        "config": {"workload": WORKLOADS[2], "batch": b.batch, "num_qo_heads": b.num_qo_heads,
+                   "num_kv_heads": b.num_kv_heads, "head_dim": b.head_dim, "page_size": b.page_size,
+                   "kv_tokens": sum(b.kv_lens), "bytes_per_step": nbytes,
+                   "parallelism": f"replicas{world}", "num_ctas": num_ctas, "merge_rows": num_merge,
+                   "l2": "flushed between timed steps (256 MiB write outside the events); KV 303 MB > L2",
+                   "timed_region_s": round(wall, 4)},
+        "roofline": {"bound": "hbm", "kernel": "decode_kernel", "achieved": round(achieved, 1),
+                     "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "peak_kind": peak_kind, "traffic": traffic,
+                     "algorithmic_bytes": nbytes, "ms_per_launch": round(ms_dec, 5)},
+        "e2e": {"value": round(world * nbytes / e2e_s / 1e9, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": round(e2e_s * 1e3, 4),
+                "includes": "host plan + metadata upload + H2D q/kv_indices + run + D2H o/lse; "
+                            "KV cache resident in HBM"},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        gbs, n, dt, cores = oracle_decode_rate(b)
+        line["cpu_baseline"] = {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                                "sample": f"first {n} of {b.batch} requests, every query head "
+                                          f"({dt:.1f} s, fp64)"}
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

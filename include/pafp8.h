@@ -181,6 +181,21 @@ pafp8_status pafp8_run(const pafp8_plan *plan, int32_t q_dtype, const void *q,
                        int32_t o_dtype, void *o, float *lse, void *workspace,
                        size_t workspace_bytes, void *stream);
 
+/* pafp8_run restricted to one stage of the launch sequence, for callers that
+ * time or overlap the stages separately:
+ *   stage 0  everything (same as pafp8_run);
+ *   stage 1  the attention kernel only (decode: it writes the outputs of
+ *            unsplit requests and the partial states of split ones);
+ *   stage 2  the split-KV merge only (decode: combines the partial states of
+ *            split requests, writes o = 0 / lse = -inf for empty ones).
+ * Running stage 1 then stage 2 on one stream equals stage 0.  Arguments and
+ * checks are those of pafp8_run. */
+pafp8_status pafp8_run_stage(const pafp8_plan *plan, int32_t stage, int32_t q_dtype, const void *q,
+                             int32_t k_dtype, const void *k_cache, int32_t v_dtype,
+                             const void *v_cache, const int32_t *kv_indices, float q_scale,
+                             float k_scale, float v_scale, int32_t o_dtype, void *o, float *lse,
+                             void *workspace, size_t workspace_bytes, void *stream);
+
 /* Synchronize `stream`, read and clear the workspace status word that the
  * kernels set.  Returns PAFP8_OK, PAFP8_ERR_BOUNDS (a page index was out of
  * range) or PAFP8_ERR_TIMEOUT (a bounded pipeline wait expired). */

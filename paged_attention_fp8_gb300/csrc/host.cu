@@ -441,7 +441,18 @@ pafp8_status pafp8_run(const pafp8_plan* plan, int32_t q_dtype, const void* q, i
                        const int32_t* kv_indices, float q_scale, float k_scale, float v_scale,
                        int32_t o_dtype, void* o, float* lse, void* workspace,
                        size_t workspace_bytes, void* stream) {
+    return pafp8_run_stage(plan, 0, q_dtype, q, k_dtype, k_cache, v_dtype, v_cache, kv_indices,
+                           q_scale, k_scale, v_scale, o_dtype, o, lse, workspace, workspace_bytes,
+                           stream);
+}
+
+pafp8_status pafp8_run_stage(const pafp8_plan* plan, int32_t stage, int32_t q_dtype, const void* q,
+                             int32_t k_dtype, const void* k_cache, int32_t v_dtype,
+                             const void* v_cache, const int32_t* kv_indices, float q_scale,
+                             float k_scale, float v_scale, int32_t o_dtype, void* o, float* lse,
+                             void* workspace, size_t workspace_bytes, void* stream) {
     if (plan == nullptr) return fail(PAFP8_ERR_ARG, "plan is NULL");
+    if (stage < 0 || stage > 2) return fail(PAFP8_ERR_ARG, "stage %d is not 0, 1 or 2", (int)stage);
     const pafp8_plan_desc& d = plan->desc;
     pafp8_status st;
     if (k_dtype != v_dtype)
@@ -505,13 +516,13 @@ pafp8_status pafp8_run(const pafp8_plan* plan, int32_t q_dtype, const void* q, i
     p.v_scale = v_scale;
 
     cudaError_t e = cudaSuccess;
-    if (plan->num_ctas > 0) {
+    if (stage != 2 && plan->num_ctas > 0) {
         CUtensorMap tk, tv;
         if ((st = encode_cache_map(&tk, k_cache, d.num_pages, d.num_kv_heads)) != PAFP8_OK) return st;
         if ((st = encode_cache_map(&tv, v_cache, d.num_pages, d.num_kv_heads)) != PAFP8_OK) return st;
         e = launch_decode(p, tk, tv, plan->num_ctas, plan->heads_per_cta, plan->group, s);
     }
-    if (e == cudaSuccess && plan->num_merge > 0)
+    if (e == cudaSuccess && stage != 1 && plan->num_merge > 0)
         e = launch_merge(p, plan->num_merge, plan->heads_per_cta, plan->group, s);
     if (e != cudaSuccess) {
         cudaGetLastError();
