@@ -49,7 +49,7 @@ def test_group_and_head_block_shapes(cuda_device, hq, hkv):
     ("e4m3fn", "e5m2", "bf16")])
 def test_dtype_combinations(cuda_device, q_dtype, kv_dtype, o_dtype):
     b = make_batch(RAGGED, num_qo_heads=16, num_kv_heads=4, q_dtype=q_dtype, kv_dtype=kv_dtype,
-                   o_dtype=o_dtype, seed=5, pool_pages=80)
+                   o_dtype=o_dtype, seed=5, pool_pages=140)
     o, lse = run_gpu(b, cuda_device, num_ctas=16)
     ro, rl = oracle_on(b)
     assert_close(o, lse, ro, rl, f"{q_dtype}/{kv_dtype}/{o_dtype}")
