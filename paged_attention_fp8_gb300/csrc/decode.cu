@@ -35,144 +35,17 @@
 
 #include "../../include/pafp8.h"
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace pafp8 {
 namespace {
 
+using namespace ptx;
+
 constexpr int D = kHeadDim;
 constexpr int P = kPageSize;
 constexpr int kTileBytes = P * D;           // one KV head of one page
-constexpr long long kWaitCycles = 2000000000LL;  // ~1 s at 2 GHz
-constexpr int kStageBudget = 192 * 1024;
-
-__device__ __forceinline__ uint32_t smem_addr(const void* p) {
-    return (uint32_t)__cvta_generic_to_shared(p);
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-        " selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-// Wait for the phase of `parity` to complete; false after ~kWaitCycles.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const long long t0 = clock64();
-    while (!mbar_try_wait(bar, parity))
-        if (clock64() - t0 > kWaitCycles) return false;
-    return true;
-}
-
-__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
-                                            int c0, int c1, int c2, int c3) {
-    asm volatile(
-        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
-        : "memory");
-}
-
-__device__ __forceinline__ uint4 lds128(uint32_t addr) {
-    uint4 v;
-    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "r"(addr)
-                 : "memory");
-    return v;
-}
-
-__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
-    uint32_t r;
-    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
-    return r;
-}
-
-// Two fp8 codes (bytes 0,1 or 2,3 of w) -> f16x2, exactly.  e4m3fn uses the
-// hardware conversion; an e5m2 code is the high byte of the f16 with the same
-// value (same exponent bias and width, two mantissa bits instead of ten).
-template <int KT>
-__device__ __forceinline__ uint32_t fp8x2_lo(uint32_t w);
-template <int KT>
-__device__ __forceinline__ uint32_t fp8x2_hi(uint32_t w);
-
-template <>
-__device__ __forceinline__ uint32_t fp8x2_lo<PAFP8_E4M3FN>(uint32_t w) {
-    uint32_t r;
-    asm("{\n .reg .b16 l, h;\n mov.b32 {l, h}, %1;\n cvt.rn.f16x2.e4m3x2 %0, l;\n}\n"
-        : "=r"(r)
-        : "r"(w));
-    return r;
-}
-template <>
-__device__ __forceinline__ uint32_t fp8x2_hi<PAFP8_E4M3FN>(uint32_t w) {
-    uint32_t r;
-    asm("{\n .reg .b16 l, h;\n mov.b32 {l, h}, %1;\n cvt.rn.f16x2.e4m3x2 %0, h;\n}\n"
-        : "=r"(r)
-        : "r"(w));
-    return r;
-}
-template <>
-__device__ __forceinline__ uint32_t fp8x2_lo<PAFP8_E5M2>(uint32_t w) {
-    return prmt(w, 0u, 0x1404u);
-}
-template <>
-__device__ __forceinline__ uint32_t fp8x2_hi<PAFP8_E5M2>(uint32_t w) {
-    return prmt(w, 0u, 0x3424u);
-}
-
-__device__ __forceinline__ void mma_16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                          uint32_t a3, uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7},"
-        " {%8, %9}, {%0, %1, %2, %3};"
-        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
-    uint32_t r;
-    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(r) : "r"(x));
-    return r;
-}
-
-__device__ __forceinline__ float ex2(float x) {
-    float r;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
-    return r;
-}
-
-__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
-    __half2 h = __floats2half2_rn(lo, hi);
-    return *reinterpret_cast<uint32_t*>(&h);
-}
-
-__device__ __forceinline__ uint32_t pack_out2(float lo, float hi, int o_dtype) {
-    if (o_dtype == PAFP8_BF16) {
-        __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
-        return *reinterpret_cast<uint32_t*>(&h);
-    }
-    return pack_half2(lo, hi);
-}
-
+constexpr int kStageBudget = 192 * 1024;    // shared memory for the page ring
 __device__ __forceinline__ void flag(uint32_t* status, uint32_t bit) { atomicOr(status, bit); }
 
 // Q fragment for the QK product: B operand (K = head dim, N = 8 query heads).

@@ -252,6 +252,66 @@ void build_decode_meta(pafp8_plan* pl) {
     pl->num_merge = (int)merge_rows.size();
 }
 
+// Prefill work tiles: for every request b, KV head hk and block of
+// TQ = 128 / group consecutive new tokens starting at t0, one tile of
+// TQ * group packed query rows.  n_kv = the KV tiles of 128 keys the tile's
+// last token may see (bottom-right causal).  Tiles are ordered longest first
+// (stable), and persistent CTA i takes tiles i, i + G, ... (G = min(num_ctas,
+// #tiles)).
+void build_prefill_meta(pafp8_plan* pl) {
+    const int B = pl->desc.batch;
+    const int g = pl->group;
+    const int TQ = kTileRows / g;
+    struct T { int32_t b, hk, t0, nkv; };
+    std::vector<T> tiles;
+    std::vector<int32_t> req_page(B), req_kv(B);
+    for (int b = 0; b < B; ++b) {
+        req_page[b] = pl->kv_indptr[b];
+        const int32_t n = pl->kv_indptr[b + 1] - pl->kv_indptr[b];
+        req_kv[b] = n > 0 ? (n - 1) * pl->desc.page_size + pl->last_page_len[b] : 0;
+        const int qo = pl->qo_indptr[b + 1] - pl->qo_indptr[b];
+        for (int hk = 0; hk < pl->desc.num_kv_heads; ++hk)
+            for (int t0 = 0; t0 < qo; t0 += TQ) {
+                const int last = std::min(t0 + TQ, qo) - 1;
+                const int lim = last + req_kv[b] - qo;
+                const int nkv = std::min((req_kv[b] + kTileKeys - 1) / kTileKeys, lim / kTileKeys + 1);
+                tiles.push_back({b, hk, t0, nkv});
+            }
+    }
+    std::stable_sort(tiles.begin(), tiles.end(), [](const T& a, const T& c) { return a.nkv > c.nkv; });
+    const int G = (int)std::min<int64_t>(pl->desc.num_ctas, (int64_t)tiles.size());
+
+    std::vector<int32_t>& m = pl->meta;
+    m.assign(kMetaHeaderWords, 0);
+    auto put = [&](int field, const std::vector<int32_t>& arr) {
+        m[field] = (int32_t)m.size();
+        m.insert(m.end(), arr.begin(), arr.end());
+    };
+    m[kMetaMagic] = kMetaMagicValue;
+    m[kMetaMode] = PAFP8_MODE_PREFILL;
+    m[kMetaBatch] = B;
+    m[kMetaHeadBlocks] = pl->desc.num_kv_heads;
+    m[kMetaHeadsPerCta] = 1;
+    m[kMetaGroup] = g;
+    m[kMetaNumCtas] = G;
+    m[kMetaNumTiles] = (int32_t)tiles.size();
+    m[kMetaTileRows] = TQ;
+    put(kMetaOffReqPage, req_page);
+    put(kMetaOffReqKvLen, req_kv);
+    put(kMetaOffReqQo, pl->qo_indptr);
+    std::vector<int32_t> tw;
+    for (auto& t : tiles) {
+        tw.push_back(t.b);
+        tw.push_back(t.hk);
+        tw.push_back(t.t0);
+        tw.push_back(t.nkv);
+    }
+    put(kMetaOffTile, tw);
+    pl->num_ctas = G;
+    pl->num_partials = 0;
+    pl->num_merge = 0;
+}
+
 void layout_workspace(pafp8_plan* pl) {
     const size_t heads = (size_t)pl->heads_per_cta * pl->group;
     pl->meta_bytes = align_up(pl->meta.size() * sizeof(int32_t), 256);
@@ -298,6 +358,28 @@ pafp8_status encode_cache_map(CUtensorMap* map, const void* base, int num_pages,
     return PAFP8_OK;
 }
 
+// 3-D map over q [nnz_qo, Hq, D]: dims (d, head, row), innermost first.  One
+// box is the query tile of one KV head: `rows` consecutive new tokens x the
+// group's heads x 64 elements (2-byte q, two boxes per tile) or 128 elements
+// (fp8 q), 128B-swizzled, landing as [rows*group][128 bytes].
+pafp8_status encode_q_map(CUtensorMap* map, const void* base, int nnz_qo, int hq, int group,
+                          int rows, bool fp8) {
+    auto enc = get_encode();
+    if (!enc) return fail(PAFP8_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    const cuuint64_t es = fp8 ? 1 : 2;
+    cuuint64_t dims[3] = {(cuuint64_t)kHeadDim, (cuuint64_t)hq, (cuuint64_t)nnz_qo};
+    cuuint64_t strides[2] = {kHeadDim * es, (cuuint64_t)hq * kHeadDim * es};
+    cuuint32_t box[3] = {fp8 ? 128u : 64u, (cuuint32_t)group, (cuuint32_t)rows};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(map, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16, 3,
+                     const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(PAFP8_ERR_CUDA, "cuTensorMapEncodeTiled failed for q (CUresult %d)", (int)r);
+    return PAFP8_OK;
+}
+
 bool scale_ok(float s) { return std::isfinite(s) && s > 0.0f; }
 
 }  // namespace
@@ -318,8 +400,6 @@ pafp8_status pafp8_plan_create(const pafp8_plan_desc* desc_in, const int32_t* kv
 
     if (d.mode != PAFP8_MODE_DECODE && d.mode != PAFP8_MODE_PREFILL)
         return fail(PAFP8_ERR_ARG, "mode %d is neither decode (0) nor prefill (1)", (int)d.mode);
-    if (d.mode == PAFP8_MODE_PREFILL)
-        return fail(PAFP8_ERR_UNSUPPORTED, "prefill is not served by this build yet");
 
     pafp8_status st;
     if ((st = check_kv_dtype(d.kv_dtype, "the KV cache")) != PAFP8_OK) return st;
@@ -335,10 +415,12 @@ pafp8_status pafp8_plan_create(const pafp8_plan_desc* desc_in, const int32_t* kv
         return fail(PAFP8_ERR_SHAPE, "num_qo_heads %d is not a multiple of num_kv_heads %d",
                     (int)d.num_qo_heads, (int)d.num_kv_heads);
     const int group = d.num_qo_heads / d.num_kv_heads;
-    if (group > kMaxGroupDecode)
+    const int max_group = d.mode == PAFP8_MODE_DECODE ? kMaxGroupDecode : kMaxGroupPrefill;
+    if (group > max_group)
         return fail(PAFP8_ERR_UNSUPPORTED,
-                    "decode serves up to %d query heads per KV head; got %d (%d / %d)",
-                    kMaxGroupDecode, group, (int)d.num_qo_heads, (int)d.num_kv_heads);
+                    "%s serves up to %d query heads per KV head; got %d (%d / %d)",
+                    d.mode == PAFP8_MODE_DECODE ? "decode" : "prefill", max_group, group,
+                    (int)d.num_qo_heads, (int)d.num_kv_heads);
     if (d.head_dim != kHeadDim)
         return fail(PAFP8_ERR_UNSUPPORTED, "head_dim %d is not served by this build (only %d)",
                     (int)d.head_dim, kHeadDim);
@@ -356,6 +438,8 @@ pafp8_status pafp8_plan_create(const pafp8_plan_desc* desc_in, const int32_t* kv
         return fail(PAFP8_ERR_ARG, "kv_indptr and last_page_len host arrays are required");
     if (d.mode == PAFP8_MODE_DECODE && qo_indptr_h != nullptr)
         return fail(PAFP8_ERR_ARG, "decode takes no qo_indptr (one query row per request)");
+    if (d.mode == PAFP8_MODE_PREFILL && d.batch > 0 && qo_indptr_h == nullptr)
+        return fail(PAFP8_ERR_ARG, "prefill needs the qo_indptr host array");
 
     if (d.batch > 0 && kv_indptr_h[0] != 0)
         return fail(PAFP8_ERR_SHAPE, "kv_indptr[0] is %d, not 0", (int)kv_indptr_h[0]);
@@ -369,6 +453,20 @@ pafp8_status pafp8_plan_create(const pafp8_plan_desc* desc_in, const int32_t* kv
                         (int)last_page_len_h[b], (int)d.page_size);
         if (n > 0 && d.num_pages == 0)
             return fail(PAFP8_ERR_SHAPE, "request %d has pages but num_pages is 0", b);
+        if (d.mode == PAFP8_MODE_PREFILL) {
+            if (b == 0 && qo_indptr_h[0] != 0)
+                return fail(PAFP8_ERR_SHAPE, "qo_indptr[0] is %d, not 0", (int)qo_indptr_h[0]);
+            const int64_t qo = (int64_t)qo_indptr_h[b + 1] - qo_indptr_h[b];
+            const int64_t kv = n > 0 ? (n - 1) * d.page_size + last_page_len_h[b] : 0;
+            if (qo < 0)
+                return fail(PAFP8_ERR_SHAPE, "qo_indptr decreases at request %d (%d -> %d)", b,
+                            (int)qo_indptr_h[b], (int)qo_indptr_h[b + 1]);
+            if (qo > kv)
+                return fail(PAFP8_ERR_SHAPE,
+                            "request %d has qo_len %lld > kv_len %lld: the new rows must be the "
+                            "last qo_len tokens of the KV sequence",
+                            b, (long long)qo, (long long)kv);
+        }
     }
 
     if (d.num_ctas == 0) {
@@ -395,8 +493,17 @@ pafp8_status pafp8_plan_create(const pafp8_plan_desc* desc_in, const int32_t* kv
         pl->kv_indptr.assign(1, 0);
     }
     pl->nnz_pages = pl->kv_indptr.back();
-    pl->nnz_qo = d.batch;
-    build_decode_meta(pl);
+    if (d.mode == PAFP8_MODE_PREFILL) {
+        if (d.batch > 0)
+            pl->qo_indptr.assign(qo_indptr_h, qo_indptr_h + d.batch + 1);
+        else
+            pl->qo_indptr.assign(1, 0);
+        pl->nnz_qo = pl->qo_indptr.back();
+        build_prefill_meta(pl);
+    } else {
+        pl->nnz_qo = d.batch;
+        build_decode_meta(pl);
+    }
     layout_workspace(pl);
     *out = pl;
     return PAFP8_OK;
@@ -496,6 +603,40 @@ pafp8_status pafp8_run_stage(const pafp8_plan* plan, int32_t stage, int32_t q_dt
 
     cudaStream_t s = (cudaStream_t)stream;
     char* ws = (char*)workspace;
+    const float sm_log2 = (float)((double)d.sm_scale * (is_fp8(q_dtype) ? (double)q_scale : 1.0) *
+                                  (double)k_scale * 1.4426950408889634);
+    if (d.mode == PAFP8_MODE_PREFILL) {
+        if (stage == 2 || plan->num_ctas == 0) return PAFP8_OK;  // prefill has no merge stage
+        PrefillParams pp{};
+        pp.q = q;
+        pp.kv_indices = kv_indices;
+        pp.o = o;
+        pp.lse = lse;
+        pp.meta = (const int32_t*)ws;
+        pp.status = (uint32_t*)(ws + plan->status_off);
+        pp.q_dtype = q_dtype;
+        pp.kv_dtype = k_dtype;
+        pp.o_dtype = o_dtype;
+        pp.num_qo_heads = d.num_qo_heads;
+        pp.num_kv_heads = d.num_kv_heads;
+        pp.num_pages = d.num_pages;
+        pp.group = plan->group;
+        pp.tile_tokens = kTileRows / plan->group;
+        pp.sm_scale_log2 = sm_log2;
+        pp.v_scale = v_scale;
+        CUtensorMap tq, tk, tv;
+        if ((st = encode_q_map(&tq, q, (int)plan->nnz_qo, d.num_qo_heads, plan->group,
+                               pp.tile_tokens, is_fp8(q_dtype))) != PAFP8_OK)
+            return st;
+        if ((st = encode_cache_map(&tk, k_cache, d.num_pages, d.num_kv_heads)) != PAFP8_OK) return st;
+        if ((st = encode_cache_map(&tv, v_cache, d.num_pages, d.num_kv_heads)) != PAFP8_OK) return st;
+        cudaError_t e = launch_prefill(pp, tq, tk, tv, plan->num_ctas, s);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            return fail(PAFP8_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(e));
+        }
+        return PAFP8_OK;
+    }
     DecodeParams p{};
     p.q = q;
     p.kv_indices = kv_indices;
@@ -511,8 +652,7 @@ pafp8_status pafp8_run_stage(const pafp8_plan* plan, int32_t stage, int32_t q_dt
     p.num_qo_heads = d.num_qo_heads;
     p.num_kv_heads = d.num_kv_heads;
     p.num_pages = d.num_pages;
-    p.sm_scale_log2 = (float)((double)d.sm_scale * (is_fp8(q_dtype) ? (double)q_scale : 1.0) *
-                              (double)k_scale * 1.4426950408889634);
+    p.sm_scale_log2 = sm_log2;
     p.v_scale = v_scale;
 
     cudaError_t e = cudaSuccess;

@@ -11,6 +11,9 @@ namespace pafp8 {
 constexpr int kHeadDim = 128;   // head_dim served by this build
 constexpr int kPageSize = 16;   // page_size served by this build
 constexpr int kMaxGroupDecode = 8;
+constexpr int kMaxGroupPrefill = 16;
+constexpr int kTileRows = 128;   // prefill query rows (token x head) per tile
+constexpr int kTileKeys = 128;   // prefill keys per KV tile (8 pages)
 
 // Layout of the int32 partition metadata that the plan builds on the host and
 // uploads to the head of the workspace.  Word offsets of the variable-length
@@ -62,11 +65,29 @@ struct DecodeParams {
     float v_scale;
 };
 
-// Launchers (decode.cu).  Return the launch's cudaError_t.
+struct PrefillParams {
+    const void* q;           // [nnz_qo, Hq, D]
+    const int32_t* kv_indices;
+    void* o;                 // [nnz_qo, Hq, D]
+    float* lse;              // [nnz_qo, Hq] or nullptr
+    const int32_t* meta;     // device copy of the metadata words
+    uint32_t* status;
+    int q_dtype, kv_dtype, o_dtype;
+    int num_qo_heads, num_kv_heads, num_pages;
+    int group;               // query heads per KV head
+    int tile_tokens;         // query tokens per 128-row tile (128 / group)
+    float sm_scale_log2;     // sm_scale * q_scale * k_scale * log2(e)
+    float v_scale;
+};
+
+// Launchers (decode.cu, prefill.cu).  Return the launch's cudaError_t.
 cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& tmap_k,
                           const CUtensorMap& tmap_v, int num_ctas, int heads_per_cta,
                           int group, cudaStream_t stream);
 cudaError_t launch_merge(const DecodeParams& p, int num_merge, int heads_per_cta, int group,
                          cudaStream_t stream);
+cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& tmap_q,
+                           const CUtensorMap& tmap_k, const CUtensorMap& tmap_v, int num_ctas,
+                           cudaStream_t stream);
 
 }  // namespace pafp8

@@ -1,0 +1,617 @@
+// prefill.cu -- ragged causal prefill attention over a paged fp8 KV cache on
+// the tcgen05 tensor cores (sm_103a).
+//
+// What it computes: for request b with qo_len new query rows and kv_len keys,
+// query row i (0-based among the new rows) of head h attends to keys
+// j <= i + kv_len - qo_len (bottom-right aligned causal mask) of KV head
+// h / group: o = v_scale * softmax(sm_scale * q_scale * k_scale * q.k) V,
+// lse = ln sum exp(logits).  KV stays fp8 in HBM and is dequantized on load
+// ("fp8 KV cache in the in-tree prefill kernel", Kernel note: KV is widened
+// into a 2-byte shared-memory tile in the global -> shared path); with an fp8
+// query the QK product runs natively in fp8 ("Enable Hopper FA3 FP8 attention
+// in decode.py", review note on q_scale folding into sm_scale for FP8 BMM1).
+//
+// Work tile: one KV head of one request and 128 query rows packed as
+// (token, head-of-group) pairs -- 128/group consecutive new tokens times the
+// group's query heads -- so a K/V tile is loaded and dequantized once for all
+// query heads that share it.  KV tiles are 128 keys (8 pages).  Persistent
+// CTAs take tiles i, i + grid, ... from a longest-first list built by the plan.
+//
+// Roles (320 threads):
+//   warps 0-3  dequant: raw fp8 K -> f16 K tile (2-byte query path); raw fp8
+//              V -> f16 V^T tile (both paths), zero beyond the request's keys;
+//   warps 4-7  softmax: thread r owns TMEM lane r = query row r.  Reads S,
+//              masks, keeps the running max and sum, writes P (f16) into TMEM,
+//              rescales O in TMEM only when the max rises by more than 2^8,
+//              and in the epilogue normalizes O and stores o and lse.  With a
+//              bf16 query it first brings its Q row into f16 range by an exact
+//              per-row power of two and converts it in place;
+//   warp 8     TMA producer: Q tile, K and V pages (one box per page);
+//   warp 9     MMA issuer and TMEM owner:
+//                S  = Q K^T   M=128 N=128, f16 (kind::f16) or fp8 (kind::f8f6f4)
+//                O += P V     M=128 N=128, A = P from TMEM, B = V^T (kind::f16)
+// TMEM columns: S double buffer 0-255, O 256-383, P 384-447.  Every operand
+// in shared memory is K-major with the 128-byte swizzle.  All waits are
+// bounded; on expiry the kernel records a status bit and winds down.
+#include "../../include/pafp8.h"
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace pafp8 {
+namespace {
+
+using namespace ptx;
+
+constexpr int D = kHeadDim;
+constexpr int kThreads = 320;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColS = 0, kColO = 256, kColP = 384;
+constexpr uint32_t kRawTile = kTileKeys * D;      // 16 KB of fp8
+constexpr uint32_t kHalfTile = kTileKeys * 128;  // 16 KB: 128 rows x 128 B
+constexpr uint32_t kF16Tile = 2 * kHalfTile;       // 32 KB of f16
+
+template <bool kF8>
+struct Layout {
+    static constexpr int NKR = kF8 ? 4 : 2;    // raw K stages
+    static constexpr int NVR = 2;              // raw V stages
+    static constexpr int NK16 = kF8 ? 0 : 2;   // f16 K stages
+    static constexpr int NV16 = kF8 ? 2 : 1;   // f16 V^T stages
+    static constexpr uint32_t q = 0;
+    static constexpr uint32_t kr = 32768;
+    static constexpr uint32_t vr = kr + NKR * kRawTile;
+    static constexpr uint32_t k16 = vr + NVR * kRawTile;
+    static constexpr uint32_t v16 = k16 + NK16 * kF16Tile;
+    static constexpr uint32_t bars = v16 + NV16 * kF16Tile;
+    // barrier indices (8 bytes each)
+    static constexpr int bQFull = 0, bQReady = 1, bQEmpty = 2;
+    static constexpr int bKrFull = 3, bKrEmpty = bKrFull + NKR;
+    static constexpr int bVrFull = bKrEmpty + NKR, bVrEmpty = bVrFull + NVR;
+    static constexpr int bK16Full = bVrEmpty + NVR, bK16Empty = bK16Full + NK16;
+    static constexpr int bV16Full = bK16Empty + NK16, bV16Empty = bV16Full + NV16;
+    static constexpr int bSFull = bV16Empty + NV16, bSEmpty = bSFull + 2;
+    static constexpr int bPFull = bSEmpty + 2, bPEmpty = bPFull + 1;
+    static constexpr int nBars = bPEmpty + 1;
+    static constexpr uint32_t tmem_slot = bars + 8 * nBars;
+    static constexpr uint32_t abort_flag = tmem_slot + 4;
+    static constexpr uint32_t bytes = abort_flag + 4;
+};
+
+struct Ring {
+    int idx = 0;
+    uint32_t phase = 0;
+    __device__ __forceinline__ void next(int n) {
+        if (++idx == n) {
+            idx = 0;
+            phase ^= 1u;
+        }
+    }
+};
+
+struct Tile {
+    int b, hk, t0, nkv;
+};
+
+__device__ __forceinline__ Tile load_tile(const int* meta, int t) {
+    const int* tl = meta + meta[kMetaOffTile] + 4 * t;
+    return Tile{tl[0], tl[1], tl[2], tl[3]};
+}
+
+__device__ __forceinline__ void set_abort(uint32_t flag_addr, uint32_t* status) {
+    asm volatile("st.shared.u32 [%0], 1;" ::"r"(flag_addr) : "memory");
+    atomicOr(status, kStatusTimeout);
+}
+
+__device__ __forceinline__ bool aborted(uint32_t flag_addr) {
+    uint32_t v;
+    asm volatile("ld.volatile.shared.u32 %0, [%1];" : "=r"(v) : "r"(flag_addr) : "memory");
+    return v != 0;
+}
+
+// Bounded wait that also gives up once another role has aborted.
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, uint32_t flag_addr,
+                                              uint32_t* status) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity)) {
+        if (aborted(flag_addr)) return false;
+        if (clock64() - t0 > kWaitCycles) {
+            set_abort(flag_addr, status);
+            return false;
+        }
+    }
+    return true;
+}
+
+template <bool kF8, int KT>
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_constant__ CUtensorMap tmq,
+                   const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv) {
+    using L = Layout<kF8>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t base = (smem_addr(smem_raw) + 1023u) & ~1023u;
+    auto bar = [&](int i) -> uint32_t { return base + L::bars + 8u * (uint32_t)i; };
+    const uint32_t flag_addr = base + L::abort_flag;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int* meta = p.meta;
+    const int n_tiles = meta[kMetaNumTiles];
+    const int* req_page = meta + meta[kMetaOffReqPage];
+    const int* req_kv = meta + meta[kMetaOffReqKvLen];
+    const int* qo_ptr = meta + meta[kMetaOffReqQo];
+    const int g = p.group, TQ = p.tile_tokens;
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar(L::bQFull), 1);
+        mbar_init(bar(L::bQReady), 128);
+        mbar_init(bar(L::bQEmpty), 1);
+        for (int i = 0; i < L::NKR; ++i) {
+            mbar_init(bar(L::bKrFull + i), 1);
+            mbar_init(bar(L::bKrEmpty + i), kF8 ? 1 : 128);
+        }
+        for (int i = 0; i < L::NVR; ++i) {
+            mbar_init(bar(L::bVrFull + i), 1);
+            mbar_init(bar(L::bVrEmpty + i), 128);
+        }
+        for (int i = 0; i < L::NK16; ++i) {
+            mbar_init(bar(L::bK16Full + i), 128);
+            mbar_init(bar(L::bK16Empty + i), 1);
+        }
+        for (int i = 0; i < L::NV16; ++i) {
+            mbar_init(bar(L::bV16Full + i), 128);
+            mbar_init(bar(L::bV16Empty + i), 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar(L::bSFull + i), 1);
+            mbar_init(bar(L::bSEmpty + i), 128);
+        }
+        mbar_init(bar(L::bPFull), 128);
+        mbar_init(bar(L::bPEmpty), 1);
+        asm volatile("st.shared.u32 [%0], 0;" ::"r"(flag_addr) : "memory");
+        mbar_init_fence();
+    }
+    if (warp == 9) tc_alloc(base + L::tmem_slot, kTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    uint32_t tmem;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(tmem) : "r"(base + L::tmem_slot) : "memory");
+
+    if (warp == 8) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            prefetch_tmap(&tmq);
+            prefetch_tmap(&tmk);
+            prefetch_tmap(&tmv);
+        }
+        Ring kr, vr;
+        uint32_t qphase = 0;
+        long long issued_k = 0, issued_v = 0, issued_q = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
+            const Tile tl = load_tile(meta, t);
+            const int q0 = qo_ptr[tl.b] + tl.t0;
+            if (lane == 0) {
+                ok = wait_or_abort(bar(L::bQEmpty), qphase ^ 1u, flag_addr, p.status);
+                if (ok) {
+                    const uint32_t qb = bar(L::bQFull);
+                    if (kF8) {
+                        mbar_arrive_expect_tx(qb, (uint32_t)(128 * g * TQ));
+                        tma_load_3d(base + L::q, &tmq, qb, 0, tl.hk * g, q0);
+                    } else {
+                        mbar_arrive_expect_tx(qb, (uint32_t)(2 * 128 * g * TQ));
+                        tma_load_3d(base + L::q, &tmq, qb, 0, tl.hk * g, q0);
+                        tma_load_3d(base + L::q + kHalfTile, &tmq, qb, 64, tl.hk * g, q0);
+                    }
+                    ++issued_q;
+                }
+            }
+            ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+            qphase ^= 1u;
+            const int kv_len = req_kv[tl.b];
+            const int npages = (kv_len + kPageSize - 1) / kPageSize;
+            const int* idx = p.kv_indices + req_page[tl.b];
+            for (int j = 0; j < tl.nkv && ok; ++j) {
+                const int pg0 = j * (kTileKeys / kPageSize);
+                const int np = min(kTileKeys / kPageSize, npages - pg0);
+                int page = lane < np ? __ldg(idx + pg0 + lane) : 0;
+                const bool bad = lane < np && (page < 0 || page >= p.num_pages);
+                if (bad) page = 0;
+                if (__any_sync(0xFFFFFFFFu, bad) && lane == 0) atomicOr(p.status, kStatusBounds);
+                // Page ids live in lanes 0..np-1; lane 0 issues every copy.
+                int pages[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) pages[i] = __shfl_sync(0xFFFFFFFFu, page, i);
+                if (lane == 0) {
+                    ok = wait_or_abort(bar(L::bKrEmpty + kr.idx), kr.phase ^ 1u, flag_addr, p.status);
+                    if (ok) {
+                        const uint32_t fb = bar(L::bKrFull + kr.idx);
+                        const uint32_t dst = base + L::kr + kr.idx * kRawTile;
+                        mbar_arrive_expect_tx(fb, (uint32_t)np * kPageSize * D);
+                        for (int i = 0; i < np; ++i)
+                            tma_load_4d(dst + i * 2048u, &tmk, fb, 0, tl.hk, 0, pages[i]);
+                        ++issued_k;
+                    }
+                }
+                ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+                if (!ok) break;
+                kr.next(L::NKR);
+                if (lane == 0) {
+                    ok = wait_or_abort(bar(L::bVrEmpty + vr.idx), vr.phase ^ 1u, flag_addr, p.status);
+                    if (ok) {
+                        const uint32_t fb = bar(L::bVrFull + vr.idx);
+                        const uint32_t dst = base + L::vr + vr.idx * kRawTile;
+                        mbar_arrive_expect_tx(fb, (uint32_t)np * kPageSize * D);
+                        for (int i = 0; i < np; ++i)
+                            tma_load_4d(dst + i * 2048u, &tmv, fb, 0, tl.hk, 0, pages[i]);
+                        ++issued_v;
+                    }
+                }
+                ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+                vr.next(L::NVR);
+            }
+        }
+        if (lane == 0) {
+            // Let every copy issued by this CTA land before it may exit.
+            if (issued_q > 0) mbar_wait(bar(L::bQFull), (uint32_t)((issued_q - 1) & 1));
+            for (int s = 0; s < L::NKR && s < issued_k; ++s)
+                mbar_wait(bar(L::bKrFull + s), (uint32_t)(((issued_k - 1 - s) / L::NKR) & 1));
+            for (int s = 0; s < L::NVR && s < issued_v; ++s)
+                mbar_wait(bar(L::bVrFull + s), (uint32_t)(((issued_v - 1 - s) / L::NVR) & 1));
+        }
+    } else if (warp == 9) {
+        // ------------------------------------------------------------- MMA
+        if (lane == 0) {
+            const uint32_t idesc_qk =
+                kF8 ? make_idesc(p.q_dtype == PAFP8_E5M2 ? 1 : 0, KT == PAFP8_E5M2 ? 1 : 0, 128, 128)
+                    : make_idesc(0, 0, 128, 128);
+            const uint32_t idesc_pv = make_idesc(0, 0, 128, 128);
+            Ring kring, v16;
+            uint32_t qphase = 0, pvphase = 0;
+            long long G = 0;
+            bool ok = true;
+            auto issue_pv = [&](int jj) -> bool {
+                if (!wait_or_abort(bar(L::bPFull), pvphase, flag_addr, p.status)) return false;
+                if (!wait_or_abort(bar(L::bV16Full + v16.idx), v16.phase, flag_addr, p.status)) return false;
+                tc_fence_after();
+                const uint32_t vt = base + L::v16 + v16.idx * kF16Tile;
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    const uint64_t bd = sw128_kmajor_desc(vt + (ks >> 2) * kHalfTile + (ks & 3) * 32);
+                    tc_mma_f16_ts(tmem + kColO, tmem + kColP + 8 * ks, bd, idesc_pv,
+                                  (jj > 0 || ks > 0) ? 1u : 0u);
+                }
+                tc_commit(bar(L::bPEmpty));
+                tc_commit(bar(L::bV16Empty + v16.idx));
+                v16.next(L::NV16);
+                pvphase ^= 1u;
+                return true;
+            };
+            for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
+                const Tile tl = load_tile(meta, t);
+                ok = wait_or_abort(bar(kF8 ? L::bQFull : L::bQReady), qphase, flag_addr, p.status);
+                qphase ^= 1u;
+                if (!ok) break;
+                tc_fence_after();
+                for (int j = 0; j < tl.nkv && ok; ++j) {
+                    const int nk = kF8 ? L::NKR : L::NK16;
+                    const int kfull = kF8 ? L::bKrFull : L::bK16Full;
+                    const int kempty = kF8 ? L::bKrEmpty : L::bK16Empty;
+                    const int sb = (int)(G & 1);
+                    ok = wait_or_abort(bar(kfull + kring.idx), kring.phase, flag_addr, p.status) &&
+                         wait_or_abort(bar(L::bSEmpty + sb), (uint32_t)((G >> 1) & 1) ^ 1u, flag_addr,
+                                       p.status);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint32_t dS = tmem + kColS + 128u * sb;
+                    if (kF8) {
+                        const uint32_t kt = base + L::kr + kring.idx * kRawTile;
+#pragma unroll
+                        for (int ks = 0; ks < 4; ++ks)
+                            tc_mma_f8_ss(dS, sw128_kmajor_desc(base + L::q + ks * 32),
+                                         sw128_kmajor_desc(kt + ks * 32), idesc_qk, ks > 0 ? 1u : 0u);
+                    } else {
+                        const uint32_t kt = base + L::k16 + kring.idx * kF16Tile;
+#pragma unroll
+                        for (int ks = 0; ks < 8; ++ks) {
+                            const uint32_t off = (ks >> 2) * kHalfTile + (ks & 3) * 32;
+                            tc_mma_f16_ss(dS, sw128_kmajor_desc(base + L::q + off),
+                                          sw128_kmajor_desc(kt + off), idesc_qk, ks > 0 ? 1u : 0u);
+                        }
+                    }
+                    tc_commit(bar(L::bSFull + sb));
+                    tc_commit(bar(kempty + kring.idx));
+                    if (j == tl.nkv - 1) tc_commit(bar(L::bQEmpty));
+                    kring.next(nk);
+                    ++G;
+                    if (j >= 1) ok = issue_pv(j - 1);
+                }
+                if (ok) ok = issue_pv(tl.nkv - 1);
+            }
+            // Drain: wait until every MMA issued above has completed.
+            if (G > 0) mbar_wait(bar(L::bPEmpty), pvphase ^ 1u);
+        }
+        __syncwarp();
+    } else if (warp < 4) {
+        // ---------------------------------------------------------- dequant
+        const int tid = threadIdx.x;  // 0..127
+        const int wd = warp, q8 = lane >> 3, e = lane & 7;
+        Ring kr, vr, k16, v16;
+        bool ok = true;
+        for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
+            const Tile tl = load_tile(meta, t);
+            const int kv_len = req_kv[tl.b];
+            for (int j = 0; j < tl.nkv && ok; ++j) {
+                const int valid = min(kTileKeys, kv_len - j * kTileKeys);
+                if (!kF8) {
+                    ok = wait_or_abort(bar(L::bKrFull + kr.idx), kr.phase, flag_addr, p.status) &&
+                         wait_or_abort(bar(L::bK16Empty + k16.idx), k16.phase ^ 1u, flag_addr, p.status);
+                    if (!ok) break;
+                    const uint32_t src = base + L::kr + kr.idx * kRawTile;
+                    const uint32_t dst = base + L::k16 + k16.idx * kF16Tile;
+#pragma unroll 2
+                    for (int it = 0; it < 8; ++it) {
+                        const int combo = wd * 8 + it;
+                        const int row = (combo >> 1) * 8 + e;
+                        const int c = (combo & 1) * 4 + q8;
+                        const uint4 w = lds128(src + row * 128 + ((c ^ e) << 4));
+                        const uint32_t hb = dst + (c >> 2) * kHalfTile + row * 128;
+                        sts128(hb + (((2 * q8) ^ e) << 4), fp8x2_lo<KT>(w.x), fp8x2_hi<KT>(w.x),
+                               fp8x2_lo<KT>(w.y), fp8x2_hi<KT>(w.y));
+                        sts128(hb + (((2 * q8 + 1) ^ e) << 4), fp8x2_lo<KT>(w.z), fp8x2_hi<KT>(w.z),
+                               fp8x2_lo<KT>(w.w), fp8x2_hi<KT>(w.w));
+                    }
+                    fence_async_smem();
+                    mbar_arrive(bar(L::bK16Full + k16.idx));
+                    mbar_arrive(bar(L::bKrEmpty + kr.idx));
+                    kr.next(L::NKR);
+                    k16.next(L::NK16);
+                }
+                ok = wait_or_abort(bar(L::bVrFull + vr.idx), vr.phase, flag_addr, p.status) &&
+                     wait_or_abort(bar(L::bV16Empty + v16.idx), v16.phase ^ 1u, flag_addr, p.status);
+                if (!ok) break;
+                const uint32_t src = base + L::vr + vr.idx * kRawTile;
+                const uint32_t dst = base + L::v16 + v16.idx * kF16Tile;
+                const int kb = e + 8 * (q8 >> 1);  // key block (8 keys)
+#pragma unroll 1
+                for (int rr = 0; rr < 2; ++rr) {
+                    const int rot = 2 * wd + rr;
+                    const int a = (q8 & 1) * 8 + ((e + rot) & 7);  // dim block (8 dims)
+                    uint32_t w0[8], w1[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const int row = kb * 8 + i;
+                        const uint2 v = lds64(src + row * 128 + ((((a >> 1) ^ i) << 4)) + (a & 1) * 8);
+                        const bool live = row < valid;
+                        w0[i] = live ? v.x : 0u;
+                        w1[i] = live ? v.y : 0u;
+                    }
+                    // T[d][k] = f16x2 of (key 2k, key 2k+1) for dim d of the block.
+                    uint32_t T[8][4];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const uint32_t x0 = prmt(w0[2 * k], w0[2 * k + 1], 0x5140u);
+                        const uint32_t x1 = prmt(w0[2 * k], w0[2 * k + 1], 0x7362u);
+                        const uint32_t y0 = prmt(w1[2 * k], w1[2 * k + 1], 0x5140u);
+                        const uint32_t y1 = prmt(w1[2 * k], w1[2 * k + 1], 0x7362u);
+                        T[0][k] = fp8x2_lo<KT>(x0);
+                        T[1][k] = fp8x2_hi<KT>(x0);
+                        T[2][k] = fp8x2_lo<KT>(x1);
+                        T[3][k] = fp8x2_hi<KT>(x1);
+                        T[4][k] = fp8x2_lo<KT>(y0);
+                        T[5][k] = fp8x2_hi<KT>(y0);
+                        T[6][k] = fp8x2_lo<KT>(y1);
+                        T[7][k] = fp8x2_hi<KT>(y1);
+                    }
+                    const uint32_t hb = dst + (kb >> 3) * kHalfTile;
+#pragma unroll
+                    for (int d = 0; d < 8; ++d) {
+                        const int row = a * 8 + d;
+                        sts128(hb + row * 128 + (((kb & 7) ^ d) << 4), T[d][0], T[d][1], T[d][2], T[d][3]);
+                    }
+                }
+                fence_async_smem();
+                mbar_arrive(bar(L::bV16Full + v16.idx));
+                mbar_arrive(bar(L::bVrEmpty + vr.idx));
+                vr.next(L::NVR);
+                v16.next(L::NV16);
+            }
+        }
+        (void)tid;
+    } else {
+        // ---------------------------------------------------------- softmax
+        const int r = threadIdx.x - 128;  // TMEM lane = query row of the tile
+        const uint32_t lane_base = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+        uint32_t qphase = 0, pphase = 0;
+        long long G = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
+            const Tile tl = load_tile(meta, t);
+            const int qo0 = qo_ptr[tl.b];
+            const int qo_len = qo_ptr[tl.b + 1] - qo0;
+            const int kv_len = req_kv[tl.b];
+            const int tok = r / g, hh = r - tok * g;
+            const bool valid_row = (tok < TQ) && (tl.t0 + tok < qo_len);
+            const int limit = valid_row ? tl.t0 + tok + kv_len - qo_len : -1;
+            float scale = p.sm_scale_log2;
+            if (!kF8) {
+                ok = wait_or_abort(bar(L::bQFull), qphase, flag_addr, p.status);
+                qphase ^= 1u;
+                if (!ok) break;
+                if (p.q_dtype == PAFP8_BF16 && r < TQ * g) {
+                    // Bring the row into f16 range by an exact power of two.
+                    uint32_t mx = 0;
+#pragma unroll
+                    for (int c = 0; c < 16; ++c) {
+                        const uint4 w = lds128(base + L::q + (c >> 3) * kHalfTile + r * 128 +
+                                               (((c & 7) ^ (r & 7)) << 4));
+                        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            mx = max(mx, (ws[k] & 0x7FFFu) << 16);
+                            mx = max(mx, ws[k] & 0x7FFF0000u);
+                        }
+                    }
+                    const int ex = (int)((mx >> 23) & 0xFF) - 127;
+                    const int shift = ex > 14 ? ex - 14 : 0;
+                    const float down = __int_as_float((127 - shift) << 23);
+                    scale *= __int_as_float((127 + shift) << 23);
+#pragma unroll
+                    for (int c = 0; c < 16; ++c) {
+                        const uint32_t a = base + L::q + (c >> 3) * kHalfTile + r * 128 +
+                                           (((c & 7) ^ (r & 7)) << 4);
+                        const uint4 w = lds128(a);
+                        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+                        uint32_t o4[4];
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            o4[k] = pack_half2(__uint_as_float(ws[k] << 16) * down,
+                                               __uint_as_float(ws[k] & 0xFFFF0000u) * down);
+                        sts128(a, o4[0], o4[1], o4[2], o4[3]);
+                    }
+                    fence_async_smem();
+                }
+                mbar_arrive(bar(L::bQReady));
+            }
+            float m = -INFINITY, l = 0.f;
+            for (int j = 0; j < tl.nkv && ok; ++j) {
+                const int sb = (int)(G & 1);
+                ok = wait_or_abort(bar(L::bSFull + sb), (uint32_t)((G >> 1) & 1), flag_addr, p.status);
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t sS = lane_base + kColS + 128u * sb;
+                const int key0 = j * kTileKeys;
+                const bool need_mask = key0 + kTileKeys - 1 > limit;
+                // pass 1: row max
+                float mx = -INFINITY;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t v[32];
+                    tc_ld32(sS + 32 * c, v);
+                    tc_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        float x = __uint_as_float(v[i]) * scale;
+                        if (need_mask && key0 + 32 * c + i > limit) x = -INFINITY;
+                        mx = fmaxf(mx, x);
+                    }
+                }
+                const float m_new = fmaxf(m, mx);
+                float m_use = m;
+                bool rescale = false;
+                if (j == 0) {
+                    m_use = m_new;
+                } else if (m_new > m + 8.0f) {
+                    m_use = m_new;
+                    rescale = true;
+                }
+                if (m_use == -INFINITY) m_use = 0.f;  // row with no admissible key so far
+                // P must not be overwritten before the previous P.V has completed.
+                if (j >= 1) {
+                    ok = wait_or_abort(bar(L::bPEmpty), pphase, flag_addr, p.status);
+                    pphase ^= 1u;
+                    if (!ok) break;
+                    tc_fence_after();
+                }
+                if (rescale) {
+                    const float alpha = ex2(m - m_use);
+                    l *= alpha;
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        uint32_t v[32];
+                        tc_ld32(lane_base + kColO + 32 * c, v);
+                        tc_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
+                        tc_st32(lane_base + kColO + 32 * c, v);
+                    }
+                    tc_wait_st();
+                }
+                // pass 2: P = exp2(x - m), row sum, P -> TMEM as f16
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t v[32];
+                    tc_ld32(sS + 32 * c, v);
+                    tc_wait_ld();
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        float x0 = __uint_as_float(v[2 * i]) * scale;
+                        float x1 = __uint_as_float(v[2 * i + 1]) * scale;
+                        if (need_mask && key0 + 32 * c + 2 * i > limit) x0 = -INFINITY;
+                        if (need_mask && key0 + 32 * c + 2 * i + 1 > limit) x1 = -INFINITY;
+                        const float e0 = ex2(x0 - m_use), e1 = ex2(x1 - m_use);
+                        l += e0 + e1;
+                        pk[i] = pack_half2(e0, e1);
+                    }
+                    tc_st16(lane_base + kColP + 16 * c, pk);
+                }
+                tc_wait_st();
+                tc_fence_before();
+                mbar_arrive(bar(L::bSEmpty + sb));
+                mbar_arrive(bar(L::bPFull));
+                m = m_use;
+                ++G;
+            }
+            if (!ok) break;
+            // epilogue: the tile's last P.V must have completed.
+            ok = wait_or_abort(bar(L::bPEmpty), pphase, flag_addr, p.status);
+            pphase ^= 1u;
+            if (!ok) break;
+            tc_fence_after();
+            const float inv = valid_row && l > 0.f ? p.v_scale / l : 0.f;
+            const size_t orow = (size_t)(qo0 + tl.t0 + tok) * p.num_qo_heads + (size_t)tl.hk * g + hh;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t v[32];
+                tc_ld32(lane_base + kColO + 32 * c, v);
+                tc_wait_ld();
+                if (valid_row) {
+                    uint32_t w[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        w[i] = pack_out2(__uint_as_float(v[2 * i]) * inv, __uint_as_float(v[2 * i + 1]) * inv,
+                                         p.o_dtype);
+                    uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + orow * D + 32 * c);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+                }
+            }
+            if (valid_row && p.lse != nullptr) p.lse[orow] = (m + __log2f(l)) * 0.69314718055994531f;
+            tc_fence_before();
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 9) {
+        tc_fence_after();
+        tc_dealloc(tmem, kTmemCols);
+    }
+}
+
+template <bool kF8, int KT>
+cudaError_t launch_one(const PrefillParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
+                       const CUtensorMap& tv, int num_ctas, cudaStream_t stream) {
+    const size_t smem = 1024 + Layout<kF8>::bytes;
+    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<kF8, KT>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    prefill_kernel<kF8, KT><<<num_ctas, kThreads, smem, stream>>>(p, tq, tk, tv);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& tmap_q, const CUtensorMap& tmap_k,
+                           const CUtensorMap& tmap_v, int num_ctas, cudaStream_t stream) {
+    const bool f8 = p.q_dtype == PAFP8_E4M3FN || p.q_dtype == PAFP8_E5M2;
+    if (f8)
+        return p.kv_dtype == PAFP8_E4M3FN
+                   ? launch_one<true, PAFP8_E4M3FN>(p, tmap_q, tmap_k, tmap_v, num_ctas, stream)
+                   : launch_one<true, PAFP8_E5M2>(p, tmap_q, tmap_k, tmap_v, num_ctas, stream);
+    return p.kv_dtype == PAFP8_E4M3FN
+               ? launch_one<false, PAFP8_E4M3FN>(p, tmap_q, tmap_k, tmap_v, num_ctas, stream)
+               : launch_one<false, PAFP8_E5M2>(p, tmap_q, tmap_k, tmap_v, num_ctas, stream);
+}
+
+}  // namespace pafp8
