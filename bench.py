@@ -153,35 +153,40 @@ def gpu_id_for(torch, dev) -> str:
         return str(dev.index or 0)
 
 
-def oracle_decode_rate(b, budget_s: float = 12.0):
-    """Oracle GB/s on a prefix of the batch's requests (doubling until the
-    last run takes ~budget_s/2 or covers every request)."""
+def oracle_decode_sample(b, n: int):
+    """Run the oracle on the first n requests (every query head); returns
+    (seconds, algorithmic bytes of the sample, threads used)."""
     import numpy as np
 
     import oracle
     from paged_attention_fp8_gb300.workloads import raw_numpy
 
-    raw = dict(q=raw_numpy(b.q), k=raw_numpy(b.k_cache), v=raw_numpy(b.v_cache))
-    n = 1
-    while True:
-        rows = np.repeat(np.arange(n), b.num_qo_heads)
-        heads = np.tile(np.arange(b.num_qo_heads), n)
-        t0 = time.perf_counter()
-        oracle.paged_attention(q=raw["q"], q_dtype=b.q_dtype, k_cache=raw["k"], v_cache=raw["v"],
-                               kv_dtype=b.kv_dtype, qo_indptr=b.qo_indptr.numpy(),
-                               kv_indptr=b.kv_indptr.numpy(), kv_indices=b.kv_indices.numpy(),
-                               last_page_len=b.last_page_len.numpy(), num_qo_heads=b.num_qo_heads,
-                               num_kv_heads=b.num_kv_heads, q_scale=b.q_scale, k_scale=b.k_scale,
-                               v_scale=b.v_scale, sm_scale=b.sm_scale, causal=False, rows=rows,
-                               heads=heads)
-        dt = time.perf_counter() - t0
-        if dt >= budget_s / 2 or n >= b.batch:
-            break
-        n = min(b.batch, max(n + 1, int(n * min(4.0, budget_s / 2 / max(dt, 1e-3)))))
+    raw = getattr(b, "_raw_cache", None)
+    if raw is None:
+        raw = dict(q=raw_numpy(b.q), k=raw_numpy(b.k_cache), v=raw_numpy(b.v_cache))
+        b._raw_cache = raw
+    rows = np.repeat(np.arange(n), b.num_qo_heads)
+    heads = np.tile(np.arange(b.num_qo_heads), n)
+    t0 = time.perf_counter()
+    oracle.paged_attention(q=raw["q"], q_dtype=b.q_dtype, k_cache=raw["k"], v_cache=raw["v"],
+                           kv_dtype=b.kv_dtype, qo_indptr=b.qo_indptr.numpy(),
+                           kv_indptr=b.kv_indptr.numpy(), kv_indices=b.kv_indices.numpy(),
+                           last_page_len=b.last_page_len.numpy(), num_qo_heads=b.num_qo_heads,
+                           num_kv_heads=b.num_kv_heads, q_scale=b.q_scale, k_scale=b.k_scale,
+                           v_scale=b.v_scale, sm_scale=b.sm_scale, causal=False, rows=rows,
+                           heads=heads)
+    dt = time.perf_counter() - t0
     kv_tokens = sum(b.kv_lens[:n])
     by = 2 * kv_tokens * b.num_kv_heads * b.head_dim + n * b.num_qo_heads * b.head_dim * 6 + \
         4 * int(b.kv_indptr[n])
-    return by / dt / 1e9, n, dt, oracle.num_threads()
+    return dt, by, oracle.num_threads()
+
+
+def oracle_sample_size(b, budget_s: float) -> int:
+    """Requests per oracle sample so that one sample takes about budget_s."""
+    dt, by, _ = oracle_decode_sample(b, 1)
+    per_req = max(dt, 1e-4)
+    return max(1, min(b.batch, int(budget_s / per_req)))
 
 
 def run_reference(args):
@@ -191,12 +196,16 @@ def run_reference(args):
     from paged_attention_fp8_gb300.workloads import WORKLOADS, workload
 
     b = workload(2)
+    # Every step is the same bounded sample, sized so the whole run takes a
+    # couple of minutes at most.
+    budget = max(0.01, min(10.0, 120.0 / max(1, args.steps + args.warmup)))
+    n = oracle_sample_size(b, budget)
     times, rates = [], []
-    budget = max(2.0, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
+    cores = 1
     for i in range(args.warmup + args.steps):
-        gbs, n, dt, cores = oracle_decode_rate(b, budget)
+        dt, by, cores = oracle_decode_sample(b, n)
         if i >= args.warmup:
-            rates.append(gbs)
+            rates.append(by / dt / 1e9)
             times.append(dt)
     value = statistics.median(rates)
     line = {
@@ -365,10 +374,12 @@ def run_ours(args):
         "clocks": clocks,
     }
     if world == 1 and not args.no_cpu_baseline:
-        gbs, n, dt, cores = oracle_decode_rate(b)
-        line["cpu_baseline"] = {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+        n = oracle_sample_size(b, 15.0)
+        dt, by, cores = oracle_decode_sample(b, n)
+        line["cpu_baseline"] = {"value": round(by / dt / 1e9, 4), "unit": "GB/s", "cores": cores,
+                                "kind": "oracle",
                                 "sample": f"first {n} of {b.batch} requests, every query head "
-                                          f"({dt:.1f} s, fp64)"}
+                                          f"({dt:.2f} s, fp64)"}
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
