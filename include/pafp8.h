@@ -201,6 +201,38 @@ pafp8_status pafp8_run_stage(const pafp8_plan *plan, int32_t stage, int32_t q_dt
  * range) or PAFP8_ERR_TIMEOUT (a bounded pipeline wait expired). */
 pafp8_status pafp8_device_status(const pafp8_plan *plan, void *workspace, void *stream);
 
+/* Decode without a workspace argument, for callers that may not allocate
+ * device memory themselves: for example an inference engine's plugin or
+ * enqueue callback that runs on a stream the host framework owns, where
+ * cudaMalloc is off limits because it can synchronize the device and the
+ * framework hands out all device memory.  Such callers still pass q, the
+ * cache, kv_indices, o and lse (their own buffers); the plan's metadata, the
+ * split-KV partial states and the status word go to a scratch array built
+ * into the library instead of a caller workspace.  This entry point has no
+ * counterpart on the pages the method comes from; it is a deployment
+ * convenience of this library.
+ *
+ * Arguments and checks are those of pafp8_run for a decode plan (prefill
+ * plans are refused).  The scratch holds 16 MiB (PAFP8_NOALLOC_SCRATCH_BYTES)
+ * on every GPU that loads the library, until the process exits; a plan whose
+ * pafp8_workspace_bytes exceeds it is refused with PAFP8_ERR_WORKSPACE
+ * (fewer CTAs or splits shrink it).  The first call on a device looks up the
+ * scratch's device address (cudaGetSymbolAddress) with that device current,
+ * so make it before any stream capture.  No call allocates or frees device
+ * memory.  Every call re-loads its plan's metadata into the scratch and
+ * clears the status word, so a call never depends on the previous call's
+ * contents; but all calls share the one array, so calls that can overlap on
+ * the GPU (different streams, or different threads without ordering) race
+ * and must be serialized by the caller.  The status word is internal here:
+ * page-index and timeout reports are available only through pafp8_run with a
+ * workspace. */
+#define PAFP8_NOALLOC_SCRATCH_BYTES (16u << 20)
+pafp8_status pafp8_run_decode_noalloc(const pafp8_plan *plan, int32_t q_dtype, const void *q,
+                                      int32_t k_dtype, const void *k_cache, int32_t v_dtype,
+                                      const void *v_cache, const int32_t *kv_indices,
+                                      float q_scale, float k_scale, float v_scale,
+                                      int32_t o_dtype, void *o, float *lse, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

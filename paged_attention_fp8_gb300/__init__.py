@@ -39,7 +39,7 @@ _NAME_CODES = {"default": DTYPE_DEFAULT, "f16": F16, "float16": F16, "bf16": BF1
 # Every entry point include/pafp8.h declares.
 EXPORTS = ("pafp8_abi_version", "pafp8_last_error", "pafp8_plan_create", "pafp8_plan_destroy",
            "pafp8_workspace_bytes", "pafp8_plan_metadata", "pafp8_plan_upload", "pafp8_run",
-           "pafp8_run_stage", "pafp8_device_status")
+           "pafp8_run_stage", "pafp8_device_status", "pafp8_run_decode_noalloc")
 
 
 class Pafp8Error(RuntimeError):
@@ -90,6 +90,9 @@ def lib() -> ctypes.CDLL:
                                   vp, sz, vp]
     L.pafp8_run_stage.restype = i32
     L.pafp8_device_status.argtypes, L.pafp8_device_status.restype = [vp, vp, vp], i32
+    L.pafp8_run_decode_noalloc.argtypes = [vp, i32, vp, i32, vp, i32, vp, vp, f32, f32, f32, i32, vp,
+                                           vp, vp]
+    L.pafp8_run_decode_noalloc.restype = i32
     _lib = L
     return L
 
@@ -200,6 +203,19 @@ def pafp8_run_stage(handle: int, stage: int, q, k_cache, v_cache, kv_indices, o,
 
 def pafp8_device_status(handle: int, workspace, stream=None) -> None:
     _check(lib().pafp8_device_status(handle, _ptr(workspace), _stream(stream)))
+
+
+def pafp8_run_decode_noalloc(handle: int, q, k_cache, v_cache, kv_indices, o, lse, *, q_scale=1.0,
+                             k_scale=1.0, v_scale=1.0, q_dtype=None, k_dtype=None, v_dtype=None,
+                             o_dtype=None, stream=None) -> None:
+    """Decode with the library's built-in scratch instead of a workspace, for
+    callers that may not allocate device memory (see include/pafp8.h)."""
+    _check(lib().pafp8_run_decode_noalloc(
+        handle, dtype_code(q_dtype if q_dtype is not None else q.dtype), _ptr(q),
+        dtype_code(k_dtype if k_dtype is not None else k_cache.dtype), _ptr(k_cache),
+        dtype_code(v_dtype if v_dtype is not None else v_cache.dtype), _ptr(v_cache),
+        _ptr(kv_indices), float(q_scale), float(k_scale), float(v_scale),
+        dtype_code(o_dtype if o_dtype is not None else o.dtype), _ptr(o), _ptr(lse), _stream(stream)))
 
 
 # ---- convenience owner of a plan ---------------------------------------

@@ -33,6 +33,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <mutex>
+
 #include "../../include/pafp8.h"
 #include "internal.h"
 #include "ptx.cuh"
@@ -404,6 +406,34 @@ __global__ void __launch_bounds__(128)
 }
 
 }  // namespace
+
+// Built-in scratch for callers that cannot allocate device memory (see
+// pafp8_run_decode_noalloc).  It stands in for the caller's workspace: the
+// plan's metadata, the split-KV partial states and the status word.  Every
+// GPU that loads the library holds these bytes until the process exits, and
+// every call shares them.
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+
+// Device address of g_noalloc_scratch on the current device.  The symbol's
+// host-side name is only a stand-in, so the address is looked up once per
+// device (with that device current) and cached.
+cudaError_t noalloc_scratch(void** ptr) {
+    static std::mutex mu;
+    static void* addr[kMaxDevices] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    if (addr[dev] == nullptr) {
+        void* a = nullptr;
+        e = cudaGetSymbolAddress(&a, g_noalloc_scratch);
+        if (e != cudaSuccess) return e;
+        addr[dev] = a;
+    }
+    *ptr = addr[dev];
+    return cudaSuccess;
+}
 
 cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& tmap_k, const CUtensorMap& tmap_v,
                           int num_ctas, int hpc, int group, cudaStream_t stream) {

@@ -692,4 +692,100 @@ pafp8_status pafp8_device_status(const pafp8_plan* plan, void* workspace, void* 
     return PAFP8_OK;
 }
 
+// Decode without a caller-supplied workspace: the library's built-in scratch
+// (noalloc_scratch) takes its place.  Nothing here allocates device memory.
+pafp8_status pafp8_run_decode_noalloc(const pafp8_plan* plan, int32_t q_dtype, const void* q,
+                                      int32_t k_dtype, const void* k_cache, int32_t v_dtype,
+                                      const void* v_cache, const int32_t* kv_indices,
+                                      float q_scale, float k_scale, float v_scale,
+                                      int32_t o_dtype, void* o, float* lse, void* stream) {
+    if (plan == nullptr) return fail(PAFP8_ERR_ARG, "plan is NULL");
+    const pafp8_plan_desc& d = plan->desc;
+    if (d.mode != PAFP8_MODE_DECODE)
+        return fail(PAFP8_ERR_ARG, "pafp8_run_decode_noalloc serves decode plans only");
+    if (plan->ws_bytes > kNoAllocScratchBytes)
+        return fail(PAFP8_ERR_WORKSPACE,
+                    "the plan needs %zu bytes of scratch but the built-in scratch holds %zu; "
+                    "use pafp8_run with a workspace, or plan with fewer CTAs or splits",
+                    plan->ws_bytes, kNoAllocScratchBytes);
+    pafp8_status st;
+    if (k_dtype != v_dtype)
+        return fail(PAFP8_ERR_DTYPE, "k_cache has dtype %s but v_cache has %s",
+                    dtype_name(k_dtype), dtype_name(v_dtype));
+    if ((st = check_kv_dtype(k_dtype, "k_cache")) != PAFP8_OK) return st;
+    if ((st = check_q_dtype(q_dtype)) != PAFP8_OK) return st;
+    if ((st = check_o_dtype(o_dtype, q_dtype)) != PAFP8_OK) return st;
+    if (q_dtype != d.q_dtype || k_dtype != d.kv_dtype || o_dtype != d.o_dtype)
+        return fail(PAFP8_ERR_DTYPE,
+                    "dtypes q %s, kv %s, o %s differ from the plan's q %s, kv %s, o %s",
+                    dtype_name(q_dtype), dtype_name(k_dtype), dtype_name(o_dtype),
+                    dtype_name(d.q_dtype), dtype_name(d.kv_dtype), dtype_name(d.o_dtype));
+    if (!scale_ok(q_scale) || !scale_ok(k_scale) || !scale_ok(v_scale))
+        return fail(PAFP8_ERR_ARG, "scales must be finite and > 0 (q %g, k %g, v %g)",
+                    (double)q_scale, (double)k_scale, (double)v_scale);
+    if (is_2byte(q_dtype) && q_scale != 1.0f)
+        return fail(PAFP8_ERR_ARG,
+                    "q_scale %g given with a %s query: only an fp8 query is dequantized by "
+                    "q_scale, so it would be silently ignored",
+                    (double)q_scale, dtype_name(q_dtype));
+    if (plan->nnz_qo > 0 && (q == nullptr || o == nullptr))
+        return fail(PAFP8_ERR_ARG, "q and o must be non-NULL");
+    if (plan->nnz_pages > 0 && (k_cache == nullptr || v_cache == nullptr || kv_indices == nullptr))
+        return fail(PAFP8_ERR_ARG, "k_cache, v_cache and kv_indices must be non-NULL");
+    if (((uintptr_t)q | (uintptr_t)o | (uintptr_t)k_cache | (uintptr_t)v_cache) % 16 != 0)
+        return fail(PAFP8_ERR_ARG, "q, o, k_cache and v_cache must be 16-byte aligned");
+    if ((uintptr_t)lse % 4 != 0 || (uintptr_t)kv_indices % 4 != 0)
+        return fail(PAFP8_ERR_ARG, "lse and kv_indices must be 4-byte aligned");
+
+    void* scratch = nullptr;
+    cudaError_t e = noalloc_scratch(&scratch);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(PAFP8_ERR_CUDA, "looking up the built-in scratch failed: %s",
+                    cudaGetErrorString(e));
+    }
+    cudaStream_t s = (cudaStream_t)stream;
+    char* ws = (char*)scratch;
+    // The scratch keeps the previous call's bytes: load this plan's metadata
+    // and clear the status word; partial states are written before read.
+    e = cudaMemcpyAsync(ws, plan->meta.data(), plan->meta.size() * 4, cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(ws + plan->status_off, 0, 256, s);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(PAFP8_ERR_CUDA, "loading the plan into the built-in scratch failed: %s",
+                    cudaGetErrorString(e));
+    }
+    DecodeParams p{};
+    p.q = q;
+    p.kv_indices = kv_indices;
+    p.o = o;
+    p.lse = lse;
+    p.meta = (const int32_t*)ws;
+    p.part_o = (float*)(ws + plan->part_o_off);
+    p.part_lse = (float*)(ws + plan->part_lse_off);
+    p.status = (uint32_t*)(ws + plan->status_off);
+    p.q_dtype = q_dtype;
+    p.kv_dtype = k_dtype;
+    p.o_dtype = o_dtype;
+    p.num_qo_heads = d.num_qo_heads;
+    p.num_kv_heads = d.num_kv_heads;
+    p.num_pages = d.num_pages;
+    p.sm_scale_log2 = (float)((double)d.sm_scale * (is_fp8(q_dtype) ? (double)q_scale : 1.0) *
+                              (double)k_scale * 1.4426950408889634);
+    p.v_scale = v_scale;
+    if (plan->num_ctas > 0) {
+        CUtensorMap tk, tv;
+        if ((st = encode_cache_map(&tk, k_cache, d.num_pages, d.num_kv_heads)) != PAFP8_OK) return st;
+        if ((st = encode_cache_map(&tv, v_cache, d.num_pages, d.num_kv_heads)) != PAFP8_OK) return st;
+        e = launch_decode(p, tk, tv, plan->num_ctas, plan->heads_per_cta, plan->group, s);
+    }
+    if (e == cudaSuccess && plan->num_merge > 0)
+        e = launch_merge(p, plan->num_merge, plan->heads_per_cta, plan->group, s);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(PAFP8_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(e));
+    }
+    return PAFP8_OK;
+}
+
 }  // extern "C"

@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "../../include/pafp8.h"
+
 namespace pafp8 {
 
 constexpr int kHeadDim = 128;   // head_dim served by this build
@@ -86,6 +88,14 @@ cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& tmap_k,
                           int group, cudaStream_t stream);
 cudaError_t launch_merge(const DecodeParams& p, int num_merge, int heads_per_cta, int group,
                          cudaStream_t stream);
+// Size of the built-in scratch of the no-allocation decode entry point, and
+// the device ordinals it serves.
+constexpr size_t kNoAllocScratchBytes = PAFP8_NOALLOC_SCRATCH_BYTES;
+constexpr int kMaxDevices = 64;
+// Device address of the built-in scratch on the current device (looked up
+// once per device; decode.cu).
+cudaError_t noalloc_scratch(void** ptr);
+
 cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& tmap_q,
                            const CUtensorMap& tmap_k, const CUtensorMap& tmap_v, int num_ctas,
                            cudaStream_t stream);
