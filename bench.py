@@ -45,6 +45,7 @@ if ROOT not in sys.path:
 
 METRIC = "paged fp8-KV decode HBM GB/s (% of peak); causal prefill TFLOPS (% of peak)"
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
 L2_FLUSH_BYTES = 256 << 20
 
 # DRAM bytes (read + write) per launch of the decode kernel on the serving
@@ -61,6 +62,9 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--mode", choices=["all", "decode", "prefill"], default="all",
+                    help="which parts to time (profiling runs use one)")
+    ap.add_argument("--prefill-steps", type=int, default=30)
     return ap.parse_args()
 
 
@@ -90,6 +94,77 @@ def measured_peaks():
         return float(d["hbm_gbs"]), "measured"
     except Exception:
         return FALLBACK_HBM_GBS, "fallback"
+
+
+def measured_bf16_tflops():
+    """Dense bf16 tensor peak (burst, for a kernel timed alone)."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops"]), "measured"
+    except Exception:
+        return FALLBACK_BF16_TFLOPS, "fallback"
+
+
+def time_prefill(index, dev, steps, warmup):
+    """Device time of the prefill kernel on named workload `index`; returns
+    a dict with TFLOPS over the admitted causal pairs and its roofline."""
+    import torch
+
+    import paged_attention_fp8_gb300 as pa
+    from paged_attention_fp8_gb300.workloads import TORCH_DTYPES, WORKLOADS, workload
+
+    b = workload(index)
+    flops = b.causal_flops()
+    q = b.q.to(dev)
+    k = b.k_cache.to(dev)
+    v = b.v_cache.to(dev)
+    idx = b.kv_indices.to(dev)
+    plan = pa.Plan(mode="prefill", num_qo_heads=b.num_qo_heads, num_kv_heads=b.num_kv_heads,
+                   num_pages=b.num_pages, kv_indptr=b.kv_indptr, last_page_len=b.last_page_len,
+                   qo_indptr=b.qo_indptr, q_dtype=b.q_dtype, kv_dtype=b.kv_dtype, o_dtype=b.o_dtype,
+                   sm_scale=b.sm_scale)
+    ws = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device=dev)
+    plan.upload(ws)
+    o = torch.empty(b.nnz_qo, b.num_qo_heads, b.head_dim, dtype=TORCH_DTYPES[b.o_dtype], device=dev)
+    lse = torch.empty(b.nnz_qo, b.num_qo_heads, dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    kw = dict(q_scale=b.q_scale, k_scale=b.k_scale, v_scale=b.v_scale)
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        flush.zero_()
+        plan.run(q, k, v, idx, o, lse, ws, **kw)
+    torch.cuda.synchronize()
+    plan.device_status(ws)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+    for i in range(steps):
+        flush.zero_()
+        ev[i][0].record(stream)
+        plan.run(q, k, v, idx, o, lse, ws, **kw)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    plan.device_status(ws)
+    ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    tflops = flops / (ms * 1e-3) / 1e12
+    p16, kind = measured_bf16_tflops()
+    fp8 = b.q_dtype in ("e4m3fn", "e5m2")
+    out = {"workload": WORKLOADS[index], "value": round(tflops, 2), "unit": "TFLOP/s",
+           "ms_per_launch": round(ms, 5), "flops": flops, "launches": steps,
+           "mma": ("QK^T fp8 kind::f8f6f4, PV f16 kind::f16" if fp8 else "f16 kind::f16 (fp8 KV dequantized)")}
+    if fp8:
+        p8 = 2.0 * p16  # another dtype's measured peak x the nominal fp8/bf16 ratio
+        blended = 2.0 / (1.0 / p8 + 1.0 / p16)
+        out["roofline"] = {"bound": "tensor", "achieved": round(tflops, 2), "peak": round(blended, 1),
+                           "unit": "TFLOP/s", "frac": round(tflops / blended, 4), "traffic": None,
+                           "peak_kind": f"{kind} bf16 x nominal fp8 ratio 2, blended for half the flops at each rate",
+                           "frac_of_dense_bf16": round(tflops / p16, 4)}
+    else:
+        out["roofline"] = {"bound": "tensor", "achieved": round(tflops, 2), "peak": p16, "unit": "TFLOP/s",
+                           "frac": round(tflops / p16, 4), "traffic": None, "peak_kind": f"{kind} dense bf16"}
+    del q, k, v, idx, o, lse, ws, flush
+    torch.cuda.empty_cache()
+    return out
 
 
 def kernel_sha(name: str) -> str:
@@ -240,6 +315,14 @@ def run_ours(args):
     dev = torch.device("cuda", local)
     pbuild.build()
 
+    if args.mode == "prefill":
+        res = {str(i): time_prefill(i, dev, args.prefill_steps, max(3, args.warmup)) for i in (4, 5)}
+        if rank == 0:
+            print(json.dumps({"mode": "prefill", "prefill": res}), flush=True)
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
     b = workload(2)
     nbytes = decode_bytes(b)
     q = b.q.to(dev)
@@ -340,6 +423,13 @@ def run_ours(args):
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         e2e_s = float(t[0])
 
+    prefill_res = {}
+    if args.mode == "all":
+        del flush
+        torch.cuda.empty_cache()
+        for i in (4, 5):
+            prefill_res[i] = time_prefill(i, dev, args.prefill_steps, max(3, min(args.warmup, 10)))
+
     if rank != 0:
         dist.destroy_process_group()
         return
@@ -373,6 +463,8 @@ def run_ours(args):
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
     }
+    if args.mode == "all":
+        line["prefill"] = {"ragged_bf16": prefill_res[4], "fp8_fp8": prefill_res[5]}
     if world == 1 and not args.no_cpu_baseline:
         n = oracle_sample_size(b, 15.0)
         dt, by, cores = oracle_decode_sample(b, n)
