@@ -14,10 +14,18 @@ fixed-split and disable-split options; the balanced rule is this library's):
 * otherwise (balanced): T = total pages of all rows, G = min(num_ctas, T);
   CTA i owns global pages [i*T//G, (i+1)*T//G) of the rows laid end to end,
   cut at row boundaries.
-* A segment that spans its whole row has out_slot -1; the others get slots
-  0, 1, 2, ... in segment order (CTA by CTA).
-* Merge rows: rows with no pages or with two or more segments, ascending;
-  each lists its slots ordered by first page.
+* Rows with no pages get a zero-page segment (r, 0, 0); the k-th such row
+  (ascending r) goes to CTA k mod G, after that CTA's other segments.  If no
+  row has pages, G = 1 when some row exists.
+* Within each CTA, segments that cover only part of their row come first
+  (keeping their order), then the rest.
+* A segment that spans its whole row (including a zero-page one) has
+  out_slot -1; the others get slots 0, 1, 2, ... in final segment order
+  (CTA by CTA).
+* Merge rows: rows with two or more segments, ascending; each lists its
+  slots ordered by first page.  row_merge[r] is the merge entry of row r, or
+  -1.  The merge is done inside the decode kernel by the warp that finishes
+  a split row's last segment.
 """
 from __future__ import annotations
 
@@ -71,21 +79,35 @@ def decode_metadata(kv_indptr, last_page_len, *, num_qo_heads, num_kv_heads, num
                 if e > a:
                     per_cta[i].append([r, a, e, 0])
 
+    empty = [r for r in range(R) if npages[r] == 0]
+    if empty and not per_cta:
+        per_cta = [[]]
+    for k, r in enumerate(empty):
+        per_cta[k % len(per_cta)].append([r, 0, 0, 0])
+
+    def is_partial(sg):
+        return not (sg[1] == 0 and sg[2] == npages[sg[0]])
+
+    per_cta = [[sg for sg in segs if is_partial(sg)] + [sg for sg in segs if not is_partial(sg)]
+               for segs in per_cta]
+
     slot = 0
     seg_count = [0] * R
     row_slots = [[] for _ in range(R)]
     for segs in per_cta:
         for s in segs:
             seg_count[s[0]] += 1
-            if s[1] == 0 and s[2] == npages[s[0]]:
+            if not is_partial(s):
                 s[3] = -1
             else:
                 s[3] = slot
                 row_slots[s[0]].append((s[1], slot))
                 slot += 1
     merge_rows, merge_ptr, merge_slots = [], [0], []
+    row_merge = [-1] * R
     for r in range(R):
-        if npages[r] == 0 or seg_count[r] >= 2:
+        if seg_count[r] >= 2:
+            row_merge[r] = len(merge_rows)
             merge_rows.append(r)
             merge_slots += [sl for _, sl in sorted(row_slots[r])]
             merge_ptr.append(len(merge_slots))
@@ -125,4 +147,56 @@ def decode_metadata(kv_indptr, last_page_len, *, num_qo_heads, num_kv_heads, num
     put(14, merge_ptr)
     put(15, merge_rows)
     put(16, merge_slots)
+    put(21, row_merge)
+    return words
+
+
+def prefill_metadata(kv_indptr, last_page_len, qo_indptr, *, num_qo_heads, num_kv_heads, num_ctas,
+                     page_size=16):
+    """Prefill work tiles.  For request b, KV head hk and each block of
+    TQ = 128 // group consecutive new tokens starting at t0, one tile; its
+    KV-tile count is the number of 128-key tiles its last token may see under
+    the bottom-right causal rule, capped by the request's own key tiles.
+    Tiles are sorted by that count, descending, ties in (b, hk, t0) order;
+    G = min(num_ctas, #tiles) persistent CTAs take tiles i, i + G, ..."""
+    kv_indptr = [int(x) for x in kv_indptr]
+    last_page_len = [int(x) for x in last_page_len]
+    qo_indptr = [int(x) for x in qo_indptr]
+    B = len(kv_indptr) - 1
+    group = num_qo_heads // num_kv_heads
+    TQ = 128 // group
+    req_page, req_kv, tiles = [], [], []
+    for b in range(B):
+        n = kv_indptr[b + 1] - kv_indptr[b]
+        kv = (n - 1) * page_size + last_page_len[b] if n > 0 else 0
+        req_page.append(kv_indptr[b])
+        req_kv.append(kv)
+        qo = qo_indptr[b + 1] - qo_indptr[b]
+        for hk in range(num_kv_heads):
+            for t0 in range(0, qo, TQ):
+                last = min(t0 + TQ, qo) - 1
+                lim = last + kv - qo
+                nkv = min((kv + 127) // 128, lim // 128 + 1)
+                tiles.append((b, hk, t0, nkv))
+    tiles = sorted(tiles, key=lambda t: -t[3])  # stable
+    G = min(num_ctas, len(tiles))
+    words = [0] * HEADER_WORDS
+    words[0] = MAGIC
+    words[1] = 1
+    words[2] = B
+    words[3] = num_kv_heads
+    words[4] = 1
+    words[5] = group
+    words[6] = G
+    words[18] = len(tiles)
+    words[20] = TQ
+
+    def put(field, arr):
+        words[field] = len(words)
+        words.extend(arr)
+
+    put(10, req_page)
+    put(11, req_kv)
+    put(17, qo_indptr)
+    put(19, [x for t in tiles for x in t])
     return words

@@ -12,8 +12,9 @@
 // Design (one persistent CTA per SM):
 //  * Warp `HPC` is the producer.  It walks the CTA's segments (row, page
 //    range) from the plan, prefetches 32 page indices per warp-wide load, and
-//    for each page issues one TMA box per KV head and tensor (16 tokens x 128
-//    bytes, 128B-swizzled) into a ring of shared-memory stages guarded by
+//    for each page issues one TMA box per tensor covering the block's KV
+//    heads (or one per head), 16 tokens x 128 bytes per head, 128B-swizzled,
+//    head-major in shared memory, into a ring of stages guarded by
 //    full/empty mbarriers.  Every wait is bounded; on expiry the kernel sets a
 //    status bit and returns after its copies in flight have landed.
 //  * Warps 0..HPC-1 are consumers, one per KV head of the block.  Each
@@ -29,7 +30,10 @@
 //    dims 16g..16g+15), so every shared-memory read is one conflict-free
 //    16-byte load.
 //  * A segment covering its whole request writes o and lse; a partial one
-//    writes (O/l, lse in log2 units) to the workspace for the merge kernel.
+//    writes (O/l, lse in log2 units) to the workspace, and the warp that
+//    completes the last partial segment of a (request, KV head) merges them
+//    by their log-sum-exp (a counter per (row, head) in the workspace, reset
+//    after use).  A request with no KV writes o = 0, lse = -inf.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -114,10 +118,69 @@ __device__ __forceinline__ float load_q(uint32_t (&qf)[16], const void* q, int q
     return factor;
 }
 
+// One warp combines the partial states of the `group` query heads of KV head
+// `kvh` (index `hl` within its block) of request b: L = log2 sum 2^lse_c,
+// o = v_scale * sum 2^(lse_c - L) O_c, over slots merge_slot[s0..s1) in page
+// order (running max and rescaled sums, one slot per step).  Lane i handles
+// dims 4i .. 4i+3 of every head.  The partial states were written by other
+// CTAs, so they are read through L2, all loads of a step issued before any
+// is used: the merging warp holds up its CTA's page ring meanwhile.
+__device__ __forceinline__ void merge_head_group(const DecodeParams& p, const int* merge_slot, int s0,
+                                                 int s1, int hpc, int group, int hl, int b, int kvh,
+                                                 int lane) {
+    const int hpb = hpc * group;
+    float Lr[kMaxGroupDecode], Sr[kMaxGroupDecode];
+    float4 Ar[kMaxGroupDecode];
+#pragma unroll
+    for (int n = 0; n < kMaxGroupDecode; ++n) {
+        Lr[n] = -INFINITY;
+        Sr[n] = 0.f;
+        Ar[n] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    for (int s = s0; s < s1; ++s) {
+        const size_t b0 = (size_t)merge_slot[s] * hpb + (size_t)hl * group;
+        float l0[kMaxGroupDecode];
+        float4 v0[kMaxGroupDecode];
+#pragma unroll
+        for (int n = 0; n < kMaxGroupDecode; ++n) {
+            if (n < group) {
+                l0[n] = __ldcg(p.part_lse + b0 + n);
+                v0[n] = __ldcg(reinterpret_cast<const float4*>(p.part_o + (b0 + n) * D) + lane);
+            }
+        }
+#pragma unroll
+        for (int n = 0; n < kMaxGroupDecode; ++n) {
+            if (n < group) {
+                const float mx = fmaxf(Lr[n], l0[n]);
+                const float a = ex2(Lr[n] - mx), w0 = ex2(l0[n] - mx);
+                Sr[n] = Sr[n] * a + w0;
+                Ar[n].x = Ar[n].x * a + w0 * v0[n].x;
+                Ar[n].y = Ar[n].y * a + w0 * v0[n].y;
+                Ar[n].z = Ar[n].z * a + w0 * v0[n].z;
+                Ar[n].w = Ar[n].w * a + w0 * v0[n].w;
+                Lr[n] = mx;
+            }
+        }
+    }
+#pragma unroll
+    for (int n = 0; n < kMaxGroupDecode; ++n) {
+        if (n < group) {
+            const float sc = p.v_scale / Sr[n];
+            const size_t oh = (size_t)b * p.num_qo_heads + (size_t)kvh * group + n;
+            uint2 wv;
+            wv.x = pack_out2(Ar[n].x * sc, Ar[n].y * sc, p.o_dtype);
+            wv.y = pack_out2(Ar[n].z * sc, Ar[n].w * sc, p.o_dtype);
+            *reinterpret_cast<uint2*>(static_cast<uint16_t*>(p.o) + oh * D + 4 * lane) = wv;
+            if (lane == 0 && p.lse != nullptr) p.lse[oh] = (Lr[n] + __log2f(Sr[n])) * 0.69314718055994531f;
+        }
+    }
+}
+
 template <int KT>
 __global__ void __launch_bounds__(32 * 9, 1)
     decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtensorMap tmk,
-                  const __grid_constant__ CUtensorMap tmv, int hpc, int group, int stages) {
+                  const __grid_constant__ CUtensorMap tmv, int hpc, int group, int stages,
+                  int heads_per_box) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;      // 128B swizzle wants 1024-B alignment
@@ -133,6 +196,9 @@ __global__ void __launch_bounds__(32 * 9, 1)
     const int* cta_seg = meta + meta[kMetaOffCtaSeg];
     const int* segs = meta + meta[kMetaOffSeg];
     const int seg_begin = cta_seg[blockIdx.x], seg_end = cta_seg[blockIdx.x + 1];
+    const int* merge_ptr = meta + meta[kMetaOffMergePtr];
+    const int* merge_slot = meta + meta[kMetaOffMergeSlot];
+    const int* row_merge = meta + meta[kMetaOffRowMerge];
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < stages; ++s) {
@@ -174,9 +240,16 @@ __global__ void __launch_bounds__(32 * 9, 1)
                             mbar_arrive_expect_tx(fb, stage_bytes);
                             const uint32_t sk = base + stage * stage_bytes;
                             const uint32_t sv = sk + hpc * kTileBytes;
-                            for (int h = 0; h < hpc; ++h) {
-                                tma_load_4d(sk + h * kTileBytes, &tmk, fb, 0, hb * hpc + h, 0, pg);
-                                tma_load_4d(sv + h * kTileBytes, &tmv, fb, 0, hb * hpc + h, 0, pg);
+                            if (heads_per_box == hpc) {
+                                // one box = every head of the block: (d, token, head, page)
+                                tma_load_4d(sk, &tmk, fb, 0, 0, hb * hpc, pg);
+                                tma_load_4d(sv, &tmv, fb, 0, 0, hb * hpc, pg);
+                            } else {
+                                // one box per head: (d, head, token, page)
+                                for (int h = 0; h < hpc; ++h) {
+                                    tma_load_4d(sk + h * kTileBytes, &tmk, fb, 0, hb * hpc + h, 0, pg);
+                                    tma_load_4d(sv + h * kTileBytes, &tmv, fb, 0, hb * hpc + h, 0, pg);
+                                }
                             }
                             ++issued;
                         }
@@ -216,6 +289,20 @@ __global__ void __launch_bounds__(32 * 9, 1)
         const int b = row / nhb, hb = row - b * nhb;
         const int kvh = hb * hpc + warp;
         const int kv_len = req_kv[b];
+
+        if (p0 == p1) {  // a request with no KV: o = 0, lse = -inf
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const int n = 2 * t + hh;
+                if (n >= group) continue;
+                const size_t oh = (size_t)b * Hq + (size_t)kvh * group + n;
+                uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + oh * D + 16 * g);
+                dst[0] = make_uint4(0, 0, 0, 0);
+                dst[1] = make_uint4(0, 0, 0, 0);
+                if (g == 0 && p.lse != nullptr) p.lse[oh] = -INFINITY;
+            }
+            continue;
+        }
 
         uint32_t qf[16];
         const size_t q_head_off = ((size_t)b * Hq + (size_t)kvh * group + g) * D;
@@ -357,52 +444,24 @@ __global__ void __launch_bounds__(32 * 9, 1)
                 if (g == 0) p.part_lse[(size_t)slot * hpb + warp * group + n] = m + __log2f(l);
             }
         }
+        if (slot >= 0) {
+            // The warp that completes the last partial segment of this
+            // (row, KV head) combines every partial state of it.
+            __threadfence();
+            __syncwarp();
+            int done = 0;
+            if (lane == 0) done = atomicAdd(p.counters + (size_t)row * hpc + warp, 1);
+            done = __shfl_sync(0xFFFFFFFFu, done, 0);
+            const int e = row_merge[row];
+            const int s0 = merge_ptr[e], s1 = merge_ptr[e + 1];
+            if (done == s1 - s0 - 1) {
+                __threadfence();
+                merge_head_group(p, merge_slot, s0, s1, hpc, group, warp, b, kvh, lane);
+                if (lane == 0) p.counters[(size_t)row * hpc + warp] = 0;
+            }
+        }
     }
     if (!ok && lane == 0) flag(p.status, kStatusTimeout);
-}
-
-// Combine the partial states of each split request (and write o = 0,
-// lse = -inf for requests with no KV).  Block = one (merge row, KV head of the
-// block), 128 threads = the head dimension.
-__global__ void __launch_bounds__(128)
-    merge_kernel(const __grid_constant__ DecodeParams p, int hpc, int group) {
-    const int* meta = p.meta;
-    const int nhb = meta[kMetaHeadBlocks];
-    const int* mptr = meta + meta[kMetaOffMergePtr];
-    const int* mrow = meta + meta[kMetaOffMergeRow];
-    const int* mslot = meta + meta[kMetaOffMergeSlot];
-    const int e = blockIdx.x, hl = blockIdx.y, d = threadIdx.x;
-    const int row = mrow[e];
-    const int b = row / nhb, hb = row - b * nhb;
-    const int s0 = mptr[e], s1 = mptr[e + 1];
-    const int hpb = hpc * group;
-    const int Hq = p.num_qo_heads;
-    for (int n = 0; n < group; ++n) {
-        const int hh = hl * group + n;
-        const int head = (hb * hpc + hl) * group + n;
-        float L = -INFINITY;
-        for (int s = s0; s < s1; ++s) L = fmaxf(L, p.part_lse[(size_t)mslot[s] * hpb + hh]);
-        float o = 0.f, lse = -INFINITY;
-        if (L != -INFINITY) {
-            float sum = 0.f;
-            for (int s = s0; s < s1; ++s) {
-                const float w = ex2(p.part_lse[(size_t)mslot[s] * hpb + hh] - L);
-                sum += w;
-                o += w * p.part_o[((size_t)mslot[s] * hpb + hh) * D + d];
-            }
-            o = o / sum * p.v_scale;
-            lse = (L + __log2f(sum)) * 0.69314718055994531f;
-        }
-        uint16_t* dst = static_cast<uint16_t*>(p.o) + ((size_t)b * Hq + head) * D + d;
-        if (p.o_dtype == PAFP8_BF16) {
-            __nv_bfloat16 h = __float2bfloat16_rn(o);
-            *dst = *reinterpret_cast<uint16_t*>(&h);
-        } else {
-            __half h = __float2half_rn(o);
-            *dst = *reinterpret_cast<uint16_t*>(&h);
-        }
-        if (d == 0 && p.lse != nullptr) p.lse[(size_t)b * Hq + head] = lse;
-    }
 }
 
 }  // namespace
@@ -436,7 +495,7 @@ cudaError_t noalloc_scratch(void** ptr) {
 }
 
 cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& tmap_k, const CUtensorMap& tmap_v,
-                          int num_ctas, int hpc, int group, cudaStream_t stream) {
+                          int num_ctas, int hpc, int group, int heads_per_box, cudaStream_t stream) {
     const int stage_bytes = 2 * hpc * kTileBytes;
     int stages = kStageBudget / stage_bytes;
     if (stages > 8) stages = 8;
@@ -448,20 +507,17 @@ cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& tmap_k, cons
         e = cudaFuncSetAttribute(decode_kernel<PAFP8_E4M3FN>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        decode_kernel<PAFP8_E4M3FN><<<grid, block, smem, stream>>>(p, tmap_k, tmap_v, hpc, group, stages);
+        decode_kernel<PAFP8_E4M3FN><<<grid, block, smem, stream>>>(p, tmap_k, tmap_v, hpc, group, stages,
+                                                                   heads_per_box);
     } else {
         e = cudaFuncSetAttribute(decode_kernel<PAFP8_E5M2>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        decode_kernel<PAFP8_E5M2><<<grid, block, smem, stream>>>(p, tmap_k, tmap_v, hpc, group, stages);
+        decode_kernel<PAFP8_E5M2><<<grid, block, smem, stream>>>(p, tmap_k, tmap_v, hpc, group, stages,
+                                                                 heads_per_box);
     }
     return cudaGetLastError();
 }
 
-cudaError_t launch_merge(const DecodeParams& p, int num_merge, int hpc, int group,
-                         cudaStream_t stream) {
-    merge_kernel<<<dim3(num_merge, hpc), 128, 0, stream>>>(p, hpc, group);
-    return cudaGetLastError();
-}
 
 }  // namespace pafp8

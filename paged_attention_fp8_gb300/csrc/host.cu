@@ -115,7 +115,8 @@ struct pafp8_plan {
     int64_t nnz_pages = 0, nnz_qo = 0;
     int heads_per_cta = 1, head_blocks = 1, group = 1;
     int num_ctas = 0, num_partials = 0, num_merge = 0;
-    size_t meta_bytes = 0, part_o_off = 0, part_lse_off = 0, status_off = 0, ws_bytes = 0;
+    size_t meta_bytes = 0, part_o_off = 0, part_lse_off = 0, counters_off = 0, status_off = 0,
+           ws_bytes = 0;
     void* uploaded_ws = nullptr;
 };
 
@@ -132,9 +133,12 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 //                     G = min(num_ctas, T), CTA i takes the global page range
 //                     [floor(i*T/G), floor((i+1)*T/G)) of the rows laid end to
 //                     end, cut at row boundaries into segments.
-// A segment spanning its whole row writes the final output (slot -1); every
-// other segment writes a partial state to the next free slot (in segment
-// order).  Rows with no pages or with several segments are merged.
+// Rows with no pages get a zero-page segment (written as o = 0, lse = -inf)
+// dealt round-robin after the other segments, and each CTA runs its partial
+// segments first.  A segment spanning its whole row writes the final output
+// (slot -1); every other segment writes a partial state to the next free slot
+// (in final segment order), and the warp that completes a split row's last
+// segment merges its partial states by their log-sum-exp.
 void build_decode_meta(pafp8_plan* pl) {
     const int B = pl->desc.batch;
     const int nhb = pl->head_blocks;
@@ -178,6 +182,20 @@ void build_decode_meta(pafp8_plan* pl) {
         }
     }
 
+    // Rows with no pages: a zero-page segment each (it writes o = 0 and
+    // lse = -inf), the k-th one appended to CTA k mod G.
+    std::vector<int> empty;
+    for (int r = 0; r < R; ++r)
+        if (np[r] == 0) empty.push_back(r);
+    if (!empty.empty() && per_cta.empty()) per_cta.assign(1, {});
+    for (size_t k = 0; k < empty.size(); ++k)
+        per_cta[k % per_cta.size()].push_back({empty[k], 0, 0, 0});
+
+    // Within a CTA, segments covering part of their row run first, so the
+    // merges of split rows happen early rather than in the kernel's tail.
+    auto partial = [&](const Seg& sg) { return !(sg.p0 == 0 && sg.p1 == np[sg.row]); };
+    for (auto& v : per_cta) std::stable_partition(v.begin(), v.end(), partial);
+
     // Output slots and the merge lists.
     std::vector<int> nseg_row(R, 0);
     for (auto& v : per_cta)
@@ -186,17 +204,18 @@ void build_decode_meta(pafp8_plan* pl) {
     std::vector<std::vector<std::pair<int32_t, int32_t>>> row_slots(R);  // (p0, slot)
     for (auto& v : per_cta)
         for (auto& s : v) {
-            if (s.p0 == 0 && s.p1 == np[s.row]) {
+            if (!partial(s)) {
                 s.slot = -1;
             } else {
                 s.slot = nslot++;
                 row_slots[s.row].push_back({s.p0, s.slot});
             }
         }
-    std::vector<int32_t> merge_rows, merge_ptr{0}, merge_slots;
+    std::vector<int32_t> merge_rows, merge_ptr{0}, merge_slots, row_merge(R, -1);
     for (int r = 0; r < R; ++r) {
-        if (np[r] == 0 || nseg_row[r] >= 2) {
+        if (nseg_row[r] >= 2) {
             std::sort(row_slots[r].begin(), row_slots[r].end());
+            row_merge[r] = (int32_t)merge_rows.size();
             merge_rows.push_back(r);
             for (auto& ps : row_slots[r]) merge_slots.push_back(ps.second);
             merge_ptr.push_back((int32_t)merge_slots.size());
@@ -246,6 +265,7 @@ void build_decode_meta(pafp8_plan* pl) {
     put(kMetaOffMergePtr, merge_ptr);
     put(kMetaOffMergeRow, merge_rows);
     put(kMetaOffMergeSlot, merge_slots);
+    put(kMetaOffRowMerge, row_merge);
 
     pl->num_ctas = G;
     pl->num_partials = nslot;
@@ -317,7 +337,11 @@ void layout_workspace(pafp8_plan* pl) {
     pl->meta_bytes = align_up(pl->meta.size() * sizeof(int32_t), 256);
     pl->part_o_off = pl->meta_bytes;
     pl->part_lse_off = align_up(pl->part_o_off + (size_t)pl->num_partials * heads * kHeadDim * 4, 256);
-    pl->status_off = align_up(pl->part_lse_off + (size_t)pl->num_partials * heads * 4, 256);
+    pl->counters_off = align_up(pl->part_lse_off + (size_t)pl->num_partials * heads * 4, 256);
+    const size_t rows = pl->desc.mode == PAFP8_MODE_DECODE
+                            ? (size_t)pl->desc.batch * pl->head_blocks * pl->heads_per_cta
+                            : 0;
+    pl->status_off = align_up(pl->counters_off + rows * 4, 256);
     pl->ws_bytes = pl->status_off + 256;
 }
 
@@ -377,6 +401,45 @@ pafp8_status encode_q_map(CUtensorMap* map, const void* base, int nnz_qo, int hq
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS)
         return fail(PAFP8_ERR_CUDA, "cuTensorMapEncodeTiled failed for q (CUresult %d)", (int)r);
+    return PAFP8_OK;
+}
+
+// Decode maps over one cache tensor.  First choice: dims (d, token, head,
+// page) with a box of {128, 16, hpc, 1}, so one TMA box brings a whole page
+// of the head block, landing head-major ([head][token][128 B]).  If the
+// driver does not accept that dimension order, fall back to one box per head
+// (encode_cache_map); the shared-memory layout is the same either way.
+pafp8_status encode_decode_maps(CUtensorMap* tk, CUtensorMap* tv, const void* k, const void* v,
+                                int num_pages, int hkv, int hpc, int* heads_per_box) {
+    if (num_pages == 0 || k == nullptr || v == nullptr) {
+        // No request has pages: the kernel issues no copy, the maps are unused.
+        memset(tk, 0, sizeof(*tk));
+        memset(tv, 0, sizeof(*tv));
+        *heads_per_box = 1;
+        return PAFP8_OK;
+    }
+    auto enc = get_encode();
+    if (!enc) return fail(PAFP8_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    cuuint64_t dims[4] = {(cuuint64_t)kHeadDim, (cuuint64_t)kPageSize, (cuuint64_t)hkv,
+                          (cuuint64_t)num_pages};
+    cuuint64_t strides[3] = {(cuuint64_t)hkv * kHeadDim, (cuuint64_t)kHeadDim,
+                             (cuuint64_t)kPageSize * hkv * kHeadDim};
+    cuuint32_t box[4] = {(cuuint32_t)kHeadDim, (cuuint32_t)kPageSize, (cuuint32_t)hpc, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult rk = enc(tk, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(k), dims, strides, box,
+                      estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult rv = enc(tv, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(v), dims, strides, box,
+                      estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (rk == CUDA_SUCCESS && rv == CUDA_SUCCESS) {
+        *heads_per_box = hpc;
+        return PAFP8_OK;
+    }
+    pafp8_status st;
+    if ((st = encode_cache_map(tk, k, num_pages, hkv)) != PAFP8_OK) return st;
+    if ((st = encode_cache_map(tv, v, num_pages, hkv)) != PAFP8_OK) return st;
+    *heads_per_box = 1;
     return PAFP8_OK;
 }
 
@@ -534,7 +597,8 @@ pafp8_status pafp8_plan_upload(pafp8_plan* plan, void* workspace, size_t workspa
     cudaError_t e = cudaMemcpyAsync(workspace, plan->meta.data(), plan->meta.size() * 4,
                                     cudaMemcpyHostToDevice, s);
     if (e == cudaSuccess)
-        e = cudaMemsetAsync((char*)workspace + plan->status_off, 0, 256, s);
+        e = cudaMemsetAsync((char*)workspace + plan->counters_off, 0,
+                            plan->status_off + 256 - plan->counters_off, s);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return fail(PAFP8_ERR_CUDA, "metadata upload failed: %s", cudaGetErrorString(e));
@@ -645,6 +709,7 @@ pafp8_status pafp8_run_stage(const pafp8_plan* plan, int32_t stage, int32_t q_dt
     p.meta = (const int32_t*)ws;
     p.part_o = (float*)(ws + plan->part_o_off);
     p.part_lse = (float*)(ws + plan->part_lse_off);
+    p.counters = (int*)(ws + plan->counters_off);
     p.status = (uint32_t*)(ws + plan->status_off);
     p.q_dtype = q_dtype;
     p.kv_dtype = k_dtype;
@@ -656,14 +721,14 @@ pafp8_status pafp8_run_stage(const pafp8_plan* plan, int32_t stage, int32_t q_dt
     p.v_scale = v_scale;
 
     cudaError_t e = cudaSuccess;
-    if (stage != 2 && plan->num_ctas > 0) {
+    if (stage != 2 && plan->num_ctas > 0) {  // decode has one launch: merges are fused
         CUtensorMap tk, tv;
-        if ((st = encode_cache_map(&tk, k_cache, d.num_pages, d.num_kv_heads)) != PAFP8_OK) return st;
-        if ((st = encode_cache_map(&tv, v_cache, d.num_pages, d.num_kv_heads)) != PAFP8_OK) return st;
-        e = launch_decode(p, tk, tv, plan->num_ctas, plan->heads_per_cta, plan->group, s);
+        int hpb = 1;
+        if ((st = encode_decode_maps(&tk, &tv, k_cache, v_cache, d.num_pages, d.num_kv_heads,
+                                     plan->heads_per_cta, &hpb)) != PAFP8_OK)
+            return st;
+        e = launch_decode(p, tk, tv, plan->num_ctas, plan->heads_per_cta, plan->group, hpb, s);
     }
-    if (e == cudaSuccess && stage != 1 && plan->num_merge > 0)
-        e = launch_merge(p, plan->num_merge, plan->heads_per_cta, plan->group, s);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return fail(PAFP8_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(e));
@@ -749,7 +814,8 @@ pafp8_status pafp8_run_decode_noalloc(const pafp8_plan* plan, int32_t q_dtype, c
     // The scratch keeps the previous call's bytes: load this plan's metadata
     // and clear the status word; partial states are written before read.
     e = cudaMemcpyAsync(ws, plan->meta.data(), plan->meta.size() * 4, cudaMemcpyHostToDevice, s);
-    if (e == cudaSuccess) e = cudaMemsetAsync(ws + plan->status_off, 0, 256, s);
+    if (e == cudaSuccess)
+        e = cudaMemsetAsync(ws + plan->counters_off, 0, plan->status_off + 256 - plan->counters_off, s);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return fail(PAFP8_ERR_CUDA, "loading the plan into the built-in scratch failed: %s",
@@ -763,6 +829,7 @@ pafp8_status pafp8_run_decode_noalloc(const pafp8_plan* plan, int32_t q_dtype, c
     p.meta = (const int32_t*)ws;
     p.part_o = (float*)(ws + plan->part_o_off);
     p.part_lse = (float*)(ws + plan->part_lse_off);
+    p.counters = (int*)(ws + plan->counters_off);
     p.status = (uint32_t*)(ws + plan->status_off);
     p.q_dtype = q_dtype;
     p.kv_dtype = k_dtype;
@@ -775,12 +842,12 @@ pafp8_status pafp8_run_decode_noalloc(const pafp8_plan* plan, int32_t q_dtype, c
     p.v_scale = v_scale;
     if (plan->num_ctas > 0) {
         CUtensorMap tk, tv;
-        if ((st = encode_cache_map(&tk, k_cache, d.num_pages, d.num_kv_heads)) != PAFP8_OK) return st;
-        if ((st = encode_cache_map(&tv, v_cache, d.num_pages, d.num_kv_heads)) != PAFP8_OK) return st;
-        e = launch_decode(p, tk, tv, plan->num_ctas, plan->heads_per_cta, plan->group, s);
+        int hpb = 1;
+        if ((st = encode_decode_maps(&tk, &tv, k_cache, v_cache, d.num_pages, d.num_kv_heads,
+                                     plan->heads_per_cta, &hpb)) != PAFP8_OK)
+            return st;
+        e = launch_decode(p, tk, tv, plan->num_ctas, plan->heads_per_cta, plan->group, hpb, s);
     }
-    if (e == cudaSuccess && plan->num_merge > 0)
-        e = launch_merge(p, plan->num_merge, plan->heads_per_cta, plan->group, s);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return fail(PAFP8_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(e));

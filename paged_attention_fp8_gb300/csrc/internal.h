@@ -42,6 +42,7 @@ enum MetaHeader : int {
     kMetaNumTiles,       // prefill tiles
     kMetaOffTile,        // int32[4*num_tiles] prefill tiles
     kMetaTileRows,       // packed query rows per prefill tile
+    kMetaOffRowMerge,    // int32[rows] merge entry of each decode row, or -1
     kMetaHeaderWords = 32
 };
 constexpr int32_t kMetaMagicValue = 0x38464150;
@@ -60,6 +61,7 @@ struct DecodeParams {
     const int32_t* meta;     // device copy of the metadata words
     float* part_o;           // [num_partials, hpc*group, D]
     float* part_lse;         // [num_partials, hpc*group] (log2 domain)
+    int* counters;           // [rows * hpc] finished partial segments per (row, head)
     uint32_t* status;
     int q_dtype, kv_dtype, o_dtype;
     int num_qo_heads, num_kv_heads, num_pages;
@@ -83,11 +85,11 @@ struct PrefillParams {
 };
 
 // Launchers (decode.cu, prefill.cu).  Return the launch's cudaError_t.
+// heads_per_box: KV heads covered by one TMA box of the cache maps (the
+// whole head block when the page-wide map could be encoded, else 1).
 cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& tmap_k,
                           const CUtensorMap& tmap_v, int num_ctas, int heads_per_cta,
-                          int group, cudaStream_t stream);
-cudaError_t launch_merge(const DecodeParams& p, int num_merge, int heads_per_cta, int group,
-                         cudaStream_t stream);
+                          int group, int heads_per_box, cudaStream_t stream);
 // Size of the built-in scratch of the no-allocation decode entry point, and
 // the device ordinals it serves.
 constexpr size_t kNoAllocScratchBytes = PAFP8_NOALLOC_SCRATCH_BYTES;

@@ -222,3 +222,81 @@ def test_run_refuses_bad_scales():
             assert st == 3 and "scales" in pa.pafp8_last_error()
     finally:
         pa.pafp8_plan_destroy(h)
+
+
+# ------------------------------------------------------------ prefill plans
+
+def _prefill_plan(kv_lens, qo_lens, *, hq=32, hkv=8, num_ctas=152):
+    P = 16
+    npages = [(L + P - 1) // P for L in kv_lens]
+    indptr = np.concatenate([[0], np.cumsum(npages)]).astype(np.int32)
+    last = np.array([(L - (n - 1) * P) if n else 0 for L, n in zip(kv_lens, npages)], dtype=np.int32)
+    qo_indptr = np.concatenate([[0], np.cumsum(qo_lens)]).astype(np.int32)
+    plan = pa.Plan(mode="prefill", num_qo_heads=hq, num_kv_heads=hkv, num_pages=max(1, int(indptr[-1])),
+                   kv_indptr=indptr, last_page_len=last, qo_indptr=qo_indptr, q_dtype="bf16",
+                   kv_dtype="e4m3fn", num_ctas=num_ctas)
+    ref = plan_rule.prefill_metadata(indptr, last, qo_indptr, num_qo_heads=hq, num_kv_heads=hkv,
+                                     num_ctas=num_ctas)
+    return plan, np.array(ref, dtype=np.int32)
+
+
+PREFILL_CASES = [
+    dict(kv_lens=[40], qo_lens=[40], hq=8, hkv=2),
+    dict(kv_lens=[5, 200, 1000, 3000], qo_lens=[5, 40, 1000, 17], hq=32, hkv=8, num_ctas=7),
+    dict(kv_lens=[129, 128, 127, 0], qo_lens=[129, 1, 100, 0], hq=16, hkv=1),
+    dict(kv_lens=[300, 700], qo_lens=[300, 33], hq=24, hkv=8, num_ctas=2),
+    dict(kv_lens=[2048] * 8, qo_lens=[2048] * 8, hq=32, hkv=8),
+    dict(kv_lens=[100, 90], qo_lens=[60, 90], hq=6, hkv=2, num_ctas=1000),
+]
+
+
+@pytest.mark.parametrize("case", PREFILL_CASES)
+def test_prefill_plan_metadata_bit_exact(case):
+    plan, ref = _prefill_plan(**case)
+    assert np.array_equal(plan.metadata(), ref)
+
+
+@pytest.mark.parametrize("case", PREFILL_CASES)
+def test_prefill_tiles_cover_every_row_head_once(case):
+    plan, _ = _prefill_plan(**case)
+    m = plan.metadata()
+    hq, hkv = case.get("hq", 32), case.get("hkv", 8)
+    g = hq // hkv
+    tq = int(m[20])
+    tiles = m[m[19]:m[19] + 4 * int(m[18])].reshape(-1, 4)
+    seen = set()
+    for b, hk, t0, nkv in tiles:
+        qo, kv = case["qo_lens"][b], case["kv_lens"][b]
+        for tok in range(t0, min(t0 + tq, qo)):
+            for h in range(hk * g, hk * g + g):
+                assert (b, tok, h) not in seen
+                seen.add((b, tok, h))
+            # every key the token may see lies in the tile's KV tiles
+            assert tok + kv - qo < nkv * 128
+    want = {(b, t, h) for b, qo in enumerate(case["qo_lens"]) for t in range(qo) for h in range(hq)}
+    assert seen == want
+    assert list(tiles[:, 3]) == sorted(tiles[:, 3], reverse=True)
+
+
+@pytest.mark.parametrize("qo,kv,word", [([50], [40], "qo_len"), ([3, 2], [2, 5], "qo_len")])
+def test_prefill_refuses_more_rows_than_keys(qo, kv, word):
+    with pytest.raises(pa.Pafp8Error, match=word):
+        _prefill_plan(kv, qo, hq=8, hkv=2)
+
+
+def test_prefill_refusals():
+    indptr = np.array([0, 2], np.int32)
+    last = np.array([5], np.int32)
+    with pytest.raises(pa.Pafp8Error, match="qo_indptr"):
+        pa.Plan(mode="prefill", num_qo_heads=8, num_kv_heads=2, num_pages=4, kv_indptr=indptr,
+                last_page_len=last, q_dtype="bf16", kv_dtype="e4m3fn", num_ctas=4)
+    with pytest.raises(pa.Pafp8Error) as ei:
+        pa.Plan(mode="prefill", num_qo_heads=64, num_kv_heads=2, num_pages=4, kv_indptr=indptr,
+                last_page_len=last, qo_indptr=np.array([0, 3], np.int32), q_dtype="bf16",
+                kv_dtype="e4m3fn", num_ctas=4)
+    assert ei.value.status == 8 and "prefill" in str(ei.value)
+    with pytest.raises(pa.Pafp8Error) as ei:
+        pa.Plan(mode="prefill", num_qo_heads=8, num_kv_heads=2, num_pages=4, kv_indptr=indptr,
+                last_page_len=last, qo_indptr=np.array([0, 3], np.int32), q_dtype="e4m3fn",
+                kv_dtype="e4m3fn", o_dtype="e5m2", num_ctas=4)
+    assert ei.value.status == 1

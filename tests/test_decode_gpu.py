@@ -171,3 +171,31 @@ def test_long_context_workload_sampled(cuda_device):
     ro, rl = oracle_on(b, rows=rows, heads=heads)
     assert_close(o[rows, heads], lse[rows, heads], ro, rl, "long-context decode")
     assert np.all(np.isfinite(o)) and np.all(np.isfinite(lse))
+
+
+def test_fused_merge_many_partials_and_repeat_runs(cuda_device):
+    """One-page splits give up to 256 partial states per (request, KV head),
+    merged inside the decode kernel; running the same plan again (merge
+    counters reset by the kernel) gives bit-identical results."""
+    b = make_batch([4096, 1, 700, 0, 33], num_qo_heads=32, num_kv_heads=8, seed=41)
+    db = DeviceBatch(b, cuda_device, fixed_split_pages=1)
+    db.run()
+    o1, l1 = db.result()
+    ro, rl = oracle_on(b)
+    assert_close(o1, l1, ro, rl, "one-page splits")
+    for _ in range(2):
+        db.o.zero_()
+        db.lse.zero_()
+        db.run()
+        o2, l2 = db.result()
+        assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+
+
+def test_balanced_plan_on_few_ctas_repeats_bitwise(cuda_device):
+    b = workload(1)
+    db = DeviceBatch(b, cuda_device, num_ctas=3)
+    db.run()
+    o1, l1 = db.result()
+    db.run()
+    o2, l2 = db.result()
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
