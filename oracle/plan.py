@@ -153,10 +153,11 @@ def decode_metadata(kv_indptr, last_page_len, *, num_qo_heads, num_kv_heads, num
 
 def prefill_metadata(kv_indptr, last_page_len, qo_indptr, *, num_qo_heads, num_kv_heads, num_ctas,
                      page_size=16):
-    """Prefill work tiles.  For request b, KV head hk and each block of
-    TQ = 128 // group consecutive new tokens starting at t0, one tile; its
-    KV-tile count is the number of 128-key tiles its last token may see under
-    the bottom-right causal rule, capped by the request's own key tiles.
+    """Prefill work items.  For request b, KV head hk and each block of
+    2 * TQ consecutive new tokens starting at t0 (TQ = 128 // group), one item
+    of two query tiles (A = [t0, t0+TQ), B = the next TQ); its KV-tile count
+    is the number of 128-key tiles its last token may see under the
+    bottom-right causal rule, capped by the request's own key tiles.
     Tiles are sorted by that count, descending, ties in (b, hk, t0) order;
     G = min(num_ctas, #tiles) persistent CTAs take tiles i, i + G, ..."""
     kv_indptr = [int(x) for x in kv_indptr]
@@ -173,8 +174,8 @@ def prefill_metadata(kv_indptr, last_page_len, qo_indptr, *, num_qo_heads, num_k
         req_kv.append(kv)
         qo = qo_indptr[b + 1] - qo_indptr[b]
         for hk in range(num_kv_heads):
-            for t0 in range(0, qo, TQ):
-                last = min(t0 + TQ, qo) - 1
+            for t0 in range(0, qo, 2 * TQ):
+                last = min(t0 + 2 * TQ, qo) - 1
                 lim = last + kv - qo
                 nkv = min((kv + 127) // 128, lim // 128 + 1)
                 tiles.append((b, hk, t0, nkv))

@@ -272,12 +272,12 @@ void build_decode_meta(pafp8_plan* pl) {
     pl->num_merge = (int)merge_rows.size();
 }
 
-// Prefill work tiles: for every request b, KV head hk and block of
-// TQ = 128 / group consecutive new tokens starting at t0, one tile of
-// TQ * group packed query rows.  n_kv = the KV tiles of 128 keys the tile's
-// last token may see (bottom-right causal).  Tiles are ordered longest first
-// (stable), and persistent CTA i takes tiles i, i + G, ... (G = min(num_ctas,
-// #tiles)).
+// Prefill work items: for every request b, KV head hk and block of 2 * TQ
+// consecutive new tokens starting at t0 (TQ = 128 / group), one item of two
+// query tiles of TQ * group packed rows each.  n_kv = the KV tiles of 128 keys
+// the item's last token may see (bottom-right causal).  Items are ordered
+// longest first (stable), and persistent CTA i takes items i, i + G, ...
+// (G = min(num_ctas, #items)).
 void build_prefill_meta(pafp8_plan* pl) {
     const int B = pl->desc.batch;
     const int g = pl->group;
@@ -291,8 +291,10 @@ void build_prefill_meta(pafp8_plan* pl) {
         req_kv[b] = n > 0 ? (n - 1) * pl->desc.page_size + pl->last_page_len[b] : 0;
         const int qo = pl->qo_indptr[b + 1] - pl->qo_indptr[b];
         for (int hk = 0; hk < pl->desc.num_kv_heads; ++hk)
-            for (int t0 = 0; t0 < qo; t0 += TQ) {
-                const int last = std::min(t0 + TQ, qo) - 1;
+            for (int t0 = 0; t0 < qo; t0 += 2 * TQ) {
+                // An item is two query tiles, A = [t0, t0+TQ) and B right after;
+                // its KV tiles are those of its last token.
+                const int last = std::min(t0 + 2 * TQ, qo) - 1;
                 const int lim = last + req_kv[b] - qo;
                 const int nkv = std::min((req_kv[b] + kTileKeys - 1) / kTileKeys, lim / kTileKeys + 1);
                 tiles.push_back({b, hk, t0, nkv});

@@ -11,28 +11,39 @@
 // query the QK product runs natively in fp8 ("Enable Hopper FA3 FP8 attention
 // in decode.py", review note on q_scale folding into sm_scale for FP8 BMM1).
 //
-// Work tile: one KV head of one request and 128 query rows packed as
-// (token, head-of-group) pairs -- 128/group consecutive new tokens times the
-// group's query heads -- so a K/V tile is loaded and dequantized once for all
-// query heads that share it.  KV tiles are 128 keys (8 pages).  Persistent
-// CTAs take tiles i, i + grid, ... from a longest-first list built by the plan.
+// Work item: one KV head of one request and two query tiles A and B of 128
+// rows each, packed as (token, head-of-group) pairs -- 128/group consecutive
+// new tokens times the group's query heads per tile, B right after A -- so a
+// dequantized K/V tile serves 256 query rows.  KV tiles are 128 keys (8
+// pages).  Persistent CTAs take items i, i + grid, ... from a longest-first
+// list built by the plan.
 //
-// Roles (320 threads):
-//   warps 0-3  dequant: raw fp8 K -> f16 K tile (2-byte query path); raw fp8
-//              V -> f16 V^T tile (both paths), zero beyond the request's keys;
-//   warps 4-7  softmax: thread r owns TMEM lane r = query row r.  Reads S,
-//              masks, keeps the running max and sum, writes P (f16) into TMEM,
-//              rescales O in TMEM only when the max rises by more than 2^8,
-//              and in the epilogue normalizes O and stores o and lse.  With a
-//              bf16 query it first brings its Q row into f16 range by an exact
-//              per-row power of two and converts it in place;
-//   warp 8     TMA producer: Q tile, K and V pages (one box per page);
-//   warp 9     MMA issuer and TMEM owner:
-//                S  = Q K^T   M=128 N=128, f16 (kind::f16) or fp8 (kind::f8f6f4)
-//                O += P V     M=128 N=128, A = P from TMEM, B = V^T (kind::f16)
-// TMEM columns: S double buffer 0-255, O 256-383, P 384-447.  Every operand
-// in shared memory is K-major with the 128-byte swizzle.  All waits are
-// bounded; on expiry the kernel records a status bit and winds down.
+// Roles (448 threads):
+//   warps 0-3   dequant: raw fp8 K -> f16 K tile (2-byte query path); raw fp8
+//               V -> f16 V^T tile (both paths), zero beyond the request's keys;
+//   warps 4-7   softmax of tile A, warps 8-11 softmax of tile B: thread r owns
+//               TMEM lane r = query row r of its tile.  Reads S, masks, keeps
+//               the running max and sum, writes P (f16) over the first half of
+//               S in TMEM, rescales O in TMEM only when the max rises by more
+//               than 2^8, and in the epilogue normalizes O and stores o, lse.
+//               With a bf16 query each thread first brings its Q row into f16
+//               range by an exact power of two and converts it in place;
+//   warp 12     TMA producer: both Q tiles, K and V pages (one box per page);
+//   warp 13     MMA issuer and TMEM owner.  Per KV tile j:
+//                 S_A = Q_A K_j^T, S_B = Q_B K_j^T    (kind::f16 or kind::f8f6f4)
+//                 O_A += P_A V_j,  O_B += P_B V_j      (kind::f16, A = P from TMEM)
+//               issued as ... PV_A(j), QK_A(j+1), PV_B(j), QK_B(j+1) ... so
+//               each tile's softmax overlaps the other tile's tensor work.
+// TMEM columns: S_A/P_A 0-127, S_B/P_B 128-255, O_A 256-383, O_B 384-511.
+// O_X is released by its softmax warps after each epilogue they run; the
+// MMA warp waits for that release only before the first O_X write of the
+// next item in which tile X has rows (so an empty tile B never advances the
+// barrier ahead of the wait).
+// The tensor pipe runs one CTA's MMAs in order, so an MMA writing S_X after
+// O_X += P_X V has been issued cannot overtake it, and s_full(X, j) implies
+// that the previous O update of X is complete.  Every operand in shared
+// memory is K-major with the 128-byte swizzle.  All waits are bounded; on
+// expiry the kernel records a status bit and winds down.
 #include "../../include/pafp8.h"
 #include "internal.h"
 #include "ptx.cuh"
@@ -43,9 +54,10 @@ namespace {
 using namespace ptx;
 
 constexpr int D = kHeadDim;
-constexpr int kThreads = 320;
+constexpr int kThreads = 448;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0, kColO = 256, kColP = 384;
+__device__ __forceinline__ uint32_t col_s(int x) { return 128u * (uint32_t)x; }        // S_X / P_X
+__device__ __forceinline__ uint32_t col_o(int x) { return 256u + 128u * (uint32_t)x; }  // O_X
 constexpr uint32_t kRawTile = kTileKeys * D;      // 16 KB of fp8
 constexpr uint32_t kHalfTile = kTileKeys * 128;  // 16 KB: 128 rows x 128 B
 constexpr uint32_t kF16Tile = 2 * kHalfTile;       // 32 KB of f16
@@ -54,10 +66,11 @@ template <bool kF8>
 struct Layout {
     static constexpr int NKR = kF8 ? 4 : 2;    // raw K stages
     static constexpr int NVR = 2;              // raw V stages
-    static constexpr int NK16 = kF8 ? 0 : 2;   // f16 K stages
-    static constexpr int NV16 = kF8 ? 2 : 1;   // f16 V^T stages
-    static constexpr uint32_t q = 0;
-    static constexpr uint32_t kr = 32768;
+    static constexpr int NK16 = kF8 ? 0 : 1;   // f16 K stages
+    static constexpr int NV16 = 2;             // f16 V^T stages
+    static constexpr uint32_t kQTile = kF8 ? kHalfTile : kF16Tile;
+    static constexpr uint32_t q = 0;                     // Q_A, then Q_B
+    static constexpr uint32_t kr = 2 * kQTile;
     static constexpr uint32_t vr = kr + NKR * kRawTile;
     static constexpr uint32_t k16 = vr + NVR * kRawTile;
     static constexpr uint32_t v16 = k16 + NK16 * kF16Tile;
@@ -68,13 +81,18 @@ struct Layout {
     static constexpr int bVrFull = bKrEmpty + NKR, bVrEmpty = bVrFull + NVR;
     static constexpr int bK16Full = bVrEmpty + NVR, bK16Empty = bK16Full + NK16;
     static constexpr int bV16Full = bK16Empty + NK16, bV16Empty = bV16Full + NV16;
-    static constexpr int bSFull = bV16Empty + NV16, bSEmpty = bSFull + 2;
-    static constexpr int bPFull = bSEmpty + 2, bPEmpty = bPFull + 1;
-    static constexpr int nBars = bPEmpty + 1;
+    static constexpr int bSFull = bV16Empty + NV16;  // [2]
+    static constexpr int bPFull = bSFull + 2;        // [2]
+    static constexpr int bOFull = bPFull + 2;        // [2]
+    static constexpr int bOEmpty = bOFull + 2;       // [2]
+    static constexpr int bDrain = bOEmpty + 2;
+    static constexpr int nBars = bDrain + 1;
     static constexpr uint32_t tmem_slot = bars + 8 * nBars;
     static constexpr uint32_t abort_flag = tmem_slot + 4;
     static constexpr uint32_t bytes = abort_flag + 4;
 };
+static_assert(1024 + Layout<false>::bytes <= 232448, "shared memory budget (2-byte query)");
+static_assert(1024 + Layout<true>::bytes <= 232448, "shared memory budget (fp8 query)");
 
 struct Ring {
     int idx = 0;
@@ -87,13 +105,24 @@ struct Ring {
     }
 };
 
-struct Tile {
-    int b, hk, t0, nkv;
+struct Item {
+    int b, hk, t0, nkv;  // nkv: KV tiles of the item (tile B's, or A's if B is empty)
 };
 
-__device__ __forceinline__ Tile load_tile(const int* meta, int t) {
+__device__ __forceinline__ Item load_item(const int* meta, int t) {
     const int* tl = meta + meta[kMetaOffTile] + 4 * t;
-    return Tile{tl[0], tl[1], tl[2], tl[3]};
+    return Item{tl[0], tl[1], tl[2], tl[3]};
+}
+
+// KV tiles that query tile `x` (0 = A, 1 = B) of an item needs: its last
+// token's causal limit, capped by the request's own key tiles; 0 if the tile
+// has no rows.
+__device__ __forceinline__ int tile_nkv(int t0, int x, int TQ, int qo_len, int kv_len) {
+    const int first = t0 + x * TQ;
+    if (first >= qo_len) return 0;
+    const int last = min(first + TQ, qo_len) - 1;
+    const int lim = last + kv_len - qo_len;
+    return min((kv_len + kTileKeys - 1) / kTileKeys, lim / kTileKeys + 1);
 }
 
 __device__ __forceinline__ void set_abort(uint32_t flag_addr, uint32_t* status) {
@@ -134,7 +163,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int* meta = p.meta;
-    const int n_tiles = meta[kMetaNumTiles];
+    const int n_items = meta[kMetaNumTiles];
     const int* req_page = meta + meta[kMetaOffReqPage];
     const int* req_kv = meta + meta[kMetaOffReqKvLen];
     const int* qo_ptr = meta + meta[kMetaOffReqQo];
@@ -142,7 +171,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         mbar_init(bar(L::bQFull), 1);
-        mbar_init(bar(L::bQReady), 128);
+        mbar_init(bar(L::bQReady), 256);
         mbar_init(bar(L::bQEmpty), 1);
         for (int i = 0; i < L::NKR; ++i) {
             mbar_init(bar(L::bKrFull + i), 1);
@@ -160,23 +189,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar(L::bV16Full + i), 128);
             mbar_init(bar(L::bV16Empty + i), 1);
         }
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(bar(L::bSFull + i), 1);
-            mbar_init(bar(L::bSEmpty + i), 128);
+        for (int x = 0; x < 2; ++x) {
+            mbar_init(bar(L::bSFull + x), 1);
+            mbar_init(bar(L::bPFull + x), 128);
+            mbar_init(bar(L::bOFull + x), 1);
+            mbar_init(bar(L::bOEmpty + x), 128);
         }
-        mbar_init(bar(L::bPFull), 128);
-        mbar_init(bar(L::bPEmpty), 1);
+        mbar_init(bar(L::bDrain), 1);
         asm volatile("st.shared.u32 [%0], 0;" ::"r"(flag_addr) : "memory");
         mbar_init_fence();
     }
-    if (warp == 9) tc_alloc(base + L::tmem_slot, kTmemCols);
+    if (warp == 13) tc_alloc(base + L::tmem_slot, kTmemCols);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     uint32_t tmem;
     asm volatile("ld.shared.u32 %0, [%1];" : "=r"(tmem) : "r"(base + L::tmem_slot) : "memory");
 
-    if (warp == 8) {
+    if (warp == 12) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
             prefetch_tmap(&tmq);
@@ -187,33 +217,48 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t qphase = 0;
         long long issued_k = 0, issued_v = 0, issued_q = 0;
         bool ok = true;
-        for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
-            const Tile tl = load_tile(meta, t);
-            const int q0 = qo_ptr[tl.b] + tl.t0;
+        for (int t = blockIdx.x; t < n_items && ok; t += gridDim.x) {
+            const Item it = load_item(meta, t);
+            const int q0 = qo_ptr[it.b] + it.t0;
             if (lane == 0) {
                 ok = wait_or_abort(bar(L::bQEmpty), qphase ^ 1u, flag_addr, p.status);
                 if (ok) {
                     const uint32_t qb = bar(L::bQFull);
                     if (kF8) {
-                        mbar_arrive_expect_tx(qb, (uint32_t)(128 * g * TQ));
-                        tma_load_3d(base + L::q, &tmq, qb, 0, tl.hk * g, q0);
-                    } else {
                         mbar_arrive_expect_tx(qb, (uint32_t)(2 * 128 * g * TQ));
-                        tma_load_3d(base + L::q, &tmq, qb, 0, tl.hk * g, q0);
-                        tma_load_3d(base + L::q + kHalfTile, &tmq, qb, 64, tl.hk * g, q0);
+                        tma_load_3d(base + L::q, &tmq, qb, 0, it.hk * g, q0);
+                        tma_load_3d(base + L::q + L::kQTile, &tmq, qb, 0, it.hk * g, q0 + TQ);
+                    } else {
+                        mbar_arrive_expect_tx(qb, (uint32_t)(4 * 128 * g * TQ));
+                        for (int x = 0; x < 2; ++x) {
+                            const uint32_t dst = base + L::q + x * L::kQTile;
+                            tma_load_3d(dst, &tmq, qb, 0, it.hk * g, q0 + x * TQ);
+                            tma_load_3d(dst + kHalfTile, &tmq, qb, 64, it.hk * g, q0 + x * TQ);
+                        }
                     }
                     ++issued_q;
                 }
             }
             ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
             qphase ^= 1u;
-            const int kv_len = req_kv[tl.b];
+            const int kv_len = req_kv[it.b];
             const int npages = (kv_len + kPageSize - 1) / kPageSize;
-            const int* idx = p.kv_indices + req_page[tl.b];
-            for (int j = 0; j < tl.nkv && ok; ++j) {
+            const int* idx = p.kv_indices + req_page[it.b];
+            // Page ids of the next KV tile are fetched one tile ahead.
+            int page_next = 0;
+            {
+                const int np0 = min(kTileKeys / kPageSize, npages);
+                page_next = lane < np0 ? __ldg(idx + lane) : 0;
+            }
+            for (int j = 0; j < it.nkv && ok; ++j) {
                 const int pg0 = j * (kTileKeys / kPageSize);
                 const int np = min(kTileKeys / kPageSize, npages - pg0);
-                int page = lane < np ? __ldg(idx + pg0 + lane) : 0;
+                int page = page_next;
+                if (j + 1 < it.nkv) {
+                    const int pg1 = pg0 + kTileKeys / kPageSize;
+                    const int np1 = min(kTileKeys / kPageSize, npages - pg1);
+                    page_next = lane < np1 ? __ldg(idx + pg1 + lane) : 0;
+                }
                 const bool bad = lane < np && (page < 0 || page >= p.num_pages);
                 if (bad) page = 0;
                 if (__any_sync(0xFFFFFFFFu, bad) && lane == 0) atomicOr(p.status, kStatusBounds);
@@ -228,7 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint32_t dst = base + L::kr + kr.idx * kRawTile;
                         mbar_arrive_expect_tx(fb, (uint32_t)np * kPageSize * D);
                         for (int i = 0; i < np; ++i)
-                            tma_load_4d(dst + i * 2048u, &tmk, fb, 0, tl.hk, 0, pages[i]);
+                            tma_load_4d(dst + i * 2048u, &tmk, fb, 0, it.hk, 0, pages[i]);
                         ++issued_k;
                     }
                 }
@@ -242,7 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint32_t dst = base + L::vr + vr.idx * kRawTile;
                         mbar_arrive_expect_tx(fb, (uint32_t)np * kPageSize * D);
                         for (int i = 0; i < np; ++i)
-                            tma_load_4d(dst + i * 2048u, &tmv, fb, 0, tl.hk, 0, pages[i]);
+                            tma_load_4d(dst + i * 2048u, &tmv, fb, 0, it.hk, 0, pages[i]);
                         ++issued_v;
                     }
                 }
@@ -258,89 +303,132 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int s = 0; s < L::NVR && s < issued_v; ++s)
                 mbar_wait(bar(L::bVrFull + s), (uint32_t)(((issued_v - 1 - s) / L::NVR) & 1));
         }
-    } else if (warp == 9) {
+    } else if (warp == 13) {
         // ------------------------------------------------------------- MMA
         if (lane == 0) {
             const uint32_t idesc_qk =
                 kF8 ? make_idesc(p.q_dtype == PAFP8_E5M2 ? 1 : 0, KT == PAFP8_E5M2 ? 1 : 0, 128, 128)
                     : make_idesc(0, 0, 128, 128);
             const uint32_t idesc_pv = make_idesc(0, 0, 128, 128);
+            const int nk = kF8 ? L::NKR : L::NK16;
+            const int kfull = kF8 ? L::bKrFull : L::bK16Full;
+            const int kempty = kF8 ? L::bKrEmpty : L::bK16Empty;
             Ring kring, v16;
-            uint32_t qphase = 0, pvphase = 0;
-            long long G = 0;
+            uint32_t qphase = 0;
+            uint32_t pphase[2] = {0, 0};
+            int nonempty[2] = {0, 0};  // earlier items in which tile A / B had rows
+            long long issued_any = 0;
             bool ok = true;
-            auto issue_pv = [&](int jj) -> bool {
-                if (!wait_or_abort(bar(L::bPFull), pvphase, flag_addr, p.status)) return false;
-                if (!wait_or_abort(bar(L::bV16Full + v16.idx), v16.phase, flag_addr, p.status)) return false;
+            // S_X = Q_X K^T for the K tile at the head of kring.
+            auto qk = [&](int x) {
+                const uint32_t dS = tmem + col_s(x);
+                const uint32_t qa = base + L::q + x * L::kQTile;
+                if (kF8) {
+                    const uint32_t kt = base + L::kr + kring.idx * kRawTile;
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks)
+                        tc_mma_f8_ss(dS, sw128_kmajor_desc(qa + ks * 32), sw128_kmajor_desc(kt + ks * 32),
+                                     idesc_qk, ks > 0 ? 1u : 0u);
+                } else {
+                    const uint32_t kt = base + L::k16 + kring.idx * kF16Tile;
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks) {
+                        const uint32_t off = (ks >> 2) * kHalfTile + (ks & 3) * 32;
+                        tc_mma_f16_ss(dS, sw128_kmajor_desc(qa + off), sw128_kmajor_desc(kt + off),
+                                      idesc_qk, ks > 0 ? 1u : 0u);
+                    }
+                }
+                tc_commit(bar(L::bSFull + x));
+                ++issued_any;
+            };
+            // O_X (+)= P_X V for the V tile at the head of the v16 ring.
+            auto pv = [&](int x, bool accumulate) -> bool {
+                // The first O_X write of an item waits for the epilogue of the
+                // previous item that used O_X.
+                if (!accumulate && nonempty[x] > 0 &&
+                    !wait_or_abort(bar(L::bOEmpty + x), (uint32_t)((nonempty[x] - 1) & 1), flag_addr,
+                                   p.status))
+                    return false;
+                if (!wait_or_abort(bar(L::bPFull + x), pphase[x], flag_addr, p.status)) return false;
+                pphase[x] ^= 1u;
                 tc_fence_after();
                 const uint32_t vt = base + L::v16 + v16.idx * kF16Tile;
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {
                     const uint64_t bd = sw128_kmajor_desc(vt + (ks >> 2) * kHalfTile + (ks & 3) * 32);
-                    tc_mma_f16_ts(tmem + kColO, tmem + kColP + 8 * ks, bd, idesc_pv,
-                                  (jj > 0 || ks > 0) ? 1u : 0u);
+                    tc_mma_f16_ts(tmem + col_o(x), tmem + col_s(x) + 8 * ks, bd, idesc_pv,
+                                  (accumulate || ks > 0) ? 1u : 0u);
                 }
-                tc_commit(bar(L::bPEmpty));
-                tc_commit(bar(L::bV16Empty + v16.idx));
-                v16.next(L::NV16);
-                pvphase ^= 1u;
+                ++issued_any;
                 return true;
             };
-            for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
-                const Tile tl = load_tile(meta, t);
+            for (int t = blockIdx.x; t < n_items && ok; t += gridDim.x) {
+                const Item it = load_item(meta, t);
+                const int qo_len = qo_ptr[it.b + 1] - qo_ptr[it.b];
+                const int kv_len = req_kv[it.b];
+                const int nA = tile_nkv(it.t0, 0, TQ, qo_len, kv_len);
+                const int nB = tile_nkv(it.t0, 1, TQ, qo_len, kv_len);
+                const int n = it.nkv;
                 ok = wait_or_abort(bar(kF8 ? L::bQFull : L::bQReady), qphase, flag_addr, p.status);
                 qphase ^= 1u;
                 if (!ok) break;
                 tc_fence_after();
-                for (int j = 0; j < tl.nkv && ok; ++j) {
-                    const int nk = kF8 ? L::NKR : L::NK16;
-                    const int kfull = kF8 ? L::bKrFull : L::bK16Full;
-                    const int kempty = kF8 ? L::bKrEmpty : L::bK16Empty;
-                    const int sb = (int)(G & 1);
-                    ok = wait_or_abort(bar(kfull + kring.idx), kring.phase, flag_addr, p.status) &&
-                         wait_or_abort(bar(L::bSEmpty + sb), (uint32_t)((G >> 1) & 1) ^ 1u, flag_addr,
-                                       p.status);
+                // K tile 0 for both query tiles.
+                ok = wait_or_abort(bar(kfull + kring.idx), kring.phase, flag_addr, p.status);
+                if (!ok) break;
+                tc_fence_after();
+                if (nA > 0) qk(0);
+                if (nB > 0) qk(1);
+                tc_commit(bar(kempty + kring.idx));
+                kring.next(nk);
+                if (n == 1) tc_commit(bar(L::bQEmpty));
+                for (int j = 0; j < n && ok; ++j) {
+                    ok = wait_or_abort(bar(L::bV16Full + v16.idx), v16.phase, flag_addr, p.status);
                     if (!ok) break;
                     tc_fence_after();
-                    const uint32_t dS = tmem + kColS + 128u * sb;
-                    if (kF8) {
-                        const uint32_t kt = base + L::kr + kring.idx * kRawTile;
-#pragma unroll
-                        for (int ks = 0; ks < 4; ++ks)
-                            tc_mma_f8_ss(dS, sw128_kmajor_desc(base + L::q + ks * 32),
-                                         sw128_kmajor_desc(kt + ks * 32), idesc_qk, ks > 0 ? 1u : 0u);
-                    } else {
-                        const uint32_t kt = base + L::k16 + kring.idx * kF16Tile;
-#pragma unroll
-                        for (int ks = 0; ks < 8; ++ks) {
-                            const uint32_t off = (ks >> 2) * kHalfTile + (ks & 3) * 32;
-                            tc_mma_f16_ss(dS, sw128_kmajor_desc(base + L::q + off),
-                                          sw128_kmajor_desc(kt + off), idesc_qk, ks > 0 ? 1u : 0u);
-                        }
+                    if (j < nA) {
+                        if (!(ok = pv(0, j > 0))) break;
+                        if (j == nA - 1) tc_commit(bar(L::bOFull + 0));
                     }
-                    tc_commit(bar(L::bSFull + sb));
-                    tc_commit(bar(kempty + kring.idx));
-                    if (j == tl.nkv - 1) tc_commit(bar(L::bQEmpty));
-                    kring.next(nk);
-                    ++G;
-                    if (j >= 1) ok = issue_pv(j - 1);
+                    const bool more = j + 1 < n;
+                    if (more) {
+                        ok = wait_or_abort(bar(kfull + kring.idx), kring.phase, flag_addr, p.status);
+                        if (!ok) break;
+                        tc_fence_after();
+                        if (j + 1 < nA) qk(0);
+                    }
+                    if (j < nB) {
+                        if (!(ok = pv(1, j > 0))) break;
+                        if (j == nB - 1) tc_commit(bar(L::bOFull + 1));
+                    }
+                    tc_commit(bar(L::bV16Empty + v16.idx));
+                    v16.next(L::NV16);
+                    if (more) {
+                        if (j + 1 < nB) qk(1);
+                        tc_commit(bar(kempty + kring.idx));
+                        kring.next(nk);
+                        if (j + 1 == n - 1) tc_commit(bar(L::bQEmpty));
+                    }
                 }
-                if (ok) ok = issue_pv(tl.nkv - 1);
+                nonempty[0] += nA > 0;
+                nonempty[1] += nB > 0;
             }
-            // Drain: wait until every MMA issued above has completed.
-            if (G > 0) mbar_wait(bar(L::bPEmpty), pvphase ^ 1u);
+            // Drain: every MMA issued above completes before TMEM is freed.
+            if (issued_any > 0) {
+                tc_commit(bar(L::bDrain));
+                mbar_wait(bar(L::bDrain), 0);
+            }
         }
         __syncwarp();
     } else if (warp < 4) {
         // ---------------------------------------------------------- dequant
-        const int tid = threadIdx.x;  // 0..127
         const int wd = warp, q8 = lane >> 3, e = lane & 7;
         Ring kr, vr, k16, v16;
         bool ok = true;
-        for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
-            const Tile tl = load_tile(meta, t);
-            const int kv_len = req_kv[tl.b];
-            for (int j = 0; j < tl.nkv && ok; ++j) {
+        for (int t = blockIdx.x; t < n_items && ok; t += gridDim.x) {
+            const Item it = load_item(meta, t);
+            const int kv_len = req_kv[it.b];
+            for (int j = 0; j < it.nkv && ok; ++j) {
                 const int valid = min(kTileKeys, kv_len - j * kTileKeys);
                 if (!kF8) {
                     ok = wait_or_abort(bar(L::bKrFull + kr.idx), kr.phase, flag_addr, p.status) &&
@@ -349,8 +437,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t src = base + L::kr + kr.idx * kRawTile;
                     const uint32_t dst = base + L::k16 + k16.idx * kF16Tile;
 #pragma unroll 2
-                    for (int it = 0; it < 8; ++it) {
-                        const int combo = wd * 8 + it;
+                    for (int i = 0; i < 8; ++i) {
+                        const int combo = wd * 8 + i;
                         const int row = (combo >> 1) * 8 + e;
                         const int c = (combo & 1) * 4 + q8;
                         const uint4 w = lds128(src + row * 128 + ((c ^ e) << 4));
@@ -416,22 +504,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                 v16.next(L::NV16);
             }
         }
-        (void)tid;
     } else {
         // ---------------------------------------------------------- softmax
-        const int r = threadIdx.x - 128;  // TMEM lane = query row of the tile
+        const int x = warp < 8 ? 0 : 1;        // query tile A or B
+        const int r = threadIdx.x - 128 * (1 + x);  // row of the tile = TMEM lane
         const uint32_t lane_base = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
-        uint32_t qphase = 0, pphase = 0;
-        long long G = 0;
+        const uint32_t tS = lane_base + col_s(x), tO = lane_base + col_o(x);
+        uint32_t qphase = 0, sphase = 0, ophase = 0;
         bool ok = true;
-        for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
-            const Tile tl = load_tile(meta, t);
-            const int qo0 = qo_ptr[tl.b];
-            const int qo_len = qo_ptr[tl.b + 1] - qo0;
-            const int kv_len = req_kv[tl.b];
+        for (int t = blockIdx.x; t < n_items && ok; t += gridDim.x) {
+            const Item it = load_item(meta, t);
+            const int qo0 = qo_ptr[it.b];
+            const int qo_len = qo_ptr[it.b + 1] - qo0;
+            const int kv_len = req_kv[it.b];
+            const int t0 = it.t0 + x * TQ;
+            const int nX = tile_nkv(it.t0, x, TQ, qo_len, kv_len);
             const int tok = r / g, hh = r - tok * g;
-            const bool valid_row = (tok < TQ) && (tl.t0 + tok < qo_len);
-            const int limit = valid_row ? tl.t0 + tok + kv_len - qo_len : -1;
+            const bool valid_row = (tok < TQ) && (t0 + tok < qo_len);
+            const int limit = valid_row ? t0 + tok + kv_len - qo_len : -1;
             float scale = p.sm_scale_log2;
             if (!kF8) {
                 ok = wait_or_abort(bar(L::bQFull), qphase, flag_addr, p.status);
@@ -439,11 +529,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!ok) break;
                 if (p.q_dtype == PAFP8_BF16 && r < TQ * g) {
                     // Bring the row into f16 range by an exact power of two.
+                    const uint32_t qrow = base + L::q + x * L::kQTile + r * 128;
                     uint32_t mx = 0;
 #pragma unroll
                     for (int c = 0; c < 16; ++c) {
-                        const uint4 w = lds128(base + L::q + (c >> 3) * kHalfTile + r * 128 +
-                                               (((c & 7) ^ (r & 7)) << 4));
+                        const uint4 w = lds128(qrow + (c >> 3) * kHalfTile + (((c & 7) ^ (r & 7)) << 4));
                         const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
                         for (int k = 0; k < 4; ++k) {
@@ -455,10 +545,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int shift = ex > 14 ? ex - 14 : 0;
                     const float down = __int_as_float((127 - shift) << 23);
                     scale *= __int_as_float((127 + shift) << 23);
-#pragma unroll
+#pragma unroll 4
                     for (int c = 0; c < 16; ++c) {
-                        const uint32_t a = base + L::q + (c >> 3) * kHalfTile + r * 128 +
-                                           (((c & 7) ^ (r & 7)) << 4);
+                        const uint32_t a = qrow + (c >> 3) * kHalfTile + (((c & 7) ^ (r & 7)) << 4);
                         const uint4 w = lds128(a);
                         const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
                         uint32_t o4[4];
@@ -472,30 +561,31 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 mbar_arrive(bar(L::bQReady));
             }
-            float m = -INFINITY, l = 0.f;
-            for (int j = 0; j < tl.nkv && ok; ++j) {
-                const int sb = (int)(G & 1);
-                ok = wait_or_abort(bar(L::bSFull + sb), (uint32_t)((G >> 1) & 1), flag_addr, p.status);
+            if (nX == 0) continue;  // tile B past the request's last row
+            float m = -INFINITY, l = 0.f;  // m in scaled (log2) units
+            for (int j = 0; j < nX && ok; ++j) {
+                ok = wait_or_abort(bar(L::bSFull + x), sphase, flag_addr, p.status);
+                sphase ^= 1u;
                 if (!ok) break;
                 tc_fence_after();
-                const uint32_t sS = lane_base + kColS + 128u * sb;
                 const int key0 = j * kTileKeys;
                 const bool need_mask = key0 + kTileKeys - 1 > limit;
-                // pass 1: row max
+                // pass 1: row max of the raw logits (scale > 0)
                 float mx = -INFINITY;
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t v[32];
-                    tc_ld32(sS + 32 * c, v);
+                for (int h = 0; h < 2; ++h) {
+                    uint32_t v[64];
+                    tc_ld32(tS + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(v));
+                    tc_ld32(tS + 64 * h + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
                     tc_wait_ld();
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        float x = __uint_as_float(v[i]) * scale;
-                        if (need_mask && key0 + 32 * c + i > limit) x = -INFINITY;
-                        mx = fmaxf(mx, x);
+                    for (int i = 0; i < 64; ++i) {
+                        float s = __uint_as_float(v[i]);
+                        if (need_mask && key0 + 64 * h + i > limit) s = -INFINITY;
+                        mx = fmaxf(mx, s);
                     }
                 }
-                const float m_new = fmaxf(m, mx);
+                const float m_new = fmaxf(m, mx * scale);
                 float m_use = m;
                 bool rescale = false;
                 if (j == 0) {
@@ -505,65 +595,60 @@ __global__ void __launch_bounds__(kThreads, 1)
                     rescale = true;
                 }
                 if (m_use == -INFINITY) m_use = 0.f;  // row with no admissible key so far
-                // P must not be overwritten before the previous P.V has completed.
-                if (j >= 1) {
-                    ok = wait_or_abort(bar(L::bPEmpty), pphase, flag_addr, p.status);
-                    pphase ^= 1u;
-                    if (!ok) break;
-                    tc_fence_after();
-                }
                 if (rescale) {
+                    // O_X += P V of the previous KV tile has completed (in-order
+                    // tensor pipe, S of this tile was written after it).
                     const float alpha = ex2(m - m_use);
                     l *= alpha;
-#pragma unroll
+#pragma unroll 1
                     for (int c = 0; c < 4; ++c) {
                         uint32_t v[32];
-                        tc_ld32(lane_base + kColO + 32 * c, v);
+                        tc_ld32(tO + 32 * c, v);
                         tc_wait_ld();
 #pragma unroll
                         for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
-                        tc_st32(lane_base + kColO + 32 * c, v);
+                        tc_st32(tO + 32 * c, v);
                     }
                     tc_wait_st();
                 }
-                // pass 2: P = exp2(x - m), row sum, P -> TMEM as f16
+                // pass 2: P = exp2(s * scale - m), row sum, P -> TMEM (f16, over S)
+                const float negm = -m_use;
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t v[32];
-                    tc_ld32(sS + 32 * c, v);
+                for (int h = 0; h < 2; ++h) {
+                    uint32_t v[64];
+                    tc_ld32(tS + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(v));
+                    tc_ld32(tS + 64 * h + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
                     tc_wait_ld();
-                    uint32_t pk[16];
+                    uint32_t pk[32];
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        float x0 = __uint_as_float(v[2 * i]) * scale;
-                        float x1 = __uint_as_float(v[2 * i + 1]) * scale;
-                        if (need_mask && key0 + 32 * c + 2 * i > limit) x0 = -INFINITY;
-                        if (need_mask && key0 + 32 * c + 2 * i + 1 > limit) x1 = -INFINITY;
-                        const float e0 = ex2(x0 - m_use), e1 = ex2(x1 - m_use);
+                    for (int i = 0; i < 32; ++i) {
+                        float x0 = fmaf(__uint_as_float(v[2 * i]), scale, negm);
+                        float x1 = fmaf(__uint_as_float(v[2 * i + 1]), scale, negm);
+                        if (need_mask && key0 + 64 * h + 2 * i > limit) x0 = -INFINITY;
+                        if (need_mask && key0 + 64 * h + 2 * i + 1 > limit) x1 = -INFINITY;
+                        const float e0 = ex2(x0), e1 = ex2(x1);
                         l += e0 + e1;
                         pk[i] = pack_half2(e0, e1);
                     }
-                    tc_st16(lane_base + kColP + 16 * c, pk);
+                    tc_st32(tS + 32 * h, pk);
                 }
                 tc_wait_st();
                 tc_fence_before();
-                mbar_arrive(bar(L::bSEmpty + sb));
-                mbar_arrive(bar(L::bPFull));
+                mbar_arrive(bar(L::bPFull + x));
                 m = m_use;
-                ++G;
             }
             if (!ok) break;
-            // epilogue: the tile's last P.V must have completed.
-            ok = wait_or_abort(bar(L::bPEmpty), pphase, flag_addr, p.status);
-            pphase ^= 1u;
+            // epilogue: the tile's last O update must have completed.
+            ok = wait_or_abort(bar(L::bOFull + x), ophase, flag_addr, p.status);
+            ophase ^= 1u;
             if (!ok) break;
             tc_fence_after();
             const float inv = valid_row && l > 0.f ? p.v_scale / l : 0.f;
-            const size_t orow = (size_t)(qo0 + tl.t0 + tok) * p.num_qo_heads + (size_t)tl.hk * g + hh;
-#pragma unroll
+            const size_t orow = (size_t)(qo0 + t0 + tok) * p.num_qo_heads + (size_t)it.hk * g + hh;
+#pragma unroll 1
             for (int c = 0; c < 4; ++c) {
                 uint32_t v[32];
-                tc_ld32(lane_base + kColO + 32 * c, v);
+                tc_ld32(tO + 32 * c, v);
                 tc_wait_ld();
                 if (valid_row) {
                     uint32_t w[16];
@@ -578,12 +663,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (valid_row && p.lse != nullptr) p.lse[orow] = (m + __log2f(l)) * 0.69314718055994531f;
             tc_fence_before();
+            mbar_arrive(bar(L::bOEmpty + x));
         }
     }
 
     tc_fence_before();
     __syncthreads();
-    if (warp == 9) {
+    if (warp == 13) {
         tc_fence_after();
         tc_dealloc(tmem, kTmemCols);
     }

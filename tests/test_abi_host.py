@@ -267,7 +267,7 @@ def test_prefill_tiles_cover_every_row_head_once(case):
     seen = set()
     for b, hk, t0, nkv in tiles:
         qo, kv = case["qo_lens"][b], case["kv_lens"][b]
-        for tok in range(t0, min(t0 + tq, qo)):
+        for tok in range(t0, min(t0 + 2 * tq, qo)):  # two query tiles per item
             for h in range(hk * g, hk * g + g):
                 assert (b, tok, h) not in seen
                 seen.add((b, tok, h))
