@@ -18,7 +18,9 @@
 // pages).  Persistent CTAs take items i, i + grid, ... from a longest-first
 // list built by the plan.
 //
-// Roles (448 threads):
+// Roles (512 threads, four warpgroups; registers are moved by setmaxnreg from
+// the dequant warpgroup (104) and the producer/MMA warpgroup (56) to the two
+// softmax warpgroups (168)):
 //   warps 0-3   dequant: raw fp8 K -> f16 K tile (2-byte query path); raw fp8
 //               V -> f16 V^T tile (both paths), zero beyond the request's keys;
 //   warps 4-7   softmax of tile A, warps 8-11 softmax of tile B: thread r owns
@@ -29,7 +31,7 @@
 //               With a bf16 query each thread first brings its Q row into f16
 //               range by an exact power of two and converts it in place;
 //   warp 12     TMA producer: both Q tiles, K and V pages (one box per page);
-//   warp 13     MMA issuer and TMEM owner.  Per KV tile j:
+//   warp 13     MMA issuer and TMEM owner (warps 14-15 idle).  Per KV tile j:
 //                 S_A = Q_A K_j^T, S_B = Q_B K_j^T    (kind::f16 or kind::f8f6f4)
 //                 O_A += P_A V_j,  O_B += P_B V_j      (kind::f16, A = P from TMEM)
 //               issued as ... PV_A(j), QK_A(j+1), PV_B(j), QK_B(j+1) ... so
@@ -54,7 +56,7 @@ namespace {
 using namespace ptx;
 
 constexpr int D = kHeadDim;
-constexpr int kThreads = 448;
+constexpr int kThreads = 512;  // four warpgroups; warps 14-15 only lend registers
 constexpr uint32_t kTmemCols = 512;
 __device__ __forceinline__ uint32_t col_s(int x) { return 128u * (uint32_t)x; }        // S_X / P_X
 __device__ __forceinline__ uint32_t col_o(int x) { return 256u + 128u * (uint32_t)x; }  // O_X
@@ -205,8 +207,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     uint32_t tmem;
     asm volatile("ld.shared.u32 %0, [%1];" : "=r"(tmem) : "r"(base + L::tmem_slot) : "memory");
+    // Registers per thread: launched at 128; each warpgroup's branch below
+    // starts by resizing: softmax 168, dequant 96, producer/MMA 80
+    // (4 x 32 x (96 + 2 x 168 + 80) = 65,536, what the block launched with).
 
-    if (warp == 12) {
+    if (warp >= 12) {
+      asm volatile("setmaxnreg.dec.sync.aligned.u32 80;" ::: "memory");
+      if (warp == 12) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
             prefetch_tmap(&tmq);
@@ -303,7 +310,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int s = 0; s < L::NVR && s < issued_v; ++s)
                 mbar_wait(bar(L::bVrFull + s), (uint32_t)(((issued_v - 1 - s) / L::NVR) & 1));
         }
-    } else if (warp == 13) {
+      } else if (warp == 13) {
         // ------------------------------------------------------------- MMA
         if (lane == 0) {
             const uint32_t idesc_qk =
@@ -420,7 +427,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         __syncwarp();
+      }
     } else if (warp < 4) {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 96;" ::: "memory");
         // ---------------------------------------------------------- dequant
         const int wd = warp, q8 = lane >> 3, e = lane & 7;
         Ring kr, vr, k16, v16;
@@ -505,6 +514,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
     } else {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 168;" ::: "memory");
         // ---------------------------------------------------------- softmax
         const int x = warp < 8 ? 0 : 1;        // query tile A or B
         const int r = threadIdx.x - 128 * (1 + x);  // row of the tile = TMEM lane
@@ -570,21 +580,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 const int key0 = j * kTileKeys;
                 const bool need_mask = key0 + kTileKeys - 1 > limit;
-                // pass 1: row max of the raw logits (scale > 0)
-                float mx = -INFINITY;
+                // The whole S row (128 columns) in registers, one wait.
+                uint32_t v[128];
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    uint32_t v[64];
-                    tc_ld32(tS + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(v));
-                    tc_ld32(tS + 64 * h + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
-                    tc_wait_ld();
+                for (int c = 0; c < 4; ++c) tc_ld32(tS + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(v + 32 * c));
+                tc_wait_ld();
+                // row max of the raw logits (scale > 0); masked logits -> -inf.
+                // Eight independent partial maxima keep the chain short.
+                if (need_mask) {
+                    const int lim = limit - key0;
 #pragma unroll
-                    for (int i = 0; i < 64; ++i) {
-                        float s = __uint_as_float(v[i]);
-                        if (need_mask && key0 + 64 * h + i > limit) s = -INFINITY;
-                        mx = fmaxf(mx, s);
-                    }
+                    for (int i = 0; i < 128; ++i)
+                        if (i > lim) v[i] = __float_as_uint(-INFINITY);
                 }
+                float pm[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) pm[k] = __uint_as_float(v[k]);
+#pragma unroll
+                for (int i = 8; i < 128; ++i) pm[i & 7] = fmaxf(pm[i & 7], __uint_as_float(v[i]));
+                const float mx = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
+                                       fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
                 const float m_new = fmaxf(m, mx * scale);
                 float m_use = m;
                 bool rescale = false;
@@ -611,27 +626,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     tc_wait_st();
                 }
-                // pass 2: P = exp2(s * scale - m), row sum, P -> TMEM (f16, over S)
+                // P = exp2(s * scale - m) (masked logits are -inf: P = 0), row
+                // sum, P -> TMEM as f16 over the first half of S.
                 const float negm = -m_use;
+                // P overwrites the S values it consumed: P of columns 2i, 2i+1
+                // goes to v[i], which held column i (already used).  Four
+                // independent partial sums keep the chain short.
+                float ps[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    uint32_t v[64];
-                    tc_ld32(tS + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(v));
-                    tc_ld32(tS + 64 * h + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
-                    tc_wait_ld();
-                    uint32_t pk[32];
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        float x0 = fmaf(__uint_as_float(v[2 * i]), scale, negm);
-                        float x1 = fmaf(__uint_as_float(v[2 * i + 1]), scale, negm);
-                        if (need_mask && key0 + 64 * h + 2 * i > limit) x0 = -INFINITY;
-                        if (need_mask && key0 + 64 * h + 2 * i + 1 > limit) x1 = -INFINITY;
-                        const float e0 = ex2(x0), e1 = ex2(x1);
-                        l += e0 + e1;
-                        pk[i] = pack_half2(e0, e1);
-                    }
-                    tc_st32(tS + 32 * h, pk);
+                for (int i = 0; i < 64; ++i) {
+                    const float e0 = ex2(fmaf(__uint_as_float(v[2 * i]), scale, negm));
+                    const float e1 = ex2(fmaf(__uint_as_float(v[2 * i + 1]), scale, negm));
+                    ps[i & 3] += e0 + e1;
+                    v[i] = pack_half2(e0, e1);
                 }
+                l += (ps[0] + ps[1]) + (ps[2] + ps[3]);
+                tc_st32(tS, *reinterpret_cast<uint32_t(*)[32]>(v));
+                tc_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
                 tc_wait_st();
                 tc_fence_before();
                 mbar_arrive(bar(L::bPFull + x));
