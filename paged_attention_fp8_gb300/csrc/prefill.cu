@@ -66,9 +66,12 @@ constexpr uint32_t kF16Tile = 2 * kHalfTile;       // 32 KB of f16
 
 template <bool kF8>
 struct Layout {
-    static constexpr int NKR = kF8 ? 4 : 2;    // raw K stages
-    static constexpr int NVR = 2;              // raw V stages
-    static constexpr int NK16 = kF8 ? 0 : 1;   // f16 K stages
+    // The 2-byte-query path spends its shared memory on two f16 K tiles (the
+    // dequant of K_{j+1} may start while QK_B(j) still reads K_j) and keeps a
+    // single raw fp8 stage per tensor; the fp8 path multiplies raw K directly.
+    static constexpr int NKR = kF8 ? 4 : 1;    // raw K stages
+    static constexpr int NVR = kF8 ? 2 : 1;    // raw V stages
+    static constexpr int NK16 = kF8 ? 0 : 2;   // f16 K stages
     static constexpr int NV16 = 2;             // f16 V^T stages
     static constexpr uint32_t kQTile = kF8 ? kHalfTile : kF16Tile;
     static constexpr uint32_t q = 0;                     // Q_A, then Q_B
