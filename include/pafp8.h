@@ -139,8 +139,7 @@ pafp8_status pafp8_plan_create(const pafp8_plan_desc *desc, const int32_t *kv_in
 void pafp8_plan_destroy(pafp8_plan *plan);
 
 /* Bytes of device workspace pafp8_run needs for this plan: the uploaded
- * partition metadata, the split-KV partial states, one merge counter per
- * (request, KV head) and a status word. */
+ * partition metadata, the split-KV partial states and a status word. */
 size_t pafp8_workspace_bytes(const pafp8_plan *plan);
 
 /* Read-only host view of the plan's partition metadata, the exact int32 words
@@ -149,8 +148,7 @@ size_t pafp8_workspace_bytes(const pafp8_plan *plan);
 pafp8_status pafp8_plan_metadata(const pafp8_plan *plan, const int32_t **words, size_t *count);
 
 /* Copy the plan's metadata into the head of `workspace` (device memory of at
- * least pafp8_workspace_bytes) on `stream` and clear its merge counters and
- * status word (kernels leave the counters at zero after every run).  Must
+ * least pafp8_workspace_bytes) on `stream` and clear its status word.  Must
  * precede pafp8_run with this workspace; the plan records the workspace
  * address and pafp8_run refuses any other. */
 pafp8_status pafp8_plan_upload(pafp8_plan *plan, void *workspace, size_t workspace_bytes,
@@ -186,11 +184,12 @@ pafp8_status pafp8_run(const pafp8_plan *plan, int32_t q_dtype, const void *q,
 /* pafp8_run restricted to one stage of the launch sequence, for callers that
  * time or overlap the stages separately:
  *   stage 0  everything (same as pafp8_run);
- *   stage 1  the attention kernel, which for decode also merges the partial
- *            states of split requests (fused; it is decode's only launch);
- *   stage 2  work after the attention kernel: none in this build (decode's
- *            merge is fused into stage 1, prefill has no split), so stage 2
- *            launches nothing and returns PAFP8_OK after the checks.
+ *   stage 1  the attention kernel only (decode: it writes the outputs of
+ *            unsplit requests and of requests with no KV, and the partial
+ *            states of split ones);
+ *   stage 2  the split-KV merge only (decode: combines the partial states
+ *            of split requests; launched as a programmatic dependent of the
+ *            preceding kernel on the stream); prefill has no stage 2.
  * Running stage 1 then stage 2 on one stream equals stage 0.  Arguments and
  * checks are those of pafp8_run. */
 pafp8_status pafp8_run_stage(const pafp8_plan *plan, int32_t stage, int32_t q_dtype, const void *q,

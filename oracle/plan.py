@@ -24,8 +24,7 @@ fixed-split and disable-split options; the balanced rule is this library's):
   (CTA by CTA).
 * Merge rows: rows with two or more segments, ascending; each lists its
   slots ordered by first page.  row_merge[r] is the merge entry of row r, or
-  -1.  The merge is done inside the decode kernel by the warp that finishes
-  a split row's last segment.
+  -1.  A separate merge pass combines each merge row's slots in that order.
 """
 from __future__ import annotations
 

@@ -30,10 +30,11 @@
 //    dims 16g..16g+15), so every shared-memory read is one conflict-free
 //    16-byte load.
 //  * A segment covering its whole request writes o and lse; a partial one
-//    writes (O/l, lse in log2 units) to the workspace, and the warp that
-//    completes the last partial segment of a (request, KV head) merges them
-//    by their log-sum-exp (a counter per (row, head) in the workspace, reset
-//    after use).  A request with no KV writes o = 0, lse = -inf.
+//    writes (O/l, lse in log2 units) to the workspace, and a separate merge
+//    kernel (one block per split row and query head, launched as a
+//    programmatic dependent) combines them by their log-sum-exp.  Folding
+//    the merge into this kernel made the warps that merged stall their
+//    CTA's page ring.  A request with no KV writes o = 0, lse = -inf.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -118,64 +119,6 @@ __device__ __forceinline__ float load_q(uint32_t (&qf)[16], const void* q, int q
     return factor;
 }
 
-// One warp combines the partial states of the `group` query heads of KV head
-// `kvh` (index `hl` within its block) of request b: L = log2 sum 2^lse_c,
-// o = v_scale * sum 2^(lse_c - L) O_c, over slots merge_slot[s0..s1) in page
-// order (running max and rescaled sums, one slot per step).  Lane i handles
-// dims 4i .. 4i+3 of every head.  The partial states were written by other
-// CTAs, so they are read through L2, all loads of a step issued before any
-// is used: the merging warp holds up its CTA's page ring meanwhile.
-__device__ __forceinline__ void merge_head_group(const DecodeParams& p, const int* merge_slot, int s0,
-                                                 int s1, int hpc, int group, int hl, int b, int kvh,
-                                                 int lane) {
-    const int hpb = hpc * group;
-    float Lr[kMaxGroupDecode], Sr[kMaxGroupDecode];
-    float4 Ar[kMaxGroupDecode];
-#pragma unroll
-    for (int n = 0; n < kMaxGroupDecode; ++n) {
-        Lr[n] = -INFINITY;
-        Sr[n] = 0.f;
-        Ar[n] = make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-    for (int s = s0; s < s1; ++s) {
-        const size_t b0 = (size_t)merge_slot[s] * hpb + (size_t)hl * group;
-        float l0[kMaxGroupDecode];
-        float4 v0[kMaxGroupDecode];
-#pragma unroll
-        for (int n = 0; n < kMaxGroupDecode; ++n) {
-            if (n < group) {
-                l0[n] = __ldcg(p.part_lse + b0 + n);
-                v0[n] = __ldcg(reinterpret_cast<const float4*>(p.part_o + (b0 + n) * D) + lane);
-            }
-        }
-#pragma unroll
-        for (int n = 0; n < kMaxGroupDecode; ++n) {
-            if (n < group) {
-                const float mx = fmaxf(Lr[n], l0[n]);
-                const float a = ex2(Lr[n] - mx), w0 = ex2(l0[n] - mx);
-                Sr[n] = Sr[n] * a + w0;
-                Ar[n].x = Ar[n].x * a + w0 * v0[n].x;
-                Ar[n].y = Ar[n].y * a + w0 * v0[n].y;
-                Ar[n].z = Ar[n].z * a + w0 * v0[n].z;
-                Ar[n].w = Ar[n].w * a + w0 * v0[n].w;
-                Lr[n] = mx;
-            }
-        }
-    }
-#pragma unroll
-    for (int n = 0; n < kMaxGroupDecode; ++n) {
-        if (n < group) {
-            const float sc = p.v_scale / Sr[n];
-            const size_t oh = (size_t)b * p.num_qo_heads + (size_t)kvh * group + n;
-            uint2 wv;
-            wv.x = pack_out2(Ar[n].x * sc, Ar[n].y * sc, p.o_dtype);
-            wv.y = pack_out2(Ar[n].z * sc, Ar[n].w * sc, p.o_dtype);
-            *reinterpret_cast<uint2*>(static_cast<uint16_t*>(p.o) + oh * D + 4 * lane) = wv;
-            if (lane == 0 && p.lse != nullptr) p.lse[oh] = (Lr[n] + __log2f(Sr[n])) * 0.69314718055994531f;
-        }
-    }
-}
-
 template <int KT>
 __global__ void __launch_bounds__(32 * 9, 1)
     decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtensorMap tmk,
@@ -196,15 +139,13 @@ __global__ void __launch_bounds__(32 * 9, 1)
     const int* cta_seg = meta + meta[kMetaOffCtaSeg];
     const int* segs = meta + meta[kMetaOffSeg];
     const int seg_begin = cta_seg[blockIdx.x], seg_end = cta_seg[blockIdx.x + 1];
-    const int* merge_ptr = meta + meta[kMetaOffMergePtr];
-    const int* merge_slot = meta + meta[kMetaOffMergeSlot];
-    const int* row_merge = meta + meta[kMetaOffRowMerge];
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < stages; ++s) {
             mbar_init(bar_full + 8u * s, 1);
             mbar_init(bar_empty + 8u * s, 32u * hpc);
         }
+
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
@@ -444,24 +385,62 @@ __global__ void __launch_bounds__(32 * 9, 1)
                 if (g == 0) p.part_lse[(size_t)slot * hpb + warp * group + n] = m + __log2f(l);
             }
         }
-        if (slot >= 0) {
-            // The warp that completes the last partial segment of this
-            // (row, KV head) combines every partial state of it.
-            __threadfence();
-            __syncwarp();
-            int done = 0;
-            if (lane == 0) done = atomicAdd(p.counters + (size_t)row * hpc + warp, 1);
-            done = __shfl_sync(0xFFFFFFFFu, done, 0);
-            const int e = row_merge[row];
-            const int s0 = merge_ptr[e], s1 = merge_ptr[e + 1];
-            if (done == s1 - s0 - 1) {
-                __threadfence();
-                merge_head_group(p, merge_slot, s0, s1, hpc, group, warp, b, kvh, lane);
-                if (lane == 0) p.counters[(size_t)row * hpc + warp] = 0;
-            }
-        }
     }
     if (!ok && lane == 0) flag(p.status, kStatusTimeout);
+}
+
+// Combine the partial states of each split (request, KV-head block) row.
+// Block = one (merge entry, query head of the block); thread = one of the 128
+// dims.  Over the row's slots (page order) it keeps a running max of the
+// log2-domain lse_c and the rescaled sums of 2^lse_c and 2^lse_c O_c, four
+// slots' loads in flight per step, then writes o = v_scale * sum / sum and
+// lse = ln(sum) + max.  Launched as a programmatic dependent of the decode
+// kernel: griddepcontrol.wait returns once that grid has completed and its
+// writes are visible.
+__global__ void __launch_bounds__(128)
+    merge_kernel(const __grid_constant__ DecodeParams p, int hpc, int group) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int* meta = p.meta;
+    const int nhb = meta[kMetaHeadBlocks];
+    const int* mptr = meta + meta[kMetaOffMergePtr];
+    const int* mrow = meta + meta[kMetaOffMergeRow];
+    const int* mslot = meta + meta[kMetaOffMergeSlot];
+    const int hpb = hpc * group;
+    const int e = blockIdx.x / hpb, hh = blockIdx.x - e * hpb, d = threadIdx.x;
+    const int row = mrow[e];
+    const int b = row / nhb, hb = row - b * nhb;
+    const int s0 = mptr[e], s1 = mptr[e + 1];
+    float m = -INFINITY, sum = 0.f, acc = 0.f;
+    for (int s = s0; s < s1; s += 4) {
+        float l[4], o[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const bool in = s + k < s1;
+            const size_t idx = (size_t)mslot[in ? s + k : s0] * hpb + hh;
+            l[k] = in ? __ldcg(p.part_lse + idx) : -INFINITY;
+            o[k] = in ? __ldcg(p.part_o + idx * D + d) : 0.f;
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float mn = fmaxf(m, l[k]);
+            const float a = ex2(m - mn), w = ex2(l[k] - mn);
+            sum = sum * a + w;
+            acc = acc * a + w * o[k];
+            m = mn;
+        }
+    }
+    const int head = hb * hpb + hh;  // query head: (hb * hpc + hh / group) * group + hh % group
+    const size_t oh = (size_t)b * p.num_qo_heads + head;
+    const float val = acc / sum * p.v_scale;
+    uint16_t* dst = static_cast<uint16_t*>(p.o) + oh * D + d;
+    if (p.o_dtype == PAFP8_BF16) {
+        __nv_bfloat16 h = __float2bfloat16_rn(val);
+        *dst = *reinterpret_cast<uint16_t*>(&h);
+    } else {
+        __half h = __float2half_rn(val);
+        *dst = *reinterpret_cast<uint16_t*>(&h);
+    }
+    if (d == 0 && p.lse != nullptr) p.lse[oh] = (m + __log2f(sum)) * 0.69314718055994531f;
 }
 
 }  // namespace
@@ -519,5 +498,18 @@ cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& tmap_k, cons
     return cudaGetLastError();
 }
 
+cudaError_t launch_merge(const DecodeParams& p, int num_merge, int hpc, int group, cudaStream_t stream) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(num_merge * hpc * group);
+    cfg.blockDim = dim3(128);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, merge_kernel, p, hpc, group);
+}
 
 }  // namespace pafp8

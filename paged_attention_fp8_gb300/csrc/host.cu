@@ -115,8 +115,7 @@ struct pafp8_plan {
     int64_t nnz_pages = 0, nnz_qo = 0;
     int heads_per_cta = 1, head_blocks = 1, group = 1;
     int num_ctas = 0, num_partials = 0, num_merge = 0;
-    size_t meta_bytes = 0, part_o_off = 0, part_lse_off = 0, counters_off = 0, status_off = 0,
-           ws_bytes = 0;
+    size_t meta_bytes = 0, part_o_off = 0, part_lse_off = 0, status_off = 0, ws_bytes = 0;
     void* uploaded_ws = nullptr;
 };
 
@@ -137,8 +136,8 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 // dealt round-robin after the other segments, and each CTA runs its partial
 // segments first.  A segment spanning its whole row writes the final output
 // (slot -1); every other segment writes a partial state to the next free slot
-// (in final segment order), and the warp that completes a split row's last
-// segment merges its partial states by their log-sum-exp.
+// (in final segment order); a merge kernel combines the partial states of
+// every row with two or more segments.
 void build_decode_meta(pafp8_plan* pl) {
     const int B = pl->desc.batch;
     const int nhb = pl->head_blocks;
@@ -339,11 +338,7 @@ void layout_workspace(pafp8_plan* pl) {
     pl->meta_bytes = align_up(pl->meta.size() * sizeof(int32_t), 256);
     pl->part_o_off = pl->meta_bytes;
     pl->part_lse_off = align_up(pl->part_o_off + (size_t)pl->num_partials * heads * kHeadDim * 4, 256);
-    pl->counters_off = align_up(pl->part_lse_off + (size_t)pl->num_partials * heads * 4, 256);
-    const size_t rows = pl->desc.mode == PAFP8_MODE_DECODE
-                            ? (size_t)pl->desc.batch * pl->head_blocks * pl->heads_per_cta
-                            : 0;
-    pl->status_off = align_up(pl->counters_off + rows * 4, 256);
+    pl->status_off = align_up(pl->part_lse_off + (size_t)pl->num_partials * heads * 4, 256);
     pl->ws_bytes = pl->status_off + 256;
 }
 
@@ -599,8 +594,7 @@ pafp8_status pafp8_plan_upload(pafp8_plan* plan, void* workspace, size_t workspa
     cudaError_t e = cudaMemcpyAsync(workspace, plan->meta.data(), plan->meta.size() * 4,
                                     cudaMemcpyHostToDevice, s);
     if (e == cudaSuccess)
-        e = cudaMemsetAsync((char*)workspace + plan->counters_off, 0,
-                            plan->status_off + 256 - plan->counters_off, s);
+        e = cudaMemsetAsync((char*)workspace + plan->status_off, 0, 256, s);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return fail(PAFP8_ERR_CUDA, "metadata upload failed: %s", cudaGetErrorString(e));
@@ -711,7 +705,6 @@ pafp8_status pafp8_run_stage(const pafp8_plan* plan, int32_t stage, int32_t q_dt
     p.meta = (const int32_t*)ws;
     p.part_o = (float*)(ws + plan->part_o_off);
     p.part_lse = (float*)(ws + plan->part_lse_off);
-    p.counters = (int*)(ws + plan->counters_off);
     p.status = (uint32_t*)(ws + plan->status_off);
     p.q_dtype = q_dtype;
     p.kv_dtype = k_dtype;
@@ -723,7 +716,7 @@ pafp8_status pafp8_run_stage(const pafp8_plan* plan, int32_t stage, int32_t q_dt
     p.v_scale = v_scale;
 
     cudaError_t e = cudaSuccess;
-    if (stage != 2 && plan->num_ctas > 0) {  // decode has one launch: merges are fused
+    if (stage != 2 && plan->num_ctas > 0) {
         CUtensorMap tk, tv;
         int hpb = 1;
         if ((st = encode_decode_maps(&tk, &tv, k_cache, v_cache, d.num_pages, d.num_kv_heads,
@@ -731,6 +724,8 @@ pafp8_status pafp8_run_stage(const pafp8_plan* plan, int32_t stage, int32_t q_dt
             return st;
         e = launch_decode(p, tk, tv, plan->num_ctas, plan->heads_per_cta, plan->group, hpb, s);
     }
+    if (e == cudaSuccess && stage != 1 && plan->num_merge > 0)
+        e = launch_merge(p, plan->num_merge, plan->heads_per_cta, plan->group, s);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return fail(PAFP8_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(e));
@@ -816,8 +811,7 @@ pafp8_status pafp8_run_decode_noalloc(const pafp8_plan* plan, int32_t q_dtype, c
     // The scratch keeps the previous call's bytes: load this plan's metadata
     // and clear the status word; partial states are written before read.
     e = cudaMemcpyAsync(ws, plan->meta.data(), plan->meta.size() * 4, cudaMemcpyHostToDevice, s);
-    if (e == cudaSuccess)
-        e = cudaMemsetAsync(ws + plan->counters_off, 0, plan->status_off + 256 - plan->counters_off, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(ws + plan->status_off, 0, 256, s);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return fail(PAFP8_ERR_CUDA, "loading the plan into the built-in scratch failed: %s",
@@ -831,7 +825,6 @@ pafp8_status pafp8_run_decode_noalloc(const pafp8_plan* plan, int32_t q_dtype, c
     p.meta = (const int32_t*)ws;
     p.part_o = (float*)(ws + plan->part_o_off);
     p.part_lse = (float*)(ws + plan->part_lse_off);
-    p.counters = (int*)(ws + plan->counters_off);
     p.status = (uint32_t*)(ws + plan->status_off);
     p.q_dtype = q_dtype;
     p.kv_dtype = k_dtype;
@@ -850,6 +843,8 @@ pafp8_status pafp8_run_decode_noalloc(const pafp8_plan* plan, int32_t q_dtype, c
             return st;
         e = launch_decode(p, tk, tv, plan->num_ctas, plan->heads_per_cta, plan->group, hpb, s);
     }
+    if (e == cudaSuccess && plan->num_merge > 0)
+        e = launch_merge(p, plan->num_merge, plan->heads_per_cta, plan->group, s);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return fail(PAFP8_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(e));

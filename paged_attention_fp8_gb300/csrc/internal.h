@@ -61,7 +61,6 @@ struct DecodeParams {
     const int32_t* meta;     // device copy of the metadata words
     float* part_o;           // [num_partials, hpc*group, D]
     float* part_lse;         // [num_partials, hpc*group] (log2 domain)
-    int* counters;           // [rows * hpc] finished partial segments per (row, head)
     uint32_t* status;
     int q_dtype, kv_dtype, o_dtype;
     int num_qo_heads, num_kv_heads, num_pages;
@@ -98,6 +97,8 @@ constexpr int kMaxDevices = 64;
 // once per device; decode.cu).
 cudaError_t noalloc_scratch(void** ptr);
 
+cudaError_t launch_merge(const DecodeParams& p, int num_merge, int heads_per_cta, int group,
+                         cudaStream_t stream);
 cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& tmap_q,
                            const CUtensorMap& tmap_k, const CUtensorMap& tmap_v, int num_ctas,
                            cudaStream_t stream);

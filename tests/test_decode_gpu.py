@@ -173,10 +173,10 @@ def test_long_context_workload_sampled(cuda_device):
     assert np.all(np.isfinite(o)) and np.all(np.isfinite(lse))
 
 
-def test_fused_merge_many_partials_and_repeat_runs(cuda_device):
+def test_merge_many_partials_and_repeat_runs(cuda_device):
     """One-page splits give up to 256 partial states per (request, KV head),
-    merged inside the decode kernel; running the same plan again (merge
-    counters reset by the kernel) gives bit-identical results."""
+    combined by the merge kernel; running the same plan again gives
+    bit-identical results."""
     b = make_batch([4096, 1, 700, 0, 33], num_qo_heads=32, num_kv_heads=8, seed=41)
     db = DeviceBatch(b, cuda_device, fixed_split_pages=1)
     db.run()
