@@ -256,7 +256,9 @@ __global__ void __launch_bounds__(32 * 9, 1)
         for (int i = 0; i < 8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
 
         for (int pg = p0; pg < p1; ++pg) {
-            if (!mbar_wait(bar_full + 8u * stage, phase)) {
+            // mma.sync and movmatrix below are warp-collective: the warp
+            // leaves together if any lane's wait gave up.
+            if (!__all_sync(0xFFFFFFFFu, mbar_wait(bar_full + 8u * stage, phase))) {
                 ok = false;
                 break;
             }

@@ -537,7 +537,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int limit = valid_row ? t0 + tok + kv_len - qo_len : -1;
             float scale = p.sm_scale_log2;
             if (!kF8) {
-                ok = wait_or_abort(bar(L::bQFull), qphase, flag_addr, p.status);
+                ok = __all_sync(0xFFFFFFFFu, wait_or_abort(bar(L::bQFull), qphase, flag_addr, p.status));
                 qphase ^= 1u;
                 if (!ok) break;
                 if (p.q_dtype == PAFP8_BF16 && r < TQ * g) {
@@ -577,7 +577,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (nX == 0) continue;  // tile B past the request's last row
             float m = -INFINITY, l = 0.f;  // m in scaled (log2) units
             for (int j = 0; j < nX && ok; ++j) {
-                ok = wait_or_abort(bar(L::bSFull + x), sphase, flag_addr, p.status);
+                ok = __all_sync(0xFFFFFFFFu, wait_or_abort(bar(L::bSFull + x), sphase, flag_addr, p.status));
                 sphase ^= 1u;
                 if (!ok) break;
                 tc_fence_after();
@@ -596,13 +596,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int i = 0; i < 128; ++i)
                         if (i > lim) v[i] = __float_as_uint(-INFINITY);
                 }
-                float pm[8];
+                // Four independent three-input maxima keep the chain short.
+                float pm[4];
 #pragma unroll
-                for (int k = 0; k < 8; ++k) pm[k] = __uint_as_float(v[k]);
+                for (int k = 0; k < 4; ++k) pm[k] = __uint_as_float(v[k]);
 #pragma unroll
-                for (int i = 8; i < 128; ++i) pm[i & 7] = fmaxf(pm[i & 7], __uint_as_float(v[i]));
-                const float mx = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
-                                       fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
+                for (int i = 4; i < 128; i += 2)
+                    pm[(i >> 1) & 3] = max3(pm[(i >> 1) & 3], __uint_as_float(v[i]), __uint_as_float(v[i + 1]));
+                const float mx = fmaxf(max3(pm[0], pm[1], pm[2]), pm[3]);
                 const float m_new = fmaxf(m, mx * scale);
                 float m_use = m;
                 bool rescale = false;
@@ -613,10 +614,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     rescale = true;
                 }
                 if (m_use == -INFINITY) m_use = 0.f;  // row with no admissible key so far
-                if (rescale) {
+                // tcgen05.ld/st are warp-collective: the whole warp rescales
+                // when any of its rows must (alpha = 1 for the others).
+                if (__any_sync(0xFFFFFFFFu, rescale)) {
                     // O_X += P V of the previous KV tile has completed (in-order
                     // tensor pipe, S of this tile was written after it).
-                    const float alpha = ex2(m - m_use);
+                    const float alpha = rescale ? ex2(m - m_use) : 1.f;
+                    const f32x2 alpha2 = make_f32x2(alpha, alpha);
                     l *= alpha;
 #pragma unroll 1
                     for (int c = 0; c < 4; ++c) {
@@ -624,26 +628,43 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tc_ld32(tO + 32 * c, v);
                         tc_wait_ld();
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
+                        for (int i = 0; i < 16; ++i) {
+                            float a, b;
+                            split_f32x2(mul2(make_f32x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1])),
+                                             alpha2),
+                                        a, b);
+                            v[2 * i] = __float_as_uint(a);
+                            v[2 * i + 1] = __float_as_uint(b);
+                        }
                         tc_st32(tO + 32 * c, v);
                     }
                     tc_wait_st();
                 }
                 // P = exp2(s * scale - m) (masked logits are -inf: P = 0), row
-                // sum, P -> TMEM as f16 over the first half of S.
-                const float negm = -m_use;
+                // sum, P -> TMEM as f16 over the first half of S.  Pairs of
+                // columns go through the packed fp32 pipe.
+                const f32x2 scale2 = make_f32x2(scale, scale), negm2 = make_f32x2(-m_use, -m_use);
                 // P overwrites the S values it consumed: P of columns 2i, 2i+1
-                // goes to v[i], which held column i (already used).  Four
-                // independent partial sums keep the chain short.
-                float ps[4] = {0.f, 0.f, 0.f, 0.f};
+                // goes to v[i], which held column i (already used).  Two
+                // independent packed partial sums keep the chain short.
+                f32x2 ps[2] = {make_f32x2(0.f, 0.f), make_f32x2(0.f, 0.f)};
 #pragma unroll
                 for (int i = 0; i < 64; ++i) {
-                    const float e0 = ex2(fmaf(__uint_as_float(v[2 * i]), scale, negm));
-                    const float e1 = ex2(fmaf(__uint_as_float(v[2 * i + 1]), scale, negm));
-                    ps[i & 3] += e0 + e1;
+                    float a, b;
+                    split_f32x2(fma2(make_f32x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1])), scale2,
+                                     negm2),
+                                a, b);
+                    const float e0 = ex2(a), e1 = ex2(b);
+                    const f32x2 e = make_f32x2(e0, e1);
+                    ps[i & 1] = add2(ps[i & 1], e);
                     v[i] = pack_half2(e0, e1);
                 }
-                l += (ps[0] + ps[1]) + (ps[2] + ps[3]);
+                {
+                    float a, b, c, d;
+                    split_f32x2(ps[0], a, b);
+                    split_f32x2(ps[1], c, d);
+                    l += (a + b) + (c + d);
+                }
                 tc_st32(tS, *reinterpret_cast<uint32_t(*)[32]>(v));
                 tc_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
                 tc_wait_st();
@@ -653,7 +674,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (!ok) break;
             // epilogue: the tile's last O update must have completed.
-            ok = wait_or_abort(bar(L::bOFull + x), ophase, flag_addr, p.status);
+            ok = __all_sync(0xFFFFFFFFu, wait_or_abort(bar(L::bOFull + x), ophase, flag_addr, p.status));
             ophase ^= 1u;
             if (!ok) break;
             tc_fence_after();
@@ -666,10 +687,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_wait_ld();
                 if (valid_row) {
                     uint32_t w[16];
+                    const f32x2 inv2 = make_f32x2(inv, inv);
 #pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        w[i] = pack_out2(__uint_as_float(v[2 * i]) * inv, __uint_as_float(v[2 * i + 1]) * inv,
-                                         p.o_dtype);
+                    for (int i = 0; i < 16; ++i) {
+                        float a, b;
+                        split_f32x2(mul2(make_f32x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1])), inv2),
+                                    a, b);
+                        w[i] = pack_out2(a, b, p.o_dtype);
+                    }
                     uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + orow * D + 32 * c);
 #pragma unroll
                     for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
