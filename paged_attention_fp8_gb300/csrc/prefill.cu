@@ -19,8 +19,8 @@
 // list built by the plan.
 //
 // Roles (512 threads, four warpgroups; registers are moved by setmaxnreg from
-// the dequant warpgroup (104) and the producer/MMA warpgroup (56) to the two
-// softmax warpgroups (168)):
+// the dequant warpgroup (64) and the producer/MMA warpgroup (64) to the two
+// softmax warpgroups (192), which hold a whole S row without spilling):
 //   warps 0-3   dequant: raw fp8 K -> f16 K tile (2-byte query path); raw fp8
 //               V -> f16 V^T tile (both paths), zero beyond the request's keys;
 //   warps 4-7   softmax of tile A, warps 8-11 softmax of tile B: thread r owns
@@ -211,11 +211,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t tmem;
     asm volatile("ld.shared.u32 %0, [%1];" : "=r"(tmem) : "r"(base + L::tmem_slot) : "memory");
     // Registers per thread: launched at 128; each warpgroup's branch below
-    // starts by resizing: softmax 168, dequant 96, producer/MMA 80
-    // (4 x 32 x (96 + 2 x 168 + 80) = 65,536, what the block launched with).
+    // starts by resizing: softmax 192, dequant 64, producer/MMA 64
+    // (4 x 32 x (64 + 2 x 192 + 64) = 65,536, what the block launched with).
 
     if (warp >= 12) {
-      asm volatile("setmaxnreg.dec.sync.aligned.u32 80;" ::: "memory");
+      asm volatile("setmaxnreg.dec.sync.aligned.u32 64;" ::: "memory");
       if (warp == 12) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
@@ -333,20 +333,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             auto qk = [&](int x) {
                 const uint32_t dS = tmem + col_s(x);
                 const uint32_t qa = base + L::q + x * L::kQTile;
+                // Descriptor offsets are added inside each MMA block (see
+                // tc_mma_*_at): start addresses are 16-byte units.
                 if (kF8) {
-                    const uint32_t kt = base + L::kr + kring.idx * kRawTile;
+                    const uint64_t dq = sw128_kmajor_desc(qa);
+                    const uint64_t dk = sw128_kmajor_desc(base + L::kr + kring.idx * kRawTile);
 #pragma unroll
                     for (int ks = 0; ks < 4; ++ks)
-                        tc_mma_f8_ss(dS, sw128_kmajor_desc(qa + ks * 32), sw128_kmajor_desc(kt + ks * 32),
-                                     idesc_qk, ks > 0 ? 1u : 0u);
+                        tc_mma_f8_ss_at(dS, dq, dk, (uint32_t)(ks * 32) >> 4, idesc_qk, ks > 0 ? 1u : 0u);
                 } else {
-                    const uint32_t kt = base + L::k16 + kring.idx * kF16Tile;
+                    const uint64_t dq = sw128_kmajor_desc(qa);
+                    const uint64_t dk = sw128_kmajor_desc(base + L::k16 + kring.idx * kF16Tile);
 #pragma unroll
-                    for (int ks = 0; ks < 8; ++ks) {
-                        const uint32_t off = (ks >> 2) * kHalfTile + (ks & 3) * 32;
-                        tc_mma_f16_ss(dS, sw128_kmajor_desc(qa + off), sw128_kmajor_desc(kt + off),
-                                      idesc_qk, ks > 0 ? 1u : 0u);
-                    }
+                    for (int ks = 0; ks < 8; ++ks)
+                        tc_mma_f16_ss_at(dS, dq, dk, ((ks >> 2) * kHalfTile + (ks & 3) * 32) >> 4, idesc_qk,
+                                         ks > 0 ? 1u : 0u);
                 }
                 tc_commit(bar(L::bSFull + x));
                 ++issued_any;
@@ -362,13 +363,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!wait_or_abort(bar(L::bPFull + x), pphase[x], flag_addr, p.status)) return false;
                 pphase[x] ^= 1u;
                 tc_fence_after();
-                const uint32_t vt = base + L::v16 + v16.idx * kF16Tile;
+                const uint64_t dv = sw128_kmajor_desc(base + L::v16 + v16.idx * kF16Tile);
 #pragma unroll
-                for (int ks = 0; ks < 8; ++ks) {
-                    const uint64_t bd = sw128_kmajor_desc(vt + (ks >> 2) * kHalfTile + (ks & 3) * 32);
-                    tc_mma_f16_ts(tmem + col_o(x), tmem + col_s(x) + 8 * ks, bd, idesc_pv,
-                                  (accumulate || ks > 0) ? 1u : 0u);
-                }
+                for (int ks = 0; ks < 8; ++ks)
+                    tc_mma_f16_ts_at(tmem + col_o(x), tmem + col_s(x) + 8 * ks, dv,
+                                     ((ks >> 2) * kHalfTile + (ks & 3) * 32) >> 4, idesc_pv,
+                                     (accumulate || ks > 0) ? 1u : 0u);
                 ++issued_any;
                 return true;
             };
@@ -432,7 +432,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
       }
     } else if (warp < 4) {
-        asm volatile("setmaxnreg.dec.sync.aligned.u32 96;" ::: "memory");
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 64;" ::: "memory");
         // ---------------------------------------------------------- dequant
         const int wd = warp, q8 = lane >> 3, e = lane & 7;
         Ring kr, vr, k16, v16;
@@ -517,7 +517,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
     } else {
-        asm volatile("setmaxnreg.inc.sync.aligned.u32 168;" ::: "memory");
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 192;" ::: "memory");
         // ---------------------------------------------------------- softmax
         const int x = warp < 8 ? 0 : 1;        // query tile A or B
         const int r = threadIdx.x - 128 * (1 + x);  // row of the tile = TMEM lane

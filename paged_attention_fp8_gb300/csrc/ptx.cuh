@@ -276,6 +276,39 @@ __device__ __forceinline__ void tc_mma_f8_ss(uint32_t d_tmem, uint64_t a, uint64
         : "memory");
 }
 
+// The same MMAs with both shared-memory descriptors advanced by `off`
+// (a byte offset >> 4) inside the instruction block, so that a loop over K
+// steps keeps one base descriptor per operand live instead of one per step.
+__device__ __forceinline__ void tc_mma_f16_ss_at(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t off,
+                                                 uint32_t idesc, uint32_t accum) {
+    asm volatile(
+        "{\n .reg .pred p;\n .reg .b64 da, db, o;\n setp.ne.b32 p, %5, 0;\n cvt.u64.u32 o, %3;\n"
+        " add.s64 da, %1, o;\n add.s64 db, %2, o;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %4, p;\n}\n" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(off), "r"(idesc), "r"(accum)
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_mma_f8_ss_at(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t off,
+                                                uint32_t idesc, uint32_t accum) {
+    asm volatile(
+        "{\n .reg .pred p;\n .reg .b64 da, db, o;\n setp.ne.b32 p, %5, 0;\n cvt.u64.u32 o, %3;\n"
+        " add.s64 da, %1, o;\n add.s64 db, %2, o;\n"
+        " tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], da, db, %4, p;\n}\n" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(off), "r"(idesc), "r"(accum)
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_mma_f16_ts_at(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t off,
+                                                 uint32_t idesc, uint32_t accum) {
+    asm volatile(
+        "{\n .reg .pred p;\n .reg .b64 db, o;\n setp.ne.b32 p, %5, 0;\n cvt.u64.u32 o, %3;\n"
+        " add.s64 db, %2, o;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %4, p;\n}\n" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b), "r"(off), "r"(idesc), "r"(accum)
+        : "memory");
+}
+
 // Arrive (count 1) on `bar` when every tcgen05 operation this thread issued
 // before has completed.
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
