@@ -57,7 +57,12 @@ L2_FLUSH_BYTES = 256 << 20
 # changed kernel reports null until it is captured again.
 NCU_TRAFFIC = {
     # profiles/decode_kernel_serving_decode.md
-    "e79874c8279b12c540bfbfc2fe90444f670456379e8632632d857815a5c93020": 310342400,
+    "00b491a4f458ec81a015407acf80532fbb30ecce2b5d02d3c23338ca98337e0e": 310217472,
+}
+# The same for the prefill kernel, per workload index, keyed by the SHA-256
+# of its source (profiles/prefill_kernel_ragged_bf16_and_fp8.md).
+NCU_TRAFFIC_PREFILL = {
+    "c78441c474bd12dd5fd4d527e566d3b5ca5c51b2acf5ec57f55f200481616c23": {4: 165958656, 5: 187395840},
 }
 
 
