@@ -160,6 +160,7 @@ def time_prefill(index, dev, steps, warmup):
     ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
     tflops = flops / (ms * 1e-3) / 1e12
     p16, kind = measured_bf16_tflops()
+    traffic = NCU_TRAFFIC_PREFILL.get(kernel_sha("prefill.cu"), {}).get(index)
     fp8 = b.q_dtype in ("e4m3fn", "e5m2")
     out = {"workload": WORKLOADS[index], "value": round(tflops, 2), "unit": "TFLOP/s",
            "ms_per_launch": round(ms, 5), "flops": flops, "launches": steps,
@@ -168,12 +169,12 @@ def time_prefill(index, dev, steps, warmup):
         p8 = 2.0 * p16  # another dtype's measured peak x the nominal fp8/bf16 ratio
         blended = 2.0 / (1.0 / p8 + 1.0 / p16)
         out["roofline"] = {"bound": "tensor", "achieved": round(tflops, 2), "peak": round(blended, 1),
-                           "unit": "TFLOP/s", "frac": round(tflops / blended, 4), "traffic": None,
+                           "unit": "TFLOP/s", "frac": round(tflops / blended, 4), "traffic": traffic,
                            "peak_kind": f"{kind} bf16 x nominal fp8 ratio 2, blended for half the flops at each rate",
                            "frac_of_dense_bf16": round(tflops / p16, 4)}
     else:
         out["roofline"] = {"bound": "tensor", "achieved": round(tflops, 2), "peak": p16, "unit": "TFLOP/s",
-                           "frac": round(tflops / p16, 4), "traffic": None, "peak_kind": f"{kind} dense bf16"}
+                           "frac": round(tflops / p16, 4), "traffic": traffic, "peak_kind": f"{kind} dense bf16"}
     del q, k, v, idx, o, lse, ws, flush
     torch.cuda.empty_cache()
     return out
