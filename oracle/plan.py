@@ -157,7 +157,9 @@ def prefill_metadata(kv_indptr, last_page_len, qo_indptr, *, num_qo_heads, num_k
     of two query tiles (A = [t0, t0+TQ), B = the next TQ); its KV-tile count
     is the number of 128-key tiles its last token may see under the
     bottom-right causal rule, capped by the request's own key tiles.
-    Tiles are sorted by that count, descending, ties in (b, hk, t0) order;
+    Each tile record is (b, hk, t0, nkv, qo_indptr[b], qo_len, kv_len,
+    kv_indptr[b]).  Tiles are sorted by that count, descending, ties in
+    (b, hk, t0) order;
     G = min(num_ctas, #tiles) persistent CTAs take tiles i, i + G, ..."""
     kv_indptr = [int(x) for x in kv_indptr]
     last_page_len = [int(x) for x in last_page_len]
@@ -177,7 +179,7 @@ def prefill_metadata(kv_indptr, last_page_len, qo_indptr, *, num_qo_heads, num_k
                 last = min(t0 + 2 * TQ, qo) - 1
                 lim = last + kv - qo
                 nkv = min((kv + 127) // 128, lim // 128 + 1)
-                tiles.append((b, hk, t0, nkv))
+                tiles.append((b, hk, t0, nkv, qo_indptr[b], qo, kv, kv_indptr[b]))
     tiles = sorted(tiles, key=lambda t: -t[3])  # stable
     G = min(num_ctas, len(tiles))
     words = [0] * HEADER_WORDS

@@ -320,12 +320,18 @@ void build_prefill_meta(pafp8_plan* pl) {
     put(kMetaOffReqPage, req_page);
     put(kMetaOffReqKvLen, req_kv);
     put(kMetaOffReqQo, pl->qo_indptr);
+    // Each item record carries the request fields the kernel needs, so a CTA
+    // reads one record per item and no dependent loads.
     std::vector<int32_t> tw;
     for (auto& t : tiles) {
         tw.push_back(t.b);
         tw.push_back(t.hk);
         tw.push_back(t.t0);
         tw.push_back(t.nkv);
+        tw.push_back(pl->qo_indptr[t.b]);
+        tw.push_back(pl->qo_indptr[t.b + 1] - pl->qo_indptr[t.b]);
+        tw.push_back(req_kv[t.b]);
+        tw.push_back(req_page[t.b]);
     }
     put(kMetaOffTile, tw);
     pl->num_ctas = G;

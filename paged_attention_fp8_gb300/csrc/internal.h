@@ -40,7 +40,7 @@ enum MetaHeader : int {
     kMetaOffMergeSlot,   // int32[num_partials]
     kMetaOffReqQo,       // int32[batch+1] qo_indptr (prefill)
     kMetaNumTiles,       // prefill tiles
-    kMetaOffTile,        // int32[4*num_tiles] prefill tiles
+    kMetaOffTile,        // int32[8*num_tiles] prefill items: b, hk, t0, nkv, qo_begin, qo_len, kv_len, page_begin
     kMetaTileRows,       // packed query rows per prefill tile
     kMetaOffRowMerge,    // int32[rows] merge entry of each decode row, or -1
     kMetaHeaderWords = 32

@@ -111,12 +111,15 @@ struct Ring {
 };
 
 struct Item {
-    int b, hk, t0, nkv;  // nkv: KV tiles of the item (tile B's, or A's if B is empty)
+    int b, hk, t0, nkv;          // nkv: KV tiles of the item (tile B's, or A's if B is empty)
+    int qo0, qo_len, kv_len, page0;  // the request's first query row, rows, keys, first page entry
 };
 
-__device__ __forceinline__ Item load_item(const int* meta, int t) {
-    const int* tl = meta + meta[kMetaOffTile] + 4 * t;
-    return Item{tl[0], tl[1], tl[2], tl[3]};
+// One plan record per item, with the request fields the kernel needs, so an
+// item start costs one round of independent loads.
+__device__ __forceinline__ Item load_item(const int* items, int t) {
+    const int* r = items + 8 * t;
+    return Item{__ldg(r), __ldg(r + 1), __ldg(r + 2), __ldg(r + 3), __ldg(r + 4), __ldg(r + 5), __ldg(r + 6), __ldg(r + 7)};
 }
 
 // KV tiles that query tile `x` (0 = A, 1 = B) of an item needs: its last
@@ -169,9 +172,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int* meta = p.meta;
     const int n_items = meta[kMetaNumTiles];
-    const int* req_page = meta + meta[kMetaOffReqPage];
-    const int* req_kv = meta + meta[kMetaOffReqKvLen];
-    const int* qo_ptr = meta + meta[kMetaOffReqQo];
+    const int* items = meta + meta[kMetaOffTile];
     const int g = p.group, TQ = p.tile_tokens;
 
     if (threadIdx.x == 0) {
@@ -228,8 +229,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         long long issued_k = 0, issued_v = 0, issued_q = 0;
         bool ok = true;
         for (int t = blockIdx.x; t < n_items && ok; t += gridDim.x) {
-            const Item it = load_item(meta, t);
-            const int q0 = qo_ptr[it.b] + it.t0;
+            const Item it = load_item(items, t);
+            const int q0 = it.qo0 + it.t0;
             if (lane == 0) {
                 ok = wait_or_abort(bar(L::bQEmpty), qphase ^ 1u, flag_addr, p.status);
                 if (ok) {
@@ -251,9 +252,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
             qphase ^= 1u;
-            const int kv_len = req_kv[it.b];
+            const int kv_len = it.kv_len;
             const int npages = (kv_len + kPageSize - 1) / kPageSize;
-            const int* idx = p.kv_indices + req_page[it.b];
+            const int* idx = p.kv_indices + it.page0;
             // Page ids of the next KV tile are fetched one tile ahead.
             int page_next = 0;
             {
@@ -373,9 +374,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 return true;
             };
             for (int t = blockIdx.x; t < n_items && ok; t += gridDim.x) {
-                const Item it = load_item(meta, t);
-                const int qo_len = qo_ptr[it.b + 1] - qo_ptr[it.b];
-                const int kv_len = req_kv[it.b];
+                const Item it = load_item(items, t);
+                const int qo_len = it.qo_len;
+                const int kv_len = it.kv_len;
                 const int nA = tile_nkv(it.t0, 0, TQ, qo_len, kv_len);
                 const int nB = tile_nkv(it.t0, 1, TQ, qo_len, kv_len);
                 const int n = it.nkv;
@@ -438,8 +439,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         Ring kr, vr, k16, v16;
         bool ok = true;
         for (int t = blockIdx.x; t < n_items && ok; t += gridDim.x) {
-            const Item it = load_item(meta, t);
-            const int kv_len = req_kv[it.b];
+            const Item it = load_item(items, t);
+            const int kv_len = it.kv_len;
             for (int j = 0; j < it.nkv && ok; ++j) {
                 const int valid = min(kTileKeys, kv_len - j * kTileKeys);
                 if (!kF8) {
@@ -526,10 +527,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t qphase = 0, sphase = 0, ophase = 0;
         bool ok = true;
         for (int t = blockIdx.x; t < n_items && ok; t += gridDim.x) {
-            const Item it = load_item(meta, t);
-            const int qo0 = qo_ptr[it.b];
-            const int qo_len = qo_ptr[it.b + 1] - qo0;
-            const int kv_len = req_kv[it.b];
+            const Item it = load_item(items, t);
+            const int qo0 = it.qo0;
+            const int qo_len = it.qo_len;
+            const int kv_len = it.kv_len;
             const int t0 = it.t0 + x * TQ;
             const int nX = tile_nkv(it.t0, x, TQ, qo_len, kv_len);
             const int tok = r / g, hh = r - tok * g;

@@ -263,10 +263,14 @@ def test_prefill_tiles_cover_every_row_head_once(case):
     hq, hkv = case.get("hq", 32), case.get("hkv", 8)
     g = hq // hkv
     tq = int(m[20])
-    tiles = m[m[19]:m[19] + 4 * int(m[18])].reshape(-1, 4)
+    tiles = m[m[19]:m[19] + 8 * int(m[18])].reshape(-1, 8)
+    qo_ptr = np.concatenate([[0], np.cumsum(case["qo_lens"])])
     seen = set()
-    for b, hk, t0, nkv in tiles:
+    for b, hk, t0, nkv, qo0, qo_len, kv_len, page0 in tiles:
         qo, kv = case["qo_lens"][b], case["kv_lens"][b]
+        # the record repeats the request's own fields
+        assert (qo0, qo_len, kv_len) == (qo_ptr[b], qo, kv)
+        assert page0 == m[m[10] + b]
         for tok in range(t0, min(t0 + 2 * tq, qo)):  # two query tiles per item
             for h in range(hk * g, hk * g + g):
                 assert (b, tok, h) not in seen
