@@ -180,6 +180,52 @@ def time_prefill(index, dev, steps, warmup):
     return out
 
 
+def time_decode_2byte(dev, steps, warmup):
+    """Device time of one decode step (decode + merge kernels) on the serving
+    workload's shape with a bf16 cache; GB/s over its algorithmic bytes (KV at
+    2 bytes per element)."""
+    import torch
+
+    import paged_attention_fp8_gb300 as pa
+    from paged_attention_fp8_gb300.workloads import TORCH_DTYPES, WORKLOADS, workload
+
+    b = workload(6)
+    nbytes = decode_bytes(b)
+    q, k, v, idx = b.q.to(dev), b.k_cache.to(dev), b.v_cache.to(dev), b.kv_indices.to(dev)
+    plan = pa.Plan(mode="decode", num_qo_heads=b.num_qo_heads, num_kv_heads=b.num_kv_heads,
+                   num_pages=b.num_pages, kv_indptr=b.kv_indptr, last_page_len=b.last_page_len,
+                   q_dtype=b.q_dtype, kv_dtype=b.kv_dtype, o_dtype=b.o_dtype, sm_scale=b.sm_scale)
+    ws = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device=dev)
+    plan.upload(ws)
+    o = torch.empty(b.nnz_qo, b.num_qo_heads, b.head_dim, dtype=TORCH_DTYPES[b.o_dtype], device=dev)
+    lse = torch.empty(b.nnz_qo, b.num_qo_heads, dtype=torch.float32, device=dev)
+    flush = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    kw = dict(q_scale=b.q_scale, k_scale=b.k_scale, v_scale=b.v_scale)
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        flush.sum()
+        plan.run(q, k, v, idx, o, lse, ws, **kw)
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+    for i in range(steps):
+        flush.sum()
+        ev[i][0].record(stream)
+        plan.run(q, k, v, idx, o, lse, ws, **kw)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    plan.device_status(ws)
+    ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    peak, kind = measured_peaks()
+    del q, k, v, idx, o, lse, ws, flush
+    torch.cuda.empty_cache()
+    return {"workload": WORKLOADS[6], "value": round(gbs, 1), "unit": "GB/s", "ms_per_step": round(ms, 5),
+            "bytes_per_step": nbytes, "steps": steps,
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(gbs / peak, 4), "peak_kind": kind,
+                         "note": "whole step (decode + merge kernels)"}}
+
+
 def kernel_sha(name: str) -> str:
     with open(os.path.join(ROOT, "paged_attention_fp8_gb300", "csrc", name), "rb") as f:
         return hashlib.sha256(f.read()).hexdigest()
@@ -447,6 +493,7 @@ def run_ours(args):
         torch.cuda.empty_cache()
         for i in (4, 5):
             prefill_res[i] = time_prefill(i, dev, args.prefill_steps, max(3, min(args.warmup, 10)))
+        decode16 = time_decode_2byte(dev, min(args.steps, 200), max(3, min(args.warmup, 20)))
 
     if rank != 0:
         dist.destroy_process_group()
@@ -485,6 +532,7 @@ def run_ours(args):
     }
     if args.mode == "all":
         line["prefill"] = {"ragged_bf16": prefill_res[4], "fp8_fp8": prefill_res[5]}
+        line["decode_2byte_cache"] = decode16
     if world == 1 and not args.no_cpu_baseline:
         n = oracle_sample_size(b, 15.0)
         dt, by, cores = oracle_decode_sample(b, n)

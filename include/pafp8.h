@@ -75,8 +75,14 @@ enum { PAFP8_MODE_DECODE = 0, PAFP8_MODE_PREFILL = 1 };
  * group size num_qo_heads/num_kv_heads <= 8 (decode) or <= 16 (prefill).
  *
  * Dtype rules (checked by pafp8_plan_create, re-checked by pafp8_run):
- *   kv_dtype   E4M3FN or E5M2.  F16/BF16 caches are refused by this build;
- *              F32/INT8/UINT8 caches are refused with their own sentence.
+ *   kv_dtype   E4M3FN or E5M2.  Decode also takes an F16 or BF16 cache
+ *              with an F16 or BF16 query in any mix ("fp8 KV cache in the
+ *              in-tree prefill kernel", Test plan: decode is exempt from the
+ *              rule that the cache matches the query); an fp8 query with a
+ *              2-byte cache, and a 2-byte cache in prefill, are refused.  An
+ *              fp8 cache and its exact f16 widening give bit-identical decode
+ *              results.  F32/INT8/UINT8 caches are refused with their own
+ *              sentence.
  *   q_dtype    F16 or BF16 (a 2-byte query against the fp8 cache, which is
  *              dequantized on load), or E4M3FN/E5M2 (an fp8 query; q_scale
  *              then folds into sm_scale like the FP8 BMM1 scale).

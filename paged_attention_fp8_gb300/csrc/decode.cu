@@ -29,6 +29,14 @@
 //    owns dims 32t..32t+31 of every row) and between V and O (thread g owns
 //    dims 16g..16g+15), so every shared-memory read is one conflict-free
 //    16-byte load.
+//  * A 2-byte cache (f16 or bf16, which the pages exempt from the rule that
+//    the cache matches the query in decode) runs through the same kernel:
+//    each 128-element row arrives as two 128-byte halves, every thread loads
+//    the same dims of the same tokens as in the fp8 case, and the MMA operand
+//    words it assembles are exactly the converted words the fp8 path feeds
+//    the tensor cores.  So an fp8 cache and its f16 dequantization give
+//    bit-identical results.  A bf16 cache runs bf16 MMAs with P rounded to
+//    bf16; an f16 query enters them as two bf16 words whose sum is exact.
 //  * A segment covering its whole request writes o and lse; a partial one
 //    writes (O/l, lse in log2 units) to the workspace, and a separate merge
 //    kernel (one block per split row and query head, launched as a
@@ -51,20 +59,58 @@ using namespace ptx;
 
 constexpr int D = kHeadDim;
 constexpr int P = kPageSize;
-constexpr int kTileBytes = P * D;           // one KV head of one page
 constexpr int kStageBudget = 192 * 1024;    // shared memory for the page ring
+__host__ __device__ constexpr bool is_2byte_kv(int kt) { return kt == PAFP8_F16 || kt == PAFP8_BF16; }
+// One KV head of one page in shared memory: 16 token rows of 128 B (fp8), or
+// of two 128-B halves (2-byte cache).
+__host__ __device__ constexpr int tile_bytes(int kt) { return P * D * (is_2byte_kv(kt) ? 2 : 1); }
 __device__ __forceinline__ void flag(uint32_t* status, uint32_t bit) { atomicOr(status, bit); }
+
+template <bool kBF16>
+__device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+    if (kBF16)
+        mma_16816_bf16(c, a0, a1, a2, a3, b0, b1);
+    else
+        mma_16816(c, a0, a1, a2, a3, b0, b1);
+}
 
 // Q fragment for the QK product: B operand (K = head dim, N = 8 query heads).
 // Lane (g, t) holds head g of the group, dims 32t .. 32t+31, as 16 f16x2
 // words; word j = dims 32t+2j, 32t+2j+1.  Returns the power-of-two factor the
 // logits must be multiplied by (a bf16 query is brought into f16 range by an
 // exact power-of-two scaling when its magnitude needs it).
-template <int KT_UNUSED>
-__device__ __forceinline__ float load_q(uint32_t (&qf)[16], const void* q, int q_dtype,
+template <bool kBF16>
+__device__ __forceinline__ float load_q(uint32_t (&qf)[16], uint32_t (&qlo)[16], const void* q, int q_dtype,
                                         size_t head_off, bool active, int t) {
     float factor = 1.0f;
-    if (q_dtype == PAFP8_F16 || q_dtype == PAFP8_BF16) {
+    if (kBF16) {
+        // bf16 MMAs (bf16 cache): a bf16 query as is; an f16 query as the sum
+        // of two bf16 words, its bf16 rounding (qf) and the exact remainder
+        // (qlo: an f16 has 11 significant bits, so the remainder needs at most
+        // 4 of bf16's 8), so the QK product loses nothing.
+        uint4 w[4] = {};
+        if (active) {
+            const uint4* src = reinterpret_cast<const uint4*>(
+                static_cast<const uint16_t*>(q) + head_off + 32 * t);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) w[i] = __ldg(src + i);
+        }
+        const uint32_t* ws = reinterpret_cast<const uint32_t*>(w);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            if (q_dtype == PAFP8_BF16) {
+                qf[j] = ws[j];
+            } else {
+                const __half2 h = *reinterpret_cast<const __half2*>(&ws[j]);
+                const float2 f = __half22float2(h);
+                const float hx = __bfloat162float(__float2bfloat16_rn(f.x));
+                const float hy = __bfloat162float(__float2bfloat16_rn(f.y));
+                qf[j] = pack_bf162(hx, hy);
+                qlo[j] = pack_bf162(f.x - hx, f.y - hy);
+            }
+        }
+    } else if (q_dtype == PAFP8_F16 || q_dtype == PAFP8_BF16) {
         uint4 w[4] = {};
         if (active) {
             const uint4* src = reinterpret_cast<const uint4*>(
@@ -127,6 +173,8 @@ __global__ void __launch_bounds__(32 * 9, 1)
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;      // 128B swizzle wants 1024-B alignment
+    constexpr bool k2 = is_2byte_kv(KT), kBF = KT == PAFP8_BF16;
+    constexpr uint32_t kTileBytes = (uint32_t)tile_bytes(KT);
     const uint32_t stage_bytes = 2u * hpc * kTileBytes;  // K heads then V heads
     const uint32_t bar_full = base + stages * stage_bytes;
     const uint32_t bar_empty = bar_full + 8u * stages;
@@ -181,7 +229,19 @@ __global__ void __launch_bounds__(32 * 9, 1)
                             mbar_arrive_expect_tx(fb, stage_bytes);
                             const uint32_t sk = base + stage * stage_bytes;
                             const uint32_t sv = sk + hpc * kTileBytes;
-                            if (heads_per_box == hpc) {
+                            if (k2) {
+                                // (d % 64, d / 64, token, head, page) or, per head,
+                                // (d % 64, d / 64, head, token, page)
+                                if (heads_per_box == hpc) {
+                                    tma_load_5d(sk, &tmk, fb, 0, 0, 0, hb * hpc, pg);
+                                    tma_load_5d(sv, &tmv, fb, 0, 0, 0, hb * hpc, pg);
+                                } else {
+                                    for (int h = 0; h < hpc; ++h) {
+                                        tma_load_5d(sk + h * kTileBytes, &tmk, fb, 0, 0, hb * hpc + h, 0, pg);
+                                        tma_load_5d(sv + h * kTileBytes, &tmv, fb, 0, 0, hb * hpc + h, 0, pg);
+                                    }
+                                }
+                            } else if (heads_per_box == hpc) {
                                 // one box = every head of the block: (d, token, head, page)
                                 tma_load_4d(sk, &tmk, fb, 0, 0, hb * hpc, pg);
                                 tma_load_4d(sv, &tmv, fb, 0, 0, hb * hpc, pg);
@@ -245,9 +305,10 @@ __global__ void __launch_bounds__(32 * 9, 1)
             continue;
         }
 
-        uint32_t qf[16];
+        uint32_t qf[16], qlo[16];
         const size_t q_head_off = ((size_t)b * Hq + (size_t)kvh * group + g) * D;
-        const float qfactor = load_q<KT>(qf, p.q, p.q_dtype, q_head_off, g < group, t);
+        const float qfactor = load_q<kBF>(qf, qlo, p.q, p.q_dtype, q_head_off, g < group, t);
+        const bool split_q = kBF && p.q_dtype == PAFP8_F16;
         const float sc = p.sm_scale_log2 * qfactor;
 
         float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
@@ -264,16 +325,47 @@ __global__ void __launch_bounds__(32 * 9, 1)
             }
             const uint32_t kt = base + stage * stage_bytes + warp * kTileBytes;
             const uint32_t vt = kt + hpc * kTileBytes;
-            // K rows g and g+8, 16-byte chunks 2t and 2t+1 (swizzled by row & 7 = g).
-            const uint4 k0 = lds128(kt + g * 128 + (((2 * t) ^ g) << 4));
-            const uint4 k1 = lds128(kt + g * 128 + (((2 * t + 1) ^ g) << 4));
-            const uint4 k2 = lds128(kt + (g + 8) * 128 + (((2 * t) ^ g) << 4));
-            const uint4 k3 = lds128(kt + (g + 8) * 128 + (((2 * t + 1) ^ g) << 4));
-            // V rows 2t, 2t+1, 2t+8, 2t+9, chunk g (swizzled by the row's low 3 bits).
-            uint4 v0 = lds128(vt + (2 * t) * 128 + ((g ^ (2 * t)) << 4));
-            uint4 v1 = lds128(vt + (2 * t + 1) * 128 + ((g ^ (2 * t + 1)) << 4));
-            uint4 v2 = lds128(vt + (2 * t + 8) * 128 + ((g ^ (2 * t)) << 4));
-            uint4 v3 = lds128(vt + (2 * t + 9) * 128 + ((g ^ (2 * t + 1)) << 4));
+            // fp8 cache: K rows g and g+8, 16-byte chunks 2t and 2t+1 (swizzled by
+            // row & 7 = g), converted pairwise right before each MMA; V rows 2t,
+            // 2t+1, 2t+8, 2t+9, chunk g.  2-byte cache: the same dims of the same
+            // tokens as 16-bit words (K: dims 32t .. 32t+31 of tokens g and g+8,
+            // word w = dims 32t+2w, 32t+2w+1; V: dims 16g .. 16g+15 of the four
+            // tokens, word w = dims 16g+2w, 16g+2w+1), so the operand words match
+            // the fp8 path's converted words exactly.
+            uint4 k0, k1, k2w, k3, v0, v1, v2, v3;
+            uint32_t kw0[16], kw8[16], vw[4][8];
+            if constexpr (k2) {
+                // A token row is two swizzled 128-B rows (dims 0-63, 64-127):
+                // row index 2 * token + half.
+                const int rk = (t >> 1) + 2 * g;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int c = 4 * (t & 1) + i;
+                    const uint4 x = lds128(kt + rk * 128 + ((c ^ (rk & 7)) << 4));
+                    const uint4 y = lds128(kt + (rk + 16) * 128 + ((c ^ (rk & 7)) << 4));
+                    kw0[4 * i] = x.x, kw0[4 * i + 1] = x.y, kw0[4 * i + 2] = x.z, kw0[4 * i + 3] = x.w;
+                    kw8[4 * i] = y.x, kw8[4 * i + 1] = y.y, kw8[4 * i + 2] = y.z, kw8[4 * i + 3] = y.w;
+                }
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    const int rv = (g >> 2) + 2 * (2 * t + (r & 1) + 8 * (r >> 1));
+#pragma unroll
+                    for (int i = 0; i < 2; ++i) {
+                        const int c = 2 * (g & 3) + i;
+                        const uint4 x = lds128(vt + rv * 128 + ((c ^ (rv & 7)) << 4));
+                        vw[r][4 * i] = x.x, vw[r][4 * i + 1] = x.y, vw[r][4 * i + 2] = x.z, vw[r][4 * i + 3] = x.w;
+                    }
+                }
+            } else {
+                k0 = lds128(kt + g * 128 + (((2 * t) ^ g) << 4));
+                k1 = lds128(kt + g * 128 + (((2 * t + 1) ^ g) << 4));
+                k2w = lds128(kt + (g + 8) * 128 + (((2 * t) ^ g) << 4));
+                k3 = lds128(kt + (g + 8) * 128 + (((2 * t + 1) ^ g) << 4));
+                v0 = lds128(vt + (2 * t) * 128 + ((g ^ (2 * t)) << 4));
+                v1 = lds128(vt + (2 * t + 1) * 128 + ((g ^ (2 * t + 1)) << 4));
+                v2 = lds128(vt + (2 * t + 8) * 128 + ((g ^ (2 * t)) << 4));
+                v3 = lds128(vt + (2 * t + 9) * 128 + ((g ^ (2 * t + 1)) << 4));
+            }
             mbar_arrive(bar_empty + 8u * stage);
             if (++stage == stages) {
                 stage = 0;
@@ -282,25 +374,57 @@ __global__ void __launch_bounds__(32 * 9, 1)
 
             const int valid = kv_len - pg * P;  // tokens of this page that exist (>= 1)
             if (valid < P) {
-                const uint4 z = make_uint4(0, 0, 0, 0);
-                if (2 * t >= valid) v0 = z;
-                if (2 * t + 1 >= valid) v1 = z;
-                if (2 * t + 8 >= valid) v2 = z;
-                if (2 * t + 9 >= valid) v3 = z;
+                if constexpr (k2) {
+#pragma unroll
+                    for (int r = 0; r < 4; ++r)
+                        if (2 * t + (r & 1) + 8 * (r >> 1) >= valid) {
+#pragma unroll
+                            for (int w = 0; w < 8; ++w) vw[r][w] = 0u;
+                        }
+                } else {
+                    const uint4 z = make_uint4(0, 0, 0, 0);
+                    if (2 * t >= valid) v0 = z;
+                    if (2 * t + 1 >= valid) v1 = z;
+                    if (2 * t + 8 >= valid) v2 = z;
+                    if (2 * t + 9 >= valid) v3 = z;
+                }
             }
 
             // S^T = K . Q^T over 8 k-steps, two accumulators for ILP.
             float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
-            const uint32_t kr0[8] = {k0.x, k0.y, k0.z, k0.w, k1.x, k1.y, k1.z, k1.w};
-            const uint32_t kr8[8] = {k2.x, k2.y, k2.z, k2.w, k3.x, k3.y, k3.z, k3.w};
+            if constexpr (k2) {
 #pragma unroll
-            for (int s = 0; s < 8; ++s) {
-                const uint32_t a0 = fp8x2_lo<KT>(kr0[s]), a1 = fp8x2_lo<KT>(kr8[s]);
-                const uint32_t a2 = fp8x2_hi<KT>(kr0[s]), a3 = fp8x2_hi<KT>(kr8[s]);
-                if (s & 1)
-                    mma_16816(sb, a0, a1, a2, a3, qf[2 * s], qf[2 * s + 1]);
-                else
-                    mma_16816(sa, a0, a1, a2, a3, qf[2 * s], qf[2 * s + 1]);
+                for (int s = 0; s < 8; ++s) {
+                    if (s & 1)
+                        mma16816<kBF>(sb, kw0[2 * s], kw8[2 * s], kw0[2 * s + 1], kw8[2 * s + 1], qf[2 * s],
+                                      qf[2 * s + 1]);
+                    else
+                        mma16816<kBF>(sa, kw0[2 * s], kw8[2 * s], kw0[2 * s + 1], kw8[2 * s + 1], qf[2 * s],
+                                      qf[2 * s + 1]);
+                }
+                if (kBF && split_q) {
+#pragma unroll
+                    for (int s = 0; s < 8; ++s) {
+                        if (s & 1)
+                            mma16816<kBF>(sb, kw0[2 * s], kw8[2 * s], kw0[2 * s + 1], kw8[2 * s + 1], qlo[2 * s],
+                                          qlo[2 * s + 1]);
+                        else
+                            mma16816<kBF>(sa, kw0[2 * s], kw8[2 * s], kw0[2 * s + 1], kw8[2 * s + 1], qlo[2 * s],
+                                          qlo[2 * s + 1]);
+                    }
+                }
+            } else {
+                const uint32_t kr0[8] = {k0.x, k0.y, k0.z, k0.w, k1.x, k1.y, k1.z, k1.w};
+                const uint32_t kr8[8] = {k2w.x, k2w.y, k2w.z, k2w.w, k3.x, k3.y, k3.z, k3.w};
+#pragma unroll
+                for (int s = 0; s < 8; ++s) {
+                    const uint32_t a0 = fp8x2_lo<KT>(kr0[s]), a1 = fp8x2_lo<KT>(kr8[s]);
+                    const uint32_t a2 = fp8x2_hi<KT>(kr0[s]), a3 = fp8x2_hi<KT>(kr8[s]);
+                    if (s & 1)
+                        mma_16816(sb, a0, a1, a2, a3, qf[2 * s], qf[2 * s + 1]);
+                    else
+                        mma_16816(sa, a0, a1, a2, a3, qf[2 * s], qf[2 * s + 1]);
+                }
             }
             // (tok g | tok g+8) x (head 2t | head 2t+1), log2 units.
             float x0 = (sa[0] + sb[0]) * sc, x1 = (sa[1] + sb[1]) * sc;
@@ -329,19 +453,29 @@ __global__ void __launch_bounds__(32 * 9, 1)
                 acc[i][3] *= al1;
             }
             // P^T as the B operand: transpose the two 8x8 (token x head) blocks.
-            const uint32_t pb0 = movmatrix_t(pack_half2(e0, e1));
-            const uint32_t pb1 = movmatrix_t(pack_half2(e2, e3));
+            const uint32_t pb0 = movmatrix_t(kBF ? pack_bf162(e0, e1) : pack_half2(e0, e1));
+            const uint32_t pb1 = movmatrix_t(kBF ? pack_bf162(e2, e3) : pack_half2(e2, e3));
 
-            const uint32_t va[4] = {v0.x, v0.y, v0.z, v0.w}, vb[4] = {v1.x, v1.y, v1.z, v1.w};
-            const uint32_t vc[4] = {v2.x, v2.y, v2.z, v2.w}, vd[4] = {v3.x, v3.y, v3.z, v3.w};
+            // O^T += V^T . P^T: MMA 2j takes dims 16g+4j (rows g) and 16g+4j+1
+            // (rows g+8), MMA 2j+1 the next two; the k columns are the tokens
+            // (2t, 2t+1 | 2t+8, 2t+9), each operand word one dim of two tokens.
+            if constexpr (k2) {
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const uint32_t ab_lo = prmt(va[j], vb[j], 0x5140u), ab_hi = prmt(va[j], vb[j], 0x7362u);
-                const uint32_t cd_lo = prmt(vc[j], vd[j], 0x5140u), cd_hi = prmt(vc[j], vd[j], 0x7362u);
-                mma_16816(acc[2 * j], fp8x2_lo<KT>(ab_lo), fp8x2_hi<KT>(ab_lo), fp8x2_lo<KT>(cd_lo),
-                          fp8x2_hi<KT>(cd_lo), pb0, pb1);
-                mma_16816(acc[2 * j + 1], fp8x2_lo<KT>(ab_hi), fp8x2_hi<KT>(ab_hi),
-                          fp8x2_lo<KT>(cd_hi), fp8x2_hi<KT>(cd_hi), pb0, pb1);
+                for (int w = 0; w < 8; ++w)
+                    mma16816<kBF>(acc[w], prmt(vw[0][w], vw[1][w], 0x5410u), prmt(vw[0][w], vw[1][w], 0x7632u),
+                                  prmt(vw[2][w], vw[3][w], 0x5410u), prmt(vw[2][w], vw[3][w], 0x7632u), pb0, pb1);
+            } else {
+                const uint32_t va[4] = {v0.x, v0.y, v0.z, v0.w}, vb[4] = {v1.x, v1.y, v1.z, v1.w};
+                const uint32_t vc[4] = {v2.x, v2.y, v2.z, v2.w}, vd[4] = {v3.x, v3.y, v3.z, v3.w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const uint32_t ab_lo = prmt(va[j], vb[j], 0x5140u), ab_hi = prmt(va[j], vb[j], 0x7362u);
+                    const uint32_t cd_lo = prmt(vc[j], vd[j], 0x5140u), cd_hi = prmt(vc[j], vd[j], 0x7362u);
+                    mma_16816(acc[2 * j], fp8x2_lo<KT>(ab_lo), fp8x2_hi<KT>(ab_lo), fp8x2_lo<KT>(cd_lo),
+                              fp8x2_hi<KT>(cd_lo), pb0, pb1);
+                    mma_16816(acc[2 * j + 1], fp8x2_lo<KT>(ab_hi), fp8x2_hi<KT>(ab_hi), fp8x2_lo<KT>(cd_hi),
+                              fp8x2_hi<KT>(cd_hi), pb0, pb1);
+                }
             }
         }
         if (!ok) break;
@@ -475,29 +609,35 @@ cudaError_t noalloc_scratch(void** ptr) {
     return cudaSuccess;
 }
 
-cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& tmap_k, const CUtensorMap& tmap_v,
-                          int num_ctas, int hpc, int group, int heads_per_box, cudaStream_t stream) {
-    const int stage_bytes = 2 * hpc * kTileBytes;
+template <int KT>
+cudaError_t launch_decode_t(const DecodeParams& p, const CUtensorMap& tmap_k, const CUtensorMap& tmap_v,
+                            int num_ctas, int hpc, int group, int heads_per_box, cudaStream_t stream) {
+    const int stage_bytes = 2 * hpc * tile_bytes(KT);
     int stages = kStageBudget / stage_bytes;
     if (stages > 8) stages = 8;
     if (stages < 2) stages = 2;
     const size_t smem = 1024 + (size_t)stages * stage_bytes + 16 * (size_t)stages;
     const dim3 grid(num_ctas), block(32 * (hpc + 1));
-    cudaError_t e;
-    if (p.kv_dtype == PAFP8_E4M3FN) {
-        e = cudaFuncSetAttribute(decode_kernel<PAFP8_E4M3FN>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        decode_kernel<PAFP8_E4M3FN><<<grid, block, smem, stream>>>(p, tmap_k, tmap_v, hpc, group, stages,
-                                                                   heads_per_box);
-    } else {
-        e = cudaFuncSetAttribute(decode_kernel<PAFP8_E5M2>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        decode_kernel<PAFP8_E5M2><<<grid, block, smem, stream>>>(p, tmap_k, tmap_v, hpc, group, stages,
-                                                                 heads_per_box);
-    }
+    cudaError_t e = cudaFuncSetAttribute(decode_kernel<KT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    decode_kernel<KT><<<grid, block, smem, stream>>>(p, tmap_k, tmap_v, hpc, group, stages, heads_per_box);
     return cudaGetLastError();
+}
+
+cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& tmap_k, const CUtensorMap& tmap_v,
+                          int num_ctas, int hpc, int group, int heads_per_box, cudaStream_t stream) {
+    switch (p.kv_dtype) {
+        case PAFP8_E4M3FN:
+            return launch_decode_t<PAFP8_E4M3FN>(p, tmap_k, tmap_v, num_ctas, hpc, group, heads_per_box, stream);
+        case PAFP8_E5M2:
+            return launch_decode_t<PAFP8_E5M2>(p, tmap_k, tmap_v, num_ctas, hpc, group, heads_per_box, stream);
+        case PAFP8_F16:
+            return launch_decode_t<PAFP8_F16>(p, tmap_k, tmap_v, num_ctas, hpc, group, heads_per_box, stream);
+        case PAFP8_BF16:
+            return launch_decode_t<PAFP8_BF16>(p, tmap_k, tmap_v, num_ctas, hpc, group, heads_per_box, stream);
+        default:
+            return cudaErrorInvalidValue;
+    }
 }
 
 cudaError_t launch_merge(const DecodeParams& p, int num_merge, int hpc, int group, cudaStream_t stream) {

@@ -56,8 +56,20 @@ const char* dtype_name(int32_t dt) {
 bool is_fp8(int32_t dt) { return dt == PAFP8_E4M3FN || dt == PAFP8_E5M2; }
 bool is_2byte(int32_t dt) { return dt == PAFP8_F16 || dt == PAFP8_BF16; }
 
-pafp8_status check_kv_dtype(int32_t kv, const char* what) {
+// The cache dtype.  fp8 everywhere; a 2-byte cache (f16/bf16) in decode,
+// whose query may be either 2-byte type ("fp8 KV cache in the in-tree prefill
+// kernel", Test plan: decode is exempt from the rule that the cache matches
+// the query), but not with an fp8 query.
+pafp8_status check_kv_dtype(int32_t kv, const char* what, int32_t mode, int32_t q) {
     if (is_fp8(kv)) return PAFP8_OK;
+    if (is_2byte(kv) && mode == PAFP8_MODE_DECODE) {
+        if (is_fp8(q))
+            return fail(PAFP8_ERR_DTYPE,
+                        "%s has dtype %s but q is %s: an fp8 query needs an fp8 cache (the QK "
+                        "product runs on the tensor cores in one operand type)",
+                        what, dtype_name(kv), dtype_name(q));
+        return PAFP8_OK;
+    }
     if (kv == PAFP8_INT8 || kv == PAFP8_UINT8)
         return fail(PAFP8_ERR_DTYPE,
                     "%s has dtype %s: an integer cache has no floating-point reading, and this "
@@ -66,8 +78,8 @@ pafp8_status check_kv_dtype(int32_t kv, const char* what) {
                     what, dtype_name(kv));
     if (is_2byte(kv))
         return fail(PAFP8_ERR_DTYPE,
-                    "%s has dtype %s: a 2-byte KV cache is not served by this build; the cache "
-                    "must be float8_e4m3fn or float8_e5m2",
+                    "%s has dtype %s: a 2-byte KV cache is served in decode only by this build; "
+                    "prefill needs a float8_e4m3fn or float8_e5m2 cache",
                     what, dtype_name(kv));
     if (kv == PAFP8_F32)
         return fail(PAFP8_ERR_DTYPE,
@@ -412,8 +424,50 @@ pafp8_status encode_q_map(CUtensorMap* map, const void* base, int nnz_qo, int hq
 // of the head block, landing head-major ([head][token][128 B]).  If the
 // driver does not accept that dimension order, fall back to one box per head
 // (encode_cache_map); the shared-memory layout is the same either way.
+// A 2-byte cache row (128 elements, 256 B) is split into two 128-B halves so
+// that the 128-byte swizzle applies: dims (d % 64, d / 64, token, head, page)
+// with a box of {64, 2, 16, hpc, 1}, landing per head as 32 rows of 128 B
+// (row 2 * token + half); the fallback is one box per head with dims (d % 64,
+// d / 64, head, token, page) and the same layout.
+pafp8_status encode_decode_maps_2byte(CUtensorMap* tk, CUtensorMap* tv, const void* k, const void* v,
+                                      int num_pages, int hkv, int hpc, int* heads_per_box) {
+    auto enc = get_encode();
+    if (!enc) return fail(PAFP8_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    const cuuint64_t row = (cuuint64_t)kHeadDim * 2;  // bytes of one (token, head) row
+    cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    {
+        cuuint64_t dims[5] = {64, 2, (cuuint64_t)kPageSize, (cuuint64_t)hkv, (cuuint64_t)num_pages};
+        cuuint64_t strides[4] = {128, (cuuint64_t)hkv * row, row, (cuuint64_t)kPageSize * hkv * row};
+        cuuint32_t box[5] = {64, 2, (cuuint32_t)kPageSize, (cuuint32_t)hpc, 1};
+        CUresult rk = enc(tk, CU_TENSOR_MAP_DATA_TYPE_UINT16, 5, const_cast<void*>(k), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        CUresult rv = enc(tv, CU_TENSOR_MAP_DATA_TYPE_UINT16, 5, const_cast<void*>(v), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (rk == CUDA_SUCCESS && rv == CUDA_SUCCESS) {
+            *heads_per_box = hpc;
+            return PAFP8_OK;
+        }
+    }
+    cuuint64_t dims[5] = {64, 2, (cuuint64_t)hkv, (cuuint64_t)kPageSize, (cuuint64_t)num_pages};
+    cuuint64_t strides[4] = {128, row, (cuuint64_t)hkv * row, (cuuint64_t)kPageSize * hkv * row};
+    cuuint32_t box[5] = {64, 2, 1, (cuuint32_t)kPageSize, 1};
+    CUresult rk = enc(tk, CU_TENSOR_MAP_DATA_TYPE_UINT16, 5, const_cast<void*>(k), dims, strides, box, estr,
+                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult rv = enc(tv, CU_TENSOR_MAP_DATA_TYPE_UINT16, 5, const_cast<void*>(v), dims, strides, box, estr,
+                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (rk != CUDA_SUCCESS || rv != CUDA_SUCCESS)
+        return fail(PAFP8_ERR_CUDA, "cuTensorMapEncodeTiled failed for the 2-byte KV cache (CUresult %d, %d)",
+                    (int)rk, (int)rv);
+    *heads_per_box = 1;
+    return PAFP8_OK;
+}
+
 pafp8_status encode_decode_maps(CUtensorMap* tk, CUtensorMap* tv, const void* k, const void* v,
-                                int num_pages, int hkv, int hpc, int* heads_per_box) {
+                                int num_pages, int hkv, int hpc, int* heads_per_box, bool two_byte) {
     if (num_pages == 0 || k == nullptr || v == nullptr) {
         // No request has pages: the kernel issues no copy, the maps are unused.
         memset(tk, 0, sizeof(*tk));
@@ -421,6 +475,7 @@ pafp8_status encode_decode_maps(CUtensorMap* tk, CUtensorMap* tv, const void* k,
         *heads_per_box = 1;
         return PAFP8_OK;
     }
+    if (two_byte) return encode_decode_maps_2byte(tk, tv, k, v, num_pages, hkv, hpc, heads_per_box);
     auto enc = get_encode();
     if (!enc) return fail(PAFP8_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
     cuuint64_t dims[4] = {(cuuint64_t)kHeadDim, (cuuint64_t)kPageSize, (cuuint64_t)hkv,
@@ -468,8 +523,8 @@ pafp8_status pafp8_plan_create(const pafp8_plan_desc* desc_in, const int32_t* kv
         return fail(PAFP8_ERR_ARG, "mode %d is neither decode (0) nor prefill (1)", (int)d.mode);
 
     pafp8_status st;
-    if ((st = check_kv_dtype(d.kv_dtype, "the KV cache")) != PAFP8_OK) return st;
     if ((st = check_q_dtype(d.q_dtype)) != PAFP8_OK) return st;
+    if ((st = check_kv_dtype(d.kv_dtype, "the KV cache", d.mode, d.q_dtype)) != PAFP8_OK) return st;
     if (d.o_dtype == PAFP8_DTYPE_DEFAULT) d.o_dtype = is_2byte(d.q_dtype) ? d.q_dtype : PAFP8_BF16;
     if ((st = check_o_dtype(d.o_dtype, d.q_dtype)) != PAFP8_OK) return st;
 
@@ -631,7 +686,7 @@ pafp8_status pafp8_run_stage(const pafp8_plan* plan, int32_t stage, int32_t q_dt
     if (k_dtype != v_dtype)
         return fail(PAFP8_ERR_DTYPE, "k_cache has dtype %s but v_cache has %s",
                     dtype_name(k_dtype), dtype_name(v_dtype));
-    if ((st = check_kv_dtype(k_dtype, "k_cache")) != PAFP8_OK) return st;
+    if ((st = check_kv_dtype(k_dtype, "k_cache", d.mode, q_dtype)) != PAFP8_OK) return st;
     if ((st = check_q_dtype(q_dtype)) != PAFP8_OK) return st;
     if ((st = check_o_dtype(o_dtype, q_dtype)) != PAFP8_OK) return st;
     if (q_dtype != d.q_dtype)
@@ -726,7 +781,7 @@ pafp8_status pafp8_run_stage(const pafp8_plan* plan, int32_t stage, int32_t q_dt
         CUtensorMap tk, tv;
         int hpb = 1;
         if ((st = encode_decode_maps(&tk, &tv, k_cache, v_cache, d.num_pages, d.num_kv_heads,
-                                     plan->heads_per_cta, &hpb)) != PAFP8_OK)
+                                     plan->heads_per_cta, &hpb, is_2byte(k_dtype))) != PAFP8_OK)
             return st;
         e = launch_decode(p, tk, tv, plan->num_ctas, plan->heads_per_cta, plan->group, hpb, s);
     }
@@ -780,7 +835,7 @@ pafp8_status pafp8_run_decode_noalloc(const pafp8_plan* plan, int32_t q_dtype, c
     if (k_dtype != v_dtype)
         return fail(PAFP8_ERR_DTYPE, "k_cache has dtype %s but v_cache has %s",
                     dtype_name(k_dtype), dtype_name(v_dtype));
-    if ((st = check_kv_dtype(k_dtype, "k_cache")) != PAFP8_OK) return st;
+    if ((st = check_kv_dtype(k_dtype, "k_cache", d.mode, q_dtype)) != PAFP8_OK) return st;
     if ((st = check_q_dtype(q_dtype)) != PAFP8_OK) return st;
     if ((st = check_o_dtype(o_dtype, q_dtype)) != PAFP8_OK) return st;
     if (q_dtype != d.q_dtype || k_dtype != d.kv_dtype || o_dtype != d.o_dtype)
@@ -845,7 +900,7 @@ pafp8_status pafp8_run_decode_noalloc(const pafp8_plan* plan, int32_t q_dtype, c
         CUtensorMap tk, tv;
         int hpb = 1;
         if ((st = encode_decode_maps(&tk, &tv, k_cache, v_cache, d.num_pages, d.num_kv_heads,
-                                     plan->heads_per_cta, &hpb)) != PAFP8_OK)
+                                     plan->heads_per_cta, &hpb, is_2byte(k_dtype))) != PAFP8_OK)
             return st;
         e = launch_decode(p, tk, tv, plan->num_ctas, plan->heads_per_cta, plan->group, hpb, s);
     }

@@ -80,8 +80,10 @@ class PagedBatch:
         return int(self.qo_indptr[-1])
 
     def kv_bytes(self) -> int:
-        """Bytes of K and V the requests own (1 byte per fp8 element)."""
-        return 2 * sum(self.kv_lens) * self.num_kv_heads * self.head_dim
+        """Bytes of K and V the requests own (1 byte per fp8 element, 2 for a
+        2-byte cache)."""
+        esz = 1 if self.kv_dtype in FP8_MAX else 2
+        return 2 * sum(self.kv_lens) * self.num_kv_heads * self.head_dim * esz
 
     def causal_flops(self) -> int:
         """4*D*Hq per admitted (query row, key) pair, causal pairs only."""
@@ -165,14 +167,20 @@ def make_batch(kv_lens: Sequence[int], qo_lens: Optional[Sequence[int]] = None, 
     else:
         q, q_scale = qf.to(TORCH_DTYPES[q_dtype]), 1.0
     del qf
-    kq, k_scale = _quantize(kf, kv_dtype)
-    del kf
-    vq, v_scale = _quantize(vf, kv_dtype)
-    del vf
+    if kv_dtype in FP8_MAX:
+        kq, k_scale = _quantize(kf, kv_dtype)
+        del kf
+        vq, v_scale = _quantize(vf, kv_dtype)
+        del vf
+    else:  # a 2-byte cache holds the values themselves (decode only)
+        kq, k_scale = kf.to(TORCH_DTYPES[kv_dtype]), 1.0
+        vq, v_scale = vf.to(TORCH_DTYPES[kv_dtype]), 1.0
+        del kf, vf
 
     # Pool filled with random codes first; the requests' tokens overwrite
     # their own slots.
-    shape = (pool, P, Hkv, D)
+    esz = 1 if kv_dtype in FP8_MAX else 2
+    shape = (pool, P, Hkv, D * esz)
     k_cache = torch.randint(0, 256, shape, generator=gen, dtype=torch.uint8)
     v_cache = torch.randint(0, 256, shape, generator=gen, dtype=torch.uint8)
     if total_kv:
@@ -183,8 +191,8 @@ def make_batch(kv_lens: Sequence[int], qo_lens: Optional[Sequence[int]] = None, 
             pages = perm[kv_indptr[b]:kv_indptr[b + 1]].to(torch.int64)
             rows[pos:pos + L] = pages[t // P] * P + t % P
             pos += L
-        k_cache.view(pool * P, Hkv, D).index_copy_(0, rows, kq.view(torch.uint8))
-        v_cache.view(pool * P, Hkv, D).index_copy_(0, rows, vq.view(torch.uint8))
+        k_cache.view(pool * P, Hkv, D * esz).index_copy_(0, rows, kq.view(torch.uint8))
+        v_cache.view(pool * P, Hkv, D * esz).index_copy_(0, rows, vq.view(torch.uint8))
     k_cache = k_cache.view(TORCH_DTYPES[kv_dtype])
     v_cache = v_cache.view(TORCH_DTYPES[kv_dtype])
 
@@ -203,11 +211,12 @@ WORKLOADS = {
     3: "long-context decode (B=8, kv 32768, Hq 64/Hkv 8, e5m2 KV with 1% x20 outliers, f16 q/o)",
     4: "ragged causal prefill (B=16, qo U[128,1024], prefix U[0,2048], Hq 32/Hkv 8, e4m3fn KV, bf16 q/o)",
     5: "fp8 x fp8 causal prefill (B=8, qo=kv=2048, Hq 32/Hkv 8, e4m3fn q/KV, bf16 o)",
+    6: "serving batch decode with a 2-byte cache (B=64, kv U[512,4096], Hq 32/Hkv 8, bf16 q/KV/o)",
 }
 
 
 def workload(index: int, *, scale_down: int = 1) -> PagedBatch:
-    """The five named workloads, seed 1000 + index.  ``scale_down`` > 1
+    """The named workloads, seed 1000 + index.  ``scale_down`` > 1
     divides every length (keeping at least one token) for quick runs of the
     same shape mix; it changes the draws, so use it only where the full size
     is not required."""
@@ -241,4 +250,8 @@ def workload(index: int, *, scale_down: int = 1) -> PagedBatch:
         L = shrink([2048] * 8)
         return make_batch(L, L, num_qo_heads=32, num_kv_heads=8, q_dtype="e4m3fn",
                           kv_dtype="e4m3fn", o_dtype="bf16", gen=gen, name="fp8_prefill")
+    if index == 6:
+        kv = torch.randint(512, 4097, (64,), generator=gen).tolist()
+        return make_batch(shrink(kv), num_qo_heads=32, num_kv_heads=8, q_dtype="bf16",
+                          kv_dtype="bf16", o_dtype="bf16", gen=gen, name="serving_decode_bf16_cache")
     raise ValueError(f"unknown workload {index}")

@@ -124,13 +124,36 @@ def _create(**over):
 
 @pytest.mark.parametrize("kv,words", [
     (pa.INT8, ["int8", "integer"]), (pa.UINT8, ["uint8", "integer"]), (pa.F32, ["float32"]),
-    (pa.F16, ["float16", "2-byte"]), (pa.BF16, ["bfloat16", "2-byte"]), (99, ["unknown"])])
+    (99, ["unknown"])])
 def test_plan_refuses_kv_dtype(kv, words):
     with pytest.raises(pa.Pafp8Error) as ei:
         _create(kv_dtype=kv)
     assert ei.value.status == 1
     for w in words:
         assert w in str(ei.value)
+
+
+@pytest.mark.parametrize("kv", [pa.F16, pa.BF16])
+@pytest.mark.parametrize("q", [pa.F16, pa.BF16])
+def test_decode_plan_takes_2byte_cache_with_2byte_query(kv, q):
+    # decode is exempt from the rule that the cache matches the query
+    plan = _create(kv_dtype=kv, q_dtype=q)
+    pa.pafp8_plan_destroy(plan)
+
+
+@pytest.mark.parametrize("kv", [pa.F16, pa.BF16])
+def test_decode_plan_refuses_fp8_query_with_2byte_cache(kv):
+    with pytest.raises(pa.Pafp8Error) as ei:
+        _create(kv_dtype=kv, q_dtype=pa.E4M3FN)
+    assert ei.value.status == 1 and "fp8 query" in str(ei.value)
+
+
+@pytest.mark.parametrize("kv", [pa.F16, pa.BF16])
+def test_prefill_plan_refuses_2byte_cache(kv):
+    with pytest.raises(pa.Pafp8Error) as ei:
+        pa.pafp8_plan_create(_desc(mode=1, kv_dtype=kv), np.array([0, 2], np.int32), np.array([5], np.int32),
+                             np.array([0, 3], np.int32))
+    assert ei.value.status == 1 and "decode only" in str(ei.value)
 
 
 @pytest.mark.parametrize("q", [pa.F32, pa.INT8, pa.UINT8, 42])

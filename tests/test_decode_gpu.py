@@ -3,6 +3,8 @@ element, on seeded inputs (tolerance in gpu_common), plus the bit-exact page
 indexing checks and the named workloads at full size."""
 from __future__ import annotations
 
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -199,3 +201,43 @@ def test_balanced_plan_on_few_ctas_repeats_bitwise(cuda_device):
     db.run()
     o2, l2 = db.result()
     assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+
+
+@pytest.mark.parametrize("q_dtype,kv_dtype,o_dtype", [
+    ("f16", "f16", "f16"), ("bf16", "f16", "bf16"), ("bf16", "bf16", "bf16"), ("f16", "bf16", "f16")])
+def test_2byte_cache(cuda_device, q_dtype, kv_dtype, o_dtype):
+    """A 16-bit cache through the same decode kernel (ragged lengths, splits,
+    every partial-page case), against the oracle."""
+    b = make_batch(RAGGED, num_qo_heads=16, num_kv_heads=4, q_dtype=q_dtype, kv_dtype=kv_dtype,
+                   o_dtype=o_dtype, seed=17, pool_pages=140)
+    o, lse = run_gpu(b, cuda_device, num_ctas=16)
+    ro, rl = oracle_on(b)
+    assert_close(o, lse, ro, rl, f"{q_dtype} q / {kv_dtype} cache")
+
+
+@pytest.mark.parametrize("kv_dtype", ["e4m3fn", "e5m2"])
+@pytest.mark.parametrize("q_dtype", ["f16", "bf16"])
+def test_fp8_cache_equals_its_f16_dequantization_bitwise(cuda_device, kv_dtype, q_dtype):
+    """fp8 codes widen to f16 exactly, and the 2-byte path feeds the tensor
+    cores the same operand words in the same order, so an fp8 cache and its
+    f16 copy (same scales) give bit-identical o and lse, split or not."""
+    b = make_batch(RAGGED, num_qo_heads=16, num_kv_heads=4, q_dtype=q_dtype, kv_dtype=kv_dtype, seed=23,
+                   pool_pages=140)
+    o1, l1 = run_gpu(b, cuda_device, num_ctas=16)
+    b16 = dataclasses.replace(b, kv_dtype="f16", k_cache=b.k_cache.to(torch.float16),
+                              v_cache=b.v_cache.to(torch.float16))
+    o2, l2 = run_gpu(b16, cuda_device, num_ctas=16)
+    assert np.array_equal(o1, o2)
+    assert np.array_equal(l1, l2)
+
+
+def test_2byte_cache_serving_size_sampled(cuda_device):
+    """The serving workload's shape with a bf16 cache (600 MB of KV), sampled
+    outputs against the oracle."""
+    b = workload(6)
+    o, lse = run_gpu(b, cuda_device)
+    g = np.random.default_rng(6)
+    rows = g.integers(0, b.batch, 64)
+    heads = g.integers(0, b.num_qo_heads, 64)
+    ro, rl = oracle_on(b, rows=rows, heads=heads)
+    assert_close(o[rows, heads], lse[rows, heads], ro, rl, "serving decode, bf16 cache")
