@@ -164,7 +164,9 @@ def time_prefill(index, dev, steps, warmup):
     fp8 = b.q_dtype in ("e4m3fn", "e5m2")
     out = {"workload": WORKLOADS[index], "value": round(tflops, 2), "unit": "TFLOP/s",
            "ms_per_launch": round(ms, 5), "flops": flops, "launches": steps,
-           "mma": ("QK^T fp8 kind::f8f6f4, PV f16 kind::f16" if fp8 else "f16 kind::f16 (fp8 KV dequantized)")}
+           "mma": ("QK^T fp8 kind::f8f6f4, PV f16 kind::f16" if fp8 else
+                   "bf16 kind::f16 (2-byte cache, V transposed in shared memory)" if b.kv_dtype in ("f16", "bf16")
+                   else "f16 kind::f16 (fp8 KV dequantized)")}
     if fp8:
         p8 = 2.0 * p16  # another dtype's measured peak x the nominal fp8/bf16 ratio
         blended = 2.0 / (1.0 / p8 + 1.0 / p16)
@@ -491,7 +493,7 @@ def run_ours(args):
     if args.mode == "all":
         del flush
         torch.cuda.empty_cache()
-        for i in (4, 5):
+        for i in (4, 5, 7):
             prefill_res[i] = time_prefill(i, dev, args.prefill_steps, max(3, min(args.warmup, 10)))
         decode16 = time_decode_2byte(dev, min(args.steps, 200), max(3, min(args.warmup, 20)))
 
@@ -531,7 +533,8 @@ def run_ours(args):
         "clocks": clocks,
     }
     if args.mode == "all":
-        line["prefill"] = {"ragged_bf16": prefill_res[4], "fp8_fp8": prefill_res[5]}
+        line["prefill"] = {"ragged_bf16": prefill_res[4], "fp8_fp8": prefill_res[5],
+                           "ragged_bf16_cache": prefill_res[7]}
         line["decode_2byte_cache"] = decode16
     if world == 1 and not args.no_cpu_baseline:
         n = oracle_sample_size(b, 15.0)

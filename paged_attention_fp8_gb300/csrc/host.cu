@@ -56,17 +56,22 @@ const char* dtype_name(int32_t dt) {
 bool is_fp8(int32_t dt) { return dt == PAFP8_E4M3FN || dt == PAFP8_E5M2; }
 bool is_2byte(int32_t dt) { return dt == PAFP8_F16 || dt == PAFP8_BF16; }
 
-// The cache dtype.  fp8 everywhere; a 2-byte cache (f16/bf16) in decode,
-// whose query may be either 2-byte type ("fp8 KV cache in the in-tree prefill
-// kernel", Test plan: decode is exempt from the rule that the cache matches
-// the query), but not with an fp8 query.
+// The cache dtype.  fp8 everywhere; a 2-byte cache (f16/bf16) with a 2-byte
+// query: in decode any mix ("fp8 KV cache in the in-tree prefill kernel",
+// Test plan: decode is exempt from the rule that the cache matches the
+// query), in prefill the query's own dtype; never with an fp8 query.
 pafp8_status check_kv_dtype(int32_t kv, const char* what, int32_t mode, int32_t q) {
     if (is_fp8(kv)) return PAFP8_OK;
-    if (is_2byte(kv) && mode == PAFP8_MODE_DECODE) {
+    if (is_2byte(kv)) {
         if (is_fp8(q))
             return fail(PAFP8_ERR_DTYPE,
                         "%s has dtype %s but q is %s: an fp8 query needs an fp8 cache (the QK "
                         "product runs on the tensor cores in one operand type)",
+                        what, dtype_name(kv), dtype_name(q));
+        if (mode == PAFP8_MODE_PREFILL && kv != q)
+            return fail(PAFP8_ERR_DTYPE,
+                        "%s has dtype %s but q is %s: prefill takes a 2-byte cache only of the "
+                        "query's own dtype (decode accepts either mix)",
                         what, dtype_name(kv), dtype_name(q));
         return PAFP8_OK;
     }
@@ -75,11 +80,6 @@ pafp8_status check_kv_dtype(int32_t kv, const char* what, int32_t mode, int32_t 
                     "%s has dtype %s: an integer cache has no floating-point reading, and this "
                     "library refuses it rather than reading its bytes as fp8 or as 0..255 values; "
                     "the cache must be float8_e4m3fn or float8_e5m2",
-                    what, dtype_name(kv));
-    if (is_2byte(kv))
-        return fail(PAFP8_ERR_DTYPE,
-                    "%s has dtype %s: a 2-byte KV cache is served in decode only by this build; "
-                    "prefill needs a float8_e4m3fn or float8_e5m2 cache",
                     what, dtype_name(kv));
     if (kv == PAFP8_F32)
         return fail(PAFP8_ERR_DTYPE,
@@ -393,6 +393,26 @@ pafp8_status encode_cache_map(CUtensorMap* map, const void* base, int num_pages,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS)
         return fail(PAFP8_ERR_CUDA, "cuTensorMapEncodeTiled failed for the KV cache (CUresult %d)",
+                    (int)r);
+    return PAFP8_OK;
+}
+
+// Prefill map over a 2-byte cache: dims (d % 64, d / 64, token, head, page);
+// one box is one page of one KV head for one 64-dim half, {64, 1, 16, 1, 1},
+// landing as 16 swizzled rows of 128 B (one per token).
+pafp8_status encode_cache_map_2byte(CUtensorMap* map, const void* base, int num_pages, int hkv) {
+    auto enc = get_encode();
+    if (!enc) return fail(PAFP8_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    const cuuint64_t row = (cuuint64_t)kHeadDim * 2;
+    cuuint64_t dims[5] = {64, 2, (cuuint64_t)kPageSize, (cuuint64_t)hkv, (cuuint64_t)num_pages};
+    cuuint64_t strides[4] = {128, (cuuint64_t)hkv * row, row, (cuuint64_t)kPageSize * hkv * row};
+    cuuint32_t box[5] = {64, 1, (cuuint32_t)kPageSize, 1, 1};
+    cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 5, const_cast<void*>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(PAFP8_ERR_CUDA, "cuTensorMapEncodeTiled failed for the 2-byte KV cache (CUresult %d)",
                     (int)r);
     return PAFP8_OK;
 }
@@ -749,8 +769,13 @@ pafp8_status pafp8_run_stage(const pafp8_plan* plan, int32_t stage, int32_t q_dt
         if ((st = encode_q_map(&tq, q, (int)plan->nnz_qo, d.num_qo_heads, plan->group,
                                pp.tile_tokens, is_fp8(q_dtype))) != PAFP8_OK)
             return st;
-        if ((st = encode_cache_map(&tk, k_cache, d.num_pages, d.num_kv_heads)) != PAFP8_OK) return st;
-        if ((st = encode_cache_map(&tv, v_cache, d.num_pages, d.num_kv_heads)) != PAFP8_OK) return st;
+        if (is_2byte(k_dtype)) {
+            if ((st = encode_cache_map_2byte(&tk, k_cache, d.num_pages, d.num_kv_heads)) != PAFP8_OK) return st;
+            if ((st = encode_cache_map_2byte(&tv, v_cache, d.num_pages, d.num_kv_heads)) != PAFP8_OK) return st;
+        } else {
+            if ((st = encode_cache_map(&tk, k_cache, d.num_pages, d.num_kv_heads)) != PAFP8_OK) return st;
+            if ((st = encode_cache_map(&tv, v_cache, d.num_pages, d.num_kv_heads)) != PAFP8_OK) return st;
+        }
         cudaError_t e = launch_prefill(pp, tq, tk, tv, plan->num_ctas, s);
         if (e != cudaSuccess) {
             cudaGetLastError();

@@ -64,20 +64,23 @@ constexpr uint32_t kRawTile = kTileKeys * D;      // 16 KB of fp8
 constexpr uint32_t kHalfTile = kTileKeys * 128;  // 16 KB: 128 rows x 128 B
 constexpr uint32_t kF16Tile = 2 * kHalfTile;       // 32 KB of f16
 
-template <bool kF8>
+template <bool kF8, bool k2 = false>
 struct Layout {
     // The 2-byte-query path spends its shared memory on two f16 K tiles (the
     // dequant of K_{j+1} may start while QK_B(j) still reads K_j) and keeps a
     // single raw fp8 stage per tensor; the fp8 path multiplies raw K directly.
-    static constexpr int NKR = kF8 ? 4 : 1;    // raw K stages
-    static constexpr int NVR = kF8 ? 2 : 1;    // raw V stages
+    // A 2-byte cache (k2) brings K straight into the 16-bit K tiles and only
+    // transposes V, so it has no raw K stage and a 2-byte raw V stage.
+    static constexpr int NKR = kF8 ? 4 : (k2 ? 0 : 1);  // raw K stages
+    static constexpr int NVR = kF8 ? 2 : 1;             // raw V stages
+    static constexpr uint32_t kRawV = k2 ? kF16Tile : kRawTile;
     static constexpr int NK16 = kF8 ? 0 : 2;   // f16 K stages
     static constexpr int NV16 = 2;             // f16 V^T stages
     static constexpr uint32_t kQTile = kF8 ? kHalfTile : kF16Tile;
     static constexpr uint32_t q = 0;                     // Q_A, then Q_B
     static constexpr uint32_t kr = 2 * kQTile;
     static constexpr uint32_t vr = kr + NKR * kRawTile;
-    static constexpr uint32_t k16 = vr + NVR * kRawTile;
+    static constexpr uint32_t k16 = vr + NVR * kRawV;
     static constexpr uint32_t v16 = k16 + NK16 * kF16Tile;
     static constexpr uint32_t bars = v16 + NV16 * kF16Tile;
     // barrier indices (8 bytes each)
@@ -98,6 +101,7 @@ struct Layout {
 };
 static_assert(1024 + Layout<false>::bytes <= 232448, "shared memory budget (2-byte query)");
 static_assert(1024 + Layout<true>::bytes <= 232448, "shared memory budget (fp8 query)");
+static_assert(1024 + Layout<false, true>::bytes <= 232448, "shared memory budget (2-byte cache)");
 
 struct Ring {
     int idx = 0;
@@ -163,7 +167,9 @@ template <bool kF8, int KT>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_constant__ CUtensorMap tmq,
                    const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv) {
-    using L = Layout<kF8>;
+    constexpr bool k2 = KT == PAFP8_F16 || KT == PAFP8_BF16;  // 2-byte cache, same dtype as q
+    constexpr bool kBF = KT == PAFP8_BF16;                    // bf16 MMA operands
+    using L = Layout<kF8, k2>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t base = (smem_addr(smem_raw) + 1023u) & ~1023u;
     auto bar = [&](int i) -> uint32_t { return base + L::bars + 8u * (uint32_t)i; };
@@ -188,7 +194,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar(L::bVrEmpty + i), 128);
         }
         for (int i = 0; i < L::NK16; ++i) {
-            mbar_init(bar(L::bK16Full + i), 128);
+            mbar_init(bar(L::bK16Full + i), k2 ? 1 : 128);  // TMA, or the dequant warps
             mbar_init(bar(L::bK16Empty + i), 1);
         }
         for (int i = 0; i < L::NV16; ++i) {
@@ -224,9 +230,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             prefetch_tmap(&tmk);
             prefetch_tmap(&tmv);
         }
-        Ring kr, vr;
+        Ring kr, vr;  // kr: raw K ring, or the 16-bit K ring for a 2-byte cache
         uint32_t qphase = 0;
         long long issued_k = 0, issued_v = 0, issued_q = 0;
+        constexpr int nkr = k2 ? L::NK16 : L::NKR;
+        constexpr int bkf = k2 ? L::bK16Full : L::bKrFull, bke = k2 ? L::bK16Empty : L::bKrEmpty;
         bool ok = true;
         for (int t = blockIdx.x; t < n_items && ok; t += gridDim.x) {
             const Item it = load_item(items, t);
@@ -278,27 +286,44 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int i = 0; i < 8; ++i) pages[i] = __shfl_sync(0xFFFFFFFFu, page, i);
                 if (lane == 0) {
-                    ok = wait_or_abort(bar(L::bKrEmpty + kr.idx), kr.phase ^ 1u, flag_addr, p.status);
+                    ok = wait_or_abort(bar(bke + kr.idx), kr.phase ^ 1u, flag_addr, p.status);
                     if (ok) {
-                        const uint32_t fb = bar(L::bKrFull + kr.idx);
-                        const uint32_t dst = base + L::kr + kr.idx * kRawTile;
-                        mbar_arrive_expect_tx(fb, (uint32_t)np * kPageSize * D);
-                        for (int i = 0; i < np; ++i)
-                            tma_load_4d(dst + i * 2048u, &tmk, fb, 0, it.hk, 0, pages[i]);
+                        const uint32_t fb = bar(bkf + kr.idx);
+                        if (k2) {
+                            // Each page as two boxes (dims 0-63, 64-127) into the two
+                            // halves of the 16-bit K tile: [half][key][128 B].
+                            const uint32_t dst = base + L::k16 + kr.idx * kF16Tile;
+                            mbar_arrive_expect_tx(fb, (uint32_t)np * kPageSize * D * 2);
+                            for (int i = 0; i < np; ++i)
+                                for (int h = 0; h < 2; ++h)
+                                    tma_load_5d(dst + h * kHalfTile + i * 2048u, &tmk, fb, 0, h, 0, it.hk, pages[i]);
+                        } else {
+                            const uint32_t dst = base + L::kr + kr.idx * kRawTile;
+                            mbar_arrive_expect_tx(fb, (uint32_t)np * kPageSize * D);
+                            for (int i = 0; i < np; ++i)
+                                tma_load_4d(dst + i * 2048u, &tmk, fb, 0, it.hk, 0, pages[i]);
+                        }
                         ++issued_k;
                     }
                 }
                 ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
                 if (!ok) break;
-                kr.next(L::NKR);
+                kr.next(nkr);
                 if (lane == 0) {
                     ok = wait_or_abort(bar(L::bVrEmpty + vr.idx), vr.phase ^ 1u, flag_addr, p.status);
                     if (ok) {
                         const uint32_t fb = bar(L::bVrFull + vr.idx);
-                        const uint32_t dst = base + L::vr + vr.idx * kRawTile;
-                        mbar_arrive_expect_tx(fb, (uint32_t)np * kPageSize * D);
-                        for (int i = 0; i < np; ++i)
-                            tma_load_4d(dst + i * 2048u, &tmv, fb, 0, it.hk, 0, pages[i]);
+                        const uint32_t dst = base + L::vr + vr.idx * L::kRawV;
+                        if (k2) {
+                            mbar_arrive_expect_tx(fb, (uint32_t)np * kPageSize * D * 2);
+                            for (int i = 0; i < np; ++i)
+                                for (int h = 0; h < 2; ++h)
+                                    tma_load_5d(dst + h * kHalfTile + i * 2048u, &tmv, fb, 0, h, 0, it.hk, pages[i]);
+                        } else {
+                            mbar_arrive_expect_tx(fb, (uint32_t)np * kPageSize * D);
+                            for (int i = 0; i < np; ++i)
+                                tma_load_4d(dst + i * 2048u, &tmv, fb, 0, it.hk, 0, pages[i]);
+                        }
                         ++issued_v;
                     }
                 }
@@ -309,8 +334,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             // Let every copy issued by this CTA land before it may exit.
             if (issued_q > 0) mbar_wait(bar(L::bQFull), (uint32_t)((issued_q - 1) & 1));
-            for (int s = 0; s < L::NKR && s < issued_k; ++s)
-                mbar_wait(bar(L::bKrFull + s), (uint32_t)(((issued_k - 1 - s) / L::NKR) & 1));
+            for (int s = 0; s < nkr && s < issued_k; ++s)
+                mbar_wait(bar(bkf + s), (uint32_t)(((issued_k - 1 - s) / nkr) & 1));
             for (int s = 0; s < L::NVR && s < issued_v; ++s)
                 mbar_wait(bar(L::bVrFull + s), (uint32_t)(((issued_v - 1 - s) / L::NVR) & 1));
         }
@@ -319,8 +344,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             const uint32_t idesc_qk =
                 kF8 ? make_idesc(p.q_dtype == PAFP8_E5M2 ? 1 : 0, KT == PAFP8_E5M2 ? 1 : 0, 128, 128)
-                    : make_idesc(0, 0, 128, 128);
-            const uint32_t idesc_pv = make_idesc(0, 0, 128, 128);
+                    : make_idesc(kBF ? 1 : 0, kBF ? 1 : 0, 128, 128);
+            const uint32_t idesc_pv = make_idesc(kBF ? 1 : 0, kBF ? 1 : 0, 128, 128);
             const int nk = kF8 ? L::NKR : L::NK16;
             const int kfull = kF8 ? L::bKrFull : L::bK16Full;
             const int kempty = kF8 ? L::bKrEmpty : L::bK16Empty;
@@ -443,7 +468,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int kv_len = it.kv_len;
             for (int j = 0; j < it.nkv && ok; ++j) {
                 const int valid = min(kTileKeys, kv_len - j * kTileKeys);
-                if (!kF8) {
+                if constexpr (!kF8 && !k2) {
                     ok = wait_or_abort(bar(L::bKrFull + kr.idx), kr.phase, flag_addr, p.status) &&
                          wait_or_abort(bar(L::bK16Empty + k16.idx), k16.phase ^ 1u, flag_addr, p.status);
                     if (!ok) break;
@@ -470,8 +495,34 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ok = wait_or_abort(bar(L::bVrFull + vr.idx), vr.phase, flag_addr, p.status) &&
                      wait_or_abort(bar(L::bV16Empty + v16.idx), v16.phase ^ 1u, flag_addr, p.status);
                 if (!ok) break;
-                const uint32_t src = base + L::vr + vr.idx * kRawTile;
+                const uint32_t src = base + L::vr + vr.idx * L::kRawV;
                 const uint32_t dst = base + L::v16 + v16.idx * kF16Tile;
+                if constexpr (k2) {
+                    // 16-bit V [half][key][128 B] -> V^T [key half][dim][128 B], by
+                    // 8x8 tiles (8 keys x 8 dims) transposed in ldmatrix: warp wd
+                    // takes key blocks 4wd .. 4wd+3, all 16 dim blocks; keys past the
+                    // request's end are zeroed.
+                    const int tr = lane & 7, tm = lane >> 3;
+#pragma unroll 1
+                    for (int ab = 0; ab < 16; ++ab) {
+                        const int a = 4 * wd + (ab >> 2), b = 4 * (ab & 3) + tm;  // this lane's source tile
+                        const int key_row = 8 * a + tr;
+                        uint32_t w[4];
+                        ldsm_x4_trans(src + (b >> 3) * kHalfTile + key_row * 128 + (((b & 7) ^ tr) << 4), w[0], w[1],
+                                      w[2], w[3]);
+                        const int k0 = 8 * a + 2 * (lane & 3);  // keys k0, k0+1 of word m
+#pragma unroll
+                        for (int m = 0; m < 4; ++m) {
+                            const int bm = 4 * (ab & 3) + m;
+                            const int dim = 8 * bm + (lane >> 2);
+                            uint32_t x = w[m];
+                            if (k0 >= valid) x &= 0xFFFF0000u;
+                            if (k0 + 1 >= valid) x &= 0x0000FFFFu;
+                            sts32(dst + (a >> 3) * kHalfTile + dim * 128 + (((a & 7) ^ (dim & 7)) << 4) + 4 * (lane & 3),
+                                  x);
+                        }
+                    }
+                } else {
                 const int kb = e + 8 * (q8 >> 1);  // key block (8 keys)
 #pragma unroll 1
                 for (int rr = 0; rr < 2; ++rr) {
@@ -510,6 +561,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         sts128(hb + row * 128 + (((kb & 7) ^ d) << 4), T[d][0], T[d][1], T[d][2], T[d][3]);
                     }
                 }
+                }
                 fence_async_smem();
                 mbar_arrive(bar(L::bV16Full + v16.idx));
                 mbar_arrive(bar(L::bVrEmpty + vr.idx));
@@ -541,7 +593,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ok = __all_sync(0xFFFFFFFFu, wait_or_abort(bar(L::bQFull), qphase, flag_addr, p.status));
                 qphase ^= 1u;
                 if (!ok) break;
-                if (p.q_dtype == PAFP8_BF16 && r < TQ * g) {
+                if (!k2 && p.q_dtype == PAFP8_BF16 && r < TQ * g) {
                     // Bring the row into f16 range by an exact power of two.
                     const uint32_t qrow = base + L::q + x * L::kQTile + r * 128;
                     uint32_t mx = 0;
@@ -658,7 +710,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const float e0 = ex2(a), e1 = ex2(b);
                     const f32x2 e = make_f32x2(e0, e1);
                     ps[i & 1] = add2(ps[i & 1], e);
-                    v[i] = pack_half2(e0, e1);
+                    v[i] = kBF ? pack_bf162(e0, e1) : pack_half2(e0, e1);
                 }
                 {
                     float a, b, c, d;
@@ -718,7 +770,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <bool kF8, int KT>
 cudaError_t launch_one(const PrefillParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
                        const CUtensorMap& tv, int num_ctas, cudaStream_t stream) {
-    const size_t smem = 1024 + Layout<kF8>::bytes;
+    const size_t smem = 1024 + Layout<kF8, KT == PAFP8_F16 || KT == PAFP8_BF16>::bytes;
     cudaError_t e = cudaFuncSetAttribute(prefill_kernel<kF8, KT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
@@ -735,9 +787,13 @@ cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& tmap_q, co
         return p.kv_dtype == PAFP8_E4M3FN
                    ? launch_one<true, PAFP8_E4M3FN>(p, tmap_q, tmap_k, tmap_v, num_ctas, stream)
                    : launch_one<true, PAFP8_E5M2>(p, tmap_q, tmap_k, tmap_v, num_ctas, stream);
-    return p.kv_dtype == PAFP8_E4M3FN
-               ? launch_one<false, PAFP8_E4M3FN>(p, tmap_q, tmap_k, tmap_v, num_ctas, stream)
-               : launch_one<false, PAFP8_E5M2>(p, tmap_q, tmap_k, tmap_v, num_ctas, stream);
+    switch (p.kv_dtype) {
+        case PAFP8_E4M3FN: return launch_one<false, PAFP8_E4M3FN>(p, tmap_q, tmap_k, tmap_v, num_ctas, stream);
+        case PAFP8_E5M2: return launch_one<false, PAFP8_E5M2>(p, tmap_q, tmap_k, tmap_v, num_ctas, stream);
+        case PAFP8_F16: return launch_one<false, PAFP8_F16>(p, tmap_q, tmap_k, tmap_v, num_ctas, stream);
+        case PAFP8_BF16: return launch_one<false, PAFP8_BF16>(p, tmap_q, tmap_k, tmap_v, num_ctas, stream);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace pafp8

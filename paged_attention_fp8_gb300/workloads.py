@@ -212,6 +212,7 @@ WORKLOADS = {
     4: "ragged causal prefill (B=16, qo U[128,1024], prefix U[0,2048], Hq 32/Hkv 8, e4m3fn KV, bf16 q/o)",
     5: "fp8 x fp8 causal prefill (B=8, qo=kv=2048, Hq 32/Hkv 8, e4m3fn q/KV, bf16 o)",
     6: "serving batch decode with a 2-byte cache (B=64, kv U[512,4096], Hq 32/Hkv 8, bf16 q/KV/o)",
+    7: "ragged causal prefill with a 2-byte cache (B=16, qo U[128,1024], prefix U[0,2048], Hq 32/Hkv 8, bf16 q/KV/o)",
 }
 
 
@@ -254,4 +255,12 @@ def workload(index: int, *, scale_down: int = 1) -> PagedBatch:
         kv = torch.randint(512, 4097, (64,), generator=gen).tolist()
         return make_batch(shrink(kv), num_qo_heads=32, num_kv_heads=8, q_dtype="bf16",
                           kv_dtype="bf16", o_dtype="bf16", gen=gen, name="serving_decode_bf16_cache")
+    if index == 7:
+        qo = torch.randint(128, 1025, (16,), generator=gen).tolist()
+        prefix = torch.randint(0, 2049, (16,), generator=gen).tolist()
+        qo = shrink(qo)
+        prefix = [p // sd for p in prefix]
+        kv = [a + b for a, b in zip(qo, prefix)]
+        return make_batch(kv, qo, num_qo_heads=32, num_kv_heads=8, q_dtype="bf16",
+                          kv_dtype="bf16", o_dtype="bf16", gen=gen, name="ragged_prefill_bf16_cache")
     raise ValueError(f"unknown workload {index}")

@@ -148,12 +148,19 @@ def test_decode_plan_refuses_fp8_query_with_2byte_cache(kv):
     assert ei.value.status == 1 and "fp8 query" in str(ei.value)
 
 
-@pytest.mark.parametrize("kv", [pa.F16, pa.BF16])
-def test_prefill_plan_refuses_2byte_cache(kv):
+@pytest.mark.parametrize("q,kv", [(pa.F16, pa.BF16), (pa.BF16, pa.F16)])
+def test_prefill_plan_refuses_2byte_cache_of_another_dtype(q, kv):
     with pytest.raises(pa.Pafp8Error) as ei:
-        pa.pafp8_plan_create(_desc(mode=1, kv_dtype=kv), np.array([0, 2], np.int32), np.array([5], np.int32),
-                             np.array([0, 3], np.int32))
-    assert ei.value.status == 1 and "decode only" in str(ei.value)
+        pa.pafp8_plan_create(_desc(mode=1, q_dtype=q, kv_dtype=kv), np.array([0, 2], np.int32),
+                             np.array([5], np.int32), np.array([0, 3], np.int32))
+    assert ei.value.status == 1 and "own dtype" in str(ei.value)
+
+
+@pytest.mark.parametrize("kv", [pa.F16, pa.BF16])
+def test_prefill_plan_takes_2byte_cache_of_the_query_dtype(kv):
+    plan = pa.pafp8_plan_create(_desc(mode=1, q_dtype=kv, kv_dtype=kv), np.array([0, 2], np.int32),
+                                np.array([5], np.int32), np.array([0, 3], np.int32))
+    pa.pafp8_plan_destroy(plan)
 
 
 @pytest.mark.parametrize("q", [pa.F32, pa.INT8, pa.UINT8, 42])

@@ -134,3 +134,31 @@ def test_fp8_output_refused(cuda_device):
             kv_indptr=b.kv_indptr, last_page_len=b.last_page_len, qo_indptr=b.qo_indptr,
             q_dtype="e4m3fn", kv_dtype="e4m3fn", o_dtype="e4m3fn")
     assert ei.value.status == 1 and "float8_e4m3fn" in str(ei.value)
+
+
+@pytest.mark.parametrize("dt", ["f16", "bf16"])
+@pytest.mark.parametrize("kv,qo", [([260, 77], [200, 77]), ([129, 128, 127, 1000], [129, 1, 100, 333])])
+def test_2byte_cache_of_the_query_dtype(cuda_device, dt, kv, qo):
+    """A 16-bit cache of the query's dtype: K tiles come in by TMA as they
+    are, V is transposed in shared memory; ragged rows, partial tiles."""
+    b = make_batch(kv, qo, num_qo_heads=16, num_kv_heads=4, q_dtype=dt, kv_dtype=dt, o_dtype=dt,
+                   seed=29 + len(kv))
+    o, lse = run_gpu(b, cuda_device, num_ctas=11)
+    ro, rl = oracle_on(b)
+    assert_close(o, lse, ro, rl, f"prefill {dt} cache {kv}/{qo}")
+
+
+@pytest.mark.parametrize("kv_dtype", ["e4m3fn", "e5m2"])
+def test_fp8_cache_equals_its_f16_dequantization_bitwise(cuda_device, kv_dtype):
+    """With an f16 query, the fp8 path dequantizes into the same f16 K and
+    V^T tiles the 2-byte path builds from the widened cache, so both give
+    bit-identical o and lse."""
+    import dataclasses
+    b = make_batch([260, 77, 1000], [200, 77, 150], num_qo_heads=16, num_kv_heads=4, q_dtype="f16",
+                   kv_dtype=kv_dtype, o_dtype="f16", seed=31)
+    o1, l1 = run_gpu(b, cuda_device, num_ctas=11)
+    b16 = dataclasses.replace(b, kv_dtype="f16", k_cache=b.k_cache.to(torch.float16),
+                              v_cache=b.v_cache.to(torch.float16))
+    o2, l2 = run_gpu(b16, cuda_device, num_ctas=11)
+    assert np.array_equal(o1, o2)
+    assert np.array_equal(l1, l2)
