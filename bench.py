@@ -57,12 +57,12 @@ L2_FLUSH_BYTES = 256 << 20
 # changed kernel reports null until it is captured again.
 NCU_TRAFFIC = {
     # profiles/decode_kernel_serving_decode.md
-    "00b491a4f458ec81a015407acf80532fbb30ecce2b5d02d3c23338ca98337e0e": 310217472,
+    "d1459b7d4ca07482bda116b489374c18a7a37d5042caf4f03a7bcf217a31c79e": 309701120,
 }
 # The same for the prefill kernel, per workload index, keyed by the SHA-256
 # of its source (profiles/prefill_kernel_ragged_bf16_and_fp8.md).
 NCU_TRAFFIC_PREFILL = {
-    "c78441c474bd12dd5fd4d527e566d3b5ca5c51b2acf5ec57f55f200481616c23": {4: 165958656, 5: 187395840},
+    "52d43204539250f62b39b005dd0bb17822a72879bc01d45cc680de39bde8e58f": {4: 165803264, 5: 188006400},
 }
 
 
