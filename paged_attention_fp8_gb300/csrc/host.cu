@@ -776,7 +776,11 @@ pafp8_status pafp8_run_stage(const pafp8_plan* plan, int32_t stage, int32_t q_dt
             if ((st = encode_cache_map(&tk, k_cache, d.num_pages, d.num_kv_heads)) != PAFP8_OK) return st;
             if ((st = encode_cache_map(&tv, v_cache, d.num_pages, d.num_kv_heads)) != PAFP8_OK) return st;
         }
-        cudaError_t e = launch_prefill(pp, tq, tk, tv, plan->num_ctas, s);
+        CUtensorMap to;
+        if ((st = encode_q_map(&to, o, (int)plan->nnz_qo, d.num_qo_heads, plan->group, pp.tile_tokens,
+                               false)) != PAFP8_OK)
+            return st;
+        cudaError_t e = launch_prefill(pp, tq, tk, tv, to, plan->num_ctas, s);
         if (e != cudaSuccess) {
             cudaGetLastError();
             return fail(PAFP8_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(e));

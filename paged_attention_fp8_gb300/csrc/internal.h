@@ -99,8 +99,10 @@ cudaError_t noalloc_scratch(void** ptr);
 
 cudaError_t launch_merge(const DecodeParams& p, int num_merge, int heads_per_cta, int group,
                          cudaStream_t stream);
+// tmap_o: map over o with the 2-byte query tile's box (the fp8-query kernel
+// writes full output tiles with bulk tensor stores through it).
 cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& tmap_q,
-                           const CUtensorMap& tmap_k, const CUtensorMap& tmap_v, int num_ctas,
-                           cudaStream_t stream);
+                           const CUtensorMap& tmap_k, const CUtensorMap& tmap_v,
+                           const CUtensorMap& tmap_o, int num_ctas, cudaStream_t stream);
 
 }  // namespace pafp8

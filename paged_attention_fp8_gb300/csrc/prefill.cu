@@ -82,7 +82,10 @@ struct Layout {
     static constexpr uint32_t vr = kr + NKR * kRawTile;
     static constexpr uint32_t k16 = vr + NVR * kRawV;
     static constexpr uint32_t v16 = k16 + NK16 * kF16Tile;
-    static constexpr uint32_t bars = v16 + NV16 * kF16Tile;
+    // fp8 query: a 16 KB staging half per query tile for the output's bulk
+    // tensor stores (64 dims of 128 rows, swizzled like the Q tile).
+    static constexpr uint32_t ostage = v16 + NV16 * kF16Tile;
+    static constexpr uint32_t bars = ostage + (kF8 ? 2 * kHalfTile : 0);
     // barrier indices (8 bytes each)
     static constexpr int bQFull = 0, bQReady = 1, bQEmpty = 2;
     static constexpr int bKrFull = 3, bKrEmpty = bKrFull + NKR;
@@ -93,7 +96,9 @@ struct Layout {
     static constexpr int bPFull = bSFull + 2;        // [2]
     static constexpr int bOFull = bPFull + 2;        // [2]
     static constexpr int bOEmpty = bOFull + 2;       // [2]
-    static constexpr int bDrain = bOEmpty + 2;
+    static constexpr int bStageFree = bOEmpty + 2;    // [2]
+    static constexpr int bStageReady = bStageFree + 2;  // [2]
+    static constexpr int bDrain = bStageReady + 2;
     static constexpr int nBars = bDrain + 1;
     static constexpr uint32_t tmem_slot = bars + 8 * nBars;
     static constexpr uint32_t abort_flag = tmem_slot + 4;
@@ -166,7 +171,8 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, uin
 template <bool kF8, int KT>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_constant__ CUtensorMap tmq,
-                   const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv) {
+                   const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
+                   const __grid_constant__ CUtensorMap tmo) {
     constexpr bool k2 = KT == PAFP8_F16 || KT == PAFP8_BF16;  // 2-byte cache, same dtype as q
     constexpr bool kBF = KT == PAFP8_BF16;                    // bf16 MMA operands
     using L = Layout<kF8, k2>;
@@ -206,6 +212,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar(L::bPFull + x), 128);
             mbar_init(bar(L::bOFull + x), 1);
             mbar_init(bar(L::bOEmpty + x), 128);
+            mbar_init(bar(L::bStageFree + x), 1);
+            mbar_init(bar(L::bStageReady + x), 128);
         }
         mbar_init(bar(L::bDrain), 1);
         asm volatile("st.shared.u32 [%0], 0;" ::"r"(flag_addr) : "memory");
@@ -577,6 +585,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t lane_base = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
         const uint32_t tS = lane_base + col_s(x), tO = lane_base + col_o(x);
         uint32_t qphase = 0, sphase = 0, ophase = 0;
+        uint32_t stage_round = 0;  // staging rounds of this tile so far (fp8 query)
+        const bool issuer = (threadIdx.x & 127) == 0;
         bool ok = true;
         for (int t = blockIdx.x; t < n_items && ok; t += gridDim.x) {
             const Item it = load_item(items, t);
@@ -733,6 +743,58 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             const float inv = valid_row && l > 0.f ? p.v_scale / l : 0.f;
             const size_t orow = (size_t)(qo0 + t0 + tok) * p.num_qo_heads + (size_t)it.hk * g + hh;
+            if (kF8 && t0 + TQ <= qo_len) {
+                // A full tile: two rounds of 64 dims through this tile's staging
+                // half, each written out by one bulk tensor store (asynchronous;
+                // the next round waits until the store has read the staging).
+                const uint32_t stg = base + L::ostage + (uint32_t)x * kHalfTile;
+                bool sok = true;
+#pragma unroll 1
+                for (int h = 0; h < 2 && sok; ++h, ++stage_round) {
+                    uint32_t v[64];
+                    tc_ld32(tO + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(v));
+                    tc_ld32(tO + 64 * h + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
+                    tc_wait_ld();
+                    if (h == 1) {
+                        // O_X is read: release it to the next item's first PV.
+                        tc_fence_before();
+                        mbar_arrive(bar(L::bOEmpty + x));
+                    }
+                    uint32_t w[32];
+                    const f32x2 inv2 = make_f32x2(inv, inv);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        float a0, a1;
+                        split_f32x2(mul2(make_f32x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1])), inv2),
+                                    a0, a1);
+                        w[i] = pack_out2(a0, a1, p.o_dtype);
+                    }
+                    if (issuer) {
+                        bulk_wait_read_all();
+                        mbar_arrive(bar(L::bStageFree + x));
+                    }
+                    sok = __all_sync(0xFFFFFFFFu, wait_or_abort(bar(L::bStageFree + x), stage_round & 1u, flag_addr,
+                                                                p.status));
+                    if (!sok) break;
+#pragma unroll
+                    for (int c = 0; c < 8; ++c)
+                        sts128(stg + r * 128 + ((c ^ (r & 7)) << 4), w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+                    fence_async_smem();
+                    mbar_arrive(bar(L::bStageReady + x));
+                    if (issuer) {
+                        sok = wait_or_abort(bar(L::bStageReady + x), stage_round & 1u, flag_addr, p.status);
+                        if (sok) {
+                            tma_store_3d(&tmo, stg, 64 * h, it.hk * g, qo0 + t0);
+                            bulk_commit();
+                        }
+                    }
+                    sok = __all_sync(0xFFFFFFFFu, sok);
+                }
+                ok = sok;
+                if (!ok) break;
+                if (valid_row && p.lse != nullptr) p.lse[orow] = (m + __log2f(l)) * 0.69314718055994531f;
+                continue;
+            }
 #pragma unroll 1
             for (int c = 0; c < 4; ++c) {
                 uint32_t v[32];
@@ -759,6 +821,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
 
+    if (kF8 && (warp == 4 || warp == 8) && lane == 0) bulk_wait_all();  // this thread's output stores
     tc_fence_before();
     __syncthreads();
     if (warp == 13) {
@@ -769,29 +832,30 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <bool kF8, int KT>
 cudaError_t launch_one(const PrefillParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
-                       const CUtensorMap& tv, int num_ctas, cudaStream_t stream) {
+                       const CUtensorMap& tv, const CUtensorMap& to, int num_ctas, cudaStream_t stream) {
     const size_t smem = 1024 + Layout<kF8, KT == PAFP8_F16 || KT == PAFP8_BF16>::bytes;
     cudaError_t e = cudaFuncSetAttribute(prefill_kernel<kF8, KT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    prefill_kernel<kF8, KT><<<num_ctas, kThreads, smem, stream>>>(p, tq, tk, tv);
+    prefill_kernel<kF8, KT><<<num_ctas, kThreads, smem, stream>>>(p, tq, tk, tv, to);
     return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& tmap_q, const CUtensorMap& tmap_k,
-                           const CUtensorMap& tmap_v, int num_ctas, cudaStream_t stream) {
+                           const CUtensorMap& tmap_v, const CUtensorMap& tmap_o, int num_ctas,
+                           cudaStream_t stream) {
     const bool f8 = p.q_dtype == PAFP8_E4M3FN || p.q_dtype == PAFP8_E5M2;
     if (f8)
         return p.kv_dtype == PAFP8_E4M3FN
-                   ? launch_one<true, PAFP8_E4M3FN>(p, tmap_q, tmap_k, tmap_v, num_ctas, stream)
-                   : launch_one<true, PAFP8_E5M2>(p, tmap_q, tmap_k, tmap_v, num_ctas, stream);
+                   ? launch_one<true, PAFP8_E4M3FN>(p, tmap_q, tmap_k, tmap_v, tmap_o, num_ctas, stream)
+                   : launch_one<true, PAFP8_E5M2>(p, tmap_q, tmap_k, tmap_v, tmap_o, num_ctas, stream);
     switch (p.kv_dtype) {
-        case PAFP8_E4M3FN: return launch_one<false, PAFP8_E4M3FN>(p, tmap_q, tmap_k, tmap_v, num_ctas, stream);
-        case PAFP8_E5M2: return launch_one<false, PAFP8_E5M2>(p, tmap_q, tmap_k, tmap_v, num_ctas, stream);
-        case PAFP8_F16: return launch_one<false, PAFP8_F16>(p, tmap_q, tmap_k, tmap_v, num_ctas, stream);
-        case PAFP8_BF16: return launch_one<false, PAFP8_BF16>(p, tmap_q, tmap_k, tmap_v, num_ctas, stream);
+        case PAFP8_E4M3FN: return launch_one<false, PAFP8_E4M3FN>(p, tmap_q, tmap_k, tmap_v, tmap_o, num_ctas, stream);
+        case PAFP8_E5M2: return launch_one<false, PAFP8_E5M2>(p, tmap_q, tmap_k, tmap_v, tmap_o, num_ctas, stream);
+        case PAFP8_F16: return launch_one<false, PAFP8_F16>(p, tmap_q, tmap_k, tmap_v, tmap_o, num_ctas, stream);
+        case PAFP8_BF16: return launch_one<false, PAFP8_BF16>(p, tmap_q, tmap_k, tmap_v, tmap_o, num_ctas, stream);
         default: return cudaErrorInvalidValue;
     }
 }
