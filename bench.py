@@ -62,7 +62,7 @@ NCU_TRAFFIC = {
 # The same for the prefill kernel, per workload index, keyed by the SHA-256
 # of its source (profiles/prefill_kernel_ragged_bf16_and_fp8.md).
 NCU_TRAFFIC_PREFILL = {
-    "52d43204539250f62b39b005dd0bb17822a72879bc01d45cc680de39bde8e58f": {4: 165803264, 5: 188006400},
+    "b1072fc59ae620fb833bb535cbdbf2926e1b5806cd9813424f28e01ee6eb8483": {4: 165543936, 5: 192773888},
 }
 
 
