@@ -28,8 +28,10 @@
 //               the running max and sum, writes P (f16) over the first half of
 //               S in TMEM, rescales O in TMEM only when the max rises by more
 //               than 2^8, and in the epilogue normalizes O and stores o, lse.
-//               With a bf16 query each thread first brings its Q row into f16
-//               range by an exact power of two and converts it in place;
+//               With a bf16 query on an fp8 cache each thread brings its Q
+//               row into f16 range by an exact power of two and converts it in
+//               place, for the next item as soon as its last pass of the
+//               current one is done (before that item's epilogue);
 //   warp 12     TMA producer: both Q tiles, K and V pages (one box per page);
 //   warp 13     MMA issuer and TMEM owner (warps 14-15 idle).  Per KV tile j:
 //                 S_A = Q_A K_j^T, S_B = Q_B K_j^T    (kind::f16 or kind::f8f6f4)
@@ -175,6 +177,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const __grid_constant__ CUtensorMap tmo) {
     constexpr bool k2 = KT == PAFP8_F16 || KT == PAFP8_BF16;  // 2-byte cache, same dtype as q
     constexpr bool kBF = KT == PAFP8_BF16;                    // bf16 MMA operands
+    // A bf16 query on an fp8 cache is brought into f16 range (per row, by the
+    // softmax warps) before the QK MMAs; every other path multiplies Q as loaded.
+    const bool fit_q = !kF8 && !k2 && p.q_dtype == PAFP8_BF16;
     using L = Layout<kF8, k2>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t base = (smem_addr(smem_raw) + 1023u) & ~1023u;
@@ -413,7 +418,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int nA = tile_nkv(it.t0, 0, TQ, qo_len, kv_len);
                 const int nB = tile_nkv(it.t0, 1, TQ, qo_len, kv_len);
                 const int n = it.nkv;
-                ok = wait_or_abort(bar(kF8 ? L::bQFull : L::bQReady), qphase, flag_addr, p.status);
+                ok = wait_or_abort(bar(fit_q ? L::bQReady : L::bQFull), qphase, flag_addr, p.status);
                 qphase ^= 1u;
                 if (!ok) break;
                 tc_fence_after();
@@ -587,7 +592,56 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t qphase = 0, sphase = 0, ophase = 0;
         uint32_t stage_round = 0;  // staging rounds of this tile so far (fp8 query)
         const bool issuer = (threadIdx.x & 127) == 0;
+        const bool o_32b = (reinterpret_cast<uintptr_t>(p.o) & 31u) == 0;  // rows are 256 B apart
         bool ok = true;
+        // Range fit of this thread's Q row (bf16 query on an fp8 cache): wait
+        // for the item's Q tiles, scale the row into f16 range by an exact power
+        // of two, convert it in place and return the power (it multiplies the
+        // logit scale).  Both warpgroups arrive on q_ready for every item.
+        auto fit_row = [&]() -> float {
+            float up = 1.f;
+            ok = __all_sync(0xFFFFFFFFu, wait_or_abort(bar(L::bQFull), qphase, flag_addr, p.status));
+            qphase ^= 1u;
+            if (!ok) return up;
+            if (r < TQ * g) {
+                const uint32_t qrow = base + L::q + x * L::kQTile + r * 128;
+                uint32_t mx = 0;
+#pragma unroll
+                for (int c = 0; c < 16; ++c) {
+                    const uint4 w = lds128(qrow + (c >> 3) * kHalfTile + (((c & 7) ^ (r & 7)) << 4));
+                    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        mx = max(mx, (ws[k] & 0x7FFFu) << 16);
+                        mx = max(mx, ws[k] & 0x7FFF0000u);
+                    }
+                }
+                const int ex = (int)((mx >> 23) & 0xFF) - 127;
+                const int shift = ex > 14 ? ex - 14 : 0;
+                const float down = __int_as_float((127 - shift) << 23);
+                up = __int_as_float((127 + shift) << 23);
+#pragma unroll 4
+                for (int c = 0; c < 16; ++c) {
+                    const uint32_t a = qrow + (c >> 3) * kHalfTile + (((c & 7) ^ (r & 7)) << 4);
+                    const uint4 w = lds128(a);
+                    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+                    uint32_t o4[4];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        o4[k] = pack_half2(__uint_as_float(ws[k] << 16) * down,
+                                           __uint_as_float(ws[k] & 0xFFFF0000u) * down);
+                    sts128(a, o4[0], o4[1], o4[2], o4[3]);
+                }
+                fence_async_smem();
+            }
+            mbar_arrive(bar(L::bQReady));
+            return up;
+        };
+        // The next item's Q is fitted right after this item's last softmax pass
+        // and before its epilogue, so the next item's first QK does not wait
+        // for the epilogues.
+        float up_next = 1.f;
+        if (fit_q && (int)blockIdx.x < n_items) up_next = fit_row();
         for (int t = blockIdx.x; t < n_items && ok; t += gridDim.x) {
             const Item it = load_item(items, t);
             const int qo0 = it.qo0;
@@ -598,46 +652,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int tok = r / g, hh = r - tok * g;
             const bool valid_row = (tok < TQ) && (t0 + tok < qo_len);
             const int limit = valid_row ? t0 + tok + kv_len - qo_len : -1;
-            float scale = p.sm_scale_log2;
-            if (!kF8) {
-                ok = __all_sync(0xFFFFFFFFu, wait_or_abort(bar(L::bQFull), qphase, flag_addr, p.status));
-                qphase ^= 1u;
-                if (!ok) break;
-                if (!k2 && p.q_dtype == PAFP8_BF16 && r < TQ * g) {
-                    // Bring the row into f16 range by an exact power of two.
-                    const uint32_t qrow = base + L::q + x * L::kQTile + r * 128;
-                    uint32_t mx = 0;
-#pragma unroll
-                    for (int c = 0; c < 16; ++c) {
-                        const uint4 w = lds128(qrow + (c >> 3) * kHalfTile + (((c & 7) ^ (r & 7)) << 4));
-                        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            mx = max(mx, (ws[k] & 0x7FFFu) << 16);
-                            mx = max(mx, ws[k] & 0x7FFF0000u);
-                        }
-                    }
-                    const int ex = (int)((mx >> 23) & 0xFF) - 127;
-                    const int shift = ex > 14 ? ex - 14 : 0;
-                    const float down = __int_as_float((127 - shift) << 23);
-                    scale *= __int_as_float((127 + shift) << 23);
-#pragma unroll 4
-                    for (int c = 0; c < 16; ++c) {
-                        const uint32_t a = qrow + (c >> 3) * kHalfTile + (((c & 7) ^ (r & 7)) << 4);
-                        const uint4 w = lds128(a);
-                        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-                        uint32_t o4[4];
-#pragma unroll
-                        for (int k = 0; k < 4; ++k)
-                            o4[k] = pack_half2(__uint_as_float(ws[k] << 16) * down,
-                                               __uint_as_float(ws[k] & 0xFFFF0000u) * down);
-                        sts128(a, o4[0], o4[1], o4[2], o4[3]);
-                    }
-                    fence_async_smem();
-                }
-                mbar_arrive(bar(L::bQReady));
-            }
-            if (nX == 0) continue;  // tile B past the request's last row
+            const float scale = p.sm_scale_log2 * up_next;
             float m = -INFINITY, l = 0.f;  // m in scaled (log2) units
             for (int j = 0; j < nX && ok; ++j) {
                 ok = __all_sync(0xFFFFFFFFu, wait_or_abort(bar(L::bSFull + x), sphase, flag_addr, p.status));
@@ -736,6 +751,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 m = m_use;
             }
             if (!ok) break;
+            if (fit_q && t + (int)gridDim.x < n_items) {
+                up_next = fit_row();
+                if (!ok) break;
+            }
+            if (nX == 0) continue;  // tile B past the request's last row
             // epilogue: the tile's last O update must have completed.
             ok = __all_sync(0xFFFFFFFFu, wait_or_abort(bar(L::bOFull + x), ophase, flag_addr, p.status));
             ophase ^= 1u;
@@ -810,9 +830,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     a, b);
                         w[i] = pack_out2(a, b, p.o_dtype);
                     }
-                    uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + orow * D + 32 * c);
+                    uint16_t* dst = static_cast<uint16_t*>(p.o) + orow * D + 32 * c;
+                    if (o_32b) {
+                        // 32-byte stores: every access fills whole sectors.
+                        stg256(dst, w);
+                        stg256(dst + 16, w + 8);
+                    } else {
+                        uint4* d4 = reinterpret_cast<uint4*>(dst);
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+                        for (int i = 0; i < 4; ++i) d4[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+                    }
                 }
             }
             if (valid_row && p.lse != nullptr) p.lse[orow] = (m + __log2f(l)) * 0.69314718055994531f;

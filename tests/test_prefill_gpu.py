@@ -162,3 +162,23 @@ def test_fp8_cache_equals_its_f16_dequantization_bitwise(cuda_device, kv_dtype):
     o2, l2 = run_gpu(b16, cuda_device, num_ctas=11)
     assert np.array_equal(o1, o2)
     assert np.array_equal(l1, l2)
+
+
+@pytest.mark.parametrize("q_dtype", ["bf16", "e4m3fn"])
+def test_output_only_16_byte_aligned(cuda_device, q_dtype):
+    """o at 16 bytes past a 32-byte boundary (the interface asks for 16): the
+    rows that are not written by bulk tensor stores take 16-byte stores, and
+    the result is bitwise the same as with an aligned buffer."""
+    from gpu_common import DeviceBatch
+    b = make_batch([300, 150], [300, 90], num_qo_heads=8, num_kv_heads=2, q_dtype=q_dtype, seed=29)
+    db = DeviceBatch(b, cuda_device, num_ctas=5)
+    db.run()
+    o1, l1 = db.result()
+    big = torch.full((db.o.numel() + 8,), float("nan"), dtype=db.o.dtype, device=cuda_device)
+    db.o = big[8:].view(db.o.shape)
+    assert db.o.data_ptr() % 32 == 16
+    db.run()
+    o2, l2 = db.result()
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+    ro, rl = oracle_on(b)
+    assert_close(o2, l2, ro, rl, f"prefill {q_dtype}, o 16-byte aligned")
