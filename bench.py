@@ -74,7 +74,7 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--mode", choices=["all", "decode", "prefill"], default="all",
+    ap.add_argument("--mode", choices=["all", "decode", "prefill", "append"], default="all",
                     help="which parts to time (profiling runs use one)")
     ap.add_argument("--prefill-steps", type=int, default=30)
     return ap.parse_args()
@@ -226,6 +226,75 @@ def time_decode_2byte(dev, steps, warmup):
             "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(gbs / peak, 4), "peak_kind": kind,
                          "note": "whole step (decode + merge kernels)"}}
+
+
+def append_bytes(a) -> int:
+    """Algorithmic bytes of one KV append: the new K and V rows read, their
+    fp8 codes written, and each token's request index and position."""
+    el = a.nnz * a.base.num_kv_heads * a.base.head_dim
+    return 2 * el * a.k_new.element_size() + 2 * el + 8 * a.nnz
+
+
+def time_append(index, dev, steps, warmup):
+    """Device time of one pafp8_append_kv launch on a named append workload
+    (inputs resident, L2 evicted before each timed sample); GB/s over its
+    algorithmic bytes.  The one-token-per-request workload is timed as 20
+    back-to-back launches per sample (a single launch of it is shorter than
+    the host's launch call): the 20 launches are captured once in a CUDA
+    graph and each sample replays it."""
+    import torch
+
+    import paged_attention_fp8_gb300 as pa
+    from paged_attention_fp8_gb300.workloads import APPEND_WORKLOADS, append_workload
+
+    a = append_workload(index)
+    b = a.base
+    nbytes = append_bytes(a)
+    kn, vn = a.k_new.to(dev), a.v_new.to(dev)
+    bi, ps = a.batch_indices.to(dev), a.positions.to(dev)
+    ip, ix = b.kv_indptr.to(dev), b.kv_indices.to(dev)
+    kc, vc = b.k_cache.to(dev), b.v_cache.to(dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    flush = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def launch():  # on torch's current stream (the capture stream inside a graph capture)
+        pa.pafp8_append_kv(kn, vn, bi, ps, ip, ix, kc, vc, k_scale=b.k_scale, v_scale=b.v_scale, status=st)
+
+    reps = 20 if a.nnz < 1024 else 1
+    for _ in range(warmup):
+        flush.sum()
+        launch()
+    torch.cuda.synchronize()
+    sample = launch
+    if reps > 1:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for _ in range(reps):
+                launch()
+        sample = graph.replay
+        for _ in range(warmup):
+            sample()
+        torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+    for i in range(steps):
+        flush.sum()
+        ev[i][0].record(stream)
+        sample()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    if int(st.item()) != 0:
+        raise RuntimeError("append skipped tokens on a well-formed workload")
+    ms = statistics.median(e[0].elapsed_time(e[1]) for e in ev) / reps
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    peak, kind = measured_peaks()
+    del kn, vn, bi, ps, ip, ix, kc, vc, st, flush
+    torch.cuda.empty_cache()
+    return {"workload": APPEND_WORKLOADS[index], "tokens": a.nnz, "value": round(gbs, 1), "unit": "GB/s",
+            "us_per_launch": round(ms * 1e3, 2), "bytes_per_launch": nbytes, "launches": steps * reps,
+            "launches_per_sample": reps,
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(gbs / peak, 4), "peak_kind": kind}}
 
 
 def kernel_sha(name: str) -> str:
@@ -384,6 +453,14 @@ def run_ours(args):
             dist.destroy_process_group()
         return
 
+    if args.mode == "append":
+        res = {str(i): time_append(i, dev, min(args.steps, 200), max(3, args.warmup)) for i in (8, 9)}
+        if rank == 0:
+            print(json.dumps({"mode": "append", "append_kv": res}), flush=True)
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
     b = workload(2)
     nbytes = decode_bytes(b)
     q = b.q.to(dev)
@@ -496,6 +573,8 @@ def run_ours(args):
         for i in (4, 5, 7):
             prefill_res[i] = time_prefill(i, dev, args.prefill_steps, max(3, min(args.warmup, 10)))
         decode16 = time_decode_2byte(dev, min(args.steps, 200), max(3, min(args.warmup, 20)))
+        append_res = {i: time_append(i, dev, min(args.steps, 200), max(3, min(args.warmup, 20)))
+                      for i in (8, 9)}
 
     if rank != 0:
         dist.destroy_process_group()
@@ -536,6 +615,7 @@ def run_ours(args):
         line["prefill"] = {"ragged_bf16": prefill_res[4], "fp8_fp8": prefill_res[5],
                            "ragged_bf16_cache": prefill_res[7]}
         line["decode_2byte_cache"] = decode16
+        line["append_kv"] = {"prefill_tokens": append_res[8], "decode_step": append_res[9]}
     if world == 1 and not args.no_cpu_baseline:
         n = oracle_sample_size(b, 15.0)
         dt, by, cores = oracle_decode_sample(b, n)

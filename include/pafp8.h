@@ -241,6 +241,51 @@ pafp8_status pafp8_run_decode_noalloc(const pafp8_plan *plan, int32_t q_dtype, c
                                       float q_scale, float k_scale, float v_scale,
                                       int32_t o_dtype, void *o, float *lse, void *stream);
 
+/* Quantize new K/V tokens into the paged fp8 cache: the step that writes the
+ * cache every other entry point reads.  The pages take such a cache as given
+ * (fp8 K/V with per-tensor k_scale/v_scale, dequantized as code * scale, "fp8
+ * KV cache in the in-tree prefill kernel", What changed and Test plan); the
+ * inverse of that dequantization is this library's reading:
+ *
+ *   code = fp8(RNE, saturating)( fp32(x) * fp32(1 / scale) )
+ *
+ * in IEEE fp32 (1/scale rounded once, the product rounded once), then rounded
+ * to the nearest kv_dtype value with ties to even; magnitudes above the
+ * largest finite value (e4m3fn 448, e5m2 57344), infinities included, store
+ * that value with their sign; +-0 keep their sign; NaN stores a NaN code.
+ *
+ *   src_dtype      F16, BF16 or F32: the type of the new tokens
+ *   k_new, v_new   device [nnz, num_kv_heads, head_dim] of src_dtype,
+ *                  16-byte aligned
+ *   nnz            new tokens (0: nothing is launched)
+ *   batch_indices  device int32 [nnz]: request of each new token
+ *   positions      device int32 [nnz]: the token's position in its request's
+ *                  KV sequence; it goes to page kv_indices[kv_indptr[b] +
+ *                  pos / page_size], slot pos % page_size
+ *   batch          requests in kv_indptr
+ *   kv_indptr      device int32 [batch + 1], kv_indices device int32
+ *                  [kv_indptr[batch]]: the page table of pafp8_plan_create /
+ *                  pafp8_run (already covering the new tokens)
+ *   kv_dtype       E4M3FN or E5M2 (the cache's format; 2-byte caches and
+ *                  every other dtype are refused)
+ *   k_cache,
+ *   v_cache        device [num_pages, page_size, num_kv_heads, head_dim] of
+ *                  kv_dtype, 16-byte aligned; only the new tokens' rows are
+ *                  written
+ *   k_scale,
+ *   v_scale        the per-tensor scales the cache is read with; finite, > 0
+ *   status         device uint32 or NULL: the kernel ORs in 1 for a token it
+ *                  did not write because its request index, position or page
+ *                  index lies outside the table or the pool
+ * Shapes served: head_dim 128, page_size 16.  Nothing is allocated or
+ * synchronized. */
+pafp8_status pafp8_append_kv(int32_t src_dtype, const void *k_new, const void *v_new, int64_t nnz,
+                             int32_t num_kv_heads, int32_t head_dim, const int32_t *batch_indices,
+                             const int32_t *positions, int32_t batch, const int32_t *kv_indptr,
+                             const int32_t *kv_indices, int32_t kv_dtype, void *k_cache,
+                             void *v_cache, int32_t num_pages, int32_t page_size, float k_scale,
+                             float v_scale, uint32_t *status, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

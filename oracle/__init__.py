@@ -66,6 +66,13 @@ def _load():
         lib.orc_dense_attention_row.restype = i32
         lib.orc_merge_states.argtypes = [i64, i64, vp, vp, vp, vp]
         lib.orc_merge_states.restype = None
+        lib.orc_encode_fp8.argtypes = [i32, ctypes.c_float]
+        lib.orc_encode_fp8.restype = ctypes.c_uint8
+        lib.orc_quantize_array.argtypes = [i32, vp, i64, ctypes.c_float, vp]
+        lib.orc_quantize_array.restype = i32
+        lib.orc_append_kv.argtypes = [i32, vp, vp, i64, i32, i32, vp, vp, i32, vp, vp, i32, i32,
+                                      ctypes.c_float, ctypes.c_float, vp, vp]
+        lib.orc_append_kv.restype = i64
         _lib = lib
         return lib
 
@@ -102,6 +109,51 @@ def decode(dtype: str, raw) -> np.ndarray:
 def fp8_table(fmt: str) -> np.ndarray:
     """The 256 values of an fp8 format, indexed by code."""
     return decode(fmt, np.arange(256, dtype=np.uint8))
+
+
+def as_f32(src, src_dtype: str) -> np.ndarray:
+    """New-token rows as fp32: raw f16/bf16 codes decoded (exact), or fp32."""
+    if src_dtype == "f32":
+        return np.ascontiguousarray(src, dtype=np.float32)
+    return decode(src_dtype, src).astype(np.float32)
+
+
+def encode_fp8(fmt: str, y: float) -> int:
+    """Code of the fp32 value ``y`` in ``fmt`` (nearest, ties to even,
+    saturating; NaN -> 0x7F)."""
+    return int(_load().orc_encode_fp8(DTYPE_CODES[fmt], float(np.float32(y))))
+
+
+def quantize(fmt: str, x, scale: float) -> np.ndarray:
+    """fp8 codes of fl32(x * fl32(1/scale)) for fp32 ``x`` (same shape)."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    out = np.empty(x.shape, dtype=np.uint8)
+    rc = _load().orc_quantize_array(DTYPE_CODES[fmt], _ptr(x), x.size, float(scale), _ptr(out))
+    if rc != 0:
+        raise ValueError(f"oracle quantize failed ({rc})")
+    return out
+
+
+def append_kv(*, fmt, k_new, v_new, batch_indices, positions, kv_indptr, kv_indices, k_cache,
+              v_cache, k_scale, v_scale):
+    """Write new tokens (fp32 rows [nnz, hkv, d]) into copies of the fp8 caches
+    (uint8 codes [num_pages, page_size, hkv, d]).  Returns (k_cache, v_cache,
+    tokens not written)."""
+    k_new = np.ascontiguousarray(k_new, dtype=np.float32)
+    v_new = np.ascontiguousarray(v_new, dtype=np.float32)
+    kc = np.array(k_cache, dtype=np.uint8, copy=True, order="C")
+    vc = np.array(v_cache, dtype=np.uint8, copy=True, order="C")
+    bi = np.ascontiguousarray(batch_indices, dtype=np.int32)
+    ps = np.ascontiguousarray(positions, dtype=np.int32)
+    ip = np.ascontiguousarray(kv_indptr, dtype=np.int32)
+    ix = np.ascontiguousarray(kv_indices, dtype=np.int32)
+    nnz, hkv, d = k_new.shape
+    skipped = _load().orc_append_kv(DTYPE_CODES[fmt], _ptr(k_new), _ptr(v_new), nnz, hkv, d, _ptr(bi),
+                                    _ptr(ps), len(ip) - 1, _ptr(ip), _ptr(ix), kc.shape[0], kc.shape[1],
+                                    float(k_scale), float(v_scale), _ptr(kc), _ptr(vc))
+    if skipped < 0:
+        raise ValueError("oracle append failed")
+    return kc, vc, int(skipped)
 
 
 def paged_attention(*, q, q_dtype, k_cache, v_cache, kv_dtype, qo_indptr, kv_indptr,

@@ -140,6 +140,89 @@ int orc_decode_array(int dtype, const void *src, int64_t n, double *dst) {
     return 0;
 }
 
+/* ---- 7. writing new tokens into the cache -----------------------------
+ *
+ * The inverse of step 2 for K and V.  The pages take the fp8 cache as given
+ * (codes whose decoded values times the per-tensor scale are the keys and
+ * values); writing a new row is read here as
+ *
+ *   y    = fl32( fl32(x) * fl32(1 / scale) )          (IEEE single, RNE)
+ *   code = the format's value nearest to y, a tie going to the code whose
+ *          mantissa LSB is 0; magnitudes above the largest finite value
+ *          (e4m3fn 448, e5m2 57344), infinities included, store that value
+ *          with their sign; +0 and -0 keep their sign; NaN stores 0x7F,
+ *          a NaN code in both formats.
+ *
+ * The rounding is done on exact doubles: y / spacing is an exact power-of-two
+ * scaling, and nearbyint() in the default rounding mode rounds half to even. */
+uint8_t orc_encode_fp8(int fmt, float y) {
+    const int mbits = fmt == ORC_E4M3FN ? 3 : 2;
+    const int bias = fmt == ORC_E4M3FN ? 7 : 15;
+    const double maxv = fmt == ORC_E4M3FN ? 448.0 : 57344.0;
+    if (isnan(y)) return 0x7F;
+    const uint8_t sign = signbit(y) ? 0x80 : 0x00;
+    double a = fabs((double)y);
+    if (a > maxv) a = maxv; /* saturation; beyond the largest value every value rounds to it or past it */
+    /* Spacing of the values around a: 2^(E - mbits) in the binade [2^E, 2^(E+1)) of a normal
+     * value, 2^(1 - bias - mbits) below the smallest normal 2^(1 - bias). */
+    int E = 1 - bias;
+    if (a >= ldexp(1.0, 1 - bias)) {
+        frexp(a, &E);
+        E -= 1;
+    }
+    const double step = ldexp(1.0, E - mbits);
+    double v = nearbyint(a / step) * step;
+    if (v > maxv) v = maxv;
+    if (v == 0.0) return sign;
+    int ev;
+    frexp(v, &ev);
+    ev -= 1; /* v = 1.f * 2^ev */
+    if (ev < 1 - bias) /* subnormal: exponent field 0, mantissa = v / smallest spacing */
+        return (uint8_t)(sign | (uint8_t)(v / ldexp(1.0, 1 - bias - mbits)));
+    const int mant = (int)((v / ldexp(1.0, ev) - 1.0) * (double)(1 << mbits));
+    return (uint8_t)(sign | (uint8_t)(((ev + bias) << mbits) | mant));
+}
+
+/* codes[i] = encode(fl32(x[i] * fl32(1 / scale))).  Returns 0, or -1 for a
+ * format that is not fp8. */
+int orc_quantize_array(int fmt, const float *x, int64_t n, float scale, uint8_t *codes) {
+    if (fmt != ORC_E4M3FN && fmt != ORC_E5M2) return -1;
+    const float inv = 1.0f / scale; /* single precision throughout (FLT_EVAL_METHOD 0) */
+    for (int64_t i = 0; i < n; ++i) {
+        const float y = x[i] * inv;
+        codes[i] = orc_encode_fp8(fmt, y);
+    }
+    return 0;
+}
+
+/* Write nnz new tokens (rows [nnz, hkv, d] of k_new and v_new, as fp32) into
+ * the paged caches [num_pages, page_size, hkv, d] of fp8 codes: token i of
+ * request b = batch_idx[i] at position p = pos[i] goes to page
+ * kv_indices[kv_indptr[b] + p / page_size], slot p % page_size (the gather of
+ * step 3, written instead of read).  A token whose request, position or page
+ * is outside the table or the pool is not written.  Returns the number of
+ * tokens not written, or -1 for a format that is not fp8. */
+int64_t orc_append_kv(int fmt, const float *k_new, const float *v_new, int64_t nnz, int hkv, int d,
+                      const int32_t *batch_idx, const int32_t *pos, int batch, const int32_t *kv_indptr,
+                      const int32_t *kv_indices, int num_pages, int page_size, float k_scale,
+                      float v_scale, uint8_t *k_cache, uint8_t *v_cache) {
+    if (fmt != ORC_E4M3FN && fmt != ORC_E5M2) return -1;
+    int64_t skipped = 0;
+    const int64_t row = (int64_t)hkv * d;
+    for (int64_t i = 0; i < nnz; ++i) {
+        const int b = batch_idx[i], p = pos[i];
+        if (b < 0 || b >= batch || p < 0) { ++skipped; continue; }
+        const int64_t e = (int64_t)kv_indptr[b] + p / page_size;
+        if (kv_indptr[b] < 0 || e >= kv_indptr[b + 1]) { ++skipped; continue; }
+        const int page = kv_indices[e];
+        if (page < 0 || page >= num_pages) { ++skipped; continue; }
+        const int64_t dst = ((int64_t)page * page_size + p % page_size) * row;
+        orc_quantize_array(fmt, k_new + i * row, row, k_scale, k_cache + dst);
+        orc_quantize_array(fmt, v_new + i * row, row, v_scale, v_cache + dst);
+    }
+    return skipped;
+}
+
 int orc_num_threads(void) {
 #ifdef _OPENMP
     return omp_get_max_threads();

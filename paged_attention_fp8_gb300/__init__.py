@@ -39,7 +39,7 @@ _NAME_CODES = {"default": DTYPE_DEFAULT, "f16": F16, "float16": F16, "bf16": BF1
 # Every entry point include/pafp8.h declares.
 EXPORTS = ("pafp8_abi_version", "pafp8_last_error", "pafp8_plan_create", "pafp8_plan_destroy",
            "pafp8_workspace_bytes", "pafp8_plan_metadata", "pafp8_plan_upload", "pafp8_run",
-           "pafp8_run_stage", "pafp8_device_status", "pafp8_run_decode_noalloc")
+           "pafp8_run_stage", "pafp8_device_status", "pafp8_run_decode_noalloc", "pafp8_append_kv")
 
 
 class Pafp8Error(RuntimeError):
@@ -93,6 +93,9 @@ def lib() -> ctypes.CDLL:
     L.pafp8_run_decode_noalloc.argtypes = [vp, i32, vp, i32, vp, i32, vp, vp, f32, f32, f32, i32, vp,
                                            vp, vp]
     L.pafp8_run_decode_noalloc.restype = i32
+    L.pafp8_append_kv.argtypes = [i32, vp, vp, ctypes.c_int64, i32, i32, vp, vp, i32, vp, vp, i32, vp, vp,
+                                  i32, i32, f32, f32, vp, vp]
+    L.pafp8_append_kv.restype = i32
     _lib = L
     return L
 
@@ -216,6 +219,21 @@ def pafp8_run_decode_noalloc(handle: int, q, k_cache, v_cache, kv_indices, o, ls
         dtype_code(v_dtype if v_dtype is not None else v_cache.dtype), _ptr(v_cache),
         _ptr(kv_indices), float(q_scale), float(k_scale), float(v_scale),
         dtype_code(o_dtype if o_dtype is not None else o.dtype), _ptr(o), _ptr(lse), _stream(stream)))
+
+
+def pafp8_append_kv(k_new, v_new, batch_indices, positions, kv_indptr, kv_indices, k_cache, v_cache, *,
+                    k_scale=1.0, v_scale=1.0, status=None, src_dtype=None, kv_dtype=None,
+                    num_pages=None, stream=None) -> None:
+    """Quantize new tokens k_new/v_new [nnz, Hkv, D] into the paged fp8 cache
+    (see include/pafp8.h).  Index arrays are device int32; dtype codes,
+    head counts and sizes default to what the tensors say."""
+    nnz, hkv, d = k_new.shape
+    _check(lib().pafp8_append_kv(
+        dtype_code(src_dtype if src_dtype is not None else k_new.dtype), _ptr(k_new), _ptr(v_new), int(nnz),
+        int(hkv), int(d), _ptr(batch_indices), _ptr(positions), int(kv_indptr.numel() - 1), _ptr(kv_indptr),
+        _ptr(kv_indices), dtype_code(kv_dtype if kv_dtype is not None else k_cache.dtype), _ptr(k_cache),
+        _ptr(v_cache), int(num_pages if num_pages is not None else k_cache.shape[0]), int(k_cache.shape[1]),
+        float(k_scale), float(v_scale), _ptr(status), _stream(stream)))
 
 
 # ---- convenience owner of a plan ---------------------------------------

@@ -942,4 +942,74 @@ pafp8_status pafp8_run_decode_noalloc(const pafp8_plan* plan, int32_t q_dtype, c
     return PAFP8_OK;
 }
 
+pafp8_status pafp8_append_kv(int32_t src_dtype, const void* k_new, const void* v_new, int64_t nnz,
+                             int32_t num_kv_heads, int32_t head_dim, const int32_t* batch_indices,
+                             const int32_t* positions, int32_t batch, const int32_t* kv_indptr,
+                             const int32_t* kv_indices, int32_t kv_dtype, void* k_cache,
+                             void* v_cache, int32_t num_pages, int32_t page_size, float k_scale,
+                             float v_scale, uint32_t* status, void* stream) {
+    if (src_dtype != PAFP8_F16 && src_dtype != PAFP8_BF16 && src_dtype != PAFP8_F32)
+        return fail(PAFP8_ERR_DTYPE, "new tokens of dtype %s: append takes f16, bf16 or f32 rows",
+                    dtype_name(src_dtype));
+    if (!is_fp8(kv_dtype)) {
+        if (is_2byte(kv_dtype))
+            return fail(PAFP8_ERR_UNSUPPORTED,
+                        "a %s cache holds the new rows as they are; append quantizes into an "
+                        "e4m3fn or e5m2 cache only",
+                        dtype_name(kv_dtype));
+        return fail(PAFP8_ERR_DTYPE, "append writes an e4m3fn or e5m2 cache, not %s",
+                    dtype_name(kv_dtype));
+    }
+    if (nnz < 0 || batch < 0 || num_pages < 0)
+        return fail(PAFP8_ERR_SHAPE, "nnz %lld, batch %d and num_pages %d must not be negative",
+                    (long long)nnz, (int)batch, (int)num_pages);
+    if (num_kv_heads <= 0)
+        return fail(PAFP8_ERR_SHAPE, "num_kv_heads %d must be positive", (int)num_kv_heads);
+    if (head_dim != kHeadDim)
+        return fail(PAFP8_ERR_UNSUPPORTED, "head_dim %d is not served by this build (only %d)",
+                    (int)head_dim, kHeadDim);
+    if (page_size != kPageSize)
+        return fail(PAFP8_ERR_UNSUPPORTED, "page_size %d is not served by this build (only %d)",
+                    (int)page_size, kPageSize);
+    if (!scale_ok(k_scale) || !scale_ok(v_scale))
+        return fail(PAFP8_ERR_ARG, "scales must be finite and > 0 (k %g, v %g)", (double)k_scale,
+                    (double)v_scale);
+    if (nnz == 0) return PAFP8_OK;
+    if (k_new == nullptr || v_new == nullptr || k_cache == nullptr || v_cache == nullptr ||
+        batch_indices == nullptr || positions == nullptr || kv_indptr == nullptr || kv_indices == nullptr)
+        return fail(PAFP8_ERR_ARG,
+                    "k_new, v_new, k_cache, v_cache, batch_indices, positions, kv_indptr and "
+                    "kv_indices must be non-NULL");
+    if (((uintptr_t)k_new | (uintptr_t)v_new | (uintptr_t)k_cache | (uintptr_t)v_cache) % 16 != 0)
+        return fail(PAFP8_ERR_ARG, "k_new, v_new, k_cache and v_cache must be 16-byte aligned");
+    if (((uintptr_t)batch_indices | (uintptr_t)positions | (uintptr_t)kv_indptr | (uintptr_t)kv_indices |
+         (uintptr_t)status) % 4 != 0)
+        return fail(PAFP8_ERR_ARG, "batch_indices, positions, kv_indptr, kv_indices and status must be "
+                                   "4-byte aligned");
+    AppendParams p{};
+    p.k_new = k_new;
+    p.v_new = v_new;
+    p.batch_indices = batch_indices;
+    p.positions = positions;
+    p.kv_indptr = kv_indptr;
+    p.kv_indices = kv_indices;
+    p.k_cache = k_cache;
+    p.v_cache = v_cache;
+    p.status = status;
+    p.nnz = (long long)nnz;
+    p.num_kv_heads = num_kv_heads;
+    p.batch = batch;
+    p.num_pages = num_pages;
+    p.src_dtype = src_dtype;
+    p.kv_dtype = kv_dtype;
+    p.k_inv = 1.0f / k_scale;  // IEEE fp32 division: fp32(1/scale)
+    p.v_inv = 1.0f / v_scale;
+    const cudaError_t e = launch_append(p, (cudaStream_t)stream);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(PAFP8_ERR_CUDA, "append kernel launch failed: %s", cudaGetErrorString(e));
+    }
+    return PAFP8_OK;
+}
+
 }  // extern "C"

@@ -68,6 +68,22 @@ struct DecodeParams {
     float v_scale;
 };
 
+struct AppendParams {
+    const void* k_new;       // [nnz, Hkv, D] of src_dtype
+    const void* v_new;
+    const int32_t* batch_indices;  // [nnz]
+    const int32_t* positions;      // [nnz]
+    const int32_t* kv_indptr;      // [batch + 1]
+    const int32_t* kv_indices;
+    void* k_cache;           // [num_pages, page_size, Hkv, D] of kv_dtype (fp8)
+    void* v_cache;
+    uint32_t* status;        // or nullptr
+    long long nnz;
+    int num_kv_heads, batch, num_pages;
+    int src_dtype, kv_dtype;
+    float k_inv, v_inv;      // fp32(1 / scale)
+};
+
 struct PrefillParams {
     const void* q;           // [nnz_qo, Hq, D]
     const int32_t* kv_indices;
@@ -89,6 +105,7 @@ struct PrefillParams {
 cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& tmap_k,
                           const CUtensorMap& tmap_v, int num_ctas, int heads_per_cta,
                           int group, int heads_per_box, cudaStream_t stream);
+cudaError_t launch_append(const AppendParams& p, cudaStream_t stream);
 // Size of the built-in scratch of the no-allocation decode entry point, and
 // the device ordinals it serves.
 constexpr size_t kNoAllocScratchBytes = PAFP8_NOALLOC_SCRATCH_BYTES;

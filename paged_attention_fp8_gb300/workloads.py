@@ -264,3 +264,60 @@ def workload(index: int, *, scale_down: int = 1) -> PagedBatch:
         return make_batch(kv, qo, num_qo_heads=32, num_kv_heads=8, q_dtype="bf16",
                           kv_dtype="bf16", o_dtype="bf16", gen=gen, name="ragged_prefill_bf16_cache")
     raise ValueError(f"unknown workload {index}")
+
+
+@dataclasses.dataclass
+class AppendBatch:
+    """New tokens to be written into the paged cache of ``base``: one row of
+    K and of V per (token, KV head), at the given (request, position)."""
+    base: PagedBatch
+    src_dtype: str                 # "f16", "bf16" or "f32"
+    k_new: torch.Tensor            # [nnz, Hkv, D] of src_dtype
+    v_new: torch.Tensor
+    batch_indices: torch.Tensor    # int32 [nnz]
+    positions: torch.Tensor        # int32 [nnz]
+
+    @property
+    def nnz(self) -> int:
+        return int(self.batch_indices.numel())
+
+
+SRC_DTYPES = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}
+
+
+def new_tokens(base: PagedBatch, *, src_dtype: str = "bf16", seed: int = 0, std: float = 1.0) -> AppendBatch:
+    """The last qo_len positions of every request of ``base`` (a prefill's new
+    tokens, or one token per request for a decode batch), drawn N(0, std) in
+    fp32 from a generator seeded with ``seed`` (K, then V) and cast to
+    ``src_dtype`` (round to nearest)."""
+    gen = torch.Generator().manual_seed(seed)
+    b_idx, pos = [], []
+    for b, (qo, kv) in enumerate(zip(base.qo_lens, base.kv_lens)):
+        b_idx.extend([b] * qo)
+        pos.extend(range(kv - qo, kv))
+    nnz = len(b_idx)
+    shape = (nnz, base.num_kv_heads, base.head_dim)
+    kf = torch.randn(shape, generator=gen) * std
+    vf = torch.randn(shape, generator=gen) * std
+    dt = SRC_DTYPES[src_dtype]
+    return AppendBatch(base=base, src_dtype=src_dtype, k_new=kf.to(dt), v_new=vf.to(dt),
+                       batch_indices=torch.tensor(b_idx, dtype=torch.int32),
+                       positions=torch.tensor(pos, dtype=torch.int32))
+
+
+APPEND_WORKLOADS = {
+    8: "KV append of the ragged prefill's new tokens (workload 4: 16 requests, qo U[128,1024], "
+       "Hkv 8, bf16 rows -> e4m3fn cache)",
+    9: "KV append of one decode step (workload 2: 64 requests, one token each, Hkv 8, "
+       "bf16 rows -> e4m3fn cache)",
+}
+
+
+def append_workload(index: int, *, scale_down: int = 1) -> AppendBatch:
+    """The named append workloads: new tokens (seed 1000 + index) for the cache
+    of workload 4 (index 8) or workload 2 (index 9)."""
+    if index == 8:
+        return new_tokens(workload(4, scale_down=scale_down), src_dtype="bf16", seed=1008)
+    if index == 9:
+        return new_tokens(workload(2, scale_down=scale_down), src_dtype="bf16", seed=1009)
+    raise ValueError(f"unknown append workload {index}")
