@@ -70,6 +70,15 @@ typedef enum pafp8_status {
 
 enum { PAFP8_MODE_DECODE = 0, PAFP8_MODE_PREFILL = 1 };
 
+/* Layout of k_cache / v_cache (head_dim is always innermost):
+ *   NHD  [num_pages, page_size, num_kv_heads, head_dim]  (token-major page)
+ *   HND  [num_pages, num_kv_heads, page_size, head_dim]  (head-major page)
+ * The pages fix no layout beyond separate K and V caches with head_dim last
+ * ("Enable Hopper FA3 FP8 attention in decode.py", review note on
+ * v_cache.shape[-1:]); NHD is the default and HND the head-major variant,
+ * read by the same kernels through differently strided tensor maps. */
+enum { PAFP8_LAYOUT_NHD = 0, PAFP8_LAYOUT_HND = 1 };
+
 /* Static description of one batch.  Shapes served by this build:
  * head_dim 128, page_size 16, num_qo_heads a multiple of num_kv_heads with
  * group size num_qo_heads/num_kv_heads <= 8 (decode) or <= 16 (prefill).
@@ -97,7 +106,9 @@ enum { PAFP8_MODE_DECODE = 0, PAFP8_MODE_PREFILL = 1 };
  *                          (request, KV-head block) rows are cut into
  *                          num_ctas equal ranges, one per CTA.
  * num_ctas     persistent CTAs to launch; 0 = the SM count of the device that
- *              is current when the plan is created. */
+ *              is current when the plan is created.
+ * kv_layout    NHD (0, also what a zeroed description gives) or HND; the
+ *              caches given to pafp8_run are read in that layout. */
 typedef struct pafp8_plan_desc {
     int32_t mode;  /* PAFP8_MODE_DECODE or PAFP8_MODE_PREFILL */
     int32_t batch;
@@ -113,6 +124,7 @@ typedef struct pafp8_plan_desc {
     int32_t fixed_split_pages;
     int32_t disable_split_kv;
     int32_t num_ctas;
+    int32_t kv_layout; /* PAFP8_LAYOUT_NHD (0) or PAFP8_LAYOUT_HND (1) */
 } pafp8_plan_desc;
 
 typedef struct pafp8_plan pafp8_plan;
@@ -164,8 +176,9 @@ pafp8_status pafp8_plan_upload(pafp8_plan *plan, void *workspace, size_t workspa
  *   q           device, [nnz_qo, num_qo_heads, head_dim] of q_dtype
  *               (nnz_qo = batch for decode, qo_indptr_h[batch] for prefill)
  *   k_cache,
- *   v_cache     device, [num_pages, page_size, num_kv_heads, head_dim] of
- *               kv_dtype (token-major within a page), 16-byte aligned
+ *   v_cache     device, [num_pages, page_size, num_kv_heads, head_dim] (NHD)
+ *               or [num_pages, num_kv_heads, page_size, head_dim] (HND, as
+ *               planned) of kv_dtype, 16-byte aligned
  *   kv_indices  device int32 [kv_indptr_h[batch]], each in [0, num_pages)
  *   q_scale     dequantization scale of an fp8 query; must be 1 for a 2-byte
  *               query (it would otherwise be silently ignored)
@@ -268,10 +281,10 @@ pafp8_status pafp8_run_decode_noalloc(const pafp8_plan *plan, int32_t q_dtype, c
  *                  pafp8_run (already covering the new tokens)
  *   kv_dtype       E4M3FN or E5M2 (the cache's format; 2-byte caches and
  *                  every other dtype are refused)
+ *   kv_layout      PAFP8_LAYOUT_NHD or PAFP8_LAYOUT_HND
  *   k_cache,
- *   v_cache        device [num_pages, page_size, num_kv_heads, head_dim] of
- *                  kv_dtype, 16-byte aligned; only the new tokens' rows are
- *                  written
+ *   v_cache        device caches of kv_dtype in that layout, 16-byte aligned;
+ *                  only the new tokens' rows are written
  *   k_scale,
  *   v_scale        the per-tensor scales the cache is read with; finite, > 0
  *   status         device uint32 or NULL: the kernel ORs in 1 for a token it
@@ -282,9 +295,9 @@ pafp8_status pafp8_run_decode_noalloc(const pafp8_plan *plan, int32_t q_dtype, c
 pafp8_status pafp8_append_kv(int32_t src_dtype, const void *k_new, const void *v_new, int64_t nnz,
                              int32_t num_kv_heads, int32_t head_dim, const int32_t *batch_indices,
                              const int32_t *positions, int32_t batch, const int32_t *kv_indptr,
-                             const int32_t *kv_indices, int32_t kv_dtype, void *k_cache,
-                             void *v_cache, int32_t num_pages, int32_t page_size, float k_scale,
-                             float v_scale, uint32_t *status, void *stream);
+                             const int32_t *kv_indices, int32_t kv_dtype, int32_t kv_layout,
+                             void *k_cache, void *v_cache, int32_t num_pages, int32_t page_size,
+                             float k_scale, float v_scale, uint32_t *status, void *stream);
 
 #ifdef __cplusplus
 }

@@ -60,7 +60,7 @@ def _load():
         lib.orc_num_threads.argtypes = []
         lib.orc_num_threads.restype = i32
         lib.orc_paged_attention.argtypes = (
-            [i64] * 6 + [vp] * 4 + [i32, vp, dbl, i32, vp, vp, dbl, dbl, dbl, i32, i64, vp, vp, vp, vp])
+            [i64] * 6 + [vp] * 4 + [i32, vp, dbl, i32, vp, vp, dbl, dbl, dbl, i32, i32, i64, vp, vp, vp, vp])
         lib.orc_paged_attention.restype = i32
         lib.orc_dense_attention_row.argtypes = [i64, i64, i64, vp, i64, vp, vp, dbl, vp, vp]
         lib.orc_dense_attention_row.restype = i32
@@ -70,7 +70,7 @@ def _load():
         lib.orc_encode_fp8.restype = ctypes.c_uint8
         lib.orc_quantize_array.argtypes = [i32, vp, i64, ctypes.c_float, vp]
         lib.orc_quantize_array.restype = i32
-        lib.orc_append_kv.argtypes = [i32, vp, vp, i64, i32, i32, vp, vp, i32, vp, vp, i32, i32,
+        lib.orc_append_kv.argtypes = [i32, vp, vp, i64, i32, i32, vp, vp, i32, vp, vp, i32, i32, i32,
                                       ctypes.c_float, ctypes.c_float, vp, vp]
         lib.orc_append_kv.restype = i64
         _lib = lib
@@ -135,10 +135,11 @@ def quantize(fmt: str, x, scale: float) -> np.ndarray:
 
 
 def append_kv(*, fmt, k_new, v_new, batch_indices, positions, kv_indptr, kv_indices, k_cache,
-              v_cache, k_scale, v_scale):
+              v_cache, k_scale, v_scale, kv_layout="NHD"):
     """Write new tokens (fp32 rows [nnz, hkv, d]) into copies of the fp8 caches
-    (uint8 codes [num_pages, page_size, hkv, d]).  Returns (k_cache, v_cache,
-    tokens not written)."""
+    (uint8 codes [num_pages, page_size, hkv, d], or [num_pages, hkv,
+    page_size, d] for kv_layout "HND").  Returns (k_cache, v_cache, tokens
+    not written)."""
     k_new = np.ascontiguousarray(k_new, dtype=np.float32)
     v_new = np.ascontiguousarray(v_new, dtype=np.float32)
     kc = np.array(k_cache, dtype=np.uint8, copy=True, order="C")
@@ -148,8 +149,10 @@ def append_kv(*, fmt, k_new, v_new, batch_indices, positions, kv_indptr, kv_indi
     ip = np.ascontiguousarray(kv_indptr, dtype=np.int32)
     ix = np.ascontiguousarray(kv_indices, dtype=np.int32)
     nnz, hkv, d = k_new.shape
+    hnd = {"NHD": 0, "HND": 1}[kv_layout]
+    page_size = kc.shape[2] if hnd else kc.shape[1]
     skipped = _load().orc_append_kv(DTYPE_CODES[fmt], _ptr(k_new), _ptr(v_new), nnz, hkv, d, _ptr(bi),
-                                    _ptr(ps), len(ip) - 1, _ptr(ip), _ptr(ix), kc.shape[0], kc.shape[1],
+                                    _ptr(ps), len(ip) - 1, _ptr(ip), _ptr(ix), kc.shape[0], page_size, hnd,
                                     float(k_scale), float(v_scale), _ptr(kc), _ptr(vc))
     if skipped < 0:
         raise ValueError("oracle append failed")
@@ -159,11 +162,12 @@ def append_kv(*, fmt, k_new, v_new, batch_indices, positions, kv_indptr, kv_indi
 def paged_attention(*, q, q_dtype, k_cache, v_cache, kv_dtype, qo_indptr, kv_indptr,
                     kv_indices, last_page_len, num_qo_heads, num_kv_heads,
                     q_scale=1.0, k_scale=1.0, v_scale=1.0, sm_scale=None,
-                    causal=True, rows=None, heads=None):
+                    causal=True, rows=None, heads=None, kv_layout="NHD"):
     """fp64 attention of q against the paged cache; see ``oracle.c``.
 
     q: raw codes [nnz_qo, Hq, D]; k_cache/v_cache: raw codes
-    [num_pages, P, Hkv, D]; index arrays int32.  ``rows``/``heads`` (equal
+    [num_pages, P, Hkv, D] (kv_layout "NHD") or [num_pages, Hkv, P, D]
+    ("HND"); index arrays int32.  ``rows``/``heads`` (equal
     length) select which (query row, head) outputs to compute; None = all.
     Returns (o, lse): o [n, D] fp64 and lse [n] fp64 in selection order
     (all: n = nnz_qo * Hq, row-major over (row, head)).
@@ -172,7 +176,11 @@ def paged_attention(*, q, q_dtype, k_cache, v_cache, kv_dtype, qo_indptr, kv_ind
     q = _raw(q, q_dtype)
     k_cache = _raw(k_cache, kv_dtype)
     v_cache = _raw(v_cache, kv_dtype)
-    num_pages, page_size, hkv, head_dim = k_cache.shape
+    hnd = {"NHD": 0, "HND": 1}[kv_layout]
+    if hnd:
+        num_pages, hkv, page_size, head_dim = k_cache.shape
+    else:
+        num_pages, page_size, hkv, head_dim = k_cache.shape
     if hkv != num_kv_heads or q.shape[-1] != head_dim or q.shape[-2] != num_qo_heads:
         raise ValueError("oracle: shape mismatch between q, cache and head counts")
     qo_indptr = np.ascontiguousarray(qo_indptr, dtype=np.int32)
@@ -196,7 +204,7 @@ def paged_attention(*, q, q_dtype, k_cache, v_cache, kv_dtype, qo_indptr, kv_ind
         _ptr(qo_indptr), _ptr(kv_indptr), _ptr(kv_indices), _ptr(last_page_len),
         DTYPE_CODES[q_dtype], _ptr(q), float(q_scale),
         DTYPE_CODES[kv_dtype], _ptr(k_cache), _ptr(v_cache),
-        float(k_scale), float(v_scale), float(sm_scale), int(bool(causal)),
+        float(k_scale), float(v_scale), float(sm_scale), int(bool(causal)), hnd,
         n, None if sel_r is None else _ptr(sel_r), None if sel_h is None else _ptr(sel_h),
         _ptr(o), _ptr(lse))
     if rc != 0:

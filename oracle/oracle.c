@@ -140,6 +140,15 @@ int orc_decode_array(int dtype, const void *src, int64_t n, double *dst) {
     return 0;
 }
 
+/* Element offset of the row of (page, slot, KV head) in a cache laid out
+ * NHD [num_pages][P][Hkv][D] (kv_layout 0) or HND [num_pages][Hkv][P][D]
+ * (kv_layout 1). */
+static int64_t orc_row_offset(int kv_layout, int64_t page, int64_t slot, int64_t h, int64_t P,
+                              int64_t Hkv, int64_t D) {
+    if (kv_layout == 1) return ((page * Hkv + h) * P + slot) * D;
+    return ((page * P + slot) * Hkv + h) * D;
+}
+
 /* ---- 7. writing new tokens into the cache -----------------------------
  *
  * The inverse of step 2 for K and V.  The pages take the fp8 cache as given
@@ -196,7 +205,8 @@ int orc_quantize_array(int fmt, const float *x, int64_t n, float scale, uint8_t 
 }
 
 /* Write nnz new tokens (rows [nnz, hkv, d] of k_new and v_new, as fp32) into
- * the paged caches [num_pages, page_size, hkv, d] of fp8 codes: token i of
+ * the paged caches (NHD [num_pages, page_size, hkv, d] for kv_layout 0, HND
+ * [num_pages, hkv, page_size, d] for 1) of fp8 codes: token i of
  * request b = batch_idx[i] at position p = pos[i] goes to page
  * kv_indices[kv_indptr[b] + p / page_size], slot p % page_size (the gather of
  * step 3, written instead of read).  A token whose request, position or page
@@ -204,8 +214,8 @@ int orc_quantize_array(int fmt, const float *x, int64_t n, float scale, uint8_t 
  * tokens not written, or -1 for a format that is not fp8. */
 int64_t orc_append_kv(int fmt, const float *k_new, const float *v_new, int64_t nnz, int hkv, int d,
                       const int32_t *batch_idx, const int32_t *pos, int batch, const int32_t *kv_indptr,
-                      const int32_t *kv_indices, int num_pages, int page_size, float k_scale,
-                      float v_scale, uint8_t *k_cache, uint8_t *v_cache) {
+                      const int32_t *kv_indices, int num_pages, int page_size, int kv_layout,
+                      float k_scale, float v_scale, uint8_t *k_cache, uint8_t *v_cache) {
     if (fmt != ORC_E4M3FN && fmt != ORC_E5M2) return -1;
     int64_t skipped = 0;
     const int64_t row = (int64_t)hkv * d;
@@ -216,9 +226,11 @@ int64_t orc_append_kv(int fmt, const float *k_new, const float *v_new, int64_t n
         if (kv_indptr[b] < 0 || e >= kv_indptr[b + 1]) { ++skipped; continue; }
         const int page = kv_indices[e];
         if (page < 0 || page >= num_pages) { ++skipped; continue; }
-        const int64_t dst = ((int64_t)page * page_size + p % page_size) * row;
-        orc_quantize_array(fmt, k_new + i * row, row, k_scale, k_cache + dst);
-        orc_quantize_array(fmt, v_new + i * row, row, v_scale, v_cache + dst);
+        for (int h = 0; h < hkv; ++h) {
+            const int64_t dst = orc_row_offset(kv_layout, page, p % page_size, h, page_size, hkv, d);
+            orc_quantize_array(fmt, k_new + i * row + (int64_t)h * d, d, k_scale, k_cache + dst);
+            orc_quantize_array(fmt, v_new + i * row + (int64_t)h * d, d, v_scale, v_cache + dst);
+        }
     }
     return skipped;
 }
@@ -252,7 +264,7 @@ int orc_paged_attention(
     const int32_t *kv_indices, const int32_t *last_page_len,
     int q_dtype, const void *q, double q_scale,
     int kv_dtype, const void *k_cache, const void *v_cache,
-    double k_scale, double v_scale, double sm_scale, int causal,
+    double k_scale, double v_scale, double sm_scale, int causal, int kv_layout,
     int64_t n_sel, const int64_t *sel_row, const int32_t *sel_head,
     double *o, double *lse)
 {
@@ -331,7 +343,7 @@ int orc_paged_attention(
             for (int64_t j = 0; j < n_keys; ++j) {
                 const int64_t page = kv_indices[kv_indptr[b] + j / P];
                 const int64_t slot = j % P;
-                const int64_t base = ((page * P + slot) * Hkv + h_kv) * D;
+                const int64_t base = orc_row_offset(kv_layout, page, slot, h_kv, P, Hkv, D);
                 double acc = 0.0;
                 for (int64_t d = 0; d < D; ++d)
                     acc += qh[d] * (orc_decode_one(kv_dtype, k_cache, base + d) * k_scale);
@@ -352,7 +364,7 @@ int orc_paged_attention(
                 const double p = exp(s[j] - m) / l;
                 const int64_t page = kv_indices[kv_indptr[b] + j / P];
                 const int64_t slot = j % P;
-                const int64_t base = ((page * P + slot) * Hkv + h_kv) * D;
+                const int64_t base = orc_row_offset(kv_layout, page, slot, h_kv, P, Hkv, D);
                 for (int64_t d = 0; d < D; ++d)
                     ok[d] += p * (orc_decode_one(kv_dtype, v_cache, base + d) * v_scale);
             }

@@ -30,6 +30,8 @@ LIB_PATH = os.path.join(_HERE, "libpafp8.so")
 # dtype codes of include/pafp8.h
 DTYPE_DEFAULT, F16, BF16, E4M3FN, E5M2, F32, INT8, UINT8 = range(8)
 MODE_DECODE, MODE_PREFILL = 0, 1
+LAYOUT_NHD, LAYOUT_HND = 0, 1
+_LAYOUTS = {"NHD": LAYOUT_NHD, "HND": LAYOUT_HND}
 STATUS = {0: "OK", 1: "ERR_DTYPE", 2: "ERR_SHAPE", 3: "ERR_ARG", 4: "ERR_WORKSPACE", 5: "ERR_CUDA",
           6: "ERR_TIMEOUT", 7: "ERR_BOUNDS", 8: "ERR_UNSUPPORTED"}
 _NAME_CODES = {"default": DTYPE_DEFAULT, "f16": F16, "float16": F16, "bf16": BF16, "bfloat16": BF16,
@@ -58,7 +60,8 @@ class plan_desc(ctypes.Structure):
                 ("num_pages", ctypes.c_int32), ("q_dtype", ctypes.c_int32),
                 ("kv_dtype", ctypes.c_int32), ("o_dtype", ctypes.c_int32),
                 ("sm_scale", ctypes.c_float), ("fixed_split_pages", ctypes.c_int32),
-                ("disable_split_kv", ctypes.c_int32), ("num_ctas", ctypes.c_int32)]
+                ("disable_split_kv", ctypes.c_int32), ("num_ctas", ctypes.c_int32),
+                ("kv_layout", ctypes.c_int32)]
 
 
 _lib = None
@@ -93,8 +96,8 @@ def lib() -> ctypes.CDLL:
     L.pafp8_run_decode_noalloc.argtypes = [vp, i32, vp, i32, vp, i32, vp, vp, f32, f32, f32, i32, vp,
                                            vp, vp]
     L.pafp8_run_decode_noalloc.restype = i32
-    L.pafp8_append_kv.argtypes = [i32, vp, vp, ctypes.c_int64, i32, i32, vp, vp, i32, vp, vp, i32, vp, vp,
-                                  i32, i32, f32, f32, vp, vp]
+    L.pafp8_append_kv.argtypes = [i32, vp, vp, ctypes.c_int64, i32, i32, vp, vp, i32, vp, vp, i32, i32, vp,
+                                  vp, i32, i32, f32, f32, vp, vp]
     L.pafp8_append_kv.restype = i32
     _lib = L
     return L
@@ -223,17 +226,19 @@ def pafp8_run_decode_noalloc(handle: int, q, k_cache, v_cache, kv_indices, o, ls
 
 def pafp8_append_kv(k_new, v_new, batch_indices, positions, kv_indptr, kv_indices, k_cache, v_cache, *,
                     k_scale=1.0, v_scale=1.0, status=None, src_dtype=None, kv_dtype=None,
-                    num_pages=None, stream=None) -> None:
+                    kv_layout="NHD", num_pages=None, stream=None) -> None:
     """Quantize new tokens k_new/v_new [nnz, Hkv, D] into the paged fp8 cache
     (see include/pafp8.h).  Index arrays are device int32; dtype codes,
     head counts and sizes default to what the tensors say."""
     nnz, hkv, d = k_new.shape
+    layout = _LAYOUTS[kv_layout] if isinstance(kv_layout, str) else int(kv_layout)
+    page_size = int(k_cache.shape[2] if layout == LAYOUT_HND else k_cache.shape[1])
     _check(lib().pafp8_append_kv(
         dtype_code(src_dtype if src_dtype is not None else k_new.dtype), _ptr(k_new), _ptr(v_new), int(nnz),
         int(hkv), int(d), _ptr(batch_indices), _ptr(positions), int(kv_indptr.numel() - 1), _ptr(kv_indptr),
-        _ptr(kv_indices), dtype_code(kv_dtype if kv_dtype is not None else k_cache.dtype), _ptr(k_cache),
-        _ptr(v_cache), int(num_pages if num_pages is not None else k_cache.shape[0]), int(k_cache.shape[1]),
-        float(k_scale), float(v_scale), _ptr(status), _stream(stream)))
+        _ptr(kv_indices), dtype_code(kv_dtype if kv_dtype is not None else k_cache.dtype), layout,
+        _ptr(k_cache), _ptr(v_cache), int(num_pages if num_pages is not None else k_cache.shape[0]),
+        page_size, float(k_scale), float(v_scale), _ptr(status), _stream(stream)))
 
 
 # ---- convenience owner of a plan ---------------------------------------
@@ -244,7 +249,8 @@ class Plan:
     def __init__(self, *, mode: str, num_qo_heads: int, num_kv_heads: int, num_pages: int,
                  kv_indptr, last_page_len, qo_indptr=None, q_dtype, kv_dtype, o_dtype=None,
                  head_dim: int = 128, page_size: int = 16, sm_scale: float = 0.0,
-                 fixed_split_pages: int = 0, disable_split_kv: bool = False, num_ctas: int = 0):
+                 fixed_split_pages: int = 0, disable_split_kv: bool = False, num_ctas: int = 0,
+                 kv_layout: str = "NHD"):
         kv_indptr_h = _i32_host(kv_indptr)
         self.desc = plan_desc(
             mode=MODE_DECODE if mode == "decode" else MODE_PREFILL, batch=len(kv_indptr_h) - 1,
@@ -253,7 +259,8 @@ class Plan:
             kv_dtype=dtype_code(kv_dtype),
             o_dtype=DTYPE_DEFAULT if o_dtype is None else dtype_code(o_dtype),
             sm_scale=float(sm_scale), fixed_split_pages=int(fixed_split_pages),
-            disable_split_kv=int(bool(disable_split_kv)), num_ctas=int(num_ctas))
+            disable_split_kv=int(bool(disable_split_kv)), num_ctas=int(num_ctas),
+            kv_layout=_LAYOUTS[kv_layout] if isinstance(kv_layout, str) else int(kv_layout))
         self.handle = None
         self.handle = pafp8_plan_create(self.desc, kv_indptr_h, last_page_len, qo_indptr)
 

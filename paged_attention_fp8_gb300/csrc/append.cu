@@ -13,8 +13,9 @@
 // cvt.rn.satfinite.{e4m3x2,e5m2x2}.f32 (round to nearest even, magnitudes
 // above the largest finite value saturate to it, NaN stays NaN), one 16-byte
 // store of the 16 codes.  Eight consecutive threads cover a 128-element row,
-// so a warp reads four consecutive rows and writes four consecutive rows of a
-// page slot.  The page comes from the request's CSR page table; a token whose
+// so a warp reads four consecutive rows and writes four rows of one page
+// slot (consecutive in the NHD layout [page][slot][head][d], 2 KB apart in
+// the HND layout [page][head][slot][d]).  The page comes from the request's CSR page table; a token whose
 // request, position or page lies outside the table or the pool is skipped
 // and reported in *status.  The work is a pure stream of reads and writes,
 // bounded by HBM bandwidth.
@@ -116,7 +117,9 @@ __global__ void __launch_bounds__(kThreads) append_kernel(const AppendParams p) 
             if (c == 0 && p.status != nullptr) atomicOr(p.status, kStatusBounds);
             continue;
         }
-        const size_t dst = (((size_t)page * kPageSize + pos % kPageSize) * p.num_kv_heads + h) * D + 16 * c;
+        const size_t slot = (size_t)(pos % kPageSize);
+        const size_t dst = (p.hnd ? ((size_t)page * p.num_kv_heads + h) * kPageSize + slot
+                                  : ((size_t)page * kPageSize + slot) * p.num_kv_heads + h) * D + 16 * c;
         *reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.k_cache) + dst) = quantize16<KV>(rk, p.k_inv);
         *reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.v_cache) + dst) = quantize16<KV>(rv, p.v_inv);
     }

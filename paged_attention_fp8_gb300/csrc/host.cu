@@ -377,15 +377,29 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
 
 // 4-D map over one cache tensor [num_pages, P, Hkv, D] (bytes), dims listed
 // innermost first: (d, kv head, token slot, page).  One box is one KV head of
+// Byte strides of a cache tensor [num_pages, page_size, Hkv, D] (NHD) or
+// [num_pages, Hkv, page_size, D] (HND) with esz-byte elements.  Every TMA map
+// below names the same dimensions (dims, token, head, page) and only these
+// strides differ, so the boxes land in shared memory the same way for both.
+struct KvStrides {
+    cuuint64_t token, head, page;
+};
+KvStrides kv_strides(int layout, int hkv, int esz) {
+    const cuuint64_t row = (cuuint64_t)kHeadDim * esz;
+    const cuuint64_t page = (cuuint64_t)kPageSize * hkv * row;
+    if (layout == PAFP8_LAYOUT_HND) return KvStrides{row, (cuuint64_t)kPageSize * row, page};
+    return KvStrides{(cuuint64_t)hkv * row, row, page};
+}
+
 // one page, 16 tokens x 128 bytes, landing in shared memory as [16][128] with
 // the 128-byte swizzle (16-byte chunk c of token row t stored at c ^ (t & 7)).
-pafp8_status encode_cache_map(CUtensorMap* map, const void* base, int num_pages, int hkv) {
+pafp8_status encode_cache_map(CUtensorMap* map, const void* base, int num_pages, int hkv, int layout) {
     auto enc = get_encode();
     if (!enc) return fail(PAFP8_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    const KvStrides ks = kv_strides(layout, hkv, 1);
     cuuint64_t dims[4] = {(cuuint64_t)kHeadDim, (cuuint64_t)hkv, (cuuint64_t)kPageSize,
                           (cuuint64_t)num_pages};
-    cuuint64_t strides[3] = {(cuuint64_t)kHeadDim, (cuuint64_t)hkv * kHeadDim,
-                             (cuuint64_t)kPageSize * hkv * kHeadDim};
+    cuuint64_t strides[3] = {ks.head, ks.token, ks.page};
     cuuint32_t box[4] = {(cuuint32_t)kHeadDim, 1, (cuuint32_t)kPageSize, 1};
     cuuint32_t estr[4] = {1, 1, 1, 1};
     CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(base), dims, strides,
@@ -400,12 +414,12 @@ pafp8_status encode_cache_map(CUtensorMap* map, const void* base, int num_pages,
 // Prefill map over a 2-byte cache: dims (d % 64, d / 64, token, head, page);
 // one box is one page of one KV head for one 64-dim half, {64, 1, 16, 1, 1},
 // landing as 16 swizzled rows of 128 B (one per token).
-pafp8_status encode_cache_map_2byte(CUtensorMap* map, const void* base, int num_pages, int hkv) {
+pafp8_status encode_cache_map_2byte(CUtensorMap* map, const void* base, int num_pages, int hkv, int layout) {
     auto enc = get_encode();
     if (!enc) return fail(PAFP8_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
-    const cuuint64_t row = (cuuint64_t)kHeadDim * 2;
+    const KvStrides ks = kv_strides(layout, hkv, 2);
     cuuint64_t dims[5] = {64, 2, (cuuint64_t)kPageSize, (cuuint64_t)hkv, (cuuint64_t)num_pages};
-    cuuint64_t strides[4] = {128, (cuuint64_t)hkv * row, row, (cuuint64_t)kPageSize * hkv * row};
+    cuuint64_t strides[4] = {128, ks.token, ks.head, ks.page};
     cuuint32_t box[5] = {64, 1, (cuuint32_t)kPageSize, 1, 1};
     cuuint32_t estr[5] = {1, 1, 1, 1, 1};
     CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 5, const_cast<void*>(base), dims, strides, box, estr,
@@ -450,14 +464,14 @@ pafp8_status encode_q_map(CUtensorMap* map, const void* base, int nnz_qo, int hq
 // (row 2 * token + half); the fallback is one box per head with dims (d % 64,
 // d / 64, head, token, page) and the same layout.
 pafp8_status encode_decode_maps_2byte(CUtensorMap* tk, CUtensorMap* tv, const void* k, const void* v,
-                                      int num_pages, int hkv, int hpc, int* heads_per_box) {
+                                      int num_pages, int hkv, int hpc, int* heads_per_box, int layout) {
     auto enc = get_encode();
     if (!enc) return fail(PAFP8_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
-    const cuuint64_t row = (cuuint64_t)kHeadDim * 2;  // bytes of one (token, head) row
+    const KvStrides ks = kv_strides(layout, hkv, 2);
     cuuint32_t estr[5] = {1, 1, 1, 1, 1};
     {
         cuuint64_t dims[5] = {64, 2, (cuuint64_t)kPageSize, (cuuint64_t)hkv, (cuuint64_t)num_pages};
-        cuuint64_t strides[4] = {128, (cuuint64_t)hkv * row, row, (cuuint64_t)kPageSize * hkv * row};
+        cuuint64_t strides[4] = {128, ks.token, ks.head, ks.page};
         cuuint32_t box[5] = {64, 2, (cuuint32_t)kPageSize, (cuuint32_t)hpc, 1};
         CUresult rk = enc(tk, CU_TENSOR_MAP_DATA_TYPE_UINT16, 5, const_cast<void*>(k), dims, strides, box, estr,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -471,7 +485,7 @@ pafp8_status encode_decode_maps_2byte(CUtensorMap* tk, CUtensorMap* tv, const vo
         }
     }
     cuuint64_t dims[5] = {64, 2, (cuuint64_t)hkv, (cuuint64_t)kPageSize, (cuuint64_t)num_pages};
-    cuuint64_t strides[4] = {128, row, (cuuint64_t)hkv * row, (cuuint64_t)kPageSize * hkv * row};
+    cuuint64_t strides[4] = {128, ks.head, ks.token, ks.page};
     cuuint32_t box[5] = {64, 2, 1, (cuuint32_t)kPageSize, 1};
     CUresult rk = enc(tk, CU_TENSOR_MAP_DATA_TYPE_UINT16, 5, const_cast<void*>(k), dims, strides, box, estr,
                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -487,7 +501,7 @@ pafp8_status encode_decode_maps_2byte(CUtensorMap* tk, CUtensorMap* tv, const vo
 }
 
 pafp8_status encode_decode_maps(CUtensorMap* tk, CUtensorMap* tv, const void* k, const void* v,
-                                int num_pages, int hkv, int hpc, int* heads_per_box, bool two_byte) {
+                                int num_pages, int hkv, int hpc, int* heads_per_box, bool two_byte, int layout) {
     if (num_pages == 0 || k == nullptr || v == nullptr) {
         // No request has pages: the kernel issues no copy, the maps are unused.
         memset(tk, 0, sizeof(*tk));
@@ -495,13 +509,13 @@ pafp8_status encode_decode_maps(CUtensorMap* tk, CUtensorMap* tv, const void* k,
         *heads_per_box = 1;
         return PAFP8_OK;
     }
-    if (two_byte) return encode_decode_maps_2byte(tk, tv, k, v, num_pages, hkv, hpc, heads_per_box);
+    if (two_byte) return encode_decode_maps_2byte(tk, tv, k, v, num_pages, hkv, hpc, heads_per_box, layout);
     auto enc = get_encode();
     if (!enc) return fail(PAFP8_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    const KvStrides ks = kv_strides(layout, hkv, 1);
     cuuint64_t dims[4] = {(cuuint64_t)kHeadDim, (cuuint64_t)kPageSize, (cuuint64_t)hkv,
                           (cuuint64_t)num_pages};
-    cuuint64_t strides[3] = {(cuuint64_t)hkv * kHeadDim, (cuuint64_t)kHeadDim,
-                             (cuuint64_t)kPageSize * hkv * kHeadDim};
+    cuuint64_t strides[3] = {ks.token, ks.head, ks.page};
     cuuint32_t box[4] = {(cuuint32_t)kHeadDim, (cuuint32_t)kPageSize, (cuuint32_t)hpc, 1};
     cuuint32_t estr[4] = {1, 1, 1, 1};
     CUresult rk = enc(tk, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(k), dims, strides, box,
@@ -515,8 +529,8 @@ pafp8_status encode_decode_maps(CUtensorMap* tk, CUtensorMap* tv, const void* k,
         return PAFP8_OK;
     }
     pafp8_status st;
-    if ((st = encode_cache_map(tk, k, num_pages, hkv)) != PAFP8_OK) return st;
-    if ((st = encode_cache_map(tv, v, num_pages, hkv)) != PAFP8_OK) return st;
+    if ((st = encode_cache_map(tk, k, num_pages, hkv, layout)) != PAFP8_OK) return st;
+    if ((st = encode_cache_map(tv, v, num_pages, hkv, layout)) != PAFP8_OK) return st;
     *heads_per_box = 1;
     return PAFP8_OK;
 }
@@ -569,6 +583,8 @@ pafp8_status pafp8_plan_create(const pafp8_plan_desc* desc_in, const int32_t* kv
         return fail(PAFP8_ERR_UNSUPPORTED, "page_size %d is not served by this build (only %d)",
                     (int)d.page_size, kPageSize);
     if (d.num_pages < 0) return fail(PAFP8_ERR_SHAPE, "num_pages %d is negative", (int)d.num_pages);
+    if (d.kv_layout != PAFP8_LAYOUT_NHD && d.kv_layout != PAFP8_LAYOUT_HND)
+        return fail(PAFP8_ERR_ARG, "kv_layout %d is neither NHD (0) nor HND (1)", (int)d.kv_layout);
     if (std::isnan(d.sm_scale) || std::isinf(d.sm_scale))
         return fail(PAFP8_ERR_ARG, "sm_scale is not finite");
     if (d.sm_scale <= 0.0f) d.sm_scale = 1.0f / std::sqrt((float)d.head_dim);
@@ -770,11 +786,13 @@ pafp8_status pafp8_run_stage(const pafp8_plan* plan, int32_t stage, int32_t q_dt
                                pp.tile_tokens, is_fp8(q_dtype))) != PAFP8_OK)
             return st;
         if (is_2byte(k_dtype)) {
-            if ((st = encode_cache_map_2byte(&tk, k_cache, d.num_pages, d.num_kv_heads)) != PAFP8_OK) return st;
-            if ((st = encode_cache_map_2byte(&tv, v_cache, d.num_pages, d.num_kv_heads)) != PAFP8_OK) return st;
+            if ((st = encode_cache_map_2byte(&tk, k_cache, d.num_pages, d.num_kv_heads, d.kv_layout)) != PAFP8_OK)
+                return st;
+            if ((st = encode_cache_map_2byte(&tv, v_cache, d.num_pages, d.num_kv_heads, d.kv_layout)) != PAFP8_OK)
+                return st;
         } else {
-            if ((st = encode_cache_map(&tk, k_cache, d.num_pages, d.num_kv_heads)) != PAFP8_OK) return st;
-            if ((st = encode_cache_map(&tv, v_cache, d.num_pages, d.num_kv_heads)) != PAFP8_OK) return st;
+            if ((st = encode_cache_map(&tk, k_cache, d.num_pages, d.num_kv_heads, d.kv_layout)) != PAFP8_OK) return st;
+            if ((st = encode_cache_map(&tv, v_cache, d.num_pages, d.num_kv_heads, d.kv_layout)) != PAFP8_OK) return st;
         }
         CUtensorMap to;
         if ((st = encode_q_map(&to, o, (int)plan->nnz_qo, d.num_qo_heads, plan->group, pp.tile_tokens,
@@ -810,7 +828,7 @@ pafp8_status pafp8_run_stage(const pafp8_plan* plan, int32_t stage, int32_t q_dt
         CUtensorMap tk, tv;
         int hpb = 1;
         if ((st = encode_decode_maps(&tk, &tv, k_cache, v_cache, d.num_pages, d.num_kv_heads,
-                                     plan->heads_per_cta, &hpb, is_2byte(k_dtype))) != PAFP8_OK)
+                                     plan->heads_per_cta, &hpb, is_2byte(k_dtype), d.kv_layout)) != PAFP8_OK)
             return st;
         e = launch_decode(p, tk, tv, plan->num_ctas, plan->heads_per_cta, plan->group, hpb, s);
     }
@@ -929,7 +947,7 @@ pafp8_status pafp8_run_decode_noalloc(const pafp8_plan* plan, int32_t q_dtype, c
         CUtensorMap tk, tv;
         int hpb = 1;
         if ((st = encode_decode_maps(&tk, &tv, k_cache, v_cache, d.num_pages, d.num_kv_heads,
-                                     plan->heads_per_cta, &hpb, is_2byte(k_dtype))) != PAFP8_OK)
+                                     plan->heads_per_cta, &hpb, is_2byte(k_dtype), d.kv_layout)) != PAFP8_OK)
             return st;
         e = launch_decode(p, tk, tv, plan->num_ctas, plan->heads_per_cta, plan->group, hpb, s);
     }
@@ -945,9 +963,9 @@ pafp8_status pafp8_run_decode_noalloc(const pafp8_plan* plan, int32_t q_dtype, c
 pafp8_status pafp8_append_kv(int32_t src_dtype, const void* k_new, const void* v_new, int64_t nnz,
                              int32_t num_kv_heads, int32_t head_dim, const int32_t* batch_indices,
                              const int32_t* positions, int32_t batch, const int32_t* kv_indptr,
-                             const int32_t* kv_indices, int32_t kv_dtype, void* k_cache,
-                             void* v_cache, int32_t num_pages, int32_t page_size, float k_scale,
-                             float v_scale, uint32_t* status, void* stream) {
+                             const int32_t* kv_indices, int32_t kv_dtype, int32_t kv_layout,
+                             void* k_cache, void* v_cache, int32_t num_pages, int32_t page_size,
+                             float k_scale, float v_scale, uint32_t* status, void* stream) {
     if (src_dtype != PAFP8_F16 && src_dtype != PAFP8_BF16 && src_dtype != PAFP8_F32)
         return fail(PAFP8_ERR_DTYPE, "new tokens of dtype %s: append takes f16, bf16 or f32 rows",
                     dtype_name(src_dtype));
@@ -960,6 +978,8 @@ pafp8_status pafp8_append_kv(int32_t src_dtype, const void* k_new, const void* v
         return fail(PAFP8_ERR_DTYPE, "append writes an e4m3fn or e5m2 cache, not %s",
                     dtype_name(kv_dtype));
     }
+    if (kv_layout != PAFP8_LAYOUT_NHD && kv_layout != PAFP8_LAYOUT_HND)
+        return fail(PAFP8_ERR_ARG, "kv_layout %d is neither NHD (0) nor HND (1)", (int)kv_layout);
     if (nnz < 0 || batch < 0 || num_pages < 0)
         return fail(PAFP8_ERR_SHAPE, "nnz %lld, batch %d and num_pages %d must not be negative",
                     (long long)nnz, (int)batch, (int)num_pages);
@@ -1002,6 +1022,7 @@ pafp8_status pafp8_append_kv(int32_t src_dtype, const void* k_new, const void* v
     p.num_pages = num_pages;
     p.src_dtype = src_dtype;
     p.kv_dtype = kv_dtype;
+    p.hnd = kv_layout == PAFP8_LAYOUT_HND;
     p.k_inv = 1.0f / k_scale;  // IEEE fp32 division: fp32(1/scale)
     p.v_inv = 1.0f / v_scale;
     const cudaError_t e = launch_append(p, (cudaStream_t)stream);

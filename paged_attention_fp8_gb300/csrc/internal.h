@@ -81,6 +81,7 @@ struct AppendParams {
     long long nnz;
     int num_kv_heads, batch, num_pages;
     int src_dtype, kv_dtype;
+    int hnd;                 // cache layout: 0 [page][slot][head][d], 1 [page][head][slot][d]
     float k_inv, v_inv;      // fp32(1 / scale)
 };
 

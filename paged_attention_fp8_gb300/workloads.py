@@ -66,6 +66,7 @@ class PagedBatch:
     k_scale: float
     v_scale: float
     sm_scale: float
+    kv_layout: str = "NHD"  # "HND": caches are [num_pages, Hkv, P, D]
 
     @property
     def batch(self) -> int:
@@ -203,6 +204,17 @@ def make_batch(kv_lens: Sequence[int], qo_lens: Optional[Sequence[int]] = None, 
         kv_indices=perm, last_page_len=last_page_len, qo_lens=qo_lens, kv_lens=kv_lens,
         q_scale=float(q_scale), k_scale=float(k_scale), v_scale=float(v_scale),
         sm_scale=float(sm_scale) if sm_scale is not None else 1.0 / math.sqrt(D))
+
+
+def with_layout(batch: PagedBatch, layout: str) -> PagedBatch:
+    """The same batch with its caches stored in ``layout`` ("NHD" or "HND");
+    every value is unchanged, only the order of the (slot, head) rows."""
+    if layout == batch.kv_layout:
+        return batch
+
+    def perm(c):
+        return c.view(torch.uint8).permute(0, 2, 1, 3).contiguous().view(c.dtype)
+    return dataclasses.replace(batch, k_cache=perm(batch.k_cache), v_cache=perm(batch.v_cache), kv_layout=layout)
 
 
 WORKLOADS = {

@@ -22,7 +22,8 @@ def oracle_on(batch: PagedBatch, rows=None, heads=None, **over):
         num_qo_heads=batch.num_qo_heads, num_kv_heads=batch.num_kv_heads,
         q_scale=over.pop("q_scale", batch.q_scale), k_scale=over.pop("k_scale", batch.k_scale),
         v_scale=over.pop("v_scale", batch.v_scale), sm_scale=over.pop("sm_scale", batch.sm_scale),
-        causal=over.pop("causal", batch.causal), rows=rows, heads=heads)
+        causal=over.pop("causal", batch.causal), rows=rows, heads=heads,
+        kv_layout=over.pop("kv_layout", batch.kv_layout))
     if over:
         raise TypeError(f"unknown overrides {sorted(over)}")
     o, lse = oracle.paged_attention(**kw)

@@ -181,7 +181,7 @@ def test_plan_refuses_o_dtype(o, word):
 @pytest.mark.parametrize("over,status", [
     (dict(num_qo_heads=6, num_kv_heads=4), 2), (dict(head_dim=64), 8), (dict(page_size=32), 8),
     (dict(num_qo_heads=32, num_kv_heads=2), 8), (dict(mode=5), 3), (dict(num_ctas=-1), 3),
-    (dict(fixed_split_pages=-2), 3), (dict(sm_scale=float("nan")), 3)])
+    (dict(fixed_split_pages=-2), 3), (dict(sm_scale=float("nan")), 3), (dict(kv_layout=2), 3)])
 def test_plan_refuses_shapes_and_args(over, status):
     with pytest.raises(pa.Pafp8Error) as ei:
         _create(**over)
@@ -334,3 +334,32 @@ def test_prefill_refusals():
                 last_page_len=last, qo_indptr=np.array([0, 3], np.int32), q_dtype="e4m3fn",
                 kv_dtype="e4m3fn", o_dtype="e5m2", num_ctas=4)
     assert ei.value.status == 1
+
+
+def _append_raw(**over):
+    """pafp8_append_kv with plausible arguments (fake, aligned device
+    addresses: every refusal below happens before any of them is used)."""
+    a = dict(src=pa.BF16, k_new=0x10000, v_new=0x20000, nnz=4, hkv=2, d=128, bi=0x30000, pos=0x40000, batch=2,
+             indptr=0x50000, indices=0x60000, kv=pa.E4M3FN, layout=0, k_cache=0x70000, v_cache=0x80000,
+             num_pages=8, page_size=16, ks=0.5, vs=0.25, status=None)
+    a.update(over)
+    return pa.lib().pafp8_append_kv(a["src"], a["k_new"], a["v_new"], a["nnz"], a["hkv"], a["d"], a["bi"],
+                                    a["pos"], a["batch"], a["indptr"], a["indices"], a["kv"], a["layout"],
+                                    a["k_cache"], a["v_cache"], a["num_pages"], a["page_size"], a["ks"],
+                                    a["vs"], a["status"], None)
+
+
+@pytest.mark.parametrize("over,status,word", [
+    (dict(src=pa.E4M3FN), 1, "append takes"), (dict(src=pa.INT8), 1, "int8"),
+    (dict(kv=pa.BF16), 8, "bfloat16"), (dict(kv=pa.F16), 8, "float16"), (dict(kv=pa.UINT8), 1, "uint8"),
+    (dict(kv=pa.F32), 1, "float32"), (dict(d=64), 8, "head_dim"), (dict(page_size=32), 8, "page_size"),
+    (dict(hkv=0), 2, "num_kv_heads"), (dict(nnz=-1), 2, "negative"), (dict(ks=0.0), 3, "scales"),
+    (dict(vs=float("inf")), 3, "scales"), (dict(layout=3), 3, "kv_layout"), (dict(k_new=None), 3, "non-NULL"),
+    (dict(indices=None), 3, "non-NULL"), (dict(k_cache=0x70008), 3, "16-byte"), (dict(pos=0x40002), 3, "4-byte")])
+def test_append_refuses_before_touching_memory(over, status, word):
+    st = _append_raw(**over)
+    assert st == status and word in pa.pafp8_last_error(), (st, pa.pafp8_last_error())
+
+
+def test_append_of_nothing_is_a_no_op():
+    assert _append_raw(nnz=0, k_new=None, v_new=None, k_cache=None, v_cache=None) == 0

@@ -329,3 +329,21 @@ def test_mixed_2byte_decode_agrees_with_bf16_bf16():
     o_bf, _ = oracle_on(base, q=qf.to(torch.bfloat16), q_dtype="bf16", **kw)
     gap = float(np.max(np.abs(o_mixed - o_bf)))
     assert 0 < gap <= _page_number("mixed_2byte_decode_max_abs_diff")
+
+
+@pytest.mark.parametrize("mode", ["decode", "prefill"])
+def test_hnd_layout_reads_the_same_rows(mode):
+    """The head-major cache is the token-major one with (slot, head) swapped
+    by numpy; the oracle's HND gather gives the same result bit for bit, and
+    a gather that mixed slot and head (a wrong stride) would not."""
+    from paged_attention_fp8_gb300.workloads import with_layout
+    qo = None if mode == "decode" else [20, 5, 33]
+    b = make_batch([20, 70, 33], qo, num_qo_heads=8, num_kv_heads=4, seed=61, pool_pages=12)
+    o1, l1 = oracle_on(b)
+    h = with_layout(b, "HND")
+    assert h.k_cache.shape == (b.num_pages, 4, 16, 128)
+    o2, l2 = oracle_on(h)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+    # the HND bytes read as NHD are a different cache, and give a different result
+    o3, _ = oracle_on(b, k_cache=h.k_cache.view(b.k_cache.shape), v_cache=h.v_cache.view(b.v_cache.shape))
+    assert not np.allclose(o1, o3)

@@ -119,3 +119,22 @@ def test_scatter_matches_brute_force_on_a_tiny_table():
                 ev[page, p % page_size, h, j] = oracle.encode_fp8("e4m3fn", np.float32(v_new[i, h, j]) *
                                                                   (np.float32(1) / np.float32(0.05)))
     assert np.array_equal(kc, ek) and np.array_equal(vc, ev)
+
+
+def test_hnd_scatter_is_the_transposed_nhd_scatter():
+    rng = np.random.default_rng(10)
+    kv_indptr = np.array([0, 2, 5], dtype=np.int32)
+    kv_indices = np.array([3, 0, 6, 1, 5], dtype=np.int32)
+    bi = np.array([0, 0, 1, 1, 1], dtype=np.int32)
+    ps = np.array([3, 20, 0, 37, 47], dtype=np.int32)
+    k_new = rng.standard_normal((5, 4, 128)).astype(np.float32)
+    v_new = rng.standard_normal((5, 4, 128)).astype(np.float32)
+    k0 = rng.integers(0, 256, (8, 16, 4, 128), dtype=np.uint8)
+    v0 = rng.integers(0, 256, (8, 16, 4, 128), dtype=np.uint8)
+    common = dict(fmt="e5m2", k_new=k_new, v_new=v_new, batch_indices=bi, positions=ps, kv_indptr=kv_indptr,
+                  kv_indices=kv_indices, k_scale=0.02, v_scale=0.03)
+    kn, vn, sn = oracle.append_kv(k_cache=k0, v_cache=v0, **common)
+    kh, vh, sh = oracle.append_kv(k_cache=k0.transpose(0, 2, 1, 3), v_cache=v0.transpose(0, 2, 1, 3),
+                                  kv_layout="HND", **common)
+    assert sn == sh == 0
+    assert np.array_equal(kh, kn.transpose(0, 2, 1, 3)) and np.array_equal(vh, vn.transpose(0, 2, 1, 3))
