@@ -217,6 +217,27 @@ pafp8_status pafp8_run_stage(const pafp8_plan *plan, int32_t stage, int32_t q_dt
                              float k_scale, float v_scale, int32_t o_dtype, void *o, float *lse,
                              void *workspace, size_t workspace_bytes, void *stream);
 
+/* pafp8_run with per-head scale tensors in place of the per-tensor scales:
+ * the "FP8 scale tensors" that "Enable Hopper FA3 FP8 attention in
+ * decode.py" threads through the backends (Changes table; review note "FP8
+ * scale tensor passing"), read here as one scale per head.
+ *   q_scales  device float [num_qo_heads], or NULL (1 for every head).  An
+ *             fp8 query only; must be NULL for a 2-byte query.
+ *   k_scales,
+ *   v_scales  device float [num_kv_heads], required: the dequantization
+ *             scales of KV head j's codes.
+ * Query head h uses q_scales[h], k_scales[h / group] and v_scales[h / group]
+ * the way pafp8_run uses its scalars; the softmax scale is folded per head in
+ * double, in the order pafp8_run folds it, so equal entries give pafp8_run's
+ * result bit for bit.  The entries must be finite and > 0 (device memory,
+ * not checked).  Every other argument and check is pafp8_run's. */
+pafp8_status pafp8_run_head_scales(const pafp8_plan *plan, int32_t q_dtype, const void *q,
+                                   int32_t k_dtype, const void *k_cache, int32_t v_dtype,
+                                   const void *v_cache, const int32_t *kv_indices,
+                                   const float *q_scales, const float *k_scales,
+                                   const float *v_scales, int32_t o_dtype, void *o, float *lse,
+                                   void *workspace, size_t workspace_bytes, void *stream);
+
 /* Synchronize `stream`, read and clear the workspace status word that the
  * kernels set.  Returns PAFP8_OK, PAFP8_ERR_BOUNDS (a page index was out of
  * range) or PAFP8_ERR_TIMEOUT (a bounded pipeline wait expired). */

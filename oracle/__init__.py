@@ -60,7 +60,8 @@ def _load():
         lib.orc_num_threads.argtypes = []
         lib.orc_num_threads.restype = i32
         lib.orc_paged_attention.argtypes = (
-            [i64] * 6 + [vp] * 4 + [i32, vp, dbl, i32, vp, vp, dbl, dbl, dbl, i32, i32, i64, vp, vp, vp, vp])
+            [i64] * 6 + [vp] * 4 + [i32, vp, dbl, i32, vp, vp, dbl, dbl, dbl, i32, i32, vp, vp, vp, i64, vp, vp,
+                                     vp, vp])
         lib.orc_paged_attention.restype = i32
         lib.orc_dense_attention_row.argtypes = [i64, i64, i64, vp, i64, vp, vp, dbl, vp, vp]
         lib.orc_dense_attention_row.restype = i32
@@ -167,12 +168,24 @@ def paged_attention(*, q, q_dtype, k_cache, v_cache, kv_dtype, qo_indptr, kv_ind
 
     q: raw codes [nnz_qo, Hq, D]; k_cache/v_cache: raw codes
     [num_pages, P, Hkv, D] (kv_layout "NHD") or [num_pages, Hkv, P, D]
-    ("HND"); index arrays int32.  ``rows``/``heads`` (equal
+    ("HND"); index arrays int32.  ``q_scale``, ``k_scale`` and ``v_scale``
+    are floats (per tensor) or arrays of one scale per query head (q) or per
+    KV head (k, v).  ``rows``/``heads`` (equal
     length) select which (query row, head) outputs to compute; None = all.
     Returns (o, lse): o [n, D] fp64 and lse [n] fp64 in selection order
     (all: n = nnz_qo * Hq, row-major over (row, head)).
     """
     lib = _load()
+    scales = {}
+    for name, val, n_heads in (("q", q_scale, num_qo_heads), ("k", k_scale, num_kv_heads),
+                               ("v", v_scale, num_kv_heads)):
+        if np.ndim(val) == 0:
+            scales[name] = (float(val), None)
+        else:
+            arr = np.ascontiguousarray(val, dtype=np.float64)
+            if arr.shape != (n_heads,):
+                raise ValueError(f"oracle: {name}_scale has shape {arr.shape}, expected ({n_heads},)")
+            scales[name] = (1.0, arr)
     q = _raw(q, q_dtype)
     k_cache = _raw(k_cache, kv_dtype)
     v_cache = _raw(v_cache, kv_dtype)
@@ -202,9 +215,10 @@ def paged_attention(*, q, q_dtype, k_cache, v_cache, kv_dtype, qo_indptr, kv_ind
     rc = lib.orc_paged_attention(
         batch, num_qo_heads, num_kv_heads, head_dim, page_size, num_pages,
         _ptr(qo_indptr), _ptr(kv_indptr), _ptr(kv_indices), _ptr(last_page_len),
-        DTYPE_CODES[q_dtype], _ptr(q), float(q_scale),
+        DTYPE_CODES[q_dtype], _ptr(q), scales["q"][0],
         DTYPE_CODES[kv_dtype], _ptr(k_cache), _ptr(v_cache),
-        float(k_scale), float(v_scale), float(sm_scale), int(bool(causal)), hnd,
+        scales["k"][0], scales["v"][0], float(sm_scale), int(bool(causal)), hnd,
+        *[None if scales[x][1] is None else _ptr(scales[x][1]) for x in ("q", "k", "v")],
         n, None if sel_r is None else _ptr(sel_r), None if sel_h is None else _ptr(sel_h),
         _ptr(o), _ptr(lse))
     if rc != 0:

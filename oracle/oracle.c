@@ -17,6 +17,9 @@
  *      kernel", Test plan (k_scale into sm_scale, v_scale linear on the
  *      output) are equivalent to.  The query scale is the FP8 BMM1 scale of
  *      "Enable Hopper FA3 FP8 attention in decode.py", review note on q_scale.
+ *      The scales may instead be per-head scale tensors (the "FP8 scale
+ *      tensors" that page threads through): q_scale[h] for query head h,
+ *      k_scale[h_kv] and v_scale[h_kv] for KV head h_kv, applied the same way.
  *   3. The KV rows of request b are gathered through the CSR page table
  *      (kv_indptr, kv_indices, last_page_len): token t lives in page
  *      kv_indices[kv_indptr[b] + t / P], slot t % P.
@@ -265,6 +268,7 @@ int orc_paged_attention(
     int q_dtype, const void *q, double q_scale,
     int kv_dtype, const void *k_cache, const void *v_cache,
     double k_scale, double v_scale, double sm_scale, int causal, int kv_layout,
+    const double *q_scales, const double *k_scales, const double *v_scales,
     int64_t n_sel, const int64_t *sel_row, const int32_t *sel_head,
     double *o, double *lse)
 {
@@ -326,10 +330,14 @@ int orc_paged_attention(
             const int64_t np = kv_indptr[b + 1] - kv_indptr[b];
             const int64_t kv_len = np > 0 ? (np - 1) * P + last_page_len[b] : 0;
             const int64_t h_kv = h / group;
+            /* Per-tensor scales, or per-head scale tensors (query head h, KV head h_kv). */
+            const double qs = q_scales ? q_scales[h] : q_scale;
+            const double ks = k_scales ? k_scales[h_kv] : k_scale;
+            const double vs = v_scales ? v_scales[h_kv] : v_scale;
 
             /* Step 2: Q^ for this row and head. */
             for (int64_t d = 0; d < D; ++d)
-                qh[d] = orc_decode_one(q_dtype, q, (row * Hq + h) * D + d) * q_scale;
+                qh[d] = orc_decode_one(q_dtype, q, (row * Hq + h) * D + d) * qs;
 
             /* Admissible keys: j < n_keys. */
             int64_t n_keys = kv_len;
@@ -346,7 +354,7 @@ int orc_paged_attention(
                 const int64_t base = orc_row_offset(kv_layout, page, slot, h_kv, P, Hkv, D);
                 double acc = 0.0;
                 for (int64_t d = 0; d < D; ++d)
-                    acc += qh[d] * (orc_decode_one(kv_dtype, k_cache, base + d) * k_scale);
+                    acc += qh[d] * (orc_decode_one(kv_dtype, k_cache, base + d) * ks);
                 s[j] = sm_scale * acc;
             }
 
@@ -366,7 +374,7 @@ int orc_paged_attention(
                 const int64_t slot = j % P;
                 const int64_t base = orc_row_offset(kv_layout, page, slot, h_kv, P, Hkv, D);
                 for (int64_t d = 0; d < D; ++d)
-                    ok[d] += p * (orc_decode_one(kv_dtype, v_cache, base + d) * v_scale);
+                    ok[d] += p * (orc_decode_one(kv_dtype, v_cache, base + d) * vs);
             }
             lse[k] = m + log(l);
         }

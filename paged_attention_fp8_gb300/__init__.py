@@ -41,7 +41,8 @@ _NAME_CODES = {"default": DTYPE_DEFAULT, "f16": F16, "float16": F16, "bf16": BF1
 # Every entry point include/pafp8.h declares.
 EXPORTS = ("pafp8_abi_version", "pafp8_last_error", "pafp8_plan_create", "pafp8_plan_destroy",
            "pafp8_workspace_bytes", "pafp8_plan_metadata", "pafp8_plan_upload", "pafp8_run",
-           "pafp8_run_stage", "pafp8_device_status", "pafp8_run_decode_noalloc", "pafp8_append_kv")
+           "pafp8_run_stage", "pafp8_device_status", "pafp8_run_decode_noalloc", "pafp8_append_kv",
+           "pafp8_run_head_scales")
 
 
 class Pafp8Error(RuntimeError):
@@ -99,6 +100,8 @@ def lib() -> ctypes.CDLL:
     L.pafp8_append_kv.argtypes = [i32, vp, vp, ctypes.c_int64, i32, i32, vp, vp, i32, vp, vp, i32, i32, vp,
                                   vp, i32, i32, f32, f32, vp, vp]
     L.pafp8_append_kv.restype = i32
+    L.pafp8_run_head_scales.argtypes = [vp, i32, vp, i32, vp, i32, vp, vp, vp, vp, vp, i32, vp, vp, vp, sz, vp]
+    L.pafp8_run_head_scales.restype = i32
     _lib = L
     return L
 
@@ -207,6 +210,20 @@ def pafp8_run_stage(handle: int, stage: int, q, k_cache, v_cache, kv_indices, o,
         _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
+def pafp8_run_head_scales(handle: int, q, k_cache, v_cache, kv_indices, o, lse, workspace, *, q_scales=None,
+                          k_scales, v_scales, q_dtype=None, k_dtype=None, v_dtype=None, o_dtype=None,
+                          stream=None) -> None:
+    """pafp8_run with per-head scale tensors (device float32: q_scales [Hq] or
+    None, k_scales and v_scales [Hkv])."""
+    _check(lib().pafp8_run_head_scales(
+        handle, dtype_code(q_dtype if q_dtype is not None else q.dtype), _ptr(q),
+        dtype_code(k_dtype if k_dtype is not None else k_cache.dtype), _ptr(k_cache),
+        dtype_code(v_dtype if v_dtype is not None else v_cache.dtype), _ptr(v_cache),
+        _ptr(kv_indices), _ptr(q_scales), _ptr(k_scales), _ptr(v_scales),
+        dtype_code(o_dtype if o_dtype is not None else o.dtype), _ptr(o), _ptr(lse),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
 def pafp8_device_status(handle: int, workspace, stream=None) -> None:
     _check(lib().pafp8_device_status(handle, _ptr(workspace), _stream(stream)))
 
@@ -281,6 +298,9 @@ class Plan:
 
     def run(self, q, k_cache, v_cache, kv_indices, o, lse, workspace, **kw) -> None:
         pafp8_run(self.handle, q, k_cache, v_cache, kv_indices, o, lse, workspace, **kw)
+
+    def run_head_scales(self, q, k_cache, v_cache, kv_indices, o, lse, workspace, **kw) -> None:
+        pafp8_run_head_scales(self.handle, q, k_cache, v_cache, kv_indices, o, lse, workspace, **kw)
 
     def run_stage(self, stage, q, k_cache, v_cache, kv_indices, o, lse, workspace, **kw) -> None:
         pafp8_run_stage(self.handle, stage, q, k_cache, v_cache, kv_indices, o, lse, workspace, **kw)

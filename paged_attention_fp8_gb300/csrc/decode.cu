@@ -309,7 +309,23 @@ __global__ void __launch_bounds__(32 * 9, 1)
         const size_t q_head_off = ((size_t)b * Hq + (size_t)kvh * group + g) * D;
         const float qfactor = load_q<kBF>(qf, qlo, p.q, p.q_dtype, q_head_off, g < group, t);
         const bool split_q = kBF && p.q_dtype == PAFP8_F16;
-        const float sc = p.sm_scale_log2 * qfactor;
+        // log2 softmax scale of heads 2t and 2t+1 (this lane's S columns).
+        // Per-query-head scales exist only for an fp8 query, which a 2-byte
+        // cache never has: there one scale serves both columns.
+        float sc0 = p.sm_scale_log2 * qfactor, sc1 = sc0;
+        if (p.k_scales != nullptr) {
+            const float ks = __ldg(p.k_scales + kvh);
+            if constexpr (k2) {
+                sc0 = fold_scale_log2(p.sm_scale, 1.0f, ks) * qfactor;
+            } else {
+                const int h0 = kvh * group + min(2 * t, group - 1), h1 = kvh * group + min(2 * t + 1, group - 1);
+                const float q0 = p.q_scales != nullptr ? __ldg(p.q_scales + h0) : 1.0f;
+                const float q1 = p.q_scales != nullptr ? __ldg(p.q_scales + h1) : 1.0f;
+                sc0 = fold_scale_log2(p.sm_scale, q0, ks) * qfactor;
+                sc1 = fold_scale_log2(p.sm_scale, q1, ks) * qfactor;
+            }
+        }
+        if constexpr (k2) sc1 = sc0;
 
         float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
         float acc[8][4];
@@ -427,8 +443,8 @@ __global__ void __launch_bounds__(32 * 9, 1)
                 }
             }
             // (tok g | tok g+8) x (head 2t | head 2t+1), log2 units.
-            float x0 = (sa[0] + sb[0]) * sc, x1 = (sa[1] + sb[1]) * sc;
-            float x2 = (sa[2] + sb[2]) * sc, x3 = (sa[3] + sb[3]) * sc;
+            float x0 = (sa[0] + sb[0]) * sc0, x1 = (sa[1] + sb[1]) * sc1;
+            float x2 = (sa[2] + sb[2]) * sc0, x3 = (sa[3] + sb[3]) * sc1;
             if (g >= valid) x0 = x1 = -INFINITY;
             if (g + 8 >= valid) x2 = x3 = -INFINITY;
             float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
@@ -501,7 +517,7 @@ __global__ void __launch_bounds__(32 * 9, 1)
             }
             const int head = kvh * group + n;
             if (slot < 0) {
-                const float vs = p.v_scale;
+                const float vs = p.v_scales != nullptr ? __ldg(p.v_scales + kvh) : p.v_scale;
                 uint32_t w[8];
 #pragma unroll
                 for (int i = 0; i < 8; ++i) w[i] = pack_out2(vals[2 * i] * vs, vals[2 * i + 1] * vs, p.o_dtype);
@@ -567,7 +583,7 @@ __global__ void __launch_bounds__(128)
     }
     const int head = hb * hpb + hh;  // query head: (hb * hpc + hh / group) * group + hh % group
     const size_t oh = (size_t)b * p.num_qo_heads + head;
-    const float val = acc / sum * p.v_scale;
+    const float val = acc / sum * (p.v_scales != nullptr ? __ldg(p.v_scales + head / group) : p.v_scale);
     uint16_t* dst = static_cast<uint16_t*>(p.o) + oh * D + d;
     if (p.o_dtype == PAFP8_BF16) {
         __nv_bfloat16 h = __float2bfloat16_rn(val);

@@ -700,21 +700,18 @@ pafp8_status pafp8_plan_upload(pafp8_plan* plan, void* workspace, size_t workspa
     return PAFP8_OK;
 }
 
-pafp8_status pafp8_run(const pafp8_plan* plan, int32_t q_dtype, const void* q, int32_t k_dtype,
-                       const void* k_cache, int32_t v_dtype, const void* v_cache,
-                       const int32_t* kv_indices, float q_scale, float k_scale, float v_scale,
-                       int32_t o_dtype, void* o, float* lse, void* workspace,
-                       size_t workspace_bytes, void* stream) {
-    return pafp8_run_stage(plan, 0, q_dtype, q, k_dtype, k_cache, v_dtype, v_cache, kv_indices,
-                           q_scale, k_scale, v_scale, o_dtype, o, lse, workspace, workspace_bytes,
-                           stream);
-}
+}  // extern "C"
 
-pafp8_status pafp8_run_stage(const pafp8_plan* plan, int32_t stage, int32_t q_dtype, const void* q,
-                             int32_t k_dtype, const void* k_cache, int32_t v_dtype,
-                             const void* v_cache, const int32_t* kv_indices, float q_scale,
-                             float k_scale, float v_scale, int32_t o_dtype, void* o, float* lse,
-                             void* workspace, size_t workspace_bytes, void* stream) {
+namespace {
+
+// Shared body of the run entry points.  Per-head scale tensors (device
+// arrays) replace the per-tensor scales when k_scales is not NULL.
+pafp8_status run_impl(const pafp8_plan* plan, int32_t stage, int32_t q_dtype, const void* q,
+                      int32_t k_dtype, const void* k_cache, int32_t v_dtype, const void* v_cache,
+                      const int32_t* kv_indices, float q_scale, float k_scale, float v_scale,
+                      const float* q_scales, const float* k_scales, const float* v_scales,
+                      int32_t o_dtype, void* o, float* lse, void* workspace, size_t workspace_bytes,
+                      void* stream) {
     if (plan == nullptr) return fail(PAFP8_ERR_ARG, "plan is NULL");
     if (stage < 0 || stage > 2) return fail(PAFP8_ERR_ARG, "stage %d is not 0, 1 or 2", (int)stage);
     const pafp8_plan_desc& d = plan->desc;
@@ -742,6 +739,17 @@ pafp8_status pafp8_run_stage(const pafp8_plan* plan, int32_t stage, int32_t q_dt
                     "q_scale %g given with a %s query: only an fp8 query is dequantized by "
                     "q_scale, so it would be silently ignored",
                     (double)q_scale, dtype_name(q_dtype));
+    if (k_scales != nullptr) {
+        if (v_scales == nullptr)
+            return fail(PAFP8_ERR_ARG, "per-head scales need both k_scales and v_scales");
+        if (is_2byte(q_dtype) && q_scales != nullptr)
+            return fail(PAFP8_ERR_ARG,
+                        "q_scales given with a %s query: only an fp8 query is dequantized by its "
+                        "scales, so they would be silently ignored",
+                        dtype_name(q_dtype));
+        if (((uintptr_t)q_scales | (uintptr_t)k_scales | (uintptr_t)v_scales) % 4 != 0)
+            return fail(PAFP8_ERR_ARG, "q_scales, k_scales and v_scales must be 4-byte aligned");
+    }
     if (workspace == nullptr || workspace != plan->uploaded_ws)
         return fail(PAFP8_ERR_WORKSPACE,
                     "workspace %p is not the one this plan's metadata was uploaded to (%p)",
@@ -781,6 +789,10 @@ pafp8_status pafp8_run_stage(const pafp8_plan* plan, int32_t stage, int32_t q_dt
         pp.tile_tokens = kTileRows / plan->group;
         pp.sm_scale_log2 = sm_log2;
         pp.v_scale = v_scale;
+        pp.q_scales = k_scales != nullptr ? q_scales : nullptr;
+        pp.k_scales = k_scales;
+        pp.v_scales = k_scales != nullptr ? v_scales : nullptr;
+        pp.sm_scale = d.sm_scale;
         CUtensorMap tq, tk, tv;
         if ((st = encode_q_map(&tq, q, (int)plan->nnz_qo, d.num_qo_heads, plan->group,
                                pp.tile_tokens, is_fp8(q_dtype))) != PAFP8_OK)
@@ -822,6 +834,10 @@ pafp8_status pafp8_run_stage(const pafp8_plan* plan, int32_t stage, int32_t q_dt
     p.num_pages = d.num_pages;
     p.sm_scale_log2 = sm_log2;
     p.v_scale = v_scale;
+    p.q_scales = k_scales != nullptr ? q_scales : nullptr;
+    p.k_scales = k_scales;
+    p.v_scales = k_scales != nullptr ? v_scales : nullptr;
+    p.sm_scale = d.sm_scale;
 
     cudaError_t e = cudaSuccess;
     if (stage != 2 && plan->num_ctas > 0) {
@@ -839,6 +855,40 @@ pafp8_status pafp8_run_stage(const pafp8_plan* plan, int32_t stage, int32_t q_dt
         return fail(PAFP8_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(e));
     }
     return PAFP8_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+pafp8_status pafp8_run(const pafp8_plan* plan, int32_t q_dtype, const void* q, int32_t k_dtype,
+                       const void* k_cache, int32_t v_dtype, const void* v_cache,
+                       const int32_t* kv_indices, float q_scale, float k_scale, float v_scale,
+                       int32_t o_dtype, void* o, float* lse, void* workspace,
+                       size_t workspace_bytes, void* stream) {
+    return run_impl(plan, 0, q_dtype, q, k_dtype, k_cache, v_dtype, v_cache, kv_indices, q_scale, k_scale,
+                    v_scale, nullptr, nullptr, nullptr, o_dtype, o, lse, workspace, workspace_bytes, stream);
+}
+
+pafp8_status pafp8_run_stage(const pafp8_plan* plan, int32_t stage, int32_t q_dtype, const void* q,
+                             int32_t k_dtype, const void* k_cache, int32_t v_dtype,
+                             const void* v_cache, const int32_t* kv_indices, float q_scale,
+                             float k_scale, float v_scale, int32_t o_dtype, void* o, float* lse,
+                             void* workspace, size_t workspace_bytes, void* stream) {
+    return run_impl(plan, stage, q_dtype, q, k_dtype, k_cache, v_dtype, v_cache, kv_indices, q_scale,
+                    k_scale, v_scale, nullptr, nullptr, nullptr, o_dtype, o, lse, workspace,
+                    workspace_bytes, stream);
+}
+
+pafp8_status pafp8_run_head_scales(const pafp8_plan* plan, int32_t q_dtype, const void* q,
+                                   int32_t k_dtype, const void* k_cache, int32_t v_dtype,
+                                   const void* v_cache, const int32_t* kv_indices, const float* q_scales,
+                                   const float* k_scales, const float* v_scales, int32_t o_dtype, void* o,
+                                   float* lse, void* workspace, size_t workspace_bytes, void* stream) {
+    if (k_scales == nullptr || v_scales == nullptr)
+        return fail(PAFP8_ERR_ARG, "k_scales and v_scales (device arrays of num_kv_heads floats) are required");
+    return run_impl(plan, 0, q_dtype, q, k_dtype, k_cache, v_dtype, v_cache, kv_indices, 1.0f, 1.0f, 1.0f,
+                    q_scales, k_scales, v_scales, o_dtype, o, lse, workspace, workspace_bytes, stream);
 }
 
 pafp8_status pafp8_device_status(const pafp8_plan* plan, void* workspace, void* stream) {

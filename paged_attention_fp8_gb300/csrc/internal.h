@@ -47,6 +47,13 @@ enum MetaHeader : int {
 };
 constexpr int32_t kMetaMagicValue = 0x38464150;
 
+// log2-domain softmax scale of one head from per-head scales, folded in
+// double in the same order as the host folds the per-tensor ones, so equal
+// scales give the same float.
+__device__ __forceinline__ float fold_scale_log2(float sm_scale, float q_scale, float k_scale) {
+    return (float)((double)sm_scale * (double)q_scale * (double)k_scale * 1.4426950408889634);
+}
+
 // Status word bits written by the kernels into the workspace.
 enum : uint32_t {
     kStatusBounds = 1u,   // a page index outside [0, num_pages)
@@ -66,6 +73,13 @@ struct DecodeParams {
     int num_qo_heads, num_kv_heads, num_pages;
     float sm_scale_log2;     // sm_scale * q_scale * k_scale * log2(e)
     float v_scale;
+    // Per-head scale tensors (device arrays) instead of the per-tensor scales
+    // folded above, when k_scales is not null: q_scales [Hq] (or null: 1),
+    // k_scales and v_scales [Hkv]; the kernels fold sm_scale with them.
+    const float* q_scales;
+    const float* k_scales;
+    const float* v_scales;
+    float sm_scale;
 };
 
 struct AppendParams {
@@ -98,6 +112,13 @@ struct PrefillParams {
     int tile_tokens;         // query tokens per 128-row tile (128 / group)
     float sm_scale_log2;     // sm_scale * q_scale * k_scale * log2(e)
     float v_scale;
+    // Per-head scale tensors (device arrays) instead of the per-tensor scales
+    // folded above, when k_scales is not null: q_scales [Hq] (or null: 1),
+    // k_scales and v_scales [Hkv]; the kernels fold sm_scale with them.
+    const float* q_scales;
+    const float* k_scales;
+    const float* v_scales;
+    float sm_scale;
 };
 
 // Launchers (decode.cu, prefill.cu).  Return the launch's cudaError_t.

@@ -652,7 +652,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int tok = r / g, hh = r - tok * g;
             const bool valid_row = (tok < TQ) && (t0 + tok < qo_len);
             const int limit = valid_row ? t0 + tok + kv_len - qo_len : -1;
-            const float scale = p.sm_scale_log2 * up_next;
+            float scale = p.sm_scale_log2 * up_next;
+            float vsc = p.v_scale;
+            if (p.k_scales != nullptr) {  // per-head scale tensors
+                const int qh = it.hk * g + min(hh, g - 1);
+                scale = fold_scale_log2(p.sm_scale, p.q_scales != nullptr ? __ldg(p.q_scales + qh) : 1.0f,
+                                        __ldg(p.k_scales + it.hk)) *
+                        up_next;
+                vsc = __ldg(p.v_scales + it.hk);
+            }
             float m = -INFINITY, l = 0.f;  // m in scaled (log2) units
             for (int j = 0; j < nX && ok; ++j) {
                 ok = __all_sync(0xFFFFFFFFu, wait_or_abort(bar(L::bSFull + x), sphase, flag_addr, p.status));
@@ -761,7 +769,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ophase ^= 1u;
             if (!ok) break;
             tc_fence_after();
-            const float inv = valid_row && l > 0.f ? p.v_scale / l : 0.f;
+            const float inv = valid_row && l > 0.f ? vsc / l : 0.f;
             const size_t orow = (size_t)(qo0 + t0 + tok) * p.num_qo_heads + (size_t)it.hk * g + hh;
             if (kF8 && t0 + TQ <= qo_len) {
                 // A full tile: two rounds of 64 dims through this tile's staging

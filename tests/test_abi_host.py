@@ -363,3 +363,17 @@ def test_append_refuses_before_touching_memory(over, status, word):
 
 def test_append_of_nothing_is_a_no_op():
     assert _append_raw(nnz=0, k_new=None, v_new=None, k_cache=None, v_cache=None) == 0
+
+
+@pytest.mark.parametrize("q,qs,ks,vs,word", [
+    (pa.BF16, None, None, 64, "k_scales and v_scales"), (pa.BF16, None, 64, None, "k_scales and v_scales"),
+    (pa.BF16, 64, 64, 64, "silently ignored"), (pa.E4M3FN, 66, 64, 64, "4-byte"),
+    (pa.E4M3FN, None, 64, 62, "4-byte")])
+def test_run_head_scales_refuses_before_touching_memory(q, qs, ks, vs, word):
+    h = _create(q_dtype=q)
+    try:
+        st = pa.lib().pafp8_run_head_scales(h, q, 16, pa.E4M3FN, 16, pa.E4M3FN, 16, 16, qs, ks, vs, pa.BF16, 16,
+                                            None, 256, 1 << 20, None)
+        assert st == 3 and word in pa.pafp8_last_error(), pa.pafp8_last_error()
+    finally:
+        pa.pafp8_plan_destroy(h)

@@ -347,3 +347,30 @@ def test_hnd_layout_reads_the_same_rows(mode):
     # the HND bytes read as NHD are a different cache, and give a different result
     o3, _ = oracle_on(b, k_cache=h.k_cache.view(b.k_cache.shape), v_cache=h.v_cache.view(b.v_cache.shape))
     assert not np.allclose(o1, o3)
+
+
+@pytest.mark.parametrize("q_dtype", ["bf16", "e4m3fn"])
+def test_per_head_scales_reduce_to_per_tensor_scales_head_by_head(q_dtype):
+    """Per-head scale tensors: equal entries give the per-tensor result bit for
+    bit, and with distinct entries every query head's output is the
+    per-tensor result computed with that head's own scales (its KV head's k
+    and v scales), so a scale applied to the wrong head fails."""
+    mode_qo = [40, 9, 64]
+    b = make_batch([40, 100, 64], mode_qo, num_qo_heads=8, num_kv_heads=2, q_dtype=q_dtype, seed=67,
+                   pool_pages=16)
+    hq, hkv = 8, 2
+    same = oracle_on(b, q_scale=np.full(hq, b.q_scale), k_scale=np.full(hkv, b.k_scale),
+                     v_scale=np.full(hkv, b.v_scale))
+    ref = oracle_on(b)
+    assert np.array_equal(same[0], ref[0]) and np.array_equal(same[1], ref[1])
+    rng = np.random.default_rng(3)
+    qs = rng.uniform(0.5, 2.0, hq) * b.q_scale if q_dtype == "e4m3fn" else np.ones(hq)
+    ks = rng.uniform(0.5, 2.0, hkv) * b.k_scale
+    vs = rng.uniform(0.5, 2.0, hkv) * b.v_scale
+    o, lse = oracle_on(b, q_scale=qs, k_scale=ks, v_scale=vs)
+    for h in range(hq):
+        hk = h // (hq // hkv)
+        oh, lh = oracle_on(b, q_scale=qs[h], k_scale=ks[hk], v_scale=vs[hk])
+        assert np.allclose(o[:, h], oh[:, h], rtol=1e-12, atol=1e-15)
+        assert np.allclose(lse[:, h], lh[:, h], rtol=1e-12, atol=1e-12)
+    assert not np.allclose(o, ref[0])
