@@ -6,7 +6,10 @@ fixed-split and disable-split options; the balanced rule is this library's):
 
 * Rows are (request b, KV-head block hb), row r = b * nhb + hb, where a block
   holds hpc KV heads, hpc = the largest divisor of num_kv_heads that is <= 8,
-  and nhb = num_kv_heads / hpc.  Row r holds npages[b] pages.
+  and nhb = num_kv_heads / hpc.  Row r holds npages[b] pages of 16 tokens:
+  ceil(kv_len / 16), where kv_len = (pages - 1) * page_size + last_page_len
+  (a page of page_size = 16 m tokens counts as m 16-token pages; for
+  page_size 16 this is the request's page count).
 * disable_split_kv: one segment (r, 0, npages) per non-empty row; segment k
   goes to CTA k mod G, G = min(num_ctas, #segments).
 * fixed_split_pages = c > 0: each row cut into [0,c), [c,2c), ...; dealt the
@@ -46,8 +49,10 @@ def decode_metadata(kv_indptr, last_page_len, *, num_qo_heads, num_kv_heads, num
     group = num_qo_heads // num_kv_heads
     npages = []
     for b in range(B):
+        n = kv_indptr[b + 1] - kv_indptr[b]
+        kv = (n - 1) * page_size + last_page_len[b] if n > 0 else 0
         for _ in range(nhb):
-            npages.append(kv_indptr[b + 1] - kv_indptr[b])
+            npages.append((kv + 15) // 16)
     R = B * nhb
 
     per_cta = []

@@ -107,7 +107,7 @@ __global__ void __launch_bounds__(kThreads) append_kernel(const AppendParams p) 
         int page = -1;
         if (b >= 0 && b < p.batch && pos >= 0) {
             const int e0 = __ldg(p.kv_indptr + b), e1 = __ldg(p.kv_indptr + b + 1);
-            const long long e = (long long)e0 + pos / kPageSize;
+            const long long e = (long long)e0 + pos / p.page_size;
             if (e0 >= 0 && e < e1) {
                 const int pg = __ldg(p.kv_indices + e);
                 if (pg >= 0 && pg < p.num_pages) page = pg;
@@ -117,9 +117,9 @@ __global__ void __launch_bounds__(kThreads) append_kernel(const AppendParams p) 
             if (c == 0 && p.status != nullptr) atomicOr(p.status, kStatusBounds);
             continue;
         }
-        const size_t slot = (size_t)(pos % kPageSize);
-        const size_t dst = (p.hnd ? ((size_t)page * p.num_kv_heads + h) * kPageSize + slot
-                                  : ((size_t)page * kPageSize + slot) * p.num_kv_heads + h) * D + 16 * c;
+        const size_t slot = (size_t)(pos % p.page_size);
+        const size_t dst = (p.hnd ? ((size_t)page * p.num_kv_heads + h) * p.page_size + slot
+                                  : ((size_t)page * p.page_size + slot) * p.num_kv_heads + h) * D + 16 * c;
         *reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.k_cache) + dst) = quantize16<KV>(rk, p.k_inv);
         *reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.v_cache) + dst) = quantize16<KV>(rv, p.v_inv);
     }

@@ -215,9 +215,10 @@ __global__ void __launch_bounds__(32 * 9, 1)
             const int* idx = p.kv_indices + req_page[b];
             for (int pb = p0; pb < p1 && ok; pb += 32) {
                 const int n = min(32, p1 - pb);
-                int page = lane < n ? __ldg(idx + pb + lane) : 0;
-                const bool bad = lane < n && (page < 0 || page >= p.num_pages);
-                if (bad) page = 0;  // never read outside the pool
+                // Pool ids of 16-token sub-pages (a page of 16 * m tokens is m of
+                // them); an id outside the pool reads page 0 instead.
+                bool bad = false;
+                const int page = lane < n ? sub_page(idx, pb + lane, p.page_mult, p.num_pages, bad) : 0;
                 if (__any_sync(0xFFFFFFFFu, bad) && lane == 0) flag(p.status, kStatusBounds);
                 for (int j = 0; j < n; ++j) {
                     const int pg = __shfl_sync(0xFFFFFFFFu, page, j);

@@ -126,6 +126,11 @@ struct pafp8_plan {
     std::vector<int32_t> meta;
     int64_t nnz_pages = 0, nnz_qo = 0;
     int heads_per_cta = 1, head_blocks = 1, group = 1;
+    // Pages of page_size = 16 * page_mult tokens are read as page_mult
+    // consecutive 16-token sub-pages; vptr is the CSR of sub-pages per
+    // request (ceil(kv_len / 16)), the unit of the decode partition.
+    int page_mult = 1;
+    std::vector<int32_t> vptr;
     int num_ctas = 0, num_partials = 0, num_merge = 0;
     size_t meta_bytes = 0, part_o_off = 0, part_lse_off = 0, status_off = 0, ws_bytes = 0;
     void* uploaded_ws = nullptr;
@@ -157,7 +162,7 @@ void build_decode_meta(pafp8_plan* pl) {
     std::vector<int64_t> np(R);
     for (int b = 0; b < B; ++b)
         for (int hb = 0; hb < nhb; ++hb)
-            np[(size_t)b * nhb + hb] = pl->kv_indptr[b + 1] - pl->kv_indptr[b];
+            np[(size_t)b * nhb + hb] = pl->vptr[b + 1] - pl->vptr[b];
 
     struct Seg { int32_t row, p0, p1, slot; };
     std::vector<std::vector<Seg>> per_cta;
@@ -579,12 +584,20 @@ pafp8_status pafp8_plan_create(const pafp8_plan_desc* desc_in, const int32_t* kv
     if (d.head_dim != kHeadDim)
         return fail(PAFP8_ERR_UNSUPPORTED, "head_dim %d is not served by this build (only %d)",
                     (int)d.head_dim, kHeadDim);
-    if (d.page_size != kPageSize)
-        return fail(PAFP8_ERR_UNSUPPORTED, "page_size %d is not served by this build (only %d)",
-                    (int)d.page_size, kPageSize);
     if (d.num_pages < 0) return fail(PAFP8_ERR_SHAPE, "num_pages %d is negative", (int)d.num_pages);
     if (d.kv_layout != PAFP8_LAYOUT_NHD && d.kv_layout != PAFP8_LAYOUT_HND)
         return fail(PAFP8_ERR_ARG, "kv_layout %d is neither NHD (0) nor HND (1)", (int)d.kv_layout);
+    if (d.page_size <= 0 || d.page_size % kPageSize != 0 ||
+        (int64_t)d.num_pages * (d.page_size / kPageSize) > INT32_MAX)
+        return fail(PAFP8_ERR_UNSUPPORTED,
+                    "page_size %d is not served by this build (a multiple of %d tokens, with "
+                    "num_pages * page_size / %d below 2^31)",
+                    (int)d.page_size, kPageSize, kPageSize);
+    if (d.page_size != kPageSize && d.kv_layout == PAFP8_LAYOUT_HND)
+        return fail(PAFP8_ERR_UNSUPPORTED,
+                    "the HND layout is served with page_size %d only (got %d); NHD takes any "
+                    "multiple of %d",
+                    kPageSize, (int)d.page_size, kPageSize);
     if (std::isnan(d.sm_scale) || std::isinf(d.sm_scale))
         return fail(PAFP8_ERR_ARG, "sm_scale is not finite");
     if (d.sm_scale <= 0.0f) d.sm_scale = 1.0f / std::sqrt((float)d.head_dim);
@@ -650,6 +663,13 @@ pafp8_status pafp8_plan_create(const pafp8_plan_desc* desc_in, const int32_t* kv
         pl->kv_indptr.assign(1, 0);
     }
     pl->nnz_pages = pl->kv_indptr.back();
+    pl->page_mult = d.page_size / kPageSize;
+    pl->vptr.assign((size_t)d.batch + 1, 0);
+    for (int b = 0; b < d.batch; ++b) {
+        const int64_t n = (int64_t)pl->kv_indptr[b + 1] - pl->kv_indptr[b];
+        const int64_t kv = n > 0 ? (n - 1) * d.page_size + pl->last_page_len[b] : 0;
+        pl->vptr[b + 1] = pl->vptr[b] + (int32_t)((kv + kPageSize - 1) / kPageSize);
+    }
     if (d.mode == PAFP8_MODE_PREFILL) {
         if (d.batch > 0)
             pl->qo_indptr.assign(qo_indptr_h, qo_indptr_h + d.batch + 1);
@@ -770,6 +790,7 @@ pafp8_status run_impl(const pafp8_plan* plan, int32_t stage, int32_t q_dtype, co
     char* ws = (char*)workspace;
     const float sm_log2 = (float)((double)d.sm_scale * (is_fp8(q_dtype) ? (double)q_scale : 1.0) *
                                   (double)k_scale * 1.4426950408889634);
+    const int vpages = d.num_pages * plan->page_mult;  // 16-token sub-pages of the pool
     if (d.mode == PAFP8_MODE_PREFILL) {
         if (stage == 2 || plan->num_ctas == 0) return PAFP8_OK;  // prefill has no merge stage
         PrefillParams pp{};
@@ -785,6 +806,7 @@ pafp8_status run_impl(const pafp8_plan* plan, int32_t stage, int32_t q_dtype, co
         pp.num_qo_heads = d.num_qo_heads;
         pp.num_kv_heads = d.num_kv_heads;
         pp.num_pages = d.num_pages;
+        pp.page_mult = plan->page_mult;
         pp.group = plan->group;
         pp.tile_tokens = kTileRows / plan->group;
         pp.sm_scale_log2 = sm_log2;
@@ -798,13 +820,13 @@ pafp8_status run_impl(const pafp8_plan* plan, int32_t stage, int32_t q_dtype, co
                                pp.tile_tokens, is_fp8(q_dtype))) != PAFP8_OK)
             return st;
         if (is_2byte(k_dtype)) {
-            if ((st = encode_cache_map_2byte(&tk, k_cache, d.num_pages, d.num_kv_heads, d.kv_layout)) != PAFP8_OK)
+            if ((st = encode_cache_map_2byte(&tk, k_cache, vpages, d.num_kv_heads, d.kv_layout)) != PAFP8_OK)
                 return st;
-            if ((st = encode_cache_map_2byte(&tv, v_cache, d.num_pages, d.num_kv_heads, d.kv_layout)) != PAFP8_OK)
+            if ((st = encode_cache_map_2byte(&tv, v_cache, vpages, d.num_kv_heads, d.kv_layout)) != PAFP8_OK)
                 return st;
         } else {
-            if ((st = encode_cache_map(&tk, k_cache, d.num_pages, d.num_kv_heads, d.kv_layout)) != PAFP8_OK) return st;
-            if ((st = encode_cache_map(&tv, v_cache, d.num_pages, d.num_kv_heads, d.kv_layout)) != PAFP8_OK) return st;
+            if ((st = encode_cache_map(&tk, k_cache, vpages, d.num_kv_heads, d.kv_layout)) != PAFP8_OK) return st;
+            if ((st = encode_cache_map(&tv, v_cache, vpages, d.num_kv_heads, d.kv_layout)) != PAFP8_OK) return st;
         }
         CUtensorMap to;
         if ((st = encode_q_map(&to, o, (int)plan->nnz_qo, d.num_qo_heads, plan->group, pp.tile_tokens,
@@ -832,6 +854,7 @@ pafp8_status run_impl(const pafp8_plan* plan, int32_t stage, int32_t q_dtype, co
     p.num_qo_heads = d.num_qo_heads;
     p.num_kv_heads = d.num_kv_heads;
     p.num_pages = d.num_pages;
+    p.page_mult = plan->page_mult;
     p.sm_scale_log2 = sm_log2;
     p.v_scale = v_scale;
     p.q_scales = k_scales != nullptr ? q_scales : nullptr;
@@ -843,7 +866,7 @@ pafp8_status run_impl(const pafp8_plan* plan, int32_t stage, int32_t q_dtype, co
     if (stage != 2 && plan->num_ctas > 0) {
         CUtensorMap tk, tv;
         int hpb = 1;
-        if ((st = encode_decode_maps(&tk, &tv, k_cache, v_cache, d.num_pages, d.num_kv_heads,
+        if ((st = encode_decode_maps(&tk, &tv, k_cache, v_cache, vpages, d.num_kv_heads,
                                      plan->heads_per_cta, &hpb, is_2byte(k_dtype), d.kv_layout)) != PAFP8_OK)
             return st;
         e = launch_decode(p, tk, tv, plan->num_ctas, plan->heads_per_cta, plan->group, hpb, s);
@@ -990,13 +1013,14 @@ pafp8_status pafp8_run_decode_noalloc(const pafp8_plan* plan, int32_t q_dtype, c
     p.num_qo_heads = d.num_qo_heads;
     p.num_kv_heads = d.num_kv_heads;
     p.num_pages = d.num_pages;
+    p.page_mult = plan->page_mult;
     p.sm_scale_log2 = (float)((double)d.sm_scale * (is_fp8(q_dtype) ? (double)q_scale : 1.0) *
                               (double)k_scale * 1.4426950408889634);
     p.v_scale = v_scale;
     if (plan->num_ctas > 0) {
         CUtensorMap tk, tv;
         int hpb = 1;
-        if ((st = encode_decode_maps(&tk, &tv, k_cache, v_cache, d.num_pages, d.num_kv_heads,
+        if ((st = encode_decode_maps(&tk, &tv, k_cache, v_cache, d.num_pages * plan->page_mult, d.num_kv_heads,
                                      plan->heads_per_cta, &hpb, is_2byte(k_dtype), d.kv_layout)) != PAFP8_OK)
             return st;
         e = launch_decode(p, tk, tv, plan->num_ctas, plan->heads_per_cta, plan->group, hpb, s);
@@ -1038,9 +1062,12 @@ pafp8_status pafp8_append_kv(int32_t src_dtype, const void* k_new, const void* v
     if (head_dim != kHeadDim)
         return fail(PAFP8_ERR_UNSUPPORTED, "head_dim %d is not served by this build (only %d)",
                     (int)head_dim, kHeadDim);
-    if (page_size != kPageSize)
-        return fail(PAFP8_ERR_UNSUPPORTED, "page_size %d is not served by this build (only %d)",
+    if (page_size <= 0 || page_size % kPageSize != 0)
+        return fail(PAFP8_ERR_UNSUPPORTED, "page_size %d is not served by this build (a multiple of %d)",
                     (int)page_size, kPageSize);
+    if (page_size != kPageSize && kv_layout == PAFP8_LAYOUT_HND)
+        return fail(PAFP8_ERR_UNSUPPORTED, "the HND layout is served with page_size %d only (got %d)",
+                    kPageSize, (int)page_size);
     if (!scale_ok(k_scale) || !scale_ok(v_scale))
         return fail(PAFP8_ERR_ARG, "scales must be finite and > 0 (k %g, v %g)", (double)k_scale,
                     (double)v_scale);
@@ -1073,6 +1100,7 @@ pafp8_status pafp8_append_kv(int32_t src_dtype, const void* k_new, const void* v
     p.src_dtype = src_dtype;
     p.kv_dtype = kv_dtype;
     p.hnd = kv_layout == PAFP8_LAYOUT_HND;
+    p.page_size = page_size;
     p.k_inv = 1.0f / k_scale;  // IEEE fp32 division: fp32(1/scale)
     p.v_inv = 1.0f / v_scale;
     const cudaError_t e = launch_append(p, (cudaStream_t)stream);

@@ -54,6 +54,16 @@ __device__ __forceinline__ float fold_scale_log2(float sm_scale, float q_scale, 
     return (float)((double)sm_scale * (double)q_scale * (double)k_scale * 1.4426950408889634);
 }
 
+// Pool index of 16-token sub-page `vp` of a request whose page entries start
+// at `idx` (pages of 16 * m tokens): entry vp / m, sub-page vp % m.  `bad` is
+// set, and 0 returned, when the entry lies outside [0, num_pages).
+__device__ __forceinline__ int sub_page(const int32_t* idx, int vp, int m, int num_pages, bool& bad) {
+    const int e = m == 1 ? vp : vp / m;
+    const int pg = __ldg(idx + e);
+    bad = pg < 0 || pg >= num_pages;
+    return bad ? 0 : pg * m + (vp - e * m);
+}
+
 // Status word bits written by the kernels into the workspace.
 enum : uint32_t {
     kStatusBounds = 1u,   // a page index outside [0, num_pages)
@@ -71,6 +81,7 @@ struct DecodeParams {
     uint32_t* status;
     int q_dtype, kv_dtype, o_dtype;
     int num_qo_heads, num_kv_heads, num_pages;
+    int page_mult;           // page_size / 16: a page is read as page_mult 16-token sub-pages
     float sm_scale_log2;     // sm_scale * q_scale * k_scale * log2(e)
     float v_scale;
     // Per-head scale tensors (device arrays) instead of the per-tensor scales
@@ -96,6 +107,7 @@ struct AppendParams {
     int num_kv_heads, batch, num_pages;
     int src_dtype, kv_dtype;
     int hnd;                 // cache layout: 0 [page][slot][head][d], 1 [page][head][slot][d]
+    int page_size;
     float k_inv, v_inv;      // fp32(1 / scale)
 };
 
@@ -108,6 +120,7 @@ struct PrefillParams {
     uint32_t* status;
     int q_dtype, kv_dtype, o_dtype;
     int num_qo_heads, num_kv_heads, num_pages;
+    int page_mult;           // page_size / 16: a page is read as page_mult 16-token sub-pages
     int group;               // query heads per KV head
     int tile_tokens;         // query tokens per 128-row tile (128 / group)
     float sm_scale_log2;     // sm_scale * q_scale * k_scale * log2(e)

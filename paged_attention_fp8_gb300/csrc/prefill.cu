@@ -274,13 +274,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
             qphase ^= 1u;
             const int kv_len = it.kv_len;
+            // 16-token sub-pages of the request (a page of 16 * m tokens is m
+            // of them).  The page entries of the next KV tile are loaded one
+            // tile ahead and checked only when used, so the load's latency
+            // stays hidden.
+            const int m = p.page_mult;
             const int npages = (kv_len + kPageSize - 1) / kPageSize;
             const int* idx = p.kv_indices + it.page0;
-            // Page ids of the next KV tile are fetched one tile ahead.
             int page_next = 0;
             {
                 const int np0 = min(kTileKeys / kPageSize, npages);
-                page_next = lane < np0 ? __ldg(idx + lane) : 0;
+                if (lane < np0) page_next = __ldg(idx + (m == 1 ? lane : lane / m));
             }
             for (int j = 0; j < it.nkv && ok; ++j) {
                 const int pg0 = j * (kTileKeys / kPageSize);
@@ -289,10 +293,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (j + 1 < it.nkv) {
                     const int pg1 = pg0 + kTileKeys / kPageSize;
                     const int np1 = min(kTileKeys / kPageSize, npages - pg1);
-                    page_next = lane < np1 ? __ldg(idx + pg1 + lane) : 0;
+                    page_next = lane < np1 ? __ldg(idx + (m == 1 ? pg1 + lane : (pg1 + lane) / m)) : 0;
                 }
                 const bool bad = lane < np && (page < 0 || page >= p.num_pages);
                 if (bad) page = 0;
+                else if (m != 1) page = page * m + (pg0 + lane) % m;
                 if (__any_sync(0xFFFFFFFFu, bad) && lane == 0) atomicOr(p.status, kStatusBounds);
                 // Page ids live in lanes 0..np-1; lane 0 issues every copy.
                 int pages[8];

@@ -27,7 +27,8 @@ class DeviceBatch:
                             kv_indptr=batch.kv_indptr, last_page_len=batch.last_page_len,
                             qo_indptr=batch.qo_indptr if batch.mode == "prefill" else None,
                             q_dtype=batch.q_dtype, kv_dtype=batch.kv_dtype, o_dtype=batch.o_dtype,
-                            sm_scale=batch.sm_scale, kv_layout=batch.kv_layout, **plan_kw)
+                            sm_scale=batch.sm_scale, kv_layout=batch.kv_layout, page_size=batch.page_size,
+                            **plan_kw)
         self.ws = torch.empty(self.plan.workspace_bytes, dtype=torch.uint8, device=device)
         self.plan.upload(self.ws)
         n = batch.nnz_qo

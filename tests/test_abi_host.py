@@ -44,18 +44,19 @@ def test_exports_every_declared_symbol():
 
 # ------------------------------------------------------------------- plans
 
-def _decode_plan(kv_lens, *, hq=32, hkv=8, num_ctas=152, **kw):
-    P = 16
+def _decode_plan(kv_lens, *, hq=32, hkv=8, num_ctas=152, page_size=16, **kw):
+    P = page_size
     npages = [(L + P - 1) // P for L in kv_lens]
     indptr = np.concatenate([[0], np.cumsum(npages)]).astype(np.int32)
     last = np.array([(L - (n - 1) * P) if n else 0 for L, n in zip(kv_lens, npages)], dtype=np.int32)
     plan = pa.Plan(mode="decode", num_qo_heads=hq, num_kv_heads=hkv, num_pages=max(1, int(indptr[-1])),
                    kv_indptr=indptr, last_page_len=last, q_dtype="bf16", kv_dtype="e4m3fn",
-                   num_ctas=num_ctas, **kw)
+                   num_ctas=num_ctas, page_size=P, **kw)
     ref = plan_rule.decode_metadata(indptr, last, num_qo_heads=hq, num_kv_heads=hkv,
-                                    num_ctas=num_ctas, fixed_split_pages=kw.get("fixed_split_pages", 0),
+                                    num_ctas=num_ctas, page_size=P,
+                                    fixed_split_pages=kw.get("fixed_split_pages", 0),
                                     disable_split_kv=kw.get("disable_split_kv", False))
-    return plan, np.array(ref, dtype=np.int32), npages
+    return plan, np.array(ref, dtype=np.int32), [(L + 15) // 16 for L in kv_lens]
 
 
 PLAN_CASES = [
@@ -69,6 +70,9 @@ PLAN_CASES = [
     dict(kv_lens=[100] * 5, hq=24, hkv=12, num_ctas=9),  # 12 KV heads -> blocks of 6
     dict(kv_lens=[0, 0], hq=4, hkv=4, num_ctas=152),
     dict(kv_lens=[], hq=4, hkv=4, num_ctas=152),
+    dict(kv_lens=[37, 64, 100, 129, 3000], hq=8, hkv=2, num_ctas=11, page_size=32),
+    dict(kv_lens=[1, 1000, 17, 4096], hq=32, hkv=8, num_ctas=152, page_size=64),
+    dict(kv_lens=[129, 300], hq=8, hkv=8, num_ctas=5, page_size=128, fixed_split_pages=3),
 ]
 
 
@@ -179,7 +183,8 @@ def test_plan_refuses_o_dtype(o, word):
 
 
 @pytest.mark.parametrize("over,status", [
-    (dict(num_qo_heads=6, num_kv_heads=4), 2), (dict(head_dim=64), 8), (dict(page_size=32), 8),
+    (dict(num_qo_heads=6, num_kv_heads=4), 2), (dict(head_dim=64), 8), (dict(page_size=24), 8),
+    (dict(page_size=32, kv_layout=1), 8), (dict(page_size=0), 8),
     (dict(num_qo_heads=32, num_kv_heads=2), 8), (dict(mode=5), 3), (dict(num_ctas=-1), 3),
     (dict(fixed_split_pages=-2), 3), (dict(sm_scale=float("nan")), 3), (dict(kv_layout=2), 3)])
 def test_plan_refuses_shapes_and_args(over, status):
@@ -256,17 +261,17 @@ def test_run_refuses_bad_scales():
 
 # ------------------------------------------------------------ prefill plans
 
-def _prefill_plan(kv_lens, qo_lens, *, hq=32, hkv=8, num_ctas=152):
-    P = 16
+def _prefill_plan(kv_lens, qo_lens, *, hq=32, hkv=8, num_ctas=152, page_size=16):
+    P = page_size
     npages = [(L + P - 1) // P for L in kv_lens]
     indptr = np.concatenate([[0], np.cumsum(npages)]).astype(np.int32)
     last = np.array([(L - (n - 1) * P) if n else 0 for L, n in zip(kv_lens, npages)], dtype=np.int32)
     qo_indptr = np.concatenate([[0], np.cumsum(qo_lens)]).astype(np.int32)
     plan = pa.Plan(mode="prefill", num_qo_heads=hq, num_kv_heads=hkv, num_pages=max(1, int(indptr[-1])),
                    kv_indptr=indptr, last_page_len=last, qo_indptr=qo_indptr, q_dtype="bf16",
-                   kv_dtype="e4m3fn", num_ctas=num_ctas)
+                   kv_dtype="e4m3fn", num_ctas=num_ctas, page_size=P)
     ref = plan_rule.prefill_metadata(indptr, last, qo_indptr, num_qo_heads=hq, num_kv_heads=hkv,
-                                     num_ctas=num_ctas)
+                                     num_ctas=num_ctas, page_size=P)
     return plan, np.array(ref, dtype=np.int32)
 
 
@@ -277,6 +282,7 @@ PREFILL_CASES = [
     dict(kv_lens=[300, 700], qo_lens=[300, 33], hq=24, hkv=8, num_ctas=2),
     dict(kv_lens=[2048] * 8, qo_lens=[2048] * 8, hq=32, hkv=8),
     dict(kv_lens=[100, 90], qo_lens=[60, 90], hq=6, hkv=2, num_ctas=1000),
+    dict(kv_lens=[5, 200, 1000, 3000], qo_lens=[5, 40, 1000, 17], hq=32, hkv=8, num_ctas=7, page_size=64),
 ]
 
 
@@ -352,7 +358,8 @@ def _append_raw(**over):
 @pytest.mark.parametrize("over,status,word", [
     (dict(src=pa.E4M3FN), 1, "append takes"), (dict(src=pa.INT8), 1, "int8"),
     (dict(kv=pa.BF16), 8, "bfloat16"), (dict(kv=pa.F16), 8, "float16"), (dict(kv=pa.UINT8), 1, "uint8"),
-    (dict(kv=pa.F32), 1, "float32"), (dict(d=64), 8, "head_dim"), (dict(page_size=32), 8, "page_size"),
+    (dict(kv=pa.F32), 1, "float32"), (dict(d=64), 8, "head_dim"), (dict(page_size=24), 8, "page_size"),
+    (dict(page_size=32, layout=1), 8, "HND"),
     (dict(hkv=0), 2, "num_kv_heads"), (dict(nnz=-1), 2, "negative"), (dict(ks=0.0), 3, "scales"),
     (dict(vs=float("inf")), 3, "scales"), (dict(layout=3), 3, "kv_layout"), (dict(k_new=None), 3, "non-NULL"),
     (dict(indices=None), 3, "non-NULL"), (dict(k_cache=0x70008), 3, "16-byte"), (dict(pos=0x40002), 3, "4-byte")])

@@ -374,3 +374,29 @@ def test_per_head_scales_reduce_to_per_tensor_scales_head_by_head(q_dtype):
         assert np.allclose(o[:, h], oh[:, h], rtol=1e-12, atol=1e-15)
         assert np.allclose(lse[:, h], lh[:, h], rtol=1e-12, atol=1e-12)
     assert not np.allclose(o, ref[0])
+
+
+@pytest.mark.parametrize("P", [32, 64])
+def test_large_pages_read_as_16_token_pages(P):
+    """A page of 16 m tokens is m consecutive 16-token pages: the oracle reads
+    both descriptions of the same bytes to the same result bit for bit."""
+    import dataclasses
+    b = make_batch([1, 15, 33, 300], [1, 15, 20, 64], num_qo_heads=8, num_kv_heads=2, page_size=P, seed=71,
+                   pool_pages=800 // P)
+    m = P // 16
+    pool = b.k_cache.shape[0]
+    indptr, indices, last = [0], [], []
+    for i, kv in enumerate(b.kv_lens):
+        pages = b.kv_indices[b.kv_indptr[i]:b.kv_indptr[i + 1]].tolist()
+        n16 = (kv + 15) // 16
+        indices += [p * m + s for p in pages for s in range(m)][:n16]
+        indptr.append(indptr[-1] + n16)
+        last.append(kv - (n16 - 1) * 16 if n16 else 0)
+    b16 = dataclasses.replace(b, k_cache=b.k_cache.reshape(pool * m, 16, 2, 128),
+                              v_cache=b.v_cache.reshape(pool * m, 16, 2, 128), page_size=16,
+                              num_pages=pool * m, kv_indptr=torch.tensor(indptr, dtype=torch.int32),
+                              kv_indices=torch.tensor(indices, dtype=torch.int32),
+                              last_page_len=torch.tensor(last, dtype=torch.int32))
+    o1, l1 = oracle_on(b)
+    o2, l2 = oracle_on(b16)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
