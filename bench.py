@@ -57,12 +57,12 @@ L2_FLUSH_BYTES = 256 << 20
 # changed kernel reports null until it is captured again.
 NCU_TRAFFIC = {
     # profiles/decode_kernel_serving_decode.md
-    "d1459b7d4ca07482bda116b489374c18a7a37d5042caf4f03a7bcf217a31c79e": 309701120,
+    "eb81072890208ab61a2f349974c7a3a15fc90c92d2dd1f9c2b16b9682ce32644": 310214912,
 }
 # The same for the prefill kernel, per workload index, keyed by the SHA-256
 # of its source (profiles/prefill_kernel_ragged_bf16_and_fp8.md).
 NCU_TRAFFIC_PREFILL = {
-    "b1072fc59ae620fb833bb535cbdbf2926e1b5806cd9813424f28e01ee6eb8483": {4: 165543936, 5: 192773888},
+    "71798cc65a65dc09a7b0caf08f142f626eced7ef1de920df37eb290c05f9830f": {4: 170110720, 5: 191745024},
 }
 
 
