@@ -80,7 +80,7 @@ enum { PAFP8_MODE_DECODE = 0, PAFP8_MODE_PREFILL = 1 };
 enum { PAFP8_LAYOUT_NHD = 0, PAFP8_LAYOUT_HND = 1 };
 
 /* Static description of one batch.  Shapes served by this build:
- * head_dim 128; page_size a multiple of 16 (NHD) or 16 (HND), a page of
+ * head_dim 128, or 64 in decode; page_size a multiple of 16 (NHD) or 16 (HND), a page of
  * 16 m tokens being read as m consecutive 16-token sub-pages (so
  * num_pages * page_size / 16 must stay below 2^31); num_qo_heads a multiple of num_kv_heads with
  * group size num_qo_heads/num_kv_heads <= 8 (decode) or <= 16 (prefill).
@@ -313,7 +313,7 @@ pafp8_status pafp8_run_decode_noalloc(const pafp8_plan *plan, int32_t q_dtype, c
  *   status         device uint32 or NULL: the kernel ORs in 1 for a token it
  *                  did not write because its request index, position or page
  *                  index lies outside the table or the pool
- * Shapes served: head_dim 128; page_size a multiple of 16 (NHD) or 16
+ * Shapes served: head_dim 128 or 64; page_size a multiple of 16 (NHD) or 16
  * (HND).  Nothing is allocated or synchronized. */
 pafp8_status pafp8_append_kv(int32_t src_dtype, const void *k_new, const void *v_new, int64_t nnz,
                              int32_t num_kv_heads, int32_t head_dim, const int32_t *batch_indices,

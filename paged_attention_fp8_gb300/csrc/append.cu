@@ -12,12 +12,13 @@
 // product with fp32(1/scale) rounded once in fp32 (__fmul_rn), pairs packed by
 // cvt.rn.satfinite.{e4m3x2,e5m2x2}.f32 (round to nearest even, magnitudes
 // above the largest finite value saturate to it, NaN stays NaN), one 16-byte
-// store of the 16 codes.  Eight consecutive threads cover a 128-element row,
-// so a warp reads four consecutive rows and writes four rows of one page
-// slot (consecutive in the NHD layout [page][slot][head][d], 2 KB apart in
-// the HND layout [page][head][slot][d]).  The page comes from the request's CSR page table; a token whose
-// request, position or page lies outside the table or the pool is skipped
-// and reported in *status.  The work is a pure stream of reads and writes,
+// store of the 16 codes.  head_dim / 16 consecutive threads cover a row (8
+// for head_dim 128, 4 for 64), so a warp reads consecutive rows and writes
+// rows of one page slot (consecutive in the NHD layout [page][slot][head][d],
+// a page-slot stride apart in the HND layout [page][head][slot][d]).  The
+// page comes from the request's CSR page table; a token whose request,
+// position or page lies outside the table or the pool is skipped and
+// reported in *status.  The work is a pure stream of reads and writes,
 // bounded by HBM bandwidth.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -28,7 +29,6 @@
 namespace pafp8 {
 namespace {
 
-constexpr int D = kHeadDim;
 constexpr int kThreads = 256;
 
 // Raw source words of 16 elements: 8 words for a 2-byte type, 16 for fp32.
@@ -89,16 +89,16 @@ __device__ __forceinline__ uint4 quantize16(const Raw16<SRC>& r, float inv) {
 
 template <int SRC, int KV>
 __global__ void __launch_bounds__(kThreads) append_kernel(const AppendParams p) {
-    const long long total = p.nnz * (long long)p.num_kv_heads * (D / 16);
+    const long long total = p.nnz * (long long)p.num_kv_heads * (p.head_dim / 16);
     for (long long t = (long long)blockIdx.x * kThreads + threadIdx.x; t < total;
          t += (long long)gridDim.x * kThreads) {
-        const long long row = t / (D / 16);  // (token, KV head)
-        const int c = (int)(t - row * (D / 16));
+        const long long row = t / (p.head_dim / 16);  // (token, KV head)
+        const int c = (int)(t - row * (p.head_dim / 16));
         const long long tok = row / p.num_kv_heads;
         const int h = (int)(row - tok * p.num_kv_heads);
         // The source rows do not depend on the page: their loads go first and
         // overlap the page-table lookups.
-        const size_t src = (size_t)row * D + 16 * c;
+        const size_t src = (size_t)row * p.head_dim + 16 * c;
         Raw16<SRC> rk, rv;
         load_raw<SRC>(p.k_new, src, rk);
         load_raw<SRC>(p.v_new, src, rv);
@@ -119,7 +119,9 @@ __global__ void __launch_bounds__(kThreads) append_kernel(const AppendParams p) 
         }
         const size_t slot = (size_t)(pos % p.page_size);
         const size_t dst = (p.hnd ? ((size_t)page * p.num_kv_heads + h) * p.page_size + slot
-                                  : ((size_t)page * p.page_size + slot) * p.num_kv_heads + h) * D + 16 * c;
+                                  : ((size_t)page * p.page_size + slot) * p.num_kv_heads + h) *
+                               p.head_dim +
+                           16 * c;
         *reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.k_cache) + dst) = quantize16<KV>(rk, p.k_inv);
         *reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.v_cache) + dst) = quantize16<KV>(rv, p.v_inv);
     }
@@ -127,7 +129,7 @@ __global__ void __launch_bounds__(kThreads) append_kernel(const AppendParams p) 
 
 template <int SRC, int KV>
 cudaError_t launch_t(const AppendParams& p, cudaStream_t stream) {
-    const long long total = p.nnz * (long long)p.num_kv_heads * (D / 16);
+    const long long total = p.nnz * (long long)p.num_kv_heads * (p.head_dim / 16);
     const long long blocks = (total + kThreads - 1) / kThreads;
     const int grid = (int)(blocks < 65535 ? blocks : 65535);
     append_kernel<SRC, KV><<<grid, kThreads, 0, stream>>>(p);

@@ -57,13 +57,15 @@ namespace {
 
 using namespace ptx;
 
-constexpr int D = kHeadDim;
+
 constexpr int P = kPageSize;
 constexpr int kStageBudget = 192 * 1024;    // shared memory for the page ring
 __host__ __device__ constexpr bool is_2byte_kv(int kt) { return kt == PAFP8_F16 || kt == PAFP8_BF16; }
-// One KV head of one page in shared memory: 16 token rows of 128 B (fp8), or
-// of two 128-B halves (2-byte cache).
-__host__ __device__ constexpr int tile_bytes(int kt) { return P * D * (is_2byte_kv(kt) ? 2 : 1); }
+// One KV head of one page in shared memory: 16 token rows of dh bytes (fp8:
+// 128 B with the 128-byte swizzle, or 64 B with the 64-byte swizzle), or of
+// 2 dh bytes (2-byte cache: two swizzled 128-B halves per row for dh 128,
+// one 128-B row for dh 64).
+__host__ __device__ constexpr int tile_bytes(int kt, int dh) { return P * dh * (is_2byte_kv(kt) ? 2 : 1); }
 __device__ __forceinline__ void flag(uint32_t* status, uint32_t bit) { atomicOr(status, bit); }
 
 template <bool kBF16>
@@ -76,29 +78,32 @@ __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1
 }
 
 // Q fragment for the QK product: B operand (K = head dim, N = 8 query heads).
-// Lane (g, t) holds head g of the group, dims 32t .. 32t+31, as 16 f16x2
-// words; word j = dims 32t+2j, 32t+2j+1.  Returns the power-of-two factor the
-// logits must be multiplied by (a bf16 query is brought into f16 range by an
-// exact power-of-two scaling when its magnitude needs it).
-template <bool kBF16>
+// Lane (g, t) holds head g of the group, dims (DH/4)t .. (DH/4)t + DH/4 - 1, as
+// DH/8 f16x2 words; word j = dims (DH/4)t+2j, (DH/4)t+2j+1.  Returns the
+// power-of-two factor the logits must be multiplied by (a bf16 query is
+// brought into f16 range by an exact power-of-two scaling when its magnitude
+// needs it).
+template <bool kBF16, int DH>
 __device__ __forceinline__ float load_q(uint32_t (&qf)[16], uint32_t (&qlo)[16], const void* q, int q_dtype,
                                         size_t head_off, bool active, int t) {
+    constexpr int QW = DH / 8;   // words per lane
+    constexpr int Q4 = QW / 4;   // 16-byte loads of a 2-byte query
     float factor = 1.0f;
     if (kBF16) {
         // bf16 MMAs (bf16 cache): a bf16 query as is; an f16 query as the sum
         // of two bf16 words, its bf16 rounding (qf) and the exact remainder
         // (qlo: an f16 has 11 significant bits, so the remainder needs at most
         // 4 of bf16's 8), so the QK product loses nothing.
-        uint4 w[4] = {};
+        uint4 w[Q4] = {};
         if (active) {
             const uint4* src = reinterpret_cast<const uint4*>(
-                static_cast<const uint16_t*>(q) + head_off + 32 * t);
+                static_cast<const uint16_t*>(q) + head_off + (DH / 4) * t);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) w[i] = __ldg(src + i);
+            for (int i = 0; i < Q4; ++i) w[i] = __ldg(src + i);
         }
         const uint32_t* ws = reinterpret_cast<const uint32_t*>(w);
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
+        for (int j = 0; j < QW; ++j) {
             if (q_dtype == PAFP8_BF16) {
                 qf[j] = ws[j];
             } else {
@@ -111,22 +116,22 @@ __device__ __forceinline__ float load_q(uint32_t (&qf)[16], uint32_t (&qlo)[16],
             }
         }
     } else if (q_dtype == PAFP8_F16 || q_dtype == PAFP8_BF16) {
-        uint4 w[4] = {};
+        uint4 w[Q4] = {};
         if (active) {
             const uint4* src = reinterpret_cast<const uint4*>(
-                static_cast<const uint16_t*>(q) + head_off + 32 * t);
+                static_cast<const uint16_t*>(q) + head_off + (DH / 4) * t);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) w[i] = __ldg(src + i);
+            for (int i = 0; i < Q4; ++i) w[i] = __ldg(src + i);
         }
         const uint32_t* ws = reinterpret_cast<const uint32_t*>(w);
         if (q_dtype == PAFP8_F16) {
 #pragma unroll
-            for (int j = 0; j < 16; ++j) qf[j] = ws[j];
+            for (int j = 0; j < QW; ++j) qf[j] = ws[j];
         } else {
             // Largest |q| over the warp decides the power-of-two shift.
             uint32_t mx = 0;
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
+            for (int j = 0; j < QW; ++j) {
                 mx = max(mx, (ws[j] & 0x7FFFu) << 16);
                 mx = max(mx, ws[j] & 0x7FFF0000u);
             }
@@ -136,23 +141,24 @@ __device__ __forceinline__ float load_q(uint32_t (&qf)[16], uint32_t (&qlo)[16],
             const float down = __int_as_float((127 - shift) << 23);
             factor = __int_as_float((127 + shift) << 23);
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
+            for (int j = 0; j < QW; ++j) {
                 const float lo = __uint_as_float(ws[j] << 16) * down;
                 const float hi = __uint_as_float(ws[j] & 0xFFFF0000u) * down;
                 qf[j] = pack_half2(lo, hi);
             }
         }
     } else {
-        uint4 w[2] = {};
+        // fp8 query: DH/4 bytes per lane, DH/64 16-byte loads.
+        uint4 w[DH / 64] = {};
         if (active) {
             const uint4* src = reinterpret_cast<const uint4*>(
-                static_cast<const uint8_t*>(q) + head_off + 32 * t);
-            w[0] = __ldg(src);
-            w[1] = __ldg(src + 1);
+                static_cast<const uint8_t*>(q) + head_off + (DH / 4) * t);
+#pragma unroll
+            for (int i = 0; i < DH / 64; ++i) w[i] = __ldg(src + i);
         }
         const uint32_t* ws = reinterpret_cast<const uint32_t*>(w);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
+        for (int j = 0; j < QW / 2; ++j) {
             if (q_dtype == PAFP8_E4M3FN) {
                 qf[2 * j] = fp8x2_lo<PAFP8_E4M3FN>(ws[j]);
                 qf[2 * j + 1] = fp8x2_hi<PAFP8_E4M3FN>(ws[j]);
@@ -165,7 +171,7 @@ __device__ __forceinline__ float load_q(uint32_t (&qf)[16], uint32_t (&qlo)[16],
     return factor;
 }
 
-template <int KT>
+template <int KT, int DH>
 __global__ void __launch_bounds__(32 * 9, 1)
     decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtensorMap tmk,
                   const __grid_constant__ CUtensorMap tmv, int hpc, int group, int stages,
@@ -174,7 +180,8 @@ __global__ void __launch_bounds__(32 * 9, 1)
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;      // 128B swizzle wants 1024-B alignment
     constexpr bool k2 = is_2byte_kv(KT), kBF = KT == PAFP8_BF16;
-    constexpr uint32_t kTileBytes = (uint32_t)tile_bytes(KT);
+    constexpr uint32_t kTileBytes = (uint32_t)tile_bytes(KT, DH);
+    constexpr int NA = DH / 16;    // PV accumulators (MMAs) per lane; also QK k-steps
     const uint32_t stage_bytes = 2u * hpc * kTileBytes;  // K heads then V heads
     const uint32_t bar_full = base + stages * stage_bytes;
     const uint32_t bar_empty = bar_full + 8u * stages;
@@ -298,17 +305,17 @@ __global__ void __launch_bounds__(32 * 9, 1)
                 const int n = 2 * t + hh;
                 if (n >= group) continue;
                 const size_t oh = (size_t)b * Hq + (size_t)kvh * group + n;
-                uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + oh * D + 16 * g);
-                dst[0] = make_uint4(0, 0, 0, 0);
-                dst[1] = make_uint4(0, 0, 0, 0);
+                uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) + oh * DH + (DH / 8) * g);
+#pragma unroll
+                for (int i = 0; i < DH / 64; ++i) dst[i] = make_uint4(0, 0, 0, 0);
                 if (g == 0 && p.lse != nullptr) p.lse[oh] = -INFINITY;
             }
             continue;
         }
 
         uint32_t qf[16], qlo[16];
-        const size_t q_head_off = ((size_t)b * Hq + (size_t)kvh * group + g) * D;
-        const float qfactor = load_q<kBF>(qf, qlo, p.q, p.q_dtype, q_head_off, g < group, t);
+        const size_t q_head_off = ((size_t)b * Hq + (size_t)kvh * group + g) * DH;
+        const float qfactor = load_q<kBF, DH>(qf, qlo, p.q, p.q_dtype, q_head_off, g < group, t);
         const bool split_q = kBF && p.q_dtype == PAFP8_F16;
         // log2 softmax scale of heads 2t and 2t+1 (this lane's S columns).
         // Per-query-head scales exist only for an fp8 query, which a 2-byte
@@ -329,9 +336,9 @@ __global__ void __launch_bounds__(32 * 9, 1)
         if constexpr (k2) sc1 = sc0;
 
         float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-        float acc[8][4];
+        float acc[NA][4];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+        for (int i = 0; i < NA; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
 
         for (int pg = p0; pg < p1; ++pg) {
             // mma.sync and movmatrix below are warp-collective: the warp
@@ -349,9 +356,41 @@ __global__ void __launch_bounds__(32 * 9, 1)
             // word w = dims 32t+2w, 32t+2w+1; V: dims 16g .. 16g+15 of the four
             // tokens, word w = dims 16g+2w, 16g+2w+1), so the operand words match
             // the fp8 path's converted words exactly.
+            // Head dim 64 takes the same fragments at half the width: K dims
+            // 16t .. 16t+15 (one chunk), V dims 8g .. 8g+7, from 64-B fp8 rows
+            // under the 64-byte swizzle (16-byte chunk c of row r at c ^ ((r >> 1)
+            // & 3)) or from 128-B rows of a 2-byte cache.
             uint4 k0, k1, k2w, k3, v0, v1, v2, v3;
             uint32_t kw0[16], kw8[16], vw[4][8];
-            if constexpr (k2) {
+            if constexpr (k2 && DH == 64) {
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    const int c = 2 * t + i;
+                    const uint4 x = lds128(kt + g * 128 + ((c ^ g) << 4));
+                    const uint4 y = lds128(kt + (g + 8) * 128 + ((c ^ g) << 4));
+                    kw0[4 * i] = x.x, kw0[4 * i + 1] = x.y, kw0[4 * i + 2] = x.z, kw0[4 * i + 3] = x.w;
+                    kw8[4 * i] = y.x, kw8[4 * i + 1] = y.y, kw8[4 * i + 2] = y.z, kw8[4 * i + 3] = y.w;
+                }
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    const int tok = 2 * t + (r & 1) + 8 * (r >> 1);
+                    const uint4 x = lds128(vt + tok * 128 + ((g ^ (tok & 7)) << 4));
+                    vw[r][0] = x.x, vw[r][1] = x.y, vw[r][2] = x.z, vw[r][3] = x.w;
+                }
+            } else if constexpr (DH == 64) {
+                const int sw = (g >> 1) & 3;  // rows g and g+8 share it
+                k0 = lds128(kt + g * 64 + ((t ^ sw) << 4));
+                k2w = lds128(kt + (g + 8) * 64 + ((t ^ sw) << 4));
+                k1 = k3 = make_uint4(0, 0, 0, 0);
+                auto vrow = [&](int tok) {
+                    const uint2 x = lds64(vt + tok * 64 + ((((g >> 1) ^ ((tok >> 1) & 3))) << 4) + (g & 1) * 8);
+                    return make_uint4(x.x, x.y, 0u, 0u);
+                };
+                v0 = vrow(2 * t);
+                v1 = vrow(2 * t + 1);
+                v2 = vrow(2 * t + 8);
+                v3 = vrow(2 * t + 9);
+            } else if constexpr (k2) {
                 // A token row is two swizzled 128-B rows (dims 0-63, 64-127):
                 // row index 2 * token + half.
                 const int rk = (t >> 1) + 2 * g;
@@ -411,7 +450,7 @@ __global__ void __launch_bounds__(32 * 9, 1)
             float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
             if constexpr (k2) {
 #pragma unroll
-                for (int s = 0; s < 8; ++s) {
+                for (int s = 0; s < NA; ++s) {
                     if (s & 1)
                         mma16816<kBF>(sb, kw0[2 * s], kw8[2 * s], kw0[2 * s + 1], kw8[2 * s + 1], qf[2 * s],
                                       qf[2 * s + 1]);
@@ -421,7 +460,7 @@ __global__ void __launch_bounds__(32 * 9, 1)
                 }
                 if (kBF && split_q) {
 #pragma unroll
-                    for (int s = 0; s < 8; ++s) {
+                    for (int s = 0; s < NA; ++s) {
                         if (s & 1)
                             mma16816<kBF>(sb, kw0[2 * s], kw8[2 * s], kw0[2 * s + 1], kw8[2 * s + 1], qlo[2 * s],
                                           qlo[2 * s + 1]);
@@ -434,7 +473,7 @@ __global__ void __launch_bounds__(32 * 9, 1)
                 const uint32_t kr0[8] = {k0.x, k0.y, k0.z, k0.w, k1.x, k1.y, k1.z, k1.w};
                 const uint32_t kr8[8] = {k2w.x, k2w.y, k2w.z, k2w.w, k3.x, k3.y, k3.z, k3.w};
 #pragma unroll
-                for (int s = 0; s < 8; ++s) {
+                for (int s = 0; s < NA; ++s) {
                     const uint32_t a0 = fp8x2_lo<KT>(kr0[s]), a1 = fp8x2_lo<KT>(kr8[s]);
                     const uint32_t a2 = fp8x2_hi<KT>(kr0[s]), a3 = fp8x2_hi<KT>(kr8[s]);
                     if (s & 1)
@@ -463,7 +502,7 @@ __global__ void __launch_bounds__(32 * 9, 1)
             m0 = mn0;
             m1 = mn1;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
+            for (int i = 0; i < NA; ++i) {
                 acc[i][0] *= al0;
                 acc[i][1] *= al1;
                 acc[i][2] *= al0;
@@ -478,14 +517,14 @@ __global__ void __launch_bounds__(32 * 9, 1)
             // (2t, 2t+1 | 2t+8, 2t+9), each operand word one dim of two tokens.
             if constexpr (k2) {
 #pragma unroll
-                for (int w = 0; w < 8; ++w)
+                for (int w = 0; w < NA; ++w)
                     mma16816<kBF>(acc[w], prmt(vw[0][w], vw[1][w], 0x5410u), prmt(vw[0][w], vw[1][w], 0x7632u),
                                   prmt(vw[2][w], vw[3][w], 0x5410u), prmt(vw[2][w], vw[3][w], 0x7632u), pb0, pb1);
             } else {
                 const uint32_t va[4] = {v0.x, v0.y, v0.z, v0.w}, vb[4] = {v1.x, v1.y, v1.z, v1.w};
                 const uint32_t vc[4] = {v2.x, v2.y, v2.z, v2.w}, vd[4] = {v3.x, v3.y, v3.z, v3.w};
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
+                for (int j = 0; j < NA / 2; ++j) {
                     const uint32_t ab_lo = prmt(va[j], vb[j], 0x5140u), ab_hi = prmt(va[j], vb[j], 0x7362u);
                     const uint32_t cd_lo = prmt(vc[j], vd[j], 0x5140u), cd_hi = prmt(vc[j], vd[j], 0x7362u);
                     mma_16816(acc[2 * j], fp8x2_lo<KT>(ab_lo), fp8x2_hi<KT>(ab_lo), fp8x2_lo<KT>(cd_lo),
@@ -510,30 +549,30 @@ __global__ void __launch_bounds__(32 * 9, 1)
             if (n >= group) continue;
             const float l = hh ? l1 : l0, m = hh ? m1 : m0;
             const float inv = 1.0f / l;
-            float vals[16];
+            float vals[2 * NA];  // dims (DH/8)g .. (DH/8)g + DH/8 - 1
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
+            for (int i = 0; i < NA; ++i) {
                 vals[2 * i] = acc[i][hh] * inv;
                 vals[2 * i + 1] = acc[i][2 + hh] * inv;
             }
             const int head = kvh * group + n;
             if (slot < 0) {
                 const float vs = p.v_scales != nullptr ? __ldg(p.v_scales + kvh) : p.v_scale;
-                uint32_t w[8];
+                uint32_t w[NA];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) w[i] = pack_out2(vals[2 * i] * vs, vals[2 * i + 1] * vs, p.o_dtype);
+                for (int i = 0; i < NA; ++i) w[i] = pack_out2(vals[2 * i] * vs, vals[2 * i + 1] * vs, p.o_dtype);
                 uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.o) +
-                                                      ((size_t)b * Hq + head) * D + 16 * g);
-                dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-                dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+                                                      ((size_t)b * Hq + head) * DH + (DH / 8) * g);
+#pragma unroll
+                for (int i = 0; i < NA / 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
                 if (g == 0 && p.lse != nullptr)
                     p.lse[(size_t)b * Hq + head] = (m + __log2f(l)) * 0.69314718055994531f;
             } else {
                 const int hpb = hpc * group;
                 float4* dst = reinterpret_cast<float4*>(
-                    p.part_o + ((size_t)slot * hpb + warp * group + n) * D + 16 * g);
+                    p.part_o + ((size_t)slot * hpb + warp * group + n) * DH + (DH / 8) * g);
 #pragma unroll
-                for (int i = 0; i < 4; ++i)
+                for (int i = 0; i < NA / 2; ++i)
                     dst[i] = make_float4(vals[4 * i], vals[4 * i + 1], vals[4 * i + 2], vals[4 * i + 3]);
                 if (g == 0) p.part_lse[(size_t)slot * hpb + warp * group + n] = m + __log2f(l);
             }
@@ -543,8 +582,8 @@ __global__ void __launch_bounds__(32 * 9, 1)
 }
 
 // Combine the partial states of each split (request, KV-head block) row.
-// Block = one (merge entry, query head of the block); thread = one of the 128
-// dims.  Over the row's slots (page order) it keeps a running max of the
+// Block = one (merge entry, query head of the block); thread = one of the
+// head_dim dims.  Over the row's slots (page order) it keeps a running max of the
 // log2-domain lse_c and the rescaled sums of 2^lse_c and 2^lse_c O_c, four
 // slots' loads in flight per step, then writes o = v_scale * sum / sum and
 // lse = ln(sum) + max.  Launched as a programmatic dependent of the decode
@@ -571,7 +610,7 @@ __global__ void __launch_bounds__(128)
             const bool in = s + k < s1;
             const size_t idx = (size_t)mslot[in ? s + k : s0] * hpb + hh;
             l[k] = in ? __ldcg(p.part_lse + idx) : -INFINITY;
-            o[k] = in ? __ldcg(p.part_o + idx * D + d) : 0.f;
+            o[k] = in ? __ldcg(p.part_o + idx * p.head_dim + d) : 0.f;
         }
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
@@ -585,7 +624,7 @@ __global__ void __launch_bounds__(128)
     const int head = hb * hpb + hh;  // query head: (hb * hpc + hh / group) * group + hh % group
     const size_t oh = (size_t)b * p.num_qo_heads + head;
     const float val = acc / sum * (p.v_scales != nullptr ? __ldg(p.v_scales + head / group) : p.v_scale);
-    uint16_t* dst = static_cast<uint16_t*>(p.o) + oh * D + d;
+    uint16_t* dst = static_cast<uint16_t*>(p.o) + oh * p.head_dim + d;
     if (p.o_dtype == PAFP8_BF16) {
         __nv_bfloat16 h = __float2bfloat16_rn(val);
         *dst = *reinterpret_cast<uint16_t*>(&h);
@@ -626,32 +665,41 @@ cudaError_t noalloc_scratch(void** ptr) {
     return cudaSuccess;
 }
 
-template <int KT>
+template <int KT, int DH>
 cudaError_t launch_decode_t(const DecodeParams& p, const CUtensorMap& tmap_k, const CUtensorMap& tmap_v,
                             int num_ctas, int hpc, int group, int heads_per_box, cudaStream_t stream) {
-    const int stage_bytes = 2 * hpc * tile_bytes(KT);
+    const int stage_bytes = 2 * hpc * tile_bytes(KT, DH);
     int stages = kStageBudget / stage_bytes;
     if (stages > 8) stages = 8;
     if (stages < 2) stages = 2;
     const size_t smem = 1024 + (size_t)stages * stage_bytes + 16 * (size_t)stages;
     const dim3 grid(num_ctas), block(32 * (hpc + 1));
-    cudaError_t e = cudaFuncSetAttribute(decode_kernel<KT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e =
+        cudaFuncSetAttribute(decode_kernel<KT, DH>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    decode_kernel<KT><<<grid, block, smem, stream>>>(p, tmap_k, tmap_v, hpc, group, stages, heads_per_box);
+    decode_kernel<KT, DH><<<grid, block, smem, stream>>>(p, tmap_k, tmap_v, hpc, group, stages, heads_per_box);
     return cudaGetLastError();
+}
+
+template <int KT>
+cudaError_t launch_decode_kt(const DecodeParams& p, const CUtensorMap& tmap_k, const CUtensorMap& tmap_v,
+                             int num_ctas, int hpc, int group, int heads_per_box, cudaStream_t stream) {
+    if (p.head_dim == 64)
+        return launch_decode_t<KT, 64>(p, tmap_k, tmap_v, num_ctas, hpc, group, heads_per_box, stream);
+    return launch_decode_t<KT, 128>(p, tmap_k, tmap_v, num_ctas, hpc, group, heads_per_box, stream);
 }
 
 cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& tmap_k, const CUtensorMap& tmap_v,
                           int num_ctas, int hpc, int group, int heads_per_box, cudaStream_t stream) {
     switch (p.kv_dtype) {
         case PAFP8_E4M3FN:
-            return launch_decode_t<PAFP8_E4M3FN>(p, tmap_k, tmap_v, num_ctas, hpc, group, heads_per_box, stream);
+            return launch_decode_kt<PAFP8_E4M3FN>(p, tmap_k, tmap_v, num_ctas, hpc, group, heads_per_box, stream);
         case PAFP8_E5M2:
-            return launch_decode_t<PAFP8_E5M2>(p, tmap_k, tmap_v, num_ctas, hpc, group, heads_per_box, stream);
+            return launch_decode_kt<PAFP8_E5M2>(p, tmap_k, tmap_v, num_ctas, hpc, group, heads_per_box, stream);
         case PAFP8_F16:
-            return launch_decode_t<PAFP8_F16>(p, tmap_k, tmap_v, num_ctas, hpc, group, heads_per_box, stream);
+            return launch_decode_kt<PAFP8_F16>(p, tmap_k, tmap_v, num_ctas, hpc, group, heads_per_box, stream);
         case PAFP8_BF16:
-            return launch_decode_t<PAFP8_BF16>(p, tmap_k, tmap_v, num_ctas, hpc, group, heads_per_box, stream);
+            return launch_decode_kt<PAFP8_BF16>(p, tmap_k, tmap_v, num_ctas, hpc, group, heads_per_box, stream);
         default:
             return cudaErrorInvalidValue;
     }
@@ -660,7 +708,7 @@ cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& tmap_k, cons
 cudaError_t launch_merge(const DecodeParams& p, int num_merge, int hpc, int group, cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(num_merge * hpc * group);
-    cfg.blockDim = dim3(128);
+    cfg.blockDim = dim3(p.head_dim);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];

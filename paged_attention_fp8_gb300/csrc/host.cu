@@ -360,7 +360,7 @@ void layout_workspace(pafp8_plan* pl) {
     const size_t heads = (size_t)pl->heads_per_cta * pl->group;
     pl->meta_bytes = align_up(pl->meta.size() * sizeof(int32_t), 256);
     pl->part_o_off = pl->meta_bytes;
-    pl->part_lse_off = align_up(pl->part_o_off + (size_t)pl->num_partials * heads * kHeadDim * 4, 256);
+    pl->part_lse_off = align_up(pl->part_o_off + (size_t)pl->num_partials * heads * pl->desc.head_dim * 4, 256);
     pl->status_off = align_up(pl->part_lse_off + (size_t)pl->num_partials * heads * 4, 256);
     pl->ws_bytes = pl->status_off + 256;
 }
@@ -389,8 +389,8 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
 struct KvStrides {
     cuuint64_t token, head, page;
 };
-KvStrides kv_strides(int layout, int hkv, int esz) {
-    const cuuint64_t row = (cuuint64_t)kHeadDim * esz;
+KvStrides kv_strides(int layout, int hkv, int esz, int head_dim = kHeadDim) {
+    const cuuint64_t row = (cuuint64_t)head_dim * esz;
     const cuuint64_t page = (cuuint64_t)kPageSize * hkv * row;
     if (layout == PAFP8_LAYOUT_HND) return KvStrides{row, (cuuint64_t)kPageSize * row, page};
     return KvStrides{(cuuint64_t)hkv * row, row, page};
@@ -398,17 +398,19 @@ KvStrides kv_strides(int layout, int hkv, int esz) {
 
 // one page, 16 tokens x 128 bytes, landing in shared memory as [16][128] with
 // the 128-byte swizzle (16-byte chunk c of token row t stored at c ^ (t & 7)).
-pafp8_status encode_cache_map(CUtensorMap* map, const void* base, int num_pages, int hkv, int layout) {
+pafp8_status encode_cache_map(CUtensorMap* map, const void* base, int num_pages, int hkv, int layout,
+                              int head_dim = kHeadDim) {
     auto enc = get_encode();
     if (!enc) return fail(PAFP8_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
-    const KvStrides ks = kv_strides(layout, hkv, 1);
-    cuuint64_t dims[4] = {(cuuint64_t)kHeadDim, (cuuint64_t)hkv, (cuuint64_t)kPageSize,
+    const KvStrides ks = kv_strides(layout, hkv, 1, head_dim);
+    cuuint64_t dims[4] = {(cuuint64_t)head_dim, (cuuint64_t)hkv, (cuuint64_t)kPageSize,
                           (cuuint64_t)num_pages};
     cuuint64_t strides[3] = {ks.head, ks.token, ks.page};
-    cuuint32_t box[4] = {(cuuint32_t)kHeadDim, 1, (cuuint32_t)kPageSize, 1};
+    cuuint32_t box[4] = {(cuuint32_t)head_dim, 1, (cuuint32_t)kPageSize, 1};
     cuuint32_t estr[4] = {1, 1, 1, 1};
     CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(base), dims, strides,
-                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     head_dim == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS)
         return fail(PAFP8_ERR_CUDA, "cuTensorMapEncodeTiled failed for the KV cache (CUresult %d)",
@@ -469,15 +471,17 @@ pafp8_status encode_q_map(CUtensorMap* map, const void* base, int nnz_qo, int hq
 // (row 2 * token + half); the fallback is one box per head with dims (d % 64,
 // d / 64, head, token, page) and the same layout.
 pafp8_status encode_decode_maps_2byte(CUtensorMap* tk, CUtensorMap* tv, const void* k, const void* v,
-                                      int num_pages, int hkv, int hpc, int* heads_per_box, int layout) {
+                                      int num_pages, int hkv, int hpc, int* heads_per_box, int layout,
+                                      int head_dim) {
     auto enc = get_encode();
     if (!enc) return fail(PAFP8_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
-    const KvStrides ks = kv_strides(layout, hkv, 2);
+    const KvStrides ks = kv_strides(layout, hkv, 2, head_dim);
+    const cuuint32_t halves = (cuuint32_t)(head_dim / 64);  // 128-B halves of a row
     cuuint32_t estr[5] = {1, 1, 1, 1, 1};
     {
-        cuuint64_t dims[5] = {64, 2, (cuuint64_t)kPageSize, (cuuint64_t)hkv, (cuuint64_t)num_pages};
+        cuuint64_t dims[5] = {64, halves, (cuuint64_t)kPageSize, (cuuint64_t)hkv, (cuuint64_t)num_pages};
         cuuint64_t strides[4] = {128, ks.token, ks.head, ks.page};
-        cuuint32_t box[5] = {64, 2, (cuuint32_t)kPageSize, (cuuint32_t)hpc, 1};
+        cuuint32_t box[5] = {64, halves, (cuuint32_t)kPageSize, (cuuint32_t)hpc, 1};
         CUresult rk = enc(tk, CU_TENSOR_MAP_DATA_TYPE_UINT16, 5, const_cast<void*>(k), dims, strides, box, estr,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -489,9 +493,9 @@ pafp8_status encode_decode_maps_2byte(CUtensorMap* tk, CUtensorMap* tv, const vo
             return PAFP8_OK;
         }
     }
-    cuuint64_t dims[5] = {64, 2, (cuuint64_t)hkv, (cuuint64_t)kPageSize, (cuuint64_t)num_pages};
+    cuuint64_t dims[5] = {64, halves, (cuuint64_t)hkv, (cuuint64_t)kPageSize, (cuuint64_t)num_pages};
     cuuint64_t strides[4] = {128, ks.head, ks.token, ks.page};
-    cuuint32_t box[5] = {64, 2, 1, (cuuint32_t)kPageSize, 1};
+    cuuint32_t box[5] = {64, halves, 1, (cuuint32_t)kPageSize, 1};
     CUresult rk = enc(tk, CU_TENSOR_MAP_DATA_TYPE_UINT16, 5, const_cast<void*>(k), dims, strides, box, estr,
                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -506,7 +510,8 @@ pafp8_status encode_decode_maps_2byte(CUtensorMap* tk, CUtensorMap* tv, const vo
 }
 
 pafp8_status encode_decode_maps(CUtensorMap* tk, CUtensorMap* tv, const void* k, const void* v,
-                                int num_pages, int hkv, int hpc, int* heads_per_box, bool two_byte, int layout) {
+                                int num_pages, int hkv, int hpc, int* heads_per_box, bool two_byte, int layout,
+                                int head_dim) {
     if (num_pages == 0 || k == nullptr || v == nullptr) {
         // No request has pages: the kernel issues no copy, the maps are unused.
         memset(tk, 0, sizeof(*tk));
@@ -514,28 +519,31 @@ pafp8_status encode_decode_maps(CUtensorMap* tk, CUtensorMap* tv, const void* k,
         *heads_per_box = 1;
         return PAFP8_OK;
     }
-    if (two_byte) return encode_decode_maps_2byte(tk, tv, k, v, num_pages, hkv, hpc, heads_per_box, layout);
+    if (two_byte)
+        return encode_decode_maps_2byte(tk, tv, k, v, num_pages, hkv, hpc, heads_per_box, layout, head_dim);
     auto enc = get_encode();
     if (!enc) return fail(PAFP8_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
-    const KvStrides ks = kv_strides(layout, hkv, 1);
-    cuuint64_t dims[4] = {(cuuint64_t)kHeadDim, (cuuint64_t)kPageSize, (cuuint64_t)hkv,
+    const KvStrides ks = kv_strides(layout, hkv, 1, head_dim);
+    // 128-B rows take the 128-byte swizzle, 64-B rows (head_dim 64) the 64-byte one.
+    const CUtensorMapSwizzle swz = head_dim == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
+    cuuint64_t dims[4] = {(cuuint64_t)head_dim, (cuuint64_t)kPageSize, (cuuint64_t)hkv,
                           (cuuint64_t)num_pages};
     cuuint64_t strides[3] = {ks.token, ks.head, ks.page};
-    cuuint32_t box[4] = {(cuuint32_t)kHeadDim, (cuuint32_t)kPageSize, (cuuint32_t)hpc, 1};
+    cuuint32_t box[4] = {(cuuint32_t)head_dim, (cuuint32_t)kPageSize, (cuuint32_t)hpc, 1};
     cuuint32_t estr[4] = {1, 1, 1, 1};
     CUresult rk = enc(tk, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(k), dims, strides, box,
-                      estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                      estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     CUresult rv = enc(tv, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(v), dims, strides, box,
-                      estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                      estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (rk == CUDA_SUCCESS && rv == CUDA_SUCCESS) {
         *heads_per_box = hpc;
         return PAFP8_OK;
     }
     pafp8_status st;
-    if ((st = encode_cache_map(tk, k, num_pages, hkv, layout)) != PAFP8_OK) return st;
-    if ((st = encode_cache_map(tv, v, num_pages, hkv, layout)) != PAFP8_OK) return st;
+    if ((st = encode_cache_map(tk, k, num_pages, hkv, layout, head_dim)) != PAFP8_OK) return st;
+    if ((st = encode_cache_map(tv, v, num_pages, hkv, layout, head_dim)) != PAFP8_OK) return st;
     *heads_per_box = 1;
     return PAFP8_OK;
 }
@@ -581,9 +589,10 @@ pafp8_status pafp8_plan_create(const pafp8_plan_desc* desc_in, const int32_t* kv
                     "%s serves up to %d query heads per KV head; got %d (%d / %d)",
                     d.mode == PAFP8_MODE_DECODE ? "decode" : "prefill", max_group, group,
                     (int)d.num_qo_heads, (int)d.num_kv_heads);
-    if (d.head_dim != kHeadDim)
-        return fail(PAFP8_ERR_UNSUPPORTED, "head_dim %d is not served by this build (only %d)",
-                    (int)d.head_dim, kHeadDim);
+    if (d.head_dim != kHeadDim && !(d.head_dim == 64 && d.mode == PAFP8_MODE_DECODE))
+        return fail(PAFP8_ERR_UNSUPPORTED,
+                    "head_dim %d is not served by this build (%d; 64 too in decode)", (int)d.head_dim,
+                    kHeadDim);
     if (d.num_pages < 0) return fail(PAFP8_ERR_SHAPE, "num_pages %d is negative", (int)d.num_pages);
     if (d.kv_layout != PAFP8_LAYOUT_NHD && d.kv_layout != PAFP8_LAYOUT_HND)
         return fail(PAFP8_ERR_ARG, "kv_layout %d is neither NHD (0) nor HND (1)", (int)d.kv_layout);
@@ -855,6 +864,7 @@ pafp8_status run_impl(const pafp8_plan* plan, int32_t stage, int32_t q_dtype, co
     p.num_kv_heads = d.num_kv_heads;
     p.num_pages = d.num_pages;
     p.page_mult = plan->page_mult;
+    p.head_dim = d.head_dim;
     p.sm_scale_log2 = sm_log2;
     p.v_scale = v_scale;
     p.q_scales = k_scales != nullptr ? q_scales : nullptr;
@@ -867,7 +877,7 @@ pafp8_status run_impl(const pafp8_plan* plan, int32_t stage, int32_t q_dtype, co
         CUtensorMap tk, tv;
         int hpb = 1;
         if ((st = encode_decode_maps(&tk, &tv, k_cache, v_cache, vpages, d.num_kv_heads,
-                                     plan->heads_per_cta, &hpb, is_2byte(k_dtype), d.kv_layout)) != PAFP8_OK)
+                                     plan->heads_per_cta, &hpb, is_2byte(k_dtype), d.kv_layout, d.head_dim)) != PAFP8_OK)
             return st;
         e = launch_decode(p, tk, tv, plan->num_ctas, plan->heads_per_cta, plan->group, hpb, s);
     }
@@ -1014,6 +1024,7 @@ pafp8_status pafp8_run_decode_noalloc(const pafp8_plan* plan, int32_t q_dtype, c
     p.num_kv_heads = d.num_kv_heads;
     p.num_pages = d.num_pages;
     p.page_mult = plan->page_mult;
+    p.head_dim = d.head_dim;
     p.sm_scale_log2 = (float)((double)d.sm_scale * (is_fp8(q_dtype) ? (double)q_scale : 1.0) *
                               (double)k_scale * 1.4426950408889634);
     p.v_scale = v_scale;
@@ -1021,7 +1032,7 @@ pafp8_status pafp8_run_decode_noalloc(const pafp8_plan* plan, int32_t q_dtype, c
         CUtensorMap tk, tv;
         int hpb = 1;
         if ((st = encode_decode_maps(&tk, &tv, k_cache, v_cache, d.num_pages * plan->page_mult, d.num_kv_heads,
-                                     plan->heads_per_cta, &hpb, is_2byte(k_dtype), d.kv_layout)) != PAFP8_OK)
+                                     plan->heads_per_cta, &hpb, is_2byte(k_dtype), d.kv_layout, d.head_dim)) != PAFP8_OK)
             return st;
         e = launch_decode(p, tk, tv, plan->num_ctas, plan->heads_per_cta, plan->group, hpb, s);
     }
@@ -1059,8 +1070,8 @@ pafp8_status pafp8_append_kv(int32_t src_dtype, const void* k_new, const void* v
                     (long long)nnz, (int)batch, (int)num_pages);
     if (num_kv_heads <= 0)
         return fail(PAFP8_ERR_SHAPE, "num_kv_heads %d must be positive", (int)num_kv_heads);
-    if (head_dim != kHeadDim)
-        return fail(PAFP8_ERR_UNSUPPORTED, "head_dim %d is not served by this build (only %d)",
+    if (head_dim != kHeadDim && head_dim != 64)
+        return fail(PAFP8_ERR_UNSUPPORTED, "head_dim %d is not served by this build (%d or 64)",
                     (int)head_dim, kHeadDim);
     if (page_size <= 0 || page_size % kPageSize != 0)
         return fail(PAFP8_ERR_UNSUPPORTED, "page_size %d is not served by this build (a multiple of %d)",
@@ -1101,6 +1112,7 @@ pafp8_status pafp8_append_kv(int32_t src_dtype, const void* k_new, const void* v
     p.kv_dtype = kv_dtype;
     p.hnd = kv_layout == PAFP8_LAYOUT_HND;
     p.page_size = page_size;
+    p.head_dim = head_dim;
     p.k_inv = 1.0f / k_scale;  // IEEE fp32 division: fp32(1/scale)
     p.v_inv = 1.0f / v_scale;
     const cudaError_t e = launch_append(p, (cudaStream_t)stream);

@@ -79,6 +79,7 @@ struct DecodeParams {
     float* part_o;           // [num_partials, hpc*group, D]
     float* part_lse;         // [num_partials, hpc*group] (log2 domain)
     uint32_t* status;
+    int head_dim;            // 128 or 64
     int q_dtype, kv_dtype, o_dtype;
     int num_qo_heads, num_kv_heads, num_pages;
     int page_mult;           // page_size / 16: a page is read as page_mult 16-token sub-pages
@@ -108,6 +109,7 @@ struct AppendParams {
     int src_dtype, kv_dtype;
     int hnd;                 // cache layout: 0 [page][slot][head][d], 1 [page][head][slot][d]
     int page_size;
+    int head_dim;            // 128 or 64
     float k_inv, v_inv;      // fp32(1 / scale)
 };
 

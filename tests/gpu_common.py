@@ -28,6 +28,7 @@ class DeviceBatch:
                             qo_indptr=batch.qo_indptr if batch.mode == "prefill" else None,
                             q_dtype=batch.q_dtype, kv_dtype=batch.kv_dtype, o_dtype=batch.o_dtype,
                             sm_scale=batch.sm_scale, kv_layout=batch.kv_layout, page_size=batch.page_size,
+                            head_dim=batch.head_dim,
                             **plan_kw)
         self.ws = torch.empty(self.plan.workspace_bytes, dtype=torch.uint8, device=device)
         self.plan.upload(self.ws)
