@@ -87,6 +87,18 @@ def dist_env():
     return world, rank, local
 
 
+def max_over_ranks(values, device, world: int):
+    """Each value's maximum over all ranks (the slowest rank decides a
+    whole-job time); the values themselves at world size 1."""
+    if world == 1:
+        return [float(v) for v in values]
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t]
+
+
 def decode_bytes(b) -> int:
     """Algorithmic bytes of one decode pass over batch b."""
     qb = 1 if b.q_dtype in ("e4m3fn", "e5m2") else 2
@@ -521,10 +533,7 @@ def run_ours(args):
     torch.cuda.synchronize()
     dec_ms = [e[0].elapsed_time(e[1]) for e in events]
     ms_dec = statistics.mean(dec_ms)
-    if world > 1:
-        t = torch.tensor([ms_step, ms_dec], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_step, ms_dec = float(t[0]), float(t[1])
+    ms_step, ms_dec = max_over_ranks([ms_step, ms_dec], dev, world)
 
     # ---- end to end through the public API: re-plan, H2D inputs from pinned
     # host memory, run, D2H of the result, every step.
@@ -561,10 +570,7 @@ def run_ours(args):
     torch.cuda.synchronize()
     e2e_s = (time.perf_counter() - t1) / e2e_steps
     last_plan.device_status(ws)
-    if world > 1:
-        t = torch.tensor([e2e_s], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_s = float(t[0])
+    e2e_s, = max_over_ranks([e2e_s], dev, world)
 
     prefill_res = {}
     if args.mode == "all":
