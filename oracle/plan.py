@@ -23,10 +23,11 @@ fixed-split and disable-split options; the balanced rule is this library's):
 * Within each CTA, segments that cover only part of their row come first
   (keeping their order), then the rest.
 * A segment that spans its whole row (including a zero-page one) has
-  out_slot -1; the others get slots 0, 1, 2, ... in final segment order
-  (CTA by CTA).
+  out_slot -1; the others get slots 0, 1, 2, ... row by row (merge rows
+  ascending), and within a row by first page, so each merge row's slots are
+  consecutive.
 * Merge rows: rows with two or more segments, ascending; each lists its
-  slots ordered by first page.  row_merge[r] is the merge entry of row r, or
+  slots ordered by first page (so the slot list is 0, 1, 2, ...).  row_merge[r] is the merge entry of row r, or
   -1.  A separate merge pass combines each merge row's slots in that order.
 """
 from __future__ import annotations
@@ -95,25 +96,26 @@ def decode_metadata(kv_indptr, last_page_len, *, num_qo_heads, num_kv_heads, num
     per_cta = [[sg for sg in segs if is_partial(sg)] + [sg for sg in segs if not is_partial(sg)]
                for segs in per_cta]
 
-    slot = 0
     seg_count = [0] * R
-    row_slots = [[] for _ in range(R)]
+    row_parts = [[] for _ in range(R)]
     for segs in per_cta:
         for s in segs:
             seg_count[s[0]] += 1
             if not is_partial(s):
                 s[3] = -1
             else:
-                s[3] = slot
-                row_slots[s[0]].append((s[1], slot))
-                slot += 1
+                row_parts[s[0]].append(s)
+    slot = 0
     merge_rows, merge_ptr, merge_slots = [], [0], []
     row_merge = [-1] * R
     for r in range(R):
         if seg_count[r] >= 2:
             row_merge[r] = len(merge_rows)
             merge_rows.append(r)
-            merge_slots += [sl for _, sl in sorted(row_slots[r])]
+            for s in sorted(row_parts[r], key=lambda sg: sg[1]):
+                s[3] = slot
+                merge_slots.append(slot)
+                slot += 1
             merge_ptr.append(len(merge_slots))
 
     req_page = [kv_indptr[b] for b in range(B)]

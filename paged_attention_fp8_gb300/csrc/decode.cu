@@ -582,6 +582,8 @@ __global__ void __launch_bounds__(32 * 9, 1)
 }
 
 // Combine the partial states of each split (request, KV-head block) row.
+// The plan numbers a row's partial states consecutively (slots mptr[e] ..
+// mptr[e+1] - 1, in page order), so no slot list is read.
 // Block = one (merge entry, query head of the block); thread = one of the
 // head_dim dims.  Over the row's slots (page order) it keeps a running max of the
 // log2-domain lse_c and the rescaled sums of 2^lse_c and 2^lse_c O_c, four
@@ -596,7 +598,6 @@ __global__ void __launch_bounds__(128)
     const int nhb = meta[kMetaHeadBlocks];
     const int* mptr = meta + meta[kMetaOffMergePtr];
     const int* mrow = meta + meta[kMetaOffMergeRow];
-    const int* mslot = meta + meta[kMetaOffMergeSlot];
     const int hpb = hpc * group;
     const int e = blockIdx.x / hpb, hh = blockIdx.x - e * hpb, d = threadIdx.x;
     const int row = mrow[e];
@@ -608,7 +609,7 @@ __global__ void __launch_bounds__(128)
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
             const bool in = s + k < s1;
-            const size_t idx = (size_t)mslot[in ? s + k : s0] * hpb + hh;
+            const size_t idx = (size_t)(in ? s + k : s0) * hpb + hh;  // a row's slots are consecutive
             l[k] = in ? __ldcg(p.part_lse + idx) : -INFINITY;
             o[k] = in ? __ldcg(p.part_o + idx * p.head_dim + d) : 0.f;
         }

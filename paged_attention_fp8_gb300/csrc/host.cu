@@ -212,28 +212,31 @@ void build_decode_meta(pafp8_plan* pl) {
     auto partial = [&](const Seg& sg) { return !(sg.p0 == 0 && sg.p1 == np[sg.row]); };
     for (auto& v : per_cta) std::stable_partition(v.begin(), v.end(), partial);
 
-    // Output slots and the merge lists.
+    // Output slots and the merge lists.  Partial states are numbered merge
+    // row by merge row (ascending), each row's by first page, so a row's
+    // slots are consecutive and the merge reads them without an index list.
     std::vector<int> nseg_row(R, 0);
-    for (auto& v : per_cta)
-        for (auto& s : v) nseg_row[s.row]++;
-    int32_t nslot = 0;
-    std::vector<std::vector<std::pair<int32_t, int32_t>>> row_slots(R);  // (p0, slot)
+    std::vector<std::vector<Seg*>> row_parts(R);
     for (auto& v : per_cta)
         for (auto& s : v) {
-            if (!partial(s)) {
+            nseg_row[s.row]++;
+            if (!partial(s))
                 s.slot = -1;
-            } else {
-                s.slot = nslot++;
-                row_slots[s.row].push_back({s.p0, s.slot});
-            }
+            else
+                row_parts[s.row].push_back(&s);
         }
+    int32_t nslot = 0;
     std::vector<int32_t> merge_rows, merge_ptr{0}, merge_slots, row_merge(R, -1);
     for (int r = 0; r < R; ++r) {
         if (nseg_row[r] >= 2) {
-            std::sort(row_slots[r].begin(), row_slots[r].end());
+            std::sort(row_parts[r].begin(), row_parts[r].end(),
+                      [](const Seg* a, const Seg* b) { return a->p0 < b->p0; });
             row_merge[r] = (int32_t)merge_rows.size();
             merge_rows.push_back(r);
-            for (auto& ps : row_slots[r]) merge_slots.push_back(ps.second);
+            for (Seg* sg : row_parts[r]) {
+                sg->slot = nslot;
+                merge_slots.push_back(nslot++);
+            }
             merge_ptr.push_back((int32_t)merge_slots.size());
         }
     }

@@ -384,3 +384,22 @@ def test_run_head_scales_refuses_before_touching_memory(q, qs, ks, vs, word):
         assert st == 3 and word in pa.pafp8_last_error(), pa.pafp8_last_error()
     finally:
         pa.pafp8_plan_destroy(h)
+
+
+@pytest.mark.parametrize("case", PLAN_CASES)
+def test_partial_slots_are_consecutive_per_merge_row(case):
+    """The merge reads a split row's partial states at slots mptr[e] ..
+    mptr[e+1]-1 without an index list: the slot list must be 0, 1, 2, ...
+    and every partial segment's slot must lie in its own row's range, in page
+    order."""
+    plan, _, _ = _decode_plan(**case)
+    m = plan.metadata()
+    nseg, nparts, nmerge = int(m[7]), int(m[8]), int(m[9])
+    segs = m[m[13]:m[13] + 4 * nseg].reshape(-1, 4)
+    mptr = m[m[14]:m[14] + nmerge + 1]
+    mrow = m[m[15]:m[15] + nmerge]
+    mslot = m[m[16]:m[16] + nparts]
+    assert np.array_equal(mslot, np.arange(nparts))
+    for e in range(nmerge):
+        mine = sorted((int(p0), int(sl)) for r, p0, p1, sl in segs if r == mrow[e] and sl >= 0)
+        assert [sl for _, sl in mine] == list(range(mptr[e], mptr[e + 1]))
