@@ -57,7 +57,7 @@ L2_FLUSH_BYTES = 256 << 20
 # changed kernel reports null until it is captured again.
 NCU_TRAFFIC = {
     # profiles/decode_kernel_serving_decode.md
-    "eb81072890208ab61a2f349974c7a3a15fc90c92d2dd1f9c2b16b9682ce32644": 310214912,
+    "c3b0454dffeb97e1dcccd875dea46b8412816eb18e85fea91d3301223f5c2991": 309770496,
 }
 # The same for the prefill kernel, per workload index, keyed by the SHA-256
 # of its source (profiles/prefill_kernel_ragged_bf16_and_fp8.md).

@@ -87,18 +87,19 @@ __device__ __forceinline__ uint4 quantize16(const Raw16<SRC>& r, float inv) {
     return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
-template <int SRC, int KV>
+template <int SRC, int KV, int DH>
 __global__ void __launch_bounds__(kThreads) append_kernel(const AppendParams p) {
-    const long long total = p.nnz * (long long)p.num_kv_heads * (p.head_dim / 16);
+    constexpr int CPR = DH / 16;  // threads per (token, KV head) row
+    const long long total = p.nnz * (long long)p.num_kv_heads * CPR;
     for (long long t = (long long)blockIdx.x * kThreads + threadIdx.x; t < total;
          t += (long long)gridDim.x * kThreads) {
-        const long long row = t / (p.head_dim / 16);  // (token, KV head)
-        const int c = (int)(t - row * (p.head_dim / 16));
+        const long long row = t / CPR;  // (token, KV head)
+        const int c = (int)(t - row * CPR);
         const long long tok = row / p.num_kv_heads;
         const int h = (int)(row - tok * p.num_kv_heads);
         // The source rows do not depend on the page: their loads go first and
         // overlap the page-table lookups.
-        const size_t src = (size_t)row * p.head_dim + 16 * c;
+        const size_t src = (size_t)row * DH + 16 * c;
         Raw16<SRC> rk, rv;
         load_raw<SRC>(p.k_new, src, rk);
         load_raw<SRC>(p.v_new, src, rv);
@@ -120,26 +121,31 @@ __global__ void __launch_bounds__(kThreads) append_kernel(const AppendParams p) 
         const size_t slot = (size_t)(pos % p.page_size);
         const size_t dst = (p.hnd ? ((size_t)page * p.num_kv_heads + h) * p.page_size + slot
                                   : ((size_t)page * p.page_size + slot) * p.num_kv_heads + h) *
-                               p.head_dim +
+                               DH +
                            16 * c;
         *reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.k_cache) + dst) = quantize16<KV>(rk, p.k_inv);
         *reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.v_cache) + dst) = quantize16<KV>(rv, p.v_inv);
     }
 }
 
-template <int SRC, int KV>
+template <int SRC, int KV, int DH>
 cudaError_t launch_t(const AppendParams& p, cudaStream_t stream) {
-    const long long total = p.nnz * (long long)p.num_kv_heads * (p.head_dim / 16);
+    const long long total = p.nnz * (long long)p.num_kv_heads * (DH / 16);
     const long long blocks = (total + kThreads - 1) / kThreads;
     const int grid = (int)(blocks < 65535 ? blocks : 65535);
-    append_kernel<SRC, KV><<<grid, kThreads, 0, stream>>>(p);
+    append_kernel<SRC, KV, DH><<<grid, kThreads, 0, stream>>>(p);
     return cudaGetLastError();
+}
+
+template <int SRC, int KV>
+cudaError_t launch_kv(const AppendParams& p, cudaStream_t stream) {
+    return p.head_dim == 64 ? launch_t<SRC, KV, 64>(p, stream) : launch_t<SRC, KV, 128>(p, stream);
 }
 
 template <int SRC>
 cudaError_t launch_src(const AppendParams& p, cudaStream_t stream) {
-    return p.kv_dtype == PAFP8_E4M3FN ? launch_t<SRC, PAFP8_E4M3FN>(p, stream)
-                                      : launch_t<SRC, PAFP8_E5M2>(p, stream);
+    return p.kv_dtype == PAFP8_E4M3FN ? launch_kv<SRC, PAFP8_E4M3FN>(p, stream)
+                                      : launch_kv<SRC, PAFP8_E5M2>(p, stream);
 }
 
 }  // namespace
