@@ -74,7 +74,7 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--mode", choices=["all", "decode", "prefill", "append"], default="all",
+    ap.add_argument("--mode", choices=["all", "decode", "prefill", "append", "pod"], default="all",
                     help="which parts to time (profiling runs use one)")
     ap.add_argument("--prefill-steps", type=int, default=30)
     return ap.parse_args()
@@ -442,6 +442,98 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+# (prefill CTAs, decode CTAs) pairs timed; None = every SM.
+POD_SPLITS = ((-12, 12), (-16, 16), (-20, 20), (-24, 24), (-32, 32), (None, None), (None, 24), (-24, None),
+              (None, 64))
+
+
+def time_pod(dev, steps, warmup):
+    """Prefill and decode over one pool (POD workload 10): device time of
+    the two phases run one after the other, each on the whole GPU, against
+    pafp8_run_pod with the SMs split between them, over a few splits."""
+    import torch
+
+    import paged_attention_fp8_gb300 as pa
+    from paged_attention_fp8_gb300.workloads import POD_WORKLOADS, TORCH_DTYPES, pod_workload
+
+    pb = pod_workload(10)
+    pre, dec = pb.prefill, pb.decode
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    k = pre.k_cache.to(dev)
+    v = pre.v_cache.to(dev)
+    kw = dict(q_scale=pre.q_scale, k_scale=pre.k_scale, v_scale=pre.v_scale)
+
+    def side(b, ctas):
+        plan = pa.Plan(mode=b.mode, num_qo_heads=b.num_qo_heads, num_kv_heads=b.num_kv_heads,
+                       num_pages=b.num_pages, kv_indptr=b.kv_indptr, last_page_len=b.last_page_len,
+                       qo_indptr=b.qo_indptr if b.mode == "prefill" else None, q_dtype=b.q_dtype,
+                       kv_dtype=b.kv_dtype, o_dtype=b.o_dtype, sm_scale=b.sm_scale, num_ctas=ctas)
+        ws = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device=dev)
+        plan.upload(ws)
+        return plan, ws
+
+    t = {}
+    for name, b in (("p", pre), ("d", dec)):
+        t[name] = dict(q=b.q.to(dev), idx=b.kv_indices.to(dev),
+                       o=torch.empty(b.nnz_qo, b.num_qo_heads, b.head_dim, dtype=TORCH_DTYPES[b.o_dtype],
+                                     device=dev),
+                       lse=torch.empty(b.nnz_qo, b.num_qo_heads, dtype=torch.float32, device=dev))
+    flush = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def timed(call, plans):
+        for _ in range(warmup):
+            flush.sum()
+            call()
+        torch.cuda.synchronize()
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+        for i in range(steps):
+            flush.sum()
+            ev[i][0].record(stream)
+            call()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        for plan, ws in plans:
+            plan.device_status(ws)
+        return statistics.median(e[0].elapsed_time(e[1]) for e in ev) * 1e3
+
+    P, D = t["p"], t["d"]
+    pp, pw = side(pre, 0)
+    dp, dw = side(dec, 0)
+
+    def sequential():
+        pp.run(P["q"], k, v, P["idx"], P["o"], P["lse"], pw, **kw)
+        dp.run(D["q"], k, v, D["idx"], D["o"], D["lse"], dw, **kw)
+    seq_us = timed(sequential, [(pp, pw), (dp, dw)])
+    sweep = {}
+    for sp, sd in POD_SPLITS:
+        npre = sms if sp is None else sms + sp
+        ndec = sms if sd is None else sd
+        pp2, pw2 = side(pre, npre)
+        dp2, dw2 = side(dec, ndec)
+
+        def pod():
+            pa.pafp8_run_pod(pp2.handle, P["q"], P["idx"], P["o"], P["lse"], pw2, dp2.handle, D["q"], D["idx"],
+                             D["o"], D["lse"], dw2, k, v, **kw)
+        sweep[(npre, ndec)] = timed(pod, [(pp2, pw2), (dp2, dw2)])
+        del pp2, pw2, dp2, dw2
+    best = min(sweep, key=lambda x: sweep[x])
+    out = {"workload": POD_WORKLOADS[10], "unit": "us per step", "higher_is_better": False,
+           "sequential_us": round(seq_us, 2), "value": round(sweep[best], 2),
+           "prefill_ctas": best[0], "decode_ctas": best[1], "gain": round(seq_us / sweep[best], 4),
+           "sweep_us": {f"{a}+{b}": round(y, 2) for (a, b), y in sweep.items()},
+           "prefill_tflops": round(pre.causal_flops() / (sweep[best] * 1e-6) / 1e12, 2),
+           "decode_kv_gbs": round(decode_bytes(dec) / (sweep[best] * 1e-6) / 1e9, 2),
+           "steps": steps,
+           "note": "sequential = pafp8_run of the prefill then of the decode, each on every SM; value = "
+                   "pafp8_run_pod with the plans' CTA counts of the best entry of sweep_us (keys: prefill "
+                   "CTAs + decode CTAs; a sum above the SM count leaves the later CTAs waiting for SMs); "
+                   "prefill_tflops and decode_kv_gbs are each phase's work over the whole POD step"}
+    del k, v, t, P, D, flush, pp, pw, dp, dw
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -461,6 +553,14 @@ def run_ours(args):
         res = {str(i): time_prefill(i, dev, args.prefill_steps, max(3, args.warmup)) for i in (4, 5)}
         if rank == 0:
             print(json.dumps({"mode": "prefill", "prefill": res}), flush=True)
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
+    if args.mode == "pod":
+        res = time_pod(dev, args.prefill_steps, max(3, args.warmup))
+        if rank == 0:
+            print(json.dumps({"mode": "pod", "pod": res}), flush=True)
         if world > 1:
             dist.destroy_process_group()
         return
@@ -581,6 +681,7 @@ def run_ours(args):
         decode16 = time_decode_2byte(dev, min(args.steps, 200), max(3, min(args.warmup, 20)))
         append_res = {i: time_append(i, dev, min(args.steps, 200), max(3, min(args.warmup, 20)))
                       for i in (8, 9)}
+        pod_res = time_pod(dev, args.prefill_steps, max(3, min(args.warmup, 10)))
 
     if rank != 0:
         dist.destroy_process_group()
@@ -622,6 +723,7 @@ def run_ours(args):
                            "ragged_bf16_cache": prefill_res[7]}
         line["decode_2byte_cache"] = decode16
         line["append_kv"] = {"prefill_tokens": append_res[8], "decode_step": append_res[9]}
+        line["pod"] = pod_res
     if world == 1 and not args.no_cpu_baseline:
         n = oracle_sample_size(b, 15.0)
         dt, by, cores = oracle_decode_sample(b, n)

@@ -277,6 +277,57 @@ pafp8_status pafp8_run_decode_noalloc(const pafp8_plan *plan, int32_t q_dtype, c
                                       float q_scale, float k_scale, float v_scale,
                                       int32_t o_dtype, void *o, float *lse, void *stream);
 
+/* Prefill and decode over one paged cache in one call ("POD": the pages'
+ * POD and batch-POD kernels, "fp8 KV cache in the in-tree prefill kernel"
+ * (AMD-Ecosystem/flashinfer PR 368), Refusals, run a prefill batch and a
+ * decode batch together by reusing the prefill kernel's traits, and refuse an
+ * fp8 cache).  Here both phases run this library's own kernels, so every
+ * cache type pafp8_run serves is served, fp8 included.
+ *
+ * The prefill kernel is compute-bound on the tensor cores and the decode
+ * kernel bound by HBM; run together on disjoint SMs each uses what the other
+ * leaves.  The two phases are two grids launched from this one call: the
+ * decode kernel (and its split-KV merge) on a side stream of the decode plan,
+ * at the device's highest stream priority, forked from `stream` by an event
+ * and joined back to it; the prefill kernel on `stream`.  The SM split is the
+ * plans' num_ctas: a prefill plan made with num_ctas = Np and a decode plan
+ * with Nd run side by side when Np + Nd <= the SM count (152 on GB300); a
+ * larger sum is still correct, the CTAs beyond it waiting for free SMs.  On a
+ * few SMs the decode phase is bound by its per-SM rate (about 60 GB/s of KV
+ * per SM on GB300), so the best Nd balances decode bytes / (Nd * 60 GB/s)
+ * against the prefill's time on the other SMs: 20 of 152 for a 304 MB decode
+ * batch beside a 236 us prefill.
+ *
+ *   prefill   the prefill phase: a plan of PAFP8_MODE_PREFILL and its q,
+ *             kv_indices, o, lse and uploaded workspace, as pafp8_run takes
+ *             them
+ *   decode    the decode phase: a plan of PAFP8_MODE_DECODE and its buffers
+ *   k_cache,
+ *   v_cache   the one cache both phases read; both plans must describe it
+ *             alike (num_pages, page_size, num_kv_heads, head_dim, kv_layout)
+ * The dtypes and scales apply to both phases, and each phase is checked as
+ * pafp8_run checks it, before anything is launched.  The two workspaces must
+ * not overlap.  Each phase's results are bit-identical to pafp8_run of its
+ * plan alone.  On return `stream` is ordered after both phases.  The first
+ * call with a decode plan creates that plan's side stream and two events
+ * (make it outside stream capture); pafp8_plan_destroy releases them.  Later
+ * calls create nothing; nothing is allocated on the device or synchronized.
+ * A plan is not to be used by two threads at once. */
+typedef struct pafp8_pod_phase {
+    const pafp8_plan *plan;
+    const void *q;
+    const int32_t *kv_indices;
+    void *o;
+    float *lse;
+    void *workspace;
+    size_t workspace_bytes;
+} pafp8_pod_phase;
+
+pafp8_status pafp8_run_pod(const pafp8_pod_phase *prefill, const pafp8_pod_phase *decode,
+                           int32_t q_dtype, int32_t k_dtype, const void *k_cache, int32_t v_dtype,
+                           const void *v_cache, float q_scale, float k_scale, float v_scale,
+                           int32_t o_dtype, void *stream);
+
 /* Quantize new K/V tokens into the paged fp8 cache: the step that writes the
  * cache every other entry point reads.  The pages take such a cache as given
  * (fp8 K/V with per-tensor k_scale/v_scale, dequantized as code * scale, "fp8

@@ -42,7 +42,7 @@ _NAME_CODES = {"default": DTYPE_DEFAULT, "f16": F16, "float16": F16, "bf16": BF1
 EXPORTS = ("pafp8_abi_version", "pafp8_last_error", "pafp8_plan_create", "pafp8_plan_destroy",
            "pafp8_workspace_bytes", "pafp8_plan_metadata", "pafp8_plan_upload", "pafp8_run",
            "pafp8_run_stage", "pafp8_device_status", "pafp8_run_decode_noalloc", "pafp8_append_kv",
-           "pafp8_run_head_scales")
+           "pafp8_run_head_scales", "pafp8_run_pod")
 
 
 class Pafp8Error(RuntimeError):
@@ -63,6 +63,12 @@ class plan_desc(ctypes.Structure):
                 ("sm_scale", ctypes.c_float), ("fixed_split_pages", ctypes.c_int32),
                 ("disable_split_kv", ctypes.c_int32), ("num_ctas", ctypes.c_int32),
                 ("kv_layout", ctypes.c_int32)]
+
+
+class pod_phase(ctypes.Structure):
+    _fields_ = [("plan", ctypes.c_void_p), ("q", ctypes.c_void_p), ("kv_indices", ctypes.c_void_p),
+                ("o", ctypes.c_void_p), ("lse", ctypes.c_void_p), ("workspace", ctypes.c_void_p),
+                ("workspace_bytes", ctypes.c_size_t)]
 
 
 _lib = None
@@ -102,6 +108,9 @@ def lib() -> ctypes.CDLL:
     L.pafp8_append_kv.restype = i32
     L.pafp8_run_head_scales.argtypes = [vp, i32, vp, i32, vp, i32, vp, vp, vp, vp, vp, i32, vp, vp, vp, sz, vp]
     L.pafp8_run_head_scales.restype = i32
+    L.pafp8_run_pod.argtypes = [ctypes.POINTER(pod_phase), ctypes.POINTER(pod_phase), i32, i32, vp, i32, vp,
+                                f32, f32, f32, i32, vp]
+    L.pafp8_run_pod.restype = i32
     _lib = L
     return L
 
@@ -239,6 +248,28 @@ def pafp8_run_decode_noalloc(handle: int, q, k_cache, v_cache, kv_indices, o, ls
         dtype_code(v_dtype if v_dtype is not None else v_cache.dtype), _ptr(v_cache),
         _ptr(kv_indices), float(q_scale), float(k_scale), float(v_scale),
         dtype_code(o_dtype if o_dtype is not None else o.dtype), _ptr(o), _ptr(lse), _stream(stream)))
+
+
+def _phase(handle, q, kv_indices, o, lse, workspace) -> pod_phase:
+    return pod_phase(handle, _ptr(q), _ptr(kv_indices), _ptr(o), _ptr(lse), _ptr(workspace),
+                     workspace.numel() * workspace.element_size())
+
+
+def pafp8_run_pod(prefill_handle: int, prefill_q, prefill_kv_indices, prefill_o, prefill_lse, prefill_workspace,
+                  decode_handle: int, decode_q, decode_kv_indices, decode_o, decode_lse, decode_workspace,
+                  k_cache, v_cache, *, q_scale=1.0, k_scale=1.0, v_scale=1.0, q_dtype=None, k_dtype=None,
+                  v_dtype=None, o_dtype=None, stream=None) -> None:
+    """A prefill plan's phase and a decode plan's phase over one cache in one
+    call, side by side on the SMs their plans' num_ctas give (see
+    include/pafp8.h).  Dtype codes default to the prefill tensors' dtypes."""
+    pre = _phase(prefill_handle, prefill_q, prefill_kv_indices, prefill_o, prefill_lse, prefill_workspace)
+    dec = _phase(decode_handle, decode_q, decode_kv_indices, decode_o, decode_lse, decode_workspace)
+    _check(lib().pafp8_run_pod(
+        ctypes.byref(pre), ctypes.byref(dec), dtype_code(q_dtype if q_dtype is not None else prefill_q.dtype),
+        dtype_code(k_dtype if k_dtype is not None else k_cache.dtype), _ptr(k_cache),
+        dtype_code(v_dtype if v_dtype is not None else v_cache.dtype), _ptr(v_cache),
+        float(q_scale), float(k_scale), float(v_scale),
+        dtype_code(o_dtype if o_dtype is not None else prefill_o.dtype), _stream(stream)))
 
 
 def pafp8_append_kv(k_new, v_new, batch_indices, positions, kv_indptr, kv_indices, k_cache, v_cache, *,

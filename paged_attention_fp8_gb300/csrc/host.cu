@@ -134,6 +134,15 @@ struct pafp8_plan {
     int num_ctas = 0, num_partials = 0, num_merge = 0;
     size_t meta_bytes = 0, part_o_off = 0, part_lse_off = 0, status_off = 0, ws_bytes = 0;
     void* uploaded_ws = nullptr;
+    // Side stream and fork/join events of pafp8_run_pod for a decode plan,
+    // created by its first call.
+    mutable cudaStream_t pod_stream = nullptr;
+    mutable cudaEvent_t pod_fork = nullptr, pod_join = nullptr;
+    ~pafp8_plan() {
+        if (pod_join != nullptr) cudaEventDestroy(pod_join);
+        if (pod_fork != nullptr) cudaEventDestroy(pod_fork);
+        if (pod_stream != nullptr) cudaStreamDestroy(pod_stream);
+    }
 };
 
 namespace {
@@ -737,13 +746,14 @@ pafp8_status pafp8_plan_upload(pafp8_plan* plan, void* workspace, size_t workspa
 namespace {
 
 // Shared body of the run entry points.  Per-head scale tensors (device
-// arrays) replace the per-tensor scales when k_scales is not NULL.
+// arrays) replace the per-tensor scales when k_scales is not NULL.  With
+// launch false only the checks run.
 pafp8_status run_impl(const pafp8_plan* plan, int32_t stage, int32_t q_dtype, const void* q,
                       int32_t k_dtype, const void* k_cache, int32_t v_dtype, const void* v_cache,
                       const int32_t* kv_indices, float q_scale, float k_scale, float v_scale,
                       const float* q_scales, const float* k_scales, const float* v_scales,
                       int32_t o_dtype, void* o, float* lse, void* workspace, size_t workspace_bytes,
-                      void* stream) {
+                      void* stream, bool launch = true) {
     if (plan == nullptr) return fail(PAFP8_ERR_ARG, "plan is NULL");
     if (stage < 0 || stage > 2) return fail(PAFP8_ERR_ARG, "stage %d is not 0, 1 or 2", (int)stage);
     const pafp8_plan_desc& d = plan->desc;
@@ -797,6 +807,7 @@ pafp8_status run_impl(const pafp8_plan* plan, int32_t stage, int32_t q_dtype, co
         return fail(PAFP8_ERR_ARG, "q, o, k_cache and v_cache must be 16-byte aligned");
     if ((uintptr_t)lse % 4 != 0 || (uintptr_t)kv_indices % 4 != 0)
         return fail(PAFP8_ERR_ARG, "lse and kv_indices must be 4-byte aligned");
+    if (!launch) return PAFP8_OK;
 
     cudaStream_t s = (cudaStream_t)stream;
     char* ws = (char*)workspace;
@@ -1044,6 +1055,89 @@ pafp8_status pafp8_run_decode_noalloc(const pafp8_plan* plan, int32_t q_dtype, c
     if (e != cudaSuccess) {
         cudaGetLastError();
         return fail(PAFP8_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(e));
+    }
+    return PAFP8_OK;
+}
+
+// Prefill and decode phases of one call on disjoint SMs: the decode grid on
+// the decode plan's side stream (highest priority, forked from and joined to
+// `stream`), the prefill grid on `stream`.  The plans' num_ctas split the SMs.
+pafp8_status pafp8_run_pod(const pafp8_pod_phase* prefill, const pafp8_pod_phase* decode, int32_t q_dtype,
+                           int32_t k_dtype, const void* k_cache, int32_t v_dtype, const void* v_cache,
+                           float q_scale, float k_scale, float v_scale, int32_t o_dtype, void* stream) {
+    if (prefill == nullptr || decode == nullptr || prefill->plan == nullptr || decode->plan == nullptr)
+        return fail(PAFP8_ERR_ARG, "both phases and their plans are required");
+    const pafp8_plan_desc& a = prefill->plan->desc;
+    const pafp8_plan_desc& b = decode->plan->desc;
+    if (a.mode != PAFP8_MODE_PREFILL) return fail(PAFP8_ERR_ARG, "the prefill phase's plan is a decode plan");
+    if (b.mode != PAFP8_MODE_DECODE) return fail(PAFP8_ERR_ARG, "the decode phase's plan is a prefill plan");
+    if (a.num_pages != b.num_pages || a.page_size != b.page_size || a.num_kv_heads != b.num_kv_heads ||
+        a.head_dim != b.head_dim || a.kv_layout != b.kv_layout)
+        return fail(PAFP8_ERR_SHAPE,
+                    "the two plans describe different caches: prefill num_pages %d page_size %d "
+                    "num_kv_heads %d head_dim %d layout %d, decode %d %d %d %d %d",
+                    (int)a.num_pages, (int)a.page_size, (int)a.num_kv_heads, (int)a.head_dim,
+                    (int)a.kv_layout, (int)b.num_pages, (int)b.page_size, (int)b.num_kv_heads,
+                    (int)b.head_dim, (int)b.kv_layout);
+    const uintptr_t w0 = (uintptr_t)prefill->workspace, w1 = (uintptr_t)decode->workspace;
+    if (w0 != 0 && w1 != 0 && w0 < w1 + decode->workspace_bytes && w1 < w0 + prefill->workspace_bytes)
+        return fail(PAFP8_ERR_WORKSPACE, "the prefill and decode workspaces overlap");
+    pafp8_status st;
+    const pafp8_pod_phase* ph[2] = {decode, prefill};
+    for (const pafp8_pod_phase* x : ph) {
+        if ((st = run_impl(x->plan, 0, q_dtype, x->q, k_dtype, k_cache, v_dtype, v_cache, x->kv_indices,
+                           q_scale, k_scale, v_scale, nullptr, nullptr, nullptr, o_dtype, x->o, x->lse,
+                           x->workspace, x->workspace_bytes, stream, false)) != PAFP8_OK)
+            return st;
+    }
+    const pafp8_plan* dp = decode->plan;
+    if (dp->pod_stream == nullptr) {
+        int lo = 0, hi = 0;
+        cudaError_t e = cudaDeviceGetStreamPriorityRange(&lo, &hi);
+        cudaStream_t side = nullptr;
+        cudaEvent_t fork = nullptr, join = nullptr;
+        if (e == cudaSuccess) e = cudaStreamCreateWithPriority(&side, cudaStreamNonBlocking, hi);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&fork, cudaEventDisableTiming);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&join, cudaEventDisableTiming);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            if (join != nullptr) cudaEventDestroy(join);
+            if (fork != nullptr) cudaEventDestroy(fork);
+            if (side != nullptr) cudaStreamDestroy(side);
+            return fail(PAFP8_ERR_CUDA, "creating the side stream failed: %s", cudaGetErrorString(e));
+        }
+        dp->pod_stream = side;
+        dp->pod_fork = fork;
+        dp->pod_join = join;
+    }
+    cudaStream_t s = (cudaStream_t)stream;
+    cudaError_t e = cudaEventRecord(dp->pod_fork, s);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(dp->pod_stream, dp->pod_fork, 0);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(PAFP8_ERR_CUDA, "forking the side stream failed: %s", cudaGetErrorString(e));
+    }
+    // Decode first, so that its CTAs are dispatched first when both grids are
+    // ready; its stream priority keeps them ahead of the prefill CTAs.
+    const pafp8_status sd = run_impl(dp, 0, q_dtype, decode->q, k_dtype, k_cache, v_dtype, v_cache,
+                                     decode->kv_indices, q_scale, k_scale, v_scale, nullptr, nullptr, nullptr,
+                                     o_dtype, decode->o, decode->lse, decode->workspace,
+                                     decode->workspace_bytes, dp->pod_stream);
+    const pafp8_status sp =
+        sd != PAFP8_OK ? sd
+                       : run_impl(prefill->plan, 0, q_dtype, prefill->q, k_dtype, k_cache, v_dtype, v_cache,
+                                  prefill->kv_indices, q_scale, k_scale, v_scale, nullptr, nullptr, nullptr,
+                                  o_dtype, prefill->o, prefill->lse, prefill->workspace,
+                                  prefill->workspace_bytes, s);
+    // Join even after a failed launch, so that `stream` never runs ahead of
+    // work already queued on the side stream.
+    e = cudaEventRecord(dp->pod_join, dp->pod_stream);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(s, dp->pod_join, 0);
+    if (sd != PAFP8_OK) return sd;
+    if (sp != PAFP8_OK) return sp;
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(PAFP8_ERR_CUDA, "joining the side stream failed: %s", cudaGetErrorString(e));
     }
     return PAFP8_OK;
 }

@@ -333,3 +333,44 @@ def append_workload(index: int, *, scale_down: int = 1) -> AppendBatch:
     if index == 9:
         return new_tokens(workload(2, scale_down=scale_down), src_dtype="bf16", seed=1009)
     raise ValueError(f"unknown append workload {index}")
+
+
+@dataclasses.dataclass
+class PodBatch:
+    """A prefill batch and a decode batch over one page pool: ``prefill`` and
+    ``decode`` share the same ``k_cache``/``v_cache`` tensors, ``num_pages``
+    and per-tensor scales; the decode requests own pages of the pool that no
+    prefill request owns."""
+    prefill: PagedBatch
+    decode: PagedBatch
+
+
+POD_WORKLOADS = {
+    10: "prefill and decode in one call over one page pool: the ragged causal prefill of workload 4 "
+        "(16 requests) and the serving decode of workload 2 (64 requests), e4m3fn KV, bf16 q/o",
+}
+
+
+def pod_batch(prefill: PagedBatch, decode: PagedBatch) -> PodBatch:
+    """Join two batches' pools (prefill pages first) into one; the decode
+    requests' page indices move past the prefill pool and both read the cache
+    with the prefill batch's per-tensor scales (the decode batch's fp8 codes
+    are kept, so its values scale with them)."""
+    if (prefill.kv_dtype, prefill.num_kv_heads, prefill.head_dim, prefill.page_size, prefill.kv_layout) != (
+            decode.kv_dtype, decode.num_kv_heads, decode.head_dim, decode.page_size, decode.kv_layout):
+        raise ValueError("the two batches' caches differ in dtype or shape")
+    k = torch.cat([prefill.k_cache.view(torch.uint8), decode.k_cache.view(torch.uint8)]).view(prefill.k_cache.dtype)
+    v = torch.cat([prefill.v_cache.view(torch.uint8), decode.v_cache.view(torch.uint8)]).view(prefill.v_cache.dtype)
+    pool = prefill.num_pages + decode.num_pages
+    pre = dataclasses.replace(prefill, k_cache=k, v_cache=v, num_pages=pool)
+    dec = dataclasses.replace(decode, k_cache=k, v_cache=v, num_pages=pool,
+                              kv_indices=decode.kv_indices + prefill.num_pages,
+                              k_scale=prefill.k_scale, v_scale=prefill.v_scale)
+    return PodBatch(prefill=pre, decode=dec)
+
+
+def pod_workload(index: int, *, scale_down: int = 1) -> PodBatch:
+    """The named POD workloads (index 10: workloads 4 and 2 over one pool)."""
+    if index == 10:
+        return pod_batch(workload(4, scale_down=scale_down), workload(2, scale_down=scale_down))
+    raise ValueError(f"unknown POD workload {index}")

@@ -403,3 +403,58 @@ def test_partial_slots_are_consecutive_per_merge_row(case):
     for e in range(nmerge):
         mine = sorted((int(p0), int(sl)) for r, p0, p1, sl in segs if r == mrow[e] and sl >= 0)
         assert [sl for _, sl in mine] == list(range(mptr[e], mptr[e + 1]))
+
+
+# ---------------------------------------------------------------- POD refusals
+
+def _pod_plans(pre=None, dec=None):
+    hp = pa.pafp8_plan_create(_desc(mode=1, **(pre or {})), np.array([0, 2], np.int32),
+                              np.array([5], np.int32), np.array([0, 5], np.int32))
+    hd = _create(**(dec or {}))
+    return hp, hd
+
+
+def _pod_call(hp, hd, *, ws_p=1 << 20, ws_d=1 << 24, q=pa.BF16, swap=False):
+    pre = pa.pod_phase(hp, 256, 16, 512, 1024, ws_p, 4096)
+    dec = pa.pod_phase(hd, 256, 16, 512, 1024, ws_d, 4096)
+    if swap:
+        pre, dec = dec, pre
+    return pa.lib().pafp8_run_pod(ctypes.byref(pre), ctypes.byref(dec), q, pa.E4M3FN, 16, pa.E4M3FN, 16,
+                                  1.0, 1.0, 1.0, pa.BF16, None)
+
+
+@pytest.mark.parametrize("case,status,word", [
+    ("swap", 3, "decode plan"),
+    ("pages", 2, "different caches"),
+    ("heads", 2, "different caches"),
+    ("overlap", 4, "overlap"),
+    ("qdtype", 1, "plan was made for"),
+])
+def test_run_pod_refuses_before_any_launch(case, status, word):
+    """Every refusal comes back before a CUDA call (none can succeed here:
+    this host has no GPU, so reaching one would give ERR_CUDA instead)."""
+    pre, dec = {}, {}
+    if case == "pages":
+        dec = dict(num_pages=8)
+    if case == "heads":
+        pre = dict(num_qo_heads=16, num_kv_heads=4)
+    hp, hd = _pod_plans(pre, dec)
+    try:
+        kw = {}
+        if case == "swap":
+            kw["swap"] = True
+        if case == "overlap":
+            kw["ws_d"] = (1 << 20) + 2048
+        if case == "qdtype":
+            kw["q"] = pa.F16
+        st = _pod_call(hp, hd, **kw)
+        assert st == status and word in pa.pafp8_last_error(), pa.pafp8_last_error()
+    finally:
+        pa.pafp8_plan_destroy(hp)
+        pa.pafp8_plan_destroy(hd)
+
+
+def test_run_pod_refuses_missing_phase():
+    st = pa.lib().pafp8_run_pod(None, None, pa.BF16, pa.E4M3FN, 16, pa.E4M3FN, 16, 1.0, 1.0, 1.0, pa.BF16,
+                                None)
+    assert st == 3 and "both phases" in pa.pafp8_last_error()
