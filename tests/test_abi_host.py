@@ -458,3 +458,25 @@ def test_run_pod_refuses_missing_phase():
     st = pa.lib().pafp8_run_pod(None, None, pa.BF16, pa.E4M3FN, 16, pa.E4M3FN, 16, 1.0, 1.0, 1.0, pa.BF16,
                                 None)
     assert st == 3 and "both phases" in pa.pafp8_last_error()
+
+
+def test_run_pod_binding_passes_both_phases():
+    """The Python wrapper marshals both phases: a cache mismatch between the
+    two plans comes back as the C library's refusal (no GPU is touched)."""
+    import torch
+    hp, hd = _pod_plans(None, dict(num_pages=8))
+    try:
+        q = torch.zeros(5, 8, 128, dtype=torch.bfloat16)
+        qd = torch.zeros(1, 8, 128, dtype=torch.bfloat16)
+        kc = torch.zeros(8, 16, 2, 128, dtype=torch.uint8)
+        idx = torch.zeros(2, dtype=torch.int32)
+        o, od = torch.zeros_like(q), torch.zeros_like(qd)
+        lse, lsed = torch.zeros(5, 8), torch.zeros(1, 8)
+        wp, wd = torch.zeros(64, dtype=torch.uint8), torch.zeros(64, dtype=torch.uint8)
+        with pytest.raises(pa.Pafp8Error) as ei:
+            pa.pafp8_run_pod(hp, q, idx, o, lse, wp, hd, qd, idx, od, lsed, wd, kc, kc, k_dtype=pa.E4M3FN,
+                             v_dtype=pa.E4M3FN, stream=0)
+        assert ei.value.status == 2 and "different caches" in str(ei.value)
+    finally:
+        pa.pafp8_plan_destroy(hp)
+        pa.pafp8_plan_destroy(hd)
