@@ -65,7 +65,7 @@ typedef enum pafp8_status {
     PAFP8_ERR_CUDA = 5,        /* a CUDA runtime call failed                 */
     PAFP8_ERR_TIMEOUT = 6,     /* a kernel's bounded wait expired            */
     PAFP8_ERR_BOUNDS = 7,      /* a page index outside [0, num_pages)        */
-    PAFP8_ERR_UNSUPPORTED = 8  /* valid request this build does not serve    */
+    PAFP8_ERR_UNSUPPORTED = 8  /* valid request this library does not serve  */
 } pafp8_status;
 
 enum { PAFP8_MODE_DECODE = 0, PAFP8_MODE_PREFILL = 1 };
@@ -79,7 +79,7 @@ enum { PAFP8_MODE_DECODE = 0, PAFP8_MODE_PREFILL = 1 };
  * read by the same kernels through differently strided tensor maps. */
 enum { PAFP8_LAYOUT_NHD = 0, PAFP8_LAYOUT_HND = 1 };
 
-/* Static description of one batch.  Shapes served by this build:
+/* Static description of one batch.  Shapes served by this library:
  * head_dim 128, or 64 in decode; page_size a multiple of 16 (NHD) or 16 (HND), a page of
  * 16 m tokens being read as m consecutive 16-token sub-pages (so
  * num_pages * page_size / 16 must stay below 2^31); num_qo_heads a multiple of num_kv_heads with

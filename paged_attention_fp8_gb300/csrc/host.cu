@@ -603,7 +603,7 @@ pafp8_status pafp8_plan_create(const pafp8_plan_desc* desc_in, const int32_t* kv
                     (int)d.num_qo_heads, (int)d.num_kv_heads);
     if (d.head_dim != kHeadDim && !(d.head_dim == 64 && d.mode == PAFP8_MODE_DECODE))
         return fail(PAFP8_ERR_UNSUPPORTED,
-                    "head_dim %d is not served by this build (%d; 64 too in decode)", (int)d.head_dim,
+                    "head_dim %d is not served by this library (%d; 64 too in decode)", (int)d.head_dim,
                     kHeadDim);
     if (d.num_pages < 0) return fail(PAFP8_ERR_SHAPE, "num_pages %d is negative", (int)d.num_pages);
     if (d.kv_layout != PAFP8_LAYOUT_NHD && d.kv_layout != PAFP8_LAYOUT_HND)
@@ -611,7 +611,7 @@ pafp8_status pafp8_plan_create(const pafp8_plan_desc* desc_in, const int32_t* kv
     if (d.page_size <= 0 || d.page_size % kPageSize != 0 ||
         (int64_t)d.num_pages * (d.page_size / kPageSize) > INT32_MAX)
         return fail(PAFP8_ERR_UNSUPPORTED,
-                    "page_size %d is not served by this build (a multiple of %d tokens, with "
+                    "page_size %d is not served by this library (a multiple of %d tokens, with "
                     "num_pages * page_size / %d below 2^31)",
                     (int)d.page_size, kPageSize, kPageSize);
     if (d.page_size != kPageSize && d.kv_layout == PAFP8_LAYOUT_HND)
@@ -1168,10 +1168,10 @@ pafp8_status pafp8_append_kv(int32_t src_dtype, const void* k_new, const void* v
     if (num_kv_heads <= 0)
         return fail(PAFP8_ERR_SHAPE, "num_kv_heads %d must be positive", (int)num_kv_heads);
     if (head_dim != kHeadDim && head_dim != 64)
-        return fail(PAFP8_ERR_UNSUPPORTED, "head_dim %d is not served by this build (%d or 64)",
+        return fail(PAFP8_ERR_UNSUPPORTED, "head_dim %d is not served by this library (%d or 64)",
                     (int)head_dim, kHeadDim);
     if (page_size <= 0 || page_size % kPageSize != 0)
-        return fail(PAFP8_ERR_UNSUPPORTED, "page_size %d is not served by this build (a multiple of %d)",
+        return fail(PAFP8_ERR_UNSUPPORTED, "page_size %d is not served by this library (a multiple of %d)",
                     (int)page_size, kPageSize);
     if (page_size != kPageSize && kv_layout == PAFP8_LAYOUT_HND)
         return fail(PAFP8_ERR_UNSUPPORTED, "the HND layout is served with page_size %d only (got %d)",

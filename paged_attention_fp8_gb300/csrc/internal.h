@@ -10,8 +10,8 @@
 
 namespace pafp8 {
 
-constexpr int kHeadDim = 128;   // head_dim served by this build
-constexpr int kPageSize = 16;   // page_size served by this build
+constexpr int kHeadDim = 128;   // head_dim served by this library
+constexpr int kPageSize = 16;   // page_size served by this library
 constexpr int kMaxGroupDecode = 8;
 constexpr int kMaxGroupPrefill = 16;
 constexpr int kTileRows = 128;   // prefill query rows (token x head) per tile
