@@ -26,7 +26,13 @@
  *   - Every function returns a pafp8_status; on failure pafp8_last_error()
  *     returns a sentence naming the offending values (thread-local, valid
  *     until the next failing call on this thread).  Nothing aborts.
- *   - pafp8_run neither allocates nor synchronizes.
+ *   - pafp8_run neither allocates nor synchronizes, unless PAFP8_DEBUG is
+ *     set in the environment (to anything but "0"): then every run call that
+ *     launches (pafp8_run, _stage, _head_scales, _pod) synchronizes its
+ *     stream and returns the kernels' status as pafp8_device_status reports
+ *     it (PAFP8_ERR_BOUNDS, PAFP8_ERR_TIMEOUT), so a bad page index or an
+ *     expired wait surfaces at the call that caused it.  Not for use under
+ *     stream capture.
  */
 #ifndef PAFP8_H
 #define PAFP8_H

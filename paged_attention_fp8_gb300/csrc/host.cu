@@ -16,6 +16,7 @@
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <string>
 #include <vector>
@@ -745,15 +746,15 @@ pafp8_status pafp8_plan_upload(pafp8_plan* plan, void* workspace, size_t workspa
 
 namespace {
 
-// Shared body of the run entry points.  Per-head scale tensors (device
-// arrays) replace the per-tensor scales when k_scales is not NULL.  With
-// launch false only the checks run.
-pafp8_status run_impl(const pafp8_plan* plan, int32_t stage, int32_t q_dtype, const void* q,
+// Checks and launches of the run entry points.  Per-head scale tensors
+// (device arrays) replace the per-tensor scales when k_scales is not NULL.
+// With launch false only the checks run.
+pafp8_status run_body(const pafp8_plan* plan, int32_t stage, int32_t q_dtype, const void* q,
                       int32_t k_dtype, const void* k_cache, int32_t v_dtype, const void* v_cache,
                       const int32_t* kv_indices, float q_scale, float k_scale, float v_scale,
                       const float* q_scales, const float* k_scales, const float* v_scales,
                       int32_t o_dtype, void* o, float* lse, void* workspace, size_t workspace_bytes,
-                      void* stream, bool launch = true) {
+                      void* stream, bool launch) {
     if (plan == nullptr) return fail(PAFP8_ERR_ARG, "plan is NULL");
     if (stage < 0 || stage > 2) return fail(PAFP8_ERR_ARG, "stage %d is not 0, 1 or 2", (int)stage);
     const pafp8_plan_desc& d = plan->desc;
@@ -902,6 +903,32 @@ pafp8_status run_impl(const pafp8_plan* plan, int32_t stage, int32_t q_dtype, co
         return fail(PAFP8_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(e));
     }
     return PAFP8_OK;
+}
+
+}  // namespace
+
+namespace {
+
+// PAFP8_DEBUG set to anything but "0" in the environment: every launching
+// run call synchronizes its stream and returns the kernels' status (what
+// pafp8_device_status would report), so that a bad page index or an expired
+// wait surfaces at the call that caused it.  Not for use under stream capture.
+bool debug_sync() {
+    const char* v = std::getenv("PAFP8_DEBUG");
+    return v != nullptr && v[0] != '\0' && !(v[0] == '0' && v[1] == '\0');
+}
+
+pafp8_status run_impl(const pafp8_plan* plan, int32_t stage, int32_t q_dtype, const void* q,
+                      int32_t k_dtype, const void* k_cache, int32_t v_dtype, const void* v_cache,
+                      const int32_t* kv_indices, float q_scale, float k_scale, float v_scale,
+                      const float* q_scales, const float* k_scales, const float* v_scales,
+                      int32_t o_dtype, void* o, float* lse, void* workspace, size_t workspace_bytes,
+                      void* stream, bool launch = true) {
+    const pafp8_status st = run_body(plan, stage, q_dtype, q, k_dtype, k_cache, v_dtype, v_cache, kv_indices,
+                                     q_scale, k_scale, v_scale, q_scales, k_scales, v_scales, o_dtype, o, lse,
+                                     workspace, workspace_bytes, stream, launch);
+    if (st != PAFP8_OK || !launch || !debug_sync()) return st;
+    return pafp8_device_status(plan, workspace, stream);
 }
 
 }  // namespace

@@ -1,0 +1,62 @@
+"""Run-call modes: PAFP8_DEBUG (a launching call synchronizes and returns the
+kernels' status) and pafp8_run captured into a CUDA graph (bit-identical
+replays), for decode and prefill."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import paged_attention_fp8_gb300 as pa
+from common import oracle_on
+from gpu_common import DeviceBatch, assert_close
+from paged_attention_fp8_gb300.workloads import make_batch, workload
+
+pytestmark = pytest.mark.gpu
+
+
+def test_debug_mode_reports_a_bad_page_at_the_call(cuda_device, monkeypatch):
+    b = workload(1)
+    b.kv_indices = b.kv_indices.clone()
+    b.kv_indices[3] = b.num_pages + 5
+    db = DeviceBatch(b, cuda_device)
+    monkeypatch.setenv("PAFP8_DEBUG", "1")
+    with pytest.raises(pa.Pafp8Error) as ei:
+        db.run()
+    assert ei.value.status == 7  # PAFP8_ERR_BOUNDS, from the run call itself
+    db.plan.device_status(db.ws)  # the status word was read and cleared
+
+
+def test_debug_mode_is_silent_on_good_input(cuda_device, monkeypatch):
+    b = make_batch([1, 40, 300], [1, 20, 129], num_qo_heads=8, num_kv_heads=2, seed=3)
+    db = DeviceBatch(b, cuda_device, num_ctas=7)
+    monkeypatch.setenv("PAFP8_DEBUG", "1")
+    db.run()
+    monkeypatch.setenv("PAFP8_DEBUG", "0")
+    o, lse = db.result()
+    ro, rl = oracle_on(b)
+    assert_close(o, lse, ro, rl, "prefill under PAFP8_DEBUG")
+
+
+@pytest.mark.parametrize("mode", ["decode", "prefill"])
+def test_run_replays_from_a_cuda_graph(cuda_device, mode):
+    if mode == "decode":
+        b = make_batch([0, 17, 900, 2500], num_qo_heads=32, num_kv_heads=8, seed=31)
+    else:
+        b = make_batch([40, 300, 700], [40, 129, 256], num_qo_heads=32, num_kv_heads=8, seed=32)
+    db = DeviceBatch(b, cuda_device, num_ctas=24)
+    db.run()
+    o1, l1 = db.result()
+    db.o.zero_()
+    db.lse.zero_()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            db.run()
+    for _ in range(2):
+        g.replay()
+    torch.cuda.synchronize()
+    o2, l2 = db.result()
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
