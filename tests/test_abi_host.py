@@ -480,3 +480,25 @@ def test_run_pod_binding_passes_both_phases():
     finally:
         pa.pafp8_plan_destroy(hp)
         pa.pafp8_plan_destroy(hd)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_random_plans_match_the_restated_rule(seed):
+    """Seeded random batches (request counts, lengths with empty and one-token
+    requests, head shapes, page sizes, CTA counts and split modes): the
+    library's decode and prefill metadata equal the restated rule word for word."""
+    g = np.random.default_rng(100 + seed)
+    for _ in range(12):
+        B = int(g.choice([1, 2, 5, 33, 200]))
+        hkv = int(g.choice([1, 2, 4, 8, 12]))
+        hq = hkv * int(g.choice([1, 2, 4, 8]))
+        P = int(g.choice([16, 32, 64]))
+        kv = [int(x) for x in g.choice([0, 1, 15, 16, 17, 129, 1000, 5000], size=B)]
+        ctas = int(g.choice([1, 3, 37, 152, 400]))
+        kw = [{}, {"fixed_split_pages": int(g.integers(1, 40))}, {"disable_split_kv": True}][int(g.integers(0, 3))]
+        plan, ref, _ = _decode_plan(kv, hq=hq, hkv=hkv, num_ctas=ctas, page_size=P, **kw)
+        assert np.array_equal(plan.metadata(), ref), (B, hq, hkv, P, ctas, kw)
+        if hq // hkv <= 16:
+            qo = [int(g.integers(0, L + 1)) for L in kv]
+            plan, ref = _prefill_plan(kv, qo, hq=hq, hkv=hkv, num_ctas=ctas, page_size=P)
+            assert np.array_equal(plan.metadata(), ref), (B, hq, hkv, P, ctas, "prefill")
