@@ -169,136 +169,172 @@ void build_decode_meta(pafp8_plan* pl) {
     const int B = pl->desc.batch;
     const int nhb = pl->head_blocks;
     const int R = B * nhb;
-    std::vector<int64_t> np(R);
+    std::vector<int32_t> np((size_t)R);
+    std::vector<int32_t> empty;  // rows with no pages, ascending
+    int64_t T = 0;
     for (int b = 0; b < B; ++b)
-        for (int hb = 0; hb < nhb; ++hb)
-            np[(size_t)b * nhb + hb] = pl->vptr[b + 1] - pl->vptr[b];
+        for (int hb = 0; hb < nhb; ++hb) {
+            const int32_t n = pl->vptr[b + 1] - pl->vptr[b];
+            np[(size_t)b * nhb + hb] = n;
+            T += n;
+            if (n == 0) empty.push_back(b * nhb + hb);
+        }
 
+    // Segments in their final order, CTA after CTA (cta_ptr is the CSR).  A
+    // segment's slot is -1 while it covers its whole row (it writes the final
+    // output; zero-page rows too) and 0 for a part, numbered below.
     struct Seg { int32_t row, p0, p1, slot; };
-    std::vector<std::vector<Seg>> per_cta;
+    auto seg_of = [&](int32_t r, int64_t a, int64_t e) {
+        return Seg{r, (int32_t)a, (int32_t)e, (a == 0 && e == np[r]) ? -1 : 0};
+    };
+    std::vector<Seg> segs;
+    std::vector<int32_t> cta_ptr(1, 0);
     const int64_t target = pl->desc.num_ctas;
-
+    int64_t G = 0;
+    auto add_empties = [&](int64_t i, int64_t gt) {
+        for (size_t k = (size_t)i; k < empty.size(); k += (size_t)gt) segs.push_back({empty[k], 0, 0, -1});
+    };
     if (pl->desc.disable_split_kv || pl->desc.fixed_split_pages > 0) {
-        std::vector<Seg> segs;
+        std::vector<Seg> all;  // the chunks in row order, dealt round-robin
         for (int r = 0; r < R; ++r) {
-            if (np[r] == 0) continue;
             const int64_t c = pl->desc.disable_split_kv ? np[r] : pl->desc.fixed_split_pages;
             for (int64_t a = 0; a < np[r]; a += c)
-                segs.push_back({r, (int32_t)a, (int32_t)std::min<int64_t>(a + c, np[r]), 0});
+                all.push_back(seg_of(r, a, std::min<int64_t>(a + c, np[r])));
         }
-        const int64_t G = std::min<int64_t>(target, (int64_t)segs.size());
-        per_cta.assign((size_t)G, {});
-        for (size_t k = 0; k < segs.size(); ++k) per_cta[k % G].push_back(segs[k]);
+        G = std::min<int64_t>(target, (int64_t)all.size());
+        const int64_t gt = G > 0 ? G : (empty.empty() ? 0 : 1);
+        cta_ptr.reserve((size_t)gt + 1);
+        segs.reserve(all.size() + empty.size());
+        for (int64_t i = 0; i < gt; ++i) {
+            for (size_t k = (size_t)i; G > 0 && k < all.size(); k += (size_t)G) segs.push_back(all[k]);
+            add_empties(i, gt);
+            cta_ptr.push_back((int32_t)segs.size());
+        }
+        G = gt;
     } else {
-        int64_t T = 0;
-        for (int r = 0; r < R; ++r) T += np[r];
-        const int64_t G = std::min<int64_t>(target, T);
-        per_cta.assign((size_t)G, {});
-        std::vector<int64_t> row_start(R + 1, 0);
-        for (int r = 0; r < R; ++r) row_start[r + 1] = row_start[r] + np[r];
+        G = std::min<int64_t>(target, T);
+        const int64_t gt = G > 0 ? G : (empty.empty() ? 0 : 1);
+        cta_ptr.reserve((size_t)gt + 1);
+        segs.reserve((size_t)(G + R + empty.size()));
+        int64_t start = 0;  // first global page of row r
         int r = 0;
-        for (int64_t i = 0; i < G; ++i) {
-            const int64_t lo = i * T / G, hi = (i + 1) * T / G;
-            while (r < R && row_start[r + 1] <= lo) ++r;
-            for (int rr = r; rr < R && row_start[rr] < hi; ++rr) {
-                const int64_t a = std::max(lo, row_start[rr]) - row_start[rr];
-                const int64_t e = std::min(hi, row_start[rr + 1]) - row_start[rr];
-                if (e > a) per_cta[i].push_back({rr, (int32_t)a, (int32_t)e, 0});
+        // hi = floor((i + 1) T / G) kept as quotient and remainder, one step per CTA
+        const int64_t dq = G > 0 ? T / G : 0, dr = G > 0 ? T % G : 0;
+        int64_t hq = 0, hr = 0;
+        for (int64_t i = 0; i < gt; ++i) {
+            if (G > 0) {
+                const int64_t lo = hq;
+                hq += dq;
+                hr += dr;
+                if (hr >= G) {
+                    ++hq;
+                    hr -= G;
+                }
+                const int64_t hi = hq;
+                while (r < R && start + np[r] <= lo) start += np[r++];
+                int64_t rs = start;
+                for (int rr = r; rr < R && rs < hi; rs += np[rr++]) {
+                    const int64_t a = std::max(lo, rs) - rs;
+                    const int64_t e = std::min(hi, rs + np[rr]) - rs;
+                    if (e > a) segs.push_back(seg_of(rr, a, e));
+                }
             }
+            add_empties(i, gt);
+            cta_ptr.push_back((int32_t)segs.size());
         }
+        G = gt;
     }
-
-    // Rows with no pages: a zero-page segment each (it writes o = 0 and
-    // lse = -inf), the k-th one appended to CTA k mod G.
-    std::vector<int> empty;
-    for (int r = 0; r < R; ++r)
-        if (np[r] == 0) empty.push_back(r);
-    if (!empty.empty() && per_cta.empty()) per_cta.assign(1, {});
-    for (size_t k = 0; k < empty.size(); ++k)
-        per_cta[k % per_cta.size()].push_back({empty[k], 0, 0, 0});
 
     // Within a CTA, segments covering part of their row run first, so the
     // merges of split rows happen early rather than in the kernel's tail.
-    auto partial = [&](const Seg& sg) { return !(sg.p0 == 0 && sg.p1 == np[sg.row]); };
-    for (auto& v : per_cta) std::stable_partition(v.begin(), v.end(), partial);
-
-    // Output slots and the merge lists.  Partial states are numbered merge
-    // row by merge row (ascending), each row's by first page, so a row's
-    // slots are consecutive and the merge reads them without an index list.
-    std::vector<int> nseg_row(R, 0);
-    std::vector<std::vector<Seg*>> row_parts(R);
-    for (auto& v : per_cta)
-        for (auto& s : v) {
-            nseg_row[s.row]++;
-            if (!partial(s))
-                s.slot = -1;
-            else
-                row_parts[s.row].push_back(&s);
-        }
-    int32_t nslot = 0;
-    std::vector<int32_t> merge_rows, merge_ptr{0}, merge_slots, row_merge(R, -1);
-    for (int r = 0; r < R; ++r) {
-        if (nseg_row[r] >= 2) {
-            std::sort(row_parts[r].begin(), row_parts[r].end(),
-                      [](const Seg* a, const Seg* b) { return a->p0 < b->p0; });
-            row_merge[r] = (int32_t)merge_rows.size();
-            merge_rows.push_back(r);
-            for (Seg* sg : row_parts[r]) {
-                sg->slot = nslot;
-                merge_slots.push_back(nslot++);
-            }
-            merge_ptr.push_back((int32_t)merge_slots.size());
-        }
+    auto partial = [](const Seg& sg) { return sg.slot == 0; };
+    std::vector<Seg> tmp;
+    for (int64_t i = 0; i < G; ++i) {
+        Seg* a = segs.data() + cta_ptr[i];
+        Seg* e = segs.data() + cta_ptr[i + 1];
+        if (e - a < 2) continue;
+        tmp.clear();
+        for (Seg* x = a; x != e; ++x)
+            if (partial(*x)) tmp.push_back(*x);
+        for (Seg* x = a; x != e; ++x)
+            if (!partial(*x)) tmp.push_back(*x);
+        std::copy(tmp.begin(), tmp.end(), a);
     }
 
-    const int G = (int)per_cta.size();
-    int nseg = 0;
-    for (auto& v : per_cta) nseg += (int)v.size();
+    // Output slots and the merge lists.  A row cut into two or more segments
+    // has only partial ones; its partial states are numbered merge row by
+    // merge row (ascending), each row's by first page, so a row's slots are
+    // consecutive and the merge reads them without an index list.  Whole-row
+    // segments (and zero-page ones) write the final output (slot -1).
+    // Bucketed by row (a counting sort), then by first page within each row
+    // (insertion sort: a row's segments mostly arrive in page order already).
+    std::vector<int32_t> first((size_t)R + 1, 0);
+    for (const Seg& sg : segs)
+        if (partial(sg)) first[(size_t)sg.row + 1]++;
+    for (int r = 0; r < R; ++r) first[(size_t)r + 1] += first[r];
+    const int32_t nslot = first[R];
+    std::vector<int32_t> parts((size_t)nslot), fill(first.begin(), first.end() - 1);
+    for (size_t k = 0; k < segs.size(); ++k)
+        if (segs[k].slot == 0) parts[(size_t)fill[segs[k].row]++] = (int32_t)k;
+    for (int r = 0; r < R; ++r)
+        for (int32_t j = first[r] + 1; j < first[(size_t)r + 1]; ++j)
+            for (int32_t i = j; i > first[r] && segs[parts[i - 1]].p0 > segs[parts[i]].p0; --i)
+                std::swap(parts[i - 1], parts[i]);
+    std::vector<int32_t> merge_rows, merge_ptr(1, 0), row_merge((size_t)R, -1);
+    for (int32_t k = 0; k < nslot; ++k) {
+        Seg& sg = segs[parts[k]];
+        sg.slot = k;
+        if (k == 0 || segs[parts[k - 1]].row != sg.row) {
+            row_merge[sg.row] = (int32_t)merge_rows.size();
+            merge_rows.push_back(sg.row);
+        }
+        if (k + 1 == nslot || segs[parts[k + 1]].row != sg.row) merge_ptr.push_back(k + 1);
+    }
+    const int32_t nmerge = (int32_t)merge_rows.size();
+    const int32_t nseg = (int32_t)segs.size();
 
     std::vector<int32_t>& m = pl->meta;
     m.assign(kMetaHeaderWords, 0);
-    auto put = [&](int field, const std::vector<int32_t>& arr) {
-        m[field] = (int32_t)m.size();
-        m.insert(m.end(), arr.begin(), arr.end());
-    };
+    m.reserve((size_t)kMetaHeaderWords + 2 * (size_t)B + (size_t)G + 1 + 4 * (size_t)nseg + 2 * (size_t)nmerge + 1 +
+              (size_t)nslot + (size_t)R);
     m[kMetaMagic] = kMetaMagicValue;
     m[kMetaMode] = PAFP8_MODE_DECODE;
     m[kMetaBatch] = B;
     m[kMetaHeadBlocks] = nhb;
     m[kMetaHeadsPerCta] = pl->heads_per_cta;
     m[kMetaGroup] = pl->group;
-    m[kMetaNumCtas] = G;
+    m[kMetaNumCtas] = (int32_t)G;
     m[kMetaNumSegs] = nseg;
     m[kMetaNumPartials] = nslot;
-    m[kMetaNumMerge] = (int32_t)merge_rows.size();
-    std::vector<int32_t> req_page(B), req_kv(B);
+    m[kMetaNumMerge] = nmerge;
+    m[kMetaOffReqPage] = (int32_t)m.size();
+    for (int b = 0; b < B; ++b) m.push_back(pl->kv_indptr[b]);
+    m[kMetaOffReqKvLen] = (int32_t)m.size();
     for (int b = 0; b < B; ++b) {
-        req_page[b] = pl->kv_indptr[b];
         const int32_t n = pl->kv_indptr[b + 1] - pl->kv_indptr[b];
-        req_kv[b] = n > 0 ? (n - 1) * pl->desc.page_size + pl->last_page_len[b] : 0;
+        m.push_back(n > 0 ? (n - 1) * pl->desc.page_size + pl->last_page_len[b] : 0);
     }
-    put(kMetaOffReqPage, req_page);
-    put(kMetaOffReqKvLen, req_kv);
-    std::vector<int32_t> cta_ptr(G + 1, 0), seg;
-    for (int i = 0; i < G; ++i) {
-        cta_ptr[i + 1] = cta_ptr[i] + (int32_t)per_cta[i].size();
-        for (auto& s : per_cta[i]) {
-            seg.push_back(s.row);
-            seg.push_back(s.p0);
-            seg.push_back(s.p1);
-            seg.push_back(s.slot);
-        }
+    m[kMetaOffCtaSeg] = (int32_t)m.size();
+    m.insert(m.end(), cta_ptr.begin(), cta_ptr.end());
+    m[kMetaOffSeg] = (int32_t)m.size();
+    for (const Seg& sg : segs) {
+        m.push_back(sg.row);
+        m.push_back(sg.p0);
+        m.push_back(sg.p1);
+        m.push_back(sg.slot);
     }
-    put(kMetaOffCtaSeg, cta_ptr);
-    put(kMetaOffSeg, seg);
-    put(kMetaOffMergePtr, merge_ptr);
-    put(kMetaOffMergeRow, merge_rows);
-    put(kMetaOffMergeSlot, merge_slots);
-    put(kMetaOffRowMerge, row_merge);
+    m[kMetaOffMergePtr] = (int32_t)m.size();
+    m.insert(m.end(), merge_ptr.begin(), merge_ptr.end());
+    m[kMetaOffMergeRow] = (int32_t)m.size();
+    m.insert(m.end(), merge_rows.begin(), merge_rows.end());
+    m[kMetaOffMergeSlot] = (int32_t)m.size();
+    for (int32_t k = 0; k < nslot; ++k) m.push_back(k);
+    m[kMetaOffRowMerge] = (int32_t)m.size();
+    m.insert(m.end(), row_merge.begin(), row_merge.end());
 
-    pl->num_ctas = G;
+    pl->num_ctas = (int)G;
     pl->num_partials = nslot;
-    pl->num_merge = (int)merge_rows.size();
+    pl->num_merge = nmerge;
 }
 
 // Prefill work items: for every request b, KV head hk and block of 2 * TQ
@@ -393,8 +429,6 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
     return fn;
 }
 
-// 4-D map over one cache tensor [num_pages, P, Hkv, D] (bytes), dims listed
-// innermost first: (d, kv head, token slot, page).  One box is one KV head of
 // Byte strides of a cache tensor [num_pages, page_size, Hkv, D] (NHD) or
 // [num_pages, Hkv, page_size, D] (HND) with esz-byte elements.  Every TMA map
 // below names the same dimensions (dims, token, head, page) and only these
@@ -409,8 +443,12 @@ KvStrides kv_strides(int layout, int hkv, int esz, int head_dim = kHeadDim) {
     return KvStrides{(cuuint64_t)hkv * row, row, page};
 }
 
-// one page, 16 tokens x 128 bytes, landing in shared memory as [16][128] with
-// the 128-byte swizzle (16-byte chunk c of token row t stored at c ^ (t & 7)).
+// Map over an fp8 cache (bytes; the prefill's, and decode's when it takes one
+// box per head), dims listed innermost first: (d, kv head, token slot, page).
+// One box is one KV head of one page, 16 tokens x
+// head_dim bytes, landing in shared memory as [16][head_dim] with the 128-byte
+// swizzle (16-byte chunk c of token row t stored at c ^ (t & 7)), or the
+// 64-byte one for 64-byte rows.
 pafp8_status encode_cache_map(CUtensorMap* map, const void* base, int num_pages, int hkv, int layout,
                               int head_dim = kHeadDim) {
     auto enc = get_encode();
