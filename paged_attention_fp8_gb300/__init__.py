@@ -115,15 +115,22 @@ def lib() -> ctypes.CDLL:
     return L
 
 
+_OBJ_CODES = {}  # dtype objects seen before -> code (the run calls pass torch dtypes)
+
+
 def dtype_code(x) -> int:
     """int32 dtype code for a torch dtype, a name or a code."""
     if isinstance(x, int):
         return x
     if isinstance(x, str):
         return _NAME_CODES[x]
+    code = _OBJ_CODES.get(x)
+    if code is not None:
+        return code
     name = str(x).replace("torch.", "")
     if name not in _NAME_CODES:
         raise ValueError(f"no libpafp8 dtype code for {x}")
+    _OBJ_CODES[x] = _NAME_CODES[name]
     return _NAME_CODES[name]
 
 

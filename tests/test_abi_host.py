@@ -502,3 +502,17 @@ def test_random_plans_match_the_restated_rule(seed):
             qo = [int(g.integers(0, L + 1)) for L in kv]
             plan, ref = _prefill_plan(kv, qo, hq=hq, hkv=hkv, num_ctas=ctas, page_size=P)
             assert np.array_equal(plan.metadata(), ref), (B, hq, hkv, P, ctas, "prefill")
+
+
+def test_dtype_codes_of_torch_dtypes_names_and_codes():
+    import torch
+    pairs = [(torch.float16, pa.F16), (torch.bfloat16, pa.BF16), (torch.float8_e4m3fn, pa.E4M3FN),
+             (torch.float8_e5m2, pa.E5M2), (torch.float32, pa.F32), (torch.int8, pa.INT8),
+             (torch.uint8, pa.UINT8)]
+    for _ in range(2):  # the second round is served from the cache
+        for dt, code in pairs:
+            assert pa.dtype_code(dt) == code
+    assert pa.dtype_code("bf16") == pa.BF16 and pa.dtype_code("float8_e5m2") == pa.E5M2
+    assert pa.dtype_code(pa.E4M3FN) == pa.E4M3FN
+    with pytest.raises(ValueError):
+        pa.dtype_code(torch.float64)
