@@ -139,10 +139,14 @@ def _check(status: int) -> None:
         raise Pafp8Error(status, pafp8_last_error())
 
 
-def _i32_host(a) -> Optional[np.ndarray]:
+def _i32_host(a):
+    """A host int32 array: a contiguous CPU int32 tensor as it is (its
+    data_ptr is passed), anything else as a contiguous numpy int32 array."""
     if a is None:
         return None
     if hasattr(a, "cpu"):
+        if a.device.type == "cpu" and str(a.dtype) == "torch.int32" and a.is_contiguous():
+            return a
         a = a.cpu().numpy()
     return np.ascontiguousarray(a, dtype=np.int32)
 
