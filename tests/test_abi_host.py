@@ -516,3 +516,25 @@ def test_dtype_codes_of_torch_dtypes_names_and_codes():
     assert pa.dtype_code(pa.E4M3FN) == pa.E4M3FN
     with pytest.raises(ValueError):
         pa.dtype_code(torch.float64)
+
+
+def test_plan_takes_torch_and_numpy_page_tables_alike():
+    """CPU int32 tensors (passed by pointer), int64 or strided tensors and
+    numpy arrays give the same plan."""
+    import torch
+    kv = [37, 0, 700, 16, 4096]
+    npg = [(L + 15) // 16 for L in kv]
+    ind = np.concatenate([[0], np.cumsum(npg)]).astype(np.int32)
+    last = np.array([(L - (k - 1) * 16) if k else 0 for L, k in zip(kv, npg)], dtype=np.int32)
+    qo = np.array([0, 10, 10, 300, 316, 1000], dtype=np.int32)
+    for mode in ("decode", "prefill"):
+        ref = None
+        for conv in (np.asarray, torch.from_numpy, lambda a: torch.from_numpy(a).long(),
+                     lambda a: torch.from_numpy(np.repeat(a, 2))[::2]):
+            p = pa.Plan(mode=mode, num_qo_heads=32, num_kv_heads=8, num_pages=int(ind[-1]), kv_indptr=conv(ind),
+                        last_page_len=conv(last), qo_indptr=conv(qo) if mode == "prefill" else None,
+                        q_dtype="bf16", kv_dtype="e4m3fn", num_ctas=37)
+            got = p.metadata()
+            if ref is None:
+                ref = got
+            assert np.array_equal(got, ref)
