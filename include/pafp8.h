@@ -156,7 +156,11 @@ const char *pafp8_last_error(void);
  *                   rows qo_indptr_h[b] .. qo_indptr_h[b+1]-1, with
  *                   qo_len <= kv_len); NULL for decode (row b is request b).
  * The arrays are copied; the caller may free them after the call.  On
- * success *out owns a plan freed by pafp8_plan_destroy. */
+ * success *out owns a plan freed by pafp8_plan_destroy.  Planning runs on the
+ * calling host thread in time linear in batch, num_ctas and the number of
+ * segments (a decode plan for 64 requests on 152 CTAs takes a few
+ * microseconds), touches no device memory and, with num_ctas given, makes no
+ * CUDA call. */
 pafp8_status pafp8_plan_create(const pafp8_plan_desc *desc, const int32_t *kv_indptr_h,
                                const int32_t *last_page_len_h, const int32_t *qo_indptr_h,
                                pafp8_plan **out);
