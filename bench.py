@@ -22,8 +22,14 @@ steps, outside the CUDA events that time each step on the launching stream
 (a read rather than a write, so no dirty lines are written back during the
 next step).
 Under torchrun every rank runs the same workload on its own GPU (replicas, no
-collective on the data path) and rank 0 prints one JSON line with the max
-time over ranks.
+collective on the data path) and rank 0 prints the max time over ranks.
+
+Output (rank 0): one JSON line with the full record of every timed part
+(the other decode and prefill workloads, the 2-byte caches, the KV append,
+POD), then the headline JSON line, last and compact: the serving decode
+step, its roofline, the end-to-end figure with its breakdown, the clocks, a
+roofline entry for each of the five named workloads ("configs") and the CPU
+oracle baseline.
 
 --impl reference times the CPU oracle (fp64, all host cores) on a bounded
 sample of the same workload, as the reference arm.
@@ -56,11 +62,10 @@ L2_FLUSH_BYTES = 256 << 20
 # workload, from one ncu capture of the kernel source with this SHA-256; a
 # changed kernel reports null until it is captured again.
 NCU_TRAFFIC = {
-    # profiles/decode_kernel_serving_decode.md
     "c3b0454dffeb97e1dcccd875dea46b8412816eb18e85fea91d3301223f5c2991": 309770496,
 }
 # The same for the prefill kernel, per workload index, keyed by the SHA-256
-# of its source (profiles/prefill_kernel_ragged_bf16_and_fp8.md).
+# of its source.
 NCU_TRAFFIC_PREFILL = {
     "71798cc65a65dc09a7b0caf08f142f626eced7ef1de920df37eb290c05f9830f": {4: 170110720, 5: 191745024},
 }
@@ -194,21 +199,23 @@ def time_prefill(index, dev, steps, warmup):
     return out
 
 
-def time_decode_2byte(dev, steps, warmup):
-    """Device time of one decode step (decode + merge kernels) on the serving
-    workload's shape with a bf16 cache; GB/s over its algorithmic bytes (KV at
-    2 bytes per element)."""
+def time_decode(index, dev, steps, warmup):
+    """Device time of one decode step (the decode kernel and its split-KV
+    merge, one pafp8_run) on named workload `index`, L2 evicted before each
+    step, plus the decode kernel alone (stage 1, a second loop); GB/s over
+    the algorithmic bytes (KV at its element size, q, o, lse, page ids)."""
     import torch
 
     import paged_attention_fp8_gb300 as pa
     from paged_attention_fp8_gb300.workloads import TORCH_DTYPES, WORKLOADS, workload
 
-    b = workload(6)
+    b = workload(index)
     nbytes = decode_bytes(b)
     q, k, v, idx = b.q.to(dev), b.k_cache.to(dev), b.v_cache.to(dev), b.kv_indices.to(dev)
     plan = pa.Plan(mode="decode", num_qo_heads=b.num_qo_heads, num_kv_heads=b.num_kv_heads,
                    num_pages=b.num_pages, kv_indptr=b.kv_indptr, last_page_len=b.last_page_len,
                    q_dtype=b.q_dtype, kv_dtype=b.kv_dtype, o_dtype=b.o_dtype, sm_scale=b.sm_scale)
+    meta = plan.metadata()
     ws = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device=dev)
     plan.upload(ws)
     o = torch.empty(b.nnz_qo, b.num_qo_heads, b.head_dim, dtype=TORCH_DTYPES[b.o_dtype], device=dev)
@@ -216,28 +223,35 @@ def time_decode_2byte(dev, steps, warmup):
     flush = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     kw = dict(q_scale=b.q_scale, k_scale=b.k_scale, v_scale=b.v_scale)
     stream = torch.cuda.current_stream()
-    for _ in range(warmup):
-        flush.sum()
-        plan.run(q, k, v, idx, o, lse, ws, **kw)
-    torch.cuda.synchronize()
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
-    for i in range(steps):
-        flush.sum()
-        ev[i][0].record(stream)
-        plan.run(q, k, v, idx, o, lse, ws, **kw)
-        ev[i][1].record(stream)
-    torch.cuda.synchronize()
-    plan.device_status(ws)
-    ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+
+    def loop(stage):
+        for _ in range(warmup):
+            flush.sum()
+            plan.run_stage(stage, q, k, v, idx, o, lse, ws, **kw)
+        torch.cuda.synchronize()
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+        for i in range(steps):
+            flush.sum()
+            ev[i][0].record(stream)
+            plan.run_stage(stage, q, k, v, idx, o, lse, ws, **kw)
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        plan.device_status(ws)
+        return statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+
+    ms = loop(0)
+    ms_dec = loop(1)
     gbs = nbytes / (ms * 1e-3) / 1e9
     peak, kind = measured_peaks()
     del q, k, v, idx, o, lse, ws, flush
     torch.cuda.empty_cache()
-    return {"workload": WORKLOADS[6], "value": round(gbs, 1), "unit": "GB/s", "ms_per_step": round(ms, 5),
-            "bytes_per_step": nbytes, "steps": steps,
+    return {"workload": WORKLOADS[index], "value": round(gbs, 1), "unit": "GB/s", "ms_per_step": round(ms, 5),
+            "bytes_per_step": nbytes, "steps": steps, "num_ctas": int(meta[6]), "merge_rows": int(meta[9]),
+            "decode_kernel_ms": round(ms_dec, 5),
             "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(gbs / peak, 4), "peak_kind": kind,
-                         "note": "whole step (decode + merge kernels)"}}
+                         "kernel_frac": round(nbytes / (ms_dec * 1e-3) / 1e9 / peak, 4),
+                         "note": "whole step (decode + merge kernels); kernel_frac: the decode kernel alone"}}
 
 
 def append_bytes(a) -> int:
@@ -315,11 +329,15 @@ def kernel_sha(name: str) -> str:
 
 
 class ClockSampler:
-    """nvidia-smi samples of SM clock and throttle reasons while running."""
+    """nvidia-smi samples of SM clock and throttle reasons while running.
+    The summary covers the samples taken under load (the GPU-idle reason not
+    active); idle stretches (host work between the timed parts) drop the SM
+    clock and say nothing about the timed kernels."""
 
     FIELDS = ["index", "clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
               "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
-              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap",
+              "clocks_event_reasons.gpu_idle"]
 
     def __init__(self, gpu_id: str):
         self.proc = None
@@ -345,21 +363,33 @@ class ClockSampler:
         rows = [r for r in csv.reader(io.StringIO(self.file.read())) if len(r) == len(self.FIELDS)]
         self.file.close()
         os.unlink(self.file.name)
-        sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for r in rows:
-            try:
-                sm.append(float(r[1]))
-                mx.append(float(r[2]))
-            except ValueError:
-                continue
-            for n, v in zip(names, r[5:9]):
-                if v.strip().lower() == "active":
-                    reasons.add(n)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+        return summarize_clocks(rows)
+
+
+def summarize_clocks(rows):
+    """Median SM clock, max clock and the throttle reasons seen, over the
+    samples taken under load (rows of ClockSampler.FIELDS)."""
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    sm, mx, reasons, total = [], [], set(), 0
+    for r in rows:
+        if len(r) != len(ClockSampler.FIELDS):
+            continue
+        try:
+            clk, cmax = float(r[1]), float(r[2])
+        except ValueError:
+            continue
+        total += 1
+        if r[9].strip().lower() == "active":  # idle GPU: not a timed stretch
+            continue
+        sm.append(clk)
+        mx.append(cmax)
+        for n, v in zip(names, r[5:9]):
+            if v.strip().lower() == "active":
+                reasons.add(n)
+    if not sm:
+        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "samples_total": total}
+    return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+            "samples": len(sm), "samples_total": total}
 
 
 def gpu_id_for(torch, dev) -> str:
@@ -404,6 +434,89 @@ def oracle_sample_size(b, budget_s: float) -> int:
     dt, by, _ = oracle_decode_sample(b, 1)
     per_req = max(dt, 1e-4)
     return max(1, min(b.batch, int(budget_s / per_req)))
+
+
+def oracle_prefill_sample(b, nrows: int):
+    """Run the oracle on the last nrows new query rows of request 0 (every
+    query head; the rows with the most admitted keys); returns (seconds, FLOPs
+    over the admitted causal pairs, threads used)."""
+    import numpy as np
+
+    import oracle
+    from paged_attention_fp8_gb300.workloads import raw_numpy
+
+    qo, kv = b.qo_lens[0], b.kv_lens[0]
+    nrows = max(1, min(nrows, qo))
+    first = qo - nrows
+    rows = np.repeat(np.arange(first, qo), b.num_qo_heads)
+    heads = np.tile(np.arange(b.num_qo_heads), nrows)
+    raw = getattr(b, "_raw_cache", None)
+    if raw is None:
+        raw = dict(q=raw_numpy(b.q), k=raw_numpy(b.k_cache), v=raw_numpy(b.v_cache))
+        b._raw_cache = raw
+    t0 = time.perf_counter()
+    oracle.paged_attention(q=raw["q"], q_dtype=b.q_dtype, k_cache=raw["k"], v_cache=raw["v"],
+                           kv_dtype=b.kv_dtype, qo_indptr=b.qo_indptr.numpy(),
+                           kv_indptr=b.kv_indptr.numpy(), kv_indices=b.kv_indices.numpy(),
+                           last_page_len=b.last_page_len.numpy(), num_qo_heads=b.num_qo_heads,
+                           num_kv_heads=b.num_kv_heads, q_scale=b.q_scale, k_scale=b.k_scale,
+                           v_scale=b.v_scale, sm_scale=b.sm_scale, causal=True, rows=rows,
+                           heads=heads)
+    dt = time.perf_counter() - t0
+    keys = sum(kv - qo + i + 1 for i in range(first, qo))  # admitted keys of the sampled rows
+    return dt, 4 * b.head_dim * b.num_qo_heads * keys, oracle.num_threads()
+
+
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.split(":")[0].strip() in ("Model name", "Model"):
+                v = line.split(":", 1)[1].strip()
+                if v and not v.isdigit():
+                    return v
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu model")):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.machine()
+
+
+def cpu_baseline(b_decode, b_prefill, budget_s: float = 6.0):
+    """The oracle timed on this host's cores: the serving decode sample on
+    every core and on one, and a prefill sample on every core.  Each sample
+    is sized to about budget_s."""
+    import oracle
+
+    cores = oracle.num_threads()
+    n = oracle_sample_size(b_decode, budget_s)
+    dt, by, _ = oracle_decode_sample(b_decode, n)
+    oracle.set_num_threads(1)
+    try:
+        n1 = max(1, min(n, int(budget_s / max(dt / n * cores, 1e-4))))
+        dt1, by1, _ = oracle_decode_sample(b_decode, n1)
+        rows1 = 8
+        tp, fp, _ = oracle_prefill_sample(b_prefill, rows1)
+    finally:
+        oracle.set_num_threads(cores)
+    rows = max(8, min(b_prefill.qo_lens[0], int(rows1 * budget_s / max(tp / cores, 1e-4))))
+    tpa, fpa, _ = oracle_prefill_sample(b_prefill, rows)
+    return {"value": round(by / dt / 1e9, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"serving decode: first {n} of {b_decode.batch} requests, every query head ({dt:.2f} s, fp64)",
+            "value_1_thread": round(by1 / dt1 / 1e9, 4),
+            "sample_1_thread": f"first {n1} requests ({dt1:.2f} s)",
+            "prefill_tflops": round(fpa / tpa / 1e12, 5),
+            "prefill_tflops_1_thread": round(fp / tp / 1e12, 6),
+            "prefill_sample": f"ragged prefill: last {rows} (1 thread: {rows1}) rows of request 0, every query head "
+                              f"({tpa:.2f} s / {tp:.2f} s)",
+            "cpu": cpu_model()}
 
 
 def run_reference(args):
@@ -548,6 +661,8 @@ def run_ours(args):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     pbuild.build()
+    # nvidia-smi samples from here to the end of the run (every timed part).
+    sampler = ClockSampler(gpu_id_for(torch, dev)) if rank == 0 and args.mode in ("all", "decode") else None
 
     if args.mode == "prefill":
         res = {str(i): time_prefill(i, dev, args.prefill_steps, max(3, args.warmup)) for i in (4, 5)}
@@ -607,7 +722,6 @@ def run_ours(args):
 
     launches_per_step = (1 if num_ctas > 0 else 0) + (1 if num_merge > 0 else 0)
     events = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
-    sampler = ClockSampler(gpu_id_for(torch, dev)) if rank == 0 else None
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
@@ -619,7 +733,6 @@ def run_ours(args):
     if world > 1:
         dist.barrier()
     wall = time.perf_counter() - t0
-    clocks = sampler.stop() if sampler else None
     plan.device_status(ws)
     step_ms = [e[0].elapsed_time(e[1]) for e in events]
     ms_step = statistics.mean(step_ms)
@@ -635,27 +748,41 @@ def run_ours(args):
     ms_dec = statistics.mean(dec_ms)
     ms_step, ms_dec = max_over_ranks([ms_step, ms_dec], dev, world)
 
-    # ---- end to end through the public API: re-plan, H2D inputs from pinned
-    # host memory, run, D2H of the result, every step.
-    q_h = b.q.pin_memory()
-    idx_h = b.kv_indices.pin_memory()
-    o_h = torch.empty(o.shape, dtype=o.dtype).pin_memory()
-    lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
-    indptr_h, last_h = b.kv_indptr.numpy(), b.last_page_len.numpy()
-    h2d = q_h.numel() * q_h.element_size() + idx_h.numel() * 4 + int(meta.size) * 4
-    d2h = o_h.numel() * o_h.element_size() + lse_h.numel() * 4
+    # ---- end to end through the public API, every step: re-plan on the host,
+    # upload the plan, one H2D copy of the step's inputs (q and kv_indices
+    # packed in one pinned buffer), run, one D2H copy of the result (o and lse
+    # packed in one device buffer) and a synchronize.  The KV cache stays
+    # resident in HBM: it is the state a decode step reads, not an input.
+    qb = q.numel() * q.element_size()
+    ib = idx.numel() * 4
+    in_h = torch.empty(qb + ib, dtype=torch.uint8).pin_memory()
+    in_h[:qb].copy_(b.q.contiguous().view(-1).view(torch.uint8))
+    in_h[qb:].copy_(b.kv_indices.view(torch.uint8))
+    in_d = torch.empty(qb + ib, dtype=torch.uint8, device=dev)
+    q_e = in_d[:qb].view(q.dtype).view(q.shape)
+    idx_e = in_d[qb:].view(torch.int32)
+    ob = o.numel() * o.element_size()
+    lb = lse.numel() * 4
+    out_d = torch.empty(ob + lb, dtype=torch.uint8, device=dev)
+    o_e = out_d[:ob].view(o.dtype).view(o.shape)
+    lse_e = out_d[ob:].view(torch.float32).view(lse.shape)
+    out_h = torch.empty(ob + lb, dtype=torch.uint8).pin_memory()
+    indptr_h, last_h = b.kv_indptr, b.last_page_len
+    h2d = qb + ib + int(meta.size) * 4
+    d2h = ob + lb
     e2e_steps = max(1, min(args.e2e_steps, args.steps))
 
+    def new_plan():
+        return pa.Plan(mode="decode", num_qo_heads=b.num_qo_heads, num_kv_heads=b.num_kv_heads,
+                       num_pages=b.num_pages, kv_indptr=indptr_h, last_page_len=last_h,
+                       q_dtype=b.q_dtype, kv_dtype=b.kv_dtype, o_dtype=b.o_dtype, sm_scale=b.sm_scale)
+
     def e2e_step():
-        p2 = pa.Plan(mode="decode", num_qo_heads=b.num_qo_heads, num_kv_heads=b.num_kv_heads,
-                     num_pages=b.num_pages, kv_indptr=indptr_h, last_page_len=last_h,
-                     q_dtype=b.q_dtype, kv_dtype=b.kv_dtype, o_dtype=b.o_dtype, sm_scale=b.sm_scale)
+        p2 = new_plan()
         p2.upload(ws)
-        q.copy_(q_h, non_blocking=True)
-        idx.copy_(idx_h, non_blocking=True)
-        p2.run(q, k, v, idx, o, lse, ws, **scales)
-        o_h.copy_(o, non_blocking=True)
-        lse_h.copy_(lse, non_blocking=True)
+        in_d.copy_(in_h, non_blocking=True)
+        p2.run(q_e, k, v, idx_e, o_e, lse_e, ws, **scales)
+        out_h.copy_(out_d, non_blocking=True)
         torch.cuda.synchronize()
         return p2
 
@@ -671,66 +798,108 @@ def run_ours(args):
     e2e_s = (time.perf_counter() - t1) / e2e_steps
     last_plan.device_status(ws)
     e2e_s, = max_over_ranks([e2e_s], dev, world)
+    # Where an end-to-end step's time goes: the same calls, each followed by
+    # a synchronize and timed on the host (medians over the e2e steps).
+    parts = {"plan": [], "upload": [], "h2d": [], "run": [], "d2h": []}
+    for _ in range(e2e_steps):
+        t = time.perf_counter()
+        p2 = new_plan()
+        parts["plan"].append(time.perf_counter() - t)
+        t = time.perf_counter()
+        p2.upload(ws)
+        torch.cuda.synchronize()
+        parts["upload"].append(time.perf_counter() - t)
+        t = time.perf_counter()
+        in_d.copy_(in_h, non_blocking=True)
+        torch.cuda.synchronize()
+        parts["h2d"].append(time.perf_counter() - t)
+        t = time.perf_counter()
+        p2.run(q_e, k, v, idx_e, o_e, lse_e, ws, **scales)
+        torch.cuda.synchronize()
+        parts["run"].append(time.perf_counter() - t)
+        t = time.perf_counter()
+        out_h.copy_(out_d, non_blocking=True)
+        torch.cuda.synchronize()
+        parts["d2h"].append(time.perf_counter() - t)
+    breakdown = {k2: round(statistics.median(v2) * 1e6, 1) for k2, v2 in parts.items()}
+    del flush, in_d, out_d
+    torch.cuda.empty_cache()
 
-    prefill_res = {}
+    detail = {}
     if args.mode == "all":
-        del flush
-        torch.cuda.empty_cache()
+        w = max(3, min(args.warmup, 20))
+        dsteps = min(max(args.steps, 20), 200)
+        for i in (1, 3, 6):
+            detail[i] = time_decode(i, dev, dsteps, w)
         for i in (4, 5, 7):
-            prefill_res[i] = time_prefill(i, dev, args.prefill_steps, max(3, min(args.warmup, 10)))
-        decode16 = time_decode_2byte(dev, min(args.steps, 200), max(3, min(args.warmup, 20)))
-        append_res = {i: time_append(i, dev, min(args.steps, 200), max(3, min(args.warmup, 20)))
-                      for i in (8, 9)}
+            detail[i] = time_prefill(i, dev, args.prefill_steps, max(3, min(args.warmup, 10)))
+        append_res = {i: time_append(i, dev, min(args.steps, 200), w) for i in (8, 9)}
         pod_res = time_pod(dev, args.prefill_steps, max(3, min(args.warmup, 10)))
 
     if rank != 0:
         dist.destroy_process_group()
         return
+    clocks = sampler.stop() if sampler else None
 
     peak, peak_kind = measured_peaks()
     achieved = nbytes / (ms_dec * 1e-3) / 1e9
-    sha = kernel_sha("decode.cu")
-    traffic = NCU_TRAFFIC.get(sha)
+    traffic = NCU_TRAFFIC.get(kernel_sha("decode.cu"))
     value = world * nbytes / (ms_step * 1e-3) / 1e9
+    step_roof = {"bound": "hbm", "achieved": round(nbytes / (ms_step * 1e-3) / 1e9, 1), "peak": peak,
+                 "unit": "GB/s", "frac": round(nbytes / (ms_step * 1e-3) / 1e9 / peak, 4)}
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(b, workload(4))
+
+    def brief(d):
+        r = d["roofline"]
+        out = {"us": round(1e3 * d.get("ms_per_step", d.get("ms_per_launch", 0.0)), 2), "value": d["value"],
+               "unit": d["unit"],
+               "roofline": {"bound": r["bound"], "achieved": r["achieved"], "peak": r["peak"], "unit": r["unit"],
+                            "frac": r["frac"], "traffic": r.get("traffic")}}
+        if "kernel_frac" in r:
+            out["roofline"]["kernel_frac"] = r["kernel_frac"]
+        if "frac_of_dense_bf16" in r:
+            out["roofline"]["frac_of_dense_bf16"] = r["frac_of_dense_bf16"]
+        return out
+
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": f"{b.kv_dtype} KV -> f16 MMA, f32 accumulate ({b.q_dtype} q, {b.o_dtype} o)",
         "data": "synthetic",
-        "config": {"workload": WORKLOADS[2], "batch": b.batch, "num_qo_heads": b.num_qo_heads,
-                   "num_kv_heads": b.num_kv_heads, "head_dim": b.head_dim, "page_size": b.page_size,
-                   "kv_tokens": sum(b.kv_lens), "bytes_per_step": nbytes,
-                   "parallelism": f"replicas{world}", "num_ctas": num_ctas, "merge_rows": num_merge,
-                   "l2": "evicted between timed steps by reading a 256 MiB buffer outside the events "
-                         "(a write would leave dirty lines whose write-back lands in the next step); "
-                         "KV 303 MB > L2",
+        "config": {"workload": WORKLOADS[2], "bytes_per_step": nbytes, "parallelism": f"replicas{world}",
+                   "l2": "evicted between timed steps by a 256 MiB read outside the events; KV 303 MB > L2",
                    "timed_region_s": round(wall, 4)},
         "roofline": {"bound": "hbm", "kernel": "decode_kernel", "achieved": round(achieved, 1),
                      "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "peak_kind": peak_kind, "traffic": traffic,
-                     "algorithmic_bytes": nbytes, "ms_per_launch": round(ms_dec, 5)},
+                     "peak_kind": peak_kind, "traffic": traffic, "step_frac": step_roof["frac"]},
         "e2e": {"value": round(world * nbytes / e2e_s / 1e9, 2), "unit": "GB/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": round(e2e_s * 1e3, 4),
-                "includes": "host plan + metadata upload + H2D q/kv_indices + run + D2H o/lse; "
-                            "KV cache resident in HBM"},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_s * 1e3, 4),
+                "breakdown_us": breakdown},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
     }
     if args.mode == "all":
-        line["prefill"] = {"ragged_bf16": prefill_res[4], "fp8_fp8": prefill_res[5],
-                           "ragged_bf16_cache": prefill_res[7]}
-        line["decode_2byte_cache"] = decode16
-        line["append_kv"] = {"prefill_tokens": append_res[8], "decode_step": append_res[9]}
-        line["pod"] = pod_res
-    if world == 1 and not args.no_cpu_baseline:
-        n = oracle_sample_size(b, 15.0)
-        dt, by, cores = oracle_decode_sample(b, n)
-        line["cpu_baseline"] = {"value": round(by / dt / 1e9, 4), "unit": "GB/s", "cores": cores,
-                                "kind": "oracle",
-                                "sample": f"first {n} of {b.batch} requests, every query head "
-                                          f"({dt:.2f} s, fp64)"}
+        line["configs"] = {
+            "1_tiny_decode": brief(detail[1]),
+            "2_serving_decode": {"us": round(ms_step * 1e3, 2), "value": round(value / world, 1), "unit": "GB/s",
+                                 "roofline": dict(step_roof, traffic=traffic,
+                                                  kernel_frac=round(achieved / peak, 4))},
+            "3_long_context_decode": brief(detail[3]),
+            "4_ragged_prefill": brief(detail[4]),
+            "5_fp8_prefill": brief(detail[5]),
+        }
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
+    # The full records first (one JSON line), the headline line last.
+    if args.mode == "all":
+        full = {"detail": True, "decode": {str(i): detail[i] for i in (1, 3, 6)},
+                "prefill": {str(i): detail[i] for i in (4, 5, 7)},
+                "append_kv": {"prefill_tokens": append_res[8], "decode_step": append_res[9]},
+                "pod": pod_res}
+        print(json.dumps(full), flush=True)
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()

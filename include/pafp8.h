@@ -33,6 +33,13 @@
  *     it (PAFP8_ERR_BOUNDS, PAFP8_ERR_TIMEOUT), so a bad page index or an
  *     expired wait surfaces at the call that caused it.  Not for use under
  *     stream capture.
+ *   - Every wait inside a kernel is bounded (about one second of SM clock).
+ *     On expiry the kernel records PAFP8_ERR_TIMEOUT in the workspace status
+ *     word, lets its own copies and MMAs in flight finish, frees its tensor
+ *     memory and returns; the workspace and context stay usable.  The
+ *     diagnostic setting PAFP8_WAIT_CYCLES (a positive integer, in SM clock
+ *     cycles, read by each launching call) shortens the bound of the
+ *     pipeline waits, so that a test can make one expire on purpose.
  */
 #ifndef PAFP8_H
 #define PAFP8_H
@@ -273,13 +280,16 @@ pafp8_status pafp8_device_status(const pafp8_plan *plan, void *workspace, void *
  * (fewer CTAs or splits shrink it).  The first call on a device looks up the
  * scratch's device address (cudaGetSymbolAddress) with that device current,
  * so make it before any stream capture.  No call allocates or frees device
- * memory.  Every call re-loads its plan's metadata into the scratch and
- * clears the status word, so a call never depends on the previous call's
- * contents; but all calls share the one array, so calls that can overlap on
- * the GPU (different streams, or different threads without ordering) race
- * and must be serialized by the caller.  The status word is internal here:
- * page-index and timeout reports are available only through pafp8_run with a
- * workspace. */
+ * memory.  Every call re-loads its plan's metadata into the scratch (a
+ * cudaMemcpyAsync on `stream` whose source is the plan's own host memory,
+ * which is ordinary pageable memory) and clears the status word (a
+ * cudaMemsetAsync on `stream`), so a call never depends on the previous
+ * call's contents; but all calls share the one array, so calls that can
+ * overlap on the GPU (different streams, or different threads without
+ * ordering) race and must be serialized by the caller.  Page-index and
+ * timeout reports: with PAFP8_DEBUG set (see pafp8_run) the call synchronizes
+ * and returns the kernels' status (PAFP8_ERR_BOUNDS, PAFP8_ERR_TIMEOUT);
+ * otherwise the status word stays internal. */
 #define PAFP8_NOALLOC_SCRATCH_BYTES (16u << 20)
 pafp8_status pafp8_run_decode_noalloc(const pafp8_plan *plan, int32_t q_dtype, const void *q,
                                       int32_t k_dtype, const void *k_cache, int32_t v_dtype,

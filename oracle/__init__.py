@@ -59,6 +59,8 @@ def _load():
         lib.orc_decode_array.restype = i32
         lib.orc_num_threads.argtypes = []
         lib.orc_num_threads.restype = i32
+        lib.orc_set_num_threads.argtypes = [i32]
+        lib.orc_set_num_threads.restype = i32
         lib.orc_paged_attention.argtypes = (
             [i64] * 6 + [vp] * 4 + [i32, vp, dbl, i32, vp, vp, dbl, dbl, dbl, i32, i32, vp, vp, vp, i64, vp, vp,
                                      vp, vp])
@@ -95,6 +97,12 @@ def _raw(a, dtype: str) -> np.ndarray:
 def num_threads() -> int:
     """Threads the oracle's OpenMP loop uses (1 when built without OpenMP)."""
     return int(_load().orc_num_threads())
+
+
+def set_num_threads(n: int) -> int:
+    """Threads for later oracle calls (every host core by default); returns
+    the count in effect (1 when built without OpenMP)."""
+    return int(_load().orc_set_num_threads(int(n)))
 
 
 def decode(dtype: str, raw) -> np.ndarray:

@@ -246,6 +246,17 @@ int orc_num_threads(void) {
 #endif
 }
 
+/* Threads of the OpenMP loop for later calls (the benchmark times the oracle
+ * on every host core and on one); returns the count now in effect. */
+int orc_set_num_threads(int n) {
+#ifdef _OPENMP
+    if (n > 0) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+    return orc_num_threads();
+}
+
 /* ---- 2..6. paged attention ------------------------------------------------
  *
  * Layouts (all row-major, contiguous):

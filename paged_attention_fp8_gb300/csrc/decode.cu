@@ -171,7 +171,7 @@ __device__ __forceinline__ float load_q(uint32_t (&qf)[16], uint32_t (&qlo)[16],
     return factor;
 }
 
-template <int KT, int DH>
+template <int KT, int DH, bool kDiag>
 __global__ void __launch_bounds__(32 * 9, 1)
     decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtensorMap tmk,
                   const __grid_constant__ CUtensorMap tmv, int hpc, int group, int stages,
@@ -230,7 +230,7 @@ __global__ void __launch_bounds__(32 * 9, 1)
                 for (int j = 0; j < n; ++j) {
                     const int pg = __shfl_sync(0xFFFFFFFFu, page, j);
                     if (lane == 0) {
-                        if (!mbar_wait(bar_empty + 8u * stage, phase ^ 1u)) {
+                        if (!pipe_wait<kDiag>(bar_empty + 8u * stage, phase ^ 1u, p.wait_cycles)) {
                             ok = false;
                         } else {
                             const uint32_t fb = bar_full + 8u * stage;
@@ -343,7 +343,7 @@ __global__ void __launch_bounds__(32 * 9, 1)
         for (int pg = p0; pg < p1; ++pg) {
             // mma.sync and movmatrix below are warp-collective: the warp
             // leaves together if any lane's wait gave up.
-            if (!__all_sync(0xFFFFFFFFu, mbar_wait(bar_full + 8u * stage, phase))) {
+            if (!__all_sync(0xFFFFFFFFu, pipe_wait<kDiag>(bar_full + 8u * stage, phase, p.wait_cycles))) {
                 ok = false;
                 break;
             }
@@ -675,10 +675,12 @@ cudaError_t launch_decode_t(const DecodeParams& p, const CUtensorMap& tmap_k, co
     if (stages < 2) stages = 2;
     const size_t smem = 1024 + (size_t)stages * stage_bytes + 16 * (size_t)stages;
     const dim3 grid(num_ctas), block(32 * (hpc + 1));
-    cudaError_t e =
-        cudaFuncSetAttribute(decode_kernel<KT, DH>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    // The diagnostic instantiation runs only under a shortened wait bound.
+    const bool diag = p.wait_cycles < kWaitCyclesDefault;
+    auto kern = diag ? decode_kernel<KT, DH, true> : decode_kernel<KT, DH, false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    decode_kernel<KT, DH><<<grid, block, smem, stream>>>(p, tmap_k, tmap_v, hpc, group, stages, heads_per_box);
+    kern<<<grid, block, smem, stream>>>(p, tmap_k, tmap_v, hpc, group, stages, heads_per_box);
     return cudaGetLastError();
 }
 

@@ -601,6 +601,19 @@ pafp8_status encode_decode_maps(CUtensorMap* tk, CUtensorMap* tv, const void* k,
 
 bool scale_ok(float s) { return std::isfinite(s) && s > 0.0f; }
 
+// Bound of the kernels' pipeline waits: PAFP8_WAIT_CYCLES (a positive integer,
+// SM clock cycles) when set, else about one second.  A diagnostic setting: a
+// short bound makes a pipeline wait expire on purpose, which the kernels
+// report as PAFP8_ERR_TIMEOUT after winding down; their final waits for their
+// own copies in flight keep the long bound.
+long long wait_cycles() {
+    const char* v = std::getenv("PAFP8_WAIT_CYCLES");
+    if (v == nullptr || v[0] == '\0') return kWaitCyclesDefault;
+    char* end = nullptr;
+    const long long n = std::strtoll(v, &end, 10);
+    return (end != v && *end == '\0' && n > 0) ? n : kWaitCyclesDefault;
+}
+
 }  // namespace
 
 extern "C" {
@@ -877,6 +890,7 @@ pafp8_status run_body(const pafp8_plan* plan, int32_t stage, int32_t q_dtype, co
         pp.k_scales = k_scales;
         pp.v_scales = k_scales != nullptr ? v_scales : nullptr;
         pp.sm_scale = d.sm_scale;
+        pp.wait_cycles = wait_cycles();
         CUtensorMap tq, tk, tv;
         if ((st = encode_q_map(&tq, q, (int)plan->nnz_qo, d.num_qo_heads, plan->group,
                                pp.tile_tokens, is_fp8(q_dtype))) != PAFP8_OK)
@@ -924,6 +938,7 @@ pafp8_status run_body(const pafp8_plan* plan, int32_t stage, int32_t q_dtype, co
     p.k_scales = k_scales;
     p.v_scales = k_scales != nullptr ? v_scales : nullptr;
     p.sm_scale = d.sm_scale;
+    p.wait_cycles = wait_cycles();
 
     cudaError_t e = cudaSuccess;
     if (stage != 2 && plan->num_ctas > 0) {
@@ -1107,6 +1122,7 @@ pafp8_status pafp8_run_decode_noalloc(const pafp8_plan* plan, int32_t q_dtype, c
     p.sm_scale_log2 = (float)((double)d.sm_scale * (is_fp8(q_dtype) ? (double)q_scale : 1.0) *
                               (double)k_scale * 1.4426950408889634);
     p.v_scale = v_scale;
+    p.wait_cycles = wait_cycles();
     if (plan->num_ctas > 0) {
         CUtensorMap tk, tv;
         int hpb = 1;
@@ -1121,6 +1137,9 @@ pafp8_status pafp8_run_decode_noalloc(const pafp8_plan* plan, int32_t q_dtype, c
         cudaGetLastError();
         return fail(PAFP8_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(e));
     }
+    // Under PAFP8_DEBUG the call reports the kernels' status word, as the
+    // workspace entry points do.
+    if (debug_sync()) return pafp8_device_status(plan, scratch, stream);
     return PAFP8_OK;
 }
 

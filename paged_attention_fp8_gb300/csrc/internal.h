@@ -16,6 +16,8 @@ constexpr int kMaxGroupDecode = 8;
 constexpr int kMaxGroupPrefill = 16;
 constexpr int kTileRows = 128;   // prefill query rows (token x head) per tile
 constexpr int kTileKeys = 128;   // prefill keys per KV tile (8 pages)
+// Default bound of a kernel's pipeline waits, in SM clock cycles (~1 s).
+constexpr long long kWaitCyclesDefault = 2000000000LL;
 
 // Layout of the int32 partition metadata that the plan builds on the host and
 // uploads to the head of the workspace.  Word offsets of the variable-length
@@ -92,6 +94,7 @@ struct DecodeParams {
     const float* k_scales;
     const float* v_scales;
     float sm_scale;
+    long long wait_cycles;   // bound of a pipeline wait (SM clock cycles)
 };
 
 struct AppendParams {
@@ -134,6 +137,7 @@ struct PrefillParams {
     const float* k_scales;
     const float* v_scales;
     float sm_scale;
+    long long wait_cycles;   // bound of a pipeline wait (SM clock cycles)
 };
 
 // Launchers (decode.cu, prefill.cu).  Return the launch's cudaError_t.

@@ -155,9 +155,16 @@ __device__ __forceinline__ bool aborted(uint32_t flag_addr) {
     return v != 0;
 }
 
-// Bounded wait that also gives up once another role has aborted.
+// Bounded wait that also gives up once another role has aborted.  A
+// diagnostic instantiation (kDiag) polls with the host's shortened bound.
+template <bool kDiag>
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, uint32_t flag_addr,
-                                              uint32_t* status) {
+                                              uint32_t* status, long long limit) {
+    if constexpr (kDiag) {
+        if (mbar_poll(bar, parity, limit)) return true;
+        set_abort(flag_addr, status);
+        return false;
+    }
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
     while (!mbar_try_wait(bar, parity)) {
@@ -170,7 +177,7 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, uin
     return true;
 }
 
-template <bool kF8, int KT>
+template <bool kF8, int KT, bool kDiag>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_constant__ CUtensorMap tmq,
                    const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
@@ -253,7 +260,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const Item it = load_item(items, t);
             const int q0 = it.qo0 + it.t0;
             if (lane == 0) {
-                ok = wait_or_abort(bar(L::bQEmpty), qphase ^ 1u, flag_addr, p.status);
+                ok = wait_or_abort<kDiag>(bar(L::bQEmpty), qphase ^ 1u, flag_addr, p.status, p.wait_cycles);
                 if (ok) {
                     const uint32_t qb = bar(L::bQFull);
                     if (kF8) {
@@ -304,7 +311,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int i = 0; i < 8; ++i) pages[i] = __shfl_sync(0xFFFFFFFFu, page, i);
                 if (lane == 0) {
-                    ok = wait_or_abort(bar(bke + kr.idx), kr.phase ^ 1u, flag_addr, p.status);
+                    ok = wait_or_abort<kDiag>(bar(bke + kr.idx), kr.phase ^ 1u, flag_addr, p.status, p.wait_cycles);
                     if (ok) {
                         const uint32_t fb = bar(bkf + kr.idx);
                         if (k2) {
@@ -328,7 +335,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!ok) break;
                 kr.next(nkr);
                 if (lane == 0) {
-                    ok = wait_or_abort(bar(L::bVrEmpty + vr.idx), vr.phase ^ 1u, flag_addr, p.status);
+                    ok = wait_or_abort<kDiag>(bar(L::bVrEmpty + vr.idx), vr.phase ^ 1u, flag_addr, p.status, p.wait_cycles);
                     if (ok) {
                         const uint32_t fb = bar(L::bVrFull + vr.idx);
                         const uint32_t dst = base + L::vr + vr.idx * L::kRawV;
@@ -401,10 +408,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // The first O_X write of an item waits for the epilogue of the
                 // previous item that used O_X.
                 if (!accumulate && nonempty[x] > 0 &&
-                    !wait_or_abort(bar(L::bOEmpty + x), (uint32_t)((nonempty[x] - 1) & 1), flag_addr,
-                                   p.status))
+                    !wait_or_abort<kDiag>(bar(L::bOEmpty + x), (uint32_t)((nonempty[x] - 1) & 1), flag_addr,
+                                   p.status, p.wait_cycles))
                     return false;
-                if (!wait_or_abort(bar(L::bPFull + x), pphase[x], flag_addr, p.status)) return false;
+                if (!wait_or_abort<kDiag>(bar(L::bPFull + x), pphase[x], flag_addr, p.status, p.wait_cycles)) return false;
                 pphase[x] ^= 1u;
                 tc_fence_after();
                 const uint64_t dv = sw128_kmajor_desc(base + L::v16 + v16.idx * kF16Tile);
@@ -423,12 +430,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int nA = tile_nkv(it.t0, 0, TQ, qo_len, kv_len);
                 const int nB = tile_nkv(it.t0, 1, TQ, qo_len, kv_len);
                 const int n = it.nkv;
-                ok = wait_or_abort(bar(fit_q ? L::bQReady : L::bQFull), qphase, flag_addr, p.status);
+                ok = wait_or_abort<kDiag>(bar(fit_q ? L::bQReady : L::bQFull), qphase, flag_addr, p.status, p.wait_cycles);
                 qphase ^= 1u;
                 if (!ok) break;
                 tc_fence_after();
                 // K tile 0 for both query tiles.
-                ok = wait_or_abort(bar(kfull + kring.idx), kring.phase, flag_addr, p.status);
+                ok = wait_or_abort<kDiag>(bar(kfull + kring.idx), kring.phase, flag_addr, p.status, p.wait_cycles);
                 if (!ok) break;
                 tc_fence_after();
                 if (nA > 0) qk(0);
@@ -437,7 +444,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 kring.next(nk);
                 if (n == 1) tc_commit(bar(L::bQEmpty));
                 for (int j = 0; j < n && ok; ++j) {
-                    ok = wait_or_abort(bar(L::bV16Full + v16.idx), v16.phase, flag_addr, p.status);
+                    ok = wait_or_abort<kDiag>(bar(L::bV16Full + v16.idx), v16.phase, flag_addr, p.status, p.wait_cycles);
                     if (!ok) break;
                     tc_fence_after();
                     if (j < nA) {
@@ -446,7 +453,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     const bool more = j + 1 < n;
                     if (more) {
-                        ok = wait_or_abort(bar(kfull + kring.idx), kring.phase, flag_addr, p.status);
+                        ok = wait_or_abort<kDiag>(bar(kfull + kring.idx), kring.phase, flag_addr, p.status, p.wait_cycles);
                         if (!ok) break;
                         tc_fence_after();
                         if (j + 1 < nA) qk(0);
@@ -487,8 +494,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int j = 0; j < it.nkv && ok; ++j) {
                 const int valid = min(kTileKeys, kv_len - j * kTileKeys);
                 if constexpr (!kF8 && !k2) {
-                    ok = wait_or_abort(bar(L::bKrFull + kr.idx), kr.phase, flag_addr, p.status) &&
-                         wait_or_abort(bar(L::bK16Empty + k16.idx), k16.phase ^ 1u, flag_addr, p.status);
+                    ok = wait_or_abort<kDiag>(bar(L::bKrFull + kr.idx), kr.phase, flag_addr, p.status, p.wait_cycles) &&
+                         wait_or_abort<kDiag>(bar(L::bK16Empty + k16.idx), k16.phase ^ 1u, flag_addr, p.status, p.wait_cycles);
                     if (!ok) break;
                     const uint32_t src = base + L::kr + kr.idx * kRawTile;
                     const uint32_t dst = base + L::k16 + k16.idx * kF16Tile;
@@ -510,8 +517,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     kr.next(L::NKR);
                     k16.next(L::NK16);
                 }
-                ok = wait_or_abort(bar(L::bVrFull + vr.idx), vr.phase, flag_addr, p.status) &&
-                     wait_or_abort(bar(L::bV16Empty + v16.idx), v16.phase ^ 1u, flag_addr, p.status);
+                ok = wait_or_abort<kDiag>(bar(L::bVrFull + vr.idx), vr.phase, flag_addr, p.status, p.wait_cycles) &&
+                     wait_or_abort<kDiag>(bar(L::bV16Empty + v16.idx), v16.phase ^ 1u, flag_addr, p.status, p.wait_cycles);
                 if (!ok) break;
                 const uint32_t src = base + L::vr + vr.idx * L::kRawV;
                 const uint32_t dst = base + L::v16 + v16.idx * kF16Tile;
@@ -605,7 +612,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // logit scale).  Both warpgroups arrive on q_ready for every item.
         auto fit_row = [&]() -> float {
             float up = 1.f;
-            ok = __all_sync(0xFFFFFFFFu, wait_or_abort(bar(L::bQFull), qphase, flag_addr, p.status));
+            ok = __all_sync(0xFFFFFFFFu, wait_or_abort<kDiag>(bar(L::bQFull), qphase, flag_addr, p.status, p.wait_cycles));
             qphase ^= 1u;
             if (!ok) return up;
             if (r < TQ * g) {
@@ -668,7 +675,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             float m = -INFINITY, l = 0.f;  // m in scaled (log2) units
             for (int j = 0; j < nX && ok; ++j) {
-                ok = __all_sync(0xFFFFFFFFu, wait_or_abort(bar(L::bSFull + x), sphase, flag_addr, p.status));
+                ok = __all_sync(0xFFFFFFFFu, wait_or_abort<kDiag>(bar(L::bSFull + x), sphase, flag_addr, p.status, p.wait_cycles));
                 sphase ^= 1u;
                 if (!ok) break;
                 tc_fence_after();
@@ -770,7 +777,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (nX == 0) continue;  // tile B past the request's last row
             // epilogue: the tile's last O update must have completed.
-            ok = __all_sync(0xFFFFFFFFu, wait_or_abort(bar(L::bOFull + x), ophase, flag_addr, p.status));
+            ok = __all_sync(0xFFFFFFFFu, wait_or_abort<kDiag>(bar(L::bOFull + x), ophase, flag_addr, p.status, p.wait_cycles));
             ophase ^= 1u;
             if (!ok) break;
             tc_fence_after();
@@ -806,8 +813,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         bulk_wait_read_all();
                         mbar_arrive(bar(L::bStageFree + x));
                     }
-                    sok = __all_sync(0xFFFFFFFFu, wait_or_abort(bar(L::bStageFree + x), stage_round & 1u, flag_addr,
-                                                                p.status));
+                    sok = __all_sync(0xFFFFFFFFu, wait_or_abort<kDiag>(bar(L::bStageFree + x), stage_round & 1u, flag_addr,
+                                                                p.status, p.wait_cycles));
                     if (!sok) break;
 #pragma unroll
                     for (int c = 0; c < 8; ++c)
@@ -815,7 +822,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     fence_async_smem();
                     mbar_arrive(bar(L::bStageReady + x));
                     if (issuer) {
-                        sok = wait_or_abort(bar(L::bStageReady + x), stage_round & 1u, flag_addr, p.status);
+                        sok = wait_or_abort<kDiag>(bar(L::bStageReady + x), stage_round & 1u, flag_addr, p.status, p.wait_cycles);
                         if (sok) {
                             tma_store_3d(&tmo, stg, 64 * h, it.hk * g, qo0 + t0);
                             bulk_commit();
@@ -870,15 +877,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
+template <bool kF8, int KT, bool kDiag>
+cudaError_t launch_t(const PrefillParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
+                     const CUtensorMap& tv, const CUtensorMap& to, int num_ctas, cudaStream_t stream) {
+    const size_t smem = 1024 + Layout<kF8, KT == PAFP8_F16 || KT == PAFP8_BF16>::bytes;
+    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<kF8, KT, kDiag>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    prefill_kernel<kF8, KT, kDiag><<<num_ctas, kThreads, smem, stream>>>(p, tq, tk, tv, to);
+    return cudaGetLastError();
+}
+
+// The diagnostic instantiation runs only under a shortened wait bound.
 template <bool kF8, int KT>
 cudaError_t launch_one(const PrefillParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
                        const CUtensorMap& tv, const CUtensorMap& to, int num_ctas, cudaStream_t stream) {
-    const size_t smem = 1024 + Layout<kF8, KT == PAFP8_F16 || KT == PAFP8_BF16>::bytes;
-    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<kF8, KT>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    prefill_kernel<kF8, KT><<<num_ctas, kThreads, smem, stream>>>(p, tq, tk, tv, to);
-    return cudaGetLastError();
+    if (p.wait_cycles < kWaitCyclesDefault) return launch_t<kF8, KT, true>(p, tq, tk, tv, to, num_ctas, stream);
+    return launch_t<kF8, KT, false>(p, tq, tk, tv, to, num_ctas, stream);
 }
 
 }  // namespace

@@ -9,11 +9,17 @@
 #include <stdint.h>
 
 #include "../../include/pafp8.h"
+#include "internal.h"
 
 namespace pafp8 {
 namespace ptx {
 
-constexpr long long kWaitCycles = 2000000000LL;  // ~1 s at 2 GHz
+// Bound of every wait, in SM clock cycles (~1 s at 2 GHz).  The diagnostic
+// instantiations of the kernels (PAFP8_WAIT_CYCLES set) bound their pipeline
+// waits by the shorter value the host passes instead; a CTA's final waits for
+// its own copies and MMAs in flight always take this one, since those
+// complete whatever the other roles did.
+constexpr long long kWaitCycles = kWaitCyclesDefault;
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
     return (uint32_t)__cvta_generic_to_shared(p);
@@ -50,6 +56,28 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Non-blocking test of the phase of `parity`.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Poll without suspending; false after `limit` cycles.  Used by the kernels'
+// diagnostic instantiations (a shortened bound): try_wait may suspend the
+// thread until the phase completes, which would outlast a short bound.
+__device__ __forceinline__ bool mbar_poll(uint32_t bar, uint32_t parity, long long limit) {
+    const long long t0 = clock64();
+    while (!mbar_test_wait(bar, parity))
+        if (clock64() - t0 > limit) return false;
+    return true;
+}
+
 // Wait for the phase of `parity` to complete; false after ~kWaitCycles.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -57,6 +85,15 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
     while (!mbar_try_wait(bar, parity))
         if (clock64() - t0 > kWaitCycles) return false;
     return true;
+}
+
+// A pipeline wait: mbar_wait, or in a diagnostic instantiation (kDiag) a
+// poll bounded by `limit`.  The production instantiations compile to exactly
+// mbar_wait: the kernels are sensitive to every instruction of their waits.
+template <bool kDiag>
+__device__ __forceinline__ bool pipe_wait(uint32_t bar, uint32_t parity, long long limit) {
+    if constexpr (kDiag) return mbar_poll(bar, parity, limit);
+    return mbar_wait(bar, parity);
 }
 
 // Generic-proxy shared-memory writes become visible to the async proxy

@@ -84,3 +84,23 @@ def test_reference_arm_prints_the_contract_line():
     assert e2e["value"] == line["value"] and e2e["unit"] == line["unit"]
     assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
     assert "workload" in line["config"]
+
+
+def test_clock_summary_skips_idle_samples_and_collects_reasons():
+    """The clocks object describes the GPU under load: samples taken while
+    the GPU-idle reason is active (host work between timed parts, when the
+    SM clock drops) are left out; throttle reasons are collected from the
+    rest."""
+    sys.path.insert(0, ROOT)
+    import bench
+
+    def row(clk, idle, cap="Not Active", thermal="Not Active"):
+        return ["0", str(clk), "2070", "300.0", "0x0", "Not Active", "Not Active", thermal, cap, idle]
+
+    rows = [row(120, "Active")] * 50 + [row(2070, "Not Active")] * 5 + [row(1965, "Not Active", cap="Active")] * 2
+    got = bench.summarize_clocks(rows + [["garbage"]])
+    assert got["samples"] == 7 and got["samples_total"] == 57
+    assert got["sm_mhz"] == 2070 and got["sm_max_mhz"] == 2070
+    assert got["reasons"] == ["sw_power_cap"]
+    none = bench.summarize_clocks([row(120, "Active")] * 3)
+    assert none["samples"] == 0 and none["sm_mhz"] is None

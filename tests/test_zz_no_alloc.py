@@ -1,4 +1,5 @@
-"""The no-allocation decode entry point against the workspace entry point.
+"""The no-allocation decode entry point against the workspace entry point and
+the oracle.
 
 Some callers of this library may not allocate device memory at all, e.g. a
 plugin or enqueue callback inside an inference engine that owns every device
@@ -15,6 +16,7 @@ import pytest
 import torch
 
 import paged_attention_fp8_gb300 as pa
+from common import oracle_on
 from gpu_common import DeviceBatch, assert_close
 from paged_attention_fp8_gb300.workloads import make_batch, workload
 
@@ -27,16 +29,11 @@ def _noalloc(db: DeviceBatch, o, lse):
                                 q_scale=b.q_scale, k_scale=b.k_scale, v_scale=b.v_scale)
 
 
-@pytest.mark.parametrize("which", ["serving", "ragged_empty"])
-def test_noalloc_matches_workspace_entry_point_twice(cuda_device, which):
-    if which == "serving":
-        b = workload(2)  # split-KV with merge over every SM
-        db = DeviceBatch(b, cuda_device)
-    else:
-        b = make_batch([0, 1, 17, 300, 2500, 0, 64], num_qo_heads=32, num_kv_heads=8, seed=77)
-        db = DeviceBatch(b, cuda_device, num_ctas=24)
-    db.run()
-    ref_o, ref_lse = db.result()
+def _ragged_batch():
+    return make_batch([0, 1, 17, 300, 2500, 0, 64], num_qo_heads=32, num_kv_heads=8, seed=77)
+
+
+def _check_twice(db: DeviceBatch, ref_o, ref_lse, what: str):
     o = torch.empty_like(db.o)
     lse = torch.empty_like(db.lse)
     for _ in range(2):  # the scratch keeps the last call's bytes: run twice
@@ -44,8 +41,66 @@ def test_noalloc_matches_workspace_entry_point_twice(cuda_device, which):
         lse.fill_(float("nan"))
         _noalloc(db, o, lse)
         torch.cuda.synchronize()
-        assert_close(o.double().cpu().numpy(), lse.double().cpu().numpy(), ref_o, ref_lse,
-                     f"no-alloc {which}")
+        assert_close(o.double().cpu().numpy(), lse.double().cpu().numpy(), ref_o, ref_lse, what)
+
+
+@pytest.mark.parametrize("which", ["serving", "ragged_empty"])
+def test_noalloc_matches_workspace_entry_point_twice(cuda_device, which):
+    if which == "serving":
+        db = DeviceBatch(workload(2), cuda_device)  # split-KV with merge over every SM
+    else:
+        db = DeviceBatch(_ragged_batch(), cuda_device, num_ctas=24)
+    db.run()
+    ref_o, ref_lse = db.result()
+    _check_twice(db, ref_o, ref_lse, f"no-alloc {which} vs pafp8_run")
+
+
+def test_noalloc_serving_workload_against_the_oracle(cuda_device):
+    """The serving decode batch (64 requests, split-KV over every SM) through
+    the no-allocation call, compared with the fp64 oracle on every output."""
+    b = workload(2)
+    db = DeviceBatch(b, cuda_device)
+    ro, rl = oracle_on(b)
+    _check_twice(db, ro, rl, "no-alloc serving vs oracle")
+
+
+def test_noalloc_plans_back_to_back(cuda_device):
+    """A large plan, then a small one with a different partition, then the
+    large one again: each call loads its own metadata into the shared scratch,
+    so stale bytes from the previous plan never reach a result."""
+    big = DeviceBatch(workload(2), cuda_device)
+    small = DeviceBatch(_ragged_batch(), cuda_device, num_ctas=24)
+    refs = {}
+    for name, db in (("serving", big), ("ragged", small)):
+        db.run()
+        refs[name] = db.result()
+    for name, db in (("serving", big), ("ragged", small), ("serving", big)):
+        o = torch.full_like(db.o, float("nan"))
+        lse = torch.full_like(db.lse, float("nan"))
+        _noalloc(db, o, lse)
+        torch.cuda.synchronize()
+        assert_close(o.double().cpu().numpy(), lse.double().cpu().numpy(), *refs[name],
+                     f"no-alloc {name} after the other plan")
+
+
+def test_noalloc_debug_mode_reports_a_bad_page(cuda_device, monkeypatch):
+    """With PAFP8_DEBUG set the call synchronizes and returns the kernels'
+    status: a page index outside the pool comes back as PAFP8_ERR_BOUNDS."""
+    b = workload(1)
+    b.kv_indices = b.kv_indices.clone()
+    b.kv_indices[3] = b.num_pages + 5
+    db = DeviceBatch(b, cuda_device)
+    monkeypatch.setenv("PAFP8_DEBUG", "1")
+    with pytest.raises(pa.Pafp8Error) as ei:
+        _noalloc(db, db.o, db.lse)
+    assert ei.value.status == 7  # PAFP8_ERR_BOUNDS
+    good = DeviceBatch(workload(1), cuda_device)
+    _noalloc(good, good.o, good.lse)  # the status word was cleared: a good call is OK
+    monkeypatch.setenv("PAFP8_DEBUG", "0")
+    torch.cuda.synchronize()
+    ro, rl = oracle_on(workload(1))
+    assert_close(good.o.double().cpu().numpy(), good.lse.double().cpu().numpy(), ro, rl,
+                 "no-alloc after a reported bad page")
 
 
 def test_noalloc_refuses_plan_beyond_its_scratch(cuda_device):
