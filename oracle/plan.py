@@ -14,9 +14,14 @@ fixed-split and disable-split options; the balanced rule is this library's):
   goes to CTA k mod G, G = min(num_ctas, #segments).
 * fixed_split_pages = c > 0: each row cut into [0,c), [c,2c), ...; dealt the
   same way.
-* otherwise (balanced): T = total pages of all rows, G = min(num_ctas, T);
-  CTA i owns global pages [i*T//G, (i+1)*T//G) of the rows laid end to end,
-  cut at row boundaries.
+* otherwise (balanced): T = total pages of all rows, G = min(num_ctas, T).
+  When T >= 16 G and 4 R >= G (R rows), the last npages // 16 pages of every
+  row are handed out at run time (none otherwise); the rows' first ns pages
+  (the rest) are laid end to end, Ts = sum ns, and CTA i owns static pages
+  [i*Ts//G, (i+1)*Ts//G), cut at row boundaries.  The run-time pages of each
+  row, [ns, npages), are cut into chunks of c = max(4, ceil(Td / G)) pages,
+  Td = T - Ts (the last chunk of a row may be shorter); chunks are listed in
+  row and page order after every CTA's segments and numbered with them.
 * Rows with no pages get a zero-page segment (r, 0, 0); the k-th such row
   (ascending r) goes to CTA k mod G, after that CTA's other segments.  If no
   row has pages, G = 1 when some row exists.
@@ -26,14 +31,18 @@ fixed-split and disable-split options; the balanced rule is this library's):
   out_slot -1; the others get slots 0, 1, 2, ... row by row (merge rows
   ascending), and within a row by first page, so each merge row's slots are
   consecutive.
-* Merge rows: rows with two or more segments, ascending; each lists its
-  slots ordered by first page (so the slot list is 0, 1, 2, ...).  row_merge[r] is the merge entry of row r, or
-  -1.  A separate merge pass combines each merge row's slots in that order.
+* Merge rows: rows with two or more segments (chunks count as segments),
+  ascending; each lists its slots ordered by first page (so the slot list is
+  0, 1, 2, ...).  row_merge[r] is the merge entry of row r, or -1.  A
+  separate merge pass combines each merge row's slots in that order.
+* Header word 22 holds the number of chunks, word 23 the offset of their
+  (row, first page, end page, slot) records.
 """
 from __future__ import annotations
 
 HEADER_WORDS = 32
 MAGIC = 0x38464150
+DYN_DIV, DYN_CHUNKS_PER_CTA, DYN_MIN_CHUNK, DYN_MIN_PAGES_PER_CTA, DYN_MIN_ROWS_DIV = 16, 1, 4, 16, 4
 
 
 def heads_per_cta(num_kv_heads: int) -> int:
@@ -57,6 +66,7 @@ def decode_metadata(kv_indptr, last_page_len, *, num_qo_heads, num_kv_heads, num
     R = B * nhb
 
     per_cta = []
+    chunks = []
     if disable_split_kv or fixed_split_pages > 0:
         segs = []
         for r in range(R):
@@ -72,17 +82,26 @@ def decode_metadata(kv_indptr, last_page_len, *, num_qo_heads, num_kv_heads, num
     else:
         T = sum(npages)
         G = min(num_ctas, T)
+        dyn = G > 0 and T >= DYN_MIN_PAGES_PER_CTA * G and R * DYN_MIN_ROWS_DIV >= G
+        ns = [n - n // DYN_DIV if dyn else n for n in npages]
+        Ts = sum(ns)
+        Td = T - Ts
         per_cta = [[] for _ in range(G)]
         starts = [0]
-        for n in npages:
+        for n in ns:
             starts.append(starts[-1] + n)
         for i in range(G):
-            lo, hi = i * T // G, (i + 1) * T // G
+            lo, hi = i * Ts // G, (i + 1) * Ts // G
             for r in range(R):
                 a = max(lo, starts[r]) - starts[r]
                 e = min(hi, starts[r + 1]) - starts[r]
                 if e > a:
                     per_cta[i].append([r, a, e, 0])
+        if Td > 0:
+            c = max(DYN_MIN_CHUNK, -(-Td // (DYN_CHUNKS_PER_CTA * G)))
+            for r in range(R):
+                for a in range(ns[r], npages[r], c):
+                    chunks.append([r, a, min(a + c, npages[r]), 0])
 
     empty = [r for r in range(R) if npages[r] == 0]
     if empty and not per_cta:
@@ -98,7 +117,7 @@ def decode_metadata(kv_indptr, last_page_len, *, num_qo_heads, num_kv_heads, num
 
     seg_count = [0] * R
     row_parts = [[] for _ in range(R)]
-    for segs in per_cta:
+    for segs in per_cta + [chunks]:
         for s in segs:
             seg_count[s[0]] += 1
             if not is_partial(s):
@@ -154,6 +173,8 @@ def decode_metadata(kv_indptr, last_page_len, *, num_qo_heads, num_kv_heads, num
     put(15, merge_rows)
     put(16, merge_slots)
     put(21, row_merge)
+    words[22] = len(chunks)
+    put(23, [x for ch in chunks for x in ch])
     return words
 
 

@@ -60,6 +60,7 @@ using namespace ptx;
 
 constexpr int P = kPageSize;
 constexpr int kStageBudget = 192 * 1024;    // shared memory for the page ring
+constexpr int kChunkSlots = 2;              // chunk-id queue depth
 __host__ __device__ constexpr bool is_2byte_kv(int kt) { return kt == PAFP8_F16 || kt == PAFP8_BF16; }
 // One KV head of one page in shared memory: 16 token rows of dh bytes (fp8:
 // 128 B with the 128-byte swizzle, or 64 B with the 64-byte swizzle), or of
@@ -171,6 +172,158 @@ __device__ __forceinline__ float load_q(uint32_t (&qf)[16], uint32_t (&qlo)[16],
     return factor;
 }
 
+// Combine the partial states of each split (request, KV-head block) row.
+// The plan numbers a row's partial states consecutively (slots mptr[e] ..
+// mptr[e+1] - 1, in page order), so no slot list is read.
+// One warp per (merge entry, query head of the block), kMergeWarps per block;
+// lane l holds dims (D/32) l .. (D/32) l + D/32 - 1.  The warp loads the
+// row's slots in batches of kMergeBatch (every lane the batch's lse values
+// and its own dims of the O vectors, all loads of a batch in flight
+// together), keeps a running max m of the log2-domain lse_c and the rescaled
+// sums of 2^lse_c and 2^lse_c O_c, and writes
+// o = v_scale * sum(2^lse_c O_c) / sum(2^lse_c), lse = ln(sum) + m.
+// Launched as a programmatic dependent of the decode kernel: the row's
+// metadata (written by the host) is read before griddepcontrol.wait, which
+// returns once the decode grid has completed and its writes are visible.
+constexpr int kMergeBatch = 8;
+constexpr int kMergeWarps = 4;  // query heads per merge block
+
+// kMergeBatch lse values and O vectors (DPL floats) of partial states, all
+// loads issued in one instruction block (L2, bypassing L1), so the batch's
+// latencies overlap.
+template <int DPL>
+__device__ __forceinline__ void load_batch(const float* const (&lp)[kMergeBatch], const float* const (&op)[kMergeBatch],
+                                           float (&l)[kMergeBatch], float (&o)[kMergeBatch][DPL]);
+template <>
+__device__ __forceinline__ void load_batch<4>(const float* const (&lp)[kMergeBatch], const float* const (&op)[kMergeBatch],
+                                              float (&l)[kMergeBatch], float (&o)[kMergeBatch][4]) {
+    asm volatile(
+        "ld.global.cg.f32 %0, [%40];\n ld.global.cg.f32 %1, [%41];\n ld.global.cg.f32 %2, [%42];\n"
+        " ld.global.cg.f32 %3, [%43];\n ld.global.cg.f32 %4, [%44];\n ld.global.cg.f32 %5, [%45];\n"
+        " ld.global.cg.f32 %6, [%46];\n ld.global.cg.f32 %7, [%47];\n"
+        " ld.global.cg.v4.f32 {%8, %9, %10, %11}, [%48];\n ld.global.cg.v4.f32 {%12, %13, %14, %15}, [%49];\n"
+        " ld.global.cg.v4.f32 {%16, %17, %18, %19}, [%50];\n ld.global.cg.v4.f32 {%20, %21, %22, %23}, [%51];\n"
+        " ld.global.cg.v4.f32 {%24, %25, %26, %27}, [%52];\n ld.global.cg.v4.f32 {%28, %29, %30, %31}, [%53];\n"
+        " ld.global.cg.v4.f32 {%32, %33, %34, %35}, [%54];\n ld.global.cg.v4.f32 {%36, %37, %38, %39}, [%55];\n"
+        : "=f"(l[0]), "=f"(l[1]), "=f"(l[2]), "=f"(l[3]), "=f"(l[4]), "=f"(l[5]), "=f"(l[6]), "=f"(l[7]),
+          "=f"(o[0][0]), "=f"(o[0][1]), "=f"(o[0][2]), "=f"(o[0][3]), "=f"(o[1][0]), "=f"(o[1][1]), "=f"(o[1][2]),
+          "=f"(o[1][3]), "=f"(o[2][0]), "=f"(o[2][1]), "=f"(o[2][2]), "=f"(o[2][3]), "=f"(o[3][0]), "=f"(o[3][1]),
+          "=f"(o[3][2]), "=f"(o[3][3]), "=f"(o[4][0]), "=f"(o[4][1]), "=f"(o[4][2]), "=f"(o[4][3]), "=f"(o[5][0]),
+          "=f"(o[5][1]), "=f"(o[5][2]), "=f"(o[5][3]), "=f"(o[6][0]), "=f"(o[6][1]), "=f"(o[6][2]), "=f"(o[6][3]),
+          "=f"(o[7][0]), "=f"(o[7][1]), "=f"(o[7][2]), "=f"(o[7][3])
+        : "l"(lp[0]), "l"(lp[1]), "l"(lp[2]), "l"(lp[3]), "l"(lp[4]), "l"(lp[5]), "l"(lp[6]), "l"(lp[7]),
+          "l"(op[0]), "l"(op[1]), "l"(op[2]), "l"(op[3]), "l"(op[4]), "l"(op[5]), "l"(op[6]), "l"(op[7])
+        : "memory");
+    // Every result is live here, so no use of one can be scheduled before
+    // the last load of the batch has been issued.
+    asm volatile("" ::"f"(l[0]), "f"(l[1]), "f"(l[2]), "f"(l[3]), "f"(l[4]), "f"(l[5]), "f"(l[6]), "f"(l[7]),
+                 "f"(o[0][0]), "f"(o[0][1]), "f"(o[0][2]), "f"(o[0][3]), "f"(o[1][0]), "f"(o[1][1]), "f"(o[1][2]),
+                 "f"(o[1][3]), "f"(o[2][0]), "f"(o[2][1]), "f"(o[2][2]), "f"(o[2][3]), "f"(o[3][0]), "f"(o[3][1]),
+                 "f"(o[3][2]), "f"(o[3][3]), "f"(o[4][0]), "f"(o[4][1]), "f"(o[4][2]), "f"(o[4][3]), "f"(o[5][0]),
+                 "f"(o[5][1]), "f"(o[5][2]), "f"(o[5][3]), "f"(o[6][0]), "f"(o[6][1]), "f"(o[6][2]), "f"(o[6][3]),
+                 "f"(o[7][0]), "f"(o[7][1]), "f"(o[7][2]), "f"(o[7][3]));
+}
+template <>
+__device__ __forceinline__ void load_batch<2>(const float* const (&lp)[kMergeBatch], const float* const (&op)[kMergeBatch],
+                                              float (&l)[kMergeBatch], float (&o)[kMergeBatch][2]) {
+    asm volatile(
+        "ld.global.cg.f32 %0, [%24];\n ld.global.cg.f32 %1, [%25];\n ld.global.cg.f32 %2, [%26];\n"
+        " ld.global.cg.f32 %3, [%27];\n ld.global.cg.f32 %4, [%28];\n ld.global.cg.f32 %5, [%29];\n"
+        " ld.global.cg.f32 %6, [%30];\n ld.global.cg.f32 %7, [%31];\n"
+        " ld.global.cg.v2.f32 {%8, %9}, [%32];\n ld.global.cg.v2.f32 {%10, %11}, [%33];\n"
+        " ld.global.cg.v2.f32 {%12, %13}, [%34];\n ld.global.cg.v2.f32 {%14, %15}, [%35];\n"
+        " ld.global.cg.v2.f32 {%16, %17}, [%36];\n ld.global.cg.v2.f32 {%18, %19}, [%37];\n"
+        " ld.global.cg.v2.f32 {%20, %21}, [%38];\n ld.global.cg.v2.f32 {%22, %23}, [%39];\n"
+        : "=f"(l[0]), "=f"(l[1]), "=f"(l[2]), "=f"(l[3]), "=f"(l[4]), "=f"(l[5]), "=f"(l[6]), "=f"(l[7]),
+          "=f"(o[0][0]), "=f"(o[0][1]), "=f"(o[1][0]), "=f"(o[1][1]), "=f"(o[2][0]), "=f"(o[2][1]), "=f"(o[3][0]),
+          "=f"(o[3][1]), "=f"(o[4][0]), "=f"(o[4][1]), "=f"(o[5][0]), "=f"(o[5][1]), "=f"(o[6][0]), "=f"(o[6][1]),
+          "=f"(o[7][0]), "=f"(o[7][1])
+        : "l"(lp[0]), "l"(lp[1]), "l"(lp[2]), "l"(lp[3]), "l"(lp[4]), "l"(lp[5]), "l"(lp[6]), "l"(lp[7]),
+          "l"(op[0]), "l"(op[1]), "l"(op[2]), "l"(op[3]), "l"(op[4]), "l"(op[5]), "l"(op[6]), "l"(op[7])
+        : "memory");
+    asm volatile("" ::"f"(l[0]), "f"(l[1]), "f"(l[2]), "f"(l[3]), "f"(l[4]), "f"(l[5]), "f"(l[6]), "f"(l[7]),
+                 "f"(o[0][0]), "f"(o[0][1]), "f"(o[1][0]), "f"(o[1][1]), "f"(o[2][0]), "f"(o[2][1]), "f"(o[3][0]),
+                 "f"(o[3][1]), "f"(o[4][0]), "f"(o[4][1]), "f"(o[5][0]), "f"(o[5][1]), "f"(o[6][0]), "f"(o[6][1]),
+                 "f"(o[7][0]), "f"(o[7][1]));
+}
+
+template <int DPL>
+__device__ __forceinline__ void merge_head(const DecodeParams& p, int hpb, int hh, int s0, int s1, size_t oh,
+                                           float vscale) {
+    const int lane = threadIdx.x & 31;
+    float m = -INFINITY, sum = 0.f, acc[DPL];
+#pragma unroll
+    for (int i = 0; i < DPL; ++i) acc[i] = 0.f;
+    for (int s = s0; s < s1; s += kMergeBatch) {
+        float l[kMergeBatch], o[kMergeBatch][DPL];
+        const float* lp[kMergeBatch];
+        const float* op[kMergeBatch];
+#pragma unroll
+        for (int k = 0; k < kMergeBatch; ++k) {
+            const size_t idx = (size_t)(s + k < s1 ? s + k : s) * hpb + hh;  // a row's slots are consecutive
+            lp[k] = p.part_lse + idx;
+            op[k] = p.part_o + idx * p.head_dim + DPL * lane;
+        }
+        load_batch<DPL>(lp, op, l, o);  // every load of the batch in flight together
+        // Slot s (k = 0) exists, so m is finite from here on; padding slots
+        // (lse -inf) get weight 0.
+#pragma unroll
+        for (int k = 0; k < kMergeBatch; ++k) {
+            const float lk = s + k < s1 ? l[k] : -INFINITY;
+            const float mn = fmaxf(m, lk);
+            const float a = ex2(m - mn), wt = ex2(lk - mn);
+            sum = sum * a + wt;
+#pragma unroll
+            for (int i = 0; i < DPL; ++i) acc[i] = acc[i] * a + wt * o[k][i];
+            m = mn;
+        }
+    }
+    const float inv = vscale / sum;
+    uint32_t wd[DPL / 2];
+#pragma unroll
+    for (int i = 0; i < DPL / 2; ++i) wd[i] = pack_out2(acc[2 * i] * inv, acc[2 * i + 1] * inv, p.o_dtype);
+    uint16_t* dst = static_cast<uint16_t*>(p.o) + oh * p.head_dim + DPL * lane;
+    if constexpr (DPL == 4)
+        *reinterpret_cast<uint2*>(dst) = make_uint2(wd[0], wd[DPL > 2 ? 1 : 0]);
+    else
+        *reinterpret_cast<uint32_t*>(dst) = wd[0];
+    if (lane == 0 && p.lse != nullptr) p.lse[oh] = (m + __log2f(sum)) * 0.69314718055994531f;
+}
+
+// One (merge entry, query head) pair's metadata: its slots, output row and
+// v_scale.  The metadata is the host's, so it may be read before the
+// partial states are complete.
+struct MergePair {
+    int hh, s0, s1;
+    size_t oh;
+    float vscale;
+};
+
+__device__ __forceinline__ MergePair merge_pair_args(const DecodeParams& p, int hpc, int group, int e, int hh) {
+    const int* meta = p.meta;
+    const int nhb = meta[kMetaHeadBlocks];
+    const int* mptr = meta + meta[kMetaOffMergePtr];
+    const int* mrow = meta + meta[kMetaOffMergeRow];
+    const int hpb = hpc * group;
+    const int row = mrow[e];
+    const int b = row / nhb, hb = row - b * nhb;
+    const int head = hb * hpb + hh;  // query head: (hb * hpc + hh / group) * group + hh % group
+    MergePair a;
+    a.hh = hh;
+    a.s0 = mptr[e];
+    a.s1 = mptr[e + 1];
+    a.oh = (size_t)b * p.num_qo_heads + head;
+    a.vscale = p.v_scales != nullptr ? __ldg(p.v_scales + head / group) : p.v_scale;
+    return a;
+}
+
+__device__ __forceinline__ void merge_pair(const DecodeParams& p, int hpb, const MergePair& a) {
+    if (p.head_dim == 64)
+        merge_head<2>(p, hpb, a.hh, a.s0, a.s1, a.oh, a.vscale);
+    else
+        merge_head<4>(p, hpb, a.hh, a.s0, a.s1, a.oh, a.vscale);
+}
+
 template <int KT, int DH, bool kDiag>
 __global__ void __launch_bounds__(32 * 9, 1)
     decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtensorMap tmk,
@@ -185,6 +338,11 @@ __global__ void __launch_bounds__(32 * 9, 1)
     const uint32_t stage_bytes = 2u * hpc * kTileBytes;  // K heads then V heads
     const uint32_t bar_full = base + stages * stage_bytes;
     const uint32_t bar_empty = bar_full + 8u * stages;
+    // Queue of chunk ids (run-time work) from the producer to the consumers:
+    // kChunkSlots slots with full / empty barriers.
+    const uint32_t cq_full = bar_empty + 8u * stages;
+    const uint32_t cq_empty = cq_full + 8u * kChunkSlots;
+    const uint32_t cq_id = cq_empty + 8u * kChunkSlots;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int* meta = p.meta;
@@ -194,11 +352,17 @@ __global__ void __launch_bounds__(32 * 9, 1)
     const int* cta_seg = meta + meta[kMetaOffCtaSeg];
     const int* segs = meta + meta[kMetaOffSeg];
     const int seg_begin = cta_seg[blockIdx.x], seg_end = cta_seg[blockIdx.x + 1];
+    const int n_chunks = meta[kMetaNumChunks];
+    const int* chunk_rec = meta + meta[kMetaOffChunk];
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < stages; ++s) {
             mbar_init(bar_full + 8u * s, 1);
             mbar_init(bar_empty + 8u * s, 32u * hpc);
+        }
+        for (int s = 0; s < kChunkSlots; ++s) {
+            mbar_init(cq_full + 8u * s, 1);
+            mbar_init(cq_empty + 8u * s, (uint32_t)hpc);
         }
 
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -216,8 +380,37 @@ __global__ void __launch_bounds__(32 * 9, 1)
         uint32_t phase = 0;
         long long issued = 0;
         bool ok = true;
-        for (int si = seg_begin; si < seg_end && ok; ++si) {
-            const int row = segs[4 * si], p0 = segs[4 * si + 1], p1 = segs[4 * si + 2];
+        int si = seg_begin, cq = 0;
+        uint32_t cqphase = 0;
+        uint32_t* const ctr = p.status + kChunkCounterWord;
+        for (;;) {
+            // This CTA's own segments, then chunks taken from the counter
+            // until none is left; each chunk id goes to the consumers first.
+            const int* rec;
+            if (si < seg_end) {
+                rec = segs + 4 * si++;
+            } else {
+                if (n_chunks == 0) break;
+                int c = -1;
+                if (lane == 0) {
+                    c = (int)atomicAdd(ctr, 1u);
+                    if (c >= n_chunks) c = -1;
+                    ok = pipe_wait<kDiag>(cq_empty + 8u * cq, cqphase ^ 1u, p.wait_cycles);
+                    if (ok) {
+                        sts32(cq_id + 4u * cq, (uint32_t)c);
+                        mbar_arrive(cq_full + 8u * cq);
+                    }
+                }
+                ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+                c = __shfl_sync(0xFFFFFFFFu, c, 0);
+                if (++cq == kChunkSlots) {
+                    cq = 0;
+                    cqphase ^= 1u;
+                }
+                if (!ok || c < 0) break;
+                rec = chunk_rec + 4 * c;
+            }
+            const int row = rec[0], p0 = rec[1], p1 = rec[2];
             const int b = row / nhb, hb = row - b * nhb;
             const int* idx = p.kv_indices + req_page[b];
             for (int pb = p0; pb < p1 && ok; pb += 32) {
@@ -271,8 +464,19 @@ __global__ void __launch_bounds__(32 * 9, 1)
                     }
                 }
             }
+            if (!ok) break;
         }
         if (lane == 0) {
+            if (n_chunks > 0) {
+                // The last CTA done taking chunks resets the counters for the
+                // next launch (every CTA's last take comes before its count).
+                uint32_t* const done = p.status + kChunkDoneWord;
+                __threadfence();
+                if (atomicAdd(done, 1u) == gridDim.x - 1) {
+                    atomicExch(ctr, 0u);
+                    atomicExch(done, 0u);
+                }
+            }
             if (!ok) flag(p.status, kStatusTimeout);
             // Let every copy this CTA issued land before it may exit.
             for (int s = 0; s < stages && s < issued; ++s) {
@@ -283,8 +487,7 @@ __global__ void __launch_bounds__(32 * 9, 1)
                 }
             }
         }
-        return;
-    }
+    } else {
 
     // -------------------------------------------------------------- consumers
     const int g = lane >> 2, t = lane & 3;
@@ -292,9 +495,30 @@ __global__ void __launch_bounds__(32 * 9, 1)
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
-    for (int si = seg_begin; si < seg_end && ok; ++si) {
-        const int row = segs[4 * si], p0 = segs[4 * si + 1], p1 = segs[4 * si + 2];
-        const int slot = segs[4 * si + 3];
+    int si = seg_begin, cq = 0;
+    uint32_t cqphase = 0;
+    for (;;) {
+        const int* rec;
+        if (si < seg_end) {
+            rec = segs + 4 * si++;
+        } else {
+            // The next chunk the producer took (id -1: none left).
+            if (n_chunks == 0) break;
+            ok = __all_sync(0xFFFFFFFFu, pipe_wait<kDiag>(cq_full + 8u * cq, cqphase, p.wait_cycles));
+            if (!ok) break;
+            uint32_t c;
+            asm volatile("ld.shared.u32 %0, [%1];" : "=r"(c) : "r"(cq_id + 4u * cq) : "memory");
+            __syncwarp();
+            if (lane == 0) mbar_arrive(cq_empty + 8u * cq);
+            if (++cq == kChunkSlots) {
+                cq = 0;
+                cqphase ^= 1u;
+            }
+            if ((int)c < 0) break;
+            rec = chunk_rec + 4 * (int)c;
+        }
+        const int row = rec[0], p0 = rec[1], p1 = rec[2];
+        const int slot = rec[3];
         const int b = row / nhb, hb = row - b * nhb;
         const int kvh = hb * hpc + warp;
         const int kv_len = req_kv[b];
@@ -579,61 +803,21 @@ __global__ void __launch_bounds__(32 * 9, 1)
         }
     }
     if (!ok && lane == 0) flag(p.status, kStatusTimeout);
+    }  // consumers
 }
 
-// Combine the partial states of each split (request, KV-head block) row.
-// The plan numbers a row's partial states consecutively (slots mptr[e] ..
-// mptr[e+1] - 1, in page order), so no slot list is read.
-// Block = one (merge entry, query head of the block); thread = one of the
-// head_dim dims.  Over the row's slots (page order) it keeps a running max of the
-// log2-domain lse_c and the rescaled sums of 2^lse_c and 2^lse_c O_c, four
-// slots' loads in flight per step, then writes o = v_scale * sum / sum and
-// lse = ln(sum) + max.  Launched as a programmatic dependent of the decode
-// kernel: griddepcontrol.wait returns once that grid has completed and its
-// writes are visible.
-__global__ void __launch_bounds__(128)
+__global__ void __launch_bounds__(32 * kMergeWarps)
     merge_kernel(const __grid_constant__ DecodeParams p, int hpc, int group) {
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    const int* meta = p.meta;
-    const int nhb = meta[kMetaHeadBlocks];
-    const int* mptr = meta + meta[kMetaOffMergePtr];
-    const int* mrow = meta + meta[kMetaOffMergeRow];
+    // The metadata (written by the host) is read before the wait.
     const int hpb = hpc * group;
-    const int e = blockIdx.x / hpb, hh = blockIdx.x - e * hpb, d = threadIdx.x;
-    const int row = mrow[e];
-    const int b = row / nhb, hb = row - b * nhb;
-    const int s0 = mptr[e], s1 = mptr[e + 1];
-    float m = -INFINITY, sum = 0.f, acc = 0.f;
-    for (int s = s0; s < s1; s += 4) {
-        float l[4], o[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const bool in = s + k < s1;
-            const size_t idx = (size_t)(in ? s + k : s0) * hpb + hh;  // a row's slots are consecutive
-            l[k] = in ? __ldcg(p.part_lse + idx) : -INFINITY;
-            o[k] = in ? __ldcg(p.part_o + idx * p.head_dim + d) : 0.f;
-        }
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const float mn = fmaxf(m, l[k]);
-            const float a = ex2(m - mn), w = ex2(l[k] - mn);
-            sum = sum * a + w;
-            acc = acc * a + w * o[k];
-            m = mn;
-        }
-    }
-    const int head = hb * hpb + hh;  // query head: (hb * hpc + hh / group) * group + hh % group
-    const size_t oh = (size_t)b * p.num_qo_heads + head;
-    const float val = acc / sum * (p.v_scales != nullptr ? __ldg(p.v_scales + head / group) : p.v_scale);
-    uint16_t* dst = static_cast<uint16_t*>(p.o) + oh * p.head_dim + d;
-    if (p.o_dtype == PAFP8_BF16) {
-        __nv_bfloat16 h = __float2bfloat16_rn(val);
-        *dst = *reinterpret_cast<uint16_t*>(&h);
-    } else {
-        __half h = __float2half_rn(val);
-        *dst = *reinterpret_cast<uint16_t*>(&h);
-    }
-    if (d == 0 && p.lse != nullptr) p.lse[oh] = (m + __log2f(sum)) * 0.69314718055994531f;
+    const int bpr = (hpb + kMergeWarps - 1) / kMergeWarps;  // blocks per merge row
+    const int e = blockIdx.x / bpr;
+    const int hh = (blockIdx.x - e * bpr) * kMergeWarps + (threadIdx.x >> 5);
+    MergePair a{};
+    if (hh < hpb) a = merge_pair_args(p, hpc, group, e, hh);
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (hh >= hpb) return;
+    merge_pair(p, hpb, a);
 }
 
 }  // namespace
@@ -673,7 +857,7 @@ cudaError_t launch_decode_t(const DecodeParams& p, const CUtensorMap& tmap_k, co
     int stages = kStageBudget / stage_bytes;
     if (stages > 8) stages = 8;
     if (stages < 2) stages = 2;
-    const size_t smem = 1024 + (size_t)stages * stage_bytes + 16 * (size_t)stages;
+    const size_t smem = 1024 + (size_t)stages * stage_bytes + 16 * (size_t)stages + 20 * kChunkSlots;
     const dim3 grid(num_ctas), block(32 * (hpc + 1));
     // The diagnostic instantiation runs only under a shortened wait bound.
     const bool diag = p.wait_cycles < kWaitCyclesDefault;
@@ -710,8 +894,8 @@ cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& tmap_k, cons
 
 cudaError_t launch_merge(const DecodeParams& p, int num_merge, int hpc, int group, cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(num_merge * hpc * group);
-    cfg.blockDim = dim3(p.head_dim);
+    cfg.gridDim = dim3(num_merge * ((hpc * group + kMergeWarps - 1) / kMergeWarps));
+    cfg.blockDim = dim3(32 * kMergeWarps);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];

@@ -187,7 +187,7 @@ void build_decode_meta(pafp8_plan* pl) {
     auto seg_of = [&](int32_t r, int64_t a, int64_t e) {
         return Seg{r, (int32_t)a, (int32_t)e, (a == 0 && e == np[r]) ? -1 : 0};
     };
-    std::vector<Seg> segs;
+    std::vector<Seg> segs, chunks;
     std::vector<int32_t> cta_ptr(1, 0);
     const int64_t target = pl->desc.num_ctas;
     int64_t G = 0;
@@ -213,13 +213,24 @@ void build_decode_meta(pafp8_plan* pl) {
         G = gt;
     } else {
         G = std::min<int64_t>(target, T);
+        // Each row's last np / kDynDiv pages are handed out at run time in
+        // chunks (when the batch qualifies); the rows' first ns pages, laid
+        // end to end, are split statically.
+        const bool dyn = G > 0 && T >= (int64_t)kDynMinPagesPerCta * G && (int64_t)R * kDynMinRowsDiv >= G;
+        std::vector<int32_t> ns((size_t)R);
+        int64_t Ts = 0;
+        for (int rr = 0; rr < R; ++rr) {
+            ns[rr] = dyn ? np[rr] - np[rr] / kDynDiv : np[rr];
+            Ts += ns[rr];
+        }
+        const int64_t Td = T - Ts;
         const int64_t gt = G > 0 ? G : (empty.empty() ? 0 : 1);
         cta_ptr.reserve((size_t)gt + 1);
         segs.reserve((size_t)(G + R + empty.size()));
-        int64_t start = 0;  // first global page of row r
+        int64_t start = 0;  // first global static page of row r
         int r = 0;
-        // hi = floor((i + 1) T / G) kept as quotient and remainder, one step per CTA
-        const int64_t dq = G > 0 ? T / G : 0, dr = G > 0 ? T % G : 0;
+        // hi = floor((i + 1) Ts / G) kept as quotient and remainder, one step per CTA
+        const int64_t dq = G > 0 ? Ts / G : 0, dr = G > 0 ? Ts % G : 0;
         int64_t hq = 0, hr = 0;
         for (int64_t i = 0; i < gt; ++i) {
             if (G > 0) {
@@ -231,11 +242,11 @@ void build_decode_meta(pafp8_plan* pl) {
                     hr -= G;
                 }
                 const int64_t hi = hq;
-                while (r < R && start + np[r] <= lo) start += np[r++];
+                while (r < R && start + ns[r] <= lo) start += ns[r++];
                 int64_t rs = start;
-                for (int rr = r; rr < R && rs < hi; rs += np[rr++]) {
+                for (int rr = r; rr < R && rs < hi; rs += ns[rr++]) {
                     const int64_t a = std::max(lo, rs) - rs;
-                    const int64_t e = std::min(hi, rs + np[rr]) - rs;
+                    const int64_t e = std::min(hi, rs + ns[rr]) - rs;
                     if (e > a) segs.push_back(seg_of(rr, a, e));
                 }
             }
@@ -243,6 +254,13 @@ void build_decode_meta(pafp8_plan* pl) {
             cta_ptr.push_back((int32_t)segs.size());
         }
         G = gt;
+        if (Td > 0) {
+            const int64_t per = (int64_t)kDynChunksPerCta * G;
+            const int64_t c = std::max<int64_t>(kDynMinChunk, (Td + per - 1) / per);
+            for (int rr = 0; rr < R; ++rr)
+                for (int64_t a = ns[rr]; a < np[rr]; a += c)
+                    chunks.push_back(seg_of(rr, a, std::min<int64_t>(a + c, np[rr])));
+        }
     }
 
     // Within a CTA, segments covering part of their row run first, so the
@@ -260,6 +278,11 @@ void build_decode_meta(pafp8_plan* pl) {
             if (!partial(*x)) tmp.push_back(*x);
         std::copy(tmp.begin(), tmp.end(), a);
     }
+
+    // Chunks follow the static segments (records after cta_ptr[G]) and are
+    // numbered with them.
+    const int32_t nseg_static = (int32_t)segs.size();
+    segs.insert(segs.end(), chunks.begin(), chunks.end());
 
     // Output slots and the merge lists.  A row cut into two or more segments
     // has only partial ones; its partial states are numbered merge row by
@@ -291,7 +314,8 @@ void build_decode_meta(pafp8_plan* pl) {
         if (k + 1 == nslot || segs[parts[k + 1]].row != sg.row) merge_ptr.push_back(k + 1);
     }
     const int32_t nmerge = (int32_t)merge_rows.size();
-    const int32_t nseg = (int32_t)segs.size();
+    const int32_t nseg = nseg_static;
+    const int32_t nchunk = (int32_t)chunks.size();
 
     std::vector<int32_t>& m = pl->meta;
     m.assign(kMetaHeaderWords, 0);
@@ -317,7 +341,8 @@ void build_decode_meta(pafp8_plan* pl) {
     m[kMetaOffCtaSeg] = (int32_t)m.size();
     m.insert(m.end(), cta_ptr.begin(), cta_ptr.end());
     m[kMetaOffSeg] = (int32_t)m.size();
-    for (const Seg& sg : segs) {
+    for (int32_t k = 0; k < nseg; ++k) {
+        const Seg& sg = segs[(size_t)k];
         m.push_back(sg.row);
         m.push_back(sg.p0);
         m.push_back(sg.p1);
@@ -331,6 +356,15 @@ void build_decode_meta(pafp8_plan* pl) {
     for (int32_t k = 0; k < nslot; ++k) m.push_back(k);
     m[kMetaOffRowMerge] = (int32_t)m.size();
     m.insert(m.end(), row_merge.begin(), row_merge.end());
+    m[kMetaNumChunks] = nchunk;
+    m[kMetaOffChunk] = (int32_t)m.size();
+    for (int32_t k = nseg; k < nseg + nchunk; ++k) {
+        const Seg& sg = segs[(size_t)k];
+        m.push_back(sg.row);
+        m.push_back(sg.p0);
+        m.push_back(sg.p1);
+        m.push_back(sg.slot);
+    }
 
     pl->num_ctas = (int)G;
     pl->num_partials = nslot;
@@ -784,7 +818,7 @@ pafp8_status pafp8_plan_upload(pafp8_plan* plan, void* workspace, size_t workspa
     cudaError_t e = cudaMemcpyAsync(workspace, plan->meta.data(), plan->meta.size() * 4,
                                     cudaMemcpyHostToDevice, s);
     if (e == cudaSuccess)
-        e = cudaMemsetAsync((char*)workspace + plan->status_off, 0, 256, s);
+        e = cudaMemsetAsync((char*)workspace + plan->status_off, 0, plan->ws_bytes - plan->status_off, s);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return fail(PAFP8_ERR_CUDA, "metadata upload failed: %s", cudaGetErrorString(e));
@@ -1096,7 +1130,7 @@ pafp8_status pafp8_run_decode_noalloc(const pafp8_plan* plan, int32_t q_dtype, c
     // The scratch keeps the previous call's bytes: load this plan's metadata
     // and clear the status word; partial states are written before read.
     e = cudaMemcpyAsync(ws, plan->meta.data(), plan->meta.size() * 4, cudaMemcpyHostToDevice, s);
-    if (e == cudaSuccess) e = cudaMemsetAsync(ws + plan->status_off, 0, 256, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(ws + plan->status_off, 0, plan->ws_bytes - plan->status_off, s);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return fail(PAFP8_ERR_CUDA, "loading the plan into the built-in scratch failed: %s",

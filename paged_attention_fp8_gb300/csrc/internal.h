@@ -45,8 +45,27 @@ enum MetaHeader : int {
     kMetaOffTile,        // int32[8*num_tiles] prefill items: b, hk, t0, nkv, qo_begin, qo_len, kv_len, page_begin
     kMetaTileRows,       // packed query rows per prefill tile
     kMetaOffRowMerge,    // int32[rows] merge entry of each decode row, or -1
+    kMetaNumChunks,      // decode pages handed out at run time, in chunks
+    kMetaOffChunk,       // int32[4*num_chunks] (row, page_begin, page_end, out_slot)
     kMetaHeaderWords = 32
 };
+
+// Decode work handed out at run time: the last 1/kDynDiv of every row's
+// pages, cut into chunks of about 1/kDynChunksPerCta of a CTA's share of
+// them, when the batch has at least kDynMinPagesPerCta pages per CTA and at
+// least one row per kDynMinRowsDiv CTAs (with fewer, longer rows the chunks
+// would add many partial states to each row and slow its merge).  Each CTA
+// takes chunks from a counter in the workspace after its own pages; a row's
+// chunks add one or two partial states to it.
+constexpr int kDynDiv = 16;
+constexpr int kDynChunksPerCta = 1;
+constexpr int kDynMinChunk = 4;
+constexpr int kDynMinPagesPerCta = 16;
+constexpr int kDynMinRowsDiv = 4;
+// Word offsets in the workspace's 256-byte status block: the status word,
+// the chunk counter and the count of CTAs done with chunks (both reset by the
+// last CTA of each launch).
+constexpr int kStatusWord = 0, kChunkCounterWord = 32, kChunkDoneWord = 48;
 constexpr int32_t kMetaMagicValue = 0x38464150;
 
 // log2-domain softmax scale of one head from per-head scales, folded in
@@ -80,7 +99,7 @@ struct DecodeParams {
     const int32_t* meta;     // device copy of the metadata words
     float* part_o;           // [num_partials, hpc*group, D]
     float* part_lse;         // [num_partials, hpc*group] (log2 domain)
-    uint32_t* status;
+    uint32_t* status;        // status block: status word, chunk counter, CTAs done
     int head_dim;            // 128 or 64
     int q_dtype, kv_dtype, o_dtype;
     int num_qo_heads, num_kv_heads, num_pages;

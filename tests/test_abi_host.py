@@ -92,8 +92,9 @@ def test_plan_partition_covers_every_page_once(case):
     G, nseg = m[6], m[7]
     cta = m[m[12]:m[12] + G + 1]
     segs = m[m[13]:m[13] + 4 * nseg].reshape(-1, 4)
+    chunks = m[m[23]:m[23] + 4 * m[22]].reshape(-1, 4)  # handed out at run time
     cover = {}
-    for r, a, e, _ in segs:
+    for r, a, e, _ in np.concatenate([segs, chunks]):
         for p in range(a, e):
             key = (int(r), p)
             assert key not in cover
@@ -103,7 +104,14 @@ def test_plan_partition_covers_every_page_once(case):
     assert cta[0] == 0 and cta[-1] == nseg and np.all(np.diff(cta) >= 1)
     if not case.get("fixed_split_pages") and not case.get("disable_split_kv") and G > 0:
         loads = [int((segs[cta[i]:cta[i + 1], 2] - segs[cta[i]:cta[i + 1], 1]).sum()) for i in range(G)]
-        assert max(loads) - min(loads) <= 1  # balanced to within one page
+        assert max(loads) - min(loads) <= 1  # static shares balanced to within one page
+        T = sum(n for n in npages for _ in range(nhb))
+        R = len(npages) * nhb
+        run_time = int((chunks[:, 2] - chunks[:, 1]).sum()) if len(chunks) else 0
+        assert run_time == (sum(n // 16 for n in npages) * nhb if T >= 16 * G and 4 * R >= G else 0)
+        assert all(e - a <= max(4, -(-run_time // G)) for _, a, e, _ in chunks)
+        for r, a, e, _ in chunks:  # a row's chunks are its last pages
+            assert e <= npages[int(r) // nhb] and a >= npages[int(r) // nhb] - npages[int(r) // nhb] // 16
 
 
 def test_workspace_grows_with_partials():
@@ -395,7 +403,7 @@ def test_partial_slots_are_consecutive_per_merge_row(case):
     plan, _, _ = _decode_plan(**case)
     m = plan.metadata()
     nseg, nparts, nmerge = int(m[7]), int(m[8]), int(m[9])
-    segs = m[m[13]:m[13] + 4 * nseg].reshape(-1, 4)
+    segs = np.concatenate([m[m[13]:m[13] + 4 * nseg].reshape(-1, 4), m[m[23]:m[23] + 4 * m[22]].reshape(-1, 4)])
     mptr = m[m[14]:m[14] + nmerge + 1]
     mrow = m[m[15]:m[15] + nmerge]
     mslot = m[m[16]:m[16] + nparts]

@@ -241,3 +241,36 @@ def test_2byte_cache_serving_size_sampled(cuda_device):
     heads = g.integers(0, b.num_qo_heads, 64)
     ro, rl = oracle_on(b, rows=rows, heads=heads)
     assert_close(o[rows, heads], lse[rows, heads], ro, rl, "serving decode, bf16 cache")
+
+
+def test_serving_workload_repeats_bitwise_with_run_time_chunks(cuda_device):
+    """The serving batch's plan hands part of its pages out at run time from
+    a counter in the workspace (which the last CTA resets); whichever CTA takes
+    a chunk, its partial state is the same, so repeated runs (and a run after
+    the stage-by-stage path) are bit-identical."""
+    b = workload(2)
+    db = DeviceBatch(b, cuda_device)
+    assert int(db.plan.metadata()[22]) > 0  # the plan has run-time chunks
+    db.run()
+    o1, l1 = db.result()
+    for stage_by_stage in (False, True, False):
+        db.o.zero_()
+        db.lse.zero_()
+        if stage_by_stage:
+            db.run(stage=1)
+            db.run(stage=2)
+        else:
+            db.run()
+        o2, l2 = db.result()
+        assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+
+
+def test_more_ctas_than_sms_takes_the_merge_kernel(cuda_device):
+    """With more CTAs than SMs the CTAs cannot all be resident, so the decode
+    kernel does not merge itself (no grid barrier); the merge kernel does."""
+    b = make_batch([3000, 1700, 900, 4096, 37], num_qo_heads=32, num_kv_heads=8, seed=45)
+    sms = torch.cuda.get_device_properties(cuda_device).multi_processor_count
+    for ctas in (sms, 3 * sms):
+        o, lse = run_gpu(b, cuda_device, num_ctas=ctas)
+        ro, rl = oracle_on(b)
+        assert_close(o, lse, ro, rl, f"{ctas} CTAs")
