@@ -751,22 +751,27 @@ def run_ours(args):
     # ---- end to end through the public API, every step: re-plan on the host,
     # upload the plan, one H2D copy of the step's inputs (q and kv_indices
     # packed in one pinned buffer), run, one D2H copy of the result (o and lse
-    # packed in one device buffer) and a synchronize.  The KV cache stays
-    # resident in HBM: it is the state a decode step reads, not an input.
+    # packed in one device buffer) into pinned memory, and the host waits for
+    # that result.  Two steps are in flight (workspaces and buffers double-
+    # buffered): the host plans and launches step i + 1 while the GPU runs
+    # step i, then waits for step i's result.  The KV cache stays resident in
+    # HBM: it is the state a decode step reads, not an input.
     qb = q.numel() * q.element_size()
     ib = idx.numel() * 4
+    ob = o.numel() * o.element_size()
+    lb = lse.numel() * 4
     in_h = torch.empty(qb + ib, dtype=torch.uint8).pin_memory()
     in_h[:qb].copy_(b.q.contiguous().view(-1).view(torch.uint8))
     in_h[qb:].copy_(b.kv_indices.view(torch.uint8))
-    in_d = torch.empty(qb + ib, dtype=torch.uint8, device=dev)
-    q_e = in_d[:qb].view(q.dtype).view(q.shape)
-    idx_e = in_d[qb:].view(torch.int32)
-    ob = o.numel() * o.element_size()
-    lb = lse.numel() * 4
-    out_d = torch.empty(ob + lb, dtype=torch.uint8, device=dev)
-    o_e = out_d[:ob].view(o.dtype).view(o.shape)
-    lse_e = out_d[ob:].view(torch.float32).view(lse.shape)
-    out_h = torch.empty(ob + lb, dtype=torch.uint8).pin_memory()
+    bufs = []
+    for _ in range(2):
+        in_d = torch.empty(qb + ib, dtype=torch.uint8, device=dev)
+        out_d = torch.empty(ob + lb, dtype=torch.uint8, device=dev)
+        bufs.append(dict(
+            ws=torch.empty(plan.workspace_bytes, dtype=torch.uint8, device=dev), in_d=in_d, out_d=out_d,
+            q=in_d[:qb].view(q.dtype).view(q.shape), idx=in_d[qb:].view(torch.int32),
+            o=out_d[:ob].view(o.dtype).view(o.shape), lse=out_d[ob:].view(torch.float32).view(lse.shape),
+            out_h=torch.empty(ob + lb, dtype=torch.uint8).pin_memory(), ev=torch.cuda.Event(), plan=None))
     indptr_h, last_h = b.kv_indptr, b.last_page_len
     h2d = qb + ib + int(meta.size) * 4
     d2h = ob + lb
@@ -777,27 +782,36 @@ def run_ours(args):
                        num_pages=b.num_pages, kv_indptr=indptr_h, last_page_len=last_h,
                        q_dtype=b.q_dtype, kv_dtype=b.kv_dtype, o_dtype=b.o_dtype, sm_scale=b.sm_scale)
 
-    def e2e_step():
-        p2 = new_plan()
-        p2.upload(ws)
-        in_d.copy_(in_h, non_blocking=True)
-        p2.run(q_e, k, v, idx_e, o_e, lse_e, ws, **scales)
-        out_h.copy_(out_d, non_blocking=True)
-        torch.cuda.synchronize()
-        return p2
+    def launch(x):
+        x["plan"] = new_plan()
+        x["plan"].upload(x["ws"])
+        x["in_d"].copy_(in_h, non_blocking=True)
+        x["plan"].run(x["q"], k, v, x["idx"], x["o"], x["lse"], x["ws"], **scales)
+        x["out_h"].copy_(x["out_d"], non_blocking=True)
+        x["ev"].record()
 
-    for _ in range(3):
-        e2e_step()
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    t1 = time.perf_counter()
-    for _ in range(e2e_steps):
-        last_plan = e2e_step()
-    torch.cuda.synchronize()
-    e2e_s = (time.perf_counter() - t1) / e2e_steps
-    last_plan.device_status(ws)
-    e2e_s, = max_over_ranks([e2e_s], dev, world)
+    def e2e_loop(n, in_flight):
+        for i in range(n):
+            launch(bufs[i % in_flight])
+            if in_flight == 1 or i > 0:
+                bufs[(i - in_flight + 1) % in_flight]["ev"].synchronize()  # that step's result is on the host
+        torch.cuda.synchronize()
+
+    e2e = {}
+    for in_flight in (1, 2):
+        e2e_loop(3, in_flight)
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        t1 = time.perf_counter()
+        e2e_loop(e2e_steps, in_flight)
+        e2e[in_flight] = (time.perf_counter() - t1) / e2e_steps
+    for x in bufs:
+        x["plan"].device_status(x["ws"])
+    e2e_s, e2e_serial_s = max_over_ranks([e2e[2], e2e[1]], dev, world)
+    x0 = bufs[0]
+    ws, in_d, out_d, out_h = x0["ws"], x0["in_d"], x0["out_d"], x0["out_h"]
+    q_e, idx_e, o_e, lse_e = x0["q"], x0["idx"], x0["o"], x0["lse"]
     # Where an end-to-end step's time goes: the same calls, each followed by
     # a synchronize and timed on the host (medians over the e2e steps).
     parts = {"plan": [], "upload": [], "h2d": [], "run": [], "d2h": []}
@@ -822,7 +836,7 @@ def run_ours(args):
         torch.cuda.synchronize()
         parts["d2h"].append(time.perf_counter() - t)
     breakdown = {k2: round(statistics.median(v2) * 1e6, 1) for k2, v2 in parts.items()}
-    del flush, in_d, out_d
+    del flush, in_d, out_d, bufs
     torch.cuda.empty_cache()
 
     detail = {}
@@ -877,7 +891,7 @@ def run_ours(args):
                      "peak_kind": peak_kind, "traffic": traffic, "step_frac": step_roof["frac"]},
         "e2e": {"value": round(world * nbytes / e2e_s / 1e9, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_s * 1e3, 4),
-                "breakdown_us": breakdown},
+                "in_flight": 2, "serial_ms_per_step": round(e2e_serial_s * 1e3, 4), "breakdown_us": breakdown},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
     }

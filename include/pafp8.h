@@ -185,9 +185,14 @@ size_t pafp8_workspace_bytes(const pafp8_plan *plan);
 pafp8_status pafp8_plan_metadata(const pafp8_plan *plan, const int32_t **words, size_t *count);
 
 /* Copy the plan's metadata into the head of `workspace` (device memory of at
- * least pafp8_workspace_bytes) on `stream` and clear its status word.  Must
+ * least pafp8_workspace_bytes) on `stream` and clear its status block.  Must
  * precede pafp8_run with this workspace; the plan records the workspace
- * address and pafp8_run refuses any other. */
+ * address and pafp8_run refuses any other.  Outside stream capture the copy
+ * goes through a small page-locked staging ring owned by the library (up to
+ * four buffers per device, allocated on first use and kept until the process
+ * exits; a buffer is reused after the copy that last read it has run), so the
+ * host may destroy or re-plan right after the call; under capture it copies
+ * from the plan's own memory, which must then outlive the graph. */
 pafp8_status pafp8_plan_upload(pafp8_plan *plan, void *workspace, size_t workspace_bytes,
                                void *stream);
 

@@ -18,6 +18,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
 #include <string>
 #include <vector>
 
@@ -635,6 +636,58 @@ pafp8_status encode_decode_maps(CUtensorMap* tk, CUtensorMap* tv, const void* k,
 
 bool scale_ok(float s) { return std::isfinite(s) && s > 0.0f; }
 
+// Page-locked staging ring for metadata uploads, one per device: a copy from
+// page-locked memory is a plain DMA, where one from the plan's pageable
+// memory first goes through a driver bounce buffer.  A slot is reused once
+// the copy that last read it has run (an event recorded after it); slots are
+// allocated, and grow, on first use.  Copies `bytes` from `src` to device
+// `dst` on `s` through the next slot; *done is false when no slot could be
+// used (the caller then copies directly).
+constexpr int kStageSlots = 4;
+struct StageSlot {
+    void* buf = nullptr;
+    size_t cap = 0;
+    cudaEvent_t ev = nullptr;
+    bool pending = false;
+};
+std::mutex g_stage_mu;
+StageSlot g_stage[kMaxDevices][kStageSlots];
+int g_stage_next[kMaxDevices] = {};
+
+cudaError_t staged_copy(void* dst, const void* src, size_t bytes, cudaStream_t s, bool* done) {
+    *done = false;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaSuccess;
+    std::lock_guard<std::mutex> lock(g_stage_mu);
+    StageSlot& sl = g_stage[dev][g_stage_next[dev]];
+    g_stage_next[dev] = (g_stage_next[dev] + 1) % kStageSlots;
+    if (sl.pending && (e = cudaEventSynchronize(sl.ev)) != cudaSuccess) return e;
+    sl.pending = false;
+    if (sl.ev == nullptr && (e = cudaEventCreateWithFlags(&sl.ev, cudaEventDisableTiming)) != cudaSuccess) {
+        sl.ev = nullptr;
+        return e;
+    }
+    if (sl.cap < bytes) {
+        if (sl.buf != nullptr) cudaFreeHost(sl.buf);
+        sl.buf = nullptr;
+        sl.cap = 0;
+        const size_t cap = std::max<size_t>(bytes, 64 << 10);
+        if ((e = cudaHostAlloc(&sl.buf, cap, cudaHostAllocPortable)) != cudaSuccess) {
+            sl.buf = nullptr;
+            return e;
+        }
+        sl.cap = cap;
+    }
+    std::memcpy(sl.buf, src, bytes);
+    if ((e = cudaMemcpyAsync(dst, sl.buf, bytes, cudaMemcpyHostToDevice, s)) != cudaSuccess) return e;
+    *done = true;
+    e = cudaEventRecord(sl.ev, s);
+    sl.pending = e == cudaSuccess;
+    return e;
+}
+
 // Bound of the kernels' pipeline waits: PAFP8_WAIT_CYCLES (a positive integer,
 // SM clock cycles) when set, else about one second.  A diagnostic setting: a
 // short bound makes a pipeline wait expire on purpose, which the kernels
@@ -815,8 +868,16 @@ pafp8_status pafp8_plan_upload(pafp8_plan* plan, void* workspace, size_t workspa
         return fail(PAFP8_ERR_WORKSPACE, "workspace has %zu bytes; the plan needs %zu",
                     workspace_bytes, plan->ws_bytes);
     cudaStream_t s = (cudaStream_t)stream;
-    cudaError_t e = cudaMemcpyAsync(workspace, plan->meta.data(), plan->meta.size() * 4,
-                                    cudaMemcpyHostToDevice, s);
+    const size_t bytes = plan->meta.size() * 4;
+    // Through the page-locked staging ring when the stream is not being
+    // captured (a captured copy would read the staging buffer at replay,
+    // after later uploads reused it); from the plan's own memory otherwise.
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    cudaError_t e = cudaStreamIsCapturing(s, &cap);
+    bool done = false;
+    if (e == cudaSuccess && cap == cudaStreamCaptureStatusNone) e = staged_copy(workspace, plan->meta.data(), bytes, s, &done);
+    if (e == cudaSuccess && !done)
+        e = cudaMemcpyAsync(workspace, plan->meta.data(), bytes, cudaMemcpyHostToDevice, s);
     if (e == cudaSuccess)
         e = cudaMemsetAsync((char*)workspace + plan->status_off, 0, plan->ws_bytes - plan->status_off, s);
     if (e != cudaSuccess) {

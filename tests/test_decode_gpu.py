@@ -274,3 +274,18 @@ def test_more_ctas_than_sms_takes_the_merge_kernel(cuda_device):
         o, lse = run_gpu(b, cuda_device, num_ctas=ctas)
         ro, rl = oracle_on(b)
         assert_close(o, lse, ro, rl, f"{ctas} CTAs")
+
+
+def test_many_uploads_back_to_back(cuda_device):
+    """Plan uploads go through a small page-locked staging ring; more plans
+    than ring slots, uploaded back to back before any run, each keep their own
+    metadata."""
+    batches = [make_batch([17 + 150 * i, 900, 37 * i + 1], num_qo_heads=16, num_kv_heads=4, seed=60 + i)
+               for i in range(7)]
+    dbs = [DeviceBatch(bt, cuda_device, num_ctas=10 + 3 * i) for i, bt in enumerate(batches)]
+    for db in dbs:
+        db.run()
+    for db, bt in zip(dbs, batches):
+        o, lse = db.result()
+        ro, rl = oracle_on(bt)
+        assert_close(o, lse, ro, rl, "upload ring")
