@@ -507,11 +507,13 @@ pafp8_status encode_cache_map(CUtensorMap* map, const void* base, int num_pages,
 // Prefill map over a 2-byte cache: dims (d % 64, d / 64, token, head, page);
 // one box is one page of one KV head for one 64-dim half, {64, 1, 16, 1, 1},
 // landing as 16 swizzled rows of 128 B (one per token).
-pafp8_status encode_cache_map_2byte(CUtensorMap* map, const void* base, int num_pages, int hkv, int layout) {
+pafp8_status encode_cache_map_2byte(CUtensorMap* map, const void* base, int num_pages, int hkv, int layout,
+                                    int head_dim) {
     auto enc = get_encode();
     if (!enc) return fail(PAFP8_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
-    const KvStrides ks = kv_strides(layout, hkv, 2);
-    cuuint64_t dims[5] = {64, 2, (cuuint64_t)kPageSize, (cuuint64_t)hkv, (cuuint64_t)num_pages};
+    const KvStrides ks = kv_strides(layout, hkv, 2, head_dim);
+    cuuint64_t dims[5] = {64, (cuuint64_t)(head_dim / 64), (cuuint64_t)kPageSize, (cuuint64_t)hkv,
+                          (cuuint64_t)num_pages};
     cuuint64_t strides[4] = {128, ks.token, ks.head, ks.page};
     cuuint32_t box[5] = {64, 1, (cuuint32_t)kPageSize, 1, 1};
     cuuint32_t estr[5] = {1, 1, 1, 1, 1};
@@ -526,21 +528,24 @@ pafp8_status encode_cache_map_2byte(CUtensorMap* map, const void* base, int num_
 
 // 3-D map over q [nnz_qo, Hq, D]: dims (d, head, row), innermost first.  One
 // box is the query tile of one KV head: `rows` consecutive new tokens x the
-// group's heads x 64 elements (2-byte q, two boxes per tile) or 128 elements
-// (fp8 q), 128B-swizzled, landing as [rows*group][128 bytes].
+// group's heads x 64 elements (2-byte q, one box per 64-dim half of the tile)
+// or D elements (fp8 q), landing as [rows*group][128 bytes] under the
+// 128-byte swizzle, or [rows*group][64 bytes] under the 64-byte one for an
+// fp8 query of head_dim 64.
 pafp8_status encode_q_map(CUtensorMap* map, const void* base, int nnz_qo, int hq, int group,
-                          int rows, bool fp8) {
+                          int rows, bool fp8, int head_dim) {
     auto enc = get_encode();
     if (!enc) return fail(PAFP8_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
     const cuuint64_t es = fp8 ? 1 : 2;
-    cuuint64_t dims[3] = {(cuuint64_t)kHeadDim, (cuuint64_t)hq, (cuuint64_t)nnz_qo};
-    cuuint64_t strides[2] = {kHeadDim * es, (cuuint64_t)hq * kHeadDim * es};
-    cuuint32_t box[3] = {fp8 ? 128u : 64u, (cuuint32_t)group, (cuuint32_t)rows};
+    cuuint64_t dims[3] = {(cuuint64_t)head_dim, (cuuint64_t)hq, (cuuint64_t)nnz_qo};
+    cuuint64_t strides[2] = {(cuuint64_t)head_dim * es, (cuuint64_t)hq * head_dim * es};
+    cuuint32_t box[3] = {fp8 ? (cuuint32_t)head_dim : 64u, (cuuint32_t)group, (cuuint32_t)rows};
     cuuint32_t estr[3] = {1, 1, 1};
+    const bool rows64 = fp8 && head_dim == 64;
     CUresult r = enc(map, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16, 3,
                      const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                     rows64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS)
         return fail(PAFP8_ERR_CUDA, "cuTensorMapEncodeTiled failed for q (CUresult %d)", (int)r);
     return PAFP8_OK;
@@ -740,10 +745,9 @@ pafp8_status pafp8_plan_create(const pafp8_plan_desc* desc_in, const int32_t* kv
                     "%s serves up to %d query heads per KV head; got %d (%d / %d)",
                     d.mode == PAFP8_MODE_DECODE ? "decode" : "prefill", max_group, group,
                     (int)d.num_qo_heads, (int)d.num_kv_heads);
-    if (d.head_dim != kHeadDim && !(d.head_dim == 64 && d.mode == PAFP8_MODE_DECODE))
-        return fail(PAFP8_ERR_UNSUPPORTED,
-                    "head_dim %d is not served by this library (%d; 64 too in decode)", (int)d.head_dim,
-                    kHeadDim);
+    if (d.head_dim != kHeadDim && d.head_dim != 64)
+        return fail(PAFP8_ERR_UNSUPPORTED, "head_dim %d is not served by this library (%d or 64)",
+                    (int)d.head_dim, kHeadDim);
     if (d.num_pages < 0) return fail(PAFP8_ERR_SHAPE, "num_pages %d is negative", (int)d.num_pages);
     if (d.kv_layout != PAFP8_LAYOUT_NHD && d.kv_layout != PAFP8_LAYOUT_HND)
         return fail(PAFP8_ERR_ARG, "kv_layout %d is neither NHD (0) nor HND (1)", (int)d.kv_layout);
@@ -965,6 +969,7 @@ pafp8_status run_body(const pafp8_plan* plan, int32_t stage, int32_t q_dtype, co
         if (stage == 2 || plan->num_ctas == 0) return PAFP8_OK;  // prefill has no merge stage
         PrefillParams pp{};
         pp.q = q;
+        pp.head_dim = d.head_dim;
         pp.kv_indices = kv_indices;
         pp.o = o;
         pp.lse = lse;
@@ -988,20 +993,24 @@ pafp8_status run_body(const pafp8_plan* plan, int32_t stage, int32_t q_dtype, co
         pp.wait_cycles = wait_cycles();
         CUtensorMap tq, tk, tv;
         if ((st = encode_q_map(&tq, q, (int)plan->nnz_qo, d.num_qo_heads, plan->group,
-                               pp.tile_tokens, is_fp8(q_dtype))) != PAFP8_OK)
+                               pp.tile_tokens, is_fp8(q_dtype), d.head_dim)) != PAFP8_OK)
             return st;
         if (is_2byte(k_dtype)) {
-            if ((st = encode_cache_map_2byte(&tk, k_cache, vpages, d.num_kv_heads, d.kv_layout)) != PAFP8_OK)
+            if ((st = encode_cache_map_2byte(&tk, k_cache, vpages, d.num_kv_heads, d.kv_layout, d.head_dim)) !=
+                PAFP8_OK)
                 return st;
-            if ((st = encode_cache_map_2byte(&tv, v_cache, vpages, d.num_kv_heads, d.kv_layout)) != PAFP8_OK)
+            if ((st = encode_cache_map_2byte(&tv, v_cache, vpages, d.num_kv_heads, d.kv_layout, d.head_dim)) !=
+                PAFP8_OK)
                 return st;
         } else {
-            if ((st = encode_cache_map(&tk, k_cache, vpages, d.num_kv_heads, d.kv_layout)) != PAFP8_OK) return st;
-            if ((st = encode_cache_map(&tv, v_cache, vpages, d.num_kv_heads, d.kv_layout)) != PAFP8_OK) return st;
+            if ((st = encode_cache_map(&tk, k_cache, vpages, d.num_kv_heads, d.kv_layout, d.head_dim)) != PAFP8_OK)
+                return st;
+            if ((st = encode_cache_map(&tv, v_cache, vpages, d.num_kv_heads, d.kv_layout, d.head_dim)) != PAFP8_OK)
+                return st;
         }
         CUtensorMap to;
         if ((st = encode_q_map(&to, o, (int)plan->nnz_qo, d.num_qo_heads, plan->group, pp.tile_tokens,
-                               false)) != PAFP8_OK)
+                               false, d.head_dim)) != PAFP8_OK)
             return st;
         cudaError_t e = launch_prefill(pp, tq, tk, tv, to, plan->num_ctas, s);
         if (e != cudaSuccess) {

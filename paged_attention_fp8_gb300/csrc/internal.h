@@ -137,6 +137,7 @@ struct AppendParams {
 
 struct PrefillParams {
     const void* q;           // [nnz_qo, Hq, D]
+    int head_dim;            // D: 128 or 64
     const int32_t* kv_indices;
     void* o;                 // [nnz_qo, Hq, D]
     float* lse;              // [nnz_qo, Hq] or nullptr

@@ -57,17 +57,29 @@ namespace {
 
 using namespace ptx;
 
-constexpr int D = kHeadDim;
 constexpr int kThreads = 512;  // four warpgroups; warps 14-15 only lend registers
 constexpr uint32_t kTmemCols = 512;
-__device__ __forceinline__ uint32_t col_s(int x) { return 128u * (uint32_t)x; }        // S_X / P_X
-__device__ __forceinline__ uint32_t col_o(int x) { return 256u + 128u * (uint32_t)x; }  // O_X
-constexpr uint32_t kRawTile = kTileKeys * D;      // 16 KB of fp8
 constexpr uint32_t kHalfTile = kTileKeys * 128;  // 16 KB: 128 rows x 128 B
-constexpr uint32_t kF16Tile = 2 * kHalfTile;       // 32 KB of f16
+__device__ __forceinline__ uint32_t col_s(int x) { return 128u * (uint32_t)x; }  // S_X / P_X
 
-template <bool kF8, bool k2 = false>
+// Sizes that depend on the head size DH (128 or 64).  A 2-byte row of DH
+// elements is DH / 64 rows of 128 B ("halves", each under the 128-byte
+// swizzle); an fp8 row is DH bytes (128-byte swizzle for 128, 64-byte for 64).
+template <int DH>
+struct Dims {
+    static constexpr int NH = DH / 64;                       // 128-B halves of a 2-byte row
+    static constexpr uint32_t kRawTile = kTileKeys * DH;      // fp8 K or V tile (128 keys)
+    static constexpr uint32_t kRawPage = kPageSize * DH;      // fp8 page box (16 tokens)
+    static constexpr uint32_t kF16Tile = NH * kHalfTile;      // 2-byte K tile (128 keys) or Q tile
+    static constexpr uint32_t kVtHalf = DH * 128;             // V^T rows (dims) over 64 keys
+    static constexpr uint32_t kVtTile = 2 * kVtHalf;          // V^T tile: dims x 128 keys
+};
+template <int DH>
+__device__ __forceinline__ uint32_t col_o(int x) { return 256u + (uint32_t)DH * (uint32_t)x; }  // O_X
+
+template <bool kF8, bool k2, int DH>
 struct Layout {
+    using Dm = Dims<DH>;
     // The 2-byte-query path spends its shared memory on two f16 K tiles (the
     // dequant of K_{j+1} may start while QK_B(j) still reads K_j) and keeps a
     // single raw fp8 stage per tensor; the fp8 path multiplies raw K directly.
@@ -75,18 +87,18 @@ struct Layout {
     // transposes V, so it has no raw K stage and a 2-byte raw V stage.
     static constexpr int NKR = kF8 ? 4 : (k2 ? 0 : 1);  // raw K stages
     static constexpr int NVR = kF8 ? 2 : 1;             // raw V stages
-    static constexpr uint32_t kRawV = k2 ? kF16Tile : kRawTile;
+    static constexpr uint32_t kRawV = k2 ? Dm::kF16Tile : Dm::kRawTile;
     static constexpr int NK16 = kF8 ? 0 : 2;   // f16 K stages
     static constexpr int NV16 = 2;             // f16 V^T stages
-    static constexpr uint32_t kQTile = kF8 ? kHalfTile : kF16Tile;
+    static constexpr uint32_t kQTile = kF8 ? kTileRows * DH : Dm::kF16Tile;
     static constexpr uint32_t q = 0;                     // Q_A, then Q_B
     static constexpr uint32_t kr = 2 * kQTile;
-    static constexpr uint32_t vr = kr + NKR * kRawTile;
+    static constexpr uint32_t vr = kr + NKR * Dm::kRawTile;
     static constexpr uint32_t k16 = vr + NVR * kRawV;
-    static constexpr uint32_t v16 = k16 + NK16 * kF16Tile;
+    static constexpr uint32_t v16 = k16 + NK16 * Dm::kF16Tile;
     // fp8 query: a 16 KB staging half per query tile for the output's bulk
-    // tensor stores (64 dims of 128 rows, swizzled like the Q tile).
-    static constexpr uint32_t ostage = v16 + NV16 * kF16Tile;
+    // tensor stores (64 dims of 128 rows, 128-byte rows swizzled).
+    static constexpr uint32_t ostage = v16 + NV16 * Dm::kVtTile;
     static constexpr uint32_t bars = ostage + (kF8 ? 2 * kHalfTile : 0);
     // barrier indices (8 bytes each)
     static constexpr int bQFull = 0, bQReady = 1, bQEmpty = 2;
@@ -106,9 +118,16 @@ struct Layout {
     static constexpr uint32_t abort_flag = tmem_slot + 4;
     static constexpr uint32_t bytes = abort_flag + 4;
 };
-static_assert(1024 + Layout<false>::bytes <= 232448, "shared memory budget (2-byte query)");
-static_assert(1024 + Layout<true>::bytes <= 232448, "shared memory budget (fp8 query)");
-static_assert(1024 + Layout<false, true>::bytes <= 232448, "shared memory budget (2-byte cache)");
+static_assert(1024 + Layout<false, false, 128>::bytes <= 232448, "shared memory budget (2-byte query)");
+static_assert(1024 + Layout<true, false, 128>::bytes <= 232448, "shared memory budget (fp8 query)");
+static_assert(1024 + Layout<false, true, 128>::bytes <= 232448, "shared memory budget (2-byte cache)");
+static_assert(1024 + Layout<false, false, 64>::bytes <= 232448, "shared memory budget (2-byte query, D 64)");
+static_assert(1024 + Layout<true, false, 64>::bytes <= 232448, "shared memory budget (fp8 query, D 64)");
+static_assert(1024 + Layout<false, true, 64>::bytes <= 232448, "shared memory budget (2-byte cache, D 64)");
+// Swizzled tiles start on 1024-byte boundaries (the 128-byte swizzle's atom).
+static_assert(Layout<true, false, 64>::kr % 1024 == 0 && Layout<true, false, 64>::v16 % 1024 == 0 &&
+                  Layout<false, false, 64>::v16 % 1024 == 0 && Layout<false, true, 64>::v16 % 1024 == 0,
+              "1024-byte alignment of the D 64 tiles");
 
 struct Ring {
     int idx = 0;
@@ -177,7 +196,7 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, uin
     return true;
 }
 
-template <bool kF8, int KT, bool kDiag>
+template <bool kF8, int KT, bool kDiag, int DH>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_constant__ CUtensorMap tmq,
                    const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
@@ -187,7 +206,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // A bf16 query on an fp8 cache is brought into f16 range (per row, by the
     // softmax warps) before the QK MMAs; every other path multiplies Q as loaded.
     const bool fit_q = !kF8 && !k2 && p.q_dtype == PAFP8_BF16;
-    using L = Layout<kF8, k2>;
+    using L = Layout<kF8, k2, DH>;
+    using Dm = Dims<DH>;
+    constexpr int NH = Dm::NH;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t base = (smem_addr(smem_raw) + 1023u) & ~1023u;
     auto bar = [&](int i) -> uint32_t { return base + L::bars + 8u * (uint32_t)i; };
@@ -264,15 +285,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (ok) {
                     const uint32_t qb = bar(L::bQFull);
                     if (kF8) {
-                        mbar_arrive_expect_tx(qb, (uint32_t)(2 * 128 * g * TQ));
+                        mbar_arrive_expect_tx(qb, (uint32_t)(2 * DH * g * TQ));
                         tma_load_3d(base + L::q, &tmq, qb, 0, it.hk * g, q0);
                         tma_load_3d(base + L::q + L::kQTile, &tmq, qb, 0, it.hk * g, q0 + TQ);
                     } else {
-                        mbar_arrive_expect_tx(qb, (uint32_t)(4 * 128 * g * TQ));
+                        mbar_arrive_expect_tx(qb, (uint32_t)(4 * DH * g * TQ));
                         for (int x = 0; x < 2; ++x) {
                             const uint32_t dst = base + L::q + x * L::kQTile;
-                            tma_load_3d(dst, &tmq, qb, 0, it.hk * g, q0 + x * TQ);
-                            tma_load_3d(dst + kHalfTile, &tmq, qb, 64, it.hk * g, q0 + x * TQ);
+                            for (int h = 0; h < NH; ++h)
+                                tma_load_3d(dst + h * kHalfTile, &tmq, qb, 64 * h, it.hk * g, q0 + x * TQ);
                         }
                     }
                     ++issued_q;
@@ -315,18 +336,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (ok) {
                         const uint32_t fb = bar(bkf + kr.idx);
                         if (k2) {
-                            // Each page as two boxes (dims 0-63, 64-127) into the two
-                            // halves of the 16-bit K tile: [half][key][128 B].
-                            const uint32_t dst = base + L::k16 + kr.idx * kF16Tile;
-                            mbar_arrive_expect_tx(fb, (uint32_t)np * kPageSize * D * 2);
+                            // Each page as one box per 64-dim half into the halves of
+                            // the 16-bit K tile: [half][key][128 B].
+                            const uint32_t dst = base + L::k16 + kr.idx * Dm::kF16Tile;
+                            mbar_arrive_expect_tx(fb, (uint32_t)np * kPageSize * DH * 2);
                             for (int i = 0; i < np; ++i)
-                                for (int h = 0; h < 2; ++h)
+                                for (int h = 0; h < NH; ++h)
                                     tma_load_5d(dst + h * kHalfTile + i * 2048u, &tmk, fb, 0, h, 0, it.hk, pages[i]);
                         } else {
-                            const uint32_t dst = base + L::kr + kr.idx * kRawTile;
-                            mbar_arrive_expect_tx(fb, (uint32_t)np * kPageSize * D);
+                            const uint32_t dst = base + L::kr + kr.idx * Dm::kRawTile;
+                            mbar_arrive_expect_tx(fb, (uint32_t)np * kPageSize * DH);
                             for (int i = 0; i < np; ++i)
-                                tma_load_4d(dst + i * 2048u, &tmk, fb, 0, it.hk, 0, pages[i]);
+                                tma_load_4d(dst + i * Dm::kRawPage, &tmk, fb, 0, it.hk, 0, pages[i]);
                         }
                         ++issued_k;
                     }
@@ -340,14 +361,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint32_t fb = bar(L::bVrFull + vr.idx);
                         const uint32_t dst = base + L::vr + vr.idx * L::kRawV;
                         if (k2) {
-                            mbar_arrive_expect_tx(fb, (uint32_t)np * kPageSize * D * 2);
+                            mbar_arrive_expect_tx(fb, (uint32_t)np * kPageSize * DH * 2);
                             for (int i = 0; i < np; ++i)
-                                for (int h = 0; h < 2; ++h)
+                                for (int h = 0; h < NH; ++h)
                                     tma_load_5d(dst + h * kHalfTile + i * 2048u, &tmv, fb, 0, h, 0, it.hk, pages[i]);
                         } else {
-                            mbar_arrive_expect_tx(fb, (uint32_t)np * kPageSize * D);
+                            mbar_arrive_expect_tx(fb, (uint32_t)np * kPageSize * DH);
                             for (int i = 0; i < np; ++i)
-                                tma_load_4d(dst + i * 2048u, &tmv, fb, 0, it.hk, 0, pages[i]);
+                                tma_load_4d(dst + i * Dm::kRawPage, &tmv, fb, 0, it.hk, 0, pages[i]);
                         }
                         ++issued_v;
                     }
@@ -370,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t idesc_qk =
                 kF8 ? make_idesc(p.q_dtype == PAFP8_E5M2 ? 1 : 0, KT == PAFP8_E5M2 ? 1 : 0, 128, 128)
                     : make_idesc(kBF ? 1 : 0, kBF ? 1 : 0, 128, 128);
-            const uint32_t idesc_pv = make_idesc(kBF ? 1 : 0, kBF ? 1 : 0, 128, 128);
+            const uint32_t idesc_pv = make_idesc(kBF ? 1 : 0, kBF ? 1 : 0, 128, DH);
             const int nk = kF8 ? L::NKR : L::NK16;
             const int kfull = kF8 ? L::bKrFull : L::bK16Full;
             const int kempty = kF8 ? L::bKrEmpty : L::bK16Empty;
@@ -387,16 +408,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // Descriptor offsets are added inside each MMA block (see
                 // tc_mma_*_at): start addresses are 16-byte units.
                 if (kF8) {
-                    const uint64_t dq = sw128_kmajor_desc(qa);
-                    const uint64_t dk = sw128_kmajor_desc(base + L::kr + kring.idx * kRawTile);
+                    // fp8 rows of DH bytes: 128- or 64-byte swizzle, 32 B per K step
+                    const uint64_t dq = DH == 128 ? sw128_kmajor_desc(qa) : sw64_kmajor_desc(qa);
+                    const uint32_t ka = base + L::kr + kring.idx * Dm::kRawTile;
+                    const uint64_t dk = DH == 128 ? sw128_kmajor_desc(ka) : sw64_kmajor_desc(ka);
 #pragma unroll
-                    for (int ks = 0; ks < 4; ++ks)
+                    for (int ks = 0; ks < DH / 32; ++ks)
                         tc_mma_f8_ss_at(dS, dq, dk, (uint32_t)(ks * 32) >> 4, idesc_qk, ks > 0 ? 1u : 0u);
                 } else {
                     const uint64_t dq = sw128_kmajor_desc(qa);
-                    const uint64_t dk = sw128_kmajor_desc(base + L::k16 + kring.idx * kF16Tile);
+                    const uint64_t dk = sw128_kmajor_desc(base + L::k16 + kring.idx * Dm::kF16Tile);
 #pragma unroll
-                    for (int ks = 0; ks < 8; ++ks)
+                    for (int ks = 0; ks < DH / 16; ++ks)
                         tc_mma_f16_ss_at(dS, dq, dk, ((ks >> 2) * kHalfTile + (ks & 3) * 32) >> 4, idesc_qk,
                                          ks > 0 ? 1u : 0u);
                 }
@@ -414,11 +437,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!wait_or_abort<kDiag>(bar(L::bPFull + x), pphase[x], flag_addr, p.status, p.wait_cycles)) return false;
                 pphase[x] ^= 1u;
                 tc_fence_after();
-                const uint64_t dv = sw128_kmajor_desc(base + L::v16 + v16.idx * kF16Tile);
+                const uint64_t dv = sw128_kmajor_desc(base + L::v16 + v16.idx * Dm::kVtTile);
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks)
-                    tc_mma_f16_ts_at(tmem + col_o(x), tmem + col_s(x) + 8 * ks, dv,
-                                     ((ks >> 2) * kHalfTile + (ks & 3) * 32) >> 4, idesc_pv,
+                    tc_mma_f16_ts_at(tmem + col_o<DH>(x), tmem + col_s(x) + 8 * ks, dv,
+                                     ((ks >> 2) * Dm::kVtHalf + (ks & 3) * 32) >> 4, idesc_pv,
                                      (accumulate || ks > 0) ? 1u : 0u);
                 ++issued_any;
                 return true;
@@ -497,19 +520,34 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ok = wait_or_abort<kDiag>(bar(L::bKrFull + kr.idx), kr.phase, flag_addr, p.status, p.wait_cycles) &&
                          wait_or_abort<kDiag>(bar(L::bK16Empty + k16.idx), k16.phase ^ 1u, flag_addr, p.status, p.wait_cycles);
                     if (!ok) break;
-                    const uint32_t src = base + L::kr + kr.idx * kRawTile;
-                    const uint32_t dst = base + L::k16 + k16.idx * kF16Tile;
+                    const uint32_t src = base + L::kr + kr.idx * Dm::kRawTile;
+                    const uint32_t dst = base + L::k16 + k16.idx * Dm::kF16Tile;
+                    if constexpr (DH == 128) {
 #pragma unroll 2
-                    for (int i = 0; i < 8; ++i) {
-                        const int combo = wd * 8 + i;
-                        const int row = (combo >> 1) * 8 + e;
-                        const int c = (combo & 1) * 4 + q8;
-                        const uint4 w = lds128(src + row * 128 + ((c ^ e) << 4));
-                        const uint32_t hb = dst + (c >> 2) * kHalfTile + row * 128;
-                        sts128(hb + (((2 * q8) ^ e) << 4), fp8x2_lo<KT>(w.x), fp8x2_hi<KT>(w.x),
-                               fp8x2_lo<KT>(w.y), fp8x2_hi<KT>(w.y));
-                        sts128(hb + (((2 * q8 + 1) ^ e) << 4), fp8x2_lo<KT>(w.z), fp8x2_hi<KT>(w.z),
-                               fp8x2_lo<KT>(w.w), fp8x2_hi<KT>(w.w));
+                        for (int i = 0; i < 8; ++i) {
+                            const int combo = wd * 8 + i;
+                            const int row = (combo >> 1) * 8 + e;
+                            const int c = (combo & 1) * 4 + q8;
+                            const uint4 w = lds128(src + row * 128 + ((c ^ e) << 4));
+                            const uint32_t hb = dst + (c >> 2) * kHalfTile + row * 128;
+                            sts128(hb + (((2 * q8) ^ e) << 4), fp8x2_lo<KT>(w.x), fp8x2_hi<KT>(w.x),
+                                   fp8x2_lo<KT>(w.y), fp8x2_hi<KT>(w.y));
+                            sts128(hb + (((2 * q8 + 1) ^ e) << 4), fp8x2_lo<KT>(w.z), fp8x2_hi<KT>(w.z),
+                                   fp8x2_lo<KT>(w.w), fp8x2_hi<KT>(w.w));
+                        }
+                    } else {
+                        // 64-B fp8 rows under the 64-byte swizzle (16-byte chunk c of
+                        // row r at c ^ ((r >> 1) & 3)) -> one 128-B f16 half.
+#pragma unroll 2
+                        for (int i = 0; i < 4; ++i) {
+                            const int row = (wd * 4 + i) * 8 + e, c = q8;
+                            const uint4 w = lds128(src + row * 64 + ((c ^ ((row >> 1) & 3)) << 4));
+                            const uint32_t hb = dst + row * 128;
+                            sts128(hb + (((2 * c) ^ e) << 4), fp8x2_lo<KT>(w.x), fp8x2_hi<KT>(w.x),
+                                   fp8x2_lo<KT>(w.y), fp8x2_hi<KT>(w.y));
+                            sts128(hb + (((2 * c + 1) ^ e) << 4), fp8x2_lo<KT>(w.z), fp8x2_hi<KT>(w.z),
+                                   fp8x2_lo<KT>(w.w), fp8x2_hi<KT>(w.w));
+                        }
                     }
                     fence_async_smem();
                     mbar_arrive(bar(L::bK16Full + k16.idx));
@@ -521,16 +559,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                      wait_or_abort<kDiag>(bar(L::bV16Empty + v16.idx), v16.phase ^ 1u, flag_addr, p.status, p.wait_cycles);
                 if (!ok) break;
                 const uint32_t src = base + L::vr + vr.idx * L::kRawV;
-                const uint32_t dst = base + L::v16 + v16.idx * kF16Tile;
+                const uint32_t dst = base + L::v16 + v16.idx * Dm::kVtTile;
                 if constexpr (k2) {
                     // 16-bit V [half][key][128 B] -> V^T [key half][dim][128 B], by
                     // 8x8 tiles (8 keys x 8 dims) transposed in ldmatrix: warp wd
                     // takes key blocks 4wd .. 4wd+3, all 16 dim blocks; keys past the
                     // request's end are zeroed.
+                    // (DH / 32 ldmatrix groups of 4 dim blocks per key block.)
+                    constexpr int kGroups = DH / 32;
                     const int tr = lane & 7, tm = lane >> 3;
 #pragma unroll 1
-                    for (int ab = 0; ab < 16; ++ab) {
-                        const int a = 4 * wd + (ab >> 2), b = 4 * (ab & 3) + tm;  // this lane's source tile
+                    for (int ab = 0; ab < 4 * kGroups; ++ab) {
+                        const int a = 4 * wd + ab / kGroups, gq = ab % kGroups;
+                        const int b = 4 * gq + tm;  // this lane's source tile
                         const int key_row = 8 * a + tr;
                         uint32_t w[4];
                         ldsm_x4_trans(src + (b >> 3) * kHalfTile + key_row * 128 + (((b & 7) ^ tr) << 4), w[0], w[1],
@@ -538,26 +579,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const int k0 = 8 * a + 2 * (lane & 3);  // keys k0, k0+1 of word m
 #pragma unroll
                         for (int m = 0; m < 4; ++m) {
-                            const int bm = 4 * (ab & 3) + m;
+                            const int bm = 4 * gq + m;
                             const int dim = 8 * bm + (lane >> 2);
                             uint32_t x = w[m];
                             if (k0 >= valid) x &= 0xFFFF0000u;
                             if (k0 + 1 >= valid) x &= 0x0000FFFFu;
-                            sts32(dst + (a >> 3) * kHalfTile + dim * 128 + (((a & 7) ^ (dim & 7)) << 4) + 4 * (lane & 3),
+                            sts32(dst + (a >> 3) * Dm::kVtHalf + dim * 128 + (((a & 7) ^ (dim & 7)) << 4) +
+                                      4 * (lane & 3),
                                   x);
                         }
                     }
                 } else {
                 const int kb = e + 8 * (q8 >> 1);  // key block (8 keys)
+                // DH / 64 rounds: the (key block, dim block) pairs, 8 x 8 each.
 #pragma unroll 1
-                for (int rr = 0; rr < 2; ++rr) {
-                    const int rot = 2 * wd + rr;
-                    const int a = (q8 & 1) * 8 + ((e + rot) & 7);  // dim block (8 dims)
+                for (int rr = 0; rr < DH / 64; ++rr) {
+                    const int a = DH == 128 ? (q8 & 1) * 8 + ((e + 2 * wd + rr) & 7)  // dim block (8 dims)
+                                            : (q8 & 1) * 4 + ((e + wd) & 3);
                     uint32_t w0[8], w1[8];
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
                         const int row = kb * 8 + i;
-                        const uint2 v = lds64(src + row * 128 + ((((a >> 1) ^ i) << 4)) + (a & 1) * 8);
+                        // 128-B rows (128-byte swizzle, row & 7 = i) or 64-B rows
+                        // (64-byte swizzle: chunk c of row r at c ^ ((r >> 1) & 3))
+                        const uint2 v = DH == 128
+                                            ? lds64(src + row * 128 + ((((a >> 1) ^ i) << 4)) + (a & 1) * 8)
+                                            : lds64(src + row * 64 + ((((a >> 1) ^ ((row >> 1) & 3)) << 4)) + (a & 1) * 8);
                         const bool live = row < valid;
                         w0[i] = live ? v.x : 0u;
                         w1[i] = live ? v.y : 0u;
@@ -579,7 +626,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         T[6][k] = fp8x2_lo<KT>(y1);
                         T[7][k] = fp8x2_hi<KT>(y1);
                     }
-                    const uint32_t hb = dst + (kb >> 3) * kHalfTile;
+                    const uint32_t hb = dst + (kb >> 3) * Dm::kVtHalf;
 #pragma unroll
                     for (int d = 0; d < 8; ++d) {
                         const int row = a * 8 + d;
@@ -600,7 +647,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int x = warp < 8 ? 0 : 1;        // query tile A or B
         const int r = threadIdx.x - 128 * (1 + x);  // row of the tile = TMEM lane
         const uint32_t lane_base = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
-        const uint32_t tS = lane_base + col_s(x), tO = lane_base + col_o(x);
+        const uint32_t tS = lane_base + col_s(x), tO = lane_base + col_o<DH>(x);
         uint32_t qphase = 0, sphase = 0, ophase = 0;
         uint32_t stage_round = 0;  // staging rounds of this tile so far (fp8 query)
         const bool issuer = (threadIdx.x & 127) == 0;
@@ -619,7 +666,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t qrow = base + L::q + x * L::kQTile + r * 128;
                 uint32_t mx = 0;
 #pragma unroll
-                for (int c = 0; c < 16; ++c) {
+                for (int c = 0; c < 8 * NH; ++c) {
                     const uint4 w = lds128(qrow + (c >> 3) * kHalfTile + (((c & 7) ^ (r & 7)) << 4));
                     const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
@@ -633,7 +680,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float down = __int_as_float((127 - shift) << 23);
                 up = __int_as_float((127 + shift) << 23);
 #pragma unroll 4
-                for (int c = 0; c < 16; ++c) {
+                for (int c = 0; c < 8 * NH; ++c) {
                     const uint32_t a = qrow + (c >> 3) * kHalfTile + (((c & 7) ^ (r & 7)) << 4);
                     const uint4 w = lds128(a);
                     const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
@@ -721,7 +768,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const f32x2 alpha2 = make_f32x2(alpha, alpha);
                     l *= alpha;
 #pragma unroll 1
-                    for (int c = 0; c < 4; ++c) {
+                    for (int c = 0; c < DH / 32; ++c) {
                         uint32_t v[32];
                         tc_ld32(tO + 32 * c, v);
                         tc_wait_ld();
@@ -790,12 +837,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t stg = base + L::ostage + (uint32_t)x * kHalfTile;
                 bool sok = true;
 #pragma unroll 1
-                for (int h = 0; h < 2 && sok; ++h, ++stage_round) {
+                for (int h = 0; h < NH && sok; ++h, ++stage_round) {
                     uint32_t v[64];
                     tc_ld32(tO + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(v));
                     tc_ld32(tO + 64 * h + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
                     tc_wait_ld();
-                    if (h == 1) {
+                    if (h == NH - 1) {
                         // O_X is read: release it to the next item's first PV.
                         tc_fence_before();
                         mbar_arrive(bar(L::bOEmpty + x));
@@ -836,7 +883,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 continue;
             }
 #pragma unroll 1
-            for (int c = 0; c < 4; ++c) {
+            for (int c = 0; c < DH / 32; ++c) {
                 uint32_t v[32];
                 tc_ld32(tO + 32 * c, v);
                 tc_wait_ld();
@@ -850,7 +897,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     a, b);
                         w[i] = pack_out2(a, b, p.o_dtype);
                     }
-                    uint16_t* dst = static_cast<uint16_t*>(p.o) + orow * D + 32 * c;
+                    uint16_t* dst = static_cast<uint16_t*>(p.o) + orow * DH + 32 * c;
                     if (o_32b) {
                         // 32-byte stores: every access fills whole sectors.
                         stg256(dst, w);
@@ -877,14 +924,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <bool kF8, int KT, bool kDiag>
+template <bool kF8, int KT, bool kDiag, int DH>
 cudaError_t launch_t(const PrefillParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
                      const CUtensorMap& tv, const CUtensorMap& to, int num_ctas, cudaStream_t stream) {
-    const size_t smem = 1024 + Layout<kF8, KT == PAFP8_F16 || KT == PAFP8_BF16>::bytes;
-    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<kF8, KT, kDiag>,
+    const size_t smem = 1024 + Layout<kF8, KT == PAFP8_F16 || KT == PAFP8_BF16, DH>::bytes;
+    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<kF8, KT, kDiag, DH>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    prefill_kernel<kF8, KT, kDiag><<<num_ctas, kThreads, smem, stream>>>(p, tq, tk, tv, to);
+    prefill_kernel<kF8, KT, kDiag, DH><<<num_ctas, kThreads, smem, stream>>>(p, tq, tk, tv, to);
     return cudaGetLastError();
 }
 
@@ -892,8 +939,12 @@ cudaError_t launch_t(const PrefillParams& p, const CUtensorMap& tq, const CUtens
 template <bool kF8, int KT>
 cudaError_t launch_one(const PrefillParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
                        const CUtensorMap& tv, const CUtensorMap& to, int num_ctas, cudaStream_t stream) {
-    if (p.wait_cycles < kWaitCyclesDefault) return launch_t<kF8, KT, true>(p, tq, tk, tv, to, num_ctas, stream);
-    return launch_t<kF8, KT, false>(p, tq, tk, tv, to, num_ctas, stream);
+    const bool diag = p.wait_cycles < kWaitCyclesDefault;
+    if (p.head_dim == 64)
+        return diag ? launch_t<kF8, KT, true, 64>(p, tq, tk, tv, to, num_ctas, stream)
+                    : launch_t<kF8, KT, false, 64>(p, tq, tk, tv, to, num_ctas, stream);
+    return diag ? launch_t<kF8, KT, true, 128>(p, tq, tk, tv, to, num_ctas, stream)
+                : launch_t<kF8, KT, false, 128>(p, tq, tk, tv, to, num_ctas, stream);
 }
 
 }  // namespace

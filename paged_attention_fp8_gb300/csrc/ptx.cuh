@@ -339,6 +339,18 @@ __device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t saddr) {
     return d;
 }
 
+// The same for 64-byte rows under the 64-byte swizzle (an fp8 row of 64
+// elements): 8-row atoms of 512 bytes, layout type 4 (SWIZZLE_64B).
+__device__ __forceinline__ uint64_t sw64_kmajor_desc(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)1 << 16;            // leading byte offset (unused), 16 B
+    d |= (uint64_t)(512 >> 4) << 32;   // stride byte offset: 8 rows x 64 B
+    d |= (uint64_t)1 << 46;            // descriptor version
+    d |= (uint64_t)4 << 61;            // SWIZZLE_64B
+    return d;
+}
+
 // Instruction descriptor: f32 accumulator, K-major A and B, M x N.
 // a_fmt/b_fmt: kind::f16 -> 0 f16, 1 bf16; kind::f8f6f4 -> 0 e4m3, 1 e5m2.
 __host__ __device__ constexpr uint32_t make_idesc(int a_fmt, int b_fmt, int m, int n) {

@@ -191,7 +191,7 @@ def test_plan_refuses_o_dtype(o, word):
 
 
 @pytest.mark.parametrize("over,status", [
-    (dict(num_qo_heads=6, num_kv_heads=4), 2), (dict(head_dim=96), 8), (dict(head_dim=64, mode=1), 8), (dict(page_size=24), 8),
+    (dict(num_qo_heads=6, num_kv_heads=4), 2), (dict(head_dim=96), 8), (dict(head_dim=32), 8), (dict(page_size=24), 8),
     (dict(page_size=32, kv_layout=1), 8), (dict(page_size=0), 8),
     (dict(num_qo_heads=32, num_kv_heads=2), 8), (dict(mode=5), 3), (dict(num_ctas=-1), 3),
     (dict(fixed_split_pages=-2), 3), (dict(sm_scale=float("nan")), 3), (dict(kv_layout=2), 3)])
@@ -199,6 +199,14 @@ def test_plan_refuses_shapes_and_args(over, status):
     with pytest.raises(pa.Pafp8Error) as ei:
         _create(**over)
     assert ei.value.status == status and len(str(ei.value)) > 20
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+@pytest.mark.parametrize("d", [64, 128])
+def test_plan_accepts_both_head_sizes_in_both_modes(mode, d):
+    qo = np.array([0, 3], np.int32) if mode == 1 else None
+    h = pa.pafp8_plan_create(_desc(mode=mode, head_dim=d), np.array([0, 2], np.int32), np.array([5], np.int32), qo)
+    pa.pafp8_plan_destroy(h)
 
 
 def test_plan_refuses_bad_page_table():
