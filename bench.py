@@ -177,7 +177,7 @@ def time_prefill(index, dev, steps, warmup):
     ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
     tflops = flops / (ms * 1e-3) / 1e12
     p16, kind = measured_bf16_tflops()
-    traffic = NCU_TRAFFIC_PREFILL.get(kernel_sha("prefill.cu"), {}).get(index)
+    traffic = NCU_TRAFFIC_PREFILL.get(kernel_sha("prefill.cuh"), {}).get(index)
     fp8 = b.q_dtype in ("e4m3fn", "e5m2")
     out = {"workload": WORKLOADS[index], "value": round(tflops, 2), "unit": "TFLOP/s",
            "ms_per_launch": round(ms, 5), "flops": flops, "launches": steps,

@@ -93,8 +93,8 @@ enum { PAFP8_MODE_DECODE = 0, PAFP8_MODE_PREFILL = 1 };
 enum { PAFP8_LAYOUT_NHD = 0, PAFP8_LAYOUT_HND = 1 };
 
 /* Static description of one batch.  Shapes served by this library:
- * head_dim 128, or 64 in decode; page_size a multiple of 16 (NHD) or 16 (HND), a page of
- * 16 m tokens being read as m consecutive 16-token sub-pages (so
+ * head_dim 128 or 64; page_size a multiple of 16 in either layout, a page of 16 m tokens
+ * being read as m 16-token sub-pages (token slots 16 j .. 16 j + 15 of every head, so
  * num_pages * page_size / 16 must stay below 2^31); num_qo_heads a multiple of num_kv_heads with
  * group size num_qo_heads/num_kv_heads <= 8 (decode) or <= 16 (prefill).
  *

@@ -304,7 +304,7 @@ def pafp8_append_kv(k_new, v_new, batch_indices, positions, kv_indptr, kv_indice
 
 class Plan:
     """Owns one pafp8_plan.  Shapes served: head_dim 128 (or 64 in decode),
-    page_size a multiple of 16 (NHD) or 16 (HND)."""
+    page_size a multiple of 16 in either layout."""
 
     def __init__(self, *, mode: str, num_qo_heads: int, num_kv_heads: int, num_pages: int,
                  kv_indptr, last_page_len, qo_indptr=None, q_dtype, kv_dtype, o_dtype=None,

@@ -415,13 +415,17 @@ __global__ void __launch_bounds__(32 * 9, 1)
             const int* idx = p.kv_indices + req_page[b];
             for (int pb = p0; pb < p1 && ok; pb += 32) {
                 const int n = min(32, p1 - pb);
-                // Pool ids of 16-token sub-pages (a page of 16 * m tokens is m of
-                // them); an id outside the pool reads page 0 instead.
+                // Pool pages and token slots of 16-token sub-pages (a page of
+                // 16 * m tokens is m of them); an id outside the pool reads page
+                // 0 instead.
                 bool bad = false;
-                const int page = lane < n ? sub_page(idx, pb + lane, p.page_mult, p.num_pages, bad) : 0;
+                const SubPageAt sp =
+                    lane < n ? sub_page(idx, pb + lane, p.page_mult, p.num_pages, bad) : SubPageAt{0, 0};
                 if (__any_sync(0xFFFFFFFFu, bad) && lane == 0) flag(p.status, kStatusBounds);
                 for (int j = 0; j < n; ++j) {
-                    const int pg = __shfl_sync(0xFFFFFFFFu, page, j);
+                    SubPageAt at;
+                    at.page = __shfl_sync(0xFFFFFFFFu, sp.page, j);
+                    at.slot = p.page_mult == 1 ? 0 : __shfl_sync(0xFFFFFFFFu, sp.slot, j);
                     if (lane == 0) {
                         if (!pipe_wait<kDiag>(bar_empty + 8u * stage, phase ^ 1u, p.wait_cycles)) {
                             ok = false;
@@ -434,23 +438,25 @@ __global__ void __launch_bounds__(32 * 9, 1)
                                 // (d % 64, d / 64, token, head, page) or, per head,
                                 // (d % 64, d / 64, head, token, page)
                                 if (heads_per_box == hpc) {
-                                    tma_load_5d(sk, &tmk, fb, 0, 0, 0, hb * hpc, pg);
-                                    tma_load_5d(sv, &tmv, fb, 0, 0, 0, hb * hpc, pg);
+                                    tma_load_5d(sk, &tmk, fb, 0, 0, at.slot, hb * hpc, at.page);
+                                    tma_load_5d(sv, &tmv, fb, 0, 0, at.slot, hb * hpc, at.page);
                                 } else {
                                     for (int h = 0; h < hpc; ++h) {
-                                        tma_load_5d(sk + h * kTileBytes, &tmk, fb, 0, 0, hb * hpc + h, 0, pg);
-                                        tma_load_5d(sv + h * kTileBytes, &tmv, fb, 0, 0, hb * hpc + h, 0, pg);
+                                        tma_load_5d(sk + h * kTileBytes, &tmk, fb, 0, 0, hb * hpc + h, at.slot,
+                                                    at.page);
+                                        tma_load_5d(sv + h * kTileBytes, &tmv, fb, 0, 0, hb * hpc + h, at.slot,
+                                                    at.page);
                                     }
                                 }
                             } else if (heads_per_box == hpc) {
                                 // one box = every head of the block: (d, token, head, page)
-                                tma_load_4d(sk, &tmk, fb, 0, 0, hb * hpc, pg);
-                                tma_load_4d(sv, &tmv, fb, 0, 0, hb * hpc, pg);
+                                tma_load_4d(sk, &tmk, fb, 0, at.slot, hb * hpc, at.page);
+                                tma_load_4d(sv, &tmv, fb, 0, at.slot, hb * hpc, at.page);
                             } else {
                                 // one box per head: (d, head, token, page)
                                 for (int h = 0; h < hpc; ++h) {
-                                    tma_load_4d(sk + h * kTileBytes, &tmk, fb, 0, hb * hpc + h, 0, pg);
-                                    tma_load_4d(sv + h * kTileBytes, &tmv, fb, 0, hb * hpc + h, 0, pg);
+                                    tma_load_4d(sk + h * kTileBytes, &tmk, fb, 0, hb * hpc + h, at.slot, at.page);
+                                    tma_load_4d(sv + h * kTileBytes, &tmv, fb, 0, hb * hpc + h, at.slot, at.page);
                                 }
                             }
                             ++issued;

@@ -466,15 +466,18 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
 
 // Byte strides of a cache tensor [num_pages, page_size, Hkv, D] (NHD) or
 // [num_pages, Hkv, page_size, D] (HND) with esz-byte elements.  Every TMA map
-// below names the same dimensions (dims, token, head, page) and only these
-// strides differ, so the boxes land in shared memory the same way for both.
+// below names the same dimensions (dims, token slot, head, page) and only
+// these strides differ, so the boxes land in shared memory the same way for
+// both.  The token-slot dimension spans the whole page (page_size slots); a
+// box covers 16 of them, and the kernels address the 16-token sub-page j of a
+// page by the slot coordinate 16 j.
 struct KvStrides {
     cuuint64_t token, head, page;
 };
-KvStrides kv_strides(int layout, int hkv, int esz, int head_dim = kHeadDim) {
+KvStrides kv_strides(int layout, int hkv, int esz, int head_dim, int page_size) {
     const cuuint64_t row = (cuuint64_t)head_dim * esz;
-    const cuuint64_t page = (cuuint64_t)kPageSize * hkv * row;
-    if (layout == PAFP8_LAYOUT_HND) return KvStrides{row, (cuuint64_t)kPageSize * row, page};
+    const cuuint64_t page = (cuuint64_t)page_size * hkv * row;
+    if (layout == PAFP8_LAYOUT_HND) return KvStrides{row, (cuuint64_t)page_size * row, page};
     return KvStrides{(cuuint64_t)hkv * row, row, page};
 }
 
@@ -485,11 +488,11 @@ KvStrides kv_strides(int layout, int hkv, int esz, int head_dim = kHeadDim) {
 // swizzle (16-byte chunk c of token row t stored at c ^ (t & 7)), or the
 // 64-byte one for 64-byte rows.
 pafp8_status encode_cache_map(CUtensorMap* map, const void* base, int num_pages, int hkv, int layout,
-                              int head_dim = kHeadDim) {
+                              int head_dim, int page_size) {
     auto enc = get_encode();
     if (!enc) return fail(PAFP8_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
-    const KvStrides ks = kv_strides(layout, hkv, 1, head_dim);
-    cuuint64_t dims[4] = {(cuuint64_t)head_dim, (cuuint64_t)hkv, (cuuint64_t)kPageSize,
+    const KvStrides ks = kv_strides(layout, hkv, 1, head_dim, page_size);
+    cuuint64_t dims[4] = {(cuuint64_t)head_dim, (cuuint64_t)hkv, (cuuint64_t)page_size,
                           (cuuint64_t)num_pages};
     cuuint64_t strides[3] = {ks.head, ks.token, ks.page};
     cuuint32_t box[4] = {(cuuint32_t)head_dim, 1, (cuuint32_t)kPageSize, 1};
@@ -508,11 +511,11 @@ pafp8_status encode_cache_map(CUtensorMap* map, const void* base, int num_pages,
 // one box is one page of one KV head for one 64-dim half, {64, 1, 16, 1, 1},
 // landing as 16 swizzled rows of 128 B (one per token).
 pafp8_status encode_cache_map_2byte(CUtensorMap* map, const void* base, int num_pages, int hkv, int layout,
-                                    int head_dim) {
+                                    int head_dim, int page_size) {
     auto enc = get_encode();
     if (!enc) return fail(PAFP8_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
-    const KvStrides ks = kv_strides(layout, hkv, 2, head_dim);
-    cuuint64_t dims[5] = {64, (cuuint64_t)(head_dim / 64), (cuuint64_t)kPageSize, (cuuint64_t)hkv,
+    const KvStrides ks = kv_strides(layout, hkv, 2, head_dim, page_size);
+    cuuint64_t dims[5] = {64, (cuuint64_t)(head_dim / 64), (cuuint64_t)page_size, (cuuint64_t)hkv,
                           (cuuint64_t)num_pages};
     cuuint64_t strides[4] = {128, ks.token, ks.head, ks.page};
     cuuint32_t box[5] = {64, 1, (cuuint32_t)kPageSize, 1, 1};
@@ -563,14 +566,14 @@ pafp8_status encode_q_map(CUtensorMap* map, const void* base, int nnz_qo, int hq
 // d / 64, head, token, page) and the same layout.
 pafp8_status encode_decode_maps_2byte(CUtensorMap* tk, CUtensorMap* tv, const void* k, const void* v,
                                       int num_pages, int hkv, int hpc, int* heads_per_box, int layout,
-                                      int head_dim) {
+                                      int head_dim, int page_size) {
     auto enc = get_encode();
     if (!enc) return fail(PAFP8_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
-    const KvStrides ks = kv_strides(layout, hkv, 2, head_dim);
+    const KvStrides ks = kv_strides(layout, hkv, 2, head_dim, page_size);
     const cuuint32_t halves = (cuuint32_t)(head_dim / 64);  // 128-B halves of a row
     cuuint32_t estr[5] = {1, 1, 1, 1, 1};
     {
-        cuuint64_t dims[5] = {64, halves, (cuuint64_t)kPageSize, (cuuint64_t)hkv, (cuuint64_t)num_pages};
+        cuuint64_t dims[5] = {64, halves, (cuuint64_t)page_size, (cuuint64_t)hkv, (cuuint64_t)num_pages};
         cuuint64_t strides[4] = {128, ks.token, ks.head, ks.page};
         cuuint32_t box[5] = {64, halves, (cuuint32_t)kPageSize, (cuuint32_t)hpc, 1};
         CUresult rk = enc(tk, CU_TENSOR_MAP_DATA_TYPE_UINT16, 5, const_cast<void*>(k), dims, strides, box, estr,
@@ -584,7 +587,7 @@ pafp8_status encode_decode_maps_2byte(CUtensorMap* tk, CUtensorMap* tv, const vo
             return PAFP8_OK;
         }
     }
-    cuuint64_t dims[5] = {64, halves, (cuuint64_t)hkv, (cuuint64_t)kPageSize, (cuuint64_t)num_pages};
+    cuuint64_t dims[5] = {64, halves, (cuuint64_t)hkv, (cuuint64_t)page_size, (cuuint64_t)num_pages};
     cuuint64_t strides[4] = {128, ks.head, ks.token, ks.page};
     cuuint32_t box[5] = {64, halves, 1, (cuuint32_t)kPageSize, 1};
     CUresult rk = enc(tk, CU_TENSOR_MAP_DATA_TYPE_UINT16, 5, const_cast<void*>(k), dims, strides, box, estr,
@@ -602,7 +605,7 @@ pafp8_status encode_decode_maps_2byte(CUtensorMap* tk, CUtensorMap* tv, const vo
 
 pafp8_status encode_decode_maps(CUtensorMap* tk, CUtensorMap* tv, const void* k, const void* v,
                                 int num_pages, int hkv, int hpc, int* heads_per_box, bool two_byte, int layout,
-                                int head_dim) {
+                                int head_dim, int page_size) {
     if (num_pages == 0 || k == nullptr || v == nullptr) {
         // No request has pages: the kernel issues no copy, the maps are unused.
         memset(tk, 0, sizeof(*tk));
@@ -611,13 +614,14 @@ pafp8_status encode_decode_maps(CUtensorMap* tk, CUtensorMap* tv, const void* k,
         return PAFP8_OK;
     }
     if (two_byte)
-        return encode_decode_maps_2byte(tk, tv, k, v, num_pages, hkv, hpc, heads_per_box, layout, head_dim);
+        return encode_decode_maps_2byte(tk, tv, k, v, num_pages, hkv, hpc, heads_per_box, layout, head_dim,
+                                        page_size);
     auto enc = get_encode();
     if (!enc) return fail(PAFP8_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
-    const KvStrides ks = kv_strides(layout, hkv, 1, head_dim);
+    const KvStrides ks = kv_strides(layout, hkv, 1, head_dim, page_size);
     // 128-B rows take the 128-byte swizzle, 64-B rows (head_dim 64) the 64-byte one.
     const CUtensorMapSwizzle swz = head_dim == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
-    cuuint64_t dims[4] = {(cuuint64_t)head_dim, (cuuint64_t)kPageSize, (cuuint64_t)hkv,
+    cuuint64_t dims[4] = {(cuuint64_t)head_dim, (cuuint64_t)page_size, (cuuint64_t)hkv,
                           (cuuint64_t)num_pages};
     cuuint64_t strides[3] = {ks.token, ks.head, ks.page};
     cuuint32_t box[4] = {(cuuint32_t)head_dim, (cuuint32_t)kPageSize, (cuuint32_t)hpc, 1};
@@ -633,8 +637,8 @@ pafp8_status encode_decode_maps(CUtensorMap* tk, CUtensorMap* tv, const void* k,
         return PAFP8_OK;
     }
     pafp8_status st;
-    if ((st = encode_cache_map(tk, k, num_pages, hkv, layout, head_dim)) != PAFP8_OK) return st;
-    if ((st = encode_cache_map(tv, v, num_pages, hkv, layout, head_dim)) != PAFP8_OK) return st;
+    if ((st = encode_cache_map(tk, k, num_pages, hkv, layout, head_dim, page_size)) != PAFP8_OK) return st;
+    if ((st = encode_cache_map(tv, v, num_pages, hkv, layout, head_dim, page_size)) != PAFP8_OK) return st;
     *heads_per_box = 1;
     return PAFP8_OK;
 }
@@ -757,11 +761,6 @@ pafp8_status pafp8_plan_create(const pafp8_plan_desc* desc_in, const int32_t* kv
                     "page_size %d is not served by this library (a multiple of %d tokens, with "
                     "num_pages * page_size / %d below 2^31)",
                     (int)d.page_size, kPageSize, kPageSize);
-    if (d.page_size != kPageSize && d.kv_layout == PAFP8_LAYOUT_HND)
-        return fail(PAFP8_ERR_UNSUPPORTED,
-                    "the HND layout is served with page_size %d only (got %d); NHD takes any "
-                    "multiple of %d",
-                    kPageSize, (int)d.page_size, kPageSize);
     if (std::isnan(d.sm_scale) || std::isinf(d.sm_scale))
         return fail(PAFP8_ERR_ARG, "sm_scale is not finite");
     if (d.sm_scale <= 0.0f) d.sm_scale = 1.0f / std::sqrt((float)d.head_dim);
@@ -964,7 +963,6 @@ pafp8_status run_body(const pafp8_plan* plan, int32_t stage, int32_t q_dtype, co
     char* ws = (char*)workspace;
     const float sm_log2 = (float)((double)d.sm_scale * (is_fp8(q_dtype) ? (double)q_scale : 1.0) *
                                   (double)k_scale * 1.4426950408889634);
-    const int vpages = d.num_pages * plan->page_mult;  // 16-token sub-pages of the pool
     if (d.mode == PAFP8_MODE_PREFILL) {
         if (stage == 2 || plan->num_ctas == 0) return PAFP8_OK;  // prefill has no merge stage
         PrefillParams pp{};
@@ -996,16 +994,20 @@ pafp8_status run_body(const pafp8_plan* plan, int32_t stage, int32_t q_dtype, co
                                pp.tile_tokens, is_fp8(q_dtype), d.head_dim)) != PAFP8_OK)
             return st;
         if (is_2byte(k_dtype)) {
-            if ((st = encode_cache_map_2byte(&tk, k_cache, vpages, d.num_kv_heads, d.kv_layout, d.head_dim)) !=
+            if ((st = encode_cache_map_2byte(&tk, k_cache, d.num_pages, d.num_kv_heads, d.kv_layout, d.head_dim,
+                                             d.page_size)) !=
                 PAFP8_OK)
                 return st;
-            if ((st = encode_cache_map_2byte(&tv, v_cache, vpages, d.num_kv_heads, d.kv_layout, d.head_dim)) !=
+            if ((st = encode_cache_map_2byte(&tv, v_cache, d.num_pages, d.num_kv_heads, d.kv_layout, d.head_dim,
+                                             d.page_size)) !=
                 PAFP8_OK)
                 return st;
         } else {
-            if ((st = encode_cache_map(&tk, k_cache, vpages, d.num_kv_heads, d.kv_layout, d.head_dim)) != PAFP8_OK)
+            if ((st = encode_cache_map(&tk, k_cache, d.num_pages, d.num_kv_heads, d.kv_layout, d.head_dim,
+                                       d.page_size)) != PAFP8_OK)
                 return st;
-            if ((st = encode_cache_map(&tv, v_cache, vpages, d.num_kv_heads, d.kv_layout, d.head_dim)) != PAFP8_OK)
+            if ((st = encode_cache_map(&tv, v_cache, d.num_pages, d.num_kv_heads, d.kv_layout, d.head_dim,
+                                       d.page_size)) != PAFP8_OK)
                 return st;
         }
         CUtensorMap to;
@@ -1048,8 +1050,9 @@ pafp8_status run_body(const pafp8_plan* plan, int32_t stage, int32_t q_dtype, co
     if (stage != 2 && plan->num_ctas > 0) {
         CUtensorMap tk, tv;
         int hpb = 1;
-        if ((st = encode_decode_maps(&tk, &tv, k_cache, v_cache, vpages, d.num_kv_heads,
-                                     plan->heads_per_cta, &hpb, is_2byte(k_dtype), d.kv_layout, d.head_dim)) != PAFP8_OK)
+        if ((st = encode_decode_maps(&tk, &tv, k_cache, v_cache, d.num_pages, d.num_kv_heads,
+                                     plan->heads_per_cta, &hpb, is_2byte(k_dtype), d.kv_layout, d.head_dim,
+                                     d.page_size)) != PAFP8_OK)
             return st;
         e = launch_decode(p, tk, tv, plan->num_ctas, plan->heads_per_cta, plan->group, hpb, s);
     }
@@ -1230,8 +1233,9 @@ pafp8_status pafp8_run_decode_noalloc(const pafp8_plan* plan, int32_t q_dtype, c
     if (plan->num_ctas > 0) {
         CUtensorMap tk, tv;
         int hpb = 1;
-        if ((st = encode_decode_maps(&tk, &tv, k_cache, v_cache, d.num_pages * plan->page_mult, d.num_kv_heads,
-                                     plan->heads_per_cta, &hpb, is_2byte(k_dtype), d.kv_layout, d.head_dim)) != PAFP8_OK)
+        if ((st = encode_decode_maps(&tk, &tv, k_cache, v_cache, d.num_pages, d.num_kv_heads,
+                                     plan->heads_per_cta, &hpb, is_2byte(k_dtype), d.kv_layout, d.head_dim,
+                                     d.page_size)) != PAFP8_OK)
             return st;
         e = launch_decode(p, tk, tv, plan->num_ctas, plan->heads_per_cta, plan->group, hpb, s);
     }
@@ -1361,9 +1365,6 @@ pafp8_status pafp8_append_kv(int32_t src_dtype, const void* k_new, const void* v
     if (page_size <= 0 || page_size % kPageSize != 0)
         return fail(PAFP8_ERR_UNSUPPORTED, "page_size %d is not served by this library (a multiple of %d)",
                     (int)page_size, kPageSize);
-    if (page_size != kPageSize && kv_layout == PAFP8_LAYOUT_HND)
-        return fail(PAFP8_ERR_UNSUPPORTED, "the HND layout is served with page_size %d only (got %d)",
-                    kPageSize, (int)page_size);
     if (!scale_ok(k_scale) || !scale_ok(v_scale))
         return fail(PAFP8_ERR_ARG, "scales must be finite and > 0 (k %g, v %g)", (double)k_scale,
                     (double)v_scale);

@@ -75,14 +75,19 @@ __device__ __forceinline__ float fold_scale_log2(float sm_scale, float q_scale, 
     return (float)((double)sm_scale * (double)q_scale * (double)k_scale * 1.4426950408889634);
 }
 
-// Pool index of 16-token sub-page `vp` of a request whose page entries start
-// at `idx` (pages of 16 * m tokens): entry vp / m, sub-page vp % m.  `bad` is
-// set, and 0 returned, when the entry lies outside [0, num_pages).
-__device__ __forceinline__ int sub_page(const int32_t* idx, int vp, int m, int num_pages, bool& bad) {
+// A request's 16-token sub-page vp (a page of 16 m tokens is m of them) as
+// TMA coordinates: the pool page holding it and its first token slot there
+// (the cache maps span whole pages, page_size slots; sub-page j of a page
+// starts at slot 16 j).  A page id outside [0, num_pages) reads page 0 and
+// sets `bad`.
+struct SubPageAt {
+    int slot, page;
+};
+__device__ __forceinline__ SubPageAt sub_page(const int32_t* idx, int vp, int m, int num_pages, bool& bad) {
     const int e = m == 1 ? vp : vp / m;
     const int pg = __ldg(idx + e);
     bad = pg < 0 || pg >= num_pages;
-    return bad ? 0 : pg * m + (vp - e * m);
+    return SubPageAt{(vp - e * m) * kPageSize, bad ? 0 : pg};
 }
 
 // Status word bits written by the kernels into the workspace.
@@ -160,7 +165,7 @@ struct PrefillParams {
     long long wait_cycles;   // bound of a pipeline wait (SM clock cycles)
 };
 
-// Launchers (decode.cu, prefill.cu).  Return the launch's cudaError_t.
+// Launchers (decode.cu, prefill_d128.cu / prefill_d64.cu).  Return the launch's cudaError_t.
 // heads_per_box: KV heads covered by one TMA box of the cache maps (the
 // whole head block when the page-wide map could be encoded, else 1).
 cudaError_t launch_decode(const DecodeParams& p, const CUtensorMap& tmap_k,
@@ -178,9 +183,19 @@ cudaError_t noalloc_scratch(void** ptr);
 cudaError_t launch_merge(const DecodeParams& p, int num_merge, int heads_per_cta, int group,
                          cudaStream_t stream);
 // tmap_o: map over o with the 2-byte query tile's box (the fp8-query kernel
-// writes full output tiles with bulk tensor stores through it).
-cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& tmap_q,
-                           const CUtensorMap& tmap_k, const CUtensorMap& tmap_v,
-                           const CUtensorMap& tmap_o, int num_ctas, cudaStream_t stream);
+// writes full output tiles with bulk tensor stores through it).  One
+// translation unit per head size (prefill_d128.cu, prefill_d64.cu).
+cudaError_t launch_prefill_d128(const PrefillParams& p, const CUtensorMap& tmap_q,
+                                const CUtensorMap& tmap_k, const CUtensorMap& tmap_v,
+                                const CUtensorMap& tmap_o, int num_ctas, cudaStream_t stream);
+cudaError_t launch_prefill_d64(const PrefillParams& p, const CUtensorMap& tmap_q,
+                               const CUtensorMap& tmap_k, const CUtensorMap& tmap_v,
+                               const CUtensorMap& tmap_o, int num_ctas, cudaStream_t stream);
+inline cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& tmap_q,
+                                  const CUtensorMap& tmap_k, const CUtensorMap& tmap_v,
+                                  const CUtensorMap& tmap_o, int num_ctas, cudaStream_t stream) {
+    return p.head_dim == 64 ? launch_prefill_d64(p, tmap_q, tmap_k, tmap_v, tmap_o, num_ctas, stream)
+                            : launch_prefill_d128(p, tmap_q, tmap_k, tmap_v, tmap_o, num_ctas, stream);
+}
 
 }  // namespace pafp8

@@ -1,5 +1,6 @@
-// prefill.cu -- ragged causal prefill attention over a paged fp8 KV cache on
-// the tcgen05 tensor cores (sm_103a).
+// prefill.cuh -- ragged causal prefill attention over a paged fp8 KV cache on
+// the tcgen05 tensor cores (sm_103a).  Included by one translation unit per
+// head size (prefill_d128.cu, prefill_d64.cu), which compile in parallel.
 //
 // What it computes: for request b with qo_len new query rows and kv_len keys,
 // query row i (0-based among the new rows) of head h attends to keys
@@ -46,8 +47,15 @@
 // The tensor pipe runs one CTA's MMAs in order, so an MMA writing S_X after
 // O_X += P_X V has been issued cannot overtake it, and s_full(X, j) implies
 // that the previous O update of X is complete.  Every operand in shared
-// memory is K-major with the 128-byte swizzle.  All waits are bounded; on
-// expiry the kernel records a status bit and winds down.
+// memory is K-major with the 128-byte swizzle (64-byte for the 64-byte fp8
+// rows of head_dim 64).  All waits are bounded; on expiry the kernel records a
+// status bit and winds down.
+//
+// Pages of 16 m tokens (m > 1) are read as m sub-pages of 16: the TMA box of
+// sub-page j is at token slot 16 j of its page, which covers both layouts.
+// That path (kSlots) is its own instantiation so that the 16-token path keeps
+// a producer loop without the division by m.
+#pragma once
 #include "../../include/pafp8.h"
 #include "internal.h"
 #include "ptx.cuh"
@@ -196,7 +204,7 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, uin
     return true;
 }
 
-template <bool kF8, int KT, bool kDiag, int DH>
+template <bool kF8, int KT, bool kDiag, int DH, bool kSlots>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ PrefillParams p, const __grid_constant__ CUtensorMap tmq,
                    const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
@@ -325,12 +333,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 const bool bad = lane < np && (page < 0 || page >= p.num_pages);
                 if (bad) page = 0;
-                else if (m != 1) page = page * m + (pg0 + lane) % m;
+                else if (kSlots) page = page * m + (pg0 + lane) % m;
                 if (__any_sync(0xFFFFFFFFu, bad) && lane == 0) atomicOr(p.status, kStatusBounds);
-                // Page ids live in lanes 0..np-1; lane 0 issues every copy.
+                // Page ids (sub-page ids page * m + j with kSlots) live in lanes
+                // 0..np-1; lane 0 issues every copy.  Sub-page j of a page is the
+                // box at token slot 16 j of that page.
                 int pages[8];
 #pragma unroll
                 for (int i = 0; i < 8; ++i) pages[i] = __shfl_sync(0xFFFFFFFFu, page, i);
+                // Copies of the tile's np sub-pages, each by load(i, slot, page).
+                auto each_page = [&](auto&& load) {
+                    if constexpr (kSlots) {
+                        for (int i = 0; i < np; ++i) {
+                            const int pg = pages[i] / m;
+                            load(i, (pages[i] - pg * m) * kPageSize, pg);
+                        }
+                    } else {
+                        for (int i = 0; i < np; ++i) load(i, 0, pages[i]);
+                    }
+                };
                 if (lane == 0) {
                     ok = wait_or_abort<kDiag>(bar(bke + kr.idx), kr.phase ^ 1u, flag_addr, p.status, p.wait_cycles);
                     if (ok) {
@@ -340,14 +361,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                             // the 16-bit K tile: [half][key][128 B].
                             const uint32_t dst = base + L::k16 + kr.idx * Dm::kF16Tile;
                             mbar_arrive_expect_tx(fb, (uint32_t)np * kPageSize * DH * 2);
-                            for (int i = 0; i < np; ++i)
+                            each_page([&](int i, int slot, int pg) {
                                 for (int h = 0; h < NH; ++h)
-                                    tma_load_5d(dst + h * kHalfTile + i * 2048u, &tmk, fb, 0, h, 0, it.hk, pages[i]);
+                                    tma_load_5d(dst + h * kHalfTile + i * 2048u, &tmk, fb, 0, h, slot, it.hk, pg);
+                            });
                         } else {
                             const uint32_t dst = base + L::kr + kr.idx * Dm::kRawTile;
                             mbar_arrive_expect_tx(fb, (uint32_t)np * kPageSize * DH);
-                            for (int i = 0; i < np; ++i)
-                                tma_load_4d(dst + i * Dm::kRawPage, &tmk, fb, 0, it.hk, 0, pages[i]);
+                            each_page([&](int i, int slot, int pg) {
+                                tma_load_4d(dst + i * Dm::kRawPage, &tmk, fb, 0, it.hk, slot, pg);
+                            });
                         }
                         ++issued_k;
                     }
@@ -362,13 +385,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint32_t dst = base + L::vr + vr.idx * L::kRawV;
                         if (k2) {
                             mbar_arrive_expect_tx(fb, (uint32_t)np * kPageSize * DH * 2);
-                            for (int i = 0; i < np; ++i)
+                            each_page([&](int i, int slot, int pg) {
                                 for (int h = 0; h < NH; ++h)
-                                    tma_load_5d(dst + h * kHalfTile + i * 2048u, &tmv, fb, 0, h, 0, it.hk, pages[i]);
+                                    tma_load_5d(dst + h * kHalfTile + i * 2048u, &tmv, fb, 0, h, slot, it.hk, pg);
+                            });
                         } else {
                             mbar_arrive_expect_tx(fb, (uint32_t)np * kPageSize * DH);
-                            for (int i = 0; i < np; ++i)
-                                tma_load_4d(dst + i * Dm::kRawPage, &tmv, fb, 0, it.hk, 0, pages[i]);
+                            each_page([&](int i, int slot, int pg) {
+                                tma_load_4d(dst + i * Dm::kRawPage, &tmv, fb, 0, it.hk, slot, pg);
+                            });
                         }
                         ++issued_v;
                     }
@@ -924,46 +949,46 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <bool kF8, int KT, bool kDiag, int DH>
+template <bool kF8, int KT, bool kDiag, int DH, bool kSlots>
 cudaError_t launch_t(const PrefillParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
                      const CUtensorMap& tv, const CUtensorMap& to, int num_ctas, cudaStream_t stream) {
     const size_t smem = 1024 + Layout<kF8, KT == PAFP8_F16 || KT == PAFP8_BF16, DH>::bytes;
-    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<kF8, KT, kDiag, DH>,
+    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<kF8, KT, kDiag, DH, kSlots>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    prefill_kernel<kF8, KT, kDiag, DH><<<num_ctas, kThreads, smem, stream>>>(p, tq, tk, tv, to);
+    prefill_kernel<kF8, KT, kDiag, DH, kSlots><<<num_ctas, kThreads, smem, stream>>>(p, tq, tk, tv, to);
     return cudaGetLastError();
 }
 
-// The diagnostic instantiation runs only under a shortened wait bound.
-template <bool kF8, int KT>
+// The diagnostic instantiation runs only under a shortened wait bound (and
+// takes any page size); pages of 16 tokens and of 16 m tokens have one each.
+template <bool kF8, int KT, int DH>
 cudaError_t launch_one(const PrefillParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
                        const CUtensorMap& tv, const CUtensorMap& to, int num_ctas, cudaStream_t stream) {
-    const bool diag = p.wait_cycles < kWaitCyclesDefault;
-    if (p.head_dim == 64)
-        return diag ? launch_t<kF8, KT, true, 64>(p, tq, tk, tv, to, num_ctas, stream)
-                    : launch_t<kF8, KT, false, 64>(p, tq, tk, tv, to, num_ctas, stream);
-    return diag ? launch_t<kF8, KT, true, 128>(p, tq, tk, tv, to, num_ctas, stream)
-                : launch_t<kF8, KT, false, 128>(p, tq, tk, tv, to, num_ctas, stream);
+    if (p.wait_cycles < kWaitCyclesDefault)
+        return launch_t<kF8, KT, true, DH, true>(p, tq, tk, tv, to, num_ctas, stream);
+    return p.page_mult != 1 ? launch_t<kF8, KT, false, DH, true>(p, tq, tk, tv, to, num_ctas, stream)
+                            : launch_t<kF8, KT, false, DH, false>(p, tq, tk, tv, to, num_ctas, stream);
 }
 
-}  // namespace
-
-cudaError_t launch_prefill(const PrefillParams& p, const CUtensorMap& tmap_q, const CUtensorMap& tmap_k,
-                           const CUtensorMap& tmap_v, const CUtensorMap& tmap_o, int num_ctas,
-                           cudaStream_t stream) {
+// Dispatch on the query and cache dtypes for head size DH.
+template <int DH>
+cudaError_t launch_prefill_head(const PrefillParams& p, const CUtensorMap& tmap_q, const CUtensorMap& tmap_k,
+                                const CUtensorMap& tmap_v, const CUtensorMap& tmap_o, int num_ctas,
+                                cudaStream_t stream) {
     const bool f8 = p.q_dtype == PAFP8_E4M3FN || p.q_dtype == PAFP8_E5M2;
     if (f8)
         return p.kv_dtype == PAFP8_E4M3FN
-                   ? launch_one<true, PAFP8_E4M3FN>(p, tmap_q, tmap_k, tmap_v, tmap_o, num_ctas, stream)
-                   : launch_one<true, PAFP8_E5M2>(p, tmap_q, tmap_k, tmap_v, tmap_o, num_ctas, stream);
+                   ? launch_one<true, PAFP8_E4M3FN, DH>(p, tmap_q, tmap_k, tmap_v, tmap_o, num_ctas, stream)
+                   : launch_one<true, PAFP8_E5M2, DH>(p, tmap_q, tmap_k, tmap_v, tmap_o, num_ctas, stream);
     switch (p.kv_dtype) {
-        case PAFP8_E4M3FN: return launch_one<false, PAFP8_E4M3FN>(p, tmap_q, tmap_k, tmap_v, tmap_o, num_ctas, stream);
-        case PAFP8_E5M2: return launch_one<false, PAFP8_E5M2>(p, tmap_q, tmap_k, tmap_v, tmap_o, num_ctas, stream);
-        case PAFP8_F16: return launch_one<false, PAFP8_F16>(p, tmap_q, tmap_k, tmap_v, tmap_o, num_ctas, stream);
-        case PAFP8_BF16: return launch_one<false, PAFP8_BF16>(p, tmap_q, tmap_k, tmap_v, tmap_o, num_ctas, stream);
+        case PAFP8_E4M3FN: return launch_one<false, PAFP8_E4M3FN, DH>(p, tmap_q, tmap_k, tmap_v, tmap_o, num_ctas, stream);
+        case PAFP8_E5M2: return launch_one<false, PAFP8_E5M2, DH>(p, tmap_q, tmap_k, tmap_v, tmap_o, num_ctas, stream);
+        case PAFP8_F16: return launch_one<false, PAFP8_F16, DH>(p, tmap_q, tmap_k, tmap_v, tmap_o, num_ctas, stream);
+        case PAFP8_BF16: return launch_one<false, PAFP8_BF16, DH>(p, tmap_q, tmap_k, tmap_v, tmap_o, num_ctas, stream);
         default: return cudaErrorInvalidValue;
     }
 }
 
+}  // namespace
 }  // namespace pafp8

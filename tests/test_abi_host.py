@@ -192,7 +192,7 @@ def test_plan_refuses_o_dtype(o, word):
 
 @pytest.mark.parametrize("over,status", [
     (dict(num_qo_heads=6, num_kv_heads=4), 2), (dict(head_dim=96), 8), (dict(head_dim=32), 8), (dict(page_size=24), 8),
-    (dict(page_size=32, kv_layout=1), 8), (dict(page_size=0), 8),
+    (dict(page_size=0), 8),
     (dict(num_qo_heads=32, num_kv_heads=2), 8), (dict(mode=5), 3), (dict(num_ctas=-1), 3),
     (dict(fixed_split_pages=-2), 3), (dict(sm_scale=float("nan")), 3), (dict(kv_layout=2), 3)])
 def test_plan_refuses_shapes_and_args(over, status):
@@ -206,6 +206,14 @@ def test_plan_refuses_shapes_and_args(over, status):
 def test_plan_accepts_both_head_sizes_in_both_modes(mode, d):
     qo = np.array([0, 3], np.int32) if mode == 1 else None
     h = pa.pafp8_plan_create(_desc(mode=mode, head_dim=d), np.array([0, 2], np.int32), np.array([5], np.int32), qo)
+    pa.pafp8_plan_destroy(h)
+
+
+@pytest.mark.parametrize("layout", [0, 1])
+@pytest.mark.parametrize("P", [32, 48, 256])
+def test_plan_accepts_large_pages_in_both_layouts(layout, P):
+    h = pa.pafp8_plan_create(_desc(page_size=P, kv_layout=layout), np.array([0, 2], np.int32),
+                             np.array([5], np.int32))
     pa.pafp8_plan_destroy(h)
 
 
@@ -375,7 +383,6 @@ def _append_raw(**over):
     (dict(src=pa.E4M3FN), 1, "append takes"), (dict(src=pa.INT8), 1, "int8"),
     (dict(kv=pa.BF16), 8, "bfloat16"), (dict(kv=pa.F16), 8, "float16"), (dict(kv=pa.UINT8), 1, "uint8"),
     (dict(kv=pa.F32), 1, "float32"), (dict(d=96), 8, "head_dim"), (dict(page_size=24), 8, "page_size"),
-    (dict(page_size=32, layout=1), 8, "HND"),
     (dict(hkv=0), 2, "num_kv_heads"), (dict(nnz=-1), 2, "negative"), (dict(ks=0.0), 3, "scales"),
     (dict(vs=float("inf")), 3, "scales"), (dict(layout=3), 3, "kv_layout"), (dict(k_new=None), 3, "non-NULL"),
     (dict(indices=None), 3, "non-NULL"), (dict(k_cache=0x70008), 3, "16-byte"), (dict(pos=0x40002), 3, "4-byte")])
