@@ -62,12 +62,12 @@ L2_FLUSH_BYTES = 256 << 20
 # workload, from one ncu capture of the kernel source with this SHA-256; a
 # changed kernel reports null until it is captured again.
 NCU_TRAFFIC = {
-    "c3b0454dffeb97e1dcccd875dea46b8412816eb18e85fea91d3301223f5c2991": 309770496,
+    "76f9483a2b6ccb907ad2272b75e96b6549a2c979f51546963b693b97afc26503": 310123008,
 }
 # The same for the prefill kernel, per workload index, keyed by the SHA-256
 # of its source.
 NCU_TRAFFIC_PREFILL = {
-    "71798cc65a65dc09a7b0caf08f142f626eced7ef1de920df37eb290c05f9830f": {4: 170110720, 5: 191745024},
+    "b4a80b4e96c20a461369c818f8339e6ff538ca1afdf1d03cfe41fa4e296baf9c": {4: 169852928, 5: 193976064, 7: 266426624},
 }
 
 
@@ -665,7 +665,7 @@ def run_ours(args):
     sampler = ClockSampler(gpu_id_for(torch, dev)) if rank == 0 and args.mode in ("all", "decode") else None
 
     if args.mode == "prefill":
-        res = {str(i): time_prefill(i, dev, args.prefill_steps, max(3, args.warmup)) for i in (4, 5)}
+        res = {str(i): time_prefill(i, dev, args.prefill_steps, max(3, args.warmup)) for i in (4, 5, 7)}
         if rank == 0:
             print(json.dumps({"mode": "prefill", "prefill": res}), flush=True)
         if world > 1:
