@@ -353,9 +353,10 @@ POD_WORKLOADS = {
 
 def pod_batch(prefill: PagedBatch, decode: PagedBatch) -> PodBatch:
     """Join two batches' pools (prefill pages first) into one; the decode
-    requests' page indices move past the prefill pool and both read the cache
-    with the prefill batch's per-tensor scales (the decode batch's fp8 codes
-    are kept, so its values scale with them)."""
+    requests' page indices move past the prefill pool and both phases use the
+    prefill batch's per-tensor scales, q_scale included (one call takes one set
+    of scales; the decode batch's fp8 codes are kept, so its values scale with
+    them)."""
     if (prefill.kv_dtype, prefill.num_kv_heads, prefill.head_dim, prefill.page_size, prefill.kv_layout) != (
             decode.kv_dtype, decode.num_kv_heads, decode.head_dim, decode.page_size, decode.kv_layout):
         raise ValueError("the two batches' caches differ in dtype or shape")
@@ -365,7 +366,7 @@ def pod_batch(prefill: PagedBatch, decode: PagedBatch) -> PodBatch:
     pre = dataclasses.replace(prefill, k_cache=k, v_cache=v, num_pages=pool)
     dec = dataclasses.replace(decode, k_cache=k, v_cache=v, num_pages=pool,
                               kv_indices=decode.kv_indices + prefill.num_pages,
-                              k_scale=prefill.k_scale, v_scale=prefill.v_scale)
+                              q_scale=prefill.q_scale, k_scale=prefill.k_scale, v_scale=prefill.v_scale)
     return PodBatch(prefill=pre, decode=dec)
 
 

@@ -10,7 +10,7 @@ import torch
 import paged_attention_fp8_gb300 as pa
 from common import oracle_on
 from gpu_common import DeviceBatch, assert_close
-from paged_attention_fp8_gb300.workloads import make_batch, pod_batch, pod_workload
+from paged_attention_fp8_gb300.workloads import make_batch, pod_batch, pod_workload, with_layout
 
 pytestmark = pytest.mark.gpu
 
@@ -117,3 +117,21 @@ def test_pod_replays_from_a_cuda_graph(cuda_device):
     (go, gl), (eo, el) = pod.results()
     assert np.array_equal(po, go) and np.array_equal(pl, gl)
     assert np.array_equal(do, eo) and np.array_equal(dl, el)
+
+
+@pytest.mark.parametrize("variant", ["head64", "hnd_page32", "fp8_query_head64"])
+def test_pod_shapes(cuda_device, variant):
+    """POD over caches of head_dim 64 and of head-major 32-token pages: each
+    phase as alone and against the oracle."""
+    d = 64 if "head64" in variant else 128
+    P = 32 if variant == "hnd_page32" else 16
+    q = "e4m3fn" if variant.startswith("fp8") else "bf16"
+    pre = make_batch([60, 300, 129], [60, 200, 1], num_qo_heads=16, num_kv_heads=4, head_dim=d, page_size=P,
+                     q_dtype=q, seed=211, pool_pages=1000 // P)
+    dec = make_batch([0, 1, 31, 33, 700, 2100], num_qo_heads=16, num_kv_heads=4, head_dim=d, page_size=P,
+                     q_dtype=q, seed=212, pool_pages=3200 // P)
+    if variant == "hnd_page32":
+        pre, dec = with_layout(pre, "HND"), with_layout(dec, "HND")
+    pod = Pod(pod_batch(pre, dec), cuda_device, prefill_ctas=_sms(cuda_device) - 12, decode_ctas=12)
+    pod.run_pod()
+    _check(pod, f"POD {variant}")

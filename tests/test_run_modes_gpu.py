@@ -10,7 +10,7 @@ import torch
 import paged_attention_fp8_gb300 as pa
 from common import oracle_on
 from gpu_common import DeviceBatch, assert_close
-from paged_attention_fp8_gb300.workloads import make_batch, workload
+from paged_attention_fp8_gb300.workloads import make_batch, with_layout, workload
 
 pytestmark = pytest.mark.gpu
 
@@ -38,12 +38,15 @@ def test_debug_mode_is_silent_on_good_input(cuda_device, monkeypatch):
     assert_close(o, lse, ro, rl, "prefill under PAFP8_DEBUG")
 
 
-@pytest.mark.parametrize("mode", ["decode", "prefill"])
+@pytest.mark.parametrize("mode", ["decode", "prefill", "decode_head64_hnd32", "prefill_head64_hnd32"])
 def test_run_replays_from_a_cuda_graph(cuda_device, mode):
-    if mode == "decode":
-        b = make_batch([0, 17, 900, 2500], num_qo_heads=32, num_kv_heads=8, seed=31)
+    extra = dict(head_dim=64, page_size=32, pool_pages=200) if mode.endswith("hnd32") else {}
+    if mode.startswith("decode"):
+        b = make_batch([0, 17, 900, 2500], num_qo_heads=32, num_kv_heads=8, seed=31, **extra)
     else:
-        b = make_batch([40, 300, 700], [40, 129, 256], num_qo_heads=32, num_kv_heads=8, seed=32)
+        b = make_batch([40, 300, 700], [40, 129, 256], num_qo_heads=32, num_kv_heads=8, seed=32, **extra)
+    if mode.endswith("hnd32"):
+        b = with_layout(b, "HND")
     db = DeviceBatch(b, cuda_device, num_ctas=24)
     db.run()
     o1, l1 = db.result()

@@ -18,7 +18,7 @@ import torch
 import paged_attention_fp8_gb300 as pa
 from common import oracle_on
 from gpu_common import DeviceBatch, assert_close
-from paged_attention_fp8_gb300.workloads import make_batch, workload
+from paged_attention_fp8_gb300.workloads import make_batch, with_layout, workload
 
 pytestmark = pytest.mark.gpu
 
@@ -53,6 +53,29 @@ def test_noalloc_matches_workspace_entry_point_twice(cuda_device, which):
     db.run()
     ref_o, ref_lse = db.result()
     _check_twice(db, ref_o, ref_lse, f"no-alloc {which} vs pafp8_run")
+
+
+@pytest.mark.parametrize("shape", ["head64", "hnd_page32", "head64_hnd_page64_fp8q"])
+def test_noalloc_other_shapes_against_the_oracle(cuda_device, shape):
+    """head_dim 64, head-major caches and large pages through the no-allocation
+    call: the same bytes as the workspace entry point, and the oracle."""
+    d = 64 if "head64" in shape else 128
+    P = 64 if "page64" in shape else (32 if "page32" in shape else 16)
+    q = "e4m3fn" if shape.endswith("fp8q") else "bf16"
+    b = make_batch([0, 1, 33, 400, 2100], num_qo_heads=16, num_kv_heads=4, head_dim=d, page_size=P, q_dtype=q,
+                   seed=223, pool_pages=3000 // P)
+    if "hnd" in shape:
+        b = with_layout(b, "HND")
+    db = DeviceBatch(b, cuda_device, num_ctas=20)
+    db.run()
+    ref = db.result()
+    ro, rl = oracle_on(b)
+    _check_twice(db, ro, rl, f"no-alloc {shape} vs oracle")
+    o = torch.empty_like(db.o)
+    lse = torch.empty_like(db.lse)
+    _noalloc(db, o, lse)
+    torch.cuda.synchronize()
+    assert np.array_equal(o.double().cpu().numpy(), ref[0]) and np.array_equal(lse.double().cpu().numpy(), ref[1])
 
 
 def test_noalloc_serving_workload_against_the_oracle(cuda_device):
