@@ -324,7 +324,7 @@ __device__ __forceinline__ void merge_pair(const DecodeParams& p, int hpb, const
         merge_head<4>(p, hpb, a.hh, a.s0, a.s1, a.oh, a.vscale);
 }
 
-template <int KT, int DH, bool kDiag>
+template <int KT, int DH, bool kDiag, bool kSlots>
 __global__ void __launch_bounds__(32 * 9, 1)
     decode_kernel(const __grid_constant__ DecodeParams p, const __grid_constant__ CUtensorMap tmk,
                   const __grid_constant__ CUtensorMap tmv, int hpc, int group, int stages,
@@ -418,14 +418,22 @@ __global__ void __launch_bounds__(32 * 9, 1)
                 // Pool pages and token slots of 16-token sub-pages (a page of
                 // 16 * m tokens is m of them); an id outside the pool reads page
                 // 0 instead.
+                // (kSlots: pages of 16 m tokens, m > 1; the 16-token path keeps
+                // its lookup free of the division by m.)
                 bool bad = false;
-                const SubPageAt sp =
-                    lane < n ? sub_page(idx, pb + lane, p.page_mult, p.num_pages, bad) : SubPageAt{0, 0};
+                SubPageAt sp{0, 0};
+                if constexpr (kSlots) {
+                    if (lane < n) sp = sub_page(idx, pb + lane, p.page_mult, p.num_pages, bad);
+                } else if (lane < n) {
+                    const int pg = __ldg(idx + pb + lane);
+                    bad = pg < 0 || pg >= p.num_pages;
+                    sp.page = bad ? 0 : pg;
+                }
                 if (__any_sync(0xFFFFFFFFu, bad) && lane == 0) flag(p.status, kStatusBounds);
                 for (int j = 0; j < n; ++j) {
                     SubPageAt at;
                     at.page = __shfl_sync(0xFFFFFFFFu, sp.page, j);
-                    at.slot = p.page_mult == 1 ? 0 : __shfl_sync(0xFFFFFFFFu, sp.slot, j);
+                    at.slot = kSlots ? __shfl_sync(0xFFFFFFFFu, sp.slot, j) : 0;
                     if (lane == 0) {
                         if (!pipe_wait<kDiag>(bar_empty + 8u * stage, phase ^ 1u, p.wait_cycles)) {
                             ok = false;
@@ -867,7 +875,10 @@ cudaError_t launch_decode_t(const DecodeParams& p, const CUtensorMap& tmap_k, co
     const dim3 grid(num_ctas), block(32 * (hpc + 1));
     // The diagnostic instantiation runs only under a shortened wait bound.
     const bool diag = p.wait_cycles < kWaitCyclesDefault;
-    auto kern = diag ? decode_kernel<KT, DH, true> : decode_kernel<KT, DH, false>;
+    // Pages of 16 tokens and of 16 m tokens have an instantiation each; the
+    // diagnostic one takes any page size.
+    auto kern = diag ? decode_kernel<KT, DH, true, true>
+                     : (p.page_mult != 1 ? decode_kernel<KT, DH, false, true> : decode_kernel<KT, DH, false, false>);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     kern<<<grid, block, smem, stream>>>(p, tmap_k, tmap_v, hpc, group, stages, heads_per_box);
