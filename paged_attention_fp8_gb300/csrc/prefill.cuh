@@ -335,70 +335,66 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (bad) page = 0;
                 else if (kSlots) page = page * m + (pg0 + lane) % m;
                 if (__any_sync(0xFFFFFFFFu, bad) && lane == 0) atomicOr(p.status, kStatusBounds);
-                // Page ids (sub-page ids page * m + j with kSlots) live in lanes
-                // 0..np-1; lane 0 issues every copy.  Sub-page j of a page is the
-                // box at token slot 16 j of that page.
-                int pages[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) pages[i] = __shfl_sync(0xFFFFFFFFu, page, i);
-                // Copies of the tile's np sub-pages, each by load(i, slot, page).
-                auto each_page = [&](auto&& load) {
+                // Lane i < np holds the id of the tile's sub-page i (page * m + j
+                // with kSlots; sub-page j of a page is the box at token slot 16 j
+                // of that page) and issues its copies through load(slot, page).
+                auto for_page = [&](auto&& load) {
                     if constexpr (kSlots) {
-                        for (int i = 0; i < np; ++i) {
-                            const int pg = pages[i] / m;
-                            load(i, (pages[i] - pg * m) * kPageSize, pg);
-                        }
+                        const int pg = page / m;
+                        load((page - pg * m) * kPageSize, pg);
                     } else {
-                        for (int i = 0; i < np; ++i) load(i, 0, pages[i]);
+                        load(0, page);
                     }
                 };
+                // Lane 0 waits for the stage and posts the byte count; then lane
+                // i issues page i's box (a thread needs about 100 cycles per TMA
+                // box, so the eight pages go out from eight lanes at once).
                 if (lane == 0) {
                     ok = wait_or_abort<kDiag>(bar(bke + kr.idx), kr.phase ^ 1u, flag_addr, p.status, p.wait_cycles);
-                    if (ok) {
-                        const uint32_t fb = bar(bkf + kr.idx);
-                        if (k2) {
-                            // Each page as one box per 64-dim half into the halves of
-                            // the 16-bit K tile: [half][key][128 B].
-                            const uint32_t dst = base + L::k16 + kr.idx * Dm::kF16Tile;
-                            mbar_arrive_expect_tx(fb, (uint32_t)np * kPageSize * DH * 2);
-                            each_page([&](int i, int slot, int pg) {
-                                for (int h = 0; h < NH; ++h)
-                                    tma_load_5d(dst + h * kHalfTile + i * 2048u, &tmk, fb, 0, h, slot, it.hk, pg);
-                            });
-                        } else {
-                            const uint32_t dst = base + L::kr + kr.idx * Dm::kRawTile;
-                            mbar_arrive_expect_tx(fb, (uint32_t)np * kPageSize * DH);
-                            each_page([&](int i, int slot, int pg) {
-                                tma_load_4d(dst + i * Dm::kRawPage, &tmk, fb, 0, it.hk, slot, pg);
-                            });
-                        }
-                        ++issued_k;
-                    }
+                    if (ok) mbar_arrive_expect_tx(bar(bkf + kr.idx), (uint32_t)np * kPageSize * DH * (k2 ? 2 : 1));
                 }
                 ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
                 if (!ok) break;
+                if (lane < np) {
+                    const uint32_t fb = bar(bkf + kr.idx);
+                    if (k2) {
+                        // Each page as one box per 64-dim half into the halves of
+                        // the 16-bit K tile: [half][key][128 B].
+                        const uint32_t dst = base + L::k16 + kr.idx * Dm::kF16Tile;
+                        for_page([&](int slot, int pg) {
+                            for (int h = 0; h < NH; ++h)
+                                tma_load_5d(dst + h * kHalfTile + lane * 2048u, &tmk, fb, 0, h, slot, it.hk, pg);
+                        });
+                    } else {
+                        const uint32_t dst = base + L::kr + kr.idx * Dm::kRawTile;
+                        for_page([&](int slot, int pg) {
+                            tma_load_4d(dst + lane * Dm::kRawPage, &tmk, fb, 0, it.hk, slot, pg);
+                        });
+                    }
+                }
+                ++issued_k;
                 kr.next(nkr);
                 if (lane == 0) {
                     ok = wait_or_abort<kDiag>(bar(L::bVrEmpty + vr.idx), vr.phase ^ 1u, flag_addr, p.status, p.wait_cycles);
-                    if (ok) {
-                        const uint32_t fb = bar(L::bVrFull + vr.idx);
-                        const uint32_t dst = base + L::vr + vr.idx * L::kRawV;
-                        if (k2) {
-                            mbar_arrive_expect_tx(fb, (uint32_t)np * kPageSize * DH * 2);
-                            each_page([&](int i, int slot, int pg) {
-                                for (int h = 0; h < NH; ++h)
-                                    tma_load_5d(dst + h * kHalfTile + i * 2048u, &tmv, fb, 0, h, slot, it.hk, pg);
-                            });
-                        } else {
-                            mbar_arrive_expect_tx(fb, (uint32_t)np * kPageSize * DH);
-                            each_page([&](int i, int slot, int pg) {
-                                tma_load_4d(dst + i * Dm::kRawPage, &tmv, fb, 0, it.hk, slot, pg);
-                            });
-                        }
-                        ++issued_v;
-                    }
+                    if (ok) mbar_arrive_expect_tx(bar(L::bVrFull + vr.idx), (uint32_t)np * kPageSize * DH * (k2 ? 2 : 1));
                 }
                 ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+                if (!ok) break;
+                if (lane < np) {
+                    const uint32_t fb = bar(L::bVrFull + vr.idx);
+                    const uint32_t dst = base + L::vr + vr.idx * L::kRawV;
+                    if (k2) {
+                        for_page([&](int slot, int pg) {
+                            for (int h = 0; h < NH; ++h)
+                                tma_load_5d(dst + h * kHalfTile + lane * 2048u, &tmv, fb, 0, h, slot, it.hk, pg);
+                        });
+                    } else {
+                        for_page([&](int slot, int pg) {
+                            tma_load_4d(dst + lane * Dm::kRawPage, &tmv, fb, 0, it.hk, slot, pg);
+                        });
+                    }
+                }
+                ++issued_v;
                 vr.next(L::NVR);
             }
         }
