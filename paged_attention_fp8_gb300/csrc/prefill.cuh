@@ -346,31 +346,43 @@ __global__ void __launch_bounds__(kThreads, 1)
                         load(0, page);
                     }
                 };
+                // A 2-byte cache has two boxes per page (the 64-dim halves): lane
+                // 8 h + i issues half h of page i, so 16 lanes share them.
+                const int hpage = __shfl_sync(0xFFFFFFFFu, page, lane & 7);
+                auto for_half_page = [&](auto&& load) {
+                    if constexpr (kSlots) {
+                        const int pg = hpage / m;
+                        load((hpage - pg * m) * kPageSize, pg);
+                    } else {
+                        load(0, hpage);
+                    }
+                };
+                const bool half_lane = (lane & 7) < np && (lane >> 3) < NH;
                 // Lane 0 waits for the stage and posts the byte count; then lane
-                // i issues page i's box (a thread needs about 100 cycles per TMA
-                // box, so the eight pages go out from eight lanes at once).
+                // i issues page i's box, or lane 8 h + i half h of it for a
+                // 2-byte cache (a thread needs about 100 cycles per TMA box, so
+                // the pages go out from several lanes at once).
                 if (lane == 0) {
                     ok = wait_or_abort<kDiag>(bar(bke + kr.idx), kr.phase ^ 1u, flag_addr, p.status, p.wait_cycles);
                     if (ok) mbar_arrive_expect_tx(bar(bkf + kr.idx), (uint32_t)np * kPageSize * DH * (k2 ? 2 : 1));
                 }
                 ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
                 if (!ok) break;
-                if (lane < np) {
-                    const uint32_t fb = bar(bkf + kr.idx);
-                    if (k2) {
+                if (k2) {
+                    if (half_lane) {
                         // Each page as one box per 64-dim half into the halves of
                         // the 16-bit K tile: [half][key][128 B].
                         const uint32_t dst = base + L::k16 + kr.idx * Dm::kF16Tile;
-                        for_page([&](int slot, int pg) {
-                            for (int h = 0; h < NH; ++h)
-                                tma_load_5d(dst + h * kHalfTile + lane * 2048u, &tmk, fb, 0, h, slot, it.hk, pg);
-                        });
-                    } else {
-                        const uint32_t dst = base + L::kr + kr.idx * Dm::kRawTile;
-                        for_page([&](int slot, int pg) {
-                            tma_load_4d(dst + lane * Dm::kRawPage, &tmk, fb, 0, it.hk, slot, pg);
+                        const int h = lane >> 3, i = lane & 7;
+                        for_half_page([&](int slot, int pg) {
+                            tma_load_5d(dst + h * kHalfTile + i * 2048u, &tmk, bar(bkf + kr.idx), 0, h, slot, it.hk, pg);
                         });
                     }
+                } else if (lane < np) {
+                    const uint32_t dst = base + L::kr + kr.idx * Dm::kRawTile;
+                    for_page([&](int slot, int pg) {
+                        tma_load_4d(dst + lane * Dm::kRawPage, &tmk, bar(bkf + kr.idx), 0, it.hk, slot, pg);
+                    });
                 }
                 ++issued_k;
                 kr.next(nkr);
@@ -380,19 +392,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
                 if (!ok) break;
-                if (lane < np) {
-                    const uint32_t fb = bar(L::bVrFull + vr.idx);
-                    const uint32_t dst = base + L::vr + vr.idx * L::kRawV;
-                    if (k2) {
-                        for_page([&](int slot, int pg) {
-                            for (int h = 0; h < NH; ++h)
-                                tma_load_5d(dst + h * kHalfTile + lane * 2048u, &tmv, fb, 0, h, slot, it.hk, pg);
-                        });
-                    } else {
-                        for_page([&](int slot, int pg) {
-                            tma_load_4d(dst + lane * Dm::kRawPage, &tmv, fb, 0, it.hk, slot, pg);
+                if (k2) {
+                    if (half_lane) {
+                        const uint32_t dst = base + L::vr + vr.idx * L::kRawV;
+                        const int h = lane >> 3, i = lane & 7;
+                        for_half_page([&](int slot, int pg) {
+                            tma_load_5d(dst + h * kHalfTile + i * 2048u, &tmv, bar(L::bVrFull + vr.idx), 0, h, slot, it.hk,
+                                        pg);
                         });
                     }
+                } else if (lane < np) {
+                    const uint32_t dst = base + L::vr + vr.idx * L::kRawV;
+                    for_page([&](int slot, int pg) {
+                        tma_load_4d(dst + lane * Dm::kRawPage, &tmv, bar(L::bVrFull + vr.idx), 0, it.hk, slot, pg);
+                    });
                 }
                 ++issued_v;
                 vr.next(L::NVR);
