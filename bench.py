@@ -64,8 +64,8 @@ L2_FLUSH_BYTES = 256 << 20
 NCU_TRAFFIC = {
     "76f9483a2b6ccb907ad2272b75e96b6549a2c979f51546963b693b97afc26503": 310123008,
 }
-# The same for the prefill kernel, per workload index, keyed by the SHA-256
-# of its source.
+# The same for the prefill kernels, per workload index, keyed by the SHA-256
+# of their sources (prefill.cuh, then prefill_pair.cuh).
 NCU_TRAFFIC_PREFILL = {
     "b4a80b4e96c20a461369c818f8339e6ff538ca1afdf1d03cfe41fa4e296baf9c": {4: 169852928, 5: 193976064, 7: 266426624},
 }
@@ -177,12 +177,13 @@ def time_prefill(index, dev, steps, warmup):
     ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
     tflops = flops / (ms * 1e-3) / 1e12
     p16, kind = measured_bf16_tflops()
-    traffic = NCU_TRAFFIC_PREFILL.get(kernel_sha("prefill.cuh"), {}).get(index)
+    traffic = NCU_TRAFFIC_PREFILL.get(kernel_sha("prefill.cuh", "prefill_pair.cuh"), {}).get(index)
     fp8 = b.q_dtype in ("e4m3fn", "e5m2")
     out = {"workload": WORKLOADS[index], "value": round(tflops, 2), "unit": "TFLOP/s",
            "ms_per_launch": round(ms, 5), "flops": flops, "launches": steps,
            "mma": ("QK^T fp8 kind::f8f6f4, PV f16 kind::f16" if fp8 else
-                   "bf16 kind::f16 (2-byte cache, V transposed in shared memory)" if b.kv_dtype in ("f16", "bf16")
+                   "bf16 kind::f16 on CTA pairs (cta_group::2, M 256; 2-byte cache, V transposed in shared memory)"
+                   if b.kv_dtype in ("f16", "bf16")
                    else "f16 kind::f16 (fp8 KV dequantized)")}
     if fp8:
         p8 = 2.0 * p16  # another dtype's measured peak x the nominal fp8/bf16 ratio
@@ -323,9 +324,13 @@ def time_append(index, dev, steps, warmup):
                          "frac": round(gbs / peak, 4), "peak_kind": kind}}
 
 
-def kernel_sha(name: str) -> str:
-    with open(os.path.join(ROOT, "paged_attention_fp8_gb300", "csrc", name), "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()
+def kernel_sha(*names: str) -> str:
+    """SHA-256 of the named kernel sources, concatenated in order."""
+    h = hashlib.sha256()
+    for name in names:
+        with open(os.path.join(ROOT, "paged_attention_fp8_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
 
 
 class ClockSampler:

@@ -179,22 +179,27 @@ def decode_metadata(kv_indptr, last_page_len, *, num_qo_heads, num_kv_heads, num
 
 
 def prefill_metadata(kv_indptr, last_page_len, qo_indptr, *, num_qo_heads, num_kv_heads, num_ctas,
-                     page_size=16):
-    """Prefill work items.  For request b, KV head hk and each block of
-    2 * TQ consecutive new tokens starting at t0 (TQ = 128 // group), one item
-    of two query tiles (A = [t0, t0+TQ), B = the next TQ); its KV-tile count
-    is the number of 128-key tiles its last token may see under the
+                     page_size=16, head_dim=128, kv_dtype="e4m3fn"):
+    """Prefill work items.  TQ = 128 // group new tokens fill a 128-row
+    query tile.  With a 2-byte cache (f16, bf16) at head_dim 128 two CTAs
+    work as a pair on each query tile of 2 * TQ tokens (TQ per CTA);
+    otherwise one CTA works on a tile of TQ tokens.  For request b, KV head hk and each block of two such tiles
+    (A, then B right after) starting at t0, one item; its KV-tile count is
+    the number of 128-key tiles its last token may see under the
     bottom-right causal rule, capped by the request's own key tiles.
     Each tile record is (b, hk, t0, nkv, qo_indptr[b], qo_len, kv_len,
     kv_indptr[b]).  Tiles are sorted by that count, descending, ties in
-    (b, hk, t0) order;
-    G = min(num_ctas, #tiles) persistent CTAs take tiles i, i + G, ..."""
+    (b, hk, t0) order.  G persistent CTAs take items i, i + G, ... (G =
+    min(num_ctas, #items)); pairs: G = 2 min(max(1, num_ctas // 2), #items)
+    CTAs, pair i taking items i, i + G / 2, ..."""
     kv_indptr = [int(x) for x in kv_indptr]
     last_page_len = [int(x) for x in last_page_len]
     qo_indptr = [int(x) for x in qo_indptr]
     B = len(kv_indptr) - 1
     group = num_qo_heads // num_kv_heads
     TQ = 128 // group
+    pair = head_dim == 128 and kv_dtype in ("f16", "bf16")
+    span = (4 if pair else 2) * TQ  # tokens per item
     req_page, req_kv, tiles = [], [], []
     for b in range(B):
         n = kv_indptr[b + 1] - kv_indptr[b]
@@ -203,13 +208,13 @@ def prefill_metadata(kv_indptr, last_page_len, qo_indptr, *, num_qo_heads, num_k
         req_kv.append(kv)
         qo = qo_indptr[b + 1] - qo_indptr[b]
         for hk in range(num_kv_heads):
-            for t0 in range(0, qo, 2 * TQ):
-                last = min(t0 + 2 * TQ, qo) - 1
+            for t0 in range(0, qo, span):
+                last = min(t0 + span, qo) - 1
                 lim = last + kv - qo
                 nkv = min((kv + 127) // 128, lim // 128 + 1)
                 tiles.append((b, hk, t0, nkv, qo_indptr[b], qo, kv, kv_indptr[b]))
     tiles = sorted(tiles, key=lambda t: -t[3])  # stable
-    G = min(num_ctas, len(tiles))
+    G = 2 * min(max(1, num_ctas // 2), len(tiles)) if pair else min(num_ctas, len(tiles))
     words = [0] * HEADER_WORDS
     words[0] = MAGIC
     words[1] = 1

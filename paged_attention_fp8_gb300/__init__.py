@@ -303,7 +303,7 @@ def pafp8_append_kv(k_new, v_new, batch_indices, positions, kv_indptr, kv_indice
 # ---- convenience owner of a plan ---------------------------------------
 
 class Plan:
-    """Owns one pafp8_plan.  Shapes served: head_dim 128 (or 64 in decode),
+    """Owns one pafp8_plan.  Shapes served: head_dim 128 or 64,
     page_size a multiple of 16 in either layout."""
 
     def __init__(self, *, mode: str, num_qo_heads: int, num_kv_heads: int, num_pages: int,

@@ -382,6 +382,11 @@ void build_prefill_meta(pafp8_plan* pl) {
     const int B = pl->desc.batch;
     const int g = pl->group;
     const int TQ = kTileRows / g;
+    // A 2-byte cache at head_dim 128 runs on CTA pairs: a query tile is 2 TQ
+    // tokens (TQ per CTA), an item two such tiles; the rest on single CTAs
+    // (tiles of TQ).
+    const bool pair = pl->desc.head_dim == kHeadDim && is_2byte(pl->desc.kv_dtype);
+    const int span = (pair ? 4 : 2) * TQ;
     struct T { int32_t b, hk, t0, nkv; };
     std::vector<T> tiles;
     std::vector<int32_t> req_page(B), req_kv(B);
@@ -391,17 +396,18 @@ void build_prefill_meta(pafp8_plan* pl) {
         req_kv[b] = n > 0 ? (n - 1) * pl->desc.page_size + pl->last_page_len[b] : 0;
         const int qo = pl->qo_indptr[b + 1] - pl->qo_indptr[b];
         for (int hk = 0; hk < pl->desc.num_kv_heads; ++hk)
-            for (int t0 = 0; t0 < qo; t0 += 2 * TQ) {
-                // An item is two query tiles, A = [t0, t0+TQ) and B right after;
-                // its KV tiles are those of its last token.
-                const int last = std::min(t0 + 2 * TQ, qo) - 1;
+            for (int t0 = 0; t0 < qo; t0 += span) {
+                // An item is two query tiles, A starting at t0 and B right
+                // after; its KV tiles are those of its last token.
+                const int last = std::min(t0 + span, qo) - 1;
                 const int lim = last + req_kv[b] - qo;
                 const int nkv = std::min((req_kv[b] + kTileKeys - 1) / kTileKeys, lim / kTileKeys + 1);
                 tiles.push_back({b, hk, t0, nkv});
             }
     }
     std::stable_sort(tiles.begin(), tiles.end(), [](const T& a, const T& c) { return a.nkv > c.nkv; });
-    const int G = (int)std::min<int64_t>(pl->desc.num_ctas, (int64_t)tiles.size());
+    const int G = pair ? 2 * (int)std::min<int64_t>(std::max<int64_t>(1, pl->desc.num_ctas / 2), (int64_t)tiles.size())
+                       : (int)std::min<int64_t>(pl->desc.num_ctas, (int64_t)tiles.size());
 
     std::vector<int32_t>& m = pl->meta;
     m.assign(kMetaHeaderWords, 0);

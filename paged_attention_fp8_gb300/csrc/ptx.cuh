@@ -446,6 +446,121 @@ __device__ __forceinline__ void tc_dealloc(uint32_t taddr, uint32_t ncols) {
                  : "memory");
 }
 
+// ------------------------------------------------- CTA pairs (2-SM MMA)
+// A cluster of two CTAs on two SMs runs one MMA stream: the leader (rank 0)
+// issues tcgen05.mma.cta_group::2 with M = 256, each CTA holding its 128 rows
+// of A (and of D in its TMEM) and half of B's N rows at the same shared-memory
+// offset.  Every tcgen05 MMA, commit, alloc and dealloc of such a kernel uses
+// .cta_group::2.
+
+// Every thread of both CTAs.
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// The shared::cluster address of `addr` (a shared::cta offset) in CTA `rank`.
+__device__ __forceinline__ uint32_t map_shared(uint32_t addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+// Arrive on an mbarrier of either CTA of the cluster (shared::cluster address).
+// The release is at CTA scope: what an arrival in these kernels orders is the
+// arriving CTA's own shared memory and TMEM against the tensor cores' reads of
+// them (already ordered by fence.proxy.async and the tcgen05 fences before the
+// arrive), never data that the other CTA's threads load.  A cluster-scope
+// release made the arriving thread wait about half a microsecond per arrive.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cbar) {
+    asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cbar) : "memory");
+}
+// One arrival for the whole warp (all 32 lanes call it): the warp barrier
+// orders every lane's earlier work before lane 0's arrive.  Cross-SM arrives
+// are transactions between SMs, so a warp sends one instead of 32.
+__device__ __forceinline__ void warp_arrive_cluster(uint32_t cbar) {
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive_cluster(cbar);
+}
+__device__ __forceinline__ void warp_arrive(uint32_t bar) {
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+}
+// try_wait acquiring at cluster scope (for arrivals from the peer CTA).
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ bool mbar_test_wait_cluster(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Warp-wide in each CTA of the pair: allocate `ncols` TMEM columns (the same
+// address in both), written to smem `dst`; then give up further allocation.
+__device__ __forceinline__ void tc_alloc_pair(uint32_t dst, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst), "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tc_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+// Arrive (count 1) on the mbarrier at offset `bar` in each CTA of `mask` when
+// every pair MMA this thread issued before has completed.
+__device__ __forceinline__ void tc_commit_pair(uint32_t bar, uint16_t mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+        "h"(mask)
+        : "memory");
+}
+// Pair MMAs (kind::f16), A and B from shared memory (descriptor start
+// offsets oa, ob in 16-byte units), or A from TMEM.
+__device__ __forceinline__ void tc_mma_pair_f16_ss(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t oa, uint32_t ob,
+                                                   uint32_t idesc, uint32_t accum) {
+    asm volatile(
+        "{\n .reg .pred p;\n .reg .b64 da, db, o1, o2;\n setp.ne.b32 p, %6, 0;\n cvt.u64.u32 o1, %3;\n"
+        " cvt.u64.u32 o2, %4;\n add.s64 da, %1, o1;\n add.s64 db, %2, o2;\n"
+        " tcgen05.mma.cta_group::2.kind::f16 [%0], da, db, %5, p;\n}\n" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(oa), "r"(ob), "r"(idesc), "r"(accum)
+        : "memory");
+}
+__device__ __forceinline__ void tc_mma_pair_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t off,
+                                                   uint32_t idesc, uint32_t accum) {
+    asm volatile(
+        "{\n .reg .pred p;\n .reg .b64 db, o;\n setp.ne.b32 p, %5, 0;\n cvt.u64.u32 o, %3;\n"
+        " add.s64 db, %2, o;\n"
+        " tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], db, %4, p;\n}\n" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b), "r"(off), "r"(idesc), "r"(accum)
+        : "memory");
+}
+// TMA loads into this CTA's shared memory whose completion (bytes) is counted
+// on the mbarrier `cbar` (a shared::cluster address, here the leader's).
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap* map, uint32_t cbar, int c0, int c1,
+                                                 int c2) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(cbar)
+        : "memory");
+}
+__device__ __forceinline__ void tma_load_5d_pair(uint32_t dst, const CUtensorMap* map, uint32_t cbar, int c0, int c1,
+                                                 int c2, int c3, int c4) {
+    asm volatile(
+        "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
+        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(cbar)
+        : "memory");
+}
+
 // 32 lanes x 32 consecutive 32-bit columns: thread i gets lane (base + i).
 __device__ __forceinline__ void tc_ld32(uint32_t taddr, uint32_t (&r)[32]) {
     asm volatile(

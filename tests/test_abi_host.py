@@ -285,7 +285,7 @@ def test_run_refuses_bad_scales():
 
 # ------------------------------------------------------------ prefill plans
 
-def _prefill_plan(kv_lens, qo_lens, *, hq=32, hkv=8, num_ctas=152, page_size=16):
+def _prefill_plan(kv_lens, qo_lens, *, hq=32, hkv=8, num_ctas=152, page_size=16, head_dim=128, kv_dtype="e4m3fn"):
     P = page_size
     npages = [(L + P - 1) // P for L in kv_lens]
     indptr = np.concatenate([[0], np.cumsum(npages)]).astype(np.int32)
@@ -293,9 +293,9 @@ def _prefill_plan(kv_lens, qo_lens, *, hq=32, hkv=8, num_ctas=152, page_size=16)
     qo_indptr = np.concatenate([[0], np.cumsum(qo_lens)]).astype(np.int32)
     plan = pa.Plan(mode="prefill", num_qo_heads=hq, num_kv_heads=hkv, num_pages=max(1, int(indptr[-1])),
                    kv_indptr=indptr, last_page_len=last, qo_indptr=qo_indptr, q_dtype="bf16",
-                   kv_dtype="e4m3fn", num_ctas=num_ctas, page_size=P)
+                   kv_dtype=kv_dtype, num_ctas=num_ctas, page_size=P, head_dim=head_dim)
     ref = plan_rule.prefill_metadata(indptr, last, qo_indptr, num_qo_heads=hq, num_kv_heads=hkv,
-                                     num_ctas=num_ctas, page_size=P)
+                                     num_ctas=num_ctas, page_size=P, head_dim=head_dim, kv_dtype=kv_dtype)
     return plan, np.array(ref, dtype=np.int32)
 
 
@@ -307,7 +307,17 @@ PREFILL_CASES = [
     dict(kv_lens=[2048] * 8, qo_lens=[2048] * 8, hq=32, hkv=8),
     dict(kv_lens=[100, 90], qo_lens=[60, 90], hq=6, hkv=2, num_ctas=1000),
     dict(kv_lens=[5, 200, 1000, 3000], qo_lens=[5, 40, 1000, 17], hq=32, hkv=8, num_ctas=7, page_size=64),
+    dict(kv_lens=[5, 200, 1000, 3000], qo_lens=[5, 40, 1000, 17], hq=32, hkv=8, num_ctas=7, head_dim=64),
+    # a 2-byte cache at head_dim 128 runs on CTA pairs (items of four tiles' tokens, even CTA counts)
+    dict(kv_lens=[5, 200, 1000, 3000], qo_lens=[5, 40, 1000, 17], hq=32, hkv=8, num_ctas=7, kv_dtype="bf16"),
+    dict(kv_lens=[129, 128, 127, 0], qo_lens=[129, 1, 100, 0], hq=16, hkv=1, num_ctas=1, kv_dtype="bf16"),
+    dict(kv_lens=[2048] * 8, qo_lens=[2048] * 8, hq=32, hkv=8, kv_dtype="bf16"),
+    dict(kv_lens=[300, 700], qo_lens=[300, 33], hq=24, hkv=8, num_ctas=5, head_dim=64, kv_dtype="bf16"),
 ]
+
+
+def _pairs(case):
+    return case.get("head_dim", 128) == 128 and case.get("kv_dtype", "e4m3fn") in ("f16", "bf16")
 
 
 @pytest.mark.parametrize("case", PREFILL_CASES)
@@ -331,7 +341,8 @@ def test_prefill_tiles_cover_every_row_head_once(case):
         # the record repeats the request's own fields
         assert (qo0, qo_len, kv_len) == (qo_ptr[b], qo, kv)
         assert page0 == m[m[10] + b]
-        for tok in range(t0, min(t0 + 2 * tq, qo)):  # two query tiles per item
+        span = (4 if _pairs(case) else 2) * tq  # two query tiles (of TQ tokens per CTA of a pair)
+        for tok in range(t0, min(t0 + span, qo)):
             for h in range(hk * g, hk * g + g):
                 assert (b, tok, h) not in seen
                 seen.add((b, tok, h))
@@ -340,6 +351,8 @@ def test_prefill_tiles_cover_every_row_head_once(case):
     want = {(b, t, h) for b, qo in enumerate(case["qo_lens"]) for t in range(qo) for h in range(hq)}
     assert seen == want
     assert list(tiles[:, 3]) == sorted(tiles[:, 3], reverse=True)
+    if _pairs(case):
+        assert m[6] % 2 == 0 and (m[6] > 0 or len(tiles) == 0)
 
 
 @pytest.mark.parametrize("qo,kv,word", [([50], [40], "qo_len"), ([3, 2], [2, 5], "qo_len")])
