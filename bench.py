@@ -62,12 +62,12 @@ L2_FLUSH_BYTES = 256 << 20
 # workload, from one ncu capture of the kernel source with this SHA-256; a
 # changed kernel reports null until it is captured again.
 NCU_TRAFFIC = {
-    "76f9483a2b6ccb907ad2272b75e96b6549a2c979f51546963b693b97afc26503": 310123008,
+    "24f608db83bd1121191e8d71b2fc88b51739b40edecf86c2722153bb0f610010": 309843456,
 }
 # The same for the prefill kernels, per workload index, keyed by the SHA-256
 # of their sources (prefill.cuh, then prefill_pair.cuh).
 NCU_TRAFFIC_PREFILL = {
-    "b4a80b4e96c20a461369c818f8339e6ff538ca1afdf1d03cfe41fa4e296baf9c": {4: 169852928, 5: 193976064, 7: 266426624},
+    "0a4fb3437cc861471ffa743dfb1d09d5a0a929940ca9d87c0e325c2a26359840": {4: 169775616, 5: 193140480, 7: 269439488},
 }
 
 
