@@ -369,6 +369,12 @@ __global__ void __launch_bounds__(32 * 9, 1)
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
     __syncthreads();
+    // Let the merge grid (launched as a programmatic dependent) start now
+    // rather than when the last CTA of this grid exits: its small blocks fit
+    // beside this CTA, read their metadata and wait in griddepcontrol.wait,
+    // which still returns only once this grid has completed and its writes
+    // are visible.  A no-op when no merge follows.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     if (warp == hpc) {
         // ---------------------------------------------------------- producer
