@@ -754,29 +754,23 @@ def run_ours(args):
     ms_step, ms_dec = max_over_ranks([ms_step, ms_dec], dev, world)
 
     # ---- end to end through the public API, every step: re-plan on the host,
-    # upload the plan, one H2D copy of the step's inputs (q and kv_indices
-    # packed in one pinned buffer), run, one D2H copy of the result (o and lse
-    # packed in one device buffer) into pinned memory, and the host waits for
-    # that result.  Two steps are in flight (workspaces and buffers double-
-    # buffered): the host plans and launches step i + 1 while the GPU runs
-    # step i, then waits for step i's result.  The KV cache stays resident in
-    # HBM: it is the state a decode step reads, not an input.
-    qb = q.numel() * q.element_size()
-    ib = idx.numel() * 4
-    ob = o.numel() * o.element_size()
-    lb = lse.numel() * 4
-    in_h = torch.empty(qb + ib, dtype=torch.uint8).pin_memory()
-    in_h[:qb].copy_(b.q.contiguous().view(-1).view(torch.uint8))
-    in_h[qb:].copy_(b.kv_indices.view(torch.uint8))
-    bufs = []
-    for _ in range(2):
-        in_d = torch.empty(qb + ib, dtype=torch.uint8, device=dev)
-        out_d = torch.empty(ob + lb, dtype=torch.uint8, device=dev)
-        bufs.append(dict(
-            ws=torch.empty(plan.workspace_bytes, dtype=torch.uint8, device=dev), in_d=in_d, out_d=out_d,
-            q=in_d[:qb].view(q.dtype).view(q.shape), idx=in_d[qb:].view(torch.int32),
-            o=out_d[:ob].view(o.dtype).view(o.shape), lse=out_d[ob:].view(torch.float32).view(lse.shape),
-            out_h=torch.empty(ob + lb, dtype=torch.uint8).pin_memory(), ev=torch.cuda.Event(), plan=None))
+    # then one pafp8_run_host call: it uploads the plan, copies the step's
+    # inputs (q and kv_indices, pinned host memory) into the staging part of
+    # the workspace, runs, and copies the result (o and lse) back into pinned
+    # host memory; the host then waits for that result.  Two steps are in
+    # flight, each with its own workspace, output buffers and stream: the host
+    # plans and launches step i + 1 while the GPU runs step i (and its copies
+    # overlap step i's kernels), then waits for step i's result.  The KV cache
+    # stays resident in HBM: it is the state a decode step reads, not an input.
+    q_h = b.q.contiguous().pin_memory()
+    idx_h = b.kv_indices.contiguous().pin_memory()
+    qb, ib = q_h.numel() * q_h.element_size(), idx_h.numel() * 4
+    ob, lb = o.numel() * o.element_size(), lse.numel() * 4
+    host_ws = plan.host_workspace_bytes(b.q_dtype)
+    bufs = [dict(ws=torch.empty(host_ws, dtype=torch.uint8, device=dev),
+                 o_h=torch.empty(tuple(o.shape), dtype=o.dtype).pin_memory(),
+                 lse_h=torch.empty(tuple(lse.shape), dtype=torch.float32).pin_memory(),
+                 stream=torch.cuda.Stream(), ev=torch.cuda.Event(), plan=None) for _ in range(2)]
     indptr_h, last_h = b.kv_indptr, b.last_page_len
     h2d = qb + ib + int(meta.size) * 4
     d2h = ob + lb
@@ -788,12 +782,11 @@ def run_ours(args):
                        q_dtype=b.q_dtype, kv_dtype=b.kv_dtype, o_dtype=b.o_dtype, sm_scale=b.sm_scale)
 
     def launch(x):
+        # x's buffers were last used two steps ago, whose result the host has
+        # already waited for.
         x["plan"] = new_plan()
-        x["plan"].upload(x["ws"])
-        x["in_d"].copy_(in_h, non_blocking=True)
-        x["plan"].run(x["q"], k, v, x["idx"], x["o"], x["lse"], x["ws"], **scales)
-        x["out_h"].copy_(x["out_d"], non_blocking=True)
-        x["ev"].record()
+        x["plan"].run_host(q_h, k, v, idx_h, x["o_h"], x["lse_h"], x["ws"], stream=x["stream"], **scales)
+        x["ev"].record(x["stream"])
 
     def e2e_loop(n, in_flight):
         for i in range(n):
@@ -812,36 +805,26 @@ def run_ours(args):
         e2e_loop(e2e_steps, in_flight)
         e2e[in_flight] = (time.perf_counter() - t1) / e2e_steps
     for x in bufs:
-        x["plan"].device_status(x["ws"])
+        x["plan"].device_status(x["ws"], stream=x["stream"])
     e2e_s, e2e_serial_s = max_over_ranks([e2e[2], e2e[1]], dev, world)
+    # Where a step's time goes, one step at a time (medians over the e2e
+    # steps): planning on the host, the run_host call (host time to enqueue
+    # the upload, copies and kernels), and the wait until the result is on
+    # the host.
     x0 = bufs[0]
-    ws, in_d, out_d, out_h = x0["ws"], x0["in_d"], x0["out_d"], x0["out_h"]
-    q_e, idx_e, o_e, lse_e = x0["q"], x0["idx"], x0["o"], x0["lse"]
-    # Where an end-to-end step's time goes: the same calls, each followed by
-    # a synchronize and timed on the host (medians over the e2e steps).
-    parts = {"plan": [], "upload": [], "h2d": [], "run": [], "d2h": []}
+    parts = {"plan": [], "run_host_call": [], "wait": []}
     for _ in range(e2e_steps):
         t = time.perf_counter()
         p2 = new_plan()
         parts["plan"].append(time.perf_counter() - t)
         t = time.perf_counter()
-        p2.upload(ws)
-        torch.cuda.synchronize()
-        parts["upload"].append(time.perf_counter() - t)
+        p2.run_host(q_h, k, v, idx_h, x0["o_h"], x0["lse_h"], x0["ws"], stream=x0["stream"], **scales)
+        parts["run_host_call"].append(time.perf_counter() - t)
         t = time.perf_counter()
-        in_d.copy_(in_h, non_blocking=True)
-        torch.cuda.synchronize()
-        parts["h2d"].append(time.perf_counter() - t)
-        t = time.perf_counter()
-        p2.run(q_e, k, v, idx_e, o_e, lse_e, ws, **scales)
-        torch.cuda.synchronize()
-        parts["run"].append(time.perf_counter() - t)
-        t = time.perf_counter()
-        out_h.copy_(out_d, non_blocking=True)
-        torch.cuda.synchronize()
-        parts["d2h"].append(time.perf_counter() - t)
+        x0["stream"].synchronize()
+        parts["wait"].append(time.perf_counter() - t)
     breakdown = {k2: round(statistics.median(v2) * 1e6, 1) for k2, v2 in parts.items()}
-    del flush, in_d, out_d, bufs
+    del flush, bufs
     torch.cuda.empty_cache()
 
     detail = {}

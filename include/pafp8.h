@@ -224,6 +224,35 @@ pafp8_status pafp8_run(const pafp8_plan *plan, int32_t q_dtype, const void *q,
                        int32_t o_dtype, void *o, float *lse, void *workspace,
                        size_t workspace_bytes, void *stream);
 
+/* One step of the plan from and to host memory, for callers whose q,
+ * kv_indices, o and lse live on the host (the same attention as pafp8_run).
+ * On `stream`, in this order: the plan's metadata is uploaded to `workspace`
+ * (as pafp8_plan_upload), q and kv_indices are copied from host memory into
+ * a staging area at the end of `workspace`, the attention runs on them (as
+ * pafp8_run), and o and lse are copied back into host memory.  The call
+ * returns once all of it is enqueued; o_h and lse_h hold the results when the
+ * stream has reached this point (e.g. after cudaStreamSynchronize or an event
+ * recorded after the call).
+ *   q_h          host, [nnz_qo, num_qo_heads, head_dim] of q_dtype
+ *   kv_indices_h host int32 [kv_indptr_h[batch]] (may be NULL if that is 0)
+ *   o_h          host, [nnz_qo, num_qo_heads, head_dim] of o_dtype
+ *   lse_h        host float [nnz_qo, num_qo_heads] or NULL
+ *   workspace    device, 256-byte aligned, at least
+ *                pafp8_host_workspace_bytes(plan, q_dtype) bytes; the caller
+ *                owns it and must not reuse it (nor the host buffers) until
+ *                the stream has passed this call
+ * The host buffers should be page-locked (cudaHostAlloc / pinned) for the
+ * copies to be asynchronous; pageable memory works but the copies then
+ * synchronize with the host.  Other arguments and checks are those of
+ * pafp8_run; on a refusal by those checks the metadata upload may already be
+ * enqueued, nothing else is. */
+size_t pafp8_host_workspace_bytes(const pafp8_plan *plan, int32_t q_dtype);
+pafp8_status pafp8_run_host(pafp8_plan *plan, int32_t q_dtype, const void *q_h, int32_t k_dtype,
+                            const void *k_cache, int32_t v_dtype, const void *v_cache,
+                            const int32_t *kv_indices_h, float q_scale, float k_scale, float v_scale,
+                            int32_t o_dtype, void *o_h, float *lse_h, void *workspace,
+                            size_t workspace_bytes, void *stream);
+
 /* pafp8_run restricted to one stage of the launch sequence, for callers that
  * time or overlap the stages separately:
  *   stage 0  everything (same as pafp8_run);

@@ -42,7 +42,7 @@ _NAME_CODES = {"default": DTYPE_DEFAULT, "f16": F16, "float16": F16, "bf16": BF1
 EXPORTS = ("pafp8_abi_version", "pafp8_last_error", "pafp8_plan_create", "pafp8_plan_destroy",
            "pafp8_workspace_bytes", "pafp8_plan_metadata", "pafp8_plan_upload", "pafp8_run",
            "pafp8_run_stage", "pafp8_device_status", "pafp8_run_decode_noalloc", "pafp8_append_kv",
-           "pafp8_run_head_scales", "pafp8_run_pod")
+           "pafp8_run_head_scales", "pafp8_run_pod", "pafp8_host_workspace_bytes", "pafp8_run_host")
 
 
 class Pafp8Error(RuntimeError):
@@ -99,6 +99,9 @@ def lib() -> ctypes.CDLL:
     L.pafp8_run_stage.argtypes = [vp, i32, i32, vp, i32, vp, i32, vp, vp, f32, f32, f32, i32, vp, vp,
                                   vp, sz, vp]
     L.pafp8_run_stage.restype = i32
+    L.pafp8_host_workspace_bytes.argtypes, L.pafp8_host_workspace_bytes.restype = [vp, i32], sz
+    L.pafp8_run_host.argtypes = [vp, i32, vp, i32, vp, i32, vp, vp, f32, f32, f32, i32, vp, vp, vp, sz, vp]
+    L.pafp8_run_host.restype = i32
     L.pafp8_device_status.argtypes, L.pafp8_device_status.restype = [vp, vp, vp], i32
     L.pafp8_run_decode_noalloc.argtypes = [vp, i32, vp, i32, vp, i32, vp, vp, f32, f32, f32, i32, vp,
                                            vp, vp]
@@ -214,6 +217,24 @@ def pafp8_run(handle: int, q, k_cache, v_cache, kv_indices, o, lse, workspace, *
         dtype_code(v_dtype if v_dtype is not None else v_cache.dtype), _ptr(v_cache),
         _ptr(kv_indices), float(q_scale), float(k_scale), float(v_scale),
         dtype_code(o_dtype if o_dtype is not None else o.dtype), _ptr(o), _ptr(lse),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def pafp8_host_workspace_bytes(handle: int, q_dtype) -> int:
+    return int(lib().pafp8_host_workspace_bytes(handle, dtype_code(q_dtype)))
+
+
+def pafp8_run_host(handle: int, q_h, k_cache, v_cache, kv_indices_h, o_h, lse_h, workspace, *, q_scale=1.0,
+                   k_scale=1.0, v_scale=1.0, q_dtype=None, k_dtype=None, v_dtype=None, o_dtype=None,
+                   stream=None) -> None:
+    """One step from and to host memory (q_h, kv_indices_h, o_h, lse_h: CPU
+    tensors, preferably pinned); dtype codes default to the tensors' own."""
+    _check(lib().pafp8_run_host(
+        handle, dtype_code(q_dtype if q_dtype is not None else q_h.dtype), _ptr(q_h),
+        dtype_code(k_dtype if k_dtype is not None else k_cache.dtype), _ptr(k_cache),
+        dtype_code(v_dtype if v_dtype is not None else v_cache.dtype), _ptr(v_cache),
+        _ptr(kv_indices_h), float(q_scale), float(k_scale), float(v_scale),
+        dtype_code(o_dtype if o_dtype is not None else o_h.dtype), _ptr(o_h), _ptr(lse_h),
         _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
@@ -341,6 +362,12 @@ class Plan:
 
     def run(self, q, k_cache, v_cache, kv_indices, o, lse, workspace, **kw) -> None:
         pafp8_run(self.handle, q, k_cache, v_cache, kv_indices, o, lse, workspace, **kw)
+
+    def host_workspace_bytes(self, q_dtype) -> int:
+        return pafp8_host_workspace_bytes(self.handle, q_dtype)
+
+    def run_host(self, q_h, k_cache, v_cache, kv_indices_h, o_h, lse_h, workspace, **kw) -> None:
+        pafp8_run_host(self.handle, q_h, k_cache, v_cache, kv_indices_h, o_h, lse_h, workspace, **kw)
 
     def run_head_scales(self, q, k_cache, v_cache, kv_indices, o, lse, workspace, **kw) -> None:
         pafp8_run_head_scales(self.handle, q, k_cache, v_cache, kv_indices, o, lse, workspace, **kw)

@@ -151,6 +151,28 @@ namespace {
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Device staging of pafp8_run_host, after the plan's own workspace bytes: q,
+// kv_indices, o and lse, each 256-byte aligned.
+struct HostStaging {
+    size_t q, idx, o, lse, end;
+    size_t q_bytes, idx_bytes, o_bytes, lse_bytes;
+};
+HostStaging host_staging(const pafp8_plan* plan, int32_t q_dtype) {
+    const pafp8_plan_desc& d = plan->desc;
+    HostStaging h{};
+    const size_t rows = (size_t)plan->nnz_qo * (size_t)d.num_qo_heads;
+    h.q_bytes = rows * (size_t)d.head_dim * (is_fp8(q_dtype) ? 1 : 2);
+    h.idx_bytes = plan->kv_indptr.empty() ? 0 : (size_t)plan->kv_indptr.back() * 4;
+    h.o_bytes = rows * (size_t)d.head_dim * 2;
+    h.lse_bytes = rows * 4;
+    h.q = align_up(plan->ws_bytes, 256);
+    h.idx = align_up(h.q + h.q_bytes, 256);
+    h.o = align_up(h.idx + h.idx_bytes, 256);
+    h.lse = align_up(h.o + h.o_bytes, 256);
+    h.end = h.lse + h.lse_bytes;
+    return h;
+}
+
 // Decode partition.  Rows are (request b, KV-head block hb), row r = b*nhb + hb,
 // each holding the npages[b] pages of its request.  The rule:
 //   disable_split_kv: one segment per non-empty row; CTA i takes segments
@@ -1108,6 +1130,57 @@ pafp8_status pafp8_run(const pafp8_plan* plan, int32_t q_dtype, const void* q, i
                        size_t workspace_bytes, void* stream) {
     return run_impl(plan, 0, q_dtype, q, k_dtype, k_cache, v_dtype, v_cache, kv_indices, q_scale, k_scale,
                     v_scale, nullptr, nullptr, nullptr, o_dtype, o, lse, workspace, workspace_bytes, stream);
+}
+
+size_t pafp8_host_workspace_bytes(const pafp8_plan* plan, int32_t q_dtype) {
+    return plan ? host_staging(plan, q_dtype).end : 0;
+}
+
+pafp8_status pafp8_run_host(pafp8_plan* plan, int32_t q_dtype, const void* q_h, int32_t k_dtype,
+                            const void* k_cache, int32_t v_dtype, const void* v_cache,
+                            const int32_t* kv_indices_h, float q_scale, float k_scale, float v_scale,
+                            int32_t o_dtype, void* o_h, float* lse_h, void* workspace,
+                            size_t workspace_bytes, void* stream) {
+    if (plan == nullptr) return fail(PAFP8_ERR_ARG, "plan is NULL");
+    const HostStaging hs = host_staging(plan, q_dtype);
+    if (workspace_bytes < hs.end)
+        return fail(PAFP8_ERR_WORKSPACE, "workspace has %zu bytes; a host-buffer step of this plan needs %zu",
+                    workspace_bytes, hs.end);
+    if (hs.q_bytes > 0 && (q_h == nullptr || o_h == nullptr))
+        return fail(PAFP8_ERR_ARG, "q_h and o_h must be non-NULL");
+    if (hs.idx_bytes > 0 && kv_indices_h == nullptr) return fail(PAFP8_ERR_ARG, "kv_indices_h must be non-NULL");
+    pafp8_status st = pafp8_plan_upload(plan, workspace, workspace_bytes, stream);
+    if (st != PAFP8_OK) return st;
+    char* ws = (char*)workspace;
+    void* q_d = ws + hs.q;
+    void* o_d = ws + hs.o;
+    const int32_t* idx_d = (const int32_t*)(ws + hs.idx);
+    float* lse_d = lse_h != nullptr ? (float*)(ws + hs.lse) : nullptr;
+    if ((st = run_impl(plan, 0, q_dtype, q_d, k_dtype, k_cache, v_dtype, v_cache, idx_d, q_scale, k_scale,
+                       v_scale, nullptr, nullptr, nullptr, o_dtype, o_d, lse_d, workspace, workspace_bytes, stream,
+                       false)) != PAFP8_OK)
+        return st;
+    cudaStream_t s = (cudaStream_t)stream;
+    cudaError_t e = cudaSuccess;
+    if (hs.q_bytes > 0) e = cudaMemcpyAsync(q_d, q_h, hs.q_bytes, cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess && hs.idx_bytes > 0)
+        e = cudaMemcpyAsync(ws + hs.idx, kv_indices_h, hs.idx_bytes, cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(PAFP8_ERR_CUDA, "copying q and kv_indices to the device failed: %s", cudaGetErrorString(e));
+    }
+    if ((st = run_impl(plan, 0, q_dtype, q_d, k_dtype, k_cache, v_dtype, v_cache, idx_d, q_scale, k_scale,
+                       v_scale, nullptr, nullptr, nullptr, o_dtype, o_d, lse_d, workspace, workspace_bytes,
+                       stream)) != PAFP8_OK)
+        return st;
+    if (hs.o_bytes > 0) e = cudaMemcpyAsync(o_h, o_d, hs.o_bytes, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess && lse_h != nullptr && hs.lse_bytes > 0)
+        e = cudaMemcpyAsync(lse_h, lse_d, hs.lse_bytes, cudaMemcpyDeviceToHost, s);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(PAFP8_ERR_CUDA, "copying o and lse to the host failed: %s", cudaGetErrorString(e));
+    }
+    return PAFP8_OK;
 }
 
 pafp8_status pafp8_run_stage(const pafp8_plan* plan, int32_t stage, int32_t q_dtype, const void* q,

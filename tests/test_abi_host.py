@@ -283,6 +283,21 @@ def test_run_refuses_bad_scales():
         pa.pafp8_plan_destroy(h)
 
 
+def test_run_host_refuses_a_small_workspace():
+    """pafp8_run_host checks its workspace (the plan's bytes, then staging for
+    q, kv_indices, o and lse) before any device work."""
+    h = _create()
+    try:
+        need = pa.lib().pafp8_host_workspace_bytes(h, pa.BF16)
+        assert need > pa.pafp8_workspace_bytes(h)
+        assert pa.lib().pafp8_host_workspace_bytes(h, pa.E4M3FN) < need  # 1-byte q staging
+        st = pa.lib().pafp8_run_host(h, pa.BF16, 16, pa.E4M3FN, 16, pa.E4M3FN, 16, 16, 1.0, 1.0, 1.0,
+                                     pa.BF16, 16, None, 256, need - 1, None)
+        assert st == 4 and "host-buffer step" in pa.pafp8_last_error()
+    finally:
+        pa.pafp8_plan_destroy(h)
+
+
 # ------------------------------------------------------------ prefill plans
 
 def _prefill_plan(kv_lens, qo_lens, *, hq=32, hkv=8, num_ctas=152, page_size=16, head_dim=128, kv_dtype="e4m3fn"):
