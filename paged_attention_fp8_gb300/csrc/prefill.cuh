@@ -439,23 +439,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             auto qk = [&](int x) {
                 const uint32_t dS = tmem + col_s(x);
                 const uint32_t qa = base + L::q + x * L::kQTile;
-                // Descriptor offsets are added inside each MMA block (see
-                // tc_mma_*_at): start addresses are 16-byte units.
+                // The K steps' descriptor offsets are immediates inside one asm
+                // statement (tc_mma_*_k*): start addresses are 16-byte units.
                 if (kF8) {
                     // fp8 rows of DH bytes: 128- or 64-byte swizzle, 32 B per K step
                     const uint64_t dq = DH == 128 ? sw128_kmajor_desc(qa) : sw64_kmajor_desc(qa);
                     const uint32_t ka = base + L::kr + kring.idx * Dm::kRawTile;
                     const uint64_t dk = DH == 128 ? sw128_kmajor_desc(ka) : sw64_kmajor_desc(ka);
-#pragma unroll
-                    for (int ks = 0; ks < DH / 32; ++ks)
-                        tc_mma_f8_ss_at(dS, dq, dk, (uint32_t)(ks * 32) >> 4, idesc_qk, ks > 0 ? 1u : 0u);
+                    if constexpr (DH == 128) tc_mma_f8_ss_k4(dS, dq, dk, idesc_qk, 0u);
+                    else tc_mma_f8_ss_k2(dS, dq, dk, idesc_qk, 0u);
                 } else {
+                    // 2-byte rows of DH elements: DH / 64 halves of 128 B, 32 B per K step
                     const uint64_t dq = sw128_kmajor_desc(qa);
                     const uint64_t dk = sw128_kmajor_desc(base + L::k16 + kring.idx * Dm::kF16Tile);
-#pragma unroll
-                    for (int ks = 0; ks < DH / 16; ++ks)
-                        tc_mma_f16_ss_at(dS, dq, dk, ((ks >> 2) * kHalfTile + (ks & 3) * 32) >> 4, idesc_qk,
-                                         ks > 0 ? 1u : 0u);
+                    if constexpr (DH == 128) tc_mma_f16_ss_k8<kHalfTile, kHalfTile>(dS, dq, dk, idesc_qk, 0u);
+                    else tc_mma_f16_ss_k4(dS, dq, dk, idesc_qk, 0u);
                 }
                 tc_commit(bar(L::bSFull + x));
                 ++issued_any;
@@ -472,11 +470,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 pphase[x] ^= 1u;
                 tc_fence_after();
                 const uint64_t dv = sw128_kmajor_desc(base + L::v16 + v16.idx * Dm::kVtTile);
-#pragma unroll
-                for (int ks = 0; ks < 8; ++ks)
-                    tc_mma_f16_ts_at(tmem + col_o<DH>(x), tmem + col_s(x) + 8 * ks, dv,
-                                     ((ks >> 2) * Dm::kVtHalf + (ks & 3) * 32) >> 4, idesc_pv,
-                                     (accumulate || ks > 0) ? 1u : 0u);
+                // K = 128 keys: 8 steps of 16, Vᵀ's two 64-key halves kVtHalf apart.
+                tc_mma_f16_ts_k8<Dm::kVtHalf>(tmem + col_o<DH>(x), tmem + col_s(x), dv, idesc_pv,
+                                              accumulate ? 1u : 0u);
                 ++issued_any;
                 return true;
             };

@@ -304,10 +304,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             auto qk = [&](int x) {
                 const uint64_t dq = sw128_kmajor_desc(base + L::q + x * L::kQTile);
                 const uint64_t dk = sw128_kmajor_desc(base + L::k16 + kring.idx * L::kK16);
-#pragma unroll
-                for (int ks = 0; ks < DH / 16; ++ks)
-                    tc_mma_pair_f16_ss(tmem + col_s(x), dq, dk, ((ks >> 2) * kHalfTile + (ks & 3) * 32) >> 4,
-                                       ((ks >> 2) * kHalf64 + (ks & 3) * 32) >> 4, idesc_qk, ks > 0 ? 1u : 0u);
+                tc_mma_pair_f16_ss_k8<kHalfTile, kHalf64>(tmem + col_s(x), dq, dk, idesc_qk, 0u);
                 tc_commit_pair(bar(L::bSFull + x), kBoth);
                 ++issued_any;
             };
@@ -325,11 +322,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 pphase[x] ^= 1u;
                 tc_fence_after();
                 const uint64_t dv = sw128_kmajor_desc(base + L::v16 + v16.idx * L::kVt);
-#pragma unroll
-                for (int ks = 0; ks < 8; ++ks)
-                    tc_mma_pair_f16_ts(tmem + col_o<DH>(x), tmem + col_s(x) + 8 * ks, dv,
-                                       ((ks >> 2) * kHalf64 + (ks & 3) * 32) >> 4, idesc_pv,
-                                       (accumulate || ks > 0) ? 1u : 0u);
+                tc_mma_pair_f16_ts_k8<kHalf64>(tmem + col_o<DH>(x), tmem + col_s(x), dv, idesc_pv,
+                                               accumulate ? 1u : 0u);
                 ++issued_any;
                 return true;
             };

@@ -358,65 +358,97 @@ __host__ __device__ constexpr uint32_t make_idesc(int a_fmt, int b_fmt, int m, i
            ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
 }
 
-__device__ __forceinline__ void tc_mma_f16_ss(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
-                                              uint32_t accum) {
-    asm volatile(
-        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
-        "l"(a), "l"(b), "r"(idesc), "r"(accum)
-        : "memory");
-}
+// One product's K steps from a single asm statement: the descriptors'
+// start offsets (16-byte units) are immediate operands, the first MMA
+// accumulates into D when `accum` is nonzero and the others always, so an MMA
+// costs two 64-bit adds besides itself (instead of also widening a register
+// offset and setting its own predicate).  kind::f16 A and B in shared memory
+// with K = 8 x 16 over two 128-byte halves (ha, hb: bytes between a
+// descriptor's first and second half), kind::f16 with K = 4 x 16 in one half,
+// kind::f8f6f4 with K = 4 x 32 or 2 x 32, and kind::f16 with A in TMEM (8
+// columns per K step of 16 2-byte elements).
+#define PAFP8_K8_SS_BODY(CG)                                                                          \
+    "{\n .reg .pred p, t;\n .reg .b64 da, db;\n setp.ne.b32 p, %4, 0;\n setp.eq.b32 t, %4, %4;\n"     \
+    " tcgen05.mma.cta_group::" CG ".kind::f16 [%0], %1, %2, %3, p;\n"                                \
+    " add.s64 da, %1, 2;\n add.s64 db, %2, 2;\n tcgen05.mma.cta_group::" CG ".kind::f16 [%0], da, db, %3, t;\n" \
+    " add.s64 da, %1, 4;\n add.s64 db, %2, 4;\n tcgen05.mma.cta_group::" CG ".kind::f16 [%0], da, db, %3, t;\n" \
+    " add.s64 da, %1, 6;\n add.s64 db, %2, 6;\n tcgen05.mma.cta_group::" CG ".kind::f16 [%0], da, db, %3, t;\n" \
+    " add.s64 da, %1, %5;\n add.s64 db, %2, %6;\n tcgen05.mma.cta_group::" CG ".kind::f16 [%0], da, db, %3, t;\n" \
+    " add.s64 da, %1, %7;\n add.s64 db, %2, %8;\n tcgen05.mma.cta_group::" CG ".kind::f16 [%0], da, db, %3, t;\n" \
+    " add.s64 da, %1, %9;\n add.s64 db, %2, %10;\n tcgen05.mma.cta_group::" CG ".kind::f16 [%0], da, db, %3, t;\n" \
+    " add.s64 da, %1, %11;\n add.s64 db, %2, %12;\n tcgen05.mma.cta_group::" CG ".kind::f16 [%0], da, db, %3, t;\n}\n"
+#define PAFP8_K8_SS_ARGS(HA, HB)                                                                       \
+    "r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(accum), "n"((HA) >> 4), "n"((HB) >> 4), "n"(((HA) >> 4) + 2), \
+        "n"(((HB) >> 4) + 2), "n"(((HA) >> 4) + 4), "n"(((HB) >> 4) + 4), "n"(((HA) >> 4) + 6), "n"(((HB) >> 4) + 6)
+#define PAFP8_K8_TS_BODY(CG)                                                                          \
+    "{\n .reg .pred p, t;\n .reg .b64 db;\n .reg .b32 ta;\n setp.ne.b32 p, %4, 0;\n setp.eq.b32 t, %4, %4;\n" \
+    " tcgen05.mma.cta_group::" CG ".kind::f16 [%0], [%1], %2, %3, p;\n"                              \
+    " add.u32 ta, %1, 8;\n add.s64 db, %2, 2;\n tcgen05.mma.cta_group::" CG ".kind::f16 [%0], [ta], db, %3, t;\n" \
+    " add.u32 ta, %1, 16;\n add.s64 db, %2, 4;\n tcgen05.mma.cta_group::" CG ".kind::f16 [%0], [ta], db, %3, t;\n" \
+    " add.u32 ta, %1, 24;\n add.s64 db, %2, 6;\n tcgen05.mma.cta_group::" CG ".kind::f16 [%0], [ta], db, %3, t;\n" \
+    " add.u32 ta, %1, 32;\n add.s64 db, %2, %5;\n tcgen05.mma.cta_group::" CG ".kind::f16 [%0], [ta], db, %3, t;\n" \
+    " add.u32 ta, %1, 40;\n add.s64 db, %2, %6;\n tcgen05.mma.cta_group::" CG ".kind::f16 [%0], [ta], db, %3, t;\n" \
+    " add.u32 ta, %1, 48;\n add.s64 db, %2, %7;\n tcgen05.mma.cta_group::" CG ".kind::f16 [%0], [ta], db, %3, t;\n" \
+    " add.u32 ta, %1, 56;\n add.s64 db, %2, %8;\n tcgen05.mma.cta_group::" CG ".kind::f16 [%0], [ta], db, %3, t;\n}\n"
+#define PAFP8_K8_TS_ARGS(HB)                                                                           \
+    "r"(d_tmem), "r"(a_tmem), "l"(b), "r"(idesc), "r"(accum), "n"((HB) >> 4), "n"(((HB) >> 4) + 2),     \
+        "n"(((HB) >> 4) + 4), "n"(((HB) >> 4) + 6)
 
-__device__ __forceinline__ void tc_mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
-                                              uint32_t idesc, uint32_t accum) {
+template <uint32_t HA, uint32_t HB>
+__device__ __forceinline__ void tc_mma_f16_ss_k8(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                                 uint32_t accum) {
+    asm volatile(PAFP8_K8_SS_BODY("1")::PAFP8_K8_SS_ARGS(HA, HB) : "memory");
+}
+template <uint32_t HA, uint32_t HB>
+__device__ __forceinline__ void tc_mma_pair_f16_ss_k8(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                                      uint32_t accum) {
+    asm volatile(PAFP8_K8_SS_BODY("2")::PAFP8_K8_SS_ARGS(HA, HB) : "memory");
+}
+template <uint32_t HB>
+__device__ __forceinline__ void tc_mma_f16_ts_k8(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                                                 uint32_t accum) {
+    asm volatile(PAFP8_K8_TS_BODY("1")::PAFP8_K8_TS_ARGS(HB) : "memory");
+}
+template <uint32_t HB>
+__device__ __forceinline__ void tc_mma_pair_f16_ts_k8(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                                                      uint32_t accum) {
+    asm volatile(PAFP8_K8_TS_BODY("2")::PAFP8_K8_TS_ARGS(HB) : "memory");
+}
+__device__ __forceinline__ void tc_mma_f16_ss_k4(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                                 uint32_t accum) {
     asm volatile(
-        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b), "r"(idesc), "r"(accum)
+        "{\n .reg .pred p, t;\n .reg .b64 da, db;\n setp.ne.b32 p, %4, 0;\n setp.eq.b32 t, %4, %4;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n"
+        " add.s64 da, %1, 2;\n add.s64 db, %2, 2;\n tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, t;\n"
+        " add.s64 da, %1, 4;\n add.s64 db, %2, 4;\n tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, t;\n"
+        " add.s64 da, %1, 6;\n add.s64 db, %2, 6;\n tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, t;\n}\n"
+        ::"r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(accum)
         : "memory");
 }
-
-__device__ __forceinline__ void tc_mma_f8_ss(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
-                                             uint32_t accum) {
+__device__ __forceinline__ void tc_mma_f8_ss_k4(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                                uint32_t accum) {
     asm volatile(
-        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-        " tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
-        "l"(a), "l"(b), "r"(idesc), "r"(accum)
+        "{\n .reg .pred p, t;\n .reg .b64 da, db;\n setp.ne.b32 p, %4, 0;\n setp.eq.b32 t, %4, %4;\n"
+        " tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n"
+        " add.s64 da, %1, 2;\n add.s64 db, %2, 2;\n tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], da, db, %3, t;\n"
+        " add.s64 da, %1, 4;\n add.s64 db, %2, 4;\n tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], da, db, %3, t;\n"
+        " add.s64 da, %1, 6;\n add.s64 db, %2, 6;\n tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], da, db, %3, t;\n}\n"
+        ::"r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(accum)
         : "memory");
 }
-
-// The same MMAs with both shared-memory descriptors advanced by `off`
-// (a byte offset >> 4) inside the instruction block, so that a loop over K
-// steps keeps one base descriptor per operand live instead of one per step.
-__device__ __forceinline__ void tc_mma_f16_ss_at(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t off,
-                                                 uint32_t idesc, uint32_t accum) {
+__device__ __forceinline__ void tc_mma_f8_ss_k2(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                                uint32_t accum) {
     asm volatile(
-        "{\n .reg .pred p;\n .reg .b64 da, db, o;\n setp.ne.b32 p, %5, 0;\n cvt.u64.u32 o, %3;\n"
-        " add.s64 da, %1, o;\n add.s64 db, %2, o;\n"
-        " tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %4, p;\n}\n" ::"r"(d_tmem),
-        "l"(a), "l"(b), "r"(off), "r"(idesc), "r"(accum)
+        "{\n .reg .pred p, t;\n .reg .b64 da, db;\n setp.ne.b32 p, %4, 0;\n setp.eq.b32 t, %4, %4;\n"
+        " tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n"
+        " add.s64 da, %1, 2;\n add.s64 db, %2, 2;\n tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], da, db, %3, t;\n}\n"
+        ::"r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(accum)
         : "memory");
 }
-
-__device__ __forceinline__ void tc_mma_f8_ss_at(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t off,
-                                                uint32_t idesc, uint32_t accum) {
-    asm volatile(
-        "{\n .reg .pred p;\n .reg .b64 da, db, o;\n setp.ne.b32 p, %5, 0;\n cvt.u64.u32 o, %3;\n"
-        " add.s64 da, %1, o;\n add.s64 db, %2, o;\n"
-        " tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], da, db, %4, p;\n}\n" ::"r"(d_tmem),
-        "l"(a), "l"(b), "r"(off), "r"(idesc), "r"(accum)
-        : "memory");
-}
-
-__device__ __forceinline__ void tc_mma_f16_ts_at(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t off,
-                                                 uint32_t idesc, uint32_t accum) {
-    asm volatile(
-        "{\n .reg .pred p;\n .reg .b64 db, o;\n setp.ne.b32 p, %5, 0;\n cvt.u64.u32 o, %3;\n"
-        " add.s64 db, %2, o;\n"
-        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %4, p;\n}\n" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b), "r"(off), "r"(idesc), "r"(accum)
-        : "memory");
-}
+#undef PAFP8_K8_SS_BODY
+#undef PAFP8_K8_SS_ARGS
+#undef PAFP8_K8_TS_BODY
+#undef PAFP8_K8_TS_ARGS
 
 // Arrive (count 1) on `bar` when every tcgen05 operation this thread issued
 // before has completed.
@@ -520,26 +552,6 @@ __device__ __forceinline__ void tc_commit_pair(uint32_t bar, uint16_t mask) {
     asm volatile(
         "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
         "h"(mask)
-        : "memory");
-}
-// Pair MMAs (kind::f16), A and B from shared memory (descriptor start
-// offsets oa, ob in 16-byte units), or A from TMEM.
-__device__ __forceinline__ void tc_mma_pair_f16_ss(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t oa, uint32_t ob,
-                                                   uint32_t idesc, uint32_t accum) {
-    asm volatile(
-        "{\n .reg .pred p;\n .reg .b64 da, db, o1, o2;\n setp.ne.b32 p, %6, 0;\n cvt.u64.u32 o1, %3;\n"
-        " cvt.u64.u32 o2, %4;\n add.s64 da, %1, o1;\n add.s64 db, %2, o2;\n"
-        " tcgen05.mma.cta_group::2.kind::f16 [%0], da, db, %5, p;\n}\n" ::"r"(d_tmem),
-        "l"(a), "l"(b), "r"(oa), "r"(ob), "r"(idesc), "r"(accum)
-        : "memory");
-}
-__device__ __forceinline__ void tc_mma_pair_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t off,
-                                                   uint32_t idesc, uint32_t accum) {
-    asm volatile(
-        "{\n .reg .pred p;\n .reg .b64 db, o;\n setp.ne.b32 p, %5, 0;\n cvt.u64.u32 o, %3;\n"
-        " add.s64 db, %2, o;\n"
-        " tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], db, %4, p;\n}\n" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b), "r"(off), "r"(idesc), "r"(accum)
         : "memory");
 }
 // TMA loads into this CTA's shared memory whose completion (bytes) is counted
