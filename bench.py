@@ -62,12 +62,12 @@ L2_FLUSH_BYTES = 256 << 20
 # workload, from one ncu capture of the kernel source with this SHA-256; a
 # changed kernel reports null until it is captured again.
 NCU_TRAFFIC = {
-    "24f608db83bd1121191e8d71b2fc88b51739b40edecf86c2722153bb0f610010": 309843456,
+    "8c94b805d7f854b2a685a89adaf643807277c06c16f5fca2b27cb39f45c3fc53": 309745408,
 }
 # The same for the prefill kernels, per workload index, keyed by the SHA-256
 # of their sources (prefill.cuh, then prefill_pair.cuh).
 NCU_TRAFFIC_PREFILL = {
-    "0a4fb3437cc861471ffa743dfb1d09d5a0a929940ca9d87c0e325c2a26359840": {4: 169775616, 5: 193140480, 7: 269439488},
+    "e6017f6282700ff53e68771983e9aec8f4994c9cc2dcf030194270ed9ff5be19": {4: 169904896, 5: 191994112, 7: 272324096},
 }
 
 
