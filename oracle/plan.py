@@ -189,9 +189,11 @@ def prefill_metadata(kv_indptr, last_page_len, qo_indptr, *, num_qo_heads, num_k
     bottom-right causal rule, capped by the request's own key tiles.
     Each tile record is (b, hk, t0, nkv, qo_indptr[b], qo_len, kv_len,
     kv_indptr[b]).  Tiles are sorted by that count, descending, ties in
-    (b, hk, t0) order.  G persistent CTAs take items i, i + G, ... (G =
-    min(num_ctas, #items)); pairs: G = 2 min(max(1, num_ctas // 2), #items)
-    CTAs, pair i taking items i, i + G / 2, ..."""
+    (b, hk, t0) order.  G = min(num_ctas, #items) persistent CTAs (pairs:
+    G = 2 min(max(1, num_ctas // 2), #items) CTAs, G / 2 pairs) take the
+    items in snake order: in round r worker i takes item r W + i for even r
+    and r W + W - 1 - i for odd r (W = G, or G / 2 pairs).  The order is
+    the kernels'; the metadata holds the list."""
     kv_indptr = [int(x) for x in kv_indptr]
     last_page_len = [int(x) for x in last_page_len]
     qo_indptr = [int(x) for x in qo_indptr]

@@ -398,7 +398,9 @@ void build_decode_meta(pafp8_plan* pl) {
 // consecutive new tokens starting at t0 (TQ = 128 / group), one item of two
 // query tiles of TQ * group packed rows each.  n_kv = the KV tiles of 128 keys
 // the item's last token may see (bottom-right causal).  Items are ordered
-// longest first (stable), and persistent CTA i takes items i, i + G, ...
+// longest first (stable); the kernels deal them to the G persistent CTAs (or
+// CTA pairs) in snake order: round r gives worker i item r G + i for even r
+// and r G + G - 1 - i for odd r.
 // (G = min(num_ctas, #items)).
 void build_prefill_meta(pafp8_plan* pl) {
     const int B = pl->desc.batch;

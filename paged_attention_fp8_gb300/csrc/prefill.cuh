@@ -16,8 +16,8 @@
 // rows each, packed as (token, head-of-group) pairs -- 128/group consecutive
 // new tokens times the group's query heads per tile, B right after A -- so a
 // dequantized K/V tile serves 256 query rows.  KV tiles are 128 keys (8
-// pages).  Persistent CTAs take items i, i + grid, ... from a longest-first
-// list built by the plan.
+// pages).  Persistent CTAs take items from a longest-first list built by the
+// plan, dealt in snake order (item_at).
 //
 // Roles (512 threads, four warpgroups; registers are moved by setmaxnreg from
 // the dequant warpgroup (64) and the producer/MMA warpgroup (64) to the two
@@ -171,6 +171,14 @@ __device__ __forceinline__ int tile_nkv(int t0, int x, int TQ, int qo_len, int k
     return min((kv_len + kTileKeys - 1) / kTileKeys, lim / kTileKeys + 1);
 }
 
+// The item that persistent worker i of G takes in round r.  Items are sorted
+// longest first; even rounds deal them to workers 0 .. G-1, odd rounds back
+// from G-1 to 0 (a snake), so each worker's total evens out while the items
+// in flight at any time are the same neighbours as in plain round robin.  A
+// worker stops at its first round whose item is past the list (no later
+// round has one for it).
+__device__ __forceinline__ int item_at(int r, int i, int G) { return r * G + ((r & 1) ? G - 1 - i : i); }
+
 __device__ __forceinline__ void set_abort(uint32_t flag_addr, uint32_t* status) {
     asm volatile("st.shared.u32 [%0], 1;" ::"r"(flag_addr) : "memory");
     atomicOr(status, kStatusTimeout);
@@ -285,7 +293,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         constexpr int nkr = k2 ? L::NK16 : L::NKR;
         constexpr int bkf = k2 ? L::bK16Full : L::bKrFull, bke = k2 ? L::bK16Empty : L::bKrEmpty;
         bool ok = true;
-        for (int t = blockIdx.x; t < n_items && ok; t += gridDim.x) {
+        for (int rnd = 0, t = blockIdx.x; t < n_items && ok; t = item_at(++rnd, blockIdx.x, gridDim.x)) {
             const Item it = load_item(items, t);
             const int q0 = it.qo0 + it.t0;
             if (lane == 0) {
@@ -476,7 +484,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ++issued_any;
                 return true;
             };
-            for (int t = blockIdx.x; t < n_items && ok; t += gridDim.x) {
+            for (int rnd = 0, t = blockIdx.x; t < n_items && ok; t = item_at(++rnd, blockIdx.x, gridDim.x)) {
                 const Item it = load_item(items, t);
                 const int qo_len = it.qo_len;
                 const int kv_len = it.kv_len;
@@ -541,7 +549,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int wd = warp, q8 = lane >> 3, e = lane & 7;
         Ring kr, vr, k16, v16;
         bool ok = true;
-        for (int t = blockIdx.x; t < n_items && ok; t += gridDim.x) {
+        for (int rnd = 0, t = blockIdx.x; t < n_items && ok; t = item_at(++rnd, blockIdx.x, gridDim.x)) {
             const Item it = load_item(items, t);
             const int kv_len = it.kv_len;
             for (int j = 0; j < it.nkv && ok; ++j) {
@@ -731,7 +739,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // for the epilogues.
         float up_next = 1.f;
         if (fit_q && (int)blockIdx.x < n_items) up_next = fit_row();
-        for (int t = blockIdx.x; t < n_items && ok; t += gridDim.x) {
+        for (int rnd = 0, t = blockIdx.x; t < n_items && ok; t = item_at(++rnd, blockIdx.x, gridDim.x)) {
             const Item it = load_item(items, t);
             const int qo0 = it.qo0;
             const int qo_len = it.qo_len;
@@ -848,7 +856,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 m = m_use;
             }
             if (!ok) break;
-            if (fit_q && t + (int)gridDim.x < n_items) {
+            if (fit_q && item_at(rnd + 1, blockIdx.x, gridDim.x) < n_items) {
                 up_next = fit_row();
                 if (!ok) break;
             }

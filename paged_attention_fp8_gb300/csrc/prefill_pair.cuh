@@ -177,7 +177,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t qphase = 0;
         long long issued_k = 0, issued_v = 0, issued_q = 0;
         bool ok = true;
-        for (int t = pair_id; t < n_items && ok; t += n_pairs) {
+        for (int rnd = 0, t = pair_id; t < n_items && ok; t = item_at(++rnd, pair_id, n_pairs)) {
             const Item it = load_item(items, t);
             // Q: this CTA's rows of tiles A and B (tokens t0 + 2 TQ x + TQ r),
             // one box per 64-dim half, lane 2 x + h; the bytes of both CTAs
@@ -327,7 +327,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ++issued_any;
                 return true;
             };
-            for (int t = pair_id; t < n_items && ok; t += n_pairs) {
+            for (int rnd = 0, t = pair_id; t < n_items && ok; t = item_at(++rnd, pair_id, n_pairs)) {
                 const Item it = load_item(items, t);
                 const int nA = tile_nkv(it.t0, 0, TQ2, it.qo_len, it.kv_len);
                 const int nB = tile_nkv(it.t0, 1, TQ2, it.qo_len, it.kv_len);
@@ -397,7 +397,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int wd = warp;
         Ring vr, v16;
         bool ok = true;
-        for (int t = pair_id; t < n_items && ok; t += n_pairs) {
+        for (int rnd = 0, t = pair_id; t < n_items && ok; t = item_at(++rnd, pair_id, n_pairs)) {
             const Item it = load_item(items, t);
             for (int j = 0; j < it.nkv && ok; ++j) {
                 const int valid = min(kTileKeys, it.kv_len - j * kTileKeys);
@@ -445,7 +445,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t sphase = 0, ophase = 0;
         const bool o_32b = (reinterpret_cast<uintptr_t>(p.o) & 31u) == 0;  // rows are 256 B apart
         bool ok = true;
-        for (int t = pair_id; t < n_items && ok; t += n_pairs) {
+        for (int rnd = 0, t = pair_id; t < n_items && ok; t = item_at(++rnd, pair_id, n_pairs)) {
             const Item it = load_item(items, t);
             const int qo0 = it.qo0;
             const int qo_len = it.qo_len;
