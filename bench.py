@@ -67,7 +67,7 @@ NCU_TRAFFIC = {
 # The same for the prefill kernels, per workload index, keyed by the SHA-256
 # of their sources (prefill.cuh, then prefill_pair.cuh).
 NCU_TRAFFIC_PREFILL = {
-    "e6017f6282700ff53e68771983e9aec8f4994c9cc2dcf030194270ed9ff5be19": {4: 169904896, 5: 191994112, 7: 272324096},
+    "05a01c73485f3c97cb30c81eecc90fa66682ea2055eda3d1d16b331abcd96a7b": {4: 168418816, 5: 190214656, 7: 260830720},
 }
 
 
