@@ -23,7 +23,9 @@
 // the dequant warpgroup (64) and the producer/MMA warpgroup (64) to the two
 // softmax warpgroups (192), which hold a whole S row without spilling):
 //   warps 0-3   dequant: raw fp8 K -> f16 K tile (2-byte query path); raw fp8
-//               V -> f16 V^T tile (both paths), zero beyond the request's keys;
+//               V -> f16 V tile (both paths; a 2-byte V tile is copied), in
+//               the layout a 2-byte tile lands in ([64-dim half][key][128 B]),
+//               zero beyond the request's keys;
 //   warps 4-7   softmax of tile A, warps 8-11 softmax of tile B: thread r owns
 //               TMEM lane r = query row r of its tile.  Reads S, masks, keeps
 //               the running max and sum, writes P (f16) over the first half of
@@ -46,10 +48,11 @@
 // barrier ahead of the wait).
 // The tensor pipe runs one CTA's MMAs in order, so an MMA writing S_X after
 // O_X += P_X V has been issued cannot overtake it, and s_full(X, j) implies
-// that the previous O update of X is complete.  Every operand in shared
-// memory is K-major with the 128-byte swizzle (64-byte for the 64-byte fp8
-// rows of head_dim 64).  All waits are bounded; on expiry the kernel records a
-// status bit and winds down.
+// that the previous O update of X is complete.  Q and K in shared memory are
+// K-major operands with the 128-byte swizzle (64-byte for the 64-byte fp8 rows
+// of head_dim 64); V is the MN-major B operand of P V (dims along 128-byte
+// rows, one row per key), so no role transposes it.  All waits are bounded; on
+// expiry the kernel records a status bit and winds down.
 //
 // Pages of 16 m tokens (m > 1) are read as m sub-pages of 16: the TMA box of
 // sub-page j is at token slot 16 j of its page, which covers both layouts.
@@ -78,9 +81,7 @@ struct Dims {
     static constexpr int NH = DH / 64;                       // 128-B halves of a 2-byte row
     static constexpr uint32_t kRawTile = kTileKeys * DH;      // fp8 K or V tile (128 keys)
     static constexpr uint32_t kRawPage = kPageSize * DH;      // fp8 page box (16 tokens)
-    static constexpr uint32_t kF16Tile = NH * kHalfTile;      // 2-byte K tile (128 keys) or Q tile
-    static constexpr uint32_t kVtHalf = DH * 128;             // V^T rows (dims) over 64 keys
-    static constexpr uint32_t kVtTile = 2 * kVtHalf;          // V^T tile: dims x 128 keys
+    static constexpr uint32_t kF16Tile = NH * kHalfTile;      // 2-byte K or V tile (128 keys) or Q tile
 };
 template <int DH>
 __device__ __forceinline__ uint32_t col_o(int x) { return 256u + (uint32_t)DH * (uint32_t)x; }  // O_X
@@ -92,12 +93,13 @@ struct Layout {
     // dequant of K_{j+1} may start while QK_B(j) still reads K_j) and keeps a
     // single raw fp8 stage per tensor; the fp8 path multiplies raw K directly.
     // A 2-byte cache (k2) brings K straight into the 16-bit K tiles and only
-    // transposes V, so it has no raw K stage and a 2-byte raw V stage.
+    // copies V (zeroing the keys past the request's end), so it has no raw K
+    // stage and a 2-byte raw V stage.
     static constexpr int NKR = kF8 ? 4 : (k2 ? 0 : 1);  // raw K stages
     static constexpr int NVR = kF8 ? 2 : 1;             // raw V stages
     static constexpr uint32_t kRawV = k2 ? Dm::kF16Tile : Dm::kRawTile;
     static constexpr int NK16 = kF8 ? 0 : 2;   // f16 K stages
-    static constexpr int NV16 = 2;             // f16 V^T stages
+    static constexpr int NV16 = 2;             // f16 V stages
     static constexpr uint32_t kQTile = kF8 ? kTileRows * DH : Dm::kF16Tile;
     static constexpr uint32_t q = 0;                     // Q_A, then Q_B
     static constexpr uint32_t kr = 2 * kQTile;
@@ -106,7 +108,7 @@ struct Layout {
     static constexpr uint32_t v16 = k16 + NK16 * Dm::kF16Tile;
     // fp8 query: a 16 KB staging half per query tile for the output's bulk
     // tensor stores (64 dims of 128 rows, 128-byte rows swizzled).
-    static constexpr uint32_t ostage = v16 + NV16 * Dm::kVtTile;
+    static constexpr uint32_t ostage = v16 + NV16 * Dm::kF16Tile;
     static constexpr uint32_t bars = ostage + (kF8 ? 2 * kHalfTile : 0);
     // barrier indices (8 bytes each)
     static constexpr int bQFull = 0, bQReady = 1, bQEmpty = 2;
@@ -433,7 +435,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t idesc_qk =
                 kF8 ? make_idesc(p.q_dtype == PAFP8_E5M2 ? 1 : 0, KT == PAFP8_E5M2 ? 1 : 0, 128, 128)
                     : make_idesc(kBF ? 1 : 0, kBF ? 1 : 0, 128, 128);
-            const uint32_t idesc_pv = make_idesc(kBF ? 1 : 0, kBF ? 1 : 0, 128, DH);
+            const uint32_t idesc_pv = make_idesc_bmn(kBF ? 1 : 0, kBF ? 1 : 0, 128, DH);
             const int nk = kF8 ? L::NKR : L::NK16;
             const int kfull = kF8 ? L::bKrFull : L::bK16Full;
             const int kempty = kF8 ? L::bKrEmpty : L::bK16Empty;
@@ -477,10 +479,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!wait_or_abort<kDiag>(bar(L::bPFull + x), pphase[x], flag_addr, p.status, p.wait_cycles)) return false;
                 pphase[x] ^= 1u;
                 tc_fence_after();
-                const uint64_t dv = sw128_kmajor_desc(base + L::v16 + v16.idx * Dm::kVtTile);
-                // K = 128 keys: 8 steps of 16, Vᵀ's two 64-key halves kVtHalf apart.
-                tc_mma_f16_ts_k8<Dm::kVtHalf>(tmem + col_o<DH>(x), tmem + col_s(x), dv, idesc_pv,
-                                              accumulate ? 1u : 0u);
+                // V [64-dim half][key][128 B] as the MN-major B operand: K = 128
+                // keys in 8 steps of 16 rows, the dim halves kHalfTile apart.
+                const uint64_t dv = sw128_mnmajor_desc(base + L::v16 + v16.idx * Dm::kF16Tile, kHalfTile);
+                tc_mma_f16_ts_mn_k8(tmem + col_o<DH>(x), tmem + col_s(x), dv, idesc_pv, accumulate ? 1u : 0u);
                 ++issued_any;
                 return true;
             };
@@ -549,6 +551,43 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int wd = warp, q8 = lane >> 3, e = lane & 7;
         Ring kr, vr, k16, v16;
         bool ok = true;
+        // A raw fp8 K or V tile [key][DH bytes] -> f16 [64-dim half][key][128 B]
+        // under the 128-byte swizzle (the layout a 2-byte tile lands in), keys
+        // `valid` and beyond zeroed.  K serves as the K-major B operand of Q K^T,
+        // V as the MN-major B operand of P V.
+        auto widen = [&](uint32_t src, uint32_t dst, int valid) {
+            if constexpr (k2) {
+                return;  // a 2-byte cache has no fp8 tile
+            } else if constexpr (DH == 128) {
+#pragma unroll 2
+                for (int i = 0; i < 8; ++i) {
+                    const int combo = wd * 8 + i;
+                    const int row = (combo >> 1) * 8 + e;
+                    const int c = (combo & 1) * 4 + q8;
+                    uint4 w = lds128(src + row * 128 + ((c ^ e) << 4));
+                    if (row >= valid) w = make_uint4(0u, 0u, 0u, 0u);
+                    const uint32_t hb = dst + (c >> 2) * kHalfTile + row * 128;
+                    sts128(hb + (((2 * q8) ^ e) << 4), fp8x2_lo<KT>(w.x), fp8x2_hi<KT>(w.x), fp8x2_lo<KT>(w.y),
+                           fp8x2_hi<KT>(w.y));
+                    sts128(hb + (((2 * q8 + 1) ^ e) << 4), fp8x2_lo<KT>(w.z), fp8x2_hi<KT>(w.z), fp8x2_lo<KT>(w.w),
+                           fp8x2_hi<KT>(w.w));
+                }
+            } else {
+                // 64-B fp8 rows under the 64-byte swizzle (16-byte chunk c of
+                // row r at c ^ ((r >> 1) & 3)) -> one 128-B f16 half.
+#pragma unroll 2
+                for (int i = 0; i < 4; ++i) {
+                    const int row = (wd * 4 + i) * 8 + e, c = q8;
+                    uint4 w = lds128(src + row * 64 + ((c ^ ((row >> 1) & 3)) << 4));
+                    if (row >= valid) w = make_uint4(0u, 0u, 0u, 0u);
+                    const uint32_t hb = dst + row * 128;
+                    sts128(hb + (((2 * c) ^ e) << 4), fp8x2_lo<KT>(w.x), fp8x2_hi<KT>(w.x), fp8x2_lo<KT>(w.y),
+                           fp8x2_hi<KT>(w.y));
+                    sts128(hb + (((2 * c + 1) ^ e) << 4), fp8x2_lo<KT>(w.z), fp8x2_hi<KT>(w.z), fp8x2_lo<KT>(w.w),
+                           fp8x2_hi<KT>(w.w));
+                }
+            }
+        };
         for (int rnd = 0, t = blockIdx.x; t < n_items && ok; t = item_at(++rnd, blockIdx.x, gridDim.x)) {
             const Item it = load_item(items, t);
             const int kv_len = it.kv_len;
@@ -558,35 +597,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ok = wait_or_abort<kDiag>(bar(L::bKrFull + kr.idx), kr.phase, flag_addr, p.status, p.wait_cycles) &&
                          wait_or_abort<kDiag>(bar(L::bK16Empty + k16.idx), k16.phase ^ 1u, flag_addr, p.status, p.wait_cycles);
                     if (!ok) break;
-                    const uint32_t src = base + L::kr + kr.idx * Dm::kRawTile;
-                    const uint32_t dst = base + L::k16 + k16.idx * Dm::kF16Tile;
-                    if constexpr (DH == 128) {
-#pragma unroll 2
-                        for (int i = 0; i < 8; ++i) {
-                            const int combo = wd * 8 + i;
-                            const int row = (combo >> 1) * 8 + e;
-                            const int c = (combo & 1) * 4 + q8;
-                            const uint4 w = lds128(src + row * 128 + ((c ^ e) << 4));
-                            const uint32_t hb = dst + (c >> 2) * kHalfTile + row * 128;
-                            sts128(hb + (((2 * q8) ^ e) << 4), fp8x2_lo<KT>(w.x), fp8x2_hi<KT>(w.x),
-                                   fp8x2_lo<KT>(w.y), fp8x2_hi<KT>(w.y));
-                            sts128(hb + (((2 * q8 + 1) ^ e) << 4), fp8x2_lo<KT>(w.z), fp8x2_hi<KT>(w.z),
-                                   fp8x2_lo<KT>(w.w), fp8x2_hi<KT>(w.w));
-                        }
-                    } else {
-                        // 64-B fp8 rows under the 64-byte swizzle (16-byte chunk c of
-                        // row r at c ^ ((r >> 1) & 3)) -> one 128-B f16 half.
-#pragma unroll 2
-                        for (int i = 0; i < 4; ++i) {
-                            const int row = (wd * 4 + i) * 8 + e, c = q8;
-                            const uint4 w = lds128(src + row * 64 + ((c ^ ((row >> 1) & 3)) << 4));
-                            const uint32_t hb = dst + row * 128;
-                            sts128(hb + (((2 * c) ^ e) << 4), fp8x2_lo<KT>(w.x), fp8x2_hi<KT>(w.x),
-                                   fp8x2_lo<KT>(w.y), fp8x2_hi<KT>(w.y));
-                            sts128(hb + (((2 * c + 1) ^ e) << 4), fp8x2_lo<KT>(w.z), fp8x2_hi<KT>(w.z),
-                                   fp8x2_lo<KT>(w.w), fp8x2_hi<KT>(w.w));
-                        }
-                    }
+                    widen(base + L::kr + kr.idx * Dm::kRawTile, base + L::k16 + k16.idx * Dm::kF16Tile, kTileKeys);
                     fence_async_smem();
                     mbar_arrive(bar(L::bK16Full + k16.idx));
                     mbar_arrive(bar(L::bKrEmpty + kr.idx));
@@ -597,80 +608,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                      wait_or_abort<kDiag>(bar(L::bV16Empty + v16.idx), v16.phase ^ 1u, flag_addr, p.status, p.wait_cycles);
                 if (!ok) break;
                 const uint32_t src = base + L::vr + vr.idx * L::kRawV;
-                const uint32_t dst = base + L::v16 + v16.idx * Dm::kVtTile;
+                const uint32_t dst = base + L::v16 + v16.idx * Dm::kF16Tile;
                 if constexpr (k2) {
-                    // 16-bit V [half][key][128 B] -> V^T [key half][dim][128 B], by
-                    // 8x8 tiles (8 keys x 8 dims) transposed in ldmatrix: warp wd
-                    // takes key blocks 4wd .. 4wd+3, all 16 dim blocks; keys past the
-                    // request's end are zeroed.
-                    // (DH / 32 ldmatrix groups of 4 dim blocks per key block.)
-                    constexpr int kGroups = DH / 32;
-                    const int tr = lane & 7, tm = lane >> 3;
-#pragma unroll 1
-                    for (int ab = 0; ab < 4 * kGroups; ++ab) {
-                        const int a = 4 * wd + ab / kGroups, gq = ab % kGroups;
-                        const int b = 4 * gq + tm;  // this lane's source tile
-                        const int key_row = 8 * a + tr;
-                        uint32_t w[4];
-                        ldsm_x4_trans(src + (b >> 3) * kHalfTile + key_row * 128 + (((b & 7) ^ tr) << 4), w[0], w[1],
-                                      w[2], w[3]);
-                        const int k0 = 8 * a + 2 * (lane & 3);  // keys k0, k0+1 of word m
-#pragma unroll
-                        for (int m = 0; m < 4; ++m) {
-                            const int bm = 4 * gq + m;
-                            const int dim = 8 * bm + (lane >> 2);
-                            uint32_t x = w[m];
-                            if (k0 >= valid) x &= 0xFFFF0000u;
-                            if (k0 + 1 >= valid) x &= 0x0000FFFFu;
-                            sts32(dst + (a >> 3) * Dm::kVtHalf + dim * 128 + (((a & 7) ^ (dim & 7)) << 4) +
-                                      4 * (lane & 3),
-                                  x);
-                        }
+                    // A 2-byte V tile is already in the layout the MMA reads: copied
+                    // 16 bytes per thread and step (consecutive threads, consecutive
+                    // chunks), keys past the request's end zeroed.
+#pragma unroll 2
+                    for (int i = 0; i < 8 * NH; ++i) {
+                        const int q = i * 128 + (int)threadIdx.x;
+                        const uint32_t off = (uint32_t)q * 16u;  // [half][key][128 B]
+                        const int row = (q >> 3) & (kTileKeys - 1);
+                        uint4 w = lds128(src + off);
+                        if (row >= valid) w = make_uint4(0u, 0u, 0u, 0u);
+                        sts128(dst + off, w.x, w.y, w.z, w.w);
                     }
                 } else {
-                const int kb = e + 8 * (q8 >> 1);  // key block (8 keys)
-                // DH / 64 rounds: the (key block, dim block) pairs, 8 x 8 each.
-#pragma unroll 1
-                for (int rr = 0; rr < DH / 64; ++rr) {
-                    const int a = DH == 128 ? (q8 & 1) * 8 + ((e + 2 * wd + rr) & 7)  // dim block (8 dims)
-                                            : (q8 & 1) * 4 + ((e + wd) & 3);
-                    uint32_t w0[8], w1[8];
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const int row = kb * 8 + i;
-                        // 128-B rows (128-byte swizzle, row & 7 = i) or 64-B rows
-                        // (64-byte swizzle: chunk c of row r at c ^ ((r >> 1) & 3))
-                        const uint2 v = DH == 128
-                                            ? lds64(src + row * 128 + ((((a >> 1) ^ i) << 4)) + (a & 1) * 8)
-                                            : lds64(src + row * 64 + ((((a >> 1) ^ ((row >> 1) & 3)) << 4)) + (a & 1) * 8);
-                        const bool live = row < valid;
-                        w0[i] = live ? v.x : 0u;
-                        w1[i] = live ? v.y : 0u;
-                    }
-                    // T[d][k] = f16x2 of (key 2k, key 2k+1) for dim d of the block.
-                    uint32_t T[8][4];
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const uint32_t x0 = prmt(w0[2 * k], w0[2 * k + 1], 0x5140u);
-                        const uint32_t x1 = prmt(w0[2 * k], w0[2 * k + 1], 0x7362u);
-                        const uint32_t y0 = prmt(w1[2 * k], w1[2 * k + 1], 0x5140u);
-                        const uint32_t y1 = prmt(w1[2 * k], w1[2 * k + 1], 0x7362u);
-                        T[0][k] = fp8x2_lo<KT>(x0);
-                        T[1][k] = fp8x2_hi<KT>(x0);
-                        T[2][k] = fp8x2_lo<KT>(x1);
-                        T[3][k] = fp8x2_hi<KT>(x1);
-                        T[4][k] = fp8x2_lo<KT>(y0);
-                        T[5][k] = fp8x2_hi<KT>(y0);
-                        T[6][k] = fp8x2_lo<KT>(y1);
-                        T[7][k] = fp8x2_hi<KT>(y1);
-                    }
-                    const uint32_t hb = dst + (kb >> 3) * Dm::kVtHalf;
-#pragma unroll
-                    for (int d = 0; d < 8; ++d) {
-                        const int row = a * 8 + d;
-                        sts128(hb + row * 128 + (((kb & 7) ^ d) << 4), T[d][0], T[d][1], T[d][2], T[d][3]);
-                    }
-                }
+                    widen(src, dst, valid);
                 }
                 fence_async_smem();
                 mbar_arrive(bar(L::bV16Full + v16.idx));

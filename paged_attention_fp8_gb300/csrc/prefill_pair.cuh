@@ -8,24 +8,26 @@
 // h / group (bottom-right causal mask), lse = ln sum exp(logits).  The query
 // and the cache have the same 2-byte dtype, which the MMAs take as loaded.
 //
-// Why pairs here: with a 2-byte cache the single-CTA kernel is bound by its V
-// transposition (one warpgroup turns 128 keys x 128 dims of V into V^T per
-// tile) and by the TMA issue of 32 half-page boxes per tile.  A pair issues
+// Why pairs here: with a 2-byte cache a single CTA spends its producer on the
+// TMA issue of 32 half-page boxes per tile.  A pair issues
 // tcgen05.mma.cta_group::2 with M = 256 from the leader CTA: each CTA holds
 // its 128 rows of the query tile (and of S, P and O in its TMEM) and half of
-// the other operand's N rows at the same shared-memory offset -- keys
+// the other operand's N columns at the same shared-memory offset -- keys
 // 64 r .. 64 r + 63 of each K tile (QK: N = keys), dims 64 r .. 64 r + 63 of
-// V^T (PV: N = dims).  So each CTA loads half of every K and V tile and
-// transposes half of V.  (With an fp8 cache the single-CTA kernel stays
-// faster: there the serial per-tile chain QK -> softmax -> P hand-off -> PV
-// bounds it, and a pair lengthens the hand-offs, which cross SMs.)
+// each V tile (PV: N = dims).  So each CTA loads half of every K and V tile.
+// V is the MN-major B operand of P V exactly as its page boxes land
+// ([key][64 dims of 128 B]), so nothing transforms it.  (With an fp8 cache
+// the single-CTA kernel stays faster: there the serial per-tile chain QK ->
+// softmax -> P hand-off -> PV bounds it, and a pair lengthens the hand-offs,
+// which cross SMs.)
 //
 // Work item: (request, KV head, two query tiles A and B of 2 TQ tokens each);
 // CTA r of the pair owns tokens [t0 + 2 TQ x + TQ r, + TQ) of tile x, i.e.
 // 128 packed (token, head) rows per tile, as one CTA of prefill.cuh.
 //
 // Roles per CTA (512 threads; registers moved by setmaxnreg as in prefill.cuh):
-//   warps 0-3   V -> V^T of this CTA's 64 dims, zero beyond the request's keys;
+//   warps 0-3   V release: zero the keys past the request's end in a request's
+//               last V tile, then mark the tile ready for the leader;
 //   warps 4-7   softmax of tile A, warps 8-11 of tile B (prefill.cuh's);
 //   warp 12     TMA producer: this CTA's Q rows, its K pages, its V dim half;
 //   warp 13     in the leader: MMA issuer (warps 14-15 and the peer's 13-15
@@ -47,23 +49,21 @@ constexpr uint32_t kHalf64 = kPairKeys * 128;  // 8 KB: 64 rows x 128 B
 
 struct PairLayout {
     // Q: two tiles of [dim half][128 rows][128 B]; 16-bit K: [dim half][64
-    // keys][128 B] (this CTA's keys); raw V: [128 keys][128 B] (this CTA's 64
-    // dims); V^T: [key half][64 dims][128 B].
-    static constexpr int NK16 = 2, NVR = 2, NV16 = 2;
+    // keys][128 B] (this CTA's keys); V: [128 keys][128 B] (this CTA's 64
+    // dims), four stages, each held from its copy to the P V MMAs' commit.
+    static constexpr int NK16 = 2, NVR = 4;
     static constexpr uint32_t kQTile = 2 * kHalfTile;  // 32 KB
     static constexpr uint32_t kK16 = 2 * kHalf64;      // 16 KB
     static constexpr uint32_t kRawV = kTileKeys * 128;  // 16 KB
-    static constexpr uint32_t kVt = 2 * kHalf64;        // 16 KB
     static constexpr uint32_t q = 0;
     static constexpr uint32_t k16 = 2 * kQTile;
     static constexpr uint32_t vr = k16 + NK16 * kK16;
-    static constexpr uint32_t v16 = vr + NVR * kRawV;
-    static constexpr uint32_t bars = v16 + NV16 * kVt;
+    static constexpr uint32_t bars = vr + NVR * kRawV;
     static constexpr int bQFull = 0, bQEmpty = 1;
     static constexpr int bK16Full = 2, bK16Empty = bK16Full + NK16;
     static constexpr int bVrFull = bK16Empty + NK16, bVrEmpty = bVrFull + NVR;
-    static constexpr int bV16Full = bVrEmpty + NVR, bV16Empty = bV16Full + NV16;
-    static constexpr int bSFull = bV16Empty + NV16;  // [2]
+    static constexpr int bVReady = bVrEmpty + NVR;   // [NVR], in the leader
+    static constexpr int bSFull = bVReady + NVR;     // [2]
     static constexpr int bPFull = bSFull + 2;        // [2]
     static constexpr int bOFull = bPFull + 2;        // [2]
     static constexpr int bOEmpty = bOFull + 2;       // [2]
@@ -74,7 +74,7 @@ struct PairLayout {
     static constexpr uint32_t bytes = abort_flag + 4;
 };
 static_assert(1024 + PairLayout::bytes <= 232448, "shared memory budget (pair)");
-static_assert(PairLayout::k16 % 1024 == 0 && PairLayout::vr % 1024 == 0 && PairLayout::v16 % 1024 == 0,
+static_assert(PairLayout::k16 % 1024 == 0 && PairLayout::vr % 1024 == 0,
               "1024-byte alignment of the pair tiles");
 
 // wait_or_abort with acquire at cluster scope, for barriers that the peer CTA
@@ -140,11 +140,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int i = 0; i < L::NVR; ++i) {
             mbar_init(bar(L::bVrFull + i), 1);
-            mbar_init(bar(L::bVrEmpty + i), 4);  // this CTA's transposing warps
-        }
-        for (int i = 0; i < L::NV16; ++i) {
-            mbar_init(bar(L::bV16Full + i), 8);  // both CTAs' transposing warps
-            mbar_init(bar(L::bV16Empty + i), 1);
+            mbar_init(bar(L::bVrEmpty + i), 1);  // the P V MMAs' commit
+            mbar_init(bar(L::bVReady + i), 8);   // both CTAs' V-release warps
         }
         for (int x = 0; x < 2; ++x) {
             mbar_init(bar(L::bSFull + x), 1);
@@ -291,9 +288,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // commit arriving in both CTAs.
         if (lane == 0) {
             const uint32_t idesc_qk = make_idesc(kBF ? 1 : 0, kBF ? 1 : 0, 256, 128);
-            const uint32_t idesc_pv = make_idesc(kBF ? 1 : 0, kBF ? 1 : 0, 256, DH);
+            const uint32_t idesc_pv = make_idesc_bmn(kBF ? 1 : 0, kBF ? 1 : 0, 256, DH);
             constexpr uint16_t kBoth = 3;  // commit multicast to both CTAs of the pair
-            Ring kring, v16;
+            Ring kring, vring;
             uint32_t qphase = 0;
             uint32_t pphase[2] = {0, 0};
             int nonempty[2] = {0, 0};  // earlier items in which tile A / B had rows
@@ -308,8 +305,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_commit_pair(bar(L::bSFull + x), kBoth);
                 ++issued_any;
             };
-            // O_X (+)= P_X V: A = P_X from each CTA's TMEM, B = V^T [key half]
-            // [64 dims][128 B] of each CTA (N = 128 dims).
+            // O_X (+)= P_X V: A = P_X from each CTA's TMEM, B = V [key][64 dims
+            // of 128 B] of each CTA, MN-major (N = 128 dims, 64 per CTA).
             auto pv = [&](int x, bool accumulate) -> bool {
                 // The first O_X write of an item waits for the epilogue of the
                 // previous item that used O_X.
@@ -321,9 +318,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     return false;
                 pphase[x] ^= 1u;
                 tc_fence_after();
-                const uint64_t dv = sw128_kmajor_desc(base + L::v16 + v16.idx * L::kVt);
-                tc_mma_pair_f16_ts_k8<kHalf64>(tmem + col_o<DH>(x), tmem + col_s(x), dv, idesc_pv,
-                                               accumulate ? 1u : 0u);
+                // (one 64-column block per CTA: the leading byte offset is unused)
+                const uint64_t dv = sw128_mnmajor_desc(base + L::vr + vring.idx * L::kRawV, 16u);
+                tc_mma_pair_f16_ts_mn_k8(tmem + col_o<DH>(x), tmem + col_s(x), dv, idesc_pv, accumulate ? 1u : 0u);
                 ++issued_any;
                 return true;
             };
@@ -347,7 +344,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 kring.next(L::NK16);
                 if (n == 1) tc_commit_pair(bar(L::bQEmpty), kBoth);
                 for (int j = 0; j < n && ok; ++j) {
-                    ok = wait_or_abort_cl<kDiag>(bar(L::bV16Full + v16.idx), v16.phase, flag_addr, p.status,
+                    ok = wait_or_abort_cl<kDiag>(bar(L::bVReady + vring.idx), vring.phase, flag_addr, p.status,
                                                  p.wait_cycles);
                     if (!ok) break;
                     tc_fence_after();
@@ -367,8 +364,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (!(ok = pv(1, j > 0))) break;
                         if (j == nB - 1) tc_commit_pair(bar(L::bOFull + 1), kBoth);
                     }
-                    tc_commit_pair(bar(L::bV16Empty + v16.idx), kBoth);
-                    v16.next(L::NV16);
+                    tc_commit_pair(bar(L::bVrEmpty + vring.idx), kBoth);
+                    vring.next(L::NVR);
                     if (more) {
                         if (j + 1 < nB) qk(1);
                         tc_commit_pair(bar(L::bK16Empty + kring.idx), kBoth);
@@ -389,47 +386,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     } else if (warp < 4) {
         asm volatile("setmaxnreg.dec.sync.aligned.u32 64;" ::: "memory");
-        // ------------------------------------------------------- V -> V^T
-        // This CTA's 64 dims of each V tile, [key][128 B] -> [key half][dim]
-        // [128 B], by 8x8 tiles (8 keys x 8 dims) transposed in ldmatrix: warp
-        // wd takes key blocks 4 wd .. 4 wd + 3, all 8 dim blocks; keys past the
-        // request's end are zeroed.  Both CTAs arrive on the leader's barrier.
-        const int wd = warp;
-        Ring vr, v16;
+        // ------------------------------------------------------- V release
+        // Each V tile is read by the P V MMAs as it landed.  In a request's last
+        // tile the keys past its end (the tail of its last page, and rows no
+        // page of this tile filled) are zeroed first -- thread t takes key row
+        // t -- so that P = 0 there never meets a stray non-finite value.  Both
+        // CTAs arrive on the leader's barrier.
+        Ring vr;
         bool ok = true;
         for (int rnd = 0, t = pair_id; t < n_items && ok; t = item_at(++rnd, pair_id, n_pairs)) {
             const Item it = load_item(items, t);
             for (int j = 0; j < it.nkv && ok; ++j) {
                 const int valid = min(kTileKeys, it.kv_len - j * kTileKeys);
-                ok = wait_or_abort<kDiag>(bar(L::bVrFull + vr.idx), vr.phase, flag_addr, p.status, p.wait_cycles) &&
-                     wait_or_abort<kDiag>(bar(L::bV16Empty + v16.idx), v16.phase ^ 1u, flag_addr, p.status,
-                                          p.wait_cycles);
+                ok = wait_or_abort<kDiag>(bar(L::bVrFull + vr.idx), vr.phase, flag_addr, p.status, p.wait_cycles);
                 if (!ok) break;
-                const uint32_t src = base + L::vr + vr.idx * L::kRawV;
-                const uint32_t dst = base + L::v16 + v16.idx * L::kVt;
-                const int tr = lane & 7, tm = lane >> 3;
-#pragma unroll 1
-                for (int ab = 0; ab < 8; ++ab) {
-                    const int a = 4 * wd + (ab >> 1), gq = ab & 1;
-                    const int b = 4 * gq + tm;  // this lane's source tile (dim block)
-                    const int key_row = 8 * a + tr;
-                    uint32_t w[4];
-                    ldsm_x4_trans(src + key_row * 128 + ((b ^ tr) << 4), w[0], w[1], w[2], w[3]);
-                    const int k0 = 8 * a + 2 * (lane & 3);  // keys k0, k0+1 of word m
+                if (valid < kTileKeys) {
+                    if ((int)threadIdx.x >= valid) {
+                        const uint32_t row = base + L::vr + vr.idx * L::kRawV + threadIdx.x * 128u;
 #pragma unroll
-                    for (int m = 0; m < 4; ++m) {
-                        const int dim = 8 * (4 * gq + m) + (lane >> 2);
-                        uint32_t x = w[m];
-                        if (k0 >= valid) x &= 0xFFFF0000u;
-                        if (k0 + 1 >= valid) x &= 0x0000FFFFu;
-                        sts32(dst + (a >> 3) * kHalf64 + dim * 128 + (((a & 7) ^ (dim & 7)) << 4) + 4 * (lane & 3), x);
+                        for (int c = 0; c < 8; ++c) sts128(row + 16u * c, 0u, 0u, 0u, 0u);
                     }
+                    fence_async_smem();
                 }
-                fence_async_smem();
-                warp_arrive_cluster(lbar(L::bV16Full + v16.idx));
-                warp_arrive(bar(L::bVrEmpty + vr.idx));
+                warp_arrive_cluster(lbar(L::bVReady + vr.idx));
                 vr.next(L::NVR);
-                v16.next(L::NV16);
             }
         }
     } else {

@@ -177,17 +177,6 @@ __device__ __forceinline__ void sts32(uint32_t addr, uint32_t a) {
     asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(a) : "memory");
 }
 
-// Four 8x8 tiles of 16-bit elements, transposed on the way into registers:
-// lane l gives the address of row l & 7 of tile l >> 3 and receives, in word
-// m, elements (row 2(l%4), col l/4) and (row 2(l%4)+1, col l/4) of tile m.
-__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
-                                              uint32_t& r3) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-                 : "r"(addr)
-                 : "memory");
-}
-
 __device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
     asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
                  : "memory");
@@ -351,11 +340,31 @@ __device__ __forceinline__ uint64_t sw64_kmajor_desc(uint32_t saddr) {
     return d;
 }
 
+// An MN-major operand under the 128-byte swizzle: 128-byte rows of 64 2-byte
+// elements along M or N, one row per K index, 8-row atoms 1024 bytes apart
+// along K (stride byte offset); `lbo` bytes between the 64-element column
+// blocks along M or N (leading byte offset).  This is the layout a TMA box of
+// [K rows][64 elements] lands in, so a tile stored K-index-major (keys x dims)
+// serves as the B operand of O = P V without a transpose.
+__device__ __forceinline__ uint64_t sw128_mnmajor_desc(uint32_t saddr, uint32_t lbo) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;  // leading byte offset: next 64 columns
+    d |= (uint64_t)(1024 >> 4) << 32;              // stride byte offset: next 8 K rows
+    d |= (uint64_t)1 << 46;                        // descriptor version
+    d |= (uint64_t)2 << 61;                        // SWIZZLE_128B
+    return d;
+}
+
 // Instruction descriptor: f32 accumulator, K-major A and B, M x N.
 // a_fmt/b_fmt: kind::f16 -> 0 f16, 1 bf16; kind::f8f6f4 -> 0 e4m3, 1 e5m2.
 __host__ __device__ constexpr uint32_t make_idesc(int a_fmt, int b_fmt, int m, int n) {
     return (1u << 4) | ((uint32_t)a_fmt << 7) | ((uint32_t)b_fmt << 10) |
            ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+}
+// The same with an MN-major B operand (bit 16: B transposed).
+__host__ __device__ constexpr uint32_t make_idesc_bmn(int a_fmt, int b_fmt, int m, int n) {
+    return make_idesc(a_fmt, b_fmt, m, n) | (1u << 16);
 }
 
 // One product's K steps from a single asm statement: the descriptors'
@@ -366,7 +375,7 @@ __host__ __device__ constexpr uint32_t make_idesc(int a_fmt, int b_fmt, int m, i
 // with K = 8 x 16 over two 128-byte halves (ha, hb: bytes between a
 // descriptor's first and second half), kind::f16 with K = 4 x 16 in one half,
 // kind::f8f6f4 with K = 4 x 32 or 2 x 32, and kind::f16 with A in TMEM (8
-// columns per K step of 16 2-byte elements).
+// columns per K step of 16 2-byte elements) and an MN-major B.
 #define PAFP8_K8_SS_BODY(CG)                                                                          \
     "{\n .reg .pred p, t;\n .reg .b64 da, db;\n setp.ne.b32 p, %4, 0;\n setp.eq.b32 t, %4, %4;\n"     \
     " tcgen05.mma.cta_group::" CG ".kind::f16 [%0], %1, %2, %3, p;\n"                                \
@@ -380,19 +389,18 @@ __host__ __device__ constexpr uint32_t make_idesc(int a_fmt, int b_fmt, int m, i
 #define PAFP8_K8_SS_ARGS(HA, HB)                                                                       \
     "r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(accum), "n"((HA) >> 4), "n"((HB) >> 4), "n"(((HA) >> 4) + 2), \
         "n"(((HB) >> 4) + 2), "n"(((HA) >> 4) + 4), "n"(((HB) >> 4) + 4), "n"(((HA) >> 4) + 6), "n"(((HB) >> 4) + 6)
-#define PAFP8_K8_TS_BODY(CG)                                                                          \
+// The MN-major B (sw128_mnmajor_desc) of kind::f16 with A in TMEM: a K step
+// of 16 is 16 rows of 128 bytes, 2048 bytes on.
+#define PAFP8_K8_TS_MN_BODY(CG)                                                                       \
     "{\n .reg .pred p, t;\n .reg .b64 db;\n .reg .b32 ta;\n setp.ne.b32 p, %4, 0;\n setp.eq.b32 t, %4, %4;\n" \
     " tcgen05.mma.cta_group::" CG ".kind::f16 [%0], [%1], %2, %3, p;\n"                              \
-    " add.u32 ta, %1, 8;\n add.s64 db, %2, 2;\n tcgen05.mma.cta_group::" CG ".kind::f16 [%0], [ta], db, %3, t;\n" \
-    " add.u32 ta, %1, 16;\n add.s64 db, %2, 4;\n tcgen05.mma.cta_group::" CG ".kind::f16 [%0], [ta], db, %3, t;\n" \
-    " add.u32 ta, %1, 24;\n add.s64 db, %2, 6;\n tcgen05.mma.cta_group::" CG ".kind::f16 [%0], [ta], db, %3, t;\n" \
-    " add.u32 ta, %1, 32;\n add.s64 db, %2, %5;\n tcgen05.mma.cta_group::" CG ".kind::f16 [%0], [ta], db, %3, t;\n" \
-    " add.u32 ta, %1, 40;\n add.s64 db, %2, %6;\n tcgen05.mma.cta_group::" CG ".kind::f16 [%0], [ta], db, %3, t;\n" \
-    " add.u32 ta, %1, 48;\n add.s64 db, %2, %7;\n tcgen05.mma.cta_group::" CG ".kind::f16 [%0], [ta], db, %3, t;\n" \
-    " add.u32 ta, %1, 56;\n add.s64 db, %2, %8;\n tcgen05.mma.cta_group::" CG ".kind::f16 [%0], [ta], db, %3, t;\n}\n"
-#define PAFP8_K8_TS_ARGS(HB)                                                                           \
-    "r"(d_tmem), "r"(a_tmem), "l"(b), "r"(idesc), "r"(accum), "n"((HB) >> 4), "n"(((HB) >> 4) + 2),     \
-        "n"(((HB) >> 4) + 4), "n"(((HB) >> 4) + 6)
+    " add.u32 ta, %1, 8;\n add.s64 db, %2, 128;\n tcgen05.mma.cta_group::" CG ".kind::f16 [%0], [ta], db, %3, t;\n" \
+    " add.u32 ta, %1, 16;\n add.s64 db, %2, 256;\n tcgen05.mma.cta_group::" CG ".kind::f16 [%0], [ta], db, %3, t;\n" \
+    " add.u32 ta, %1, 24;\n add.s64 db, %2, 384;\n tcgen05.mma.cta_group::" CG ".kind::f16 [%0], [ta], db, %3, t;\n" \
+    " add.u32 ta, %1, 32;\n add.s64 db, %2, 512;\n tcgen05.mma.cta_group::" CG ".kind::f16 [%0], [ta], db, %3, t;\n" \
+    " add.u32 ta, %1, 40;\n add.s64 db, %2, 640;\n tcgen05.mma.cta_group::" CG ".kind::f16 [%0], [ta], db, %3, t;\n" \
+    " add.u32 ta, %1, 48;\n add.s64 db, %2, 768;\n tcgen05.mma.cta_group::" CG ".kind::f16 [%0], [ta], db, %3, t;\n" \
+    " add.u32 ta, %1, 56;\n add.s64 db, %2, 896;\n tcgen05.mma.cta_group::" CG ".kind::f16 [%0], [ta], db, %3, t;\n}\n"
 
 template <uint32_t HA, uint32_t HB>
 __device__ __forceinline__ void tc_mma_f16_ss_k8(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
@@ -404,15 +412,13 @@ __device__ __forceinline__ void tc_mma_pair_f16_ss_k8(uint32_t d_tmem, uint64_t 
                                                       uint32_t accum) {
     asm volatile(PAFP8_K8_SS_BODY("2")::PAFP8_K8_SS_ARGS(HA, HB) : "memory");
 }
-template <uint32_t HB>
-__device__ __forceinline__ void tc_mma_f16_ts_k8(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
-                                                 uint32_t accum) {
-    asm volatile(PAFP8_K8_TS_BODY("1")::PAFP8_K8_TS_ARGS(HB) : "memory");
+__device__ __forceinline__ void tc_mma_f16_ts_mn_k8(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                                                    uint32_t accum) {
+    asm volatile(PAFP8_K8_TS_MN_BODY("1")::"r"(d_tmem), "r"(a_tmem), "l"(b), "r"(idesc), "r"(accum) : "memory");
 }
-template <uint32_t HB>
-__device__ __forceinline__ void tc_mma_pair_f16_ts_k8(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
-                                                      uint32_t accum) {
-    asm volatile(PAFP8_K8_TS_BODY("2")::PAFP8_K8_TS_ARGS(HB) : "memory");
+__device__ __forceinline__ void tc_mma_pair_f16_ts_mn_k8(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
+                                                         uint32_t idesc, uint32_t accum) {
+    asm volatile(PAFP8_K8_TS_MN_BODY("2")::"r"(d_tmem), "r"(a_tmem), "l"(b), "r"(idesc), "r"(accum) : "memory");
 }
 __device__ __forceinline__ void tc_mma_f16_ss_k4(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
                                                  uint32_t accum) {
@@ -447,8 +453,7 @@ __device__ __forceinline__ void tc_mma_f8_ss_k2(uint32_t d_tmem, uint64_t a, uin
 }
 #undef PAFP8_K8_SS_BODY
 #undef PAFP8_K8_SS_ARGS
-#undef PAFP8_K8_TS_BODY
-#undef PAFP8_K8_TS_ARGS
+#undef PAFP8_K8_TS_MN_BODY
 
 // Arrive (count 1) on `bar` when every tcgen05 operation this thread issued
 // before has completed.
