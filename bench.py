@@ -67,7 +67,7 @@ NCU_TRAFFIC = {
 # The same for the prefill kernels, per workload index, keyed by the SHA-256
 # of their sources (prefill.cuh, then prefill_pair.cuh).
 NCU_TRAFFIC_PREFILL = {
-    "05a01c73485f3c97cb30c81eecc90fa66682ea2055eda3d1d16b331abcd96a7b": {4: 168418816, 5: 190214656, 7: 260830720},
+    "c34bae4595ec9e9f8938ec621e15a4b9531c4ec627d692c13ec8810ffd37c1ff": {4: 168458240, 5: 190431744, 7: 260687616},
 }
 
 
@@ -182,7 +182,7 @@ def time_prefill(index, dev, steps, warmup):
     out = {"workload": WORKLOADS[index], "value": round(tflops, 2), "unit": "TFLOP/s",
            "ms_per_launch": round(ms, 5), "flops": flops, "launches": steps,
            "mma": ("QK^T fp8 kind::f8f6f4, PV f16 kind::f16" if fp8 else
-                   "bf16 kind::f16 on CTA pairs (cta_group::2, M 256; 2-byte cache, V transposed in shared memory)"
+                   "bf16 kind::f16 on CTA pairs (cta_group::2, M 256; 2-byte cache, V read as the MN-major operand)"
                    if b.kv_dtype in ("f16", "bf16")
                    else "f16 kind::f16 (fp8 KV dequantized)")}
     if fp8:
@@ -306,6 +306,10 @@ def time_append(index, dev, steps, warmup):
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
     for i in range(steps):
         flush.sum()
+        # A ~50 us device-side wait after the eviction keeps the host's launch
+        # call ahead of the GPU, so the events bracket the append work alone
+        # (a ~10 us launch is shorter than the host's launch path).
+        torch.cuda._sleep(100_000)
         ev[i][0].record(stream)
         sample()
         ev[i][1].record(stream)
