@@ -692,8 +692,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // for the epilogues.
         float up_next = 1.f;
         if (fit_q && (int)blockIdx.x < n_items) up_next = fit_row();
+        Item it_next = (int)blockIdx.x < n_items ? load_item(items, blockIdx.x) : Item{};
         for (int rnd = 0, t = blockIdx.x; t < n_items && ok; t = item_at(++rnd, blockIdx.x, gridDim.x)) {
-            const Item it = load_item(items, t);
+            const Item it = it_next;
             const int qo0 = it.qo0;
             const int qo_len = it.qo_len;
             const int kv_len = it.kv_len;
@@ -809,6 +810,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 m = m_use;
             }
             if (!ok) break;
+            // The next item's record, loaded here so that its latency passes
+            // during the epilogue rather than before the next item's first pass.
+            {
+                const int tn = item_at(rnd + 1, blockIdx.x, gridDim.x);
+                if (tn < n_items) it_next = load_item(items, tn);
+            }
             if (fit_q && item_at(rnd + 1, blockIdx.x, gridDim.x) < n_items) {
                 up_next = fit_row();
                 if (!ok) break;

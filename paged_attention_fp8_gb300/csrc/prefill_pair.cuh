@@ -425,8 +425,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t sphase = 0, ophase = 0;
         const bool o_32b = (reinterpret_cast<uintptr_t>(p.o) & 31u) == 0;  // rows are 256 B apart
         bool ok = true;
+        Item it_next = pair_id < n_items ? load_item(items, pair_id) : Item{};
         for (int rnd = 0, t = pair_id; t < n_items && ok; t = item_at(++rnd, pair_id, n_pairs)) {
-            const Item it = load_item(items, t);
+            const Item it = it_next;
             const int qo0 = it.qo0;
             const int qo_len = it.qo_len;
             const int kv_len = it.kv_len;
@@ -529,6 +530,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 m = m_use;
             }
             if (!ok) break;
+            // The next item's record, loaded here so that its latency passes
+            // during the epilogue rather than before the next item's first pass.
+            {
+                const int tn = item_at(rnd + 1, pair_id, n_pairs);
+                if (tn < n_items) it_next = load_item(items, tn);
+            }
             if (nX == 0) continue;  // tile B past the request's last row
             // epilogue: the tile's last O update must have completed.
             ok = __all_sync(0xFFFFFFFFu,
