@@ -67,7 +67,7 @@ NCU_TRAFFIC = {
 # The same for the prefill kernels, per workload index, keyed by the SHA-256
 # of their sources (prefill.cuh, then prefill_pair.cuh).
 NCU_TRAFFIC_PREFILL = {
-    "c34bae4595ec9e9f8938ec621e15a4b9531c4ec627d692c13ec8810ffd37c1ff": {4: 168458240, 5: 190431744, 7: 260687616},
+    "777c6cad6dc1be02b46e60fa2abc794243500344954dfd0974603a89034bae74": {4: 168398592, 5: 189816064, 7: 255698176},
 }
 
 
