@@ -8,7 +8,7 @@ cudaError_t launch_prefill_d128(const PrefillParams& p, const CUtensorMap& tmap_
                                 const CUtensorMap& tmap_v, const CUtensorMap& tmap_o, int num_ctas,
                                 cudaStream_t stream) {
     if (p.kv_dtype == PAFP8_F16 || p.kv_dtype == PAFP8_BF16)
-        return launch_prefill_pair(p, tmap_q, tmap_k, tmap_v, num_ctas, stream);
+        return launch_prefill_pair(p, tmap_q, tmap_k, tmap_v, tmap_o, num_ctas, stream);
     return launch_prefill_head<128>(p, tmap_q, tmap_k, tmap_v, tmap_o, num_ctas, stream);
 }
 

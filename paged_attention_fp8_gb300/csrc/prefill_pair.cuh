@@ -58,7 +58,12 @@ struct PairLayout {
     static constexpr uint32_t q = 0;
     static constexpr uint32_t k16 = 2 * kQTile;
     static constexpr uint32_t vr = k16 + NK16 * kK16;
-    static constexpr uint32_t bars = vr + NVR * kRawV;
+    // Output staging: per query tile a [64-dim half][128 rows][128 B] copy of
+    // this CTA's O rows (the Q tile's swizzled layout), written out by two
+    // bulk tensor stores.
+    static constexpr uint32_t ostage = vr + NVR * kRawV;
+    static constexpr uint32_t kStage = 2 * kHalfTile;  // 32 KB
+    static constexpr uint32_t bars = ostage + 2 * kStage;
     static constexpr int bQFull = 0, bQEmpty = 1;
     static constexpr int bK16Full = 2, bK16Empty = bK16Full + NK16;
     static constexpr int bVrFull = bK16Empty + NK16, bVrEmpty = bVrFull + NVR;
@@ -67,14 +72,16 @@ struct PairLayout {
     static constexpr int bPFull = bSFull + 2;        // [2]
     static constexpr int bOFull = bPFull + 2;        // [2]
     static constexpr int bOEmpty = bOFull + 2;       // [2]
-    static constexpr int bDrain = bOEmpty + 2;
+    static constexpr int bStageFree = bOEmpty + 2;     // [2]
+    static constexpr int bStageReady = bStageFree + 2;  // [2]
+    static constexpr int bDrain = bStageReady + 2;
     static constexpr int nBars = bDrain + 1;
     static constexpr uint32_t tmem_slot = bars + 8 * nBars;
     static constexpr uint32_t abort_flag = tmem_slot + 4;
     static constexpr uint32_t bytes = abort_flag + 4;
 };
 static_assert(1024 + PairLayout::bytes <= 232448, "shared memory budget (pair)");
-static_assert(PairLayout::k16 % 1024 == 0 && PairLayout::vr % 1024 == 0,
+static_assert(PairLayout::k16 % 1024 == 0 && PairLayout::vr % 1024 == 0 && PairLayout::ostage % 1024 == 0,
               "1024-byte alignment of the pair tiles");
 
 // wait_or_abort with acquire at cluster scope, for barriers that the peer CTA
@@ -106,7 +113,8 @@ __device__ __forceinline__ bool wait_or_abort_cl(uint32_t bar, uint32_t parity, 
 template <int KT, bool kDiag, bool kSlots>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_pair_kernel(const __grid_constant__ PrefillParams p, const __grid_constant__ CUtensorMap tmq,
-                        const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv) {
+                        const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
+                        const __grid_constant__ CUtensorMap tmo) {
     static_assert(KT == PAFP8_F16 || KT == PAFP8_BF16, "a 2-byte cache");
     constexpr bool kBF = KT == PAFP8_BF16;  // bf16 MMA operands
     constexpr int DH = 128;
@@ -148,6 +156,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar(L::bPFull + x), 8);   // both CTAs' softmax warps of tile x
             mbar_init(bar(L::bOFull + x), 1);
             mbar_init(bar(L::bOEmpty + x), 8);
+            mbar_init(bar(L::bStageFree + x), 1);
+            mbar_init(bar(L::bStageReady + x), 128);
         }
         mbar_init(bar(L::bDrain), 1);
         asm volatile("st.shared.u32 [%0], 0;" ::"r"(flag_addr) : "memory");
@@ -423,6 +433,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t lane_base = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
         const uint32_t tS = lane_base + col_s(x), tO = lane_base + col_o<DH>(x);
         uint32_t sphase = 0, ophase = 0;
+        uint32_t stage_round = 0;  // staged epilogues of this tile so far
+        const bool issuer = r == 0;
         const bool o_32b = (reinterpret_cast<uintptr_t>(p.o) & 31u) == 0;  // rows are 256 B apart
         bool ok = true;
         Item it_next = pair_id < n_items ? load_item(items, pair_id) : Item{};
@@ -545,6 +557,63 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             const float inv = valid_row && l > 0.f ? vsc / l : 0.f;
             const size_t orow = (size_t)(qo0 + t0 + tok) * p.num_qo_heads + (size_t)it.hk * g + hh;
+            if (t0 + TQ <= qo_len) {
+                // A full tile: O normalized into this tile's staging (both 64-dim
+                // halves), then two bulk tensor stores by thread 0, which first
+                // made sure the previous stores from this staging have read it.
+                const uint32_t stg = base + L::ostage + (uint32_t)x * L::kStage;
+                if (issuer) {
+                    bulk_wait_read_all();
+                    mbar_arrive(bar(L::bStageFree + x));
+                }
+                ok = __all_sync(0xFFFFFFFFu, wait_or_abort<kDiag>(bar(L::bStageFree + x), stage_round & 1u, flag_addr,
+                                                                  p.status, p.wait_cycles));
+                if (!ok) break;
+                const f32x2 inv2 = make_f32x2(inv, inv);
+                // 32 columns (dims) at a time: 16 packed words, four 16-byte chunks
+                // of this row in dim half q >> 1.
+#pragma unroll 1
+                for (int q = 0; q < 4; ++q) {
+                    uint32_t v[32];
+                    tc_ld32(tO + 32 * q, v);
+                    tc_wait_ld();
+                    if (q == 3) {
+                        // O_X is read: release it to the next item's first PV.
+                        tc_fence_before();
+                        warp_arrive_cluster(lbar(L::bOEmpty + x));
+                    }
+                    uint32_t w[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        float a0, a1;
+                        split_f32x2(mul2(make_f32x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1])), inv2),
+                                    a0, a1);
+                        w[i] = pack_out2(a0, a1, p.o_dtype);
+                    }
+                    const uint32_t row = stg + (uint32_t)(q >> 1) * kHalfTile + (uint32_t)r * 128u;
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const int chunk = 4 * (q & 1) + c;
+                        sts128(row + ((chunk ^ (r & 7)) << 4), w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+                    }
+                }
+                fence_async_smem();
+                mbar_arrive(bar(L::bStageReady + x));
+                if (issuer) {
+                    ok = wait_or_abort<kDiag>(bar(L::bStageReady + x), stage_round & 1u, flag_addr, p.status,
+                                              p.wait_cycles);
+                    if (ok) {
+                        tma_store_3d(&tmo, stg, 0, it.hk * g, qo0 + t0);
+                        tma_store_3d(&tmo, stg + kHalfTile, 64, it.hk * g, qo0 + t0);
+                        bulk_commit();
+                    }
+                }
+                ok = __all_sync(0xFFFFFFFFu, ok);
+                ++stage_round;
+                if (!ok) break;
+                if (valid_row && p.lse != nullptr) p.lse[orow] = (m + __log2f(l)) * 0.69314718055994531f;
+                continue;
+            }
 #pragma unroll 1
             for (int c = 0; c < DH / 32; ++c) {
                 uint32_t v[32];
@@ -578,8 +647,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     // Neither CTA frees its TMEM or shared memory while the pair's MMAs or
-    // copies may still touch them: the leader's MMA thread has drained, and
-    // its producer has seen both CTAs' copies land.
+    // copies may still touch them: the leader's MMA thread has drained, its
+    // producer has seen both CTAs' copies land, and each tile's store issuer
+    // waits for its bulk stores here.
+    if ((warp == 4 || warp == 8) && lane == 0) bulk_wait_all();
     __syncwarp();
     tc_fence_before();
     cluster_sync_all();
@@ -591,7 +662,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int KT, bool kDiag, bool kSlots>
 cudaError_t launch_pair_t(const PrefillParams& p, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                          int num_ctas, cudaStream_t stream) {
+                          const CUtensorMap& to, int num_ctas, cudaStream_t stream) {
     auto kern = prefill_pair_kernel<KT, kDiag, kSlots>;
     const size_t smem = 1024 + PairLayout::bytes;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -626,7 +697,7 @@ cudaError_t launch_pair_t(const PrefillParams& p, const CUtensorMap& tq, const C
         pairs = mp;
         cfg.gridDim = dim3(2 * pairs, 1, 1);
     }
-    return cudaLaunchKernelEx(&cfg, kern, p, tq, tk, tv);
+    return cudaLaunchKernelEx(&cfg, kern, p, tq, tk, tv, to);
 }
 
 // A 2-byte cache at head_dim 128 (the query has the cache's dtype).  The
@@ -634,17 +705,18 @@ cudaError_t launch_pair_t(const PrefillParams& p, const CUtensorMap& tq, const C
 // 16 tokens and of 16 m tokens have one each.
 template <int KT>
 cudaError_t launch_pair_one(const PrefillParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
-                            const CUtensorMap& tv, int num_ctas, cudaStream_t stream) {
-    if (p.wait_cycles < kWaitCyclesDefault) return launch_pair_t<KT, true, true>(p, tq, tk, tv, num_ctas, stream);
-    return p.page_mult != 1 ? launch_pair_t<KT, false, true>(p, tq, tk, tv, num_ctas, stream)
-                            : launch_pair_t<KT, false, false>(p, tq, tk, tv, num_ctas, stream);
+                            const CUtensorMap& tv, const CUtensorMap& to, int num_ctas, cudaStream_t stream) {
+    if (p.wait_cycles < kWaitCyclesDefault) return launch_pair_t<KT, true, true>(p, tq, tk, tv, to, num_ctas, stream);
+    return p.page_mult != 1 ? launch_pair_t<KT, false, true>(p, tq, tk, tv, to, num_ctas, stream)
+                            : launch_pair_t<KT, false, false>(p, tq, tk, tv, to, num_ctas, stream);
 }
 
 inline cudaError_t launch_prefill_pair(const PrefillParams& p, const CUtensorMap& tmap_q, const CUtensorMap& tmap_k,
-                                       const CUtensorMap& tmap_v, int num_ctas, cudaStream_t stream) {
+                                       const CUtensorMap& tmap_v, const CUtensorMap& tmap_o, int num_ctas,
+                                       cudaStream_t stream) {
     switch (p.kv_dtype) {
-        case PAFP8_F16: return launch_pair_one<PAFP8_F16>(p, tmap_q, tmap_k, tmap_v, num_ctas, stream);
-        case PAFP8_BF16: return launch_pair_one<PAFP8_BF16>(p, tmap_q, tmap_k, tmap_v, num_ctas, stream);
+        case PAFP8_F16: return launch_pair_one<PAFP8_F16>(p, tmap_q, tmap_k, tmap_v, tmap_o, num_ctas, stream);
+        case PAFP8_BF16: return launch_pair_one<PAFP8_BF16>(p, tmap_q, tmap_k, tmap_v, tmap_o, num_ctas, stream);
         default: return cudaErrorInvalidValue;
     }
 }
