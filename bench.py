@@ -67,7 +67,7 @@ NCU_TRAFFIC = {
 # The same for the prefill kernels, per workload index, keyed by the SHA-256
 # of their sources (prefill.cuh, then prefill_pair.cuh).
 NCU_TRAFFIC_PREFILL = {
-    "777c6cad6dc1be02b46e60fa2abc794243500344954dfd0974603a89034bae74": {4: 168398592, 5: 189816064, 7: 255698176},
+    "8a8b8f6abc782551a2f5f796339847147b0b8e84b8d94dfafe4ad22d16bf1a66": {4: 168300544, 5: 190012928, 7: 259149824},
 }
 
 
